@@ -1,0 +1,256 @@
+/*
+ * skgemm.h -- C ABI of libskgemm.so: a single-GPU GB300 (sm_103a) GEMM
+ *
+ *     C = alpha * A * B + beta * C
+ *
+ * with fp16 / bf16 inputs, fp32 accumulation, a Stream-K work decomposition
+ * over persistent CTAs and an optional online ABFT row/column checksum check
+ * fused into the epilogue.
+ *
+ * Sources of the operations (page title, then section / algorithm / figure):
+ *  - GEMM definition and shapes: "Stream-K: Work-centric Parallel
+ *    Decomposition for Dense Matrix-Matrix Multiplication on the GPU", §A3
+ *    (Background). A is m x k, B is k x n, C is m x n, m*n*k MACs.
+ *  - Work decomposition: same page, Algorithm 5 (§4, Stream-K), Algorithm 2
+ *    (§3.2, data-parallel) and the hybrids of §5.2.
+ *  - Partial-tile fixup: same page, Algorithm 5 (StorePartials / Signal /
+ *    Wait / LoadPartials) and §4 ("the CTA that executes a tile's k = 0
+ *    iteration writes it").
+ *  - ABFT: "Anatomy of High-Performance GEMM with Online Fault Tolerance on
+ *    GPUs", thread-level FT-GEMM (Fig. 3: checksums C^c = e^T A B and
+ *    C^r = A B e, locate by the mismatching row and column, correct from the
+ *    checksum offset) and threadblock-level FT-GEMM (Figs. 5-7: one check per
+ *    output tile, checksums updated at every k step).
+ *
+ * Conventions for every entry point:
+ *  - Device pointers are plain CUDA device addresses owned by the caller.
+ *    The library allocates no device memory on the gemm path; it reads and
+ *    writes only the buffers passed in.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls that
+ *    launch work are asynchronous on it.
+ *  - Argument errors are returned synchronously and nothing is launched.
+ *    Outcomes decided on the device (fixup or pipeline timeouts, ABFT
+ *    corrections) are recorded in the workspace report and read back with
+ *    skg_report_read after the stream has run the launch.
+ *  - No entry point falls back to a CPU path. Unsupported shapes, layouts
+ *    or alignments return SKG_ERR_UNSUPPORTED.
+ */
+#ifndef SKGEMM_H
+#define SKGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Input element type of A and B (both the same). */
+typedef enum { SKG_IN_F16 = 0, SKG_IN_BF16 = 1 } skg_in_t;
+
+/* Element type of C (and of C0 when beta != 0). */
+typedef enum { SKG_OUT_F32 = 0, SKG_OUT_F16 = 1, SKG_OUT_BF16 = 2 } skg_out_t;
+
+/* Storage of A: row-major m x k (element (i,l) at A[i*lda + l]). This is
+ * the "K-major" order the tensor cores read directly. */
+typedef enum { SKG_A_ROW = 0 } skg_a_layout_t;
+
+/* Storage of B: K-major means B is stored n x k, element (l,j) at
+ * B[j*ldb + l] (the "NT" form, as for a weight matrix of a linear layer). */
+typedef enum { SKG_B_KMAJOR = 0 } skg_b_layout_t;
+
+/* Schedules (Stream-K page, §3.2, §4, §5.2):
+ *  DP       one persistent CTA walks tiles x, x+g, ... (Algorithm 2 folded
+ *           onto g persistent CTAs);
+ *  SK       basic Stream-K: all MAC iterations split evenly over g CTAs
+ *           (Algorithm 5, even split to within one iteration);
+ *  DP_SK1   "data-parallel + one-tile Stream-K": full DP waves, then the
+ *           remaining t mod g tiles iteration-balanced over g CTAs;
+ *  SK2_DP   "two-tile Stream-K + data-parallel": gives up one DP wave so
+ *           each Stream-K CTA gets between one and two tiles of iterations
+ *           (the default; the configuration the page evaluates). */
+typedef enum {
+  SKG_SCHED_DP = 0,
+  SKG_SCHED_SK = 1,
+  SKG_SCHED_DP_SK1 = 2,
+  SKG_SCHED_SK2_DP = 3
+} skg_sched_t;
+
+/* Role of one segment of a CTA's work (Algorithm 5, tile_started /
+ * tile_ended): FULL = the CTA computes and stores the whole tile; OWNER =
+ * it starts the tile, waits for its peers' partial sums, adds them and
+ * stores; PEER = it stores its partial sums to the workspace and signals. */
+typedef enum { SKG_ROLE_FULL = 0, SKG_ROLE_OWNER = 1, SKG_ROLE_PEER = 2 } skg_role_t;
+
+typedef enum {
+  SKG_OK = 0,
+  SKG_ERR_ARG = 1,              /* bad argument (negative size, null pointer, ld too small) */
+  SKG_ERR_UNSUPPORTED = 2,      /* valid BLAS call this build does not run (alignment, layout) */
+  SKG_ERR_CUDA = 3,             /* a CUDA runtime / driver call failed */
+  SKG_ERR_WORKSPACE = 4,        /* workspace missing, misaligned or too small */
+  SKG_ERR_FIXUP_TIMEOUT = 5,    /* device: an owner gave up waiting for a peer's partials */
+  SKG_ERR_PIPELINE_TIMEOUT = 6, /* device: an internal pipeline wait ran out (never expected) */
+  SKG_ABFT_CORRECTED = 16,      /* device: a single fault was located and corrected */
+  SKG_ABFT_UNCORRECTABLE = 17   /* device: a checksum mismatch could not be corrected */
+} skg_status_t;
+
+/* Largest tile side the library uses (BLK_M = 128, BLK_N <= 256). */
+#define SKG_BLK_M 128
+#define SKG_BLK_K 64
+/* Segments recorded per CTA when a trace buffer is passed. */
+#define SKG_TRACE_CAP 255
+/* ints per CTA in a trace buffer: 1 count + SKG_TRACE_CAP * 4. */
+#define SKG_TRACE_STRIDE 1024
+/* Fault records kept in the workspace report. */
+#define SKG_MAX_RECORDS 64
+
+/* Options of one gemm call. Zero-initialised fields select the defaults;
+ * call skg_opts_default to get them explicitly. */
+typedef struct {
+  int32_t sched;        /* skg_sched_t (default SKG_SCHED_SK2_DP) */
+  int32_t grid;         /* g, persistent CTAs; 0 = number of SMs. At most the
+                           number of SMs: all CTAs must be co-resident, since
+                           a tile owner waits for later CTAs. */
+  int32_t tile_n;       /* BLK_N: 128 or 256; 0 = chosen by the library */
+  int32_t abft;         /* 0 = off; 1 = verify every output tile, locate and
+                           correct a single fault, report the rest */
+  float tau_row;        /* ABFT row threshold; <= 0 = the default
+                           2^-12 * sqrt(k) * sqrt(BLK_N) * max|A| * max|B| */
+  float tau_col;        /* ABFT column threshold; <= 0 = the default
+                           2^-12 * sqrt(k) * sqrt(BLK_M) * max|A| * max|B| */
+  int32_t inject_tile;  /* fault injection for testing: < 0 = none; else the
+                           tile index whose accumulator gets one bit flipped */
+  int32_t inject_row;   /* row within the tile [0, 128) */
+  int32_t inject_col;   /* column within the tile [0, BLK_N) */
+  int32_t inject_bit;   /* bit of the fp32 accumulator [0, 32) */
+  uint64_t timeout_ns;  /* bound on every device-side wait; 0 = 2 s */
+  int32_t* trace;       /* optional device buffer, grid * SKG_TRACE_STRIDE
+                           int32: per CTA the segment count, then
+                           (tile, k_iter_begin, k_iter_end, role) per segment */
+  uint64_t* cta_clock;  /* optional device buffer, grid * 2 uint64: per CTA
+                           the %globaltimer at start and end (ns) */
+  int32_t test_drop_signal; /* testing only: 1 + index of a CTA that skips its
+                           Stream-K Signal, so the owner's bounded wait runs out
+                           and the launch reports SKG_ERR_FIXUP_TIMEOUT; 0 = none */
+  int32_t reserved0;
+} skg_opts_t;
+
+/* One segment of a schedule (Stream-K page, Algorithm 5 / §5.2). k_iter_*
+ * count MAC iterations of BLK_K within the tile. */
+typedef struct {
+  int32_t cta;
+  int32_t tile;         /* row-major tile index: tile = tm * tiles_n + tn */
+  int32_t k_iter_begin;
+  int32_t k_iter_end;   /* exclusive */
+  int32_t role;         /* skg_role_t */
+} skg_segment_t;
+
+/* One located (or uncorrectable) checksum mismatch. */
+typedef struct {
+  uint32_t launch;      /* launch epoch of the workspace (1 for the first launch) */
+  int32_t tile;
+  int32_t row;          /* row within the tile, -1 if not located */
+  int32_t col;          /* column within the tile, -1 if not located */
+  int32_t status;       /* SKG_ABFT_CORRECTED or SKG_ABFT_UNCORRECTABLE */
+  int32_t n_bad_rows;
+  int32_t n_bad_cols;
+  uint32_t injected;    /* 1 if the flip came from skg_opts_t.inject_* */
+  float before;         /* accumulator value as checked (the faulty one) */
+  float after;          /* value written back after correction */
+  float delta_row;      /* row checksum mismatch at the located row */
+  float delta_col;      /* column checksum mismatch at the located column */
+  float clean_value;    /* for injected flips: the value before the flip */
+  uint32_t pad[3];
+} skg_fault_record_t;
+
+/* Device-side outcome counters, cumulative over launches on one workspace
+ * until read with reset != 0. */
+typedef struct {
+  uint32_t status_bits;   /* bit (1 << code) set for each device outcome code seen */
+  uint32_t launches;      /* launches that ran to completion */
+  uint32_t tiles_checked; /* output tiles verified by ABFT */
+  uint32_t detected;      /* tiles with at least one checksum mismatch */
+  uint32_t corrected;
+  uint32_t uncorrectable;
+  uint32_t timeouts;      /* device waits that ran out */
+  uint32_t n_records;     /* records written (at most SKG_MAX_RECORDS kept) */
+  float max_ratio_row;    /* largest |row mismatch| / tau_row over rows that passed */
+  float max_ratio_col;    /* same for columns */
+  float tau_row;          /* thresholds used by the latest ABFT launch */
+  float tau_col;
+  uint32_t reserved[4];
+  skg_fault_record_t records[SKG_MAX_RECORDS];
+} skg_report_t;
+
+/* Fill *opts with the defaults (SK2_DP, g = #SMs, automatic BLK_N, ABFT off,
+ * no injection, 2 s wait bound, no trace). */
+void skg_opts_default(skg_opts_t* opts);
+
+/* Bytes of device workspace a gemm of this shape needs with these options
+ * (opts may be NULL): a header with the launch epoch and the report, one
+ * flag and one fp32 BLK_M x BLK_N partial-sum slot per CTA (Stream-K page,
+ * §4: fixup storage scales with g, not with the problem), the partial
+ * checksums, and with ABFT the split encodings e^T A and B e. */
+size_t skg_workspace_size(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts);
+
+/* Zero a workspace (`bytes` from skg_workspace_size) before its first use.
+ * Afterwards the library keeps it consistent itself (flags carry a launch
+ * epoch, so they never need clearing). Asynchronous on `stream`. */
+skg_status_t skg_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/* C = alpha * A B + beta * C, asynchronous on `stream`.
+ *   A: device, in_dtype, row-major m x k, lda >= k (elements).
+ *   B: device, in_dtype, K-major (stored n x k), ldb >= k.
+ *   C: device, out_dtype, row-major m x n, ldc >= n; read only if beta != 0.
+ *   A, B, C must be 16-byte aligned and lda, ldb, ldc must be multiples of
+ *   16 bytes (the TMA engine's rule); otherwise SKG_ERR_UNSUPPORTED.
+ *   workspace: device, >= skg_workspace_size(m, n, k, opts) bytes, zeroed
+ *   once with skg_workspace_init; one workspace per stream (two launches
+ *   that share a workspace must not overlap).
+ *   opts: NULL for defaults. m, n or k of zero is valid (k = 0 gives
+ *   C = beta * C). */
+skg_status_t skg_gemm(int64_t m, int64_t n, int64_t k, float alpha, const void* A, int64_t lda,
+                      const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
+                      int32_t in_dtype, int32_t out_dtype, int32_t a_layout, int32_t b_layout,
+                      const skg_opts_t* opts, void* workspace, size_t ws_bytes, void* stream);
+
+/* skg_gemm with the checksum check forced on (opts->abft = 1): every output
+ * tile's fp32 accumulator A_tile B_tile is verified against the reference
+ * checksums (e^T A) B and A (B e) before alpha, beta and the cast are
+ * applied; a single fault is located and corrected, anything else is
+ * reported. Results land in the workspace report (skg_report_read). */
+skg_status_t skg_gemm_verify(int64_t m, int64_t n, int64_t k, float alpha, const void* A,
+                             int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+                             int64_t ldc, int32_t in_dtype, int32_t out_dtype, int32_t a_layout,
+                             int32_t b_layout, const skg_opts_t* opts, void* workspace,
+                             size_t ws_bytes, void* stream);
+
+/* The schedule the kernel runs, computed on the host: for every CTA, its
+ * ordered segments (tile, k-iteration range, role). bm, bn, bk are the tile
+ * sides (bn = the BLK_N skg_gemm would use; pass skg_tile_n to get it).
+ * Writes at most `cap` segments to `out` (host memory, may be NULL when
+ * cap == 0) and the total count to *n_out. */
+skg_status_t skg_schedule_query(int64_t m, int64_t n, int64_t k, int32_t bm, int32_t bn,
+                                int32_t bk, int32_t g, int32_t sched, skg_segment_t* out,
+                                int64_t cap, int64_t* n_out);
+
+/* BLK_N and grid skg_gemm would use for this shape and options. */
+skg_status_t skg_launch_shape(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts,
+                              int32_t* tile_n, int32_t* grid);
+
+/* Copy the workspace report to host memory (synchronises `stream` first);
+ * reset != 0 also clears the counters and records. */
+skg_status_t skg_report_read(const void* workspace, skg_report_t* out, int32_t reset,
+                             void* stream);
+
+/* Number of SMs of the current device (0 if there is no device). */
+int32_t skg_device_sm_count(void);
+
+/* Short text for a status code. */
+const char* skg_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKGEMM_H */

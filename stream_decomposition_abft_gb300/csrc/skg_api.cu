@@ -1,0 +1,385 @@
+// C-ABI entry points of libskgemm.so (declared in include/skgemm.h).
+//
+// Host side of one gemm call: validate the BLAS-style arguments (the
+// problem statement C = alpha A B + beta C of "Stream-K: Work-centric
+// Parallel Decomposition for Dense Matrix-Matrix Multiplication on the GPU",
+// §A3), choose BLK_N and the grid, lay out the caller's workspace, encode the
+// TMA descriptors, run the ABFT encode pass when asked, and launch the
+// persistent kernel. Nothing here computes any part of the product.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "skg_internal.h"
+#include "skgemm.h"
+
+using namespace skg;
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr size_t kHeaderBytes = 8192;  // WsHeader + skg_report_t, rounded
+
+static_assert(256 + sizeof(skg_report_t) <= kHeaderBytes, "report does not fit the header");
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+int sm_count_cached() {
+  static int counts[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64 && counts[dev] > 0) return counts[dev];
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (dev < 64) counts[dev] = v;
+  return v;
+}
+
+struct Resolved {
+  int sched;
+  int grid;
+  int bn;
+  int abft;
+  float tau_row, tau_col;
+  int inject_tile, inject_row, inject_col, inject_bit;
+  uint64_t timeout_ns;
+  int32_t* trace;
+  uint64_t* cta_clock;
+  int drop_signal;
+};
+
+// BLK_N choice: 256 columns halve the A-operand shared-memory reads per
+// MMA and keep both TMEM accumulator buffers (2 x 256 columns) when ABFT is
+// off; with ABFT on, 128 columns keep the accumulator double-buffered
+// (2 x (128 + 32) columns). Narrow outputs (n <= 128) use 128.
+int auto_tile_n(int64_t n, int abft) {
+  if (abft) return 128;
+  return n <= 128 ? 128 : 256;
+}
+
+skg_status_t resolve(int64_t n, const skg_opts_t* o, Resolved& r, int sms) {
+  skg_opts_t d;
+  skg_opts_default(&d);
+  if (!o) o = &d;
+  r.sched = o->sched;
+  if (r.sched < SKG_SCHED_DP || r.sched > SKG_SCHED_SK2_DP) return SKG_ERR_ARG;
+  r.abft = o->abft ? 1 : 0;
+  r.bn = o->tile_n ? o->tile_n : auto_tile_n(n, r.abft);
+  if (r.bn != 128 && r.bn != 256) return SKG_ERR_UNSUPPORTED;
+  r.grid = o->grid > 0 ? o->grid : sms;
+  if (o->grid < 0) return SKG_ERR_ARG;
+  if (sms > 0 && r.grid > sms) return SKG_ERR_UNSUPPORTED;  // CTAs must be co-resident
+  r.tau_row = o->tau_row;
+  r.tau_col = o->tau_col;
+  r.inject_tile = o->inject_tile;
+  r.inject_row = o->inject_row;
+  r.inject_col = o->inject_col;
+  r.inject_bit = o->inject_bit;
+  if (r.inject_tile >= 0 && (r.inject_row < 0 || r.inject_row >= kBM || r.inject_col < 0 ||
+                             r.inject_col >= r.bn || r.inject_bit < 0 || r.inject_bit > 31))
+    return SKG_ERR_ARG;
+  r.timeout_ns = o->timeout_ns ? o->timeout_ns : kDefaultTimeoutNs;
+  r.trace = o->trace;
+  r.cta_clock = o->cta_clock;
+  r.drop_signal = o->test_drop_signal - 1;
+  return SKG_OK;
+}
+
+struct Layout {
+  size_t flags, partials, csum, sums, enc, total;
+  int kp, tiles_a, tiles_b;
+};
+
+Layout layout(int64_t m, int64_t n, int64_t k, const Resolved& r) {
+  Layout L;
+  size_t off = kHeaderBytes;
+  L.flags = off;
+  off = round_up(off + (size_t)r.grid * 4, 256);
+  L.partials = off;
+  off = round_up(off + (size_t)r.grid * kBM * r.bn * 4, 256);
+  L.csum = off;
+  off = round_up(off + (size_t)r.grid * kCsumStride * 4, 256);
+  L.kp = (int)round_up((size_t)(k > 0 ? k : 1), kBK);
+  L.tiles_a = (int)((m + kBM - 1) / kBM);
+  L.tiles_b = (int)((n + r.bn - 1) / r.bn);
+  L.sums = L.enc = off;
+  if (r.abft) {
+    L.sums = off;
+    off = round_up(off + (size_t)(L.tiles_a + L.tiles_b) * L.kp * 4, 256);
+    L.enc = off;
+    off = round_up(off + (size_t)(L.tiles_a + L.tiles_b) * kEncRows * L.kp * 2, 256);
+  }
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+CUresult make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base,
+                  uint64_t inner, uint64_t outer, uint64_t row_stride_elems, uint32_t box_inner,
+                  uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_elems * (uint64_t)elem_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return tensor_map_encoder()(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+template <int BN, bool ABFT>
+cudaError_t dispatch_out(int out_dtype, const CUtensorMap& a, const CUtensorMap& b,
+                         const CUtensorMap& c, const CUtensorMap& ea, const CUtensorMap& eb,
+                         const KernelParams& p, int grid, cudaStream_t st) {
+  switch (out_dtype) {
+    case SKG_OUT_F32: return launch_gemm<BN, ABFT, 0>(a, b, c, ea, eb, p, grid, st);
+    case SKG_OUT_F16: return launch_gemm<BN, ABFT, 1>(a, b, c, ea, eb, p, grid, st);
+    default: return launch_gemm<BN, ABFT, 2>(a, b, c, ea, eb, p, grid, st);
+  }
+}
+
+skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void* A, int64_t lda,
+                       const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
+                       int32_t in_dtype, int32_t out_dtype, int32_t a_layout, int32_t b_layout,
+                       const skg_opts_t* opts, int force_abft, void* workspace,
+                       size_t ws_bytes, void* stream_v) {
+  cudaStream_t stream = (cudaStream_t)stream_v;
+  if (m < 0 || n < 0 || k < 0) return SKG_ERR_ARG;
+  if (m > INT32_MAX / 2 || n > INT32_MAX / 2 || k > INT32_MAX / 2) return SKG_ERR_UNSUPPORTED;
+  if (in_dtype != SKG_IN_F16 && in_dtype != SKG_IN_BF16) return SKG_ERR_ARG;
+  if (out_dtype < SKG_OUT_F32 || out_dtype > SKG_OUT_BF16) return SKG_ERR_ARG;
+  if (a_layout != SKG_A_ROW || b_layout != SKG_B_KMAJOR) return SKG_ERR_UNSUPPORTED;
+  if (m == 0 || n == 0) return SKG_OK;
+  const int out_bytes = out_dtype == SKG_OUT_F32 ? 4 : 2;
+  if (!C) return SKG_ERR_ARG;
+  if (ldc < n) return SKG_ERR_ARG;
+  if (!aligned16(C) || (ldc * out_bytes) % 16) return SKG_ERR_UNSUPPORTED;
+  if (k == 0) {
+    return launch_scale(out_dtype, C, ldc, (int)m, (int)n, beta, stream) == cudaSuccess
+               ? SKG_OK
+               : SKG_ERR_CUDA;
+  }
+  if (!A || !B) return SKG_ERR_ARG;
+  if (lda < k || ldb < k) return SKG_ERR_ARG;
+  if (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 || (ldb * 2) % 16)
+    return SKG_ERR_UNSUPPORTED;
+
+  const int sms = sm_count_cached();
+  if (sms <= 0) return SKG_ERR_CUDA;
+  Resolved r;
+  skg_status_t st = resolve(n, opts, r, sms);
+  if (st != SKG_OK) return st;
+  if (force_abft) r.abft = 1, r.bn = (opts && opts->tile_n) ? opts->tile_n : auto_tile_n(n, 1);
+  if (r.inject_tile >= 0 && r.inject_col >= r.bn) return SKG_ERR_ARG;
+  const Layout L = layout(m, n, k, r);
+  if (!workspace || !aligned16(workspace) || ws_bytes < L.total) return SKG_ERR_WORKSPACE;
+  if (!tensor_map_encoder()) return SKG_ERR_CUDA;
+
+  uint8_t* ws = (uint8_t*)workspace;
+  const CUtensorMapDataType in_t =
+      in_dtype == SKG_IN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType out_t = out_dtype == SKG_OUT_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                    : out_dtype == SKG_OUT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap tmA, tmB, tmC, tmEA, tmEB;
+  if (make_map(&tmA, in_t, 2, A, (uint64_t)k, (uint64_t)m, (uint64_t)lda, kBK, kBM) !=
+          CUDA_SUCCESS ||
+      make_map(&tmB, in_t, 2, B, (uint64_t)k, (uint64_t)n, (uint64_t)ldb, kBK, r.bn) !=
+          CUDA_SUCCESS ||
+      make_map(&tmC, out_t, out_bytes, C, (uint64_t)n, (uint64_t)m, (uint64_t)ldc,
+               128 / out_bytes, 32) != CUDA_SUCCESS)
+    return SKG_ERR_UNSUPPORTED;
+  tmEA = tmA;
+  tmEB = tmB;
+  WsHeader* hdr = (WsHeader*)ws;
+  if (r.abft) {
+    void* enc = ws + L.enc;
+    void* enc_b = (uint8_t*)enc + (size_t)L.tiles_a * kEncRows * L.kp * 2;
+    if (make_map(&tmEA, in_t, 2, enc, (uint64_t)L.kp, (uint64_t)L.tiles_a * kEncRows,
+                 (uint64_t)L.kp, kBK, kEncRows) != CUDA_SUCCESS ||
+        make_map(&tmEB, in_t, 2, enc_b, (uint64_t)L.kp, (uint64_t)L.tiles_b * kEncRows,
+                 (uint64_t)L.kp, kBK, kEncRows) != CUDA_SUCCESS)
+      return SKG_ERR_UNSUPPORTED;
+    if (launch_encode(in_dtype == SKG_IN_BF16, A, lda, (int)m, B, ldb, (int)n, (int)k, L.kp,
+                      r.bn, (float*)(ws + L.sums), enc, hdr, stream) != cudaSuccess)
+      return SKG_ERR_CUDA;
+  }
+
+  KernelParams p;
+  memset(&p, 0, sizeof(p));
+  p.s = make_schedule(m, n, k, kBM, r.bn, kBK, r.grid, r.sched);
+  p.m = (int)m;
+  p.n = (int)n;
+  p.k = (int)k;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.idesc_main = idesc_f16(in_dtype == SKG_IN_BF16, kBM, r.bn);
+  p.idesc_ck = idesc_f16(in_dtype == SKG_IN_BF16, kBM, 16);
+  p.hdr = hdr;
+  p.report = (skg_report_t*)(ws + 256);
+  p.flags = (uint32_t*)(ws + L.flags);
+  p.partials = (float*)(ws + L.partials);
+  p.csum = (float*)(ws + L.csum);
+  p.tau_row = r.tau_row;
+  p.tau_col = r.tau_col;
+  p.inject_tile = r.inject_tile;
+  p.inject_row = r.inject_row;
+  p.inject_col = r.inject_col;
+  p.inject_bit = r.inject_bit;
+  p.timeout_ns = r.timeout_ns;
+  p.trace = r.trace;
+  p.cta_clock = r.cta_clock;
+  p.drop_signal = r.drop_signal;
+
+  cudaError_t e;
+  if (r.bn == 128)
+    e = r.abft ? dispatch_out<128, true>(out_dtype, tmA, tmB, tmC, tmEA, tmEB, p, r.grid, stream)
+               : dispatch_out<128, false>(out_dtype, tmA, tmB, tmC, tmEA, tmEB, p, r.grid, stream);
+  else
+    e = r.abft ? dispatch_out<256, true>(out_dtype, tmA, tmB, tmC, tmEA, tmEB, p, r.grid, stream)
+               : dispatch_out<256, false>(out_dtype, tmA, tmB, tmC, tmEA, tmEB, p, r.grid, stream);
+  return e == cudaSuccess ? SKG_OK : SKG_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+void skg_opts_default(skg_opts_t* o) {
+  if (!o) return;
+  memset(o, 0, sizeof(*o));
+  o->sched = SKG_SCHED_SK2_DP;
+  o->inject_tile = -1;
+}
+
+size_t skg_workspace_size(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts) {
+  if (m < 0 || n < 0 || k < 0) return 0;
+  Resolved r;
+  int sms = sm_count_cached();
+  if (resolve(n, opts, r, sms) != SKG_OK) return 0;
+  if (r.grid <= 0) r.grid = 256;  // no device: size for the largest grid
+  return layout(m, n, k, r).total;
+}
+
+skg_status_t skg_workspace_init(void* workspace, size_t bytes, void* stream) {
+  if (!workspace || bytes < kHeaderBytes) return SKG_ERR_WORKSPACE;
+  return cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream) == cudaSuccess ? SKG_OK
+                                                                                 : SKG_ERR_CUDA;
+}
+
+skg_status_t skg_gemm(int64_t m, int64_t n, int64_t k, float alpha, const void* A, int64_t lda,
+                      const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
+                      int32_t in_dtype, int32_t out_dtype, int32_t a_layout, int32_t b_layout,
+                      const skg_opts_t* opts, void* workspace, size_t ws_bytes, void* stream) {
+  return gemm_impl(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, a_layout,
+                   b_layout, opts, 0, workspace, ws_bytes, stream);
+}
+
+skg_status_t skg_gemm_verify(int64_t m, int64_t n, int64_t k, float alpha, const void* A,
+                             int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+                             int64_t ldc, int32_t in_dtype, int32_t out_dtype, int32_t a_layout,
+                             int32_t b_layout, const skg_opts_t* opts, void* workspace,
+                             size_t ws_bytes, void* stream) {
+  return gemm_impl(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, a_layout,
+                   b_layout, opts, 1, workspace, ws_bytes, stream);
+}
+
+skg_status_t skg_schedule_query(int64_t m, int64_t n, int64_t k, int32_t bm, int32_t bn,
+                                int32_t bk, int32_t g, int32_t sched, skg_segment_t* out,
+                                int64_t cap, int64_t* n_out) {
+  if (m < 0 || n < 0 || k < 0 || bm <= 0 || bn <= 0 || bk <= 0 || g <= 0 || !n_out)
+    return SKG_ERR_ARG;
+  if (sched < SKG_SCHED_DP || sched > SKG_SCHED_SK2_DP) return SKG_ERR_ARG;
+  if (cap > 0 && !out) return SKG_ERR_ARG;
+  const Schedule s = make_schedule(m, n, k, bm, bn, bk, g, sched);
+  int64_t count = 0;
+  if (s.t > 0 && s.ipt > 0) {
+    for (int x = 0; x < g; ++x) {
+      Cursor c;
+      c.init(s, x);
+      Work w;
+      while (c.next(s, w)) {
+        if (count < cap) {
+          out[count].cta = x;
+          out[count].tile = w.tile;
+          out[count].k_iter_begin = w.kb_begin;
+          out[count].k_iter_end = w.kb_end;
+          out[count].role = w.role;
+        }
+        ++count;
+      }
+    }
+  }
+  *n_out = count;
+  return SKG_OK;
+}
+
+skg_status_t skg_launch_shape(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts,
+                              int32_t* tile_n, int32_t* grid) {
+  (void)m;
+  (void)k;
+  Resolved r;
+  const int sms = sm_count_cached();
+  skg_status_t st = resolve(n, opts, r, sms);
+  if (st != SKG_OK) return st;
+  if (tile_n) *tile_n = r.bn;
+  if (grid) *grid = r.grid;
+  return SKG_OK;
+}
+
+skg_status_t skg_report_read(const void* workspace, skg_report_t* out, int32_t reset,
+                             void* stream) {
+  if (!workspace || !out) return SKG_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SKG_ERR_CUDA;
+  const uint8_t* rep = (const uint8_t*)workspace + 256;
+  if (cudaMemcpy(out, rep, sizeof(skg_report_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SKG_ERR_CUDA;
+  if (reset) {
+    if (cudaMemsetAsync((void*)rep, 0, sizeof(skg_report_t), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return SKG_ERR_CUDA;
+  }
+  return SKG_OK;
+}
+
+int32_t skg_device_sm_count(void) { return sm_count_cached(); }
+
+const char* skg_status_string(int32_t status) {
+  switch (status) {
+    case SKG_OK: return "ok";
+    case SKG_ERR_ARG: return "invalid argument";
+    case SKG_ERR_UNSUPPORTED: return "unsupported shape, layout or alignment";
+    case SKG_ERR_CUDA: return "CUDA error";
+    case SKG_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SKG_ERR_FIXUP_TIMEOUT: return "Stream-K fixup wait timed out";
+    case SKG_ERR_PIPELINE_TIMEOUT: return "pipeline wait timed out";
+    case SKG_ABFT_CORRECTED: return "ABFT: single fault located and corrected";
+    case SKG_ABFT_UNCORRECTABLE: return "ABFT: uncorrectable checksum mismatch";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,880 @@
+// Persistent Stream-K GEMM kernel for sm_103a with an optional fused ABFT
+// check.
+//
+//   C = alpha * A B + beta * C,   A: m x k (K-major), B: stored n x k (K-major)
+//
+// Work decomposition: "Stream-K: Work-centric Parallel Decomposition for
+// Dense Matrix-Matrix Multiplication on the GPU", Algorithm 5 and §5.2
+// (see skg_sched.cuh). One CTA per SM walks its segments:
+//
+//   warp 0      TMA producer: A and B tiles (BLK_K = 64, 128-byte swizzle)
+//               into a STAGES-deep shared-memory ring, full/empty mbarriers.
+//   warp 1      MMA issuer: tcgen05.mma kind::f16, M = 128, N = BLK_N, fp32
+//               accumulator in TMEM (double-buffered when it fits), commit
+//               to the ring's empty barrier and to the accumulator barrier.
+//   warps 2-5   epilogue (TMEM lane quadrant = warp % 4, one output row per
+//               thread): a PEER segment writes its fp32 partial tile to the
+//               workspace and releases a flag carrying the launch epoch
+//               (StorePartials / Signal); an OWNER waits for its later peers'
+//               flags and adds their partials (Wait / LoadPartials); then
+//               alpha / beta, the output cast, a swizzled staging buffer and
+//               a TMA store (StoreTile). Only the tile's k = 0 CTA writes C
+//               (§4), so C needs no atomics.
+//
+// ABFT ("Anatomy of High-Performance GEMM with Online Fault Tolerance on
+// GPUs", Figs. 3 and 5-7): the encodings e^T A (per 128-row tile) and B e
+// (per BLK_N-column tile) are pre-computed once and split into three
+// input-precision terms; at every k step the MMA warp also issues
+//   cr += A_tile * [Be_hi, Be_mid, Be_lo]          (N = 16, row checksums)
+//   cc += B_tile * [eA_hi, eA_mid, eA_lo]          (N = 16, column checksums)
+// into spare TMEM columns, so both reference checksums are updated online on
+// the tensor pipe. The epilogue forms the row sums (in-thread) and column
+// sums (warp transpose-reduction + shared memory) of the accumulator,
+// compares them with cr and cc, locates a single fault at the mismatching
+// row and column, replaces it by cr[i*] - sum_{j != j*} acc[i*, j], and only
+// then applies alpha / beta and stores.
+//
+// Every wait (mbarrier or peer flag) is bounded by a %globaltimer deadline;
+// on expiry the kernel records the error in the workspace report, sets a
+// CTA-wide abort flag, drains its own copies and MMAs, frees TMEM and exits.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "skg_ptx.cuh"
+#include "skg_sched.cuh"
+#include "skgemm.h"
+
+namespace skg {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kEncRows = 3;  // hi, mid, lo
+constexpr int kCsumStride = 384;  // floats per CTA of partial checksums
+constexpr uint32_t kSmemLimit = 232448;
+
+// Workspace header (device). The report follows at offset 256.
+struct WsHeader {
+  uint32_t epoch;          // launches completed on this workspace
+  uint32_t done;           // CTA tickets of the running launch
+  uint32_t maxabs_bits[2]; // max |A|, max |B| (fp32 bits) from the encode pass
+  uint32_t maxenc_bits[2]; // max |e^T A|, max |B e| (fp32 bits)
+  int32_t scale_exp[2];    // encodings are stored scaled by 2^scale_exp
+  uint32_t pad[56];
+};
+static_assert(sizeof(WsHeader) == 256, "header size");
+
+struct KernelParams {
+  Schedule s;
+  int m, n, k;
+  float alpha, beta;
+  uint32_t idesc_main;
+  uint32_t idesc_ck;
+  WsHeader* hdr;
+  skg_report_t* report;
+  uint32_t* flags;
+  float* partials;
+  float* csum;
+  float tau_row, tau_col;  // <= 0: derive from the encode pass maxima
+  int inject_tile, inject_row, inject_col, inject_bit;
+  uint64_t timeout_ns;
+  int32_t* trace;
+  uint64_t* cta_clock;
+  int drop_signal;  // testing: CTA index that skips its Signal, or -1
+};
+
+__host__ __device__ constexpr int pow2_at_least(int v) {
+  int p = 32;
+  while (p < v) p *= 2;
+  return p;
+}
+
+template <int BN_, bool ABFT_, int OUT_>
+struct Cfg {
+  static constexpr int BN = BN_;
+  static constexpr bool ABFT = ABFT_;
+  static constexpr int OUT = OUT_;  // 0 = f32, 1 = f16, 2 = bf16
+  static constexpr int OUT_BYTES = OUT == 0 ? 4 : 2;
+  static constexpr int EPI_COLS = 128 / OUT_BYTES;  // one 128-byte staging row
+  static constexpr int CK_COLS = ABFT ? 16 + 16 * (BN / 128) : 0;
+  static constexpr int ACC_COLS = BN + CK_COLS;
+  static constexpr int ACC_BUFS = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int TMEM_COLS = pow2_at_least(ACC_BUFS * ACC_COLS);
+  static constexpr int A_BYTES = kBM * kBK * 2;
+  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int ENC_BYTES = ABFT ? 16 * 128 : 0;  // 16 rows x 128 B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + 2 * ENC_BYTES;
+  static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + (ABFT ? 2 * kEncRows * 128 : 0);
+  static constexpr int EPI_BUF_BYTES = 32 * 128;
+  static constexpr int EPI_BUFS = 2;
+  static constexpr int EPI_BYTES = 4 * EPI_BUFS * EPI_BUF_BYTES;
+  static constexpr int AUX_BYTES = 512 + (ABFT ? 4 * BN * 4 : 0);
+  static constexpr int STAGES_FIT =
+      (int)((kSmemLimit - 1024 - EPI_BYTES - AUX_BYTES) / STAGE_BYTES);
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + AUX_BYTES;
+  static_assert(STAGES >= 2, "shared memory too small for two stages");
+  static_assert(SMEM_BYTES <= kSmemLimit, "shared memory over the per-CTA limit");
+  static_assert(TMEM_COLS <= 512, "TMEM over 512 columns");
+  static_assert(BN % EPI_COLS == 0, "epilogue chunking");
+};
+
+// Shared-memory bookkeeping that lives after the stage ring and staging.
+struct Aux {
+  uint64_t bars[48];      // full[S], empty[S], tfull[2], tempty[2], c0[4], drain
+  uint32_t tmem_slot;
+  int32_t abort_flag;
+  int32_t nbad_r, nbad_c, bad_row, bad_col;
+  float fix_value;
+  float inj_clean;
+  float d_row, d_col;
+  int32_t pad[6];
+};
+static_assert(sizeof(Aux) <= 512, "aux size");
+
+__device__ __forceinline__ void record_error(const KernelParams& p, Aux* aux, int code) {
+  atomicOr(&p.report->status_bits, 1u << code);
+  atomicAdd(&p.report->timeouts, 1u);
+  atomicExch(&aux->abort_flag, 1);
+}
+
+__device__ __forceinline__ bool aborted(Aux* aux) {
+  return *(volatile int32_t*)&aux->abort_flag != 0;
+}
+
+// Bounded mbarrier wait: true when the phase of `parity` completed; false
+// on timeout or, if `honor_abort`, when another role of this CTA aborted.
+// Drains (copies or MMAs this thread issued) pass honor_abort = false so
+// they always wait for their own operations, up to the time limit.
+static __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Aux* aux,
+                                             uint64_t limit_ns, bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31) == 0) {
+      if (honor_abort && aborted(aux)) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float f32_of(uint32_t u) { return __uint_as_float(u); }
+
+// Sum over the 32 lanes of a warp for each of 32 columns: on return lane l
+// holds the sum of column l (recursive halving, 31 shuffles).
+__device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? v[i] : v[i + off];
+      const float keep = upper ? v[i + off] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return v[0];
+}
+
+template <int OUT>
+__device__ __forceinline__ void pack_row(const float* y, uint32_t (&w)[32]);
+
+template <>
+__device__ __forceinline__ void pack_row<0>(const float* y, uint32_t (&w)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(y[i]);
+}
+
+template <>
+__device__ __forceinline__ void pack_row<1>(const float* y, uint32_t (&w)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    __half2 h = __floats2half2_rn(y[2 * i], y[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+template <>
+__device__ __forceinline__ void pack_row<2>(const float* y, uint32_t (&w)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(y[2 * i], y[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+template <int OUT>
+__device__ __forceinline__ void unpack_row(const uint32_t (&w)[32], float* y);
+
+template <>
+__device__ __forceinline__ void unpack_row<0>(const uint32_t (&w)[32], float* y) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(w[i]);
+}
+
+template <>
+__device__ __forceinline__ void unpack_row<1>(const uint32_t (&w)[32], float* y) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+    float2 f = __half22float2(h);
+    y[2 * i] = f.x;
+    y[2 * i + 1] = f.y;
+  }
+}
+
+template <>
+__device__ __forceinline__ void unpack_row<2>(const uint32_t (&w)[32], float* y) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    float2 f = __bfloat1622float2(h);
+    y[2 * i] = f.x;
+    y[2 * i + 1] = f.y;
+  }
+}
+
+// One 128-byte row of a staging buffer in the 128-byte swizzled order TMA
+// uses: 16-byte chunk j of row r sits at chunk position j ^ (r % 8).
+__device__ __forceinline__ void staging_write(uint8_t* buf, int r, const uint32_t (&w)[32]) {
+  uint8_t* row = buf + r * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint4 q = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    *reinterpret_cast<uint4*>(row + ((j ^ (r & 7)) << 4)) = q;
+  }
+}
+
+__device__ __forceinline__ void staging_read(const uint8_t* buf, int r, uint32_t (&w)[32]) {
+  const uint8_t* row = buf + r * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint4 q = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
+    w[4 * j] = q.x;
+    w[4 * j + 1] = q.y;
+    w[4 * j + 2] = q.z;
+    w[4 * j + 3] = q.w;
+  }
+}
+
+__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
+  return __ldcg(reinterpret_cast<const float4*>(p));
+}
+
+__device__ __forceinline__ void st_cg_f4(float* p, float4 v) {
+  __stcg(reinterpret_cast<float4*>(p), v);
+}
+
+// Partial tile layout (per CTA slot): 4-column groups of 128 rows, so the 32
+// lanes of a warp touch 512 contiguous bytes: float index (c4*128 + r)*4 + e.
+__device__ __forceinline__ float* partial_at(float* slot, int c4, int r) {
+  return slot + ((size_t)c4 * kBM + r) * 4;
+}
+
+template <class C>
+__global__ void __launch_bounds__(kThreads, 1)
+    skg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC,
+                    const __grid_constant__ CUtensorMap tmEA,
+                    const __grid_constant__ CUtensorMap tmEB, const KernelParams p) {
+  constexpr int BN = C::BN;
+  constexpr int STAGES = C::STAGES;
+  constexpr int ACC_BUFS = C::ACC_BUFS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* epi = ring + STAGES * C::STAGE_BYTES;
+  Aux* aux = reinterpret_cast<Aux*>(epi + C::EPI_BYTES);
+  float* colsum = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(aux) + 512);  // [4][BN]
+  uint64_t* full_bar = aux->bars;
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* tfull_bar = empty_bar + STAGES;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* c0_bar = tempty_bar + 2;
+  uint64_t* drain_bar = c0_bar + 4;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Schedule& s = p.s;
+  const uint64_t limit = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmC);
+    if (C::ABFT) {
+      prefetch_tmap(&tmEA);
+      prefetch_tmap(&tmEB);
+    }
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull_bar[i], 1);
+      mbar_init(&tempty_bar[i], kEpiThreads);
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(&c0_bar[i], 1);
+    mbar_init(drain_bar, 1);
+    aux->abort_flag = 0;
+    aux->nbad_r = aux->nbad_c = 0;
+    aux->bad_row = aux->bad_col = -1;
+    fence_barrier_init();
+    if (p.cta_clock) p.cta_clock[2 * blockIdx.x] = globaltimer();
+  }
+  if (C::ABFT) {
+    // Rows 3..15 of both 16-row encoding tiles of every stage stay zero; the
+    // TMA only ever writes rows 0..2 (hi, mid, lo).
+    for (int i = threadIdx.x; i < STAGES * 2 * 13 * 8; i += kThreads) {
+      const int st = i / (2 * 13 * 8);
+      const int rem = i % (2 * 13 * 8);
+      const int which = rem / (13 * 8);
+      const int row = 3 + (rem % (13 * 8)) / 8;
+      const int chunk = rem % 8;
+      uint8_t* base = ring + st * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES + which * C::ENC_BYTES;
+      *reinterpret_cast<uint4*>(base + row * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(&aux->tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = aux->tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      Cursor cur;
+      cur.init(s, blockIdx.x);
+      Work w;
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t pending = 0;  // bit i: stage i has a load this thread issued
+      uint32_t pend_par = 0; // parity of that load's phase
+      bool ok = true;
+      while (ok && cur.next(s, w)) {
+        const int tm = w.tile / s.tiles_n;
+        const int tn = w.tile % s.tiles_n;
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (!wait_bar(&empty_bar[stage], phase ^ 1, aux, limit)) {
+            if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+            ok = false;
+            break;
+          }
+          uint8_t* st = ring + stage * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
+          tma_load_2d(st, &tmA, &full_bar[stage], kb * kBK, tm * kBM);
+          tma_load_2d(st + C::A_BYTES, &tmB, &full_bar[stage], kb * kBK, tn * BN);
+          if (C::ABFT) {
+            tma_load_2d(st + C::A_BYTES + C::B_BYTES, &tmEB, &full_bar[stage], kb * kBK,
+                        tn * kEncRows);
+            tma_load_2d(st + C::A_BYTES + C::B_BYTES + C::ENC_BYTES, &tmEA, &full_bar[stage],
+                        kb * kBK, tm * kEncRows);
+          }
+          pending |= 1u << stage;
+          pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Never leave with a copy in flight into this CTA's shared memory.
+      for (int i = 0; i < STAGES; ++i)
+        if (pending & (1u << i)) wait_bar(&full_bar[i], (pend_par >> i) & 1, aux, limit, false);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      Cursor cur;
+      cur.init(s, blockIdx.x);
+      Work w;
+      int stage = 0;
+      uint32_t phase = 0;
+      int ab = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      bool issued = false;
+      while (ok && cur.next(s, w)) {
+        if (!wait_bar(&tempty_bar[ab], aphase ^ 1, aux, limit)) {
+          if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + ab * C::ACC_COLS;
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (!wait_bar(&full_bar[stage], phase, aux, limit)) {
+            if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(ring + stage * C::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(a_addr + kk * 32);
+            const uint64_t bd = sdesc_sw128(b_addr + kk * 32);
+            const uint32_t acc = (kb > w.kb_begin || kk > 0) ? 1u : 0u;
+            umma_f16(d, ad, bd, p.idesc_main, acc);
+            if (C::ABFT) {
+              const uint32_t eb = b_addr + C::B_BYTES;
+              const uint32_t ea = eb + C::ENC_BYTES;
+              umma_f16(d + BN, ad, sdesc_sw128(eb + kk * 32), p.idesc_ck, acc);
+#pragma unroll
+              for (int h = 0; h < BN / 128; ++h)
+                umma_f16(d + BN + 16 + 16 * h, sdesc_sw128(b_addr + h * 16384 + kk * 32),
+                         sdesc_sw128(ea + kk * 32), p.idesc_ck, acc);
+            }
+          }
+          issued = true;
+          umma_commit(&empty_bar[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar[ab]);
+        if (++ab == ACC_BUFS) {
+          ab = 0;
+          aphase ^= 1;
+        }
+      }
+      if (issued) {
+        // All MMAs this thread issued complete before TMEM is released.
+        umma_commit(drain_bar);
+        wait_bar(drain_bar, 0, aux, limit, false);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;         // epilogue warp 0..3
+    const int q = warp & 3;          // TMEM lane quadrant
+    const int r = q * 32 + lane;     // tile row of this thread
+    const int et = threadIdx.x - 64; // epilogue thread 0..127
+    uint8_t* ebuf = epi + ew * C::EPI_BUFS * C::EPI_BUF_BYTES;
+    const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr->epoch) + 1u;
+    float* my_slot = p.partials + (size_t)blockIdx.x * kBM * BN;
+
+    float tau_r = p.tau_row, tau_c = p.tau_col;
+    float unscale_a = 1.f, unscale_b = 1.f;
+    if (C::ABFT) {
+      const float maxa =
+          __uint_as_float(*reinterpret_cast<volatile uint32_t*>(&p.hdr->maxabs_bits[0]));
+      const float maxb =
+          __uint_as_float(*reinterpret_cast<volatile uint32_t*>(&p.hdr->maxabs_bits[1]));
+      const float base = ldexpf(1.f, -12) * sqrtf((float)p.k) * maxa * maxb;
+      if (!(tau_r > 0.f)) tau_r = base * sqrtf((float)BN);
+      if (!(tau_c > 0.f)) tau_c = base * sqrtf((float)kBM);
+      unscale_a = ldexpf(1.f, -*reinterpret_cast<volatile int32_t*>(&p.hdr->scale_exp[0]));
+      unscale_b = ldexpf(1.f, -*reinterpret_cast<volatile int32_t*>(&p.hdr->scale_exp[1]));
+      if (blockIdx.x == 0 && et == 0) {
+        p.report->tau_row = tau_r;
+        p.report->tau_col = tau_c;
+      }
+    }
+
+    Cursor cur;
+    cur.init(s, blockIdx.x);
+    Work w;
+    int ab = 0;
+    uint32_t aphase = 0;
+    int bsel = 0;
+    uint32_t c0_phase = 0;
+    int nseg = 0;
+    bool store_ok = true;
+    while (cur.next(s, w)) {
+      if (p.trace && et == 0) {
+        int32_t* tr = p.trace + (size_t)blockIdx.x * SKG_TRACE_STRIDE;
+        if (nseg < SKG_TRACE_CAP) {
+          tr[1 + 4 * nseg] = w.tile;
+          tr[2 + 4 * nseg] = w.kb_begin;
+          tr[3 + 4 * nseg] = w.kb_end;
+          tr[4 + 4 * nseg] = w.role;
+        }
+        tr[0] = nseg + 1;
+      }
+      ++nseg;
+      bool got = wait_bar(&tfull_bar[ab], aphase, aux, limit);
+      if (!got && !aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+      if (!epi_all(got && store_ok && !aborted(aux))) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + ab * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
+      const int tm = w.tile / s.tiles_n;
+      const int tn = w.tile % s.tiles_n;
+      const int m0 = tm * kBM;
+      const int n0 = tn * BN;
+      const bool inject_here = (w.tile == p.inject_tile) && (w.role != kRolePeer);
+
+      if (w.role == kRolePeer) {
+        // StorePartials + Signal (Algorithm 5, non-started segment).
+#pragma unroll 1
+        for (int c32 = 0; c32 < BN / 32; ++c32) {
+          uint32_t u[32];
+          tmem_ld32(tacc + c32 * 32, u);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_cg_f4(partial_at(my_slot, c32 * 8 + j, r),
+                     make_float4(f32_of(u[4 * j]), f32_of(u[4 * j + 1]), f32_of(u[4 * j + 2]),
+                                 f32_of(u[4 * j + 3])));
+        }
+        if (C::ABFT) {
+          uint32_t t4[4];
+          float* cs = p.csum + (size_t)blockIdx.x * kCsumStride;
+          tmem_ld4(tacc + BN, t4);
+          __stcg(cs + r, f32_of(t4[0]) + f32_of(t4[1]) + f32_of(t4[2]));
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) {
+            tmem_ld4(tacc + BN + 16 + 16 * h, t4);
+            __stcg(cs + 128 + 128 * h + r, f32_of(t4[0]) + f32_of(t4[1]) + f32_of(t4[2]));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty_bar[ab]);
+        named_bar_sync(1, kEpiThreads);
+        if (et == 0 && (int)blockIdx.x != p.drop_signal) {
+          __threadfence();
+          st_release_gpu(&p.flags[blockIdx.x], epoch);
+        }
+      } else {
+        const bool owner = (w.role == kRoleOwner);
+        if (owner) {
+          // Wait for every later CTA that covers part of this tile.
+          bool fine = true;
+          if (et == 0) {
+            for (int peer = blockIdx.x + 1; peer <= w.peer_last && fine; ++peer) {
+              if (ld_acquire_gpu(&p.flags[peer]) == epoch) continue;
+              const uint64_t t0 = globaltimer();
+              uint32_t spins = 0;
+              while (ld_acquire_gpu(&p.flags[peer]) != epoch) {
+                if (++spins > 64) nanosleep_ns(64);
+                if ((spins & 15) == 0 && globaltimer() - t0 > limit) {
+                  record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
+                  fine = false;
+                  break;
+                }
+              }
+            }
+          }
+          if (!epi_all(fine && !aborted(aux))) {
+            tc_fence_before();
+            mbar_arrive(&tempty_bar[ab]);
+            break;
+          }
+        }
+
+        // ------------------------------------------------ ABFT verify
+        int fix_row = -1, fix_col = -1;
+        float fix_val = 0.f;
+        if (C::ABFT) {
+          float rowsum = 0.f;
+#pragma unroll 1
+          for (int c32 = 0; c32 < BN / 32; ++c32) {
+            uint32_t u[32];
+            tmem_ld32(tacc + c32 * 32, u);
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
+            if (owner) {
+              for (int peer = blockIdx.x + 1; peer <= w.peer_last; ++peer) {
+                float* ps = p.partials + (size_t)peer * kBM * BN;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 a = ld_cg_f4(partial_at(ps, c32 * 8 + j, r));
+                  v[4 * j] += a.x;
+                  v[4 * j + 1] += a.y;
+                  v[4 * j + 2] += a.z;
+                  v[4 * j + 3] += a.w;
+                }
+              }
+            }
+            // Fault injection: one bit of one fp32 accumulator, after the
+            // fixup and before the check (warp-uniform chunk selection).
+            const bool inj_chunk = inject_here && (p.inject_row >> 5) == q &&
+                                   (p.inject_col >> 5) == c32;
+            if (inj_chunk && lane == (p.inject_row & 31)) {
+              const int jc = p.inject_col & 31;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i == jc) {
+                  aux->inj_clean = v[i];
+                  v[i] = __uint_as_float(__float_as_uint(v[i]) ^ (1u << p.inject_bit));
+                }
+            }
+            if (owner || inj_chunk) {
+              uint32_t wv[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) wv[i] = __float_as_uint(v[i]);
+              tmem_st32(tacc + c32 * 32, wv);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rowsum += v[i];
+            colsum[q * BN + c32 * 32 + lane] = warp_column_sums(v, lane);
+          }
+          // Reference checksums accumulated on the tensor pipe. Thread r
+          // holds the row checksum of row r and the column checksum of
+          // column h*128 + r (TMEM lane r of the column-checksum MMA).
+          uint32_t t4[4];
+          tmem_ld4(tacc + BN, t4);
+          float cr = f32_of(t4[0]) + f32_of(t4[1]) + f32_of(t4[2]);
+          float cc[BN / 128];
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) {
+            tmem_ld4(tacc + BN + 16 + 16 * h, t4);
+            cc[h] = f32_of(t4[0]) + f32_of(t4[1]) + f32_of(t4[2]);
+          }
+          if (owner) {
+            for (int peer = blockIdx.x + 1; peer <= w.peer_last; ++peer) {
+              const float* cs = p.csum + (size_t)peer * kCsumStride;
+              cr += __ldcg(cs + r);
+#pragma unroll
+              for (int h = 0; h < BN / 128; ++h) cc[h] += __ldcg(cs + 128 + 128 * h + r);
+            }
+          }
+          cr *= unscale_b;
+          named_bar_sync(1, kEpiThreads);  // column sums of all four warps stored
+
+          const float d_r = rowsum - cr;
+          const bool bad_r = !(fabsf(d_r) <= tau_r);
+          float ratio_r = bad_r ? 0.f : fabsf(d_r) / tau_r;
+          float ratio_c = 0.f;
+          if (bad_r) {
+            atomicAdd(&aux->nbad_r, 1);
+            aux->bad_row = r;
+            aux->d_row = d_r;
+          }
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) {
+            const int j = h * 128 + r;
+            const float tot = colsum[j] + colsum[BN + j] + colsum[2 * BN + j] + colsum[3 * BN + j];
+            const float d_c = tot - cc[h] * unscale_a;
+            if (!(fabsf(d_c) <= tau_c)) {
+              atomicAdd(&aux->nbad_c, 1);
+              aux->bad_col = j;
+              aux->d_col = d_c;
+            } else {
+              ratio_c = fmaxf(ratio_c, fabsf(d_c) / tau_c);
+            }
+          }
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) {
+            ratio_r = fmaxf(ratio_r, __shfl_xor_sync(0xffffffffu, ratio_r, off));
+            ratio_c = fmaxf(ratio_c, __shfl_xor_sync(0xffffffffu, ratio_c, off));
+          }
+          if (lane == 0) {
+            atomicMax(reinterpret_cast<int*>(&p.report->max_ratio_row), __float_as_int(ratio_r));
+            atomicMax(reinterpret_cast<int*>(&p.report->max_ratio_col), __float_as_int(ratio_c));
+          }
+          named_bar_sync(1, kEpiThreads);  // mismatch counts complete
+
+          const int nbr = aux->nbad_r, nbc = aux->nbad_c;
+          const int brow = aux->bad_row, bcol = aux->bad_col;
+          const bool single = (nbr == 1 && nbc == 1);
+          if (et == 0) atomicAdd(&p.report->tiles_checked, 1u);
+          if (single && (brow >> 5) == q) {
+            // Locate at (brow, bcol); recompute the value from the row
+            // checksum and the rest of the row (survives Inf / NaN).
+            float rest = 0.f, before = 0.f;
+#pragma unroll 1
+            for (int c32 = 0; c32 < BN / 32; ++c32) {
+              uint32_t u[32];
+              tmem_ld32(tacc + c32 * 32, u);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float x = f32_of(u[i]);
+                if (c32 * 32 + i == bcol) before = x;
+                else rest += x;
+              }
+            }
+            if (r == brow) {
+              const float after = cr - rest;
+              aux->fix_value = after;
+              atomicAdd(&p.report->detected, 1u);
+              atomicAdd(&p.report->corrected, 1u);
+              atomicOr(&p.report->status_bits, 1u << SKG_ABFT_CORRECTED);
+              const uint32_t idx = atomicAdd(&p.report->n_records, 1u);
+              if (idx < SKG_MAX_RECORDS) {
+                skg_fault_record_t* rec = &p.report->records[idx];
+                rec->launch = epoch;
+                rec->tile = w.tile;
+                rec->row = brow;
+                rec->col = bcol;
+                rec->status = SKG_ABFT_CORRECTED;
+                rec->n_bad_rows = nbr;
+                rec->n_bad_cols = nbc;
+                rec->injected = inject_here ? 1u : 0u;
+                rec->before = before;
+                rec->after = after;
+                rec->delta_row = aux->d_row;
+                rec->delta_col = aux->d_col;
+                rec->clean_value = inject_here ? aux->inj_clean : 0.f;
+              }
+            }
+          } else if (!single && (nbr != 0 || nbc != 0) && et == 0) {
+            atomicAdd(&p.report->detected, 1u);
+            atomicAdd(&p.report->uncorrectable, 1u);
+            atomicOr(&p.report->status_bits, 1u << SKG_ABFT_UNCORRECTABLE);
+            const uint32_t idx = atomicAdd(&p.report->n_records, 1u);
+            if (idx < SKG_MAX_RECORDS) {
+              skg_fault_record_t* rec = &p.report->records[idx];
+              rec->launch = epoch;
+              rec->tile = w.tile;
+              rec->row = nbr == 1 ? brow : -1;
+              rec->col = nbc == 1 ? bcol : -1;
+              rec->status = SKG_ABFT_UNCORRECTABLE;
+              rec->n_bad_rows = nbr;
+              rec->n_bad_cols = nbc;
+              rec->injected = inject_here ? 1u : 0u;
+              rec->before = 0.f;
+              rec->after = 0.f;
+              rec->delta_row = nbr ? aux->d_row : 0.f;
+              rec->delta_col = nbc ? aux->d_col : 0.f;
+              rec->clean_value = inject_here ? aux->inj_clean : 0.f;
+            }
+          }
+          named_bar_sync(1, kEpiThreads);  // corrected value published
+          if (single) {
+            fix_row = brow;
+            fix_col = bcol;
+            fix_val = aux->fix_value;
+          }
+          named_bar_sync(1, kEpiThreads);  // everyone has read the verdict
+          if (et == 0) {
+            aux->nbad_r = 0;
+            aux->nbad_c = 0;
+            aux->bad_row = -1;
+            aux->bad_col = -1;
+          }
+        }
+
+        // ------------------------------------------------ StoreTile
+        const bool rows_live = (m0 + q * 32) < p.m;
+#pragma unroll 1
+        for (int c = 0; c < BN / C::EPI_COLS; ++c) {
+          float y[C::EPI_COLS];
+#pragma unroll
+          for (int hh = 0; hh < C::EPI_COLS / 32; ++hh) {
+            uint32_t u[32];
+            const int c32 = c * (C::EPI_COLS / 32) + hh;
+            tmem_ld32(tacc + c32 * 32, u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[hh * 32 + i] = f32_of(u[i]);
+            if (!C::ABFT) {
+              if (owner) {
+                for (int peer = blockIdx.x + 1; peer <= w.peer_last; ++peer) {
+                  float* ps = p.partials + (size_t)peer * kBM * BN;
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    const float4 a = ld_cg_f4(partial_at(ps, c32 * 8 + j, r));
+                    y[hh * 32 + 4 * j] += a.x;
+                    y[hh * 32 + 4 * j + 1] += a.y;
+                    y[hh * 32 + 4 * j + 2] += a.z;
+                    y[hh * 32 + 4 * j + 3] += a.w;
+                  }
+                }
+              }
+              if (inject_here && r == p.inject_row && (p.inject_col >> 5) == c32) {
+                const int jc = p.inject_col & 31;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (i == jc)
+                    y[hh * 32 + i] =
+                        __uint_as_float(__float_as_uint(y[hh * 32 + i]) ^ (1u << p.inject_bit));
+              }
+            } else if (r == fix_row && (fix_col >> 5) == c32) {
+              const int jc = fix_col & 31;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i == jc) y[hh * 32 + i] = fix_val;
+            }
+          }
+          if (c == BN / C::EPI_COLS - 1) {
+            // Accumulator fully read: hand the TMEM buffer back to the MMA warp.
+            tc_fence_before();
+            mbar_arrive(&tempty_bar[ab]);
+          }
+          const int col0 = n0 + c * C::EPI_COLS;
+          if (!rows_live || col0 >= p.n || !store_ok) continue;  // warp-uniform
+          uint8_t* buf = ebuf + bsel * C::EPI_BUF_BYTES;
+          if (lane == 0) bulk_wait_read<C::EPI_BUFS - 1>();
+          __syncwarp();
+          if (p.beta != 0.f) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&c0_bar[ew], C::EPI_BUF_BYTES);
+              tma_load_2d(buf, &tmC, &c0_bar[ew], col0, m0 + q * 32);
+            }
+            const bool got_c0 = __all_sync(0xffffffffu, wait_bar(&c0_bar[ew], c0_phase, aux, limit));
+            if (!got_c0) {
+              if (lane == 0 && !aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+              store_ok = false;  // stop storing; the next tile boundary exits
+              continue;
+            }
+            c0_phase ^= 1;
+            uint32_t w0[32];
+            staging_read(buf, lane, w0);
+            float c0v[C::EPI_COLS];
+            unpack_row<C::OUT>(w0, c0v);
+#pragma unroll
+            for (int i = 0; i < C::EPI_COLS; ++i) y[i] = p.alpha * y[i] + p.beta * c0v[i];
+          } else {
+#pragma unroll
+            for (int i = 0; i < C::EPI_COLS; ++i) y[i] = p.alpha * y[i];
+          }
+          uint32_t wout[32];
+          pack_row<C::OUT>(y, wout);
+          staging_write(buf, lane, wout);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, buf, col0, m0 + q * 32);
+            bulk_commit();
+          }
+          bsel = (bsel + 1) % C::EPI_BUFS;
+        }
+      }
+      if (++ab == ACC_BUFS) {
+        ab = 0;
+        aphase ^= 1;
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+  if (threadIdx.x == 0) {
+    if (p.cta_clock) p.cta_clock[2 * blockIdx.x + 1] = globaltimer();
+    __threadfence();
+    const uint32_t ticket = atomicAdd(&p.hdr->done, 1u);
+    if (ticket == gridDim.x - 1) {
+      // Last CTA of the launch: every CTA has read the epoch and the encode
+      // maxima, so advance the epoch and clear the maxima for the next launch.
+      p.hdr->done = 0;
+      p.hdr->maxabs_bits[0] = p.hdr->maxabs_bits[1] = 0;
+      p.hdr->maxenc_bits[0] = p.hdr->maxenc_bits[1] = 0;
+      atomicAdd(&p.report->launches, 1u);
+      __threadfence();
+      atomicAdd(&p.hdr->epoch, 1u);
+    }
+  }
+}
+
+}  // namespace skg

@@ -1,0 +1,129 @@
+"""CPU-only checks of the C-ABI library: it loads without a GPU, exports every
+symbol include/skgemm.h declares, its host schedule query equals the oracle's
+schedule simulator bit-exactly, and argument errors are returned
+synchronously (nothing reaches the device)."""
+import ctypes
+import os
+import random
+import re
+
+import pytest
+
+from oracle import schedule_sim as ss
+from stream_decomposition_abft_gb300 import _build, skgemm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return skgemm.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "skgemm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(skg_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for name in names:
+        assert hasattr(lib, name), f"libskgemm.so does not export {name}"
+    assert set(skgemm.SYMBOLS) == set(names)
+
+
+def test_struct_sizes_match_header():
+    # Sizes fixed by the header's field lists (x86-64 and aarch64 ABIs agree).
+    assert ctypes.sizeof(skgemm.Opts) == 72
+    assert ctypes.sizeof(skgemm.Segment) == 20
+    assert ctypes.sizeof(skgemm.FaultRecord) == 64
+    assert ctypes.sizeof(skgemm.Report) == 64 + 64 * 64
+
+
+def test_defaults(lib):
+    o = skgemm.opts_default()
+    assert o.sched == skgemm.SCHED_SK2_DP and o.inject_tile == -1 and o.abft == 0
+    assert skgemm.status_string(0) == "ok"
+    assert "timed out" in skgemm.status_string(skgemm.ERR_FIXUP_TIMEOUT)
+
+
+MODES = {"dp": skgemm.SCHED_DP, "sk": skgemm.SCHED_SK, "dp_sk1": skgemm.SCHED_DP_SK1,
+         "sk2_dp": skgemm.SCHED_SK2_DP}
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+def test_schedule_query_matches_simulator_configs(lib, mode):
+    # The workloads' shapes with the kernel's tiles, on 148 CTAs and on the
+    # page's hypothetical 4-SM GPU.
+    shapes = [(384, 384, 128), (1664, 1664, 8192), (2560, 2432, 4096), (256, 256, 65536),
+              (128, 19072, 2048), (4096, 4096, 4096), (8192, 1024, 8192)]
+    for (m, n, k) in shapes:
+        for bn in (128, 256):
+            for g in (4, 148):
+                got = skgemm.schedule_query(m, n, k, 128, bn, 64, g, MODES[mode])
+                want = ss.flatten(ss.schedule(m, n, k, 128, bn, 64, g, mode=mode))
+                assert got == want, (m, n, k, bn, g, mode)
+
+
+def test_schedule_query_matches_simulator_random(lib):
+    rnd = random.Random(2024)
+    for _ in range(300):
+        m, n, k = rnd.randint(1, 3000), rnd.randint(1, 3000), rnd.randint(1, 5000)
+        bn = rnd.choice([128, 256])
+        bk = rnd.choice([4, 32, 64])
+        g = rnd.randint(1, 160)
+        mode = rnd.choice(list(MODES))
+        got = skgemm.schedule_query(m, n, k, 128, bn, bk, g, MODES[mode])
+        want = ss.flatten(ss.schedule(m, n, k, 128, bn, bk, g, mode=mode))
+        assert got == want, (m, n, k, bn, bk, g, mode)
+
+
+def test_schedule_query_page_example(lib):
+    # Stream-K page, Fig. 2b: 384x384x128, BLK_K = 4, g = 4 -> 72 iterations each.
+    rows = skgemm.schedule_query(384, 384, 128, 128, 128, 4, 4, skgemm.SCHED_SK)
+    per = [0, 0, 0, 0]
+    for (cta, tile, b, e, role) in rows:
+        per[cta] += e - b
+    assert per == [72, 72, 72, 72]
+
+
+def test_argument_errors_are_synchronous(lib):
+    o = skgemm.opts_default()
+    args = dict(alpha=1.0, beta=0.0, in_dtype=skgemm.IN_BF16, out_dtype=skgemm.OUT_BF16,
+                a_layout=0, b_layout=0, opts=o, ws_ptr=None, ws_bytes=0, stream=None)
+
+    def call(m, n, k, A=16, lda=64, B=16, ldb=64, C=16, ldc=64, **kw):
+        a = dict(args)
+        a.update(kw)
+        return skgemm.gemm(m, n, k, a["alpha"], A, lda, B, ldb, a["beta"], C, ldc,
+                           a["in_dtype"], a["out_dtype"], a["a_layout"], a["b_layout"],
+                           a["opts"], a["ws_ptr"], a["ws_bytes"], a["stream"])
+
+    assert call(-1, 4, 4) == skgemm.ERR_ARG
+    assert call(4, 4, 4, in_dtype=7) == skgemm.ERR_ARG
+    assert call(4, 4, 4, out_dtype=9) == skgemm.ERR_ARG
+    assert call(4, 4, 4, a_layout=1) == skgemm.ERR_UNSUPPORTED
+    assert call(0, 4, 4) == skgemm.OK                 # empty output: nothing to do
+    assert call(4, 4, 4, C=None) == skgemm.ERR_ARG
+    assert call(4, 64, 4, ldc=32) == skgemm.ERR_ARG     # ldc < n
+    assert call(4, 4, 4, C=24) == skgemm.ERR_UNSUPPORTED  # C not 16-byte aligned
+    assert call(4, 4, 4, ldc=5) == skgemm.ERR_UNSUPPORTED  # ldc * 2 bytes not a multiple of 16
+    assert call(4, 4, 64, lda=32) == skgemm.ERR_ARG    # lda < k
+    assert call(4, 4, 60, lda=60, ldb=64) == skgemm.ERR_UNSUPPORTED  # lda * 2 % 16 != 0
+    assert call(4, 4, 4, A=None) == skgemm.ERR_ARG
+
+
+def test_workspace_size_scales_with_grid_not_problem(lib):
+    # Stream-K page, §4 / conclusion: the fixup storage grows with g, not with
+    # the problem size.
+    o = skgemm.opts_default(grid=148, tile_n=128)
+    small = skgemm.workspace_size(1024, 1024, 1024, o)
+    big = skgemm.workspace_size(8192, 8192, 8192, o)
+    assert small == big
+    o2 = skgemm.opts_default(grid=74, tile_n=128)
+    assert skgemm.workspace_size(1024, 1024, 1024, o2) < small
+    oa = skgemm.opts_default(grid=148, tile_n=128, abft=1)
+    assert skgemm.workspace_size(1024, 1024, 1024, oa) > small

@@ -1,0 +1,278 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Floating point is compared under the parity tolerance of gpu_util; the
+schedule (device trace) and ABFT decisions are compared exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import abft_ref as ab
+from oracle import schedule_sim as ss
+from stream_decomposition_abft_gb300 import _build, inputs, skgemm
+
+from gpu_util import check_full, check_sampled, check_checksum_probe, reference, run
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["dp", "sk", "dp_sk1", "sk2_dp"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    _build.build()
+    skgemm.lib()
+
+
+def sms():
+    return skgemm.device_sm_count()
+
+
+def device_trace(p, opts_kw, g):
+    trace = torch.zeros(g * skgemm.TRACE_STRIDE, dtype=torch.int32, device="cuda")
+    opts = skgemm.opts_default(grid=g, trace=trace.data_ptr(), **opts_kw)
+    C, ws, st = run(p, opts)
+    assert st == skgemm.OK
+    torch.cuda.synchronize()
+    tr = trace.cpu().numpy().reshape(g, skgemm.TRACE_STRIDE)
+    rows = []
+    for x in range(g):
+        cnt = int(tr[x, 0])
+        for i in range(cnt):
+            t, b, e, role = tr[x, 1 + 4 * i: 5 + 4 * i]
+            rows.append((x, int(t), int(b), int(e), int(role)))
+    return rows, C, ws
+
+
+# --------------------------------------------------------------------------- example
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("g", [4, 148])
+def test_example_384_parity_and_trace(mode, g):
+    g = min(g, sms())
+    p = inputs.example_384()
+    ref = reference(p)
+    for tile_n in (128, 256):
+        rows, C, ws = device_trace(p, dict(sched=mode, tile_n=tile_n), g)
+        check_full(p, C, ref)
+        want = ss.flatten(ss.schedule(384, 384, 128, 128, tile_n, 64, g, mode=mode))
+        assert rows == want
+        rep = ws.report()
+        assert rep.status_bits == 0 and rep.launches == 1
+
+
+# --------------------------------------------------------------------------- shapes
+SMALL = [
+    (300, 500, 200, "bf16", "bf16"),
+    (129, 257, 64, "f16", "f32"),
+    (128, 128, 64, "bf16", "f32"),
+    (1, 1, 8, "f16", "f16"),
+    (17, 33, 1000, "bf16", "bf16"),
+    (640, 768, 1536, "f16", "f16"),
+    (1000, 1300, 520, "bf16", "f32"),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL)
+@pytest.mark.parametrize("mode", MODES)
+def test_small_shapes(shape, mode):
+    m, n, k, dt_in, dt_out = shape
+    p = inputs.make_problem(m, n, k, seed=m * 7 + n, in_dtype=dt_in, out_dtype=dt_out,
+                            law_a="normal", law_b="uniform", alpha=0.75, beta=-0.5)
+    ref = reference(p)
+    for tile_n in (128, 256):
+        for g in (7, sms()):
+            C, ws, st = run(p, skgemm.opts_default(sched=mode, tile_n=tile_n, grid=g))
+            assert st == skgemm.OK
+            check_full(p, C, ref)
+
+
+@pytest.mark.parametrize("k", [1, 7, 65, 100, 129])
+def test_ragged_k_with_padded_ld(k):
+    # k not a multiple of 8 needs a padded row stride (TMA stride rule);
+    # the tail of the last MAC iteration is zero-filled by the TMA engine.
+    ld = (k + 7) // 8 * 8
+    p = inputs.make_problem(200, 300, k, seed=k, in_dtype="f16", out_dtype="f32",
+                            law_a="uniform", law_b="uniform")
+    ref = reference(p)
+    C, ws, st = run(p, skgemm.opts_default(sched="sk", grid=min(40, sms())), lda=ld, ldb=ld)
+    assert st == skgemm.OK
+    check_full(p, C, ref)
+    if k % 8:
+        _, _, st = run(p, skgemm.opts_default())
+        assert st == skgemm.ERR_UNSUPPORTED
+
+
+def test_k_zero_scales_c():
+    p = inputs.make_problem(100, 60, 0, seed=3, in_dtype="bf16", out_dtype="f32", beta=2.0)
+    C, ws, st = run(p, skgemm.opts_default())
+    assert st == skgemm.OK
+    assert torch.equal(C.cpu(), (2.0 * p.C0.float()))
+
+
+def test_integer_inputs_exact():
+    # Integer-valued inputs: every product and partial sum is exact in fp32,
+    # so the GPU must equal the oracle exactly, on every schedule.
+    p = inputs.make_problem(512, 640, 768, seed=21, in_dtype="bf16", out_dtype="f32",
+                            law_a="integer", law_b="integer")
+    ref = reference(p)
+    for mode in MODES:
+        C, ws, st = run(p, skgemm.opts_default(sched=mode, grid=min(37, sms())))
+        assert st == skgemm.OK
+        assert np.array_equal(C.cpu().double().numpy(), ref), mode
+
+
+# --------------------------------------------------------------------------- Stream-K fixup
+@pytest.mark.parametrize("g", [2, 3, 16, 64, 148])
+def test_many_peers_per_tile(g):
+    # Basic Stream-K on few tiles and many CTAs: each owner accumulates
+    # several peers (the page's Fig. 9 case: one tile, deep k).
+    g = min(g, sms())
+    p = inputs.make_problem(256, 256, 8192, seed=g, in_dtype="f16", out_dtype="f32",
+                            law_a="uniform", law_b="uniform", alpha=1.5, beta=0.5)
+    ref = reference(p)
+    rows, C, ws = device_trace(p, dict(sched="sk", tile_n=128), g)
+    check_full(p, C, ref)
+    assert rows == ss.flatten(ss.schedule(256, 256, 8192, 128, 128, 64, g, mode="sk"))
+
+
+def test_workspace_reuse_across_launches():
+    # Flags carry the launch epoch: back-to-back launches on one workspace
+    # never read a stale partial.
+    opts = skgemm.opts_default(sched="sk", grid=sms(), tile_n=128)
+    ws = None
+    for i in range(6):
+        p = inputs.make_problem(384, 512, 2048, seed=100 + i, in_dtype="bf16", out_dtype="f32",
+                                law_a="normal", law_b="normal")
+        C, ws, st = run(p, opts, ws=ws)
+        assert st == skgemm.OK
+        check_full(p, C)
+    assert ws.report().launches == 6
+
+
+def test_fixup_timeout_reports_and_returns():
+    # A CTA skips its Signal, so its owner's bounded wait runs out: the
+    # launch must end with SKG_ERR_FIXUP_TIMEOUT recorded, and the context
+    # stay usable.
+    p = inputs.make_problem(256, 256, 4096, seed=5, in_dtype="bf16", out_dtype="f32")
+    rows = ss.flatten(ss.schedule(256, 256, 4096, 128, 128, 64, 8, mode="sk"))
+    peer = next(r[0] for r in rows if r[4] == ss.PEER)
+    opts = skgemm.opts_default(sched="sk", grid=8, tile_n=128, timeout_ns=50_000_000,
+                               test_drop_signal=peer + 1)
+    C, ws, st = run(p, opts)
+    assert st == skgemm.OK
+    rep = ws.report()
+    assert rep.status_bits & (1 << skgemm.ERR_FIXUP_TIMEOUT)
+    assert rep.timeouts >= 1
+    # the device still works
+    p2 = inputs.make_problem(128, 128, 128, seed=6, in_dtype="bf16", out_dtype="f32")
+    C2, ws2, st2 = run(p2, skgemm.opts_default())
+    assert st2 == skgemm.OK
+    check_full(p2, C2)
+    assert ws2.report().status_bits == 0
+
+
+# --------------------------------------------------------------------------- workloads
+def test_hostile_shapes():
+    for i, (m, n, k) in enumerate(inputs.HOSTILE_SHAPES):
+        p = inputs.hostile(m, n, k)
+        for tile_n in (128, 256):
+            C, ws, st = run(p, skgemm.opts_default(tile_n=tile_n))
+            assert st == skgemm.OK
+            if m * n * k <= 2 ** 33:
+                check_full(p, C)
+            else:
+                check_sampled(p, C, seed=i)
+            check_checksum_probe(p, C)
+            assert ws.report().status_bits == 0
+
+
+@pytest.mark.parametrize("size", inputs.SQUARE_SIZES)
+def test_square_sweep_abft(size):
+    p = inputs.square(size)
+    C, ws, st = run(p, skgemm.opts_default(abft=1))
+    assert st == skgemm.OK
+    check_sampled(p, C, seed=size)
+    check_checksum_probe(p, C)
+    rep = ws.report()
+    tiles = ((size + 127) // 128) * ((size + 127) // 128)
+    assert rep.detected == 0 and rep.status_bits == 0, "false positive on a clean run"
+    assert rep.tiles_checked == tiles
+    assert rep.max_ratio_row < 0.1 and rep.max_ratio_col < 0.1, \
+        (rep.max_ratio_row, rep.max_ratio_col)
+
+
+@pytest.mark.parametrize("shape", inputs.MLP_SHAPES)
+def test_mlp_shapes_abft(shape):
+    p = inputs.mlp(*shape)
+    C, ws, st = run(p, skgemm.opts_default(abft=1))
+    assert st == skgemm.OK
+    check_sampled(p, C, seed=sum(shape), count=512, rows=4, cols=4)
+    rep = ws.report()
+    assert rep.detected == 0 and rep.status_bits == 0
+    assert rep.max_ratio_row < 0.1 and rep.max_ratio_col < 0.1
+
+
+def test_random_shapes_subset():
+    shapes = inputs.random_shapes(1000)
+    for idx in range(0, 1000, 50):
+        m, n, k = shapes[idx]
+        p = inputs.random_problem(m, n, k, idx)
+        C, ws, st = run(p, skgemm.opts_default())
+        assert st == skgemm.OK
+        check_sampled(p, C, seed=idx, count=128, rows=2, cols=2)
+
+
+# --------------------------------------------------------------------------- ABFT faults
+def _inject(p, opts_kw, tile, row, col, bit):
+    opts = skgemm.opts_default(abft=1, inject_tile=tile, inject_row=row, inject_col=col,
+                               inject_bit=bit, **opts_kw)
+    return run(p, opts)
+
+
+@pytest.mark.parametrize("mode", ["dp", "sk", "sk2_dp"])
+@pytest.mark.parametrize("bit", [30, 29, 26, 23, 31])
+def test_injected_fault_detected_located_corrected(mode, bit):
+    p = inputs.make_problem(512, 640, 1024, seed=77, in_dtype="bf16", out_dtype="f32",
+                            law_a="normal", law_b="normal", scale_b=0.02)
+    ref = reference(p)
+    tiles_n = (640 + 127) // 128
+    rng = np.random.default_rng(bit)
+    tile = int(rng.integers(0, 4 * tiles_n))
+    row, col = int(rng.integers(0, 128)), int(rng.integers(0, 128))
+    tm, tn = divmod(tile, tiles_n)
+    gi, gj = tm * 128 + row, tn * 128 + col
+    v = ref[gi, gj] / p.alpha
+    tau = ab.default_tau(p.k, 128, float(p.A.abs().max()), float(p.B.abs().max()))
+    kind, delta = ab.classify_flip(v, bit, tau, 1e-3 * tau)
+    C, ws, st = _inject(p, dict(sched=mode, tile_n=128, grid=min(64, sms())), tile, row, col, bit)
+    assert st == skgemm.OK
+    rep = ws.report()
+    if kind == ab.MUST_DETECT:
+        assert rep.detected == 1 and rep.corrected == 1 and rep.uncorrectable == 0
+        rec = rep.records[0]
+        assert (rec.tile, rec.row, rec.col, rec.injected) == (tile, row, col, 1)
+        # the flip is exactly one bit of the GPU's own pre-fault value
+        assert ab.flip_f32(rec.clean_value, bit) == rec.before or \
+            (np.isnan(rec.before) and np.isnan(ab.flip_f32(rec.clean_value, bit)))
+        check_full(p, C, ref)   # corrected output is within parity tolerance
+    else:
+        pytest.skip(f"bit {bit} of {v} is {kind} at tau {tau}")
+
+
+def test_injection_without_abft_corrupts_output():
+    p = inputs.make_problem(256, 256, 256, seed=9, in_dtype="bf16", out_dtype="f32",
+                            law_a="normal", law_b="normal")
+    ref = reference(p)
+    opts = skgemm.opts_default(inject_tile=1, inject_row=5, inject_col=7, inject_bit=30)
+    C, ws, st = run(p, opts)
+    assert st == skgemm.OK
+    got = C.cpu().double().numpy()
+    tn = 256 // skgemm.launch_shape(256, 256, 256, opts)[0]
+    tm, tnn = divmod(1, tn)
+    bad = (tm * 128 + 5, tnn * skgemm.launch_shape(256, 256, 256, opts)[0] + 7)
+    diff = np.abs(got - ref)
+    assert not (diff[bad] < 1e-3)       # the flipped value reached C
+    diff[bad] = 0
+    assert diff.max() < 1e-2            # and nothing else changed
