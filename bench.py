@@ -1,0 +1,444 @@
+#!/usr/bin/env python
+"""Benchmark: Stream-K + ABFT GEMM on the square bf16 sweep.
+
+Workload: C = A B with m = n = k in {1024, 2048, 3072, 4096, 5120, 6144},
+bf16 inputs drawn N(0,1)/sqrt(k) (seed 1), fp32 accumulation, bf16 output,
+ABFT checksum verification on. One step runs the whole hot path on every
+shape once: the ABFT encode pass (skg_abft_encode) and the persistent
+Stream-K kernel (skg_gemm), each launch bracketed by CUDA events on the
+launching stream, with a 256 MiB write between launches so no shape starts
+with its operands in the 129 MB L2.
+
+Metric: GEMM TFLOPS = 2mnk / time, geomean over the sweep, and its fraction
+of the GB300 dense bf16 peak. The JSON line also carries the roofline of the
+dominant kernel, the oracle CPU baseline, an end-to-end number through host
+buffers, the launch count and the SM clocks seen during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With torchrun (N > 1) every rank runs the same sweep on its own GPU
+(replicas: the GEMM has no exchange step); value aggregates all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOPS (2mnk/s) and % of GB300 dense bf16 peak; geomean over shape sweep"
+FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ("stream_decomposition_abft_gb300/csrc/skg_kernel.cuh",
+                  "stream_decomposition_abft_gb300/csrc/skg_ptx.cuh",
+                  "stream_decomposition_abft_gb300/csrc/skg_sched.cuh")
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get("bf16_tflops", 1900.0), d.get("bf16_tflops_sustained", 1700.0), \
+            d.get("hbm_gbs", 6800.0), "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def geomean(xs):
+    return math.exp(sum(math.log(x) for x in xs) / len(xs)) if xs else 0.0
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index),
+                                          f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------- ours
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from stream_decomposition_abft_gb300 import _build, inputs, skgemm
+
+    if not os.path.exists(skgemm.LIB_PATH):
+        _build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    sms = skgemm.device_sm_count()
+    opts = skgemm.opts_default(abft=1, abft_preencoded=1)
+    enc_opts = skgemm.opts_default(abft=1)
+
+    problems = []
+    for size in inputs.SQUARE_SIZES:
+        p = inputs.square(size)
+        A = p.A.to(dev)
+        B = p.B.to(dev)
+        C = torch.empty((size, size), dtype=torch.bfloat16, device=dev)
+        ws = skgemm.Workspace(skgemm.workspace_size(size, size, size, opts), dev)
+        problems.append(dict(size=size, p=p, A=A, B=B, C=C, ws=ws))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    tile_n, grid = skgemm.launch_shape(4096, 4096, 4096, opts)
+
+    def launch(pr):
+        s = pr["size"]
+        st = skgemm.abft_encode(s, s, s, pr["A"].data_ptr(), s, pr["B"].data_ptr(), s,
+                                skgemm.IN_BF16, enc_opts, pr["ws"].ptr, pr["ws"].nbytes, sh)
+        if st != skgemm.OK:
+            raise skgemm.SkgError(st, "skg_abft_encode")
+        pr["ev"][1].record(stream)
+        st = skgemm.gemm(s, s, s, 1.0, pr["A"].data_ptr(), s, pr["B"].data_ptr(), s, 0.0,
+                         pr["C"].data_ptr(), s, skgemm.IN_BF16, skgemm.OUT_BF16, 0, 0, opts,
+                         pr["ws"].ptr, pr["ws"].nbytes, sh)
+        if st != skgemm.OK:
+            raise skgemm.SkgError(st, "skg_gemm")
+
+    def step(record):
+        for pr in problems:
+            flush.zero_()
+            if record:
+                pr["ev"] = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                pr["ev"][0].record(stream)
+            else:
+                pr["ev"] = [None, _Dummy(), None]
+            launch(pr)
+            if record:
+                pr["ev"][2].record(stream)
+                pr["events"].append(pr["ev"])
+
+    for pr in problems:
+        pr["events"] = []
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    for pr in problems:
+        pr["ws"].report(reset=True)
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+
+    per_shape = []
+    total_main_ms = 0.0
+    total_main_flops = 0.0
+    abft = {"tiles_checked": 0, "detected": 0, "max_ratio_row": 0.0, "max_ratio_col": 0.0}
+    for pr in problems:
+        s = pr["size"]
+        full = [e[0].elapsed_time(e[2]) for e in pr["events"]]
+        main = [e[1].elapsed_time(e[2]) for e in pr["events"]]
+        enc = [e[0].elapsed_time(e[1]) for e in pr["events"]]
+        t_full = statistics.mean(full)
+        t_main = statistics.mean(main)
+        flops = 2.0 * s * s * s
+        per_shape.append({"m": s, "n": s, "k": s, "ms": round(t_full, 5),
+                          "ms_main_kernel": round(t_main, 5),
+                          "ms_encode": round(statistics.mean(enc), 5),
+                          "tflops": round(flops / t_full / 1e9, 2),
+                          "tflops_main_kernel": round(flops / t_main / 1e9, 2)})
+        total_main_ms += sum(main)
+        total_main_flops += flops * len(main)
+        rep = pr["ws"].report()
+        abft["tiles_checked"] += rep.tiles_checked
+        abft["detected"] += rep.detected
+        abft["max_ratio_row"] = max(abft["max_ratio_row"], rep.max_ratio_row)
+        abft["max_ratio_col"] = max(abft["max_ratio_col"], rep.max_ratio_col)
+
+    # Aggregate over ranks (replicas): per-shape time = max over ranks.
+    times = [ps["ms"] for ps in per_shape]
+    if world > 1:
+        t = torch.tensor(times, dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        times = t.tolist()
+    value = geomean([world * 2.0 * ps["m"] ** 3 / t / 1e9 for ps, t in zip(per_shape, times)])
+
+    e2e = measure_e2e(args, problems, dev, stream, opts, enc_opts)
+
+    if rank != 0:
+        return
+    burst, sustained, hbm, peak_kind = peaks()
+    props = torch.cuda.get_device_properties(dev)
+    fmax = clocks.get("sm_max_mhz") or 2070.0
+    spec_peak = props.multi_processor_count * 8192 * fmax * 1e6 / 1e12
+    achieved = total_main_flops / (total_main_ms * 1e-3) / 1e12
+    traffic = load_traffic()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(sum(times), 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "square bf16 sweep m=n=k in {1024,2048,3072,4096,5120,6144}, "
+                               "N(0,1)/sqrt(k) inputs (seed 1), fp32 accumulate, bf16 out, "
+                               "ABFT verify on",
+                   "sched": "sk2_dp", "tile": f"128x{tile_n}x64", "grid": grid, "sms": sms,
+                   "l2": "flushed between launches (256 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_peak": {"measured_burst": round(100 * value / world / burst, 2),
+                        "spec_at_max_clock": round(100 * value / world / spec_peak, 2),
+                        "peak_measured_tflops": burst, "peak_spec_tflops": round(spec_peak, 1),
+                        "peak_kind": peak_kind},
+        "per_shape": per_shape,
+        "roofline": {"bound": "tensor", "kernel": "skg_gemm_kernel (Stream-K mainloop + ABFT)",
+                     "achieved": round(achieved, 2), "peak": burst,
+                     "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
+                     "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)",
+                     "traffic": traffic},
+        "abft": abft,
+        "gpu_launches": 4 * len(problems) * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": round(wall, 3),
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+class _Dummy:
+    def record(self, stream=None):
+        pass
+
+
+def measure_e2e(args, problems, dev, stream, opts, enc_opts):
+    """Same metric through the public C ABI with host buffers: each step
+    copies A and B from pinned host memory, runs the ABFT GEMM and copies C
+    back, all inside the timed region."""
+    import torch
+    from stream_decomposition_abft_gb300 import skgemm
+    sh = stream.cuda_stream
+    steps = max(3, min(args.steps, 10))
+    h2d = d2h = 0
+    tf = []
+    for pr in problems:
+        s = pr["size"]
+        hA = pr["p"].A.pin_memory()
+        hB = pr["p"].B.pin_memory()
+        hC = torch.empty((s, s), dtype=torch.bfloat16).pin_memory()
+        evs = []
+        for i in range(steps + 1):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            pr["A"].copy_(hA, non_blocking=True)
+            pr["B"].copy_(hB, non_blocking=True)
+            st = skgemm.gemm_verify(s, s, s, 1.0, pr["A"].data_ptr(), s, pr["B"].data_ptr(), s,
+                                    0.0, pr["C"].data_ptr(), s, skgemm.IN_BF16, skgemm.OUT_BF16,
+                                    0, 0, None, pr["ws"].ptr, pr["ws"].nbytes, sh)
+            if st != skgemm.OK:
+                raise skgemm.SkgError(st, "skg_gemm_verify")
+            hC.copy_(pr["C"], non_blocking=True)
+            e1.record(stream)
+            if i:
+                evs.append((e0, e1))
+        torch.cuda.synchronize()
+        t = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        tf.append(2.0 * s ** 3 / t / 1e9)
+        h2d += hA.numel() * 2 + hB.numel() * 2
+        d2h += hC.numel() * 2
+    return {"value": round(geomean(tf), 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def load_traffic():
+    """DRAM bytes per launch of the main kernel from the committed ncu summary,
+    or None when the kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "skg_gemm_kernel_square_sweep_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch_mean")
+
+
+# ---------------------------------------------------------------------------- oracle
+def cpu_baseline(budget_s: float = 15.0, shapes=None):
+    """The fp64 oracle as it stands, on a bounded sample of the sweep: for
+    each shape, whole rows of C (every entry a k-long dot product), as many
+    as fit in budget_s / len(shapes) seconds. Reported in TFLOPS."""
+    import oracle
+    from stream_decomposition_abft_gb300 import inputs
+    shapes = shapes or inputs.SQUARE_SIZES
+    oracle.build()
+    per = budget_s / len(shapes)
+    rates, rows_done = [], []
+
+    def rows_of_c(p, lo, hi):
+        s = p.n
+        r = [i for i in range(lo, hi) for _ in range(s)]
+        c = list(range(s)) * (hi - lo)
+        t0 = time.perf_counter()
+        oracle.gemm_entries(p.A, p.B, r, c)
+        return time.perf_counter() - t0
+
+    for size in shapes:
+        p = inputs.square(size)
+        dt = rows_of_c(p, 0, 1)                      # calibrate on one row
+        more = max(0, min(size - 1, int((per - dt) / max(dt, 1e-6))))
+        if more:
+            dt += rows_of_c(p, 1, 1 + more)
+        rates.append(2.0 * (1 + more) * size * size / dt / 1e12)
+        rows_done.append(1 + more)
+    return {"value": geomean(rates), "unit": "TFLOPS", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": "fp64 triple-loop oracle (OpenMP) on whole rows of C for each sweep shape: "
+                      + ", ".join(f"{s}^3: {r} rows" for s, r in zip(shapes, rows_done)),
+            "per_shape_tflops": [round(x, 8) for x in rates]}
+
+
+def run_reference(args, rank):
+    """The reference arm: the oracle timed on the host cores on bounded
+    samples of the same workload, K steps after W warm-up steps."""
+    if rank != 0:
+        return
+    import oracle
+    from stream_decomposition_abft_gb300 import inputs
+    oracle.build()
+    probs = [inputs.square(s) for s in inputs.SQUARE_SIZES]
+    rows_per_step = 1
+
+    def one_step(i):
+        ts = []
+        for p in probs:
+            s = p.m
+            row = (i * 7919) % s
+            r = [row] * s
+            c = list(range(s))
+            t0 = time.perf_counter()
+            oracle.gemm_entries(p.A, p.B, r, c)
+            ts.append(time.perf_counter() - t0)
+        return ts
+
+    for i in range(args.warmup):
+        one_step(i)
+    per = [[] for _ in probs]
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        for j, t in enumerate(one_step(args.warmup + i)):
+            per[j].append(t)
+    wall = time.perf_counter() - t0
+    rates = [2.0 * rows_per_step * p.m * p.m / statistics.mean(ts) / 1e12
+             for p, ts in zip(probs, per)]
+    value = geomean(rates)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * wall / max(1, args.steps), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "square bf16 sweep m=n=k in {1024,...,6144} (oracle: one "
+                                   "row of C per shape per step)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.threads(),
+                             "kind": "oracle",
+                             "sample": "one whole row of C per sweep shape per step"},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -132,7 +132,9 @@ typedef struct {
   int32_t test_drop_signal; /* testing only: 1 + index of a CTA that skips its
                            Stream-K Signal, so the owner's bounded wait runs out
                            and the launch reports SKG_ERR_FIXUP_TIMEOUT; 0 = none */
-  int32_t reserved0;
+  int32_t abft_preencoded; /* 1 = skg_abft_encode already wrote this call's
+                           encodings (same A, B, shape and options) into the
+                           workspace, so skg_gemm skips its encode pass */
 } skg_opts_t;
 
 /* One segment of a schedule (Stream-K page, Algorithm 5 / §5.2). k_iter_*
@@ -224,6 +226,19 @@ skg_status_t skg_gemm_verify(int64_t m, int64_t n, int64_t k, float alpha, const
                              int64_t ldc, int32_t in_dtype, int32_t out_dtype, int32_t a_layout,
                              int32_t b_layout, const skg_opts_t* opts, void* workspace,
                              size_t ws_bytes, void* stream);
+
+/* The ABFT encode pass of skg_gemm_verify on its own: e^T A over each
+ * 128-row tile of A and B e over each BLK_N-column tile of B, split into
+ * three input-precision terms, plus max|A| and max|B| for the default
+ * thresholds ("Anatomy of High-Performance GEMM with Online Fault Tolerance
+ * on GPUs", threadblock-level ABFT, Fig. 5: the encodings e^T A and B e of
+ * each threadblock's operands). Arguments as for skg_gemm (opts decides
+ * BLK_N and must be the options of the gemm call that follows with
+ * opts->abft_preencoded = 1). Asynchronous on `stream`. */
+skg_status_t skg_abft_encode(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
+                             const void* B, int64_t ldb, int32_t in_dtype,
+                             const skg_opts_t* opts, void* workspace, size_t ws_bytes,
+                             void* stream);
 
 /* The schedule the kernel runs, computed on the host: for every CTA, its
  * ordered segments (tile, k-iteration range, role). bm, bn, bk are the tile

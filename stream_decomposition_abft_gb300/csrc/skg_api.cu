@@ -67,14 +67,14 @@ struct Resolved {
   int32_t* trace;
   uint64_t* cta_clock;
   int drop_signal;
+  int preencoded;
 };
 
 // BLK_N choice: 256 columns halve the A-operand shared-memory reads per
-// MMA and keep both TMEM accumulator buffers (2 x 256 columns) when ABFT is
-// off; with ABFT on, 128 columns keep the accumulator double-buffered
-// (2 x (128 + 32) columns). Narrow outputs (n <= 128) use 128.
+// MMA and still leave room for two TMEM accumulator buffers (2 x 256
+// columns). Narrow outputs (n <= 128) use 128.
 int auto_tile_n(int64_t n, int abft) {
-  if (abft) return 128;
+  (void)abft;
   return n <= 128 ? 128 : 256;
 }
 
@@ -103,12 +103,16 @@ skg_status_t resolve(int64_t n, const skg_opts_t* o, Resolved& r, int sms) {
   r.trace = o->trace;
   r.cta_clock = o->cta_clock;
   r.drop_signal = o->test_drop_signal - 1;
+  r.preencoded = o->abft_preencoded ? 1 : 0;
   return SKG_OK;
 }
 
+// Workspace layout. Partial-tile slots are sized for the widest tile any
+// launch of the call uses (the ABFT checksum GEMMs may use BLK_N = 256).
 struct Layout {
-  size_t flags, partials, csum, sums, enc, total;
+  size_t flags, partials, sums, enc, blockmax, cr, cc, total;
   int kp, tiles_a, tiles_b;
+  int64_t ld_cr, ld_cc;
 };
 
 Layout layout(int64_t m, int64_t n, int64_t k, const Resolved& r) {
@@ -117,18 +121,25 @@ Layout layout(int64_t m, int64_t n, int64_t k, const Resolved& r) {
   L.flags = off;
   off = round_up(off + (size_t)r.grid * 4, 256);
   L.partials = off;
-  off = round_up(off + (size_t)r.grid * kBM * r.bn * 4, 256);
-  L.csum = off;
-  off = round_up(off + (size_t)r.grid * kCsumStride * 4, 256);
+  const int slot_n = r.abft ? 256 : r.bn;
+  off = round_up(off + (size_t)r.grid * kBM * slot_n * 4, 256);
   L.kp = (int)round_up((size_t)(k > 0 ? k : 1), kBK);
   L.tiles_a = (int)((m + kBM - 1) / kBM);
   L.tiles_b = (int)((n + r.bn - 1) / r.bn);
-  L.sums = L.enc = off;
+  L.ld_cr = (int64_t)round_up((size_t)kEncRows * L.tiles_b, 4);
+  L.ld_cc = (int64_t)round_up((size_t)(n > 0 ? n : 1), 4);
+  L.sums = L.enc = L.blockmax = L.cr = L.cc = off;
   if (r.abft) {
     L.sums = off;
     off = round_up(off + (size_t)(L.tiles_a + L.tiles_b) * L.kp * 4, 256);
     L.enc = off;
     off = round_up(off + (size_t)(L.tiles_a + L.tiles_b) * kEncRows * L.kp * 2, 256);
+    L.blockmax = off;
+    off = round_up(off + (size_t)(L.tiles_a + L.tiles_b) * encode_slices(L.kp) * 8, 256);
+    L.cr = off;
+    off = round_up(off + (size_t)m * L.ld_cr * 4, 256);
+    L.cc = off;
+    off = round_up(off + (size_t)kEncRows * L.tiles_a * L.ld_cc * 4, 256);
   }
   L.total = off;
   return L;
@@ -149,99 +160,65 @@ CUresult make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, cons
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// One launch of the persistent kernel: C = alpha A B^T + beta C with A
+// (m x k, row stride lda) and B (n x k, row stride ldb) in `in_dtype`.
+struct Gemm {
+  int64_t m, n, k;
+  const void* A;
+  int64_t lda;
+  const void* B;
+  int64_t ldb;
+  void* C;
+  int64_t ldc;
+  float alpha, beta;
+  int in_dtype, out_dtype;
+};
+
 template <int BN, bool ABFT>
 cudaError_t dispatch_out(int out_dtype, const CUtensorMap& a, const CUtensorMap& b,
-                         const CUtensorMap& c, const CUtensorMap& ea, const CUtensorMap& eb,
-                         const KernelParams& p, int grid, cudaStream_t st) {
+                         const CUtensorMap& c, const KernelParams& p, int grid,
+                         cudaStream_t st) {
   switch (out_dtype) {
-    case SKG_OUT_F32: return launch_gemm<BN, ABFT, 0>(a, b, c, ea, eb, p, grid, st);
-    case SKG_OUT_F16: return launch_gemm<BN, ABFT, 1>(a, b, c, ea, eb, p, grid, st);
-    default: return launch_gemm<BN, ABFT, 2>(a, b, c, ea, eb, p, grid, st);
+    case SKG_OUT_F32: return launch_gemm<BN, ABFT, 0>(a, b, c, p, grid, st);
+    case SKG_OUT_F16: return launch_gemm<BN, ABFT, 1>(a, b, c, p, grid, st);
+    default: return launch_gemm<BN, ABFT, 2>(a, b, c, p, grid, st);
   }
 }
 
-skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void* A, int64_t lda,
-                       const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
-                       int32_t in_dtype, int32_t out_dtype, int32_t a_layout, int32_t b_layout,
-                       const skg_opts_t* opts, int force_abft, void* workspace,
-                       size_t ws_bytes, void* stream_v) {
-  cudaStream_t stream = (cudaStream_t)stream_v;
-  if (m < 0 || n < 0 || k < 0) return SKG_ERR_ARG;
-  if (m > INT32_MAX / 2 || n > INT32_MAX / 2 || k > INT32_MAX / 2) return SKG_ERR_UNSUPPORTED;
-  if (in_dtype != SKG_IN_F16 && in_dtype != SKG_IN_BF16) return SKG_ERR_ARG;
-  if (out_dtype < SKG_OUT_F32 || out_dtype > SKG_OUT_BF16) return SKG_ERR_ARG;
-  if (a_layout != SKG_A_ROW || b_layout != SKG_B_KMAJOR) return SKG_ERR_UNSUPPORTED;
-  if (m == 0 || n == 0) return SKG_OK;
-  const int out_bytes = out_dtype == SKG_OUT_F32 ? 4 : 2;
-  if (!C) return SKG_ERR_ARG;
-  if (ldc < n) return SKG_ERR_ARG;
-  if (!aligned16(C) || (ldc * out_bytes) % 16) return SKG_ERR_UNSUPPORTED;
-  if (k == 0) {
-    return launch_scale(out_dtype, C, ldc, (int)m, (int)n, beta, stream) == cudaSuccess
-               ? SKG_OK
-               : SKG_ERR_CUDA;
-  }
-  if (!A || !B) return SKG_ERR_ARG;
-  if (lda < k || ldb < k) return SKG_ERR_ARG;
-  if (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 || (ldb * 2) % 16)
-    return SKG_ERR_UNSUPPORTED;
-
-  const int sms = sm_count_cached();
-  if (sms <= 0) return SKG_ERR_CUDA;
-  Resolved r;
-  skg_status_t st = resolve(n, opts, r, sms);
-  if (st != SKG_OK) return st;
-  if (force_abft) r.abft = 1, r.bn = (opts && opts->tile_n) ? opts->tile_n : auto_tile_n(n, 1);
-  if (r.inject_tile >= 0 && r.inject_col >= r.bn) return SKG_ERR_ARG;
-  const Layout L = layout(m, n, k, r);
-  if (!workspace || !aligned16(workspace) || ws_bytes < L.total) return SKG_ERR_WORKSPACE;
-  if (!tensor_map_encoder()) return SKG_ERR_CUDA;
-
-  uint8_t* ws = (uint8_t*)workspace;
-  const CUtensorMapDataType in_t =
-      in_dtype == SKG_IN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const CUtensorMapDataType out_t = out_dtype == SKG_OUT_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                    : out_dtype == SKG_OUT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  CUtensorMap tmA, tmB, tmC, tmEA, tmEB;
-  if (make_map(&tmA, in_t, 2, A, (uint64_t)k, (uint64_t)m, (uint64_t)lda, kBK, kBM) !=
+skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, uint8_t* ws,
+                        const Layout& L, cudaStream_t stream) {
+  const CUtensorMapDataType in_t = g.in_dtype == SKG_IN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType out_t = g.out_dtype == SKG_OUT_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                    : g.out_dtype == SKG_OUT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int out_bytes = g.out_dtype == SKG_OUT_F32 ? 4 : 2;
+  CUtensorMap tmA, tmB, tmC;
+  if (make_map(&tmA, in_t, 2, g.A, (uint64_t)g.k, (uint64_t)g.m, (uint64_t)g.lda, kBK, kBM) !=
           CUDA_SUCCESS ||
-      make_map(&tmB, in_t, 2, B, (uint64_t)k, (uint64_t)n, (uint64_t)ldb, kBK, r.bn) !=
+      make_map(&tmB, in_t, 2, g.B, (uint64_t)g.k, (uint64_t)g.n, (uint64_t)g.ldb, kBK, r.bn) !=
           CUDA_SUCCESS ||
-      make_map(&tmC, out_t, out_bytes, C, (uint64_t)n, (uint64_t)m, (uint64_t)ldc,
+      make_map(&tmC, out_t, out_bytes, g.C, (uint64_t)g.n, (uint64_t)g.m, (uint64_t)g.ldc,
                128 / out_bytes, 32) != CUDA_SUCCESS)
     return SKG_ERR_UNSUPPORTED;
-  tmEA = tmA;
-  tmEB = tmB;
-  WsHeader* hdr = (WsHeader*)ws;
-  if (r.abft) {
-    void* enc = ws + L.enc;
-    void* enc_b = (uint8_t*)enc + (size_t)L.tiles_a * kEncRows * L.kp * 2;
-    if (make_map(&tmEA, in_t, 2, enc, (uint64_t)L.kp, (uint64_t)L.tiles_a * kEncRows,
-                 (uint64_t)L.kp, kBK, kEncRows) != CUDA_SUCCESS ||
-        make_map(&tmEB, in_t, 2, enc_b, (uint64_t)L.kp, (uint64_t)L.tiles_b * kEncRows,
-                 (uint64_t)L.kp, kBK, kEncRows) != CUDA_SUCCESS)
-      return SKG_ERR_UNSUPPORTED;
-    if (launch_encode(in_dtype == SKG_IN_BF16, A, lda, (int)m, B, ldb, (int)n, (int)k, L.kp,
-                      r.bn, (float*)(ws + L.sums), enc, hdr, stream) != cudaSuccess)
-      return SKG_ERR_CUDA;
-  }
 
   KernelParams p;
   memset(&p, 0, sizeof(p));
-  p.s = make_schedule(m, n, k, kBM, r.bn, kBK, r.grid, r.sched);
-  p.m = (int)m;
-  p.n = (int)n;
-  p.k = (int)k;
-  p.alpha = alpha;
-  p.beta = beta;
-  p.idesc_main = idesc_f16(in_dtype == SKG_IN_BF16, kBM, r.bn);
-  p.idesc_ck = idesc_f16(in_dtype == SKG_IN_BF16, kBM, 16);
-  p.hdr = hdr;
+  p.s = make_schedule(g.m, g.n, g.k, kBM, r.bn, kBK, r.grid, r.sched);
+  p.m = (int)g.m;
+  p.n = (int)g.n;
+  p.k = (int)g.k;
+  p.alpha = g.alpha;
+  p.beta = g.beta;
+  p.idesc_main = idesc_f16(g.in_dtype == SKG_IN_BF16, kBM, r.bn);
+  p.hdr = (WsHeader*)ws;
   p.report = (skg_report_t*)(ws + 256);
   p.flags = (uint32_t*)(ws + L.flags);
   p.partials = (float*)(ws + L.partials);
-  p.csum = (float*)(ws + L.csum);
+  p.cr_all = (const float*)(ws + L.cr);
+  p.cc_all = (const float*)(ws + L.cc);
+  p.ld_cr = L.ld_cr;
+  p.ld_cc = L.ld_cc;
   p.tau_row = r.tau_row;
   p.tau_col = r.tau_col;
   p.inject_tile = r.inject_tile;
@@ -255,12 +232,98 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
 
   cudaError_t e;
   if (r.bn == 128)
-    e = r.abft ? dispatch_out<128, true>(out_dtype, tmA, tmB, tmC, tmEA, tmEB, p, r.grid, stream)
-               : dispatch_out<128, false>(out_dtype, tmA, tmB, tmC, tmEA, tmEB, p, r.grid, stream);
+    e = abft_epilogue ? dispatch_out<128, true>(g.out_dtype, tmA, tmB, tmC, p, r.grid, stream)
+                      : dispatch_out<128, false>(g.out_dtype, tmA, tmB, tmC, p, r.grid, stream);
   else
-    e = r.abft ? dispatch_out<256, true>(out_dtype, tmA, tmB, tmC, tmEA, tmEB, p, r.grid, stream)
-               : dispatch_out<256, false>(out_dtype, tmA, tmB, tmC, tmEA, tmEB, p, r.grid, stream);
+    e = abft_epilogue ? dispatch_out<256, true>(g.out_dtype, tmA, tmB, tmC, p, r.grid, stream)
+                      : dispatch_out<256, false>(g.out_dtype, tmA, tmB, tmC, p, r.grid, stream);
   return e == cudaSuccess ? SKG_OK : SKG_ERR_CUDA;
+}
+
+// The ABFT reference checksums of every output tile ("Anatomy of
+// High-Performance GEMM with Online Fault Tolerance on GPUs", Fig. 3:
+// C^r = A (B e), C^c = (e^T A) B): the encode pass, then two skinny GEMMs
+// on the same persistent kernel with fp32 output:
+//   cr_all (m x 3 tiles_b) = A      x [Be_hi; Be_mid; Be_lo]^T
+//   cc_all (3 tiles_a x n) = [eA_hi; eA_mid; eA_lo] x B^T
+skg_status_t reference_checksums(const Gemm& g, const Resolved& r, uint8_t* ws, const Layout& L,
+                                 cudaStream_t stream) {
+  void* enc = ws + L.enc;
+  void* enc_b = (uint8_t*)enc + (size_t)L.tiles_a * kEncRows * L.kp * 2;
+  if (launch_encode(g.in_dtype == SKG_IN_BF16, g.A, g.lda, (int)g.m, g.B, g.ldb, (int)g.n,
+                    (int)g.k, L.kp, r.bn, (float*)(ws + L.sums), (float2*)(ws + L.blockmax), enc,
+                    (WsHeader*)ws, stream) != cudaSuccess)
+    return SKG_ERR_CUDA;
+  Resolved rc = r;
+  rc.abft = 0;
+  rc.sched = SKG_SCHED_SK2_DP;
+  rc.inject_tile = -1;
+  rc.trace = nullptr;
+  rc.cta_clock = nullptr;
+  rc.drop_signal = -1;
+  Gemm g1{g.m, (int64_t)kEncRows * L.tiles_b, g.k, g.A, g.lda, enc_b, L.kp, ws + L.cr, L.ld_cr,
+          1.f, 0.f, g.in_dtype, SKG_OUT_F32};
+  rc.bn = g1.n <= 128 ? 128 : 256;
+  skg_status_t st = launch_one(g1, rc, false, ws, L, stream);
+  if (st != SKG_OK) return st;
+  Gemm g2{(int64_t)kEncRows * L.tiles_a, g.n, g.k, enc, L.kp, g.B, g.ldb, ws + L.cc, L.ld_cc,
+          1.f, 0.f, g.in_dtype, SKG_OUT_F32};
+  rc.bn = g2.n <= 128 ? 128 : 256;
+  return launch_one(g2, rc, false, ws, L, stream);
+}
+
+skg_status_t check_inputs(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
+                          const void* B, int64_t ldb) {
+  if (!A || !B) return SKG_ERR_ARG;
+  if (lda < k || ldb < k) return SKG_ERR_ARG;
+  if (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 || (ldb * 2) % 16)
+    return SKG_ERR_UNSUPPORTED;
+  (void)m;
+  (void)n;
+  return SKG_OK;
+}
+
+skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void* A, int64_t lda,
+                       const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
+                       int32_t in_dtype, int32_t out_dtype, int32_t a_layout, int32_t b_layout,
+                       const skg_opts_t* opts, int force_abft, void* workspace,
+                       size_t ws_bytes, void* stream_v) {
+  cudaStream_t stream = (cudaStream_t)stream_v;
+  if (m < 0 || n < 0 || k < 0) return SKG_ERR_ARG;
+  if (m > INT32_MAX / 4 || n > INT32_MAX / 4 || k > INT32_MAX / 4) return SKG_ERR_UNSUPPORTED;
+  if (in_dtype != SKG_IN_F16 && in_dtype != SKG_IN_BF16) return SKG_ERR_ARG;
+  if (out_dtype < SKG_OUT_F32 || out_dtype > SKG_OUT_BF16) return SKG_ERR_ARG;
+  if (a_layout != SKG_A_ROW || b_layout != SKG_B_KMAJOR) return SKG_ERR_UNSUPPORTED;
+  if (m == 0 || n == 0) return SKG_OK;
+  const int out_bytes = out_dtype == SKG_OUT_F32 ? 4 : 2;
+  if (!C) return SKG_ERR_ARG;
+  if (ldc < n) return SKG_ERR_ARG;
+  if (!aligned16(C) || (ldc * out_bytes) % 16) return SKG_ERR_UNSUPPORTED;
+  if (k == 0) {
+    return launch_scale(out_dtype, C, ldc, (int)m, (int)n, beta, stream) == cudaSuccess
+               ? SKG_OK
+               : SKG_ERR_CUDA;
+  }
+  skg_status_t st = check_inputs(m, n, k, A, lda, B, ldb);
+  if (st != SKG_OK) return st;
+
+  const int sms = sm_count_cached();
+  if (sms <= 0) return SKG_ERR_CUDA;
+  Resolved r;
+  st = resolve(n, opts, r, sms);
+  if (st != SKG_OK) return st;
+  if (force_abft) r.abft = 1;
+  const Layout L = layout(m, n, k, r);
+  if (!workspace || !aligned16(workspace) || ws_bytes < L.total) return SKG_ERR_WORKSPACE;
+  if (!tensor_map_encoder()) return SKG_ERR_CUDA;
+
+  uint8_t* ws = (uint8_t*)workspace;
+  const Gemm g{m, n, k, A, lda, B, ldb, C, ldc, alpha, beta, in_dtype, out_dtype};
+  if (r.abft && !r.preencoded) {
+    st = reference_checksums(g, r, ws, L, stream);
+    if (st != SKG_OK) return st;
+  }
+  return launch_one(g, r, r.abft != 0, ws, L, stream);
 }
 
 }  // namespace
@@ -304,6 +367,29 @@ skg_status_t skg_gemm_verify(int64_t m, int64_t n, int64_t k, float alpha, const
                              size_t ws_bytes, void* stream) {
   return gemm_impl(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, a_layout,
                    b_layout, opts, 1, workspace, ws_bytes, stream);
+}
+
+skg_status_t skg_abft_encode(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
+                             const void* B, int64_t ldb, int32_t in_dtype,
+                             const skg_opts_t* opts, void* workspace, size_t ws_bytes,
+                             void* stream) {
+  if (m < 0 || n < 0 || k < 0) return SKG_ERR_ARG;
+  if (m > INT32_MAX / 4 || n > INT32_MAX / 4 || k > INT32_MAX / 4) return SKG_ERR_UNSUPPORTED;
+  if (in_dtype != SKG_IN_F16 && in_dtype != SKG_IN_BF16) return SKG_ERR_ARG;
+  if (m == 0 || n == 0 || k == 0) return SKG_OK;
+  skg_status_t st = check_inputs(m, n, k, A, lda, B, ldb);
+  if (st != SKG_OK) return st;
+  const int sms = sm_count_cached();
+  if (sms <= 0) return SKG_ERR_CUDA;
+  Resolved r;
+  st = resolve(n, opts, r, sms);
+  if (st != SKG_OK) return st;
+  r.abft = 1;
+  const Layout L = layout(m, n, k, r);
+  if (!workspace || !aligned16(workspace) || ws_bytes < L.total) return SKG_ERR_WORKSPACE;
+  if (!tensor_map_encoder()) return SKG_ERR_CUDA;
+  const Gemm g{m, n, k, A, lda, B, ldb, nullptr, 0, 1.f, 0.f, in_dtype, SKG_OUT_F32};
+  return reference_checksums(g, r, (uint8_t*)workspace, L, (cudaStream_t)stream);
 }
 
 skg_status_t skg_schedule_query(int64_t m, int64_t n, int64_t k, int32_t bm, int32_t bn,

@@ -6,21 +6,20 @@ namespace skg {
 
 template <int BN, bool ABFT, int OUT>
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                        const CUtensorMap& tmEA, const CUtensorMap& tmEB, const KernelParams& p,
-                        int grid, cudaStream_t stream) {
+                        const KernelParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<BN, ABFT, OUT>;
   cudaError_t e = cudaFuncSetAttribute(skg_gemm_kernel<C>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  skg_gemm_kernel<C><<<grid, kThreads, C::SMEM_BYTES, stream>>>(tmA, tmB, tmC, tmEA, tmEB, p);
+  skg_gemm_kernel<C><<<grid, kThreads, C::SMEM_BYTES, stream>>>(tmA, tmB, tmC, p);
   return cudaGetLastError();
 }
 
 #define SKG_INST(OUT)                                                                        \
   template cudaError_t launch_gemm<128, false, OUT>( \
-      const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,       \
-      const CUtensorMap&, const KernelParams&, int, cudaStream_t);
+      const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KernelParams&, int, \
+      cudaStream_t);
 SKG_INST(0)
 SKG_INST(1)
 SKG_INST(2)

@@ -22,17 +22,19 @@
 //               (§4), so C needs no atomics.
 //
 // ABFT ("Anatomy of High-Performance GEMM with Online Fault Tolerance on
-// GPUs", Figs. 3 and 5-7): the encodings e^T A (per 128-row tile) and B e
-// (per BLK_N-column tile) are pre-computed once and split into three
-// input-precision terms; at every k step the MMA warp also issues
-//   cr += A_tile * [Be_hi, Be_mid, Be_lo]          (N = 16, row checksums)
-//   cc += B_tile * [eA_hi, eA_mid, eA_lo]          (N = 16, column checksums)
-// into spare TMEM columns, so both reference checksums are updated online on
-// the tensor pipe. The epilogue forms the row sums (in-thread) and column
-// sums (warp transpose-reduction + shared memory) of the accumulator,
-// compares them with cr and cc, locates a single fault at the mismatching
-// row and column, replaces it by cr[i*] - sum_{j != j*} acc[i*, j], and only
-// then applies alpha / beta and stores.
+// GPUs", Figs. 3 and 5-7): before this kernel runs, the encode pass forms
+// e^T A per 128-row tile and B e per BLK_N-column tile, and two skinny
+// tensor-core GEMMs (this same kernel, fp32 out) form the reference
+// checksums cr = A (B e) and cc = (e^T A) B of every output tile. Here the
+// epilogue of each tile's owner, after the Stream-K fixup, forms the row sums
+// (in-thread) and column sums (warp transpose-reduction + shared memory) of
+// the fp32 accumulator, compares them with cr and cc, locates a single fault
+// at the mismatching row and column, replaces it by
+// cr[i*] - sum_{j != j*} acc[i*, j], and only then applies alpha / beta and
+// stores. The checksums never pass through the mainloop, so the MMA reads
+// each operand tile from shared memory once (a separate N = 16 checksum MMA
+// would read the whole A or B tile again and halve the tensor-core rate on
+// shared-memory bandwidth).
 //
 // Every wait (mbarrier or peer flag) is bounded by a %globaltimer deadline;
 // on expiry the kernel records the error in the workspace report, sets a
@@ -53,16 +55,15 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
-constexpr int kEncRows = 3;  // hi, mid, lo
-constexpr int kCsumStride = 384;  // floats per CTA of partial checksums
+constexpr int kEncRows = 3;  // hi, mid, lo terms of each encoding
 constexpr uint32_t kSmemLimit = 232448;
 
 // Workspace header (device). The report follows at offset 256.
 struct WsHeader {
   uint32_t epoch;          // launches completed on this workspace
   uint32_t done;           // CTA tickets of the running launch
-  uint32_t maxabs_bits[2]; // max |A|, max |B| (fp32 bits) from the encode pass
-  uint32_t maxenc_bits[2]; // max |e^T A|, max |B e| (fp32 bits)
+  uint32_t maxabs_bits[2]; // max |A|, max |B| (fp32 bits), written by the encode pass
+  uint32_t maxenc_bits[2]; // max |e^T A|, max |B e| (fp32 bits), same
   int32_t scale_exp[2];    // encodings are stored scaled by 2^scale_exp
   uint32_t pad[56];
 };
@@ -73,12 +74,15 @@ struct KernelParams {
   int m, n, k;
   float alpha, beta;
   uint32_t idesc_main;
-  uint32_t idesc_ck;
   WsHeader* hdr;
   skg_report_t* report;
   uint32_t* flags;
   float* partials;
-  float* csum;
+  // ABFT reference checksums (hi, mid, lo partial products, scaled):
+  // cr_all[(row) * ld_cr + 3 * tn + t] and cc_all[(3 * tm + t) * ld_cc + col].
+  const float* cr_all;
+  const float* cc_all;
+  int64_t ld_cr, ld_cc;
   float tau_row, tau_col;  // <= 0: derive from the encode pass maxima
   int inject_tile, inject_row, inject_col, inject_bit;
   uint64_t timeout_ns;
@@ -100,19 +104,20 @@ struct Cfg {
   static constexpr int OUT = OUT_;  // 0 = f32, 1 = f16, 2 = bf16
   static constexpr int OUT_BYTES = OUT == 0 ? 4 : 2;
   static constexpr int EPI_COLS = 128 / OUT_BYTES;  // one 128-byte staging row
-  static constexpr int CK_COLS = ABFT ? 16 + 16 * (BN / 128) : 0;
-  static constexpr int ACC_COLS = BN + CK_COLS;
+  static constexpr int ACC_COLS = BN;
   static constexpr int ACC_BUFS = (2 * ACC_COLS <= 512) ? 2 : 1;
   static constexpr int TMEM_COLS = pow2_at_least(ACC_BUFS * ACC_COLS);
   static constexpr int A_BYTES = kBM * kBK * 2;
   static constexpr int B_BYTES = BN * kBK * 2;
-  static constexpr int ENC_BYTES = ABFT ? 16 * 128 : 0;  // 16 rows x 128 B
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + 2 * ENC_BYTES;
-  static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + (ABFT ? 2 * kEncRows * 128 : 0);
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_BUF_BYTES = 32 * 128;
   static constexpr int EPI_BUFS = 2;
   static constexpr int EPI_BYTES = 4 * EPI_BUFS * EPI_BUF_BYTES;
-  static constexpr int AUX_BYTES = 512 + (ABFT ? 4 * BN * 4 : 0);
+  static constexpr int AUX_BYTES = 512;
+  // The ABFT column partial sums of warp q (BN floats) live in warp q's own
+  // first staging buffer, which is idle while a tile is being verified.
+  static_assert(BN * 4 <= EPI_BUF_BYTES, "column sums must fit one staging buffer");
   static constexpr int STAGES_FIT =
       (int)((kSmemLimit - 1024 - EPI_BYTES - AUX_BYTES) / STAGE_BYTES);
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
@@ -279,9 +284,7 @@ __device__ __forceinline__ float* partial_at(float* slot, int c4, int r) {
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     skg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC,
-                    const __grid_constant__ CUtensorMap tmEA,
-                    const __grid_constant__ CUtensorMap tmEB, const KernelParams p) {
+                    const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
   constexpr int BN = C::BN;
   constexpr int STAGES = C::STAGES;
   constexpr int ACC_BUFS = C::ACC_BUFS;
@@ -291,7 +294,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ring = smem;
   uint8_t* epi = ring + STAGES * C::STAGE_BYTES;
   Aux* aux = reinterpret_cast<Aux*>(epi + C::EPI_BYTES);
-  float* colsum = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(aux) + 512);  // [4][BN]
   uint64_t* full_bar = aux->bars;
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* tfull_bar = empty_bar + STAGES;
@@ -308,10 +310,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
-    if (C::ABFT) {
-      prefetch_tmap(&tmEA);
-      prefetch_tmap(&tmEB);
-    }
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
@@ -327,20 +325,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     aux->bad_row = aux->bad_col = -1;
     fence_barrier_init();
     if (p.cta_clock) p.cta_clock[2 * blockIdx.x] = globaltimer();
-  }
-  if (C::ABFT) {
-    // Rows 3..15 of both 16-row encoding tiles of every stage stay zero; the
-    // TMA only ever writes rows 0..2 (hi, mid, lo).
-    for (int i = threadIdx.x; i < STAGES * 2 * 13 * 8; i += kThreads) {
-      const int st = i / (2 * 13 * 8);
-      const int rem = i % (2 * 13 * 8);
-      const int which = rem / (13 * 8);
-      const int row = 3 + (rem % (13 * 8)) / 8;
-      const int chunk = rem % 8;
-      uint8_t* base = ring + st * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES + which * C::ENC_BYTES;
-      *reinterpret_cast<uint4*>(base + row * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();
   }
   if (warp == 1) {
     tmem_alloc(&aux->tmem_slot, C::TMEM_COLS);
@@ -375,12 +359,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
           tma_load_2d(st, &tmA, &full_bar[stage], kb * kBK, tm * kBM);
           tma_load_2d(st + C::A_BYTES, &tmB, &full_bar[stage], kb * kBK, tn * BN);
-          if (C::ABFT) {
-            tma_load_2d(st + C::A_BYTES + C::B_BYTES, &tmEB, &full_bar[stage], kb * kBK,
-                        tn * kEncRows);
-            tma_load_2d(st + C::A_BYTES + C::B_BYTES + C::ENC_BYTES, &tmEA, &full_bar[stage],
-                        kb * kBK, tm * kEncRows);
-          }
           pending |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -428,15 +406,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = sdesc_sw128(b_addr + kk * 32);
             const uint32_t acc = (kb > w.kb_begin || kk > 0) ? 1u : 0u;
             umma_f16(d, ad, bd, p.idesc_main, acc);
-            if (C::ABFT) {
-              const uint32_t eb = b_addr + C::B_BYTES;
-              const uint32_t ea = eb + C::ENC_BYTES;
-              umma_f16(d + BN, ad, sdesc_sw128(eb + kk * 32), p.idesc_ck, acc);
-#pragma unroll
-              for (int h = 0; h < BN / 128; ++h)
-                umma_f16(d + BN + 16 + 16 * h, sdesc_sw128(b_addr + h * 16384 + kk * 32),
-                         sdesc_sw128(ea + kk * 32), p.idesc_ck, acc);
-            }
           }
           issued = true;
           umma_commit(&empty_bar[stage]);
@@ -466,6 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;     // tile row of this thread
     const int et = threadIdx.x - 64; // epilogue thread 0..127
     uint8_t* ebuf = epi + ew * C::EPI_BUFS * C::EPI_BUF_BYTES;
+    // Column partial sums of the warp owning lane quadrant qq.
+    auto colsum_of = [&](int qq) -> float* {
+      const int ew_of_q = (qq + 2) & 3;  // warps 2..5 own quadrants 2, 3, 0, 1
+      return reinterpret_cast<float*>(epi + ew_of_q * C::EPI_BUFS * C::EPI_BUF_BYTES);
+    };
     const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr->epoch) + 1u;
     float* my_slot = p.partials + (size_t)blockIdx.x * kBM * BN;
 
@@ -531,17 +505,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                      make_float4(f32_of(u[4 * j]), f32_of(u[4 * j + 1]), f32_of(u[4 * j + 2]),
                                  f32_of(u[4 * j + 3])));
         }
-        if (C::ABFT) {
-          uint32_t t4[4];
-          float* cs = p.csum + (size_t)blockIdx.x * kCsumStride;
-          tmem_ld4(tacc + BN, t4);
-          __stcg(cs + r, f32_of(t4[0]) + f32_of(t4[1]) + f32_of(t4[2]));
-#pragma unroll
-          for (int h = 0; h < BN / 128; ++h) {
-            tmem_ld4(tacc + BN + 16 + 16 * h, t4);
-            __stcg(cs + 128 + 128 * h + r, f32_of(t4[0]) + f32_of(t4[1]) + f32_of(t4[2]));
-          }
-        }
         tc_fence_before();
         mbar_arrive(&tempty_bar[ab]);
         named_bar_sync(1, kEpiThreads);
@@ -580,6 +543,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int fix_row = -1, fix_col = -1;
         float fix_val = 0.f;
         if (C::ABFT) {
+          // This warp's staging buffers hold its column sums below: its own
+          // earlier TMA stores must have finished reading them.
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          float* my_colsum = colsum_of(q);
           float rowsum = 0.f;
 #pragma unroll 1
           for (int c32 = 0; c32 < BN / 32; ++c32) {
@@ -622,26 +590,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int i = 0; i < 32; ++i) rowsum += v[i];
-            colsum[q * BN + c32 * 32 + lane] = warp_column_sums(v, lane);
+            my_colsum[c32 * 32 + lane] = warp_column_sums(v, lane);
           }
-          // Reference checksums accumulated on the tensor pipe. Thread r
-          // holds the row checksum of row r and the column checksum of
-          // column h*128 + r (TMEM lane r of the column-checksum MMA).
-          uint32_t t4[4];
-          tmem_ld4(tacc + BN, t4);
-          float cr = f32_of(t4[0]) + f32_of(t4[1]) + f32_of(t4[2]);
+          // Reference checksums of this tile: thread r holds the row checksum
+          // of row r and the column checksum of columns h*128 + r, each the
+          // sum of its hi, mid and lo partial products.
+          float cr = 0.f;
+          if (m0 + r < p.m) {
+            const float* crp = p.cr_all + (int64_t)(m0 + r) * p.ld_cr + kEncRows * tn;
+            cr = __ldcg(crp) + __ldcg(crp + 1) + __ldcg(crp + 2);
+          }
           float cc[BN / 128];
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h) {
-            tmem_ld4(tacc + BN + 16 + 16 * h, t4);
-            cc[h] = f32_of(t4[0]) + f32_of(t4[1]) + f32_of(t4[2]);
-          }
-          if (owner) {
-            for (int peer = blockIdx.x + 1; peer <= w.peer_last; ++peer) {
-              const float* cs = p.csum + (size_t)peer * kCsumStride;
-              cr += __ldcg(cs + r);
-#pragma unroll
-              for (int h = 0; h < BN / 128; ++h) cc[h] += __ldcg(cs + 128 + 128 * h + r);
+            const int col = n0 + h * 128 + r;
+            cc[h] = 0.f;
+            if (col < p.n) {
+              const float* ccp = p.cc_all + (int64_t)(kEncRows * tm) * p.ld_cc + col;
+              cc[h] = __ldcg(ccp) + __ldcg(ccp + p.ld_cc) + __ldcg(ccp + 2 * p.ld_cc);
             }
           }
           cr *= unscale_b;
@@ -659,7 +625,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h) {
             const int j = h * 128 + r;
-            const float tot = colsum[j] + colsum[BN + j] + colsum[2 * BN + j] + colsum[3 * BN + j];
+            const float tot =
+                colsum_of(0)[j] + colsum_of(1)[j] + colsum_of(2)[j] + colsum_of(3)[j];
             const float d_c = tot - cc[h] * unscale_a;
             if (!(fabsf(d_c) <= tau_c)) {
               atomicAdd(&aux->nbad_c, 1);
@@ -865,11 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     const uint32_t ticket = atomicAdd(&p.hdr->done, 1u);
     if (ticket == gridDim.x - 1) {
-      // Last CTA of the launch: every CTA has read the epoch and the encode
-      // maxima, so advance the epoch and clear the maxima for the next launch.
+      // Last CTA of the launch: every CTA has read the epoch, so advance it.
       p.hdr->done = 0;
-      p.hdr->maxabs_bits[0] = p.hdr->maxabs_bits[1] = 0;
-      p.hdr->maxenc_bits[0] = p.hdr->maxenc_bits[1] = 0;
       atomicAdd(&p.report->launches, 1u);
       __threadfence();
       atomicAdd(&p.hdr->epoch, 1u);

@@ -39,7 +39,7 @@ class Opts(ctypes.Structure):
                 ("inject_row", ctypes.c_int32), ("inject_col", ctypes.c_int32),
                 ("inject_bit", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64),
                 ("trace", ctypes.c_void_p), ("cta_clock", ctypes.c_void_p),
-                ("test_drop_signal", ctypes.c_int32), ("reserved0", ctypes.c_int32)]
+                ("test_drop_signal", ctypes.c_int32), ("abft_preencoded", ctypes.c_int32)]
 
 
 class Segment(ctypes.Structure):
@@ -69,7 +69,7 @@ class Report(ctypes.Structure):
 
 
 SYMBOLS = ("skg_opts_default", "skg_workspace_size", "skg_workspace_init", "skg_gemm",
-           "skg_gemm_verify", "skg_schedule_query", "skg_launch_shape", "skg_report_read",
+           "skg_gemm_verify", "skg_abft_encode", "skg_schedule_query", "skg_launch_shape", "skg_report_read",
            "skg_device_sm_count", "skg_status_string")
 
 _lib = None
@@ -104,6 +104,9 @@ def lib() -> ctypes.CDLL:
     L.skg_gemm.restype = i32
     L.skg_gemm_verify.argtypes = gemm_args
     L.skg_gemm_verify.restype = i32
+    L.skg_abft_encode.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, ctypes.POINTER(Opts),
+                                  vp, sz, vp]
+    L.skg_abft_encode.restype = i32
     L.skg_schedule_query.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32,
                                      ctypes.POINTER(Segment), i64, ctypes.POINTER(i64)]
     L.skg_schedule_query.restype = i32
@@ -150,6 +153,13 @@ def gemm_verify(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, in_dty
                 a_layout, b_layout, opts, ws_ptr, ws_bytes, stream) -> int:
     return int(lib().skg_gemm_verify(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc,
                                      in_dtype, out_dtype, a_layout, b_layout,
+                                     ctypes.byref(opts) if opts else None, ws_ptr, ws_bytes,
+                                     stream))
+
+
+def abft_encode(m, n, k, A_ptr, lda, B_ptr, ldb, in_dtype, opts, ws_ptr, ws_bytes,
+                stream) -> int:
+    return int(lib().skg_abft_encode(m, n, k, A_ptr, lda, B_ptr, ldb, in_dtype,
                                      ctypes.byref(opts) if opts else None, ws_ptr, ws_bytes,
                                      stream))
 

@@ -196,7 +196,8 @@ def test_square_sweep_abft(size):
     check_sampled(p, C, seed=size)
     check_checksum_probe(p, C)
     rep = ws.report()
-    tiles = ((size + 127) // 128) * ((size + 127) // 128)
+    tile_n, _ = skgemm.launch_shape(size, size, size, skgemm.opts_default(abft=1))
+    tiles = ((size + 127) // 128) * ((size + tile_n - 1) // tile_n)
     assert rep.detected == 0 and rep.status_bits == 0, "false positive on a clean run"
     assert rep.tiles_checked == tiles
     assert rep.max_ratio_row < 0.1 and rep.max_ratio_col < 0.1, \
