@@ -258,6 +258,30 @@ skg_status_t skg_launch_shape(int64_t m, int64_t n, int64_t k, const skg_opts_t*
 skg_status_t skg_report_read(const void* workspace, skg_report_t* out, int32_t reset,
                              void* stream);
 
+/* Size of the fixed device scratch array behind skg_gemm_noalloc. */
+#define SKG_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* skg_gemm without a caller workspace, for callers that cannot allocate
+ * device memory (for example a plugin whose host framework owns all device
+ * memory through its own allocator, or a latency-critical path that cannot
+ * afford cudaMalloc's implicit synchronisation). The pages have no
+ * counterpart: this is a packaging choice of this library. The Stream-K
+ * workspace comes from one file-scope device array of
+ * SKG_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU loading the library
+ * holds until exit; nothing is allocated per call. The first call on a
+ * device sets that device up (looks up the array's address and clears its
+ * header on `stream`), so make it before any stream capture. All calls
+ * share the array and it keeps the last call's contents: calls whose
+ * launches overlap on the GPU race and must not be issued. BLK_N defaults
+ * to 128 here; a shape or option set whose workspace exceeds the array
+ * returns SKG_ERR_WORKSPACE (ABFT does on a 152-SM GPU). Device-side
+ * outcomes are not reported through this entry point. Other arguments as
+ * for skg_gemm. */
+skg_status_t skg_gemm_noalloc(int64_t m, int64_t n, int64_t k, float alpha, const void* A,
+                              int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+                              int64_t ldc, int32_t in_dtype, int32_t out_dtype, int32_t a_layout,
+                              int32_t b_layout, const skg_opts_t* opts, void* stream);
+
 /* Number of SMs of the current device (0 if there is no device). */
 int32_t skg_device_sm_count(void);
 

@@ -70,7 +70,7 @@ class Report(ctypes.Structure):
 
 SYMBOLS = ("skg_opts_default", "skg_workspace_size", "skg_workspace_init", "skg_gemm",
            "skg_gemm_verify", "skg_abft_encode", "skg_schedule_query", "skg_launch_shape", "skg_report_read",
-           "skg_device_sm_count", "skg_status_string")
+           "skg_device_sm_count", "skg_status_string", "skg_gemm_noalloc")
 
 _lib = None
 
@@ -115,6 +115,9 @@ def lib() -> ctypes.CDLL:
     L.skg_launch_shape.restype = i32
     L.skg_report_read.argtypes = [vp, ctypes.POINTER(Report), i32, vp]
     L.skg_report_read.restype = i32
+    L.skg_gemm_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, i32,
+                                   i32, i32, i32, ctypes.POINTER(Opts), vp]
+    L.skg_gemm_noalloc.restype = i32
     L.skg_device_sm_count.argtypes = []
     L.skg_device_sm_count.restype = i32
     L.skg_status_string.argtypes = [i32]
@@ -196,6 +199,15 @@ def report_read(ws_ptr: int, reset: bool = False, stream: int = 0) -> Report:
     if st != OK:
         raise SkgError(st, "skg_report_read")
     return rep
+
+
+def gemm_noalloc(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, in_dtype, out_dtype,
+                 a_layout, b_layout, opts, stream) -> int:
+    """skg_gemm_noalloc: skg_gemm with the workspace taken from the library's
+    fixed device scratch array, for callers that cannot allocate."""
+    return int(lib().skg_gemm_noalloc(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc,
+                                      in_dtype, out_dtype, a_layout, b_layout,
+                                      ctypes.byref(opts) if opts else None, stream))
 
 
 def device_sm_count() -> int:
