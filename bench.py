@@ -138,7 +138,9 @@ def run_ours(args, rank, world, local_rank):
         ws = skgemm.Workspace(skgemm.workspace_size(size, size, size, opts), dev)
         problems.append(dict(size=size, p=p, A=A, B=B, C=C, ws=ws))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    tile_n, grid = skgemm.launch_shape(4096, 4096, 4096, opts)
+    plans = {pr["size"]: skgemm.launch_shape(pr["size"], pr["size"], pr["size"], opts)
+             for pr in problems}
+    sched_names = {v: k for k, v in skgemm.SCHED_NAMES.items()}
 
     def launch(pr):
         s = pr["size"]
@@ -248,7 +250,10 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": "square bf16 sweep m=n=k in {1024,2048,3072,4096,5120,6144}, "
                                "N(0,1)/sqrt(k) inputs (seed 1), fp32 accumulate, bf16 out, "
                                "ABFT verify on",
-                   "sched": "sk2_dp", "tile": f"128x{tile_n}x64", "grid": grid, "sms": sms,
+                   "plan_per_shape": {str(sz): {"tile": f"128x{tn}x64", "grid": g,
+                                                "sched": sched_names[sc]}
+                                      for sz, (tn, g, sc) in plans.items()},
+                   "sms": sms,
                    "l2": "flushed between launches (256 MiB write)",
                    "parallelism": f"replicas x{world}"},
         "pct_of_peak": {"measured_burst": round(100 * value / world / burst, 2),

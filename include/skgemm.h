@@ -73,7 +73,9 @@ typedef enum {
   SKG_SCHED_DP = 0,
   SKG_SCHED_SK = 1,
   SKG_SCHED_DP_SK1 = 2,
-  SKG_SCHED_SK2_DP = 3
+  SKG_SCHED_SK2_DP = 3,
+  SKG_SCHED_AUTO = 4  /* chosen per shape by the grid-size model (Stream-K page,
+                         App. A.1), with BLK_N and g when those are 0 */
 } skg_sched_t;
 
 /* Role of one segment of a CTA's work (Algorithm 5, tile_started /
@@ -107,11 +109,12 @@ typedef enum {
 /* Options of one gemm call. Zero-initialised fields select the defaults;
  * call skg_opts_default to get them explicitly. */
 typedef struct {
-  int32_t sched;        /* skg_sched_t (default SKG_SCHED_SK2_DP) */
-  int32_t grid;         /* g, persistent CTAs; 0 = number of SMs. At most the
+  int32_t sched;        /* skg_sched_t (default SKG_SCHED_AUTO) */
+  int32_t grid;         /* g, persistent CTAs; 0 = chosen by the model (AUTO)
+                           or the number of SMs (fixed schedule). At most the
                            number of SMs: all CTAs must be co-resident, since
                            a tile owner waits for later CTAs. */
-  int32_t tile_n;       /* BLK_N: 128 or 256; 0 = chosen by the library */
+  int32_t tile_n;       /* BLK_N: 128 or 256; 0 = chosen by the model */
   int32_t abft;         /* 0 = off; 1 = verify every output tile, locate and
                            correct a single fault, report the rest */
   float tau_row;        /* ABFT row threshold; <= 0 = the default
@@ -184,8 +187,8 @@ typedef struct {
   skg_fault_record_t records[SKG_MAX_RECORDS];
 } skg_report_t;
 
-/* Fill *opts with the defaults (SK2_DP, g = #SMs, automatic BLK_N, ABFT off,
- * no injection, 2 s wait bound, no trace). */
+/* Fill *opts with the defaults (schedule, g and BLK_N chosen by the model,
+ * ABFT off, no injection, 2 s wait bound, no trace). */
 void skg_opts_default(skg_opts_t* opts);
 
 /* Bytes of device workspace a gemm of this shape needs with these options
@@ -249,9 +252,18 @@ skg_status_t skg_schedule_query(int64_t m, int64_t n, int64_t k, int32_t bm, int
                                 int32_t bk, int32_t g, int32_t sched, skg_segment_t* out,
                                 int64_t cap, int64_t* n_out);
 
-/* BLK_N and grid skg_gemm would use for this shape and options. */
+/* Predicted run time (microseconds) of one launch with this schedule under
+ * the library's grid-size model (Stream-K page, App. A.1: the slowest CTA's
+ * fixed cost + per-iteration cost + partial-store cost + per-peer cost, with
+ * constants fitted on GB300). bm must be 128 and bn 128 or 256. */
+skg_status_t skg_schedule_cost(int64_t m, int64_t n, int64_t k, int32_t bm, int32_t bn,
+                               int32_t bk, int32_t g, int32_t sched, double* us);
+
+/* BLK_N, grid g and schedule skg_gemm would use for this shape and options
+ * (the model's choice for whatever opts leaves open). Any out pointer may be
+ * NULL. */
 skg_status_t skg_launch_shape(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts,
-                              int32_t* tile_n, int32_t* grid);
+                              int32_t* tile_n, int32_t* grid, int32_t* sched);
 
 /* Copy the workspace report to host memory (synchronises `stream` first);
  * reset != 0 also clears the counters and records. */

@@ -84,14 +84,22 @@ def tile_reference(A: np.ndarray, B: np.ndarray, tm: int, tn: int, bm: int, bn: 
 # --------------------------------------------------------------------------
 def default_tau(k: int, side: int, max_a: float, max_b: float) -> float:
     """Default mismatch threshold for a checksum that sums `side` products of
-    length-k dot products whose inputs are bounded by max_a and max_b.
+    length-k dot products, for one output tile whose rows of A are bounded
+    by max_a and whose columns of B are bounded by max_b.
 
-    tau = 2^-12 * sqrt(k) * sqrt(side) * max|A| * max|B|, with side = BLK_N
+    tau = 2^-12 * sqrt(k) * sqrt(side) * max_a * max_b, with side = BLK_N
     for the row checksums and BLK_M for the column checksums. The fault
     tolerance page gives no threshold; this value sits well above the
     rounding of fp32 accumulation and of the split encodings on every
     workload measured, and far below the change an exponent-bit flip makes."""
     return math.ldexp(1.0, -12) * math.sqrt(k) * math.sqrt(side) * max_a * max_b
+
+
+def tile_maxima(A: np.ndarray, B_stored: np.ndarray, tm: int, tn: int, bm: int, bn: int):
+    """(max |A| over the tile's rows, max |B| over the tile's columns); A is
+    stored m x k and B stored n x k."""
+    return (float(np.abs(A[tm * bm:(tm + 1) * bm]).max()),
+            float(np.abs(B_stored[tn * bn:(tn + 1) * bn]).max()))
 
 
 # --------------------------------------------------------------------------

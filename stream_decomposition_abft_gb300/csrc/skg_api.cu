@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "skg_internal.h"
+#include "skg_model.h"
 #include "skgemm.h"
 
 using namespace skg;
@@ -68,28 +69,31 @@ struct Resolved {
   uint64_t* cta_clock;
   int drop_signal;
   int preencoded;
+  int ws_grid;  // CTAs the workspace's flags and partial slots are sized for
 };
 
-// BLK_N choice: 256 columns halve the A-operand shared-memory reads per
-// MMA and still leave room for two TMEM accumulator buffers (2 x 256
-// columns). Narrow outputs (n <= 128) use 128.
-int auto_tile_n(int64_t n, int abft) {
-  (void)abft;
-  return n <= 128 ? 128 : 256;
-}
-
-skg_status_t resolve(int64_t n, const skg_opts_t* o, Resolved& r, int sms) {
+// Schedule, g and BLK_N: whatever the options leave open is chosen by the
+// grid-size model (skg_model.h). A fixed schedule with grid 0 runs on all
+// SMs, as the page's persistent launches do.
+skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resolved& r,
+                     int sms) {
   skg_opts_t d;
   skg_opts_default(&d);
   if (!o) o = &d;
-  r.sched = o->sched;
-  if (r.sched < SKG_SCHED_DP || r.sched > SKG_SCHED_SK2_DP) return SKG_ERR_ARG;
-  r.abft = o->abft ? 1 : 0;
-  r.bn = o->tile_n ? o->tile_n : auto_tile_n(n, r.abft);
-  if (r.bn != 128 && r.bn != 256) return SKG_ERR_UNSUPPORTED;
-  r.grid = o->grid > 0 ? o->grid : sms;
+  if (o->sched < SKG_SCHED_DP || o->sched > SKG_SCHED_AUTO) return SKG_ERR_ARG;
+  if (o->tile_n != 0 && o->tile_n != 128 && o->tile_n != 256) return SKG_ERR_UNSUPPORTED;
   if (o->grid < 0) return SKG_ERR_ARG;
-  if (sms > 0 && r.grid > sms) return SKG_ERR_UNSUPPORTED;  // CTAs must be co-resident
+  const int ms = sms > 0 ? sms : 256;  // no device: plan for a large part
+  if (o->grid > 0 && sms > 0 && o->grid > sms) return SKG_ERR_UNSUPPORTED;  // co-residency
+  r.abft = o->abft ? 1 : 0;
+  const int want_sched = o->sched == SKG_SCHED_AUTO ? -1 : o->sched;
+  const int want_grid = o->grid > 0 ? o->grid : (want_sched >= 0 ? ms : 0);
+  const Plan pl = choose_plan(m > 0 ? m : 1, n > 0 ? n : 1, k > 0 ? k : 1, o->tile_n, want_sched,
+                              want_grid, ms);
+  r.sched = pl.sched;
+  r.grid = pl.grid;
+  r.bn = pl.bn;
+  r.ws_grid = r.abft ? ms : r.grid;  // ABFT checksum GEMMs may use up to every SM
   r.tau_row = o->tau_row;
   r.tau_col = o->tau_col;
   r.inject_tile = o->inject_tile;
@@ -110,7 +114,7 @@ skg_status_t resolve(int64_t n, const skg_opts_t* o, Resolved& r, int sms) {
 // Workspace layout. Partial-tile slots are sized for the widest tile any
 // launch of the call uses (the ABFT checksum GEMMs may use BLK_N = 256).
 struct Layout {
-  size_t flags, partials, sums, enc, blockmax, cr, cc, total;
+  size_t flags, partials, sums, enc_a, enc_b, stat, pub, cr, cc, total;
   int kp, tiles_a, tiles_b;
   int64_t ld_cr, ld_cc;
 };
@@ -119,27 +123,32 @@ Layout layout(int64_t m, int64_t n, int64_t k, const Resolved& r) {
   Layout L;
   size_t off = kHeaderBytes;
   L.flags = off;
-  off = round_up(off + (size_t)r.grid * 4, 256);
+  off = round_up(off + (size_t)r.ws_grid * 4, 256);
   L.partials = off;
   const int slot_n = r.abft ? 256 : r.bn;
-  off = round_up(off + (size_t)r.grid * kBM * slot_n * 4, 256);
+  off = round_up(off + (size_t)r.ws_grid * kBM * slot_n * 4, 256);
   L.kp = (int)round_up((size_t)(k > 0 ? k : 1), kBK);
   L.tiles_a = (int)((m + kBM - 1) / kBM);
   L.tiles_b = (int)((n + r.bn - 1) / r.bn);
   L.ld_cr = (int64_t)round_up((size_t)kEncRows * L.tiles_b, 4);
-  L.ld_cc = (int64_t)round_up((size_t)(n > 0 ? n : 1), 4);
-  L.sums = L.enc = L.blockmax = L.cr = L.cc = off;
+  L.ld_cc = (int64_t)round_up((size_t)kEncRows * L.tiles_a, 4);
+  L.sums = L.enc_a = L.enc_b = L.stat = L.pub = L.cr = L.cc = off;
   if (r.abft) {
+    const size_t tiles = (size_t)L.tiles_a + L.tiles_b;
     L.sums = off;
-    off = round_up(off + (size_t)(L.tiles_a + L.tiles_b) * L.kp * 4, 256);
-    L.enc = off;
-    off = round_up(off + (size_t)(L.tiles_a + L.tiles_b) * kEncRows * L.kp * 2, 256);
-    L.blockmax = off;
-    off = round_up(off + (size_t)(L.tiles_a + L.tiles_b) * encode_slices(L.kp) * 8, 256);
+    off = round_up(off + tiles * L.kp * 4, 256);
+    L.enc_a = off;
+    off = round_up(off + (size_t)kEncRows * L.tiles_a * L.kp * 2, 256);
+    L.enc_b = off;
+    off = round_up(off + (size_t)kEncRows * L.tiles_b * L.kp * 2, 256);
+    L.stat = off;
+    off = round_up(off + tiles * sizeof(TileStat), 256);
+    L.pub = off;
+    off = round_up(off + tiles * sizeof(TilePub), 256);
     L.cr = off;
     off = round_up(off + (size_t)m * L.ld_cr * 4, 256);
     L.cc = off;
-    off = round_up(off + (size_t)kEncRows * L.tiles_a * L.ld_cc * 4, 256);
+    off = round_up(off + (size_t)n * L.ld_cc * 4, 256);
   }
   L.total = off;
   return L;
@@ -219,6 +228,8 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, ui
   p.cc_all = (const float*)(ws + L.cc);
   p.ld_cr = L.ld_cr;
   p.ld_cc = L.ld_cc;
+  p.pub_a = (const TilePub*)(ws + L.pub);
+  p.pub_b = (const TilePub*)(ws + L.pub) + L.tiles_a;
   p.tau_row = r.tau_row;
   p.tau_col = r.tau_col;
   p.inject_tile = r.inject_tile;
@@ -242,33 +253,37 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, ui
 
 // The ABFT reference checksums of every output tile ("Anatomy of
 // High-Performance GEMM with Online Fault Tolerance on GPUs", Fig. 3:
-// C^r = A (B e), C^c = (e^T A) B): the encode pass, then two skinny GEMMs
-// on the same persistent kernel with fp32 output:
-//   cr_all (m x 3 tiles_b) = A      x [Be_hi; Be_mid; Be_lo]^T
-//   cc_all (3 tiles_a x n) = [eA_hi; eA_mid; eA_lo] x B^T
+// C^r = A (B e), C^c = (e^T A) B): the encode pass, then two tall-skinny
+// GEMMs on the same persistent kernel with fp32 output, each reading its
+// large operand once:
+//   cr_all  (m x 2 tiles_b) = A x [Be_hi; Be_lo]^T
+//   ccT_all (n x 2 tiles_a) = B x [eA_hi; eA_lo]^T     (= ((e^T A) B)^T)
 skg_status_t reference_checksums(const Gemm& g, const Resolved& r, uint8_t* ws, const Layout& L,
                                  cudaStream_t stream) {
-  void* enc = ws + L.enc;
-  void* enc_b = (uint8_t*)enc + (size_t)L.tiles_a * kEncRows * L.kp * 2;
   if (launch_encode(g.in_dtype == SKG_IN_BF16, g.A, g.lda, (int)g.m, g.B, g.ldb, (int)g.n,
-                    (int)g.k, L.kp, r.bn, (float*)(ws + L.sums), (float2*)(ws + L.blockmax), enc,
-                    (WsHeader*)ws, stream) != cudaSuccess)
+                    (int)g.k, L.kp, r.bn, (float*)(ws + L.sums), ws + L.enc_a, ws + L.enc_b,
+                    (TileStat*)(ws + L.stat), (TilePub*)(ws + L.pub), stream) != cudaSuccess)
     return SKG_ERR_CUDA;
   Resolved rc = r;
   rc.abft = 0;
-  rc.sched = SKG_SCHED_SK2_DP;
   rc.inject_tile = -1;
   rc.trace = nullptr;
   rc.cta_clock = nullptr;
   rc.drop_signal = -1;
-  Gemm g1{g.m, (int64_t)kEncRows * L.tiles_b, g.k, g.A, g.lda, enc_b, L.kp, ws + L.cr, L.ld_cr,
-          1.f, 0.f, g.in_dtype, SKG_OUT_F32};
-  rc.bn = g1.n <= 128 ? 128 : 256;
+  const Gemm g1{g.m, (int64_t)kEncRows * L.tiles_b, g.k, g.A, g.lda, ws + L.enc_b, L.kp,
+                ws + L.cr, L.ld_cr, 1.f, 0.f, g.in_dtype, SKG_OUT_F32};
+  Plan pl = choose_plan(g1.m, g1.n, g1.k, 0, -1, 0, r.ws_grid);
+  rc.bn = pl.bn;
+  rc.sched = pl.sched;
+  rc.grid = pl.grid;
   skg_status_t st = launch_one(g1, rc, false, ws, L, stream);
   if (st != SKG_OK) return st;
-  Gemm g2{(int64_t)kEncRows * L.tiles_a, g.n, g.k, enc, L.kp, g.B, g.ldb, ws + L.cc, L.ld_cc,
-          1.f, 0.f, g.in_dtype, SKG_OUT_F32};
-  rc.bn = g2.n <= 128 ? 128 : 256;
+  const Gemm g2{g.n, (int64_t)kEncRows * L.tiles_a, g.k, g.B, g.ldb, ws + L.enc_a, L.kp,
+                ws + L.cc, L.ld_cc, 1.f, 0.f, g.in_dtype, SKG_OUT_F32};
+  pl = choose_plan(g2.m, g2.n, g2.k, 0, -1, 0, r.ws_grid);
+  rc.bn = pl.bn;
+  rc.sched = pl.sched;
+  rc.grid = pl.grid;
   return launch_one(g2, rc, false, ws, L, stream);
 }
 
@@ -310,9 +325,15 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
   const int sms = sm_count_cached();
   if (sms <= 0) return SKG_ERR_CUDA;
   Resolved r;
-  st = resolve(n, opts, r, sms);
+  skg_opts_t forced;
+  if (force_abft) {
+    if (opts) forced = *opts;
+    else skg_opts_default(&forced);
+    forced.abft = 1;
+    opts = &forced;
+  }
+  st = resolve(m, n, k, opts, r, sms);
   if (st != SKG_OK) return st;
-  if (force_abft) r.abft = 1;
   const Layout L = layout(m, n, k, r);
   if (!workspace || !aligned16(workspace) || ws_bytes < L.total) return SKG_ERR_WORKSPACE;
   if (!tensor_map_encoder()) return SKG_ERR_CUDA;
@@ -333,16 +354,15 @@ extern "C" {
 void skg_opts_default(skg_opts_t* o) {
   if (!o) return;
   memset(o, 0, sizeof(*o));
-  o->sched = SKG_SCHED_SK2_DP;
+  o->sched = SKG_SCHED_AUTO;
   o->inject_tile = -1;
 }
 
 size_t skg_workspace_size(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts) {
   if (m < 0 || n < 0 || k < 0) return 0;
   Resolved r;
-  int sms = sm_count_cached();
-  if (resolve(n, opts, r, sms) != SKG_OK) return 0;
-  if (r.grid <= 0) r.grid = 256;  // no device: size for the largest grid
+  const int sms = sm_count_cached();
+  if (resolve(m, n, k, opts, r, sms) != SKG_OK) return 0;
   return layout(m, n, k, r).total;
 }
 
@@ -381,10 +401,13 @@ skg_status_t skg_abft_encode(int64_t m, int64_t n, int64_t k, const void* A, int
   if (st != SKG_OK) return st;
   const int sms = sm_count_cached();
   if (sms <= 0) return SKG_ERR_CUDA;
+  skg_opts_t forced;
+  if (opts) forced = *opts;
+  else skg_opts_default(&forced);
+  forced.abft = 1;
   Resolved r;
-  st = resolve(n, opts, r, sms);
+  st = resolve(m, n, k, &forced, r, sms);
   if (st != SKG_OK) return st;
-  r.abft = 1;
   const Layout L = layout(m, n, k, r);
   if (!workspace || !aligned16(workspace) || ws_bytes < L.total) return SKG_ERR_WORKSPACE;
   if (!tensor_map_encoder()) return SKG_ERR_CUDA;
@@ -422,16 +445,26 @@ skg_status_t skg_schedule_query(int64_t m, int64_t n, int64_t k, int32_t bm, int
   return SKG_OK;
 }
 
+skg_status_t skg_schedule_cost(int64_t m, int64_t n, int64_t k, int32_t bm, int32_t bn,
+                               int32_t bk, int32_t g, int32_t sched, double* us) {
+  if (m < 0 || n < 0 || k < 0 || g <= 0 || !us) return SKG_ERR_ARG;
+  if (bm != kTileM || bk != kTileK || (bn != 128 && bn != 256)) return SKG_ERR_UNSUPPORTED;
+  if (sched < SKG_SCHED_DP || sched > SKG_SCHED_SK2_DP) return SKG_ERR_ARG;
+  const Schedule s = make_schedule(m, n, k, bm, bn, bk, g, sched);
+  *us = predict_us(s, bn == 128 ? kModel128 : kModel256);
+  return SKG_OK;
+}
+
 skg_status_t skg_launch_shape(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts,
-                              int32_t* tile_n, int32_t* grid) {
-  (void)m;
-  (void)k;
+                              int32_t* tile_n, int32_t* grid, int32_t* sched) {
+  if (m < 0 || n < 0 || k < 0) return SKG_ERR_ARG;
   Resolved r;
   const int sms = sm_count_cached();
-  skg_status_t st = resolve(n, opts, r, sms);
+  skg_status_t st = resolve(m, n, k, opts, r, sms);
   if (st != SKG_OK) return st;
   if (tile_n) *tile_n = r.bn;
   if (grid) *grid = r.grid;
+  if (sched) *sched = r.sched;
   return SKG_OK;
 }
 

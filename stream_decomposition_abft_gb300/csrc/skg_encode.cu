@@ -2,18 +2,24 @@
 //
 // "Anatomy of High-Performance GEMM with Online Fault Tolerance on GPUs",
 // threadblock-level FT-GEMM (Fig. 5): the checksum encodings of a CTA's
-// operand tiles are e^T A (sum of the tile's rows of A, one value per k)
-// and B e (sum of the tile's columns of B, one value per k). On GB300 they
-// are computed once per call here (one read of A and B, HBM-bound) instead
-// of by every CTA from shared memory, and the main kernel folds them into
-// its tensor-core MMAs at every k step.
+// operand tiles are e^T A (sum of the tile's 128 rows of A, one value per k)
+// and B e (sum of the tile's BLK_N columns of B, one value per k). On GB300
+// they are computed once per call here (one HBM-bound read of A and B)
+// rather than by every CTA from shared memory, where the extra reads would
+// compete with the tensor cores for shared-memory bandwidth.
 //
-// The tensor cores take both operands of one MMA in the same 16-bit type,
-// so each fp32 encoding x is stored as three input-precision terms
-// hi = rn(x s), mid = rn(x s - hi), lo = rn(x s - hi - mid), scaled by a
-// power of two s chosen from max|x| so fp16 cannot overflow. The residual
-// of the three-term split is below 2^-24 |x| relative for bf16 (8-bit
-// significands) and smaller still for fp16.
+// The checksum GEMMs run on the tensor cores, which take both operands of an
+// MMA in the same 16-bit type, so each fp32 encoding x is stored as two
+// input-precision terms hi = rn(x s), lo = rn(x s - hi), scaled by a power
+// of two s per tile, chosen from that tile's largest |x| so fp16 cannot
+// overflow. The residual is below 2^-15 |x| relative for bf16 and 2^-21 for
+// fp16.
+//
+// One kernel does it all: block (slice, tile) sums 256 k-columns of one
+// tile; the last block of each tile to finish (per-tile counter) picks the
+// tile's scale, writes its hi / lo rows, publishes the tile's max |element|
+// (for the default threshold) and scale, and resets the counter and maxima
+// for the next launch.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -43,30 +49,28 @@ constexpr int kEncThreads = 256;  // 8 warps; a block covers 256 k-columns of on
 constexpr int kEncCols = 8;       // k-columns per lane (one 16-byte load)
 constexpr int kEncUnroll = 4;     // rows in flight per thread
 
-// Column sums over one row group of a row-major matrix (A: m x k, or the
-// stored n x k B). blockIdx.z picks the matrix (0 = A with 128-row groups,
-// 1 = B with bn-row groups), blockIdx.y the row group, blockIdx.x a
-// 256-column slice; warp w sums rows w, w+8, ... of the group and the eight
-// warps combine through shared memory. Each block also writes its largest
-// |element| and |column sum| to blockmax[z][block] for the split pass.
+int encode_slices(int kp) { return (kp + 32 * kEncCols - 1) / (32 * kEncCols); }
+
 template <typename T>
-__global__ void __launch_bounds__(kEncThreads) encode_sums_kernel(
+__global__ void __launch_bounds__(kEncThreads) encode_kernel(
     const T* __restrict__ A, int64_t lda, int m, const T* __restrict__ B, int64_t ldb, int n,
-    int k, int kp, int bn, float* __restrict__ sums, float2* __restrict__ blockmax) {
+    int k, int kp, int bn, int tiles_a, float* __restrict__ sums, T* __restrict__ enc_a,
+    T* __restrict__ enc_b, TileStat* __restrict__ stat, TilePub* __restrict__ pub) {
   __shared__ float part[8][32 * kEncCols];
   __shared__ float2 wmax[8];
-  const int z = blockIdx.z;
+  __shared__ int last_block;
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int t = blockIdx.y;  // A tiles first, then B tiles
+  const int z = t < tiles_a ? 0 : 1;
+  const int tile = z == 0 ? t : t - tiles_a;
   const T* X = z == 0 ? A : B;
   const int64_t ld = z == 0 ? lda : ldb;
   const int rows = z == 0 ? m : n;
   const int group = z == 0 ? kBM : bn;
-  const int tiles = (rows + group - 1) / group;
-  const int g = blockIdx.y;
-  if (g >= tiles) return;
-  const int tiles_a = (m + kBM - 1) / kBM;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int col0 = blockIdx.x * 32 * kEncCols + lane * kEncCols;
-  const int r0 = g * group;
+  const int r0 = tile * group;
   const int r1 = min(rows, r0 + group);
   float acc[kEncCols];
 #pragma unroll
@@ -118,121 +122,82 @@ __global__ void __launch_bounds__(kEncThreads) encode_sums_kernel(
   __syncthreads();
   // Thread c finishes column c of the slice (256 threads, 256 columns).
   const int c = threadIdx.x;
-  float t = 0.f;
+  float s = 0.f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) t += part[w][c];
+  for (int w = 0; w < 8; ++w) s += part[w][c];
   const int col = blockIdx.x * 32 * kEncCols + c;
-  float* out = sums + (z == 0 ? 0 : (int64_t)tiles_a * kp);
-  if (col < kp) out[(int64_t)g * kp + col] = t;
-  float smax = fabsf(t);
+  float* tsums = sums + (int64_t)t * kp;
+  if (col < kp) __stcg(tsums + col, s);
+  float smax = fabsf(s);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) {
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, off));
   }
   if (lane == 0) wmax[warp] = make_float2(amax, smax);
+  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     float2 mx = wmax[0];
     for (int w = 1; w < 8; ++w) mx = make_float2(fmaxf(mx.x, wmax[w].x), fmaxf(mx.y, wmax[w].y));
-    const int slices = gridDim.x;
-    const int base = z == 0 ? 0 : slices * tiles_a;
-    blockmax[base + g * slices + blockIdx.x] = mx;
+    // Non-negative floats order like their bit patterns.
+    atomicMax(&stat[t].absmax_bits, __float_as_uint(mx.x));
+    atomicMax(&stat[t].encmax_bits, __float_as_uint(mx.y));
+    __threadfence();
+    last_block = (atomicAdd(&stat[t].count, 1u) == gridDim.x - 1) ? 1 : 0;
   }
-}
-
-// fp32 encodings -> (hi, mid, lo) rows of the input type, scaled by
-// 2^e with e chosen so max|x| * 2^e lies in [2^14, 2^15). Every block first
-// reduces the per-block maxima of its matrix; block 0 publishes max|X| (for
-// the default thresholds), max|encoding| and e in the workspace header.
-template <typename T>
-__global__ void encode_split_kernel(const float* __restrict__ sums,
-                                    const float2* __restrict__ blockmax, int slices, int tiles_a,
-                                    int tiles_b, int kp, T* __restrict__ enc, WsHeader* hdr) {
-  __shared__ float2 red[8];
-  const int z = blockIdx.z;
-  const int tiles = z == 0 ? tiles_a : tiles_b;
-  const int nmax = slices * tiles;
-  const float2* bm = blockmax + (z == 0 ? 0 : slices * tiles_a);
-  float2 mx = make_float2(0.f, 0.f);
-  for (int i = threadIdx.x; i < nmax; i += blockDim.x) {
-    const float2 v = bm[i];
-    mx = make_float2(fmaxf(mx.x, v.x), fmaxf(mx.y, v.y));
-  }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    mx.x = fmaxf(mx.x, __shfl_xor_sync(0xffffffffu, mx.x, off));
-    mx.y = fmaxf(mx.y, __shfl_xor_sync(0xffffffffu, mx.y, off));
-  }
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
   __syncthreads();
-  mx = red[0];
-  for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
-    mx = make_float2(fmaxf(mx.x, red[w].x), fmaxf(mx.y, red[w].y));
+  if (!last_block) return;
+
+  // Last block of this tile: every slice's sums and maxima are in.
+  __threadfence();
+  const float emax = __uint_as_float(atomicAdd(&stat[t].encmax_bits, 0u));
+  const float xmax = __uint_as_float(atomicAdd(&stat[t].absmax_bits, 0u));
   int ex = 0;
-  if (mx.y > 0.f) frexpf(mx.y, &ex);
-  const int e = (mx.y > 0.f) ? 15 - ex : 0;
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    hdr->maxabs_bits[z] = __float_as_uint(mx.x);
-    hdr->maxenc_bits[z] = __float_as_uint(mx.y);
-    hdr->scale_exp[z] = e;
-  }
-  const int64_t total = (int64_t)tiles * kp;
-  const int64_t base_sum = z == 0 ? 0 : (int64_t)tiles_a * kp;
-  const int64_t base_enc = z == 0 ? 0 : (int64_t)tiles_a * kEncRows * kp;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = i / kp, kk = i % kp;
-    const float x = ldexpf(sums[base_sum + i], e);
+  if (emax > 0.f) frexpf(emax, &ex);
+  const int e = (emax > 0.f) ? 15 - ex : 0;  // emax * 2^e in [2^14, 2^15)
+  T* enc = z == 0 ? enc_a : enc_b;
+  T* hi_row = enc + (int64_t)(kEncRows * tile) * kp;
+  T* lo_row = hi_row + kp;
+  for (int i = threadIdx.x; i < kp; i += kEncThreads) {
+    const float x = ldexpf(__ldcg(tsums + i), e);
     const T hi = from_f<T>(x);
-    const float x1 = x - to_f<T>(hi);
-    const T mid = from_f<T>(x1);
-    const float x2 = x1 - to_f<T>(mid);
-    const T lo = from_f<T>(x2);
-    T* dst = enc + base_enc + (t * kEncRows) * kp + kk;
-    dst[0] = hi;
-    dst[kp] = mid;
-    dst[2 * kp] = lo;
+    hi_row[i] = hi;
+    lo_row[i] = from_f<T>(x - to_f<T>(hi));
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    pub[t].maxabs = xmax;
+    pub[t].scale_exp = e;
+    stat[t].absmax_bits = 0;
+    stat[t].encmax_bits = 0;
+    stat[t].count = 0;
   }
 }
-
-int encode_slices(int kp) { return (kp + 32 * kEncCols - 1) / (32 * kEncCols); }
 
 cudaError_t launch_encode(int in_bf16, const void* A, int64_t lda, int m, const void* B,
-                          int64_t ldb, int n, int k, int kp, int bn, float* sums,
-                          float2* blockmax, void* enc, WsHeader* hdr, cudaStream_t stream) {
+                          int64_t ldb, int n, int k, int kp, int bn, float* sums, void* enc_a,
+                          void* enc_b, TileStat* stat, TilePub* pub, cudaStream_t stream) {
   const int tiles_a = (m + kBM - 1) / kBM;
   const int tiles_b = (n + bn - 1) / bn;
-  const int tiles = tiles_a > tiles_b ? tiles_a : tiles_b;
-  const int slices = encode_slices(kp);
-  const dim3 grid(slices, tiles, 2);
-  // sums: [tiles_a][kp] for A followed by [tiles_b][kp] for B.
+  const dim3 grid(encode_slices(kp), tiles_a + tiles_b);
   if (in_bf16) {
     using T = __nv_bfloat16;
-    encode_sums_kernel<T><<<grid, kEncThreads, 0, stream>>>((const T*)A, lda, m, (const T*)B,
-                                                            ldb, n, k, kp, bn, sums, blockmax);
-  } else {
-    using T = __half;
-    encode_sums_kernel<T><<<grid, kEncThreads, 0, stream>>>((const T*)A, lda, m, (const T*)B,
-                                                            ldb, n, k, kp, bn, sums, blockmax);
+    return launch_pdl(encode_kernel<T>, grid, dim3(kEncThreads), 0, stream, (const T*)A, lda, m,
+                      (const T*)B, ldb, n, k, kp, bn, tiles_a, sums, (T*)enc_a, (T*)enc_b, stat,
+                      pub);
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int64_t work = (int64_t)tiles * kp;
-  int blocks = (int)((work + 255) / 256);
-  if (blocks > 2048) blocks = 2048;
-  if (in_bf16)
-    encode_split_kernel<__nv_bfloat16><<<dim3(blocks, 1, 2), 256, 0, stream>>>(
-        sums, blockmax, slices, tiles_a, tiles_b, kp, (__nv_bfloat16*)enc, hdr);
-  else
-    encode_split_kernel<__half><<<dim3(blocks, 1, 2), 256, 0, stream>>>(
-        sums, blockmax, slices, tiles_a, tiles_b, kp, (__half*)enc, hdr);
-  return cudaGetLastError();
+  using T = __half;
+  return launch_pdl(encode_kernel<T>, grid, dim3(kEncThreads), 0, stream, (const T*)A, lda, m,
+                    (const T*)B, ldb, n, k, kp, bn, tiles_a, sums, (T*)enc_a, (T*)enc_b, stat,
+                    pub);
 }
 
 // C = beta * C (beta == 0 writes zeros without reading C).
 template <typename T>
 __global__ void scale_kernel(T* C, int64_t ldc, int m, int n, float beta) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const int64_t total = (int64_t)m * n;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -255,12 +220,13 @@ cudaError_t launch_scale(int out_dtype, void* C, int64_t ldc, int m, int n, floa
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) return cudaSuccess;
   if (out_dtype == SKG_OUT_F32)
-    scale_kernel<float><<<blocks, 256, 0, stream>>>((float*)C, ldc, m, n, beta);
-  else if (out_dtype == SKG_OUT_F16)
-    scale_kernel<__half><<<blocks, 256, 0, stream>>>((__half*)C, ldc, m, n, beta);
-  else
-    scale_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>((__nv_bfloat16*)C, ldc, m, n, beta);
-  return cudaGetLastError();
+    return launch_pdl(scale_kernel<float>, dim3(blocks), dim3(256), 0, stream, (float*)C, ldc, m,
+                      n, beta);
+  if (out_dtype == SKG_OUT_F16)
+    return launch_pdl(scale_kernel<__half>, dim3(blocks), dim3(256), 0, stream, (__half*)C, ldc, m,
+                      n, beta);
+  return launch_pdl(scale_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, stream,
+                    (__nv_bfloat16*)C, ldc, m, n, beta);
 }
 
 }  // namespace skg

@@ -1,5 +1,7 @@
 // Instantiations of the persistent kernel for BLK_N = 128, ABFT = 1
 // (one translation unit each so the build compiles them in parallel).
+#include <atomic>
+
 #include "skg_internal.h"
 
 namespace skg {
@@ -8,12 +10,20 @@ template <int BN, bool ABFT, int OUT>
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const KernelParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<BN, ABFT, OUT>;
-  cudaError_t e = cudaFuncSetAttribute(skg_gemm_kernel<C>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)C::SMEM_BYTES);
+  // The shared-memory opt-in is per device; set it once per device.
+  static std::atomic<uint64_t> done_mask{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  skg_gemm_kernel<C><<<grid, kThreads, C::SMEM_BYTES, stream>>>(tmA, tmB, tmC, p);
-  return cudaGetLastError();
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (!bit || !(done_mask.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(skg_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    done_mask.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  return launch_pdl(skg_gemm_kernel<C>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, stream, tmA,
+                    tmB, tmC, p);
 }
 
 #define SKG_INST(OUT)                                                                        \

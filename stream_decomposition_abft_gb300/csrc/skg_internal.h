@@ -7,19 +7,42 @@
 
 namespace skg {
 
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous kernel in the stream finishes; every kernel of this library
+// calls griddepcontrol.wait before it reads anything an earlier kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Launch the persistent kernel instantiated for (BN, ABFT, OUT) on `grid`
 // CTAs. Defined in the skg_inst_*.cu translation units.
 template <int BN, bool ABFT, int OUT>
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const KernelParams& p, int grid, cudaStream_t stream);
 
-// ABFT encode pass (skg_encode.cu): e^T A per 128-row tile and B e per
-// BN-row tile of the stored n x k B, split into hi / mid / lo terms.
+// ABFT encode pass (skg_encode.cu): e^T A per 128-row tile of A and B e
+// per bn-row tile of the stored n x k B, as hi / lo rows in the input type
+// (enc_a: 2 tiles_a x kp, enc_b: 2 tiles_b x kp), plus per-tile maxima and
+// scales in `pub` (A tiles first). `sums` is fp32 scratch, (tiles_a +
+// tiles_b) x kp; `stat` is scratch that must start at zero and is left at
+// zero.
 cudaError_t launch_encode(int in_bf16, const void* A, int64_t lda, int m, const void* B,
-                          int64_t ldb, int n, int k, int kp, int bn, float* sums,
-                          float2* blockmax, void* enc, WsHeader* hdr, cudaStream_t stream);
+                          int64_t ldb, int n, int k, int kp, int bn, float* sums, void* enc_a,
+                          void* enc_b, TileStat* stat, TilePub* pub, cudaStream_t stream);
 
-// 256-column slices of the encode pass (one blockmax entry per slice and tile).
+// 256-column slices of the encode pass.
 int encode_slices(int kp);
 
 // C = beta * C for k == 0 (skg_encode.cu).

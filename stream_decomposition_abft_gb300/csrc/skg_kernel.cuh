@@ -55,19 +55,30 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
-constexpr int kEncRows = 3;  // hi, mid, lo terms of each encoding
+constexpr int kEncRows = 2;  // hi and lo terms of each encoding
 constexpr uint32_t kSmemLimit = 232448;
 
 // Workspace header (device). The report follows at offset 256.
 struct WsHeader {
-  uint32_t epoch;          // launches completed on this workspace
-  uint32_t done;           // CTA tickets of the running launch
-  uint32_t maxabs_bits[2]; // max |A|, max |B| (fp32 bits), written by the encode pass
-  uint32_t maxenc_bits[2]; // max |e^T A|, max |B e| (fp32 bits), same
-  int32_t scale_exp[2];    // encodings are stored scaled by 2^scale_exp
-  uint32_t pad[56];
+  uint32_t epoch;  // launches completed on this workspace
+  uint32_t done;   // CTA tickets of the running launch
+  uint32_t pad[62];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
+
+// ABFT encode pass, per operand tile: running maxima and a block counter
+// (scratch, left at zero after every pass) ...
+struct TileStat {
+  uint32_t absmax_bits;  // max |element| over the tile (fp32 bits)
+  uint32_t encmax_bits;  // max |encoding| over the tile
+  uint32_t count;        // blocks of the tile finished
+  uint32_t pad;
+};
+// ... and what the pass publishes for the main kernel's epilogue.
+struct TilePub {
+  float maxabs;      // max |element| over the tile's rows of A (or columns of B)
+  int32_t scale_exp; // the tile's encodings are stored scaled by 2^scale_exp
+};
 
 struct KernelParams {
   Schedule s;
@@ -78,11 +89,14 @@ struct KernelParams {
   skg_report_t* report;
   uint32_t* flags;
   float* partials;
-  // ABFT reference checksums (hi, mid, lo partial products, scaled):
-  // cr_all[(row) * ld_cr + 3 * tn + t] and cc_all[(3 * tm + t) * ld_cc + col].
+  // ABFT reference checksums (hi and lo partial products, scaled):
+  // row checksums cr_all[row * ld_cr + 2 * tn + t] = A (B e)_tn, and column
+  // checksums ccT_all[col * ld_cc + 2 * tm + t] = ((e^T A)_tm B)^T.
   const float* cr_all;
   const float* cc_all;
   int64_t ld_cr, ld_cc;
+  const TilePub* pub_a;  // per 128-row tile of A
+  const TilePub* pub_b;  // per BLK_N-column tile of B
   float tau_row, tau_col;  // <= 0: derive from the encode pass maxima
   int inject_tile, inject_row, inject_col, inject_bit;
   uint64_t timeout_ns;
@@ -281,6 +295,47 @@ __device__ __forceinline__ float* partial_at(float* slot, int c4, int r) {
   return slot + ((size_t)c4 * kBM + r) * 4;
 }
 
+// LoadPartials for one 32-column chunk: v += the partials of peers
+// first..last (ascending CTA order, so the sum is deterministic). Loads are
+// issued four peers at a time before any is used, so an owner with many
+// peers waits for one L2 round trip per group rather than per peer.
+template <int BN>
+__device__ __forceinline__ void add_peer_partials(float (&v)[32], float* partials, int first,
+                                                  int last, int c32, int r) {
+  int peer = first;
+  for (; peer + 3 <= last; peer += 4) {
+    float4 t[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float* ps = partials + (size_t)(peer + u) * kBM * BN;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) t[u][j] = ld_cg_f4(partial_at(ps, c32 * 8 + j, r));
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[4 * j] += t[u][j].x;
+        v[4 * j + 1] += t[u][j].y;
+        v[4 * j + 2] += t[u][j].z;
+        v[4 * j + 3] += t[u][j].w;
+      }
+  }
+  for (; peer <= last; ++peer) {
+    float4 t[8];
+    float* ps = partials + (size_t)peer * kBM * BN;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] = ld_cg_f4(partial_at(ps, c32 * 8 + j, r));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[4 * j] += t[j].x;
+      v[4 * j + 1] += t[j].y;
+      v[4 * j + 2] += t[j].z;
+      v[4 * j + 3] += t[j].w;
+    }
+  }
+}
+
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     skg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -324,7 +379,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     aux->nbad_r = aux->nbad_c = 0;
     aux->bad_row = aux->bad_col = -1;
     fence_barrier_init();
-    if (p.cta_clock) p.cta_clock[2 * blockIdx.x] = globaltimer();
   }
   if (warp == 1) {
     tmem_alloc(&aux->tmem_slot, C::TMEM_COLS);
@@ -334,6 +388,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = aux->tmem_slot;
+  // Everything above touched only this CTA's shared memory and TMEM; from
+  // here on the kernel reads the previous kernel's outputs (inputs, ABFT
+  // checksums, the workspace epoch).
+  griddep_wait();
+  if (threadIdx.x == 0) {
+    griddep_launch_dependents();
+    if (p.cta_clock) p.cta_clock[2 * blockIdx.x] = globaltimer();
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -443,24 +505,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr->epoch) + 1u;
     float* my_slot = p.partials + (size_t)blockIdx.x * kBM * BN;
 
-    float tau_r = p.tau_row, tau_c = p.tau_col;
-    float unscale_a = 1.f, unscale_b = 1.f;
-    if (C::ABFT) {
-      const float maxa =
-          __uint_as_float(*reinterpret_cast<volatile uint32_t*>(&p.hdr->maxabs_bits[0]));
-      const float maxb =
-          __uint_as_float(*reinterpret_cast<volatile uint32_t*>(&p.hdr->maxabs_bits[1]));
-      const float base = ldexpf(1.f, -12) * sqrtf((float)p.k) * maxa * maxb;
-      if (!(tau_r > 0.f)) tau_r = base * sqrtf((float)BN);
-      if (!(tau_c > 0.f)) tau_c = base * sqrtf((float)kBM);
-      unscale_a = ldexpf(1.f, -*reinterpret_cast<volatile int32_t*>(&p.hdr->scale_exp[0]));
-      unscale_b = ldexpf(1.f, -*reinterpret_cast<volatile int32_t*>(&p.hdr->scale_exp[1]));
-      if (blockIdx.x == 0 && et == 0) {
-        p.report->tau_row = tau_r;
-        p.report->tau_col = tau_c;
-      }
-    }
-
     Cursor cur;
     cur.init(s, blockIdx.x);
     Work w;
@@ -556,19 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
-            if (owner) {
-              for (int peer = blockIdx.x + 1; peer <= w.peer_last; ++peer) {
-                float* ps = p.partials + (size_t)peer * kBM * BN;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float4 a = ld_cg_f4(partial_at(ps, c32 * 8 + j, r));
-                  v[4 * j] += a.x;
-                  v[4 * j + 1] += a.y;
-                  v[4 * j + 2] += a.z;
-                  v[4 * j + 3] += a.w;
-                }
-              }
-            }
+            if (owner) add_peer_partials<BN>(v, p.partials, blockIdx.x + 1, w.peer_last, c32, r);
             // Fault injection: one bit of one fp32 accumulator, after the
             // fixup and before the check (warp-uniform chunk selection).
             const bool inj_chunk = inject_here && (p.inject_row >> 5) == q &&
@@ -594,11 +626,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // Reference checksums of this tile: thread r holds the row checksum
           // of row r and the column checksum of columns h*128 + r, each the
-          // sum of its hi, mid and lo partial products.
+          // sum of its hi and lo partial products, unscaled by the tile's
+          // power of two. The default thresholds use the tile's own maxima:
+          //   tau = 2^-12 sqrt(k) sqrt(side) max|A_tile| max|B_tile|.
+          const TilePub pa = p.pub_a[tm];
+          const TilePub pb = p.pub_b[tn];
+          float tau_r = p.tau_row, tau_c = p.tau_col;
+          const float base = ldexpf(1.f, -12) * sqrtf((float)p.k) * pa.maxabs * pb.maxabs;
+          if (!(tau_r > 0.f)) tau_r = base * sqrtf((float)BN);
+          if (!(tau_c > 0.f)) tau_c = base * sqrtf((float)kBM);
           float cr = 0.f;
           if (m0 + r < p.m) {
             const float* crp = p.cr_all + (int64_t)(m0 + r) * p.ld_cr + kEncRows * tn;
-            cr = __ldcg(crp) + __ldcg(crp + 1) + __ldcg(crp + 2);
+            cr = ldexpf(__ldcg(crp) + __ldcg(crp + 1), -pb.scale_exp);
           }
           float cc[BN / 128];
 #pragma unroll
@@ -606,11 +646,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col = n0 + h * 128 + r;
             cc[h] = 0.f;
             if (col < p.n) {
-              const float* ccp = p.cc_all + (int64_t)(kEncRows * tm) * p.ld_cc + col;
-              cc[h] = __ldcg(ccp) + __ldcg(ccp + p.ld_cc) + __ldcg(ccp + 2 * p.ld_cc);
+              const float* ccp = p.cc_all + (int64_t)col * p.ld_cc + kEncRows * tm;
+              cc[h] = ldexpf(__ldcg(ccp) + __ldcg(ccp + 1), -pa.scale_exp);
             }
           }
-          cr *= unscale_b;
+          if (et == 0) {  // the report keeps the largest thresholds used
+            atomicMax(reinterpret_cast<int*>(&p.report->tau_row), __float_as_int(tau_r));
+            atomicMax(reinterpret_cast<int*>(&p.report->tau_col), __float_as_int(tau_c));
+          }
           named_bar_sync(1, kEpiThreads);  // column sums of all four warps stored
 
           const float d_r = rowsum - cr;
@@ -627,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = h * 128 + r;
             const float tot =
                 colsum_of(0)[j] + colsum_of(1)[j] + colsum_of(2)[j] + colsum_of(3)[j];
-            const float d_c = tot - cc[h] * unscale_a;
+            const float d_c = tot - cc[h];
             if (!(fabsf(d_c) <= tau_c)) {
               atomicAdd(&aux->nbad_c, 1);
               aux->bad_col = j;
@@ -736,23 +779,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int hh = 0; hh < C::EPI_COLS / 32; ++hh) {
             uint32_t u[32];
             const int c32 = c * (C::EPI_COLS / 32) + hh;
+            float v[32];
             tmem_ld32(tacc + c32 * 32, u);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) y[hh * 32 + i] = f32_of(u[i]);
-            if (!C::ABFT) {
-              if (owner) {
-                for (int peer = blockIdx.x + 1; peer <= w.peer_last; ++peer) {
-                  float* ps = p.partials + (size_t)peer * kBM * BN;
+            for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
+            if (!C::ABFT && owner)
+              add_peer_partials<BN>(v, p.partials, blockIdx.x + 1, w.peer_last, c32, r);
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) {
-                    const float4 a = ld_cg_f4(partial_at(ps, c32 * 8 + j, r));
-                    y[hh * 32 + 4 * j] += a.x;
-                    y[hh * 32 + 4 * j + 1] += a.y;
-                    y[hh * 32 + 4 * j + 2] += a.z;
-                    y[hh * 32 + 4 * j + 3] += a.w;
-                  }
-                }
-              }
+            for (int i = 0; i < 32; ++i) y[hh * 32 + i] = v[i];
+            if (!C::ABFT) {
               if (inject_here && r == p.inject_row && (p.inject_col >> 5) == c32) {
                 const int jc = p.inject_col & 31;
 #pragma unroll

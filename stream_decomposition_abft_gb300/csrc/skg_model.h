@@ -1,0 +1,162 @@
+// Grid-size / tile-width selection by the analytic model of "Stream-K:
+// Work-centric Parallel Decomposition for Dense Matrix-Matrix Multiplication
+// on the GPU", App. A.1: the run time of a Stream-K launch is the run time
+// of its slowest CTA, modelled as
+//
+//   t_CTA = a + c * (MAC iterations) + e * (tiles it stores)
+//             + b * [it stores a partial tile] + d * (peers it accumulates)
+//
+// a: fixed per-CTA cost (launch, pipeline fill, last epilogue); b: writing
+// a partial tile; c: one MAC iteration; d: reading and adding one peer's
+// partial tile; e: one more tile epilogue. The page fits {a, b, c, d} per
+// architecture, data type and tile by microbenchmark and prints no values;
+// the constants below were fitted on a GB300 (152 SMs, bf16, BLK_K = 64)
+// from in-kernel %globaltimer spans over 726 (shape, tile, schedule, g)
+// launches (median relative error 2 % for BLK_N = 128, 6 % for 256). The
+// per-tile term e is an addition to the page's four.
+//
+// The page uses the model to pick g; here it also picks the schedule (DP,
+// basic SK, or two-tile SK + DP) and BLK_N (128 or 256), the two-kernel
+// ensemble the page suggests for bandwidth-bound shapes (§A4).
+#pragma once
+#include <stdint.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "skg_sched.cuh"
+
+namespace skg {
+
+struct CostModel {
+  double a, c, e, b, d;  // microseconds
+};
+
+constexpr CostModel kModel128 = {2.64, 0.334, 0.17, 4.67, 1.03};
+constexpr CostModel kModel256 = {3.47, 0.364, 0.00, 8.18, 1.73};
+
+// Predicted time (us) of one launch with schedule s: max over CTAs. O(g).
+inline double predict_us(const Schedule& s, const CostModel& M) {
+  if (s.t == 0 || s.ipt == 0) return 0.0;
+  const int64_t I = s.ipt;
+  double worst = 0.0;
+  for (int x = 0; x < s.g; ++x) {
+    int64_t iters = 0, tiles = 0, partial = 0, peers = 0;
+    if (x < s.t_dp) {
+      const int64_t nd = (s.t_dp - 1 - x) / s.g + 1;
+      iters += nd * I;
+      tiles += nd;
+    }
+    if (s.sk_total > 0) {
+      int64_t b, e;
+      sk_range(s, x, b, e);
+      if (e > b) {
+        iters += e - b;
+        if (b % I != 0) partial = 1;
+        const int64_t first = (b % I == 0) ? b : (b / I + 1) * I;
+        if (first < e) {
+          const int64_t started = (e - 1 - first) / I + 1;
+          tiles += started;
+          const int64_t last = first + (started - 1) * I;
+          if (last + I > e) peers += sk_cta_of(s, last + I - 1) - x;
+        }
+      }
+    }
+    const double tx = M.a + M.c * (double)iters + M.e * (double)tiles + M.b * (double)partial +
+                      M.d * (double)peers;
+    if (tx > worst) worst = tx;
+  }
+  return worst;
+}
+
+struct Plan {
+  int bn, sched, grid;
+  double us;
+};
+
+// Best (BLK_N, schedule, g) for an m x n x k launch on `sms` SMs. Fixed
+// choices (want_* != 0 / >= 0) are kept; the rest are searched.
+inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_sched,
+                        int want_grid, int sms) {
+  static const int kCands[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 76, 96, 112, 128, 144};
+  Plan best{want_bn ? want_bn : 256, want_sched >= 0 ? want_sched : kSchedSK2DP,
+            want_grid ? want_grid : sms, 1e300};
+  for (int bn = 128; bn <= 256; bn += 128) {
+    if (want_bn && bn != want_bn) continue;
+    const CostModel& M = bn == 128 ? kModel128 : kModel256;
+    const int64_t t = ((m + kTileM - 1) / kTileM) * ((n + bn - 1) / bn);
+    int cands[64];
+    int nc = 0;
+    if (want_grid) {
+      cands[nc++] = want_grid;
+    } else {
+      for (int c : kCands)
+        if (c <= sms) cands[nc++] = c;
+      cands[nc++] = sms;
+      for (int w = 1; w <= 8 && nc < 64; ++w) {
+        const int64_t g = (t + w - 1) / w;
+        if (g >= 1 && g <= sms) cands[nc++] = (int)g;
+      }
+    }
+    int scheds[3] = {kSchedDP, kSchedSK, kSchedSK2DP};
+    int ns = 3;
+    if (want_sched >= 0) {
+      scheds[0] = want_sched;
+      ns = 1;
+    }
+    for (int si = 0; si < ns; ++si) {
+      const int sched = scheds[si];
+      for (int i = 0; i < nc; ++i) {
+        // Basic Stream-K keeps its tile-processing skew for the whole
+        // launch, which costs cache reuse the model does not see (§5.2);
+        // with two or more full waves the hybrids exist to bound it, so the
+        // automatic choice does not take basic SK there.
+        if (want_sched < 0 && sched == kSchedSK && t >= 2 * (int64_t)cands[i]) continue;
+        const Schedule s = make_schedule(m, n, k, kTileM, bn, kTileK, cands[i], sched);
+        const double us = predict_us(s, M);
+        // Prefer fewer CTAs on ties (less fixup storage and traffic).
+        if (us < best.us - 1e-9 || (us < best.us + 1e-9 && cands[i] < best.grid)) {
+          best = Plan{bn, sched, cands[i], us};
+        }
+      }
+    }
+  }
+  return best;
+}
+
+// search_plan behind a small cache: the search walks up to ~150 candidate
+// schedules of up to `sms` CTAs each, far more host time than a launch.
+inline Plan choose_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_sched,
+                        int want_grid, int sms) {
+  struct Key {
+    int64_t m, n, k;
+    int bn, sched, grid, sms;
+    bool operator==(const Key& o) const {
+      return m == o.m && n == o.n && k == o.k && bn == o.bn && sched == o.sched &&
+             grid == o.grid && sms == o.sms;
+    }
+  };
+  struct Hash {
+    size_t operator()(const Key& x) const {
+      uint64_t h = 1469598103934665603ull;
+      const int64_t v[7] = {x.m, x.n, x.k, x.bn, x.sched, x.grid, x.sms};
+      for (int64_t e : v) h = (h ^ (uint64_t)e) * 1099511628211ull;
+      return (size_t)h;
+    }
+  };
+  static std::mutex mu;
+  static std::unordered_map<Key, Plan, Hash> cache;
+  const Key key{m, n, k, want_bn, want_sched, want_grid, sms};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  const Plan p = search_plan(m, n, k, want_bn, want_sched, want_grid, sms);
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() > 4096) cache.clear();
+  cache.emplace(key, p);
+  return p;
+}
+
+}  // namespace skg

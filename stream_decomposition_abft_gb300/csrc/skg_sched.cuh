@@ -25,7 +25,11 @@
 
 namespace skg {
 
-enum : int { kSchedDP = 0, kSchedSK = 1, kSchedDPSK1 = 2, kSchedSK2DP = 3 };
+enum : int { kSchedDP = 0, kSchedSK = 1, kSchedDPSK1 = 2, kSchedSK2DP = 3, kSchedAuto = 4 };
+
+// CTA tile rows (BLK_M) and MAC-iteration depth (BLK_K) of the kernel.
+constexpr int kTileM = 128;
+constexpr int kTileK = 64;
 enum : int { kRoleFull = 0, kRoleOwner = 1, kRolePeer = 2 };
 
 struct Schedule {

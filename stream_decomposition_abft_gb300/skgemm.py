@@ -20,7 +20,7 @@ IN_F16, IN_BF16 = 0, 1
 OUT_F32, OUT_F16, OUT_BF16 = 0, 1, 2
 A_ROW = 0
 B_KMAJOR = 0
-SCHED_DP, SCHED_SK, SCHED_DP_SK1, SCHED_SK2_DP = 0, 1, 2, 3
+SCHED_DP, SCHED_SK, SCHED_DP_SK1, SCHED_SK2_DP, SCHED_AUTO = 0, 1, 2, 3, 4
 ROLE_FULL, ROLE_OWNER, ROLE_PEER = 0, 1, 2
 OK = 0
 ERR_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE = 1, 2, 3, 4
@@ -29,7 +29,8 @@ ABFT_CORRECTED, ABFT_UNCORRECTABLE = 16, 17
 BLK_M, BLK_K = 128, 64
 TRACE_CAP, TRACE_STRIDE, MAX_RECORDS = 255, 1024, 64
 
-SCHED_NAMES = {"dp": SCHED_DP, "sk": SCHED_SK, "dp_sk1": SCHED_DP_SK1, "sk2_dp": SCHED_SK2_DP}
+SCHED_NAMES = {"dp": SCHED_DP, "sk": SCHED_SK, "dp_sk1": SCHED_DP_SK1, "sk2_dp": SCHED_SK2_DP,
+               "auto": SCHED_AUTO}
 
 
 class Opts(ctypes.Structure):
@@ -70,7 +71,7 @@ class Report(ctypes.Structure):
 
 SYMBOLS = ("skg_opts_default", "skg_workspace_size", "skg_workspace_init", "skg_gemm",
            "skg_gemm_verify", "skg_abft_encode", "skg_schedule_query", "skg_launch_shape", "skg_report_read",
-           "skg_device_sm_count", "skg_status_string", "skg_gemm_noalloc")
+           "skg_device_sm_count", "skg_status_string", "skg_gemm_noalloc", "skg_schedule_cost")
 
 _lib = None
 
@@ -110,8 +111,11 @@ def lib() -> ctypes.CDLL:
     L.skg_schedule_query.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32,
                                      ctypes.POINTER(Segment), i64, ctypes.POINTER(i64)]
     L.skg_schedule_query.restype = i32
+    L.skg_schedule_cost.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32,
+                                    ctypes.POINTER(ctypes.c_double)]
+    L.skg_schedule_cost.restype = i32
     L.skg_launch_shape.argtypes = [i64, i64, i64, ctypes.POINTER(Opts), ctypes.POINTER(i32),
-                                   ctypes.POINTER(i32)]
+                                   ctypes.POINTER(i32), ctypes.POINTER(i32)]
     L.skg_launch_shape.restype = i32
     L.skg_report_read.argtypes = [vp, ctypes.POINTER(Report), i32, vp]
     L.skg_report_read.restype = i32
@@ -184,13 +188,25 @@ def schedule_query(m: int, n: int, k: int, bm: int, bn: int, bk: int, g: int,
     return [(s.cta, s.tile, s.k_iter_begin, s.k_iter_end, s.role) for s in buf[:count.value]]
 
 
-def launch_shape(m: int, n: int, k: int, opts: Optional[Opts] = None) -> Tuple[int, int]:
-    tn, g = ctypes.c_int32(0), ctypes.c_int32(0)
+def schedule_cost(m: int, n: int, k: int, bm: int, bn: int, bk: int, g: int, sched) -> float:
+    """Grid-size model's predicted time (us) of one launch."""
+    if isinstance(sched, str):
+        sched = SCHED_NAMES[sched]
+    us = ctypes.c_double(0.0)
+    st = lib().skg_schedule_cost(m, n, k, bm, bn, bk, g, sched, ctypes.byref(us))
+    if st != OK:
+        raise SkgError(st, "skg_schedule_cost")
+    return us.value
+
+
+def launch_shape(m: int, n: int, k: int, opts: Optional[Opts] = None) -> Tuple[int, int, int]:
+    """(BLK_N, g, schedule) skg_gemm would use."""
+    tn, g, sc = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
     st = lib().skg_launch_shape(m, n, k, ctypes.byref(opts) if opts else None, ctypes.byref(tn),
-                                ctypes.byref(g))
+                                ctypes.byref(g), ctypes.byref(sc))
     if st != OK:
         raise SkgError(st, "skg_launch_shape")
-    return tn.value, g.value
+    return tn.value, g.value, sc.value
 
 
 def report_read(ws_ptr: int, reset: bool = False, stream: int = 0) -> Report:

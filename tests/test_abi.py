@@ -45,7 +45,7 @@ def test_struct_sizes_match_header():
 
 def test_defaults(lib):
     o = skgemm.opts_default()
-    assert o.sched == skgemm.SCHED_SK2_DP and o.inject_tile == -1 and o.abft == 0
+    assert o.sched == skgemm.SCHED_AUTO and o.inject_tile == -1 and o.abft == 0
     assert skgemm.status_string(0) == "ok"
     assert "timed out" in skgemm.status_string(skgemm.ERR_FIXUP_TIMEOUT)
 
@@ -127,3 +127,53 @@ def test_workspace_size_scales_with_grid_not_problem(lib):
     assert skgemm.workspace_size(1024, 1024, 1024, o2) < small
     oa = skgemm.opts_default(grid=148, tile_n=128, abft=1)
     assert skgemm.workspace_size(1024, 1024, 1024, oa) > small
+
+
+# ----------------------------------------------------------------------------
+# Grid-size model (Stream-K page, App. A.1)
+# ----------------------------------------------------------------------------
+# Model constants (a, c, e, b, d) in microseconds, as fitted for each BLK_N.
+MODEL = {128: (2.64, 0.334, 0.17, 4.67, 1.03), 256: (3.47, 0.364, 0.00, 8.18, 1.73)}
+
+
+def brute_force_cost(m, n, k, bn, g, mode):
+    """The model evaluated on the simulator's explicit segment lists."""
+    a, c, e, b, d = MODEL[bn]
+    sch = ss.schedule(m, n, k, 128, bn, 64, g, mode=mode)
+    op = ss.owners_and_peers(sch)
+    worst = 0.0
+    for segs in sch:
+        iters = sum(s.k_iter_end - s.k_iter_begin for s in segs)
+        tiles = sum(1 for s in segs if s.role != ss.PEER)
+        partial = sum(1 for s in segs if s.role == ss.PEER)
+        peers = sum(len(op[s.tile][1]) for s in segs if s.role == ss.OWNER)
+        worst = max(worst, a + c * iters + e * tiles + b * partial + d * peers)
+    return worst
+
+
+def test_model_cost_matches_segment_walk(lib):
+    rnd = random.Random(99)
+    for _ in range(200):
+        m, n, k = rnd.randint(1, 4000), rnd.randint(1, 4000), rnd.randint(1, 9000)
+        bn = rnd.choice([128, 256])
+        g = rnd.randint(1, 152)
+        mode = rnd.choice(["dp", "sk", "sk2_dp", "dp_sk1"])
+        got = skgemm.schedule_cost(m, n, k, 128, bn, 64, g, MODES[mode])
+        want = brute_force_cost(m, n, k, bn, g, mode)
+        assert abs(got - want) <= 1e-9 * max(1.0, want), (m, n, k, bn, g, mode, got, want)
+
+
+def test_plan_honours_explicit_options_and_picks_minimum(lib):
+    o = skgemm.opts_default(sched="sk", grid=40, tile_n=128)
+    assert skgemm.launch_shape(2048, 2048, 2048, o) == (128, 40, skgemm.SCHED_SK)
+    sms = skgemm.device_sm_count() or 256   # without a device the plan assumes 256 SMs
+    o = skgemm.opts_default(sched="dp")     # fixed schedule, grid 0 -> every SM
+    tn, g, sc = skgemm.launch_shape(2048, 2048, 2048, o)
+    assert sc == skgemm.SCHED_DP and g == sms
+    # automatic choice is never worse than the page's default (2-tile hybrid on all SMs)
+    for (m, n, k) in [(1024, 1024, 1024), (4096, 4096, 4096), (256, 256, 65536),
+                      (128, 19072, 2048), (8192, 1024, 8192)]:
+        tn, g, sc = skgemm.launch_shape(m, n, k, skgemm.opts_default())
+        best = skgemm.schedule_cost(m, n, k, 128, tn, 64, g, sc)
+        for bn in (128, 256):
+            assert best <= skgemm.schedule_cost(m, n, k, 128, bn, 64, sms, skgemm.SCHED_SK2_DP) + 1e-9

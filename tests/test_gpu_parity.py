@@ -196,7 +196,7 @@ def test_square_sweep_abft(size):
     check_sampled(p, C, seed=size)
     check_checksum_probe(p, C)
     rep = ws.report()
-    tile_n, _ = skgemm.launch_shape(size, size, size, skgemm.opts_default(abft=1))
+    tile_n, _, _ = skgemm.launch_shape(size, size, size, skgemm.opts_default(abft=1))
     tiles = ((size + 127) // 128) * ((size + tile_n - 1) // tile_n)
     assert rep.detected == 0 and rep.status_bits == 0, "false positive on a clean run"
     assert rep.tiles_checked == tiles
@@ -245,7 +245,8 @@ def test_injected_fault_detected_located_corrected(mode, bit):
     tm, tn = divmod(tile, tiles_n)
     gi, gj = tm * 128 + row, tn * 128 + col
     v = ref[gi, gj] / p.alpha
-    tau = ab.default_tau(p.k, 128, float(p.A.abs().max()), float(p.B.abs().max()))
+    ma, mb = ab.tile_maxima(p.A.double().numpy(), p.B.double().numpy(), tm, tn, 128, 128)
+    tau = ab.default_tau(p.k, 128, ma, mb)
     kind, delta = ab.classify_flip(v, bit, tau, 1e-3 * tau)
     C, ws, st = _inject(p, dict(sched=mode, tile_n=128, grid=min(64, sms())), tile, row, col, bit)
     assert st == skgemm.OK
@@ -270,9 +271,9 @@ def test_injection_without_abft_corrupts_output():
     C, ws, st = run(p, opts)
     assert st == skgemm.OK
     got = C.cpu().double().numpy()
-    tn = 256 // skgemm.launch_shape(256, 256, 256, opts)[0]
-    tm, tnn = divmod(1, tn)
-    bad = (tm * 128 + 5, tnn * skgemm.launch_shape(256, 256, 256, opts)[0] + 7)
+    bn = skgemm.launch_shape(256, 256, 256, opts)[0]
+    tm, tnn = divmod(1, 256 // bn)
+    bad = (tm * 128 + 5, tnn * bn + 7)
     diff = np.abs(got - ref)
     assert not (diff[bad] < 1e-3)       # the flipped value reached C
     diff[bad] = 0
