@@ -416,6 +416,68 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def ncu_target(args):
+    """Profiling target (no timing): every sweep shape's ABFT GEMM through
+    skg_gemm, `--steps` times, with the library's default plan."""
+    import torch
+    from stream_decomposition_abft_gb300 import _build, inputs, skgemm
+    if not os.path.exists(skgemm.LIB_PATH):
+        _build.build()
+    dev = torch.device("cuda")
+    sh = torch.cuda.current_stream().cuda_stream
+    opts = skgemm.opts_default(abft=1)
+    sizes = [int(x) for x in args.sizes.split(",")] if args.sizes else list(inputs.SQUARE_SIZES)
+    for size in sizes:
+        p = inputs.square(size)
+        A, B = p.A.to(dev), p.B.to(dev)
+        C = torch.empty((size, size), dtype=torch.bfloat16, device=dev)
+        ws = skgemm.Workspace(skgemm.workspace_size(size, size, size, opts), dev)
+        for _ in range(args.steps):
+            st = skgemm.gemm(size, size, size, 1.0, A.data_ptr(), size, B.data_ptr(), size, 0.0,
+                             C.data_ptr(), size, skgemm.IN_BF16, skgemm.OUT_BF16, 0, 0, opts,
+                             ws.ptr, ws.nbytes, sh)
+            if st != skgemm.OK:
+                raise skgemm.SkgError(st, "skg_gemm")
+        torch.cuda.synchronize()
+        if ws.report().detected:
+            raise RuntimeError("ABFT reported a fault on a clean run")
+        print(size, skgemm.launch_shape(size, size, size, opts), flush=True)
+
+
+def write_traffic(csv_path):
+    """Turn an ncu CSV of the main kernel over `--ncu-target --steps S` into
+    profiles/skg_gemm_kernel_square_sweep_traffic.json, stamped with the
+    current kernel-source hash (bench.py reports traffic only while it holds)."""
+    import csv
+    from collections import defaultdict
+    from stream_decomposition_abft_gb300 import inputs
+    rows = list(csv.reader(open(csv_path)))
+    hi = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+    hdr, data = rows[hi], rows[hi + 1:]
+    idi, mi, vi = hdr.index("ID"), hdr.index("Metric Name"), hdr.index("Metric Value")
+    per = defaultdict(dict)
+    for r in data:
+        per[int(r[idi])][r[mi]] = float(r[vi].replace(",", ""))
+    launches = [per[i] for i in sorted(per)]
+    reps = len(launches) // len(inputs.SQUARE_SIZES)
+    out = {"kernel_hash": kernel_hash(), "source_csv": os.path.basename(csv_path),
+           "per_shape": []}
+    tot = []
+    for j, size in enumerate(inputs.SQUARE_SIZES):
+        ls = launches[j * reps:(j + 1) * reps]
+        rd = statistics.mean(x["dram__bytes_read.sum"] for x in ls)
+        wr = statistics.mean(x["dram__bytes_write.sum"] for x in ls)
+        alg = 2 * size * size * 2 + size * size * 2
+        out["per_shape"].append({"size": size, "dram_read": rd, "dram_write": wr,
+                                 "algorithmic_bytes": alg, "ratio": (rd + wr) / alg})
+        tot.append(rd + wr)
+    out["dram_bytes_per_launch_mean"] = statistics.mean(tot)
+    path = os.path.join(ROOT, "profiles", "skg_gemm_kernel_square_sweep_traffic.json")
+    with open(path, "w") as f:
+        json.dump(out, f, indent=1)
+    print(path)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -424,7 +486,18 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ncu-target", action="store_true",
+                    help="run the sweep GEMMs untimed (profiling target)")
+    ap.add_argument("--sizes", default="", help="with --ncu-target: comma-separated sizes")
+    ap.add_argument("--write-traffic", default="",
+                    help="write the traffic JSON from an ncu CSV of the main kernel")
     args = ap.parse_args()
+    if args.write_traffic:
+        write_traffic(args.write_traffic)
+        return
+    if args.ncu_target:
+        ncu_target(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -138,13 +138,19 @@ typedef struct {
   int32_t abft_preencoded; /* 1 = skg_abft_encode already wrote this call's
                            encodings (same A, B, shape and options) into the
                            workspace, so skg_gemm skips its encode pass */
+  int32_t raster_band;  /* output tiles are visited in bands of this many tile
+                           columns, row by row inside a band (L2 reuse);
+                           0 = chosen by the library; >= the number of tile
+                           columns = plain row-major order */
+  int32_t reserved1;
 } skg_opts_t;
 
 /* One segment of a schedule (Stream-K page, Algorithm 5 / §5.2). k_iter_*
  * count MAC iterations of BLK_K within the tile. */
 typedef struct {
   int32_t cta;
-  int32_t tile;         /* row-major tile index: tile = tm * tiles_n + tn */
+  int32_t tile;         /* tile index; with raster_band >= tiles_n it is
+                           row-major, tile = tm * tiles_n + tn */
   int32_t k_iter_begin;
   int32_t k_iter_end;   /* exclusive */
   int32_t role;         /* skg_role_t */

@@ -9,6 +9,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <math.h>
 #include <string.h>
 
 #include <mutex>
@@ -69,6 +70,7 @@ struct Resolved {
   uint64_t* cta_clock;
   int drop_signal;
   int preencoded;
+  int raster_band;
   int ws_grid;  // CTAs the workspace's flags and partial slots are sized for
 };
 
@@ -108,6 +110,8 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
   r.cta_clock = o->cta_clock;
   r.drop_signal = o->test_drop_signal - 1;
   r.preencoded = o->abft_preencoded ? 1 : 0;
+  if (o->raster_band < 0) return SKG_ERR_ARG;
+  r.raster_band = o->raster_band;
   return SKG_OK;
 }
 
@@ -214,6 +218,16 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, ui
   KernelParams p;
   memset(&p, 0, sizeof(p));
   p.s = make_schedule(g.m, g.n, g.k, kBM, r.bn, kBK, r.grid, r.sched);
+  // Banded raster: a wave of g tiles covers about (g / band) rows x band
+  // columns; band ~ sqrt(g * BLK_M / BLK_N) minimises the A + B bytes one
+  // wave touches per k-step.
+  int band = r.raster_band;
+  if (band == 0) {
+    const double b = sqrt((double)r.grid * kBM / r.bn);
+    band = (int)(b + 0.5);
+  }
+  if (band < 1) band = 1;
+  if (band < p.s.tiles_n) p.s.band = band;
   p.m = (int)g.m;
   p.n = (int)g.n;
   p.k = (int)g.k;
@@ -270,6 +284,7 @@ skg_status_t reference_checksums(const Gemm& g, const Resolved& r, uint8_t* ws, 
   rc.trace = nullptr;
   rc.cta_clock = nullptr;
   rc.drop_signal = -1;
+  rc.raster_band = 0;
   const Gemm g1{g.m, (int64_t)kEncRows * L.tiles_b, g.k, g.A, g.lda, ws + L.enc_b, L.kp,
                 ws + L.cr, L.ld_cr, 1.f, 0.f, g.in_dtype, SKG_OUT_F32};
   Plan pl = choose_plan(g1.m, g1.n, g1.k, 0, -1, 0, r.ws_grid);

@@ -409,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pend_par = 0; // parity of that load's phase
       bool ok = true;
       while (ok && cur.next(s, w)) {
-        const int tm = w.tile / s.tiles_n;
-        const int tn = w.tile % s.tiles_n;
+        int tm, tn;
+        tile_coords(s, w.tile, tm, tn);
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!wait_bar(&empty_bar[stage], phase ^ 1, aux, limit)) {
             if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
@@ -531,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!epi_all(got && store_ok && !aborted(aux))) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + ab * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
-      const int tm = w.tile / s.tiles_n;
-      const int tn = w.tile % s.tiles_n;
+      int tm, tn;
+      tile_coords(s, w.tile, tm, tn);
       const int m0 = tm * kBM;
       const int n0 = tn * BN;
       const bool inject_here = (w.tile == p.inject_tile) && (w.role != kRolePeer);

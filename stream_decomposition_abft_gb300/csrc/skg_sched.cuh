@@ -12,8 +12,13 @@
 //     SK + DP" gives one of them up when w >= 2 so every Stream-K CTA holds
 //     between one and two tiles of iterations. DP tiles are the first t_dp
 //     tile indices, walked x, x+g, ...; the Stream-K region is the rest.
-//   - Algorithm 3 (tile coordinates): tiles are numbered row-major,
-//     tile = tm * tiles_n + tn.
+//   - Algorithm 3 (tile coordinates): the page numbers tiles row-major,
+//     tile = tm * tiles_n + tn. Its conclusion names cache-aware tile orders
+//     as future work; here tile indices are walked in bands of `band` tile
+//     columns, row by row inside a band, so the CTAs of one wave share a few
+//     columns of B and rows of A in L2. band >= tiles_n is the page's
+//     row-major order. Only the index -> (tm, tn) map changes; the schedule
+//     (which CTA runs which tile index and k-range) does not.
 #pragma once
 #include <stdint.h>
 
@@ -41,7 +46,19 @@ struct Schedule {
   int64_t sk_total;   // Stream-K iterations (t - t_dp) * ipt
   int64_t sk_q;       // floor(sk_total / g)
   int sk_r;           // sk_total mod g
+  int band;           // tile columns per raster band (tiles_n = row-major)
 };
+
+// Output-tile coordinates of tile index `tile` under the banded raster.
+SKG_HD void tile_coords(const Schedule& s, int tile, int& tm, int& tn) {
+  const int per_band = s.band * s.tiles_m;
+  const int b = tile / per_band;
+  const int within = tile - b * per_band;
+  const int rest = s.tiles_n - b * s.band;
+  const int bw = rest < s.band ? rest : s.band;
+  tm = within / bw;
+  tn = b * s.band + within % bw;
+}
 
 SKG_HD int dp_tiles(int t, int g, int mode) {
   if (mode == kSchedDP) return t;
@@ -64,6 +81,7 @@ SKG_HD Schedule make_schedule(int64_t m, int64_t n, int64_t k, int bm, int bn, i
   s.sk_total = (int64_t)(s.t - s.t_dp) * s.ipt;
   s.sk_q = s.sk_total / g;
   s.sk_r = (int)(s.sk_total % g);
+  s.band = s.tiles_n > 0 ? s.tiles_n : 1;
   return s;
 }
 

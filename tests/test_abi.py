@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_struct_sizes_match_header():
     # Sizes fixed by the header's field lists (x86-64 and aarch64 ABIs agree).
-    assert ctypes.sizeof(skgemm.Opts) == 72
+    assert ctypes.sizeof(skgemm.Opts) == 80
     assert ctypes.sizeof(skgemm.Segment) == 20
     assert ctypes.sizeof(skgemm.FaultRecord) == 64
     assert ctypes.sizeof(skgemm.Report) == 64 + 64 * 64

@@ -278,3 +278,17 @@ def test_injection_without_abft_corrupts_output():
     assert not (diff[bad] < 1e-3)       # the flipped value reached C
     diff[bad] = 0
     assert diff.max() < 1e-2            # and nothing else changed
+
+
+@pytest.mark.parametrize("band", [1, 3, 5, 1000])
+def test_raster_bands(band):
+    # Every banded tile order covers each output tile exactly once, ragged
+    # last band included (band >= tiles_n is the row-major order).
+    p = inputs.make_problem(1000, 1900, 320, seed=band, in_dtype="bf16", out_dtype="f32",
+                            law_a="normal", law_b="normal", alpha=0.5, beta=2.0)
+    ref = reference(p)
+    for mode in ("dp", "sk2_dp"):
+        C, ws, st = run(p, skgemm.opts_default(sched=mode, tile_n=128, grid=min(23, sms()),
+                                               raster_band=band))
+        assert st == skgemm.OK
+        check_full(p, C, ref)
