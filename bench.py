@@ -267,7 +267,9 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)",
                      "traffic": traffic},
         "abft": abft,
-        "gpu_launches": 4 * len(problems) * args.steps,
+        "gpu_launches": args.steps * sum(
+            2 if (2 * ((sz + 127) // 128) <= tn and 2 * ((sz + tn - 1) // tn) <= tn) else 4
+            for sz, (tn, _, _) in plans.items()),
         "clocks": clocks,
         "wall_s_timed": round(wall, 3),
         "e2e": e2e,
@@ -478,6 +480,205 @@ def write_traffic(csv_path):
     print(path)
 
 
+# ---------------------------------------------------------------------------- other workloads
+def _time_launch(fn, flush, reps, stream):
+    """Median event time (ms) of fn() over reps launches, L2 flushed before each."""
+    import torch
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+
+def workload_hostile(args):
+    """Quantisation-hostile fp16 shapes (alpha 1.5, beta 0.5): time, plan and
+    the spread of per-CTA busy time ((max - min) / max of end - start, from
+    %globaltimer), for the automatic plan and for the page's evaluated
+    configuration (two-tile hybrid on every SM, 128 x 128 tiles)."""
+    import torch
+    from stream_decomposition_abft_gb300 import _build, inputs, skgemm
+    if not os.path.exists(skgemm.LIB_PATH):
+        _build.build()
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sms = skgemm.device_sm_count()
+    burst = peaks()[0]
+    names = {v: k for k, v in skgemm.SCHED_NAMES.items()}
+    out = []
+    for (m, n, k) in inputs.HOSTILE_SHAPES:
+        p = inputs.hostile(m, n, k)
+        A, B = p.A.to(dev), p.B.to(dev)
+        C0 = p.C0.to(dev)
+        C = C0.clone()
+        for label, kw in (("auto", {}), ("sk2_dp_all_sms_128x128",
+                                         dict(sched="sk2_dp", grid=sms, tile_n=128))):
+            opts = skgemm.opts_default(**kw)
+            tn, g, sc = skgemm.launch_shape(m, n, k, opts)
+            clk = torch.zeros(2 * g, dtype=torch.int64, device=dev)
+            opts.cta_clock = clk.data_ptr()
+            ws = skgemm.Workspace(skgemm.workspace_size(m, n, k, opts), dev)
+
+            def launch():
+                C.copy_(C0)
+                st = skgemm.gemm(m, n, k, p.alpha, A.data_ptr(), k, B.data_ptr(), k, p.beta,
+                                 C.data_ptr(), n, skgemm.IN_F16, skgemm.OUT_F16, 0, 0, opts,
+                                 ws.ptr, ws.nbytes, sh)
+                if st != skgemm.OK:
+                    raise skgemm.SkgError(st, "skg_gemm")
+
+            ms = _time_launch(launch, flush, max(5, args.steps // 10), stream)
+            c = clk.view(g, 2).cpu().double()
+            busy = (c[:, 1] - c[:, 0])
+            spread = float((busy.max() - busy.min()) / busy.max())
+            out.append({"m": m, "n": n, "k": k, "plan": label, "tile": f"128x{tn}x64",
+                        "grid": g, "sched": names[sc], "ms": round(ms, 4),
+                        "tflops": round(2.0 * m * n * k / ms / 1e9, 1),
+                        "pct_of_peak_measured": round(100 * 2.0 * m * n * k / ms / 1e9 / burst, 1),
+                        "sm_busy_spread": round(spread, 4), "sms_used": g,
+                        "status_bits": ws.report().status_bits})
+    print(json.dumps({"workload": "hostile fp16 shapes, alpha 1.5 beta 0.5 (C0 U[-1,1])",
+                      "unit": "TFLOPS", "results": out}), flush=True)
+
+
+def workload_random(args):
+    """The 1000-shape random fp16 sweep (m, n, k log-uniform on [128, 8192],
+    rounded up to 128, seed 3): geomean and 5th percentile of the fraction of
+    the measured bf16 peak. Timing only (inputs drawn on the device); parity
+    on a subset is in the GPU tests."""
+    import torch
+    from stream_decomposition_abft_gb300 import _build, inputs, skgemm
+    if not os.path.exists(skgemm.LIB_PATH):
+        _build.build()
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    burst = peaks()[0]
+    shapes = inputs.random_shapes(1000)
+    if args.limit:
+        shapes = shapes[:args.limit]
+    opts = skgemm.opts_default()
+    big = max(max(m * k, n * k, m * n) for (m, n, k) in shapes)
+    pool = torch.empty(3 * big, dtype=torch.float16, device=dev).uniform_(-1, 1)
+    ws = skgemm.Workspace(max(skgemm.workspace_size(m, n, k, opts) for (m, n, k) in shapes), dev)
+    fracs = []
+    for (m, n, k) in shapes:
+        A = pool[:m * k]
+        B = pool[big:big + n * k]
+        C = pool[2 * big:2 * big + m * n]
+
+        def launch():
+            st = skgemm.gemm(m, n, k, 1.0, A.data_ptr(), k, B.data_ptr(), k, 0.0, C.data_ptr(), n,
+                             skgemm.IN_F16, skgemm.OUT_F16, 0, 0, opts, ws.ptr, ws.nbytes, sh)
+            if st != skgemm.OK:
+                raise skgemm.SkgError(st, "skg_gemm")
+
+        ms = _time_launch(launch, flush, 3, stream)
+        fracs.append(2.0 * m * n * k / ms / 1e9 / burst)
+    fs = sorted(fracs)
+    p5 = fs[max(0, int(0.05 * len(fs)) - 1)]
+    print(json.dumps({"workload": f"random fp16 sweep, {len(shapes)} shapes (seed 3)",
+                      "geomean_frac_of_peak_measured": round(geomean(fracs), 4),
+                      "p5_frac_of_peak_measured": round(p5, 4),
+                      "median_frac": round(statistics.median(fracs), 4),
+                      "peak_tflops_measured": burst}), flush=True)
+
+
+def workload_mlp(args):
+    """Transformer-MLP bf16 shapes with ABFT on: time with ABFT on and off,
+    and a fault-injection campaign of `--launches` launches per shape with one
+    seeded single-bit flip of one fp32 accumulator per 100 launches (launch
+    ids, tile, row, column and bit drawn from seed 4). Each injected flip is
+    classified in advance with the oracle's fault model (must-detect /
+    harmless / grey) from the oracle's value of that accumulator."""
+    import torch
+    import oracle
+    from oracle import abft_ref as ab
+    from stream_decomposition_abft_gb300 import _build, inputs, skgemm
+    if not os.path.exists(skgemm.LIB_PATH):
+        _build.build()
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    results = []
+    for (m, n, k) in inputs.MLP_SHAPES:
+        p = inputs.mlp(m, n, k)
+        A, B = p.A.to(dev), p.B.to(dev)
+        C = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        o_on = skgemm.opts_default(abft=1)
+        o_off = skgemm.opts_default()
+        ws = skgemm.Workspace(skgemm.workspace_size(m, n, k, o_on), dev)
+        tn, g, sc = skgemm.launch_shape(m, n, k, o_on)
+
+        def launch(o):
+            st = skgemm.gemm(m, n, k, 1.0, A.data_ptr(), k, B.data_ptr(), k, 0.0, C.data_ptr(), n,
+                             skgemm.IN_BF16, skgemm.OUT_BF16, 0, 0, o, ws.ptr, ws.nbytes, sh)
+            if st != skgemm.OK:
+                raise skgemm.SkgError(st, "skg_gemm")
+
+        t_on = _time_launch(lambda: launch(o_on), flush, 5, stream)
+        t_off = _time_launch(lambda: launch(o_off), flush, 5, stream)
+        ws.report(reset=True)
+        ids, gen = inputs.fault_plan(args.launches, seed=4)
+        tiles_m, tiles_n = (m + 127) // 128, (n + tn - 1) // tn
+        Anp, Bnp = p.A.double().numpy(), p.B.double().numpy()
+        camp = {"injected": 0, "must_detect": 0, "detected": 0, "located": 0, "corrected": 0,
+                "harmless_or_grey": 0}
+        for launch_id in range(args.launches):
+            if launch_id not in ids:
+                launch(o_on)
+                continue
+            while True:
+                tile = int(torch.randint(0, tiles_m * tiles_n, (1,), generator=gen))
+                row = int(torch.randint(0, 128, (1,), generator=gen))
+                col = int(torch.randint(0, tn, (1,), generator=gen))
+                bit = int(torch.randint(0, 32, (1,), generator=gen))
+                tm, tnn = tile // tiles_n, tile % tiles_n     # row-major raster for the campaign
+                gi, gj = tm * 128 + row, tnn * tn + col
+                if gi >= m or gj >= n:
+                    continue
+                v = float(oracle.gemm_entries(p.A, p.B, [gi], [gj])[0])
+                ma, mb = ab.tile_maxima(Anp, Bnp, tm, tnn, 128, tn)
+                kind, _ = ab.classify_flip(v, bit, ab.default_tau(k, tn, ma, mb), 1e-6 * abs(v))
+                if kind != ab.GREY:
+                    break
+            oi = skgemm.opts_default(abft=1, inject_tile=tile, inject_row=row, inject_col=col,
+                                     inject_bit=bit, raster_band=tiles_n)
+            launch(oi)
+            rep = ws.report(reset=True)
+            camp["injected"] += 1
+            if kind == ab.MUST_DETECT:
+                camp["must_detect"] += 1
+                recs = [rep.records[i] for i in range(min(rep.n_records, skgemm.MAX_RECORDS))]
+                hit = [r for r in recs if r.injected]
+                if rep.detected:
+                    camp["detected"] += 1
+                if hit and (hit[0].tile, hit[0].row, hit[0].col) == (tile, row, col):
+                    camp["located"] += 1
+                    after = float(hit[0].after)
+                    if abs(after - float(hit[0].clean_value)) <= 1e-3 * math.sqrt(k) * \
+                            float(p.A.abs().max()) * float(p.B.abs().max()):
+                        camp["corrected"] += 1
+            else:
+                camp["harmless_or_grey"] += 1
+        results.append({"m": m, "n": n, "k": k, "plan": f"128x{tn}x64 g={g}",
+                        "ms_abft_on": round(t_on, 4), "ms_abft_off": round(t_off, 4),
+                        "abft_overhead_pct": round(100 * (t_on / t_off - 1), 2),
+                        "tflops_abft_on": round(2.0 * m * n * k / t_on / 1e9, 1),
+                        "campaign": camp, "launches": args.launches})
+    print(json.dumps({"workload": "MLP bf16 shapes, ABFT on, one seeded bit flip per 100 "
+                                  "launches", "results": results}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -491,12 +692,20 @@ def main():
     ap.add_argument("--sizes", default="", help="with --ncu-target: comma-separated sizes")
     ap.add_argument("--write-traffic", default="",
                     help="write the traffic JSON from an ncu CSV of the main kernel")
+    ap.add_argument("--workload", choices=["square", "hostile", "random", "mlp"],
+                    default="square", help="square = the metric's sweep (default)")
+    ap.add_argument("--limit", type=int, default=0, help="random: first N shapes only")
+    ap.add_argument("--launches", type=int, default=300, help="mlp: launches per shape")
     args = ap.parse_args()
     if args.write_traffic:
         write_traffic(args.write_traffic)
         return
     if args.ncu_target:
         ncu_target(args)
+        return
+    if args.workload != "square":
+        {"hostile": workload_hostile, "random": workload_random,
+         "mlp": workload_mlp}[args.workload](args)
         return
     if args.warmup < 3:
         args.warmup = 3

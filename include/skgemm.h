@@ -135,9 +135,10 @@ typedef struct {
   int32_t test_drop_signal; /* testing only: 1 + index of a CTA that skips its
                            Stream-K Signal, so the owner's bounded wait runs out
                            and the launch reports SKG_ERR_FIXUP_TIMEOUT; 0 = none */
-  int32_t abft_preencoded; /* 1 = skg_abft_encode already wrote this call's
-                           encodings (same A, B, shape and options) into the
-                           workspace, so skg_gemm skips its encode pass */
+  int32_t abft_preencoded; /* 1 = skg_abft_encode already wrote the encodings
+                           of this call's A and B (same shape and options) into
+                           the workspace, so skg_gemm skips the encode pass and
+                           only forms the checksums from them */
   int32_t raster_band;  /* output tiles are visited in bands of this many tile
                            columns, row by row inside a band (L2 reuse);
                            0 = chosen by the library; >= the number of tile
@@ -236,14 +237,15 @@ skg_status_t skg_gemm_verify(int64_t m, int64_t n, int64_t k, float alpha, const
                              int32_t b_layout, const skg_opts_t* opts, void* workspace,
                              size_t ws_bytes, void* stream);
 
-/* The ABFT encode pass of skg_gemm_verify on its own: e^T A over each
- * 128-row tile of A and B e over each BLK_N-column tile of B, split into
- * three input-precision terms, plus max|A| and max|B| for the default
- * thresholds ("Anatomy of High-Performance GEMM with Online Fault Tolerance
- * on GPUs", threadblock-level ABFT, Fig. 5: the encodings e^T A and B e of
- * each threadblock's operands). Arguments as for skg_gemm (opts decides
- * BLK_N and must be the options of the gemm call that follows with
- * opts->abft_preencoded = 1). Asynchronous on `stream`. */
+/* The ABFT encode pass of skg_gemm_verify on its own (one kernel): e^T A
+ * over each 128-row tile of A and B e over each BLK_N-column tile of B,
+ * each split into hi and lo terms of the input type with a per-tile scale,
+ * plus per-tile max |A| and max |B| for the default thresholds ("Anatomy of
+ * High-Performance GEMM with Online Fault Tolerance on GPUs",
+ * threadblock-level ABFT, Fig. 5: the encodings e^T A and B e of each
+ * threadblock's operands). Arguments as for skg_gemm; opts must be the
+ * options of the gemm call that follows with opts->abft_preencoded = 1.
+ * Asynchronous on `stream`. */
 skg_status_t skg_abft_encode(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
                              const void* B, int64_t ldb, int32_t in_dtype,
                              const skg_opts_t* opts, void* workspace, size_t ws_bytes,

@@ -71,7 +71,8 @@ struct Resolved {
   int drop_signal;
   int preencoded;
   int raster_band;
-  int ws_grid;  // CTAs the workspace's flags and partial slots are sized for
+  int ws_grid;
+  int64_t k_for_plan;  // CTAs the workspace's flags and partial slots are sized for
 };
 
 // Schedule, g and BLK_N: whatever the options leave open is chosen by the
@@ -95,7 +96,8 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
   r.sched = pl.sched;
   r.grid = pl.grid;
   r.bn = pl.bn;
-  r.ws_grid = r.abft ? ms : r.grid;  // ABFT checksum GEMMs may use up to every SM
+  r.ws_grid = r.abft ? ms : r.grid;
+  r.k_for_plan = k > 0 ? k : 1;  // ABFT checksum GEMMs may use up to every SM
   r.tau_row = o->tau_row;
   r.tau_col = o->tau_col;
   r.inject_tile = o->inject_tile;
@@ -188,36 +190,62 @@ struct Gemm {
 };
 
 template <int BN, bool ABFT>
-cudaError_t dispatch_out(int out_dtype, const CUtensorMap& a, const CUtensorMap& b,
-                         const CUtensorMap& c, const KernelParams& p, int grid,
+cudaError_t dispatch_out(int out_dtype, const Maps& mp, const KernelParams& p, int grid,
                          cudaStream_t st) {
   switch (out_dtype) {
-    case SKG_OUT_F32: return launch_gemm<BN, ABFT, 0>(a, b, c, p, grid, st);
-    case SKG_OUT_F16: return launch_gemm<BN, ABFT, 1>(a, b, c, p, grid, st);
-    default: return launch_gemm<BN, ABFT, 2>(a, b, c, p, grid, st);
+    case SKG_OUT_F32: return launch_gemm<BN, ABFT, 0>(mp, p, grid, st);
+    case SKG_OUT_F16: return launch_gemm<BN, ABFT, 1>(mp, p, grid, st);
+    default: return launch_gemm<BN, ABFT, 2>(mp, p, grid, st);
   }
 }
 
-skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, uint8_t* ws,
-                        const Layout& L, cudaStream_t stream) {
+// Fused ABFT checksum GEMMs fit one tile column each when 2 * tiles <= BN.
+bool can_fuse_checksums(const Layout& L, int bn) {
+  return kEncRows * L.tiles_a <= bn && kEncRows * L.tiles_b <= bn;
+}
+
+// One launch of the persistent kernel: C = alpha A B^T + beta C with A
+// (m x k, row stride lda) and B (n x k, row stride ldb) in `in_dtype`.
+// With fuse_ck, the tiles of the two ABFT checksum GEMMs are scheduled in
+// front of the output tiles of the same launch.
+skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bool fuse_ck,
+                        uint8_t* ws, const Layout& L, cudaStream_t stream) {
   const CUtensorMapDataType in_t = g.in_dtype == SKG_IN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const CUtensorMapDataType out_t = g.out_dtype == SKG_OUT_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                     : g.out_dtype == SKG_OUT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int out_bytes = g.out_dtype == SKG_OUT_F32 ? 4 : 2;
-  CUtensorMap tmA, tmB, tmC;
-  if (make_map(&tmA, in_t, 2, g.A, (uint64_t)g.k, (uint64_t)g.m, (uint64_t)g.lda, kBK, kBM) !=
+  Maps mp;
+  if (make_map(&mp.a, in_t, 2, g.A, (uint64_t)g.k, (uint64_t)g.m, (uint64_t)g.lda, kBK, kBM) !=
           CUDA_SUCCESS ||
-      make_map(&tmB, in_t, 2, g.B, (uint64_t)g.k, (uint64_t)g.n, (uint64_t)g.ldb, kBK, r.bn) !=
+      make_map(&mp.b, in_t, 2, g.B, (uint64_t)g.k, (uint64_t)g.n, (uint64_t)g.ldb, kBK, r.bn) !=
           CUDA_SUCCESS ||
-      make_map(&tmC, out_t, out_bytes, g.C, (uint64_t)g.n, (uint64_t)g.m, (uint64_t)g.ldc,
+      make_map(&mp.c, out_t, out_bytes, g.C, (uint64_t)g.n, (uint64_t)g.m, (uint64_t)g.ldc,
                128 / out_bytes, 32) != CUDA_SUCCESS)
     return SKG_ERR_UNSUPPORTED;
+  mp.b128 = mp.be = mp.ea = mp.cr = mp.cc = mp.a;
+  int t_ck = 0, ck_cr = 0;
+  if (fuse_ck) {
+    const int n_cr = kEncRows * L.tiles_b, n_cc = kEncRows * L.tiles_a;
+    if (make_map(&mp.b128, in_t, 2, g.B, (uint64_t)g.k, (uint64_t)g.n, (uint64_t)g.ldb, kBK,
+                 kBM) != CUDA_SUCCESS ||
+        make_map(&mp.be, in_t, 2, ws + L.enc_b, (uint64_t)L.kp, (uint64_t)n_cr, (uint64_t)L.kp,
+                 kBK, r.bn) != CUDA_SUCCESS ||
+        make_map(&mp.ea, in_t, 2, ws + L.enc_a, (uint64_t)L.kp, (uint64_t)n_cc, (uint64_t)L.kp,
+                 kBK, r.bn) != CUDA_SUCCESS ||
+        make_map(&mp.cr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws + L.cr, (uint64_t)n_cr,
+                 (uint64_t)g.m, (uint64_t)L.ld_cr, 32, 32) != CUDA_SUCCESS ||
+        make_map(&mp.cc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws + L.cc, (uint64_t)n_cc,
+                 (uint64_t)g.n, (uint64_t)L.ld_cc, 32, 32) != CUDA_SUCCESS)
+      return SKG_ERR_UNSUPPORTED;
+    ck_cr = (int)((g.m + kBM - 1) / kBM);
+    t_ck = ck_cr + (int)((g.n + kBM - 1) / kBM);
+  }
 
   KernelParams p;
   memset(&p, 0, sizeof(p));
-  p.s = make_schedule(g.m, g.n, g.k, kBM, r.bn, kBK, r.grid, r.sched);
+  p.s = make_schedule(g.m, g.n, g.k, kBM, r.bn, kBK, r.grid, r.sched, t_ck);
   // Banded raster: a wave of g tiles covers about (g / band) rows x band
   // columns; band ~ sqrt(g * BLK_M / BLK_N) minimises the A + B bytes one
   // wave touches per k-step.
@@ -234,6 +262,11 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, ui
   p.alpha = g.alpha;
   p.beta = g.beta;
   p.idesc_main = idesc_f16(g.in_dtype == SKG_IN_BF16, kBM, r.bn);
+  p.ck_cr_tiles = ck_cr;
+  p.ck_n_cr = kEncRows * L.tiles_b;
+  p.ck_n_cc = kEncRows * L.tiles_a;
+  p.idesc_cr = idesc_f16(g.in_dtype == SKG_IN_BF16, kBM, (uint32_t)round_up(p.ck_n_cr, 16));
+  p.idesc_cc = idesc_f16(g.in_dtype == SKG_IN_BF16, kBM, (uint32_t)round_up(p.ck_n_cc, 16));
   p.hdr = (WsHeader*)ws;
   p.report = (skg_report_t*)(ws + 256);
   p.flags = (uint32_t*)(ws + L.flags);
@@ -257,11 +290,11 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, ui
 
   cudaError_t e;
   if (r.bn == 128)
-    e = abft_epilogue ? dispatch_out<128, true>(g.out_dtype, tmA, tmB, tmC, p, r.grid, stream)
-                      : dispatch_out<128, false>(g.out_dtype, tmA, tmB, tmC, p, r.grid, stream);
+    e = abft_epilogue ? dispatch_out<128, true>(g.out_dtype, mp, p, r.grid, stream)
+                      : dispatch_out<128, false>(g.out_dtype, mp, p, r.grid, stream);
   else
-    e = abft_epilogue ? dispatch_out<256, true>(g.out_dtype, tmA, tmB, tmC, p, r.grid, stream)
-                      : dispatch_out<256, false>(g.out_dtype, tmA, tmB, tmC, p, r.grid, stream);
+    e = abft_epilogue ? dispatch_out<256, true>(g.out_dtype, mp, p, r.grid, stream)
+                      : dispatch_out<256, false>(g.out_dtype, mp, p, r.grid, stream);
   return e == cudaSuccess ? SKG_OK : SKG_ERR_CUDA;
 }
 
@@ -273,8 +306,9 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, ui
 //   cr_all  (m x 2 tiles_b) = A x [Be_hi; Be_lo]^T
 //   ccT_all (n x 2 tiles_a) = B x [eA_hi; eA_lo]^T     (= ((e^T A) B)^T)
 skg_status_t reference_checksums(const Gemm& g, const Resolved& r, uint8_t* ws, const Layout& L,
-                                 cudaStream_t stream) {
-  if (launch_encode(g.in_dtype == SKG_IN_BF16, g.A, g.lda, (int)g.m, g.B, g.ldb, (int)g.n,
+                                 cudaStream_t stream, bool skip_encode) {
+  if (!skip_encode &&
+      launch_encode(g.in_dtype == SKG_IN_BF16, g.A, g.lda, (int)g.m, g.B, g.ldb, (int)g.n,
                     (int)g.k, L.kp, r.bn, (float*)(ws + L.sums), ws + L.enc_a, ws + L.enc_b,
                     (TileStat*)(ws + L.stat), (TilePub*)(ws + L.pub), stream) != cudaSuccess)
     return SKG_ERR_CUDA;
@@ -291,7 +325,7 @@ skg_status_t reference_checksums(const Gemm& g, const Resolved& r, uint8_t* ws, 
   rc.bn = pl.bn;
   rc.sched = pl.sched;
   rc.grid = pl.grid;
-  skg_status_t st = launch_one(g1, rc, false, ws, L, stream);
+  skg_status_t st = launch_one(g1, rc, false, false, ws, L, stream);
   if (st != SKG_OK) return st;
   const Gemm g2{g.n, (int64_t)kEncRows * L.tiles_a, g.k, g.B, g.ldb, ws + L.enc_a, L.kp,
                 ws + L.cc, L.ld_cc, 1.f, 0.f, g.in_dtype, SKG_OUT_F32};
@@ -299,7 +333,24 @@ skg_status_t reference_checksums(const Gemm& g, const Resolved& r, uint8_t* ws, 
   rc.bn = pl.bn;
   rc.sched = pl.sched;
   rc.grid = pl.grid;
-  return launch_one(g2, rc, false, ws, L, stream);
+  return launch_one(g2, rc, false, false, ws, L, stream);
+}
+
+// With fused checksum tiles the launch has tiles_a + ceil(n / 128) more
+// full-k tiles; re-plan the grid (and schedule) for them unless fixed.
+void replan_fused(int64_t m, int64_t n, const skg_opts_t* opts, Resolved& r) {
+  skg_opts_t d;
+  if (!opts) {
+    skg_opts_default(&d);
+    opts = &d;
+  }
+  if (opts->grid != 0) return;
+  const int t_ck = (int)((m + kBM - 1) / kBM + (n + kBM - 1) / kBM);
+  const int want_sched = opts->sched == SKG_SCHED_AUTO ? -1 : opts->sched;
+  const Plan pl = choose_plan(m, n, r.k_for_plan, r.bn, want_sched,
+                              want_sched >= 0 ? r.ws_grid : 0, r.ws_grid, t_ck);
+  r.grid = pl.grid;
+  r.sched = pl.sched;
 }
 
 skg_status_t check_inputs(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
@@ -355,11 +406,22 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
 
   uint8_t* ws = (uint8_t*)workspace;
   const Gemm g{m, n, k, A, lda, B, ldb, C, ldc, alpha, beta, in_dtype, out_dtype};
-  if (r.abft && !r.preencoded) {
-    st = reference_checksums(g, r, ws, L, stream);
+  bool fuse = false;
+  if (r.abft && can_fuse_checksums(L, r.bn)) {
+    // The checksum-GEMM tiles run ahead of the output tiles in the same
+    // launch, after the encode pass (skipped when pre-encoded).
+    fuse = true;
+    replan_fused(m, n, opts, r);
+    if (!r.preencoded &&
+        launch_encode(in_dtype == SKG_IN_BF16, A, lda, (int)m, B, ldb, (int)n, (int)k, L.kp, r.bn,
+                      (float*)(ws + L.sums), ws + L.enc_a, ws + L.enc_b, (TileStat*)(ws + L.stat),
+                      (TilePub*)(ws + L.pub), stream) != cudaSuccess)
+      return SKG_ERR_CUDA;
+  } else if (r.abft) {
+    st = reference_checksums(g, r, ws, L, stream, r.preencoded != 0);
     if (st != SKG_OK) return st;
   }
-  return launch_one(g, r, r.abft != 0, ws, L, stream);
+  return launch_one(g, r, r.abft != 0, fuse, ws, L, stream);
 }
 
 }  // namespace
@@ -426,8 +488,12 @@ skg_status_t skg_abft_encode(int64_t m, int64_t n, int64_t k, const void* A, int
   const Layout L = layout(m, n, k, r);
   if (!workspace || !aligned16(workspace) || ws_bytes < L.total) return SKG_ERR_WORKSPACE;
   if (!tensor_map_encoder()) return SKG_ERR_CUDA;
-  const Gemm g{m, n, k, A, lda, B, ldb, nullptr, 0, 1.f, 0.f, in_dtype, SKG_OUT_F32};
-  return reference_checksums(g, r, (uint8_t*)workspace, L, (cudaStream_t)stream);
+  uint8_t* ws = (uint8_t*)workspace;
+  return launch_encode(in_dtype == SKG_IN_BF16, A, lda, (int)m, B, ldb, (int)n, (int)k, L.kp, r.bn,
+                       (float*)(ws + L.sums), ws + L.enc_a, ws + L.enc_b, (TileStat*)(ws + L.stat),
+                       (TilePub*)(ws + L.pub), (cudaStream_t)stream) == cudaSuccess
+             ? SKG_OK
+             : SKG_ERR_CUDA;
 }
 
 skg_status_t skg_schedule_query(int64_t m, int64_t n, int64_t k, int32_t bm, int32_t bn,
@@ -477,6 +543,8 @@ skg_status_t skg_launch_shape(int64_t m, int64_t n, int64_t k, const skg_opts_t*
   const int sms = sm_count_cached();
   skg_status_t st = resolve(m, n, k, opts, r, sms);
   if (st != SKG_OK) return st;
+  if (r.abft && m > 0 && n > 0 && k > 0 && can_fuse_checksums(layout(m, n, k, r), r.bn))
+    replan_fused(m, n, opts, r);
   if (tile_n) *tile_n = r.bn;
   if (grid) *grid = r.grid;
   if (sched) *sched = r.sched;

@@ -7,8 +7,7 @@
 namespace skg {
 
 template <int BN, bool ABFT, int OUT>
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                        const KernelParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_gemm(const Maps& mp, const KernelParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<BN, ABFT, OUT>;
   // The shared-memory opt-in is per device; set it once per device.
   static std::atomic<uint64_t> done_mask{0};
@@ -22,14 +21,13 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     if (e != cudaSuccess) return e;
     done_mask.fetch_or(bit, std::memory_order_acq_rel);
   }
-  return launch_pdl(skg_gemm_kernel<C>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, stream, tmA,
-                    tmB, tmC, p);
+  return launch_pdl(skg_gemm_kernel<C>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, stream, mp.a,
+                    mp.b, mp.c, mp.b128, mp.be, mp.ea, mp.cr, mp.cc, p);
 }
 
 #define SKG_INST(OUT)                                                                        \
   template cudaError_t launch_gemm<128, true, OUT>( \
-      const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KernelParams&, int, \
-      cudaStream_t);
+      const Maps&, const KernelParams&, int, cudaStream_t);
 SKG_INST(0)
 SKG_INST(1)
 SKG_INST(2)

@@ -22,15 +22,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
+#ifdef SKG_NO_PDL
+  cfg.numAttrs = 0;  // build variant without programmatic dependent launch
+#else
   cfg.numAttrs = 1;
+#endif
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
+
+// TMA descriptors of one launch: A (box 64 x 128), B (64 x BLK_N), C (store
+// box 128 bytes x 32 rows); with fused ABFT checksum tiles also B as an
+// A-operand (64 x 128), the hi/lo encodings of B and A (64 x BLK_N) and the
+// fp32 checksum outputs cr_all and ccT_all (32 x 32). Unused ones repeat A.
+struct Maps {
+  CUtensorMap a, b, c, b128, be, ea, cr, cc;
+};
 
 // Launch the persistent kernel instantiated for (BN, ABFT, OUT) on `grid`
 // CTAs. Defined in the skg_inst_*.cu translation units.
 template <int BN, bool ABFT, int OUT>
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                        const KernelParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_gemm(const Maps& mp, const KernelParams& p, int grid, cudaStream_t stream);
 
 // ABFT encode pass (skg_encode.cu): e^T A per 128-row tile of A and B e
 // per bn-row tile of the stored n x k B, as hi / lo rows in the input type

@@ -60,9 +60,10 @@ constexpr uint32_t kSmemLimit = 232448;
 
 // Workspace header (device). The report follows at offset 256.
 struct WsHeader {
-  uint32_t epoch;  // launches completed on this workspace
-  uint32_t done;   // CTA tickets of the running launch
-  uint32_t pad[62];
+  uint32_t epoch;    // launches completed on this workspace
+  uint32_t done;     // CTA tickets of the running launch
+  uint32_t ck_done;  // fused checksum tiles stored by the running launch
+  uint32_t pad[61];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
@@ -97,6 +98,13 @@ struct KernelParams {
   int64_t ld_cr, ld_cc;
   const TilePub* pub_a;  // per 128-row tile of A
   const TilePub* pub_b;  // per BLK_N-column tile of B
+  // Fused reference-checksum GEMMs: tiles [0, s.t_ck) of the schedule.
+  // Tile j < ck_cr_tiles computes rows [128 j, 128 j + 128) of
+  // cr_all = A x [Be_hi; Be_lo]^T (ck_n_cr columns); the others compute rows
+  // of ccT_all = B x [eA_hi; eA_lo]^T (ck_n_cc columns). Both store fp32.
+  int ck_cr_tiles;
+  int ck_n_cr, ck_n_cc;
+  uint32_t idesc_cr, idesc_cc;
   float tau_row, tau_col;  // <= 0: derive from the encode pass maxima
   int inject_tile, inject_row, inject_col, inject_bit;
   uint64_t timeout_ns;
@@ -339,7 +347,12 @@ __device__ __forceinline__ void add_peer_partials(float (&v)[32], float* partial
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     skg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
+                    const __grid_constant__ CUtensorMap tmC,
+                    const __grid_constant__ CUtensorMap tmB128,
+                    const __grid_constant__ CUtensorMap tmBE,
+                    const __grid_constant__ CUtensorMap tmEA,
+                    const __grid_constant__ CUtensorMap tmCr,
+                    const __grid_constant__ CUtensorMap tmCc, const KernelParams p) {
   constexpr int BN = C::BN;
   constexpr int STAGES = C::STAGES;
   constexpr int ACC_BUFS = C::ACC_BUFS;
@@ -365,6 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
+    if (C::ABFT && p.s.t_ck > 0) {
+      prefetch_tmap(&tmB128);
+      prefetch_tmap(&tmBE);
+      prefetch_tmap(&tmEA);
+      prefetch_tmap(&tmCr);
+      prefetch_tmap(&tmCc);
+    }
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
@@ -409,8 +429,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pend_par = 0; // parity of that load's phase
       bool ok = true;
       while (ok && cur.next(s, w)) {
-        int tm, tn;
-        tile_coords(s, w.tile, tm, tn);
+        // Operand maps and row coordinates of this tile: an output tile, or
+        // a tile of one of the fused checksum GEMMs.
+        const CUtensorMap* mapA = &tmA;
+        const CUtensorMap* mapB = &tmB;
+        int rowA, rowB;
+        if (w.tile >= s.t_ck) {
+          int tm, tn;
+          tile_coords(s, w.tile, tm, tn);
+          rowA = tm * kBM;
+          rowB = tn * BN;
+        } else if (w.tile < p.ck_cr_tiles) {
+          mapB = &tmBE;
+          rowA = w.tile * kBM;
+          rowB = 0;
+        } else {
+          mapA = &tmB128;
+          mapB = &tmEA;
+          rowA = (w.tile - p.ck_cr_tiles) * kBM;
+          rowB = 0;
+        }
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!wait_bar(&empty_bar[stage], phase ^ 1, aux, limit)) {
             if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
@@ -419,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* st = ring + stage * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
-          tma_load_2d(st, &tmA, &full_bar[stage], kb * kBK, tm * kBM);
-          tma_load_2d(st + C::A_BYTES, &tmB, &full_bar[stage], kb * kBK, tn * BN);
+          tma_load_2d(st, mapA, &full_bar[stage], kb * kBK, rowA);
+          tma_load_2d(st + C::A_BYTES, mapB, &full_bar[stage], kb * kBK, rowB);
           pending |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -453,6 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + ab * C::ACC_COLS;
+        const uint32_t idesc = w.tile >= s.t_ck ? p.idesc_main
+                               : (w.tile < p.ck_cr_tiles ? p.idesc_cr : p.idesc_cc);
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!wait_bar(&full_bar[stage], phase, aux, limit)) {
             if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
@@ -467,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t ad = sdesc_sw128(a_addr + kk * 32);
             const uint64_t bd = sdesc_sw128(b_addr + kk * 32);
             const uint32_t acc = (kb > w.kb_begin || kk > 0) ? 1u : 0u;
-            umma_f16(d, ad, bd, p.idesc_main, acc);
+            umma_f16(d, ad, bd, idesc, acc);
           }
           issued = true;
           umma_commit(&empty_bar[stage]);
@@ -514,11 +554,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t c0_phase = 0;
     int nseg = 0;
     bool store_ok = true;
+    bool ck_ready = false;
     while (cur.next(s, w)) {
       if (p.trace && et == 0) {
         int32_t* tr = p.trace + (size_t)blockIdx.x * SKG_TRACE_STRIDE;
         if (nseg < SKG_TRACE_CAP) {
-          tr[1 + 4 * nseg] = w.tile;
+          tr[1 + 4 * nseg] = w.tile - s.t_ck;
           tr[2 + 4 * nseg] = w.kb_begin;
           tr[3 + 4 * nseg] = w.kb_end;
           tr[4 + 4 * nseg] = w.role;
@@ -531,11 +572,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!epi_all(got && store_ok && !aborted(aux))) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + ab * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
-      int tm, tn;
-      tile_coords(s, w.tile, tm, tn);
+      const bool is_ck = w.tile < s.t_ck;  // a fused checksum-GEMM tile
+      int tm = 0, tn = 0;
+      if (!is_ck) tile_coords(s, w.tile, tm, tn);
       const int m0 = tm * kBM;
       const int n0 = tn * BN;
-      const bool inject_here = (w.tile == p.inject_tile) && (w.role != kRolePeer);
+      const int out_tile = w.tile - s.t_ck;  // output-tile number the caller sees
+      const bool inject_here = !is_ck && (out_tile == p.inject_tile) && (w.role != kRolePeer);
 
       if (w.role == kRolePeer) {
         // StorePartials + Signal (Algorithm 5, non-started segment).
@@ -583,9 +626,84 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 
+        if (C::ABFT && is_ck) {
+          // -------------------------------------------- fused checksum tile
+          // Store fp32 rows of cr_all or ccT_all, then count the tile done
+          // once every warp's stores have landed.
+          const bool cr_side = w.tile < p.ck_cr_tiles;
+          const CUtensorMap* mapC = cr_side ? &tmCr : &tmCc;
+          const int rows = cr_side ? p.m : p.n;
+          const int ncols = cr_side ? p.ck_n_cr : p.ck_n_cc;
+          const int r0 = (cr_side ? w.tile : w.tile - p.ck_cr_tiles) * kBM;
+          const int nchunks = (ncols + 31) / 32;
+          const bool live = (r0 + q * 32) < rows;
+#pragma unroll 1
+          for (int c = 0; c < nchunks; ++c) {
+            uint32_t u[32];
+            float v[32];
+            tmem_ld32(tacc + c * 32, u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
+            if (owner) add_peer_partials<BN>(v, p.partials, blockIdx.x + 1, w.peer_last, c, r);
+            if (c == nchunks - 1) {
+              tc_fence_before();
+              mbar_arrive(&tempty_bar[ab]);
+            }
+            if (!live || !store_ok) continue;  // warp-uniform
+            uint8_t* buf = ebuf + bsel * C::EPI_BUF_BYTES;
+            if (lane == 0) bulk_wait_read<C::EPI_BUFS - 1>();
+            __syncwarp();
+            uint32_t wv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) wv[i] = __float_as_uint(v[i]);
+            staging_write(buf, lane, wv);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(mapC, buf, c * 32, r0 + q * 32);
+              bulk_commit();
+            }
+            bsel = (bsel + 1) % C::EPI_BUFS;
+          }
+          if (lane == 0) bulk_wait<0>();
+          __syncwarp();
+          named_bar_sync(1, kEpiThreads);
+          if (et == 0) {
+            __threadfence();
+            atomicAdd(&p.hdr->ck_done, 1u);
+          }
+          if (++ab == ACC_BUFS) {
+            ab = 0;
+            aphase ^= 1;
+          }
+          continue;
+        }
+
         // ------------------------------------------------ ABFT verify
         int fix_row = -1, fix_col = -1;
         float fix_val = 0.f;
+        if (C::ABFT && s.t_ck > 0 && !ck_ready) {
+          // The fused checksum tiles must all be stored before the first
+          // verification reads them.
+          bool fine = true;
+          if (et == 0) {
+            const uint64_t t0 = globaltimer();
+            while (ld_acquire_gpu(&p.hdr->ck_done) < (uint32_t)s.t_ck) {
+              nanosleep_ns(128);
+              if (globaltimer() - t0 > limit) {
+                record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
+                fine = false;
+                break;
+              }
+            }
+          }
+          if (!epi_all(fine && !aborted(aux))) {
+            tc_fence_before();
+            mbar_arrive(&tempty_bar[ab]);
+            break;
+          }
+          ck_ready = true;
+        }
         if (C::ABFT) {
           // This warp's staging buffers hold its column sums below: its own
           // earlier TMA stores must have finished reading them.
@@ -719,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (idx < SKG_MAX_RECORDS) {
                 skg_fault_record_t* rec = &p.report->records[idx];
                 rec->launch = epoch;
-                rec->tile = w.tile;
+                rec->tile = out_tile;
                 rec->row = brow;
                 rec->col = bcol;
                 rec->status = SKG_ABFT_CORRECTED;
@@ -741,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (idx < SKG_MAX_RECORDS) {
               skg_fault_record_t* rec = &p.report->records[idx];
               rec->launch = epoch;
-              rec->tile = w.tile;
+              rec->tile = out_tile;
               rec->row = nbr == 1 ? brow : -1;
               rec->col = nbc == 1 ? bcol : -1;
               rec->status = SKG_ABFT_UNCORRECTABLE;
@@ -869,6 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ticket == gridDim.x - 1) {
       // Last CTA of the launch: every CTA has read the epoch, so advance it.
       p.hdr->done = 0;
+      p.hdr->ck_done = 0;
       atomicAdd(&p.report->launches, 1u);
       __threadfence();
       atomicAdd(&p.hdr->epoch, 1u);

@@ -77,14 +77,14 @@ struct Plan {
 // Best (BLK_N, schedule, g) for an m x n x k launch on `sms` SMs. Fixed
 // choices (want_* != 0 / >= 0) are kept; the rest are searched.
 inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_sched,
-                        int want_grid, int sms) {
+                        int want_grid, int sms, int t_ck) {
   static const int kCands[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 76, 96, 112, 128, 144};
   Plan best{want_bn ? want_bn : 256, want_sched >= 0 ? want_sched : kSchedSK2DP,
             want_grid ? want_grid : sms, 1e300};
   for (int bn = 128; bn <= 256; bn += 128) {
     if (want_bn && bn != want_bn) continue;
     const CostModel& M = bn == 128 ? kModel128 : kModel256;
-    const int64_t t = ((m + kTileM - 1) / kTileM) * ((n + bn - 1) / bn);
+    const int64_t t = ((m + kTileM - 1) / kTileM) * ((n + bn - 1) / bn) + t_ck;
     int cands[64];
     int nc = 0;
     if (want_grid) {
@@ -112,7 +112,7 @@ inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_s
         // with two or more full waves the hybrids exist to bound it, so the
         // automatic choice does not take basic SK there.
         if (want_sched < 0 && sched == kSchedSK && t >= 2 * (int64_t)cands[i]) continue;
-        const Schedule s = make_schedule(m, n, k, kTileM, bn, kTileK, cands[i], sched);
+        const Schedule s = make_schedule(m, n, k, kTileM, bn, kTileK, cands[i], sched, t_ck);
         const double us = predict_us(s, M);
         // Prefer fewer CTAs on ties (less fixup storage and traffic).
         if (us < best.us - 1e-9 || (us < best.us + 1e-9 && cands[i] < best.grid)) {
@@ -127,32 +127,32 @@ inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_s
 // search_plan behind a small cache: the search walks up to ~150 candidate
 // schedules of up to `sms` CTAs each, far more host time than a launch.
 inline Plan choose_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_sched,
-                        int want_grid, int sms) {
+                        int want_grid, int sms, int t_ck = 0) {
   struct Key {
     int64_t m, n, k;
-    int bn, sched, grid, sms;
+    int bn, sched, grid, sms, t_ck;
     bool operator==(const Key& o) const {
       return m == o.m && n == o.n && k == o.k && bn == o.bn && sched == o.sched &&
-             grid == o.grid && sms == o.sms;
+             grid == o.grid && sms == o.sms && t_ck == o.t_ck;
     }
   };
   struct Hash {
     size_t operator()(const Key& x) const {
       uint64_t h = 1469598103934665603ull;
-      const int64_t v[7] = {x.m, x.n, x.k, x.bn, x.sched, x.grid, x.sms};
+      const int64_t v[8] = {x.m, x.n, x.k, x.bn, x.sched, x.grid, x.sms, x.t_ck};
       for (int64_t e : v) h = (h ^ (uint64_t)e) * 1099511628211ull;
       return (size_t)h;
     }
   };
   static std::mutex mu;
   static std::unordered_map<Key, Plan, Hash> cache;
-  const Key key{m, n, k, want_bn, want_sched, want_grid, sms};
+  const Key key{m, n, k, want_bn, want_sched, want_grid, sms, t_ck};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
-  const Plan p = search_plan(m, n, k, want_bn, want_sched, want_grid, sms);
+  const Plan p = search_plan(m, n, k, want_bn, want_sched, want_grid, sms, t_ck);
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();
   cache.emplace(key, p);

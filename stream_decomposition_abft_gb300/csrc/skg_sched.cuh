@@ -40,7 +40,8 @@ enum : int { kRoleFull = 0, kRoleOwner = 1, kRolePeer = 2 };
 struct Schedule {
   int tiles_m, tiles_n;
   int ipt;            // MAC iterations per tile, ceil(k / BLK_K)
-  int t;              // tiles
+  int t;              // tiles (t_ck + tiles_m * tiles_n)
+  int t_ck;           // leading tiles of fused side GEMMs (0 for a plain GEMM)
   int t_dp;           // data-parallel tiles [0, t_dp)
   int g;              // persistent CTAs
   int64_t sk_total;   // Stream-K iterations (t - t_dp) * ipt
@@ -49,8 +50,10 @@ struct Schedule {
   int band;           // tile columns per raster band (tiles_n = row-major)
 };
 
-// Output-tile coordinates of tile index `tile` under the banded raster.
+// Output-tile coordinates of tile index `tile` (>= t_ck) under the banded
+// raster.
 SKG_HD void tile_coords(const Schedule& s, int tile, int& tm, int& tn) {
+  tile -= s.t_ck;
   const int per_band = s.band * s.tiles_m;
   const int b = tile / per_band;
   const int within = tile - b * per_band;
@@ -69,13 +72,16 @@ SKG_HD int dp_tiles(int t, int g, int mode) {
   return w * g;  // DP + one-tile SK, and the two-tile hybrid when w < 2
 }
 
+// `t_ck` extra full-k tiles are placed in front of the output tiles (the
+// fused ABFT checksum GEMMs); the schedule treats every tile alike.
 SKG_HD Schedule make_schedule(int64_t m, int64_t n, int64_t k, int bm, int bn, int bk, int g,
-                              int mode) {
+                              int mode, int t_ck = 0) {
   Schedule s;
   s.tiles_m = (int)((m + bm - 1) / bm);
   s.tiles_n = (int)((n + bn - 1) / bn);
   s.ipt = (int)((k + bk - 1) / bk);
-  s.t = s.tiles_m * s.tiles_n;
+  s.t_ck = (s.tiles_m * s.tiles_n > 0) ? t_ck : 0;
+  s.t = s.t_ck + s.tiles_m * s.tiles_n;
   s.g = g;
   s.t_dp = (s.t == 0 || s.ipt == 0) ? s.t : dp_tiles(s.t, g, mode);
   s.sk_total = (int64_t)(s.t - s.t_dp) * s.ipt;
