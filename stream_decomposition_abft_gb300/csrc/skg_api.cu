@@ -141,8 +141,9 @@ Layout layout(int64_t m, int64_t n, int64_t k, const Resolved& r) {
   L.sums = L.enc_a = L.enc_b = L.stat = L.pub = L.cr = L.cc = off;
   if (r.abft) {
     const size_t tiles = (size_t)L.tiles_a + L.tiles_b;
+    const size_t groups = (size_t)((m + kBM - 1) / kBM + (n + kBM - 1) / kBM);
     L.sums = off;
-    off = round_up(off + tiles * L.kp * 4, 256);
+    off = round_up(off + groups * L.kp * 4, 256);
     L.enc_a = off;
     off = round_up(off + (size_t)kEncRows * L.tiles_a * L.kp * 2, 256);
     L.enc_b = off;

@@ -292,3 +292,25 @@ def test_raster_bands(band):
                                                raster_band=band))
         assert st == skgemm.OK
         check_full(p, C, ref)
+
+
+@pytest.mark.parametrize("shape", [(300, 300, 200), (1000, 1300, 520), (129, 257, 640),
+                                   (2000, 2100, 1000)])
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_abft_ragged_shapes_clean(shape, tile_n):
+    # Ragged m, n and k with the ABFT check on: no false positives, output
+    # within tolerance, every tile checked (encode groups of 128 rows, B tiles
+    # of tile_n columns with a short last tile).
+    m, n, k = shape
+    p = inputs.make_problem(m, n, k, seed=m + n, in_dtype="bf16", out_dtype="f32",
+                            law_a="normal", law_b="normal", alpha=0.5, beta=1.5)
+    opts = skgemm.opts_default(abft=1, tile_n=tile_n)
+    ws = None
+    for _ in range(2):   # the encode scratch must be left clean for the next call
+        C, ws, st = run(p, opts, ws=ws)
+        assert st == skgemm.OK
+        check_full(p, C)
+        rep = ws.report(reset=True)
+        assert rep.detected == 0 and rep.status_bits == 0
+        assert rep.tiles_checked == ((m + 127) // 128) * ((n + tile_n - 1) // tile_n)
+        assert rep.max_ratio_row < 0.1 and rep.max_ratio_col < 0.1
