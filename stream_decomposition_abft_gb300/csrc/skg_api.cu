@@ -128,11 +128,14 @@ struct Layout {
 Layout layout(int64_t m, int64_t n, int64_t k, const Resolved& r) {
   Layout L;
   size_t off = kHeaderBytes;
+  // With ABFT the fused checksum tiles form a second split region with
+  // flags and partial slots of its own.
+  const size_t regions = r.abft ? 2 : 1;
   L.flags = off;
-  off = round_up(off + (size_t)r.ws_grid * 4, 256);
+  off = round_up(off + regions * r.ws_grid * 4, 256);
   L.partials = off;
   const int slot_n = r.abft ? 256 : r.bn;
-  off = round_up(off + (size_t)r.ws_grid * kBM * slot_n * 4, 256);
+  off = round_up(off + regions * r.ws_grid * kBM * slot_n * 4, 256);
   L.kp = (int)round_up((size_t)(k > 0 ? k : 1), kBK);
   L.tiles_a = (int)((m + kBM - 1) / kBM);
   L.tiles_b = (int)((n + r.bn - 1) / r.bn);
@@ -232,9 +235,9 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
     if (make_map(&mp.b128, in_t, 2, g.B, (uint64_t)g.k, (uint64_t)g.n, (uint64_t)g.ldb, kBK,
                  kBM) != CUDA_SUCCESS ||
         make_map(&mp.be, in_t, 2, ws + L.enc_b, (uint64_t)L.kp, (uint64_t)n_cr, (uint64_t)L.kp,
-                 kBK, r.bn) != CUDA_SUCCESS ||
+                 kBK, (uint32_t)round_up(n_cr, 16)) != CUDA_SUCCESS ||
         make_map(&mp.ea, in_t, 2, ws + L.enc_a, (uint64_t)L.kp, (uint64_t)n_cc, (uint64_t)L.kp,
-                 kBK, r.bn) != CUDA_SUCCESS ||
+                 kBK, (uint32_t)round_up(n_cc, 16)) != CUDA_SUCCESS ||
         make_map(&mp.cr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws + L.cr, (uint64_t)n_cr,
                  (uint64_t)g.m, (uint64_t)L.ld_cr, 32, 32) != CUDA_SUCCESS ||
         make_map(&mp.cc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws + L.cc, (uint64_t)n_cc,
@@ -266,12 +269,15 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   p.ck_cr_tiles = ck_cr;
   p.ck_n_cr = kEncRows * L.tiles_b;
   p.ck_n_cc = kEncRows * L.tiles_a;
+  p.ck_rows_cr = (int)round_up(p.ck_n_cr, 16);
+  p.ck_rows_cc = (int)round_up(p.ck_n_cc, 16);
   p.idesc_cr = idesc_f16(g.in_dtype == SKG_IN_BF16, kBM, (uint32_t)round_up(p.ck_n_cr, 16));
   p.idesc_cc = idesc_f16(g.in_dtype == SKG_IN_BF16, kBM, (uint32_t)round_up(p.ck_n_cc, 16));
   p.hdr = (WsHeader*)ws;
   p.report = (skg_report_t*)(ws + 256);
   p.flags = (uint32_t*)(ws + L.flags);
   p.partials = (float*)(ws + L.partials);
+  p.ws_ctas = r.ws_grid;
   p.cr_all = (const float*)(ws + L.cr);
   p.cc_all = (const float*)(ws + L.cc);
   p.ld_cr = L.ld_cr;

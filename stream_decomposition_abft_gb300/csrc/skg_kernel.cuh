@@ -88,8 +88,12 @@ struct KernelParams {
   uint32_t idesc_main;
   WsHeader* hdr;
   skg_report_t* report;
+  // Fixup storage: region 0 (output tiles) uses flags[0, ws_ctas) and
+  // partial slots [0, ws_ctas); region 1 (fused checksum tiles) the next
+  // ws_ctas of each. Slot x holds kBM x BN fp32 values.
   uint32_t* flags;
   float* partials;
+  int ws_ctas;
   // ABFT reference checksums (hi and lo partial products, scaled):
   // row checksums cr_all[row * ld_cr + 2 * tn + t] = A (B e)_tn, and column
   // checksums ccT_all[col * ld_cc + 2 * tm + t] = ((e^T A)_tm B)^T.
@@ -104,6 +108,7 @@ struct KernelParams {
   // of ccT_all = B x [eA_hi; eA_lo]^T (ck_n_cc columns). Both store fp32.
   int ck_cr_tiles;
   int ck_n_cr, ck_n_cc;
+  int ck_rows_cr, ck_rows_cc;  // encoding rows loaded per k-step (N rounded up to 16)
   uint32_t idesc_cr, idesc_cc;
   float tau_row, tau_col;  // <= 0: derive from the encode pass maxima
   int inject_tile, inject_row, inject_col, inject_bit;
@@ -433,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a tile of one of the fused checksum GEMMs.
         const CUtensorMap* mapA = &tmA;
         const CUtensorMap* mapB = &tmB;
+        uint32_t tx = C::TX_BYTES;
         int rowA, rowB;
         if (w.tile >= s.t_ck) {
           int tm, tn;
@@ -440,14 +446,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           rowA = tm * kBM;
           rowB = tn * BN;
         } else if (w.tile < p.ck_cr_tiles) {
+          // Checksum tile: the encoding box holds only the rows the MMA uses.
           mapB = &tmBE;
           rowA = w.tile * kBM;
           rowB = 0;
+          tx = C::A_BYTES + p.ck_rows_cr * kBK * 2;
         } else {
           mapA = &tmB128;
           mapB = &tmEA;
           rowA = (w.tile - p.ck_cr_tiles) * kBM;
           rowB = 0;
+          tx = C::A_BYTES + p.ck_rows_cc * kBK * 2;
         }
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!wait_bar(&empty_bar[stage], phase ^ 1, aux, limit)) {
@@ -456,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* st = ring + stage * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
+          mbar_arrive_expect_tx(&full_bar[stage], tx);
           tma_load_2d(st, mapA, &full_bar[stage], kb * kBK, rowA);
           tma_load_2d(st + C::A_BYTES, mapB, &full_bar[stage], kb * kBK, rowB);
           pending |= 1u << stage;
@@ -543,7 +552,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       return reinterpret_cast<float*>(epi + ew_of_q * C::EPI_BUFS * C::EPI_BUF_BYTES);
     };
     const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr->epoch) + 1u;
-    float* my_slot = p.partials + (size_t)blockIdx.x * kBM * BN;
 
     Cursor cur;
     cur.init(s, blockIdx.x);
@@ -579,11 +587,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = tn * BN;
       const int out_tile = w.tile - s.t_ck;  // output-tile number the caller sees
       const bool inject_here = !is_ck && (out_tile == p.inject_tile) && (w.role != kRolePeer);
+      // This segment's region of fixup storage.
+      uint32_t* rflags = p.flags + (size_t)w.region * p.ws_ctas;
+      float* rpartials = p.partials + (size_t)w.region * p.ws_ctas * kBM * BN;
+      float* my_slot = rpartials + (size_t)blockIdx.x * kBM * BN;
+      // Columns of the accumulator that carry data: a checksum tile uses
+      // only its first ck_n_* columns.
+      const int live_chunks =
+          !is_ck ? BN / 32
+                 : ((w.tile < p.ck_cr_tiles ? p.ck_n_cr : p.ck_n_cc) + 31) / 32;
 
       if (w.role == kRolePeer) {
         // StorePartials + Signal (Algorithm 5, non-started segment).
 #pragma unroll 1
-        for (int c32 = 0; c32 < BN / 32; ++c32) {
+        for (int c32 = 0; c32 < live_chunks; ++c32) {
           uint32_t u[32];
           tmem_ld32(tacc + c32 * 32, u);
 #pragma unroll
@@ -597,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, kEpiThreads);
         if (et == 0 && (int)blockIdx.x != p.drop_signal) {
           __threadfence();
-          st_release_gpu(&p.flags[blockIdx.x], epoch);
+          st_release_gpu(&rflags[blockIdx.x], epoch);
         }
       } else {
         const bool owner = (w.role == kRoleOwner);
@@ -606,10 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool fine = true;
           if (et == 0) {
             for (int peer = blockIdx.x + 1; peer <= w.peer_last && fine; ++peer) {
-              if (ld_acquire_gpu(&p.flags[peer]) == epoch) continue;
+              if (ld_acquire_gpu(&rflags[peer]) == epoch) continue;
               const uint64_t t0 = globaltimer();
               uint32_t spins = 0;
-              while (ld_acquire_gpu(&p.flags[peer]) != epoch) {
+              while (ld_acquire_gpu(&rflags[peer]) != epoch) {
                 if (++spins > 64) nanosleep_ns(64);
                 if ((spins & 15) == 0 && globaltimer() - t0 > limit) {
                   record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
@@ -644,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tacc + c * 32, u);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
-            if (owner) add_peer_partials<BN>(v, p.partials, blockIdx.x + 1, w.peer_last, c, r);
+            if (owner) add_peer_partials<BN>(v, rpartials, blockIdx.x + 1, w.peer_last, c, r);
             if (c == nchunks - 1) {
               tc_fence_before();
               mbar_arrive(&tempty_bar[ab]);
@@ -718,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
-            if (owner) add_peer_partials<BN>(v, p.partials, blockIdx.x + 1, w.peer_last, c32, r);
+            if (owner) add_peer_partials<BN>(v, rpartials, blockIdx.x + 1, w.peer_last, c32, r);
             // Fault injection: one bit of one fp32 accumulator, after the
             // fixup and before the check (warp-uniform chunk selection).
             const bool inj_chunk = inject_here && (p.inject_row >> 5) == q &&
@@ -902,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
             if (!C::ABFT && owner)
-              add_peer_partials<BN>(v, p.partials, blockIdx.x + 1, w.peer_last, c32, r);
+              add_peer_partials<BN>(v, rpartials, blockIdx.x + 1, w.peer_last, c32, r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) y[hh * 32 + i] = v[i];
             if (!C::ABFT) {

@@ -35,7 +35,26 @@ struct CostModel {
 constexpr CostModel kModel128 = {2.64, 0.334, 0.17, 4.67, 1.03};
 constexpr CostModel kModel256 = {3.47, 0.364, 0.00, 8.18, 1.73};
 
+// Segment counts of CTA x in an evenly split region of `total` iterations.
+inline void region_counts(int64_t q, int r, int64_t total, int64_t I, int x, int64_t& iters,
+                          int64_t& tiles, int64_t& partial, int64_t& peers) {
+  if (total <= 0) return;
+  int64_t b, e;
+  even_range(q, r, x, b, e);
+  if (e <= b) return;
+  iters += e - b;
+  if (b % I != 0) partial += 1;
+  const int64_t first = (b % I == 0) ? b : (b / I + 1) * I;
+  if (first < e) {
+    const int64_t started = (e - 1 - first) / I + 1;
+    tiles += started;
+    const int64_t last = first + (started - 1) * I;
+    if (last + I > e) peers += even_cta_of(q, r, last + I - 1) - x;
+  }
+}
+
 // Predicted time (us) of one launch with schedule s: max over CTAs. O(g).
+// Side-tile iterations (fused checksum GEMMs) are costed like output ones.
 inline double predict_us(const Schedule& s, const CostModel& M) {
   if (s.t == 0 || s.ipt == 0) return 0.0;
   const int64_t I = s.ipt;
@@ -47,21 +66,8 @@ inline double predict_us(const Schedule& s, const CostModel& M) {
       iters += nd * I;
       tiles += nd;
     }
-    if (s.sk_total > 0) {
-      int64_t b, e;
-      sk_range(s, x, b, e);
-      if (e > b) {
-        iters += e - b;
-        if (b % I != 0) partial = 1;
-        const int64_t first = (b % I == 0) ? b : (b / I + 1) * I;
-        if (first < e) {
-          const int64_t started = (e - 1 - first) / I + 1;
-          tiles += started;
-          const int64_t last = first + (started - 1) * I;
-          if (last + I > e) peers += sk_cta_of(s, last + I - 1) - x;
-        }
-      }
-    }
+    region_counts(s.sk_q, s.sk_r, s.sk_total, I, x, iters, tiles, partial, peers);
+    region_counts(s.ck_q, s.ck_r, s.ck_total, I, x, iters, tiles, partial, peers);
     const double tx = M.a + M.c * (double)iters + M.e * (double)tiles + M.b * (double)partial +
                       M.d * (double)peers;
     if (tx > worst) worst = tx;

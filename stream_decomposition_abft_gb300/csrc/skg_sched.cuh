@@ -11,7 +11,7 @@
 //   - §5.2: "DP + one-tile SK" keeps w = floor(t/g) full DP waves; "two-tile
 //     SK + DP" gives one of them up when w >= 2 so every Stream-K CTA holds
 //     between one and two tiles of iterations. DP tiles are the first t_dp
-//     tile indices, walked x, x+g, ...; the Stream-K region is the rest.
+//     output tiles, walked x, x+g, ...; the Stream-K region is the rest.
 //   - Algorithm 3 (tile coordinates): the page numbers tiles row-major,
 //     tile = tm * tiles_n + tn. Its conclusion names cache-aware tile orders
 //     as future work; here tile indices are walked in bands of `band` tile
@@ -42,11 +42,14 @@ struct Schedule {
   int ipt;            // MAC iterations per tile, ceil(k / BLK_K)
   int t;              // tiles (t_ck + tiles_m * tiles_n)
   int t_ck;           // leading tiles of fused side GEMMs (0 for a plain GEMM)
-  int t_dp;           // data-parallel tiles [0, t_dp)
+  int t_dp;           // data-parallel output tiles [t_ck, t_ck + t_dp)
   int g;              // persistent CTAs
-  int64_t sk_total;   // Stream-K iterations (t - t_dp) * ipt
+  int64_t sk_total;   // Stream-K iterations of the output tiles after the DP ones
   int64_t sk_q;       // floor(sk_total / g)
   int sk_r;           // sk_total mod g
+  int64_t ck_total;   // iterations of the side tiles, t_ck * ipt
+  int64_t ck_q;       // floor(ck_total / g)
+  int ck_r;           // ck_total mod g
   int band;           // tile columns per raster band (tiles_n = row-major)
 };
 
@@ -72,85 +75,116 @@ SKG_HD int dp_tiles(int t, int g, int mode) {
   return w * g;  // DP + one-tile SK, and the two-tile hybrid when w < 2
 }
 
-// `t_ck` extra full-k tiles are placed in front of the output tiles (the
-// fused ABFT checksum GEMMs); the schedule treats every tile alike.
+// The page's schedule over the output tiles (DP tiles first, then the
+// Stream-K region), preceded by `t_ck` full-k side tiles (the fused ABFT
+// checksum GEMMs). The side tiles form a region of their own whose
+// iterations are split evenly over all g CTAs, so every CTA starts with the
+// same small share of side work, whatever the schedule of the output tiles.
 SKG_HD Schedule make_schedule(int64_t m, int64_t n, int64_t k, int bm, int bn, int bk, int g,
                               int mode, int t_ck = 0) {
   Schedule s;
   s.tiles_m = (int)((m + bm - 1) / bm);
   s.tiles_n = (int)((n + bn - 1) / bn);
   s.ipt = (int)((k + bk - 1) / bk);
-  s.t_ck = (s.tiles_m * s.tiles_n > 0) ? t_ck : 0;
-  s.t = s.t_ck + s.tiles_m * s.tiles_n;
+  const int t_out = s.tiles_m * s.tiles_n;
+  s.t_ck = t_out > 0 ? t_ck : 0;
+  s.t = s.t_ck + t_out;
   s.g = g;
-  s.t_dp = (s.t == 0 || s.ipt == 0) ? s.t : dp_tiles(s.t, g, mode);
-  s.sk_total = (int64_t)(s.t - s.t_dp) * s.ipt;
+  s.t_dp = (t_out == 0 || s.ipt == 0) ? t_out : dp_tiles(t_out, g, mode);
+  s.sk_total = (int64_t)(t_out - s.t_dp) * s.ipt;
   s.sk_q = s.sk_total / g;
   s.sk_r = (int)(s.sk_total % g);
+  s.ck_total = (int64_t)s.t_ck * s.ipt;
+  s.ck_q = s.ck_total / g;
+  s.ck_r = (int)(s.ck_total % g);
   s.band = s.tiles_n > 0 ? s.tiles_n : 1;
   return s;
 }
 
+// [begin, end) of CTA x in an iteration space split evenly over the CTAs
+// (q, r) = divmod(total, g).
+SKG_HD void even_range(int64_t q, int r, int x, int64_t& begin, int64_t& end) {
+  begin = (int64_t)x * q + (x < r ? x : r);
+  end = begin + q + (x < r ? 1 : 0);
+}
+
+// CTA whose range holds iteration `it` of such a split.
+SKG_HD int even_cta_of(int64_t q, int r, int64_t it) {
+  const int64_t big = (int64_t)r * (q + 1);
+  if (it < big) return (int)(it / (q + 1));
+  return r + (int)((it - big) / q);
+}
+
 // [begin, end) of CTA x in the Stream-K iteration space (even split).
 SKG_HD void sk_range(const Schedule& s, int x, int64_t& begin, int64_t& end) {
-  begin = (int64_t)x * s.sk_q + (x < s.sk_r ? x : s.sk_r);
-  end = begin + s.sk_q + (x < s.sk_r ? 1 : 0);
+  even_range(s.sk_q, s.sk_r, x, begin, end);
 }
 
 // CTA whose Stream-K range holds iteration `it` (0 <= it < sk_total).
-SKG_HD int sk_cta_of(const Schedule& s, int64_t it) {
-  const int64_t big = (int64_t)s.sk_r * (s.sk_q + 1);
-  if (it < big) return (int)(it / (s.sk_q + 1));
-  return s.sk_r + (int)((it - big) / s.sk_q);
-}
+SKG_HD int sk_cta_of(const Schedule& s, int64_t it) { return even_cta_of(s.sk_q, s.sk_r, it); }
 
 struct Work {
   int tile;
   int kb_begin, kb_end;  // MAC iterations within the tile
   int role;
   int peer_last;         // OWNER: last peer CTA (peers are cta+1 .. peer_last)
+  int region;            // 0: output tiles, 1: side tiles (own partial slots and flags)
 };
 
-// Walks one CTA's segments in execution order: DP tiles, then its
-// Stream-K range cut at tile boundaries.
+// Walks one CTA's segments in execution order: its share of the side
+// tiles, its DP tiles, then its Stream-K range; the split regions are cut
+// at tile boundaries.
 struct Cursor {
   int x;
   int next_dp;
+  int64_t ck_it, ck_end;
   int64_t it, it_end;
 
   SKG_HD void init(const Schedule& s, int cta) {
     x = cta;
     next_dp = cta;
-    if (s.sk_total > 0) {
-      sk_range(s, cta, it, it_end);
-    } else {
-      it = it_end = 0;
-    }
+    it = it_end = ck_it = ck_end = 0;
+    if (s.sk_total > 0) sk_range(s, cta, it, it_end);
+    if (s.ck_total > 0) even_range(s.ck_q, s.ck_r, cta, ck_it, ck_end);
+  }
+
+  // Next segment of a split region whose tiles start at `base`.
+  SKG_HD static void cut(const Schedule& s, int64_t q, int r, int base, int region, int x,
+                         int64_t& pos, int64_t end, Work& w) {
+    const int64_t tile_rel = pos / s.ipt;
+    const int64_t tile_iter = tile_rel * s.ipt;
+    const int64_t tile_iter_end = tile_iter + s.ipt;
+    const bool started = (pos == tile_iter);
+    const bool ended = (end >= tile_iter_end);
+    w.tile = (int)(tile_rel + base);
+    w.kb_begin = (int)(pos - tile_iter);
+    w.kb_end = (int)((end < tile_iter_end ? end : tile_iter_end) - tile_iter);
+    w.role = !started ? kRolePeer : (ended ? kRoleFull : kRoleOwner);
+    w.peer_last = (w.role == kRoleOwner) ? even_cta_of(q, r, tile_iter_end - 1) : x;
+    w.region = region;
+    pos = tile_iter_end;
   }
 
   SKG_HD bool next(const Schedule& s, Work& w) {
+    if (ck_it < ck_end) {
+      cut(s, s.ck_q, s.ck_r, 0, 1, x, ck_it, ck_end, w);
+      return true;
+    }
     if (next_dp < s.t_dp) {
-      w.tile = next_dp;
+      w.tile = s.t_ck + next_dp;
       w.kb_begin = 0;
       w.kb_end = s.ipt;
       w.role = kRoleFull;
       w.peer_last = x;
+      w.region = 0;
       next_dp += s.g;
       return true;
     }
-    if (it >= it_end) return false;
-    const int64_t tile_sk = it / s.ipt;
-    const int64_t tile_iter = tile_sk * s.ipt;
-    const int64_t tile_iter_end = tile_iter + s.ipt;
-    const bool started = (it == tile_iter);
-    const bool ended = (it_end >= tile_iter_end);
-    w.tile = (int)(tile_sk + s.t_dp);
-    w.kb_begin = (int)(it - tile_iter);
-    w.kb_end = (int)((it_end < tile_iter_end ? it_end : tile_iter_end) - tile_iter);
-    w.role = !started ? kRolePeer : (ended ? kRoleFull : kRoleOwner);
-    w.peer_last = (w.role == kRoleOwner) ? sk_cta_of(s, tile_iter_end - 1) : x;
-    it = tile_iter_end;
-    return true;
+    if (it < it_end) {
+      cut(s, s.sk_q, s.sk_r, s.t_ck + s.t_dp, 0, x, it, it_end, w);
+      return true;
+    }
+    return false;
   }
 };
 
