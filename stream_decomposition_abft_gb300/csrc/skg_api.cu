@@ -120,7 +120,7 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
 // Workspace layout. Partial-tile slots are sized for the widest tile any
 // launch of the call uses (the ABFT checksum GEMMs may use BLK_N = 256).
 struct Layout {
-  size_t flags, partials, sums, enc_a, enc_b, stat, pub, cr, cc, total;
+  size_t flags, partials, sums, enc_a, enc_b, stat, pub, umax, cr, cc, total;
   int kp, tiles_a, tiles_b;
   int64_t ld_cr, ld_cc;
 };
@@ -141,7 +141,7 @@ Layout layout(int64_t m, int64_t n, int64_t k, const Resolved& r) {
   L.tiles_b = (int)((n + r.bn - 1) / r.bn);
   L.ld_cr = (int64_t)round_up((size_t)kEncRows * L.tiles_b, 4);
   L.ld_cc = (int64_t)round_up((size_t)kEncRows * L.tiles_a, 4);
-  L.sums = L.enc_a = L.enc_b = L.stat = L.pub = L.cr = L.cc = off;
+  L.sums = L.enc_a = L.enc_b = L.stat = L.pub = L.umax = L.cr = L.cc = off;
   if (r.abft) {
     const size_t tiles = (size_t)L.tiles_a + L.tiles_b;
     const size_t groups = (size_t)((m + kBM - 1) / kBM + (n + kBM - 1) / kBM);
@@ -155,6 +155,8 @@ Layout layout(int64_t m, int64_t n, int64_t k, const Resolved& r) {
     off = round_up(off + tiles * sizeof(TileStat), 256);
     L.pub = off;
     off = round_up(off + tiles * sizeof(TilePub), 256);
+    L.umax = off;
+    off = round_up(off + tiles * (size_t)encode_slices(L.kp) * 4, 256);
     L.cr = off;
     off = round_up(off + (size_t)m * L.ld_cr * 4, 256);
     L.cc = off;
@@ -168,15 +170,36 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 CUresult make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base,
                   uint64_t inner, uint64_t outer, uint64_t row_stride_elems, uint32_t box_inner,
-                  uint32_t box_outer) {
+                  uint32_t box_outer, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_stride_elems * (uint64_t)elem_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   return tensor_map_encoder()(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// The ABFT encode pass over A (m x k) and the stored B (n x k).
+skg_status_t run_encode(int32_t in_dtype, const void* A, int64_t lda, int64_t m, const void* B,
+                        int64_t ldb, int64_t n, int64_t k, const Resolved& r, uint8_t* ws,
+                        const Layout& L, int sms, cudaStream_t stream) {
+  const CUtensorMapDataType in_t = in_dtype == SKG_IN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap ma, mb;
+  if (make_map(&ma, in_t, 2, A, (uint64_t)k, (uint64_t)m, (uint64_t)lda, kEncBoxCols, kEncBoxRows,
+               CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS ||
+      make_map(&mb, in_t, 2, B, (uint64_t)k, (uint64_t)n, (uint64_t)ldb, kEncBoxCols, kEncBoxRows,
+               CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+    return SKG_ERR_UNSUPPORTED;
+  return launch_encode(in_dtype == SKG_IN_BF16, ma, mb, (int)m, (int)n, L.kp, r.bn, sms,
+                       (float*)(ws + L.sums), ws + L.enc_a, ws + L.enc_b, (TileStat*)(ws + L.stat),
+                       (TilePub*)(ws + L.pub), (float*)(ws + L.umax), (skg_report_t*)(ws + 256),
+                       r.timeout_ns,
+                       stream) == cudaSuccess
+             ? SKG_OK
+             : SKG_ERR_CUDA;
 }
 
 // One launch of the persistent kernel: C = alpha A B^T + beta C with A
@@ -284,6 +307,9 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   p.ld_cc = L.ld_cc;
   p.pub_a = (const TilePub*)(ws + L.pub);
   p.pub_b = (const TilePub*)(ws + L.pub) + L.tiles_a;
+  p.umax = (const float*)(ws + L.umax);
+  p.enc_slices = encode_slices(L.kp);
+  p.enc_tiles_a = L.tiles_a;
   p.tau_row = r.tau_row;
   p.tau_col = r.tau_col;
   p.inject_tile = r.inject_tile;
@@ -314,11 +340,11 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
 //   ccT_all (n x 2 tiles_a) = B x [eA_hi; eA_lo]^T     (= ((e^T A) B)^T)
 skg_status_t reference_checksums(const Gemm& g, const Resolved& r, uint8_t* ws, const Layout& L,
                                  cudaStream_t stream, bool skip_encode) {
-  if (!skip_encode &&
-      launch_encode(g.in_dtype == SKG_IN_BF16, g.A, g.lda, (int)g.m, g.B, g.ldb, (int)g.n,
-                    (int)g.k, L.kp, r.bn, (float*)(ws + L.sums), ws + L.enc_a, ws + L.enc_b,
-                    (TileStat*)(ws + L.stat), (TilePub*)(ws + L.pub), stream) != cudaSuccess)
-    return SKG_ERR_CUDA;
+  if (!skip_encode) {
+    const skg_status_t st = run_encode(g.in_dtype, g.A, g.lda, g.m, g.B, g.ldb, g.n, g.k, r, ws,
+                                       L, sm_count_cached(), stream);
+    if (st != SKG_OK) return st;
+  }
   Resolved rc = r;
   rc.abft = 0;
   rc.inject_tile = -1;
@@ -419,11 +445,10 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
     // launch, after the encode pass (skipped when pre-encoded).
     fuse = true;
     replan_fused(m, n, opts, r);
-    if (!r.preencoded &&
-        launch_encode(in_dtype == SKG_IN_BF16, A, lda, (int)m, B, ldb, (int)n, (int)k, L.kp, r.bn,
-                      (float*)(ws + L.sums), ws + L.enc_a, ws + L.enc_b, (TileStat*)(ws + L.stat),
-                      (TilePub*)(ws + L.pub), stream) != cudaSuccess)
-      return SKG_ERR_CUDA;
+    if (!r.preencoded) {
+      st = run_encode(in_dtype, A, lda, m, B, ldb, n, k, r, ws, L, sms, stream);
+      if (st != SKG_OK) return st;
+    }
   } else if (r.abft) {
     st = reference_checksums(g, r, ws, L, stream, r.preencoded != 0);
     if (st != SKG_OK) return st;
@@ -496,11 +521,7 @@ skg_status_t skg_abft_encode(int64_t m, int64_t n, int64_t k, const void* A, int
   if (!workspace || !aligned16(workspace) || ws_bytes < L.total) return SKG_ERR_WORKSPACE;
   if (!tensor_map_encoder()) return SKG_ERR_CUDA;
   uint8_t* ws = (uint8_t*)workspace;
-  return launch_encode(in_dtype == SKG_IN_BF16, A, lda, (int)m, B, ldb, (int)n, (int)k, L.kp, r.bn,
-                       (float*)(ws + L.sums), ws + L.enc_a, ws + L.enc_b, (TileStat*)(ws + L.stat),
-                       (TilePub*)(ws + L.pub), (cudaStream_t)stream) == cudaSuccess
-             ? SKG_OK
-             : SKG_ERR_CUDA;
+  return run_encode(in_dtype, A, lda, m, B, ldb, n, k, r, ws, L, sms, (cudaStream_t)stream);
 }
 
 skg_status_t skg_schedule_query(int64_t m, int64_t n, int64_t k, int32_t bm, int32_t bn,

@@ -11,18 +11,31 @@
 // The checksum GEMMs run on the tensor cores, which take both operands of an
 // MMA in the same 16-bit type, so each fp32 encoding x is stored as two
 // input-precision terms hi = rn(x s), lo = rn(x s - hi), scaled by a power
-// of two s per tile, chosen from that tile's largest |x| so fp16 cannot
-// overflow. The residual is below 2^-15 |x| relative for bf16 and 2^-21 for
-// fp16.
+// of two s per tile. For fp16, s is chosen from the tile's largest |x| so
+// the terms cannot overflow; bf16 needs no scale (s = 1). The residual is
+// below 2^-15 |x| relative for bf16 and 2^-21 for fp16.
 //
-// One kernel does it all: block (slice, group) sums 256 k-columns over a
-// group of 128 rows; the last block of each operand tile to finish
-// (per-tile counter) combines the tile's groups, picks the tile's scale,
-// writes its hi / lo rows, publishes the tile's max |element| (for the
-// default threshold) and scale, and resets the counter and maximum for the
-// next launch.
+// One persistent kernel, one CTA per SM. The work units are (operand tile,
+// slice of 128 k-columns): 128 rows of A, or the BLK_N stored rows of B, in
+// boxes of 128 rows x 128 columns. Warp 0 streams the boxes into a ring of
+// shared-memory stages with TMA (zero fill past m, n and k); warps 1-8 sum
+// each box's columns out of shared memory, so a unit's column sums are final
+// when its last box is in.
+//   - bf16 has the exponent range of fp32: the unit writes its hi / lo terms
+//     directly and the tile's scale is 2^0. No CTA waits for another.
+//   - fp16: the unit stores its fp32 sums and folds its largest |sum| into
+//     the tile's; the last unit of the tile to finish (per-tile counter)
+//     picks the tile's scale, converts the tile's sums to hi / lo terms and
+//     resets the tile's scratch for the next launch.
+// Every unit also stores its largest |element|; the main kernel's epilogue
+// takes a tile's maximum (for the default threshold) over its units. Every
+// wait is bounded; on expiry the kernel records a pipeline timeout in the
+// workspace report, waits for its own copies in flight and returns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <atomic>
+#include <type_traits>
 
 #include "skg_internal.h"
 
@@ -46,195 +59,384 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
 
-#ifndef SKG_ENC_WARPS
-#define SKG_ENC_WARPS 16
-#endif
-constexpr int kEncWarps = SKG_ENC_WARPS;
-constexpr int kEncThreads = 32 * kEncWarps;  // a block covers 256 k-columns of one row group
-constexpr int kEncCols = 8;                   // k-columns per lane (one 16-byte load)
-constexpr int kEncRowsPerGroup = 128;         // rows of A or of the stored B per block
-constexpr int kEncUnroll = kEncRowsPerGroup / kEncWarps;  // loads in flight per thread
+constexpr int kEncSliceCols = kEncBoxCols;  // k-columns per unit
+constexpr int kEncStageBytes = kEncSliceCols * kEncBoxRows * 2;
+static_assert(kBM % kEncBoxRows == 0 && 128 % kEncBoxRows == 0, "box rows divide every tile");
+static_assert(kEncSliceCols == 128 || kEncSliceCols == 256, "a box row is 16 or 32 lanes");
+constexpr int kEncWorkers = 16;     // consumer warps
+constexpr int kEncWorkerThreads = 32 * kEncWorkers;
+constexpr int kEncPartBytes = kEncWorkers * kEncSliceCols * 4;
+constexpr int kEncStagesFit = (int)((kSmemLimit - 1024 - kEncPartBytes - 256) / kEncStageBytes);
+constexpr int kEncStages = kEncStagesFit > 8 ? 8 : kEncStagesFit;
+static_assert(kEncStages >= 2, "encode ring");
+constexpr int kEncThreads = 32 + kEncWorkerThreads;
+constexpr int kEncColsPerThread = 8;  // one 16-byte shared-memory load
+constexpr int kEncLanesPerRow = kEncSliceCols / kEncColsPerThread;
+constexpr int kEncRowsPerPass = kEncWorkerThreads / kEncLanesPerRow;
+static_assert(kEncBoxRows % kEncRowsPerPass == 0, "whole passes per box");
+constexpr size_t kEncSmem = 1024 + (size_t)kEncStages * kEncStageBytes + kEncPartBytes + 256;
 
-int encode_slices(int kp) { return (kp + 32 * kEncCols - 1) / (32 * kEncCols); }
+int encode_slices(int kp) { return (kp + kEncSliceCols - 1) / kEncSliceCols; }
 
-// Block (slice, group): column sums of 256 k-columns over one group of 128
-// rows (A groups first, then groups of the stored B; a B tile of BLK_N
-// columns is BLK_N / 128 groups). The last block of each operand tile to
-// finish adds its groups' sums, finds the tile's largest |sum|, picks the
-// tile's scale, writes the hi / lo rows, publishes the tile's max |element|
-// and scale, and resets the tile's scratch for the next launch.
-template <typename T>
-__global__ void __launch_bounds__(kEncThreads) encode_kernel(
-    const T* __restrict__ A, int64_t lda, int m, const T* __restrict__ B, int64_t ldb, int n,
-    int k, int kp, int bn, int tiles_a, float* __restrict__ sums, T* __restrict__ enc_a,
-    T* __restrict__ enc_b, TileStat* __restrict__ stat, TilePub* __restrict__ pub) {
-  __shared__ float part[kEncWarps][32 * kEncCols];
-  __shared__ float wred[kEncWarps];
-  __shared__ int last_block;
-  griddep_wait();
-  if (threadIdx.x == 0) griddep_launch_dependents();
-  const int groups_a = (m + kEncRowsPerGroup - 1) / kEncRowsPerGroup;
-  const int gpt_b = bn / kEncRowsPerGroup;  // groups per B tile
-  const int grp = blockIdx.y;
-  const int z = grp < groups_a ? 0 : 1;
-  const int zgrp = z == 0 ? grp : grp - groups_a;        // group within the operand
-  const int tile = z == 0 ? zgrp : zgrp / gpt_b;          // operand tile
-  const int t = z == 0 ? tile : tiles_a + tile;            // stat / pub index
-  const T* X = z == 0 ? A : B;
-  const int64_t ld = z == 0 ? lda : ldb;
-  const int rows = z == 0 ? m : n;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int col0 = blockIdx.x * 32 * kEncCols + lane * kEncCols;
-  const int r0 = zgrp * kEncRowsPerGroup;
-  const int r1 = min(rows, r0 + kEncRowsPerGroup);
-  float acc[kEncCols];
-#pragma unroll
-  for (int i = 0; i < kEncCols; ++i) acc[i] = 0.f;
-  float amax = 0.f;
-  if (col0 < k) {
-    if (col0 + kEncCols <= k) {
-      uint4 v[kEncUnroll];
-#pragma unroll
-      for (int u = 0; u < kEncUnroll; ++u) {
-        const int r = r0 + warp + kEncWarps * u;
-        v[u] = r < r1 ? __ldg(reinterpret_cast<const uint4*>(X + (int64_t)r * ld + col0))
-                      : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < kEncUnroll; ++u) {
-        const T* e = reinterpret_cast<const T*>(&v[u]);
-#pragma unroll
-        for (int i = 0; i < kEncCols; ++i) {
-          const float f = to_f<T>(e[i]);
-          acc[i] += f;
-          amax = fmaxf(amax, fabsf(f));
-        }
-      }
-    } else {
-      for (int r = r0 + warp; r < r1; r += kEncWarps) {
-        const T* row = X + (int64_t)r * ld + col0;
-        for (int i = 0; i < kEncCols; ++i)
-          if (col0 + i < k) {
-            const float f = to_f<T>(row[i]);
-            acc[i] += f;
-            amax = fmaxf(amax, fabsf(f));
-          }
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < kEncCols; ++i) part[warp][lane * kEncCols + i] = acc[i];
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1)
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  if (lane == 0) wred[warp] = amax;
-  __syncthreads();
-  // Threads 0..255 finish one column each of the slice.
-  float* gsums = sums + (int64_t)grp * kp;
-  if (threadIdx.x < 32 * kEncCols) {
-    const int c = threadIdx.x;
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < kEncWarps; ++w) s += part[w][c];
-    const int col = blockIdx.x * 32 * kEncCols + c;
-    if (col < kp) __stcg(gsums + col, s);
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float mx = wred[0];
-    for (int w = 1; w < kEncWarps; ++w) mx = fmaxf(mx, wred[w]);
-    // Non-negative floats order like their bit patterns.
-    atomicMax(&stat[t].absmax_bits, __float_as_uint(mx));
-    __threadfence();
-    // Blocks of this tile: every slice of each of its row groups (the last
-    // B tile of a ragged n may have fewer than BLK_N / 128 groups).
-    const int groups_b = (n + kEncRowsPerGroup - 1) / kEncRowsPerGroup;
-    const uint32_t tile_groups = z == 0 ? 1u : (uint32_t)min(gpt_b, groups_b - tile * gpt_b);
-    last_block = (atomicAdd(&stat[t].count, 1u) == gridDim.x * tile_groups - 1) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!last_block) return;
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
-  // Last block of this tile: every group's sums and maxima are in.
-  __threadfence();
-  const int g_first = z == 0 ? grp : groups_a + tile * gpt_b;
-  const int g_count =
-      z == 0 ? 1 : min(gpt_b, (n + kEncRowsPerGroup - 1) / kEncRowsPerGroup - tile * gpt_b);
-  // Both passes read the tile's sums as float4 (kp is a multiple of 64),
-  // four independent loads per thread in flight.
-  const float4* tsums4 = reinterpret_cast<const float4*>(sums + (int64_t)g_first * kp);
-  const int kp4 = kp / 4;
-  auto load_sum4 = [&](int i4) {
-    float4 x = __ldcg(tsums4 + i4);
-    for (int gg = 1; gg < g_count; ++gg) {
-      const float4 y = __ldcg(tsums4 + (int64_t)gg * kp4 + i4);
-      x.x += y.x;
-      x.y += y.y;
-      x.z += y.z;
-      x.w += y.w;
+// Named barrier 1 over the consumer warps (512 threads) that also ANDs a
+// predicate.
+__device__ __forceinline__ bool workers_all(bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, 1, 512, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)v)
+      : "memory");
+  return out != 0;
+}
+
+__device__ __forceinline__ bool enc_wait(uint64_t* bar, uint32_t parity, const int* abort_flag,
+                                         uint64_t limit_ns, bool honor_abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31) == 0) {
+      if (honor_abort && *(volatile const int*)abort_flag) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
     }
-    return x;
-  };
-  float emax = 0.f;
-#pragma unroll 4
-  for (int i4 = threadIdx.x; i4 < kp4; i4 += kEncThreads) {
-    const float4 x = load_sum4(i4);
-    emax = fmaxf(emax, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
-  }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1)
-    emax = fmaxf(emax, __shfl_xor_sync(0xffffffffu, emax, off));
-  if (lane == 0) wred[warp] = emax;
-  __syncthreads();
-  emax = wred[0];
-  for (int w = 1; w < kEncWarps; ++w) emax = fmaxf(emax, wred[w]);
-  int ex = 0;
-  if (emax > 0.f) frexpf(emax, &ex);
-  const int e = (emax > 0.f) ? 15 - ex : 0;  // emax * 2^e in [2^14, 2^15)
-  T* enc = z == 0 ? enc_a : enc_b;
-  T* hi_row = enc + (int64_t)(kEncRows * tile) * kp;
-  T* lo_row = hi_row + kp;
-#pragma unroll 4
-  for (int i4 = threadIdx.x; i4 < kp4; i4 += kEncThreads) {
-    const float4 x = load_sum4(i4);
-    const float xs[4] = {ldexpf(x.x, e), ldexpf(x.y, e), ldexpf(x.z, e), ldexpf(x.w, e)};
-    T hi[4], lo[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      hi[j] = from_f<T>(xs[j]);
-      lo[j] = from_f<T>(xs[j] - to_f<T>(hi[j]));
-    }
-    *reinterpret_cast<uint2*>(hi_row + 4 * i4) = *reinterpret_cast<const uint2*>(hi);
-    *reinterpret_cast<uint2*>(lo_row + 4 * i4) = *reinterpret_cast<const uint2*>(lo);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    pub[t].maxabs = __uint_as_float(atomicAdd(&stat[t].absmax_bits, 0u));
-    pub[t].scale_exp = e;
-    stat[t].absmax_bits = 0;
-    stat[t].encmax_bits = 0;
-    stat[t].count = 0;
   }
 }
 
-cudaError_t launch_encode(int in_bf16, const void* A, int64_t lda, int m, const void* B,
-                          int64_t ldb, int n, int k, int kp, int bn, float* sums, void* enc_a,
-                          void* enc_b, TileStat* stat, TilePub* pub, cudaStream_t stream) {
-  const int tiles_a = (m + kBM - 1) / kBM;
-  const int groups = (m + kEncRowsPerGroup - 1) / kEncRowsPerGroup +
-                     (n + kEncRowsPerGroup - 1) / kEncRowsPerGroup;
-  const dim3 grid(encode_slices(kp), groups);
-  if (in_bf16) {
-    using T = __nv_bfloat16;
-    return launch_pdl(encode_kernel<T>, grid, dim3(kEncThreads), 0, stream, (const T*)A, lda, m,
-                      (const T*)B, ldb, n, k, kp, bn, tiles_a, sums, (T*)enc_a, (T*)enc_b, stat,
-                      pub);
+// Packed pairs of the input type.
+template <typename T>
+struct Pair;
+template <>
+struct Pair<__half> {
+  using type = __half2;
+};
+template <>
+struct Pair<__nv_bfloat16> {
+  using type = __nv_bfloat162;
+};
+template <typename T2>
+__device__ __forceinline__ T2 as_pair(uint32_t w) {
+  return *reinterpret_cast<const T2*>(&w);
+}
+template <typename T2>
+__device__ __forceinline__ T2 zero2() {
+  return as_pair<T2>(0u);
+}
+__device__ __forceinline__ __half lo_of(__half2 v) { return __low2half(v); }
+__device__ __forceinline__ __half hi_of(__half2 v) { return __high2half(v); }
+__device__ __forceinline__ __nv_bfloat16 lo_of(__nv_bfloat162 v) { return __low2bfloat16(v); }
+__device__ __forceinline__ __nv_bfloat16 hi_of(__nv_bfloat162 v) { return __high2bfloat16(v); }
+__device__ __forceinline__ __half2 pair_max(__half2 a, __half2 b) { return __hmax2(a, b); }
+__device__ __forceinline__ __nv_bfloat162 pair_max(__nv_bfloat162 a, __nv_bfloat162 b) {
+  return __hmax2(a, b);
+}
+
+template <typename T>
+__device__ __forceinline__ void split_store(T* hi_row, T* lo_row, int col,
+                                            const float (&x)[kEncColsPerThread], int e) {
+  T hi[kEncColsPerThread], lo[kEncColsPerThread];
+#pragma unroll
+  for (int j = 0; j < kEncColsPerThread; ++j) {
+    const float xs = ldexpf(x[j], e);
+    hi[j] = from_f<T>(xs);
+    lo[j] = from_f<T>(xs - to_f<T>(hi[j]));
   }
-  using T = __half;
-  return launch_pdl(encode_kernel<T>, grid, dim3(kEncThreads), 0, stream, (const T*)A, lda, m,
-                    (const T*)B, ldb, n, k, kp, bn, tiles_a, sums, (T*)enc_a, (T*)enc_b, stat,
-                    pub);
+  *reinterpret_cast<uint4*>(hi_row + col) = *reinterpret_cast<const uint4*>(hi);
+  *reinterpret_cast<uint4*>(lo_row + col) = *reinterpret_cast<const uint4*>(lo);
+}
+
+struct EncParams {
+  int kp, bn, tiles_a, tiles_b, slices;
+  float* sums;
+  void* enc_a;
+  void* enc_b;
+  TileStat* stat;
+  TilePub* pub;
+  float* umax;
+  skg_report_t* report;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void enc_error(const EncParams& p, int* abort_flag) {
+  atomicOr(&p.report->status_bits, 1u << SKG_ERR_PIPELINE_TIMEOUT);
+  atomicAdd(&p.report->timeouts, 1u);
+  atomicExch(abort_flag, 1);
+}
+
+// Unit u: tile t = u / slices (A tiles first, then B tiles), slice u % slices.
+// The even split of the units over the CTAs gives each a contiguous range.
+template <typename T>
+__global__ void __launch_bounds__(kEncThreads, 1)
+    encode_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const EncParams p) {
+  constexpr bool kScaled = std::is_same<T, __half>::value;
+  using T2 = typename Pair<T>::type;
+  extern __shared__ uint8_t dsmem[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) &
+                                             ~uintptr_t(1023));
+  float* part = reinterpret_cast<float*>(ring + kEncStages * kEncStageBytes);  // [workers][cols]
+  uint64_t* full = reinterpret_cast<uint64_t*>(part + kEncWorkers * kEncSliceCols);
+  uint64_t* empty = full + kEncStages;
+  int* abort_flag = reinterpret_cast<int*>(empty + kEncStages);
+  int* last_unit = abort_flag + 1;
+  float* wmax = reinterpret_cast<float*>(abort_flag + 2);  // [workers]
+  float* wsmax = wmax + kEncWorkers;                        // [workers]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    for (int i = 0; i < kEncStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kEncWorkers);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+
+  // This CTA's units: a contiguous range of the even split, so consecutive
+  // units are slices of one tile and its maxima fold locally.
+  const int units = (p.tiles_a + p.tiles_b) * p.slices;
+  const int uq = units / (int)gridDim.x, ur = units % (int)gridDim.x;
+  const int u_begin = (int)blockIdx.x * uq + min((int)blockIdx.x, ur);
+  const int u_end = u_begin + uq + ((int)blockIdx.x < ur ? 1 : 0);
+  const int sub_a = kBM / kEncBoxRows;   // boxes per A unit
+  const int sub_b = p.bn / kEncBoxRows;  // boxes per B unit
+  const uint64_t limit = p.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, pending = 0, pend_par = 0;
+      bool ok = true;
+      for (int u = u_begin; ok && u < u_end; ++u) {
+        const int t = u / p.slices, sl = u - t * p.slices;
+        const bool is_a = t < p.tiles_a;
+        const CUtensorMap* map = is_a ? &tmA : &tmB;
+        const int row0 = is_a ? t * kBM : (t - p.tiles_a) * p.bn;
+        const int nsub = is_a ? sub_a : sub_b;
+        for (int h = 0; h < nsub; ++h) {
+          if (!enc_wait(&empty[stage], phase ^ 1, abort_flag, limit, true)) {
+            if (!*(volatile int*)abort_flag) enc_error(p, abort_flag);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kEncStageBytes);
+          tma_load_2d(ring + stage * kEncStageBytes, map, &full[stage], sl * kEncSliceCols,
+                      row0 + h * kEncBoxRows);
+          pending |= 1u << stage;
+          pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kEncStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Drain: every copy this thread issued lands before the CTA exits.
+      for (int i = 0; i < kEncStages; ++i)
+        if (pending & (1u << i)) enc_wait(&full[i], (pend_par >> i) & 1, abort_flag, limit, false);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- workers
+  const int wt = threadIdx.x - 32;  // 0 .. kEncWorkerThreads - 1
+  const int ww = warp - 1;          // 0 .. kEncWorkers - 1
+  const int cg = lane % kEncLanesPerRow;  // 8-column group of the slice
+  const int rsub = wt / kEncLanesPerRow;  // first row of this thread in a box
+  int stage = 0;
+  uint32_t phase = 0;
+  // fp16: running max |sum| and unit count of the current tile (thread 0).
+  float run_smax = 0.f;
+  int run_units = 0;
+  for (int u = u_begin; u < u_end; ++u) {
+    const int t = u / p.slices, sl = u - t * p.slices;
+    const bool is_a = t < p.tiles_a;
+    const int tile = is_a ? t : t - p.tiles_a;
+    const int nsub = is_a ? sub_a : sub_b;
+    float acc[kEncColsPerThread];
+#pragma unroll
+    for (int i = 0; i < kEncColsPerThread; ++i) acc[i] = 0.f;
+    // max |element| on packed pairs: |x| is the bit pattern with the sign
+    // bits cleared, and a 16-bit float pair compares like its halves.
+    T2 amax2 = zero2<T2>();
+    bool ok = true;
+    for (int h = 0; h < nsub; ++h) {
+      ok = ok && enc_wait(&full[stage], phase, abort_flag, limit, true);
+      if (ok) {
+        const uint8_t* st = ring + stage * kEncStageBytes + cg * 16;
+#pragma unroll
+        for (int i = 0; i < kEncBoxRows / kEncRowsPerPass; ++i) {
+          const uint4 v = *reinterpret_cast<const uint4*>(
+              st + (rsub + kEncRowsPerPass * i) * (kEncSliceCols * 2));
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const T2 pr = as_pair<T2>(w4[j]);
+            acc[2 * j] += to_f<T>(lo_of(pr));
+            acc[2 * j + 1] += to_f<T>(hi_of(pr));
+            amax2 = pair_max(amax2, as_pair<T2>(w4[j] & 0x7fff7fffu));
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (++stage == kEncStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+    if (!ok && !*(volatile int*)abort_flag && lane == 0) enc_error(p, abort_flag);
+    // Fold the warp's rows, then the warps (through shared memory).
+#pragma unroll
+    for (int off = kEncLanesPerRow; off < 32; off <<= 1)
+#pragma unroll
+      for (int i = 0; i < kEncColsPerThread; ++i)
+        acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
+    if (lane < kEncLanesPerRow) {
+#pragma unroll
+      for (int i = 0; i < kEncColsPerThread; ++i)
+        part[ww * kEncSliceCols + cg * kEncColsPerThread + i] = acc[i];
+    }
+    float amax = fmaxf(to_f<T>(lo_of(amax2)), to_f<T>(hi_of(amax2)));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) wmax[ww] = amax;
+    if (!workers_all(ok)) break;  // every worker leaves together
+    // wmax is rewritten before the next unit's first barrier: read it here.
+    if (wt == 0) {
+      float mx = wmax[0];
+      for (int w = 1; w < kEncWorkers; ++w) mx = fmaxf(mx, wmax[w]);
+      p.umax[u] = mx;
+      if (!kScaled && sl == 0) p.pub[t].scale_exp = 0;
+    }
+
+    T* enc = static_cast<T*>(is_a ? p.enc_a : p.enc_b);
+    T* hi_row = enc + (int64_t)(kEncRows * tile) * p.kp;
+    T* lo_row = hi_row + p.kp;
+    const int col = sl * kEncSliceCols + wt;
+    if (wt < kEncSliceCols) {
+      float x = 0.f;
+#pragma unroll
+      for (int w = 0; w < kEncWorkers; ++w) x += part[w * kEncSliceCols + wt];
+      float smax = 0.f;
+      if (col < p.kp) {  // columns in [k, kp) hold zero sums
+        if constexpr (kScaled) {
+          __stcg(p.sums + (int64_t)t * p.kp + col, x);
+          smax = fabsf(x);
+        } else {
+          const T hi = from_f<T>(x);
+          hi_row[col] = hi;
+          lo_row[col] = from_f<T>(x - to_f<T>(hi));
+        }
+      }
+      if constexpr (kScaled) {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+          smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, off));
+        if (lane == 0) wsmax[ww] = smax;
+      }
+    }
+    named_bar_sync(1, kEncWorkerThreads);
+    if constexpr (kScaled) {
+      // wsmax and part are rewritten only after the next unit's first barrier.
+      if (wt == 0)
+        for (int w = 0; w < kEncSliceCols / 32; ++w) run_smax = fmaxf(run_smax, wsmax[w]);
+      ++run_units;
+      // Hand this CTA's share of the tile to the tile's counter when the tile
+      // ends here (next unit is another tile, or the range ends).
+      const bool tile_ends = (u + 1 == u_end) || ((u + 1) / p.slices != t);
+      if (!tile_ends) continue;
+      if (wt < kEncSliceCols) __threadfence();  // this tile's sums before the counter
+      named_bar_sync(1, kEncWorkerThreads);
+      if (wt == 0) {
+        // Non-negative floats order like their bit patterns.
+        atomicMax(&p.stat[t].encmax_bits, __float_as_uint(run_smax));
+        const uint32_t before = atom_add_acq_rel_gpu(&p.stat[t].count, (uint32_t)run_units);
+        *last_unit = before + (uint32_t)run_units == (uint32_t)p.slices ? 1 : 0;
+      }
+      run_smax = 0.f;
+      run_units = 0;
+      named_bar_sync(1, kEncWorkerThreads);
+      if (*last_unit) {
+        // Last share of this tile: every slice's sums and maxima are in.
+        __threadfence();
+        const float emax = __uint_as_float(atomicAdd(&p.stat[t].encmax_bits, 0u));
+        int ex = 0;
+        if (emax > 0.f) frexpf(emax, &ex);
+        const int e = (emax > 0.f) ? 15 - ex : 0;  // emax * 2^e in [2^14, 2^15)
+        const float* tsums = p.sums + (int64_t)t * p.kp;
+        for (int c = wt * kEncColsPerThread; c < p.kp; c += kEncWorkerThreads * kEncColsPerThread) {
+          const float4 a = __ldcg(reinterpret_cast<const float4*>(tsums + c));
+          const float4 b = __ldcg(reinterpret_cast<const float4*>(tsums + c + 4));
+          const float x[kEncColsPerThread] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          split_store<T>(hi_row, lo_row, c, x, e);
+        }
+        if (wt == 0) {
+          p.pub[t].scale_exp = e;
+          p.stat[t].encmax_bits = 0;
+          p.stat[t].count = 0;
+        }
+      }
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_encode_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const EncParams& p,
+                            int grid, cudaStream_t stream) {
+  static std::atomic<uint64_t> done_mask{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (!bit || !(done_mask.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(encode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kEncSmem);
+    if (e != cudaSuccess) return e;
+    done_mask.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  return launch_pdl(encode_kernel<T>, dim3(grid), dim3(kEncThreads), kEncSmem, stream, tmA, tmB,
+                    p);
+}
+
+cudaError_t launch_encode(int in_bf16, const CUtensorMap& tmA, const CUtensorMap& tmB, int m,
+                          int n, int kp, int bn, int sms, float* sums, void* enc_a, void* enc_b,
+                          TileStat* stat, TilePub* pub, float* umax, skg_report_t* report,
+                          uint64_t timeout_ns, cudaStream_t stream) {
+  EncParams p;
+  p.kp = kp;
+  p.bn = bn;
+  p.tiles_a = (m + kBM - 1) / kBM;
+  p.tiles_b = (n + bn - 1) / bn;
+  p.slices = encode_slices(kp);
+  p.sums = sums;
+  p.enc_a = enc_a;
+  p.enc_b = enc_b;
+  p.stat = stat;
+  p.pub = pub;
+  p.umax = umax;
+  p.report = report;
+  p.timeout_ns = timeout_ns;
+  const int64_t units = (int64_t)(p.tiles_a + p.tiles_b) * p.slices;
+  const int grid = (int)(units < sms ? units : sms);
+  if (grid <= 0) return cudaSuccess;
+  return in_bf16 ? launch_encode_t<__nv_bfloat16>(tmA, tmB, p, grid, stream)
+                 : launch_encode_t<__half>(tmA, tmB, p, grid, stream);
 }
 
 // C = beta * C (beta == 0 writes zeros without reading C).

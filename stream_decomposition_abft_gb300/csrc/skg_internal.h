@@ -45,15 +45,30 @@ cudaError_t launch_gemm(const Maps& mp, const KernelParams& p, int grid, cudaStr
 
 // ABFT encode pass (skg_encode.cu): e^T A per 128-row tile of A and B e
 // per bn-row tile of the stored n x k B, as hi / lo rows in the input type
-// (enc_a: 2 tiles_a x kp, enc_b: 2 tiles_b x kp), plus per-tile maxima and
-// scales in `pub` (A tiles first). `sums` is fp32 scratch, (tiles_a +
-// tiles_b) x kp; `stat` is scratch that must start at zero and is left at
-// zero.
-cudaError_t launch_encode(int in_bf16, const void* A, int64_t lda, int m, const void* B,
-                          int64_t ldb, int n, int k, int kp, int bn, float* sums, void* enc_a,
-                          void* enc_b, TileStat* stat, TilePub* pub, cudaStream_t stream);
+// (enc_a: 2 tiles_a x kp, enc_b: 2 tiles_b x kp), the per-tile scales in
+// `pub` and the max |element| of every unit (tile x slice) in `umax` (A tiles
+// first). tmA / tmB map A (k x m) and the stored B (k x n) with
+// kEncBoxCols x kEncBoxRows boxes and no swizzle. `sums` is fp32 scratch,
+// (tiles_a + tiles_b) x kp (fp16 only); `stat` is scratch that must start at
+// zero and is left at zero. A wait that times out sets
+// SKG_ERR_PIPELINE_TIMEOUT in `report`.
+cudaError_t launch_encode(int in_bf16, const CUtensorMap& tmA, const CUtensorMap& tmB, int m,
+                          int n, int kp, int bn, int sms, float* sums, void* enc_a, void* enc_b,
+                          TileStat* stat, TilePub* pub, float* umax, skg_report_t* report,
+                          uint64_t timeout_ns, cudaStream_t stream);
 
-// 256-column slices of the encode pass.
+// k-columns and rows of one encode box (one work unit covers kEncBoxCols
+// k-columns of a whole operand tile).
+#ifndef SKG_ENC_BOX_COLS
+#define SKG_ENC_BOX_COLS 256
+#endif
+#ifndef SKG_ENC_BOX_ROWS
+#define SKG_ENC_BOX_ROWS 64
+#endif
+constexpr int kEncBoxCols = SKG_ENC_BOX_COLS;
+constexpr int kEncBoxRows = SKG_ENC_BOX_ROWS;
+
+// kEncBoxCols-column slices of the encode pass.
 int encode_slices(int kp);
 
 // C = beta * C for k == 0 (skg_encode.cu).

@@ -67,18 +67,17 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
-// ABFT encode pass, per operand tile: running maxima and a block counter
-// (scratch, left at zero after every pass) ...
+// ABFT encode pass, per operand tile (fp16 inputs only): the running max
+// |encoding| and a unit counter (scratch, left at zero after every pass) ...
 struct TileStat {
-  uint32_t absmax_bits;  // max |element| over the tile (fp32 bits)
-  uint32_t encmax_bits;  // max |encoding| over the tile
-  uint32_t count;        // blocks of the tile finished
-  uint32_t pad;
+  uint32_t encmax_bits;  // max |encoding| over the tile (fp32 bits)
+  uint32_t count;        // units of the tile finished
+  uint32_t pad[2];
 };
 // ... and what the pass publishes for the main kernel's epilogue.
 struct TilePub {
-  float maxabs;      // max |element| over the tile's rows of A (or columns of B)
-  int32_t scale_exp; // the tile's encodings are stored scaled by 2^scale_exp
+  int32_t scale_exp;  // the tile's encodings are stored scaled by 2^scale_exp
+  int32_t pad;
 };
 
 struct KernelParams {
@@ -102,6 +101,10 @@ struct KernelParams {
   int64_t ld_cr, ld_cc;
   const TilePub* pub_a;  // per 128-row tile of A
   const TilePub* pub_b;  // per BLK_N-column tile of B
+  // max |element| of every encode unit (operand tile x slice of enc_slices
+  // per tile; A tiles first): a tile's maximum is the max over its units.
+  const float* umax;
+  int enc_slices, enc_tiles_a;
   // Fused reference-checksum GEMMs: tiles [0, s.t_ck) of the schedule.
   // Tile j < ck_cr_tiles computes rows [128 j, 128 j + 128) of
   // cr_all = A x [Be_hi; Be_lo]^T (ck_n_cr columns); the others compute rows
@@ -164,7 +167,7 @@ struct Aux {
   float fix_value;
   float inj_clean;
   float d_row, d_col;
-  int32_t pad[6];
+  float tmax_a[4], tmax_b[4];  // per epilogue warp: partial tile maxima
 };
 static_assert(sizeof(Aux) <= 512, "aux size");
 
@@ -762,14 +765,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Reference checksums of this tile: thread r holds the row checksum
           // of row r and the column checksum of columns h*128 + r, each the
           // sum of its hi and lo partial products, unscaled by the tile's
-          // power of two. The default thresholds use the tile's own maxima:
-          //   tau = 2^-12 sqrt(k) sqrt(side) max|A_tile| max|B_tile|.
+          // power of two.
           const TilePub pa = p.pub_a[tm];
           const TilePub pb = p.pub_b[tn];
-          float tau_r = p.tau_row, tau_c = p.tau_col;
-          const float base = ldexpf(1.f, -12) * sqrtf((float)p.k) * pa.maxabs * pb.maxabs;
-          if (!(tau_r > 0.f)) tau_r = base * sqrtf((float)BN);
-          if (!(tau_c > 0.f)) tau_c = base * sqrtf((float)kBM);
+          {
+            // Tile maxima for the thresholds: max over the tile's encode units.
+            const float* ua = p.umax + (int64_t)tm * p.enc_slices;
+            const float* ub = p.umax + (int64_t)(p.enc_tiles_a + tn) * p.enc_slices;
+            float ma = 0.f, mb = 0.f;
+            for (int j = et; j < p.enc_slices; j += kEpiThreads) {
+              ma = fmaxf(ma, __ldcg(ua + j));
+              mb = fmaxf(mb, __ldcg(ub + j));
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+              ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, off));
+              mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+            }
+            if (lane == 0) {
+              aux->tmax_a[q] = ma;
+              aux->tmax_b[q] = mb;
+            }
+          }
           float cr = 0.f;
           if (m0 + r < p.m) {
             const float* crp = p.cr_all + (int64_t)(m0 + r) * p.ld_cr + kEncRows * tn;
@@ -785,11 +802,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               cc[h] = ldexpf(__ldcg(ccp) + __ldcg(ccp + 1), -pa.scale_exp);
             }
           }
+          named_bar_sync(1, kEpiThreads);  // column sums and tile maxima stored
+          // Default thresholds from the tile's own maxima:
+          //   tau = 2^-12 sqrt(k) sqrt(side) max|A_tile| max|B_tile|.
+          float tau_r = p.tau_row, tau_c = p.tau_col;
+          {
+            const float ma = fmaxf(fmaxf(aux->tmax_a[0], aux->tmax_a[1]),
+                                   fmaxf(aux->tmax_a[2], aux->tmax_a[3]));
+            const float mb = fmaxf(fmaxf(aux->tmax_b[0], aux->tmax_b[1]),
+                                   fmaxf(aux->tmax_b[2], aux->tmax_b[3]));
+            const float base = ldexpf(1.f, -12) * sqrtf((float)p.k) * ma * mb;
+            if (!(tau_r > 0.f)) tau_r = base * sqrtf((float)BN);
+            if (!(tau_c > 0.f)) tau_c = base * sqrtf((float)kBM);
+          }
           if (et == 0) {  // the report keeps the largest thresholds used
             atomicMax(reinterpret_cast<int*>(&p.report->tau_row), __float_as_int(tau_r));
             atomicMax(reinterpret_cast<int*>(&p.report->tau_col), __float_as_int(tau_c));
           }
-          named_bar_sync(1, kEpiThreads);  // column sums of all four warps stored
 
           const float d_r = rowsum - cr;
           const bool bad_r = !(fabsf(d_r) <= tau_r);

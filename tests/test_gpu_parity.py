@@ -297,12 +297,13 @@ def test_raster_bands(band):
 @pytest.mark.parametrize("shape", [(300, 300, 200), (1000, 1300, 520), (129, 257, 640),
                                    (2000, 2100, 1000)])
 @pytest.mark.parametrize("tile_n", [128, 256])
-def test_abft_ragged_shapes_clean(shape, tile_n):
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_abft_ragged_shapes_clean(shape, tile_n, dtype):
     # Ragged m, n and k with the ABFT check on: no false positives, output
-    # within tolerance, every tile checked (encode groups of 128 rows, B tiles
-    # of tile_n columns with a short last tile).
+    # within tolerance, every tile checked (encode slices of 128 k-columns
+    # with a short last one, B tiles of tile_n columns with a short last tile).
     m, n, k = shape
-    p = inputs.make_problem(m, n, k, seed=m + n, in_dtype="bf16", out_dtype="f32",
+    p = inputs.make_problem(m, n, k, seed=m + n, in_dtype=dtype, out_dtype="f32",
                             law_a="normal", law_b="normal", alpha=0.5, beta=1.5)
     opts = skgemm.opts_default(abft=1, tile_n=tile_n)
     ws = None
@@ -314,3 +315,35 @@ def test_abft_ragged_shapes_clean(shape, tile_n):
         assert rep.detected == 0 and rep.status_bits == 0
         assert rep.tiles_checked == ((m + 127) // 128) * ((n + tile_n - 1) // tile_n)
         assert rep.max_ratio_row < 0.1 and rep.max_ratio_col < 0.1
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_abft_f16_large_encodings(tile_n):
+    # fp16 operands whose tile column sums exceed the fp16 range (|sum| up to
+    # 128 * 3000): the encode pass must scale each tile's encodings by a power
+    # of two before splitting them into fp16 terms. Clean run, then a flipped
+    # exponent bit that must be found and corrected.
+    m, n, k = 640, 768, 1000
+    p = inputs.make_problem(m, n, k, seed=31, in_dtype="f16", out_dtype="f32",
+                            law_a="uniform", law_b="uniform", scale_a=3000.0, scale_b=1e-3)
+    ref = reference(p)
+    C, ws, st = run(p, skgemm.opts_default(abft=1, tile_n=tile_n))
+    assert st == skgemm.OK
+    check_full(p, C, ref)
+    rep = ws.report()
+    assert rep.detected == 0 and rep.status_bits == 0
+    assert rep.max_ratio_row < 0.1 and rep.max_ratio_col < 0.1
+    tiles_n = (n + tile_n - 1) // tile_n
+    tm, tn = divmod(3, tiles_n)
+    v = ref[tm * 128 + 9, tn * tile_n + 17] / p.alpha
+    ma, mb = ab.tile_maxima(p.A.double().numpy(), p.B.double().numpy(), tm, tn, 128, tile_n)
+    tau = ab.default_tau(k, tile_n, ma, mb)
+    kind, _ = ab.classify_flip(v, 30, tau, 1e-3 * tau)
+    assert kind == ab.MUST_DETECT, (v, tau)
+    C, ws, st = run(p, skgemm.opts_default(abft=1, tile_n=tile_n, inject_tile=3, inject_row=9,
+                                           inject_col=17, inject_bit=30))
+    assert st == skgemm.OK
+    rep = ws.report()
+    assert rep.detected == 1 and rep.corrected == 1
+    assert (rep.records[0].tile, rep.records[0].row, rep.records[0].col) == (3, 9, 17)
+    check_full(p, C, ref)
