@@ -61,6 +61,7 @@ int sm_count_cached() {
 struct Resolved {
   int sched;
   int grid;
+  int grid_ck;  // dedicated checksum-tile CTAs launched after the grid ones
   int bn;
   int abft;
   float tau_row, tau_col;
@@ -95,6 +96,7 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
                               want_grid, ms);
   r.sched = pl.sched;
   r.grid = pl.grid;
+  r.grid_ck = 0;
   r.bn = pl.bn;
   r.ws_grid = r.abft ? ms : r.grid;
   r.k_for_plan = k > 0 ? k : 1;  // ABFT checksum GEMMs may use up to every SM
@@ -272,7 +274,8 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
 
   KernelParams p;
   memset(&p, 0, sizeof(p));
-  p.s = make_schedule(g.m, g.n, g.k, kBM, r.bn, kBK, r.grid, r.sched, t_ck);
+  p.s = make_schedule(g.m, g.n, g.k, kBM, r.bn, kBK, r.grid, r.sched, t_ck, t_ck ? r.grid_ck : 0);
+  const int launch_grid = r.grid + p.s.g_ck;
   // Banded raster: a wave of g tiles covers about (g / band) rows x band
   // columns; band ~ sqrt(g * BLK_M / BLK_N) minimises the A + B bytes one
   // wave touches per k-step.
@@ -323,11 +326,11 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
 
   cudaError_t e;
   if (r.bn == 128)
-    e = abft_epilogue ? dispatch_out<128, true>(g.out_dtype, mp, p, r.grid, stream)
-                      : dispatch_out<128, false>(g.out_dtype, mp, p, r.grid, stream);
+    e = abft_epilogue ? dispatch_out<128, true>(g.out_dtype, mp, p, launch_grid, stream)
+                      : dispatch_out<128, false>(g.out_dtype, mp, p, launch_grid, stream);
   else
-    e = abft_epilogue ? dispatch_out<256, true>(g.out_dtype, mp, p, r.grid, stream)
-                      : dispatch_out<256, false>(g.out_dtype, mp, p, r.grid, stream);
+    e = abft_epilogue ? dispatch_out<256, true>(g.out_dtype, mp, p, launch_grid, stream)
+                      : dispatch_out<256, false>(g.out_dtype, mp, p, launch_grid, stream);
   return e == cudaSuccess ? SKG_OK : SKG_ERR_CUDA;
 }
 
@@ -384,6 +387,7 @@ void replan_fused(int64_t m, int64_t n, const skg_opts_t* opts, Resolved& r) {
                               want_sched >= 0 ? r.ws_grid : 0, r.ws_grid, t_ck);
   r.grid = pl.grid;
   r.sched = pl.sched;
+  r.grid_ck = pl.grid_ck;
 }
 
 skg_status_t check_inputs(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
@@ -574,7 +578,7 @@ skg_status_t skg_launch_shape(int64_t m, int64_t n, int64_t k, const skg_opts_t*
   if (r.abft && m > 0 && n > 0 && k > 0 && can_fuse_checksums(layout(m, n, k, r), r.bn))
     replan_fused(m, n, opts, r);
   if (tile_n) *tile_n = r.bn;
-  if (grid) *grid = r.grid;
+  if (grid) *grid = r.grid + r.grid_ck;
   if (sched) *sched = r.sched;
   return SKG_OK;
 }

@@ -206,14 +206,22 @@ __global__ void __launch_bounds__(kEncThreads, 1)
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
 
-  // This CTA's units: a contiguous range of the even split, so consecutive
-  // units are slices of one tile and its maxima fold locally.
-  const int units = (p.tiles_a + p.tiles_b) * p.slices;
-  const int uq = units / (int)gridDim.x, ur = units % (int)gridDim.x;
-  const int u_begin = (int)blockIdx.x * uq + min((int)blockIdx.x, ur);
-  const int u_end = u_begin + uq + ((int)blockIdx.x < ur ? 1 : 0);
+  // This CTA's units: a contiguous range, so consecutive units are slices of
+  // one tile. The split is even in boxes (an A unit is kBM / kEncBoxRows
+  // boxes, a B unit bn / kEncBoxRows): CTA b takes the units whose first box
+  // lies in [b * boxes / g, (b + 1) * boxes / g).
   const int sub_a = kBM / kEncBoxRows;   // boxes per A unit
   const int sub_b = p.bn / kEncBoxRows;  // boxes per B unit
+  const int units_a = p.tiles_a * p.slices;
+  const int units = units_a + p.tiles_b * p.slices;
+  const int64_t boxes = (int64_t)units_a * sub_a + (int64_t)(units - units_a) * sub_b;
+  auto first_unit_at = [&](int64_t box) -> int {  // first unit whose first box is >= box
+    const int64_t in_a = (int64_t)units_a * sub_a;
+    if (box <= in_a) return (int)((box + sub_a - 1) / sub_a);
+    return units_a + (int)((box - in_a + sub_b - 1) / sub_b);
+  };
+  const int u_begin = first_unit_at(boxes * blockIdx.x / gridDim.x);
+  const int u_end = first_unit_at(boxes * (blockIdx.x + 1) / gridDim.x);
   const uint64_t limit = p.timeout_ns;
 
   if (warp == 0) {

@@ -198,6 +198,21 @@ static __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Aux
   }
 }
 
+// wait_bar, inlined: loads issued before it stay in flight during the wait
+// (a call would make the compiler wait for them first).
+__device__ __forceinline__ bool wait_bar_inline(uint64_t* bar, uint32_t parity, Aux* aux,
+                                                uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31) == 0) {
+      if (aborted(aux)) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
+    }
+  }
+}
+
 __device__ __forceinline__ float f32_of(uint32_t u) { return __uint_as_float(u); }
 
 // Sum over the 32 lanes of a warp for each of 32 columns: on return lane l
@@ -578,16 +593,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         tr[0] = nseg + 1;
       }
       ++nseg;
-      bool got = wait_bar(&tfull_bar[ab], aphase, aux, limit);
-      if (!got && !aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
-      if (!epi_all(got && store_ok && !aborted(aux))) break;
-      tc_fence_after();
-      const uint32_t tacc = tmem_base + ab * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
       const bool is_ck = w.tile < s.t_ck;  // a fused checksum-GEMM tile
       int tm = 0, tn = 0;
       if (!is_ck) tile_coords(s, w.tile, tm, tn);
       const int m0 = tm * kBM;
       const int n0 = tn * BN;
+
+      // Inputs of this tile's ABFT check that do not depend on its
+      // accumulator (the encode pass's maxima and scales, the reference
+      // checksums): their loads are issued before the accumulator wait and
+      // first used after it, so their latency hides behind the mainloop.
+      float pf_ma = 0.f, pf_mb = 0.f, pf_cr0 = 0.f, pf_cr1 = 0.f;
+      float pf_cc0[BN / 128], pf_cc1[BN / 128];
+#pragma unroll
+      for (int h = 0; h < BN / 128; ++h) pf_cc0[h] = pf_cc1[h] = 0.f;
+      int pf_ea = 0, pf_eb = 0;
+      if (C::ABFT && !is_ck && w.role != kRolePeer) {
+        if (s.t_ck > 0 && !ck_ready) {
+          // The fused checksum tiles must all be stored first. Every CTA runs
+          // its own share of them before its first output tile, and dedicated
+          // checksum CTAs wait for nothing, so this wait ends.
+          bool fine = true;
+          if (et == 0) {
+            const uint64_t t0 = globaltimer();
+            while (ld_acquire_gpu(&p.hdr->ck_done) < (uint32_t)s.t_ck) {
+              nanosleep_ns(128);
+              if (globaltimer() - t0 > limit) {
+                record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
+                fine = false;
+                break;
+              }
+            }
+          }
+          if (!epi_all(fine && !aborted(aux))) break;
+          ck_ready = true;
+        }
+        const float* ua = p.umax + (int64_t)tm * p.enc_slices;
+        const float* ub = p.umax + (int64_t)(p.enc_tiles_a + tn) * p.enc_slices;
+        if (et < p.enc_slices) {
+          pf_ma = __ldcg(ua + et);
+          pf_mb = __ldcg(ub + et);
+        }
+        pf_ea = p.pub_a[tm].scale_exp;
+        pf_eb = p.pub_b[tn].scale_exp;
+        if (m0 + r < p.m) {
+          const float* crp = p.cr_all + (int64_t)(m0 + r) * p.ld_cr + kEncRows * tn;
+          pf_cr0 = __ldcg(crp);
+          pf_cr1 = __ldcg(crp + 1);
+        }
+#pragma unroll
+        for (int h = 0; h < BN / 128; ++h) {
+          const int col = n0 + h * 128 + r;
+          if (col < p.n) {
+            const float* ccp = p.cc_all + (int64_t)col * p.ld_cc + kEncRows * tm;
+            pf_cc0[h] = __ldcg(ccp);
+            pf_cc1[h] = __ldcg(ccp + 1);
+          }
+        }
+        // More encode units than epilogue threads (k above 128 slices).
+        for (int j = et + kEpiThreads; j < p.enc_slices; j += kEpiThreads) {
+          pf_ma = fmaxf(pf_ma, __ldcg(ua + j));
+          pf_mb = fmaxf(pf_mb, __ldcg(ub + j));
+        }
+      }
+
+      bool got = wait_bar_inline(&tfull_bar[ab], aphase, aux, limit);
+      if (!got && !aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+      if (!epi_all(got && store_ok && !aborted(aux))) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + ab * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
       const int out_tile = w.tile - s.t_ck;  // output-tile number the caller sees
       const bool inject_here = !is_ck && (out_tile == p.inject_tile) && (w.role != kRolePeer);
       // This segment's region of fixup storage.
@@ -702,28 +776,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ ABFT verify
         int fix_row = -1, fix_col = -1;
         float fix_val = 0.f;
-        if (C::ABFT && s.t_ck > 0 && !ck_ready) {
-          // The fused checksum tiles must all be stored before the first
-          // verification reads them.
-          bool fine = true;
-          if (et == 0) {
-            const uint64_t t0 = globaltimer();
-            while (ld_acquire_gpu(&p.hdr->ck_done) < (uint32_t)s.t_ck) {
-              nanosleep_ns(128);
-              if (globaltimer() - t0 > limit) {
-                record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
-                fine = false;
-                break;
-              }
-            }
-          }
-          if (!epi_all(fine && !aborted(aux))) {
-            tc_fence_before();
-            mbar_arrive(&tempty_bar[ab]);
-            break;
-          }
-          ck_ready = true;
-        }
         if (C::ABFT) {
           // This warp's staging buffers hold its column sums below: its own
           // earlier TMA stores must have finished reading them.
@@ -765,18 +817,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Reference checksums of this tile: thread r holds the row checksum
           // of row r and the column checksum of columns h*128 + r, each the
           // sum of its hi and lo partial products, unscaled by the tile's
-          // power of two.
-          const TilePub pa = p.pub_a[tm];
-          const TilePub pb = p.pub_b[tn];
+          // power of two; tile maxima for the thresholds are the max over
+          // the tile's encode units.
+          const float cr = ldexpf(pf_cr0 + pf_cr1, -pf_eb);
+          float cc[BN / 128];
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) cc[h] = ldexpf(pf_cc0[h] + pf_cc1[h], -pf_ea);
           {
-            // Tile maxima for the thresholds: max over the tile's encode units.
-            const float* ua = p.umax + (int64_t)tm * p.enc_slices;
-            const float* ub = p.umax + (int64_t)(p.enc_tiles_a + tn) * p.enc_slices;
-            float ma = 0.f, mb = 0.f;
-            for (int j = et; j < p.enc_slices; j += kEpiThreads) {
-              ma = fmaxf(ma, __ldcg(ua + j));
-              mb = fmaxf(mb, __ldcg(ub + j));
-            }
+            float ma = pf_ma, mb = pf_mb;
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) {
               ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, off));
@@ -785,21 +833,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
               aux->tmax_a[q] = ma;
               aux->tmax_b[q] = mb;
-            }
-          }
-          float cr = 0.f;
-          if (m0 + r < p.m) {
-            const float* crp = p.cr_all + (int64_t)(m0 + r) * p.ld_cr + kEncRows * tn;
-            cr = ldexpf(__ldcg(crp) + __ldcg(crp + 1), -pb.scale_exp);
-          }
-          float cc[BN / 128];
-#pragma unroll
-          for (int h = 0; h < BN / 128; ++h) {
-            const int col = n0 + h * 128 + r;
-            cc[h] = 0.f;
-            if (col < p.n) {
-              const float* ccp = p.cc_all + (int64_t)col * p.ld_cc + kEncRows * tm;
-              cc[h] = ldexpf(__ldcg(ccp) + __ldcg(ccp + 1), -pa.scale_exp);
             }
           }
           named_bar_sync(1, kEpiThreads);  // column sums and tile maxima stored

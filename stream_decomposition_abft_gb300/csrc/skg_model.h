@@ -72,12 +72,18 @@ inline double predict_us(const Schedule& s, const CostModel& M) {
                       M.d * (double)peers;
     if (tx > worst) worst = tx;
   }
+  if (s.g_ck > 0) {  // dedicated side CTAs: whole side tiles
+    const int64_t nt = (s.t_ck + s.g_ck - 1) / s.g_ck;
+    const double tx = M.a + M.c * (double)(nt * I) + M.e * (double)nt;
+    if (tx > worst) worst = tx;
+  }
   return worst;
 }
 
 struct Plan {
   int bn, sched, grid;
   double us;
+  int grid_ck;  // dedicated side CTAs launched after the grid ones
 };
 
 // Best (BLK_N, schedule, g) for an m x n x k launch on `sms` SMs. Fixed
@@ -86,7 +92,7 @@ inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_s
                         int want_grid, int sms, int t_ck) {
   static const int kCands[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 76, 96, 112, 128, 144};
   Plan best{want_bn ? want_bn : 256, want_sched >= 0 ? want_sched : kSchedSK2DP,
-            want_grid ? want_grid : sms, 1e300};
+            want_grid ? want_grid : sms, 1e300, 0};
   for (int bn = 128; bn <= 256; bn += 128) {
     if (want_bn && bn != want_bn) continue;
     const CostModel& M = bn == 128 ? kModel128 : kModel256;
@@ -118,11 +124,21 @@ inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_s
         // with two or more full waves the hybrids exist to bound it, so the
         // automatic choice does not take basic SK there.
         if (want_sched < 0 && sched == kSchedSK && t >= 2 * (int64_t)cands[i]) continue;
-        const Schedule s = make_schedule(m, n, k, kTileM, bn, kTileK, cands[i], sched, t_ck);
-        const double us = predict_us(s, M);
-        // Prefer fewer CTAs on ties (less fixup storage and traffic).
-        if (us < best.us - 1e-9 || (us < best.us + 1e-9 && cands[i] < best.grid)) {
-          best = Plan{bn, sched, cands[i], us};
+        // Side tiles split over the grid, or (automatic grid only) one each
+        // on SMs the grid leaves idle: every verification waits for all side
+        // tiles, so they must end with the output CTAs' first tiles.
+        const int spare = want_grid ? 0 : sms - cands[i];
+        const int gck_opts[2] = {0, t_ck <= spare ? t_ck : 0};
+        for (int oi = 0; oi < (gck_opts[1] > 0 ? 2 : 1); ++oi) {
+          const int gck = gck_opts[oi];
+          const Schedule s =
+              make_schedule(m, n, k, kTileM, bn, kTileK, cands[i], sched, t_ck, gck);
+          const double us = predict_us(s, M);
+          // Prefer fewer CTAs on ties (less fixup storage and traffic).
+          if (us < best.us - 1e-9 ||
+              (us < best.us + 1e-9 && cands[i] + gck < best.grid + best.grid_ck)) {
+            best = Plan{bn, sched, cands[i], us, gck};
+          }
         }
       }
     }

@@ -47,9 +47,10 @@ struct Schedule {
   int64_t sk_total;   // Stream-K iterations of the output tiles after the DP ones
   int64_t sk_q;       // floor(sk_total / g)
   int sk_r;           // sk_total mod g
-  int64_t ck_total;   // iterations of the side tiles, t_ck * ipt
+  int64_t ck_total;   // side-tile iterations split over the g CTAs (0 with g_ck)
   int64_t ck_q;       // floor(ck_total / g)
   int ck_r;           // ck_total mod g
+  int g_ck;           // dedicated side CTAs g .. g + g_ck - 1 (0: side tiles split)
   int band;           // tile columns per raster band (tiles_n = row-major)
 };
 
@@ -76,12 +77,15 @@ SKG_HD int dp_tiles(int t, int g, int mode) {
 }
 
 // The page's schedule over the output tiles (DP tiles first, then the
-// Stream-K region), preceded by `t_ck` full-k side tiles (the fused ABFT
-// checksum GEMMs). The side tiles form a region of their own whose
-// iterations are split evenly over all g CTAs, so every CTA starts with the
-// same small share of side work, whatever the schedule of the output tiles.
+// Stream-K region) on g CTAs, plus `t_ck` full-k side tiles (the fused ABFT
+// checksum GEMMs), placed one of two ways:
+//   - g_ck == 0: a region of their own whose iterations are split evenly
+//     over the g CTAs, so every CTA starts with the same small share of side
+//     work, whatever the schedule of the output tiles;
+//   - g_ck > 0: whole tiles on g_ck more CTAs (side tile j on CTA
+//     g + j mod g_ck), for launches that leave SMs idle.
 SKG_HD Schedule make_schedule(int64_t m, int64_t n, int64_t k, int bm, int bn, int bk, int g,
-                              int mode, int t_ck = 0) {
+                              int mode, int t_ck = 0, int g_ck = 0) {
   Schedule s;
   s.tiles_m = (int)((m + bm - 1) / bm);
   s.tiles_n = (int)((n + bn - 1) / bn);
@@ -94,7 +98,8 @@ SKG_HD Schedule make_schedule(int64_t m, int64_t n, int64_t k, int bm, int bn, i
   s.sk_total = (int64_t)(t_out - s.t_dp) * s.ipt;
   s.sk_q = s.sk_total / g;
   s.sk_r = (int)(s.sk_total % g);
-  s.ck_total = (int64_t)s.t_ck * s.ipt;
+  s.g_ck = s.t_ck > 0 ? g_ck : 0;
+  s.ck_total = s.g_ck > 0 ? 0 : (int64_t)s.t_ck * s.ipt;
   s.ck_q = s.ck_total / g;
   s.ck_r = (int)(s.ck_total % g);
   s.band = s.tiles_n > 0 ? s.tiles_n : 1;
@@ -133,17 +138,23 @@ struct Work {
 
 // Walks one CTA's segments in execution order: its share of the side
 // tiles, its DP tiles, then its Stream-K range; the split regions are cut
-// at tile boundaries.
+// at tile boundaries. A dedicated side CTA (x >= g) walks whole side tiles.
 struct Cursor {
   int x;
   int next_dp;
+  int next_side;  // dedicated side CTA: next side tile, else -1
   int64_t ck_it, ck_end;
   int64_t it, it_end;
 
   SKG_HD void init(const Schedule& s, int cta) {
     x = cta;
     next_dp = cta;
+    next_side = -1;
     it = it_end = ck_it = ck_end = 0;
+    if (cta >= s.g) {
+      next_side = cta - s.g;
+      return;
+    }
     if (s.sk_total > 0) sk_range(s, cta, it, it_end);
     if (s.ck_total > 0) even_range(s.ck_q, s.ck_r, cta, ck_it, ck_end);
   }
@@ -166,6 +177,17 @@ struct Cursor {
   }
 
   SKG_HD bool next(const Schedule& s, Work& w) {
+    if (next_side >= 0) {
+      if (next_side >= s.t_ck) return false;
+      w.tile = next_side;
+      w.kb_begin = 0;
+      w.kb_end = s.ipt;
+      w.role = kRoleFull;
+      w.peer_last = x;
+      w.region = 1;
+      next_side += s.g_ck;
+      return true;
+    }
     if (ck_it < ck_end) {
       cut(s, s.ck_q, s.ck_r, 0, 1, x, ck_it, ck_end, w);
       return true;
