@@ -297,6 +297,10 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   p.ck_n_cc = kEncRows * L.tiles_a;
   p.ck_rows_cr = (int)round_up(p.ck_n_cr, 16);
   p.ck_rows_cc = (int)round_up(p.ck_n_cc, 16);
+  // Two checksum k-blocks per ring stage when the encoding box fits its
+  // 8 KB slot (64 rows of 128 bytes) and the stage holds two A tiles.
+  p.ck_kpack_cr = (r.bn == 256 && p.ck_rows_cr <= 64) ? 2 : 1;
+  p.ck_kpack_cc = (r.bn == 256 && p.ck_rows_cc <= 64) ? 2 : 1;
   p.idesc_cr = idesc_f16(g.in_dtype == SKG_IN_BF16, kBM, (uint32_t)round_up(p.ck_n_cr, 16));
   p.idesc_cc = idesc_f16(g.in_dtype == SKG_IN_BF16, kBM, (uint32_t)round_up(p.ck_n_cc, 16));
   p.hdr = (WsHeader*)ws;

@@ -112,6 +112,10 @@ struct KernelParams {
   int ck_cr_tiles;
   int ck_n_cr, ck_n_cc;
   int ck_rows_cr, ck_rows_cc;  // encoding rows loaded per k-step (N rounded up to 16)
+  // k-blocks per ring stage for checksum tiles (1 or 2): a checksum k-step
+  // needs only the A (or B) tile and a few encoding rows, so two fit in one
+  // BLK_N = 256 stage; packed stages hold A(k), A(k+1), enc(k), enc(k+1).
+  int ck_kpack_cr, ck_kpack_cc;
   uint32_t idesc_cr, idesc_cc;
   float tau_row, tau_col;  // <= 0: derive from the encode pass maxima
   int inject_tile, inject_row, inject_col, inject_bit;
@@ -141,6 +145,9 @@ struct Cfg {
   static constexpr int B_BYTES = BN * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES;
+  // Packed checksum stage: two A tiles, then two encoding slots of ENC_SLOT bytes.
+  static constexpr int ENC_SLOT = 8192;
+  static constexpr bool CK_PACK = STAGE_BYTES >= 2 * A_BYTES + 2 * ENC_SLOT;
   static constexpr int EPI_BUF_BYTES = 32 * 128;
   static constexpr int EPI_BUFS = 2;
   static constexpr int EPI_BYTES = 4 * EPI_BUFS * EPI_BUF_BYTES;
@@ -457,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* mapA = &tmA;
         const CUtensorMap* mapB = &tmB;
         uint32_t tx = C::TX_BYTES;
+        int kpack = 1;
         int rowA, rowB;
         if (w.tile >= s.t_ck) {
           int tm, tn;
@@ -469,23 +477,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           rowA = w.tile * kBM;
           rowB = 0;
           tx = C::A_BYTES + p.ck_rows_cr * kBK * 2;
+          kpack = C::CK_PACK ? p.ck_kpack_cr : 1;
         } else {
           mapA = &tmB128;
           mapB = &tmEA;
           rowA = (w.tile - p.ck_cr_tiles) * kBM;
           rowB = 0;
           tx = C::A_BYTES + p.ck_rows_cc * kBK * 2;
+          kpack = C::CK_PACK ? p.ck_kpack_cc : 1;
         }
-        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
-          if (!wait_bar(&empty_bar[stage], phase ^ 1, aux, limit)) {
+        for (int kb = w.kb_begin; kb < w.kb_end; kb += kpack) {
+          if (!mbar_try_wait(&empty_bar[stage], phase ^ 1) &&
+              !wait_bar(&empty_bar[stage], phase ^ 1, aux, limit)) {
             if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
             ok = false;
             break;
           }
           uint8_t* st = ring + stage * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full_bar[stage], tx);
-          tma_load_2d(st, mapA, &full_bar[stage], kb * kBK, rowA);
-          tma_load_2d(st + C::A_BYTES, mapB, &full_bar[stage], kb * kBK, rowB);
+          if (kpack == 1) {
+            mbar_arrive_expect_tx(&full_bar[stage], tx);
+            tma_load_2d(st, mapA, &full_bar[stage], kb * kBK, rowA);
+            tma_load_2d(st + C::A_BYTES, mapB, &full_bar[stage], kb * kBK, rowB);
+          } else {  // packed checksum stage
+            const int nk = min(2, w.kb_end - kb);
+            mbar_arrive_expect_tx(&full_bar[stage], tx * nk);
+            for (int j = 0; j < nk; ++j) {
+              tma_load_2d(st + j * C::A_BYTES, mapA, &full_bar[stage], (kb + j) * kBK, rowA);
+              tma_load_2d(st + 2 * C::A_BYTES + j * C::ENC_SLOT, mapB, &full_bar[stage],
+                          (kb + j) * kBK, rowB);
+            }
+          }
           pending |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -502,6 +523,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // Shared-memory descriptor of the ring's first byte; the ring lies in
+      // the first 256 KB of shared memory, so adding (offset >> 4) to the
+      // 14-bit address field never carries out of it.
+      const uint64_t ring_desc = sdesc_sw128(smem_u32(ring));
       Cursor cur;
       cur.init(s, blockIdx.x);
       Work w;
@@ -520,27 +545,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem_base + ab * C::ACC_COLS;
         const uint32_t idesc = w.tile >= s.t_ck ? p.idesc_main
                                : (w.tile < p.ck_cr_tiles ? p.idesc_cr : p.idesc_cc);
-        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
-          if (!wait_bar(&full_bar[stage], phase, aux, limit)) {
-            if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(ring + stage * C::STAGE_BYTES);
-          const uint32_t b_addr = a_addr + C::A_BYTES;
+        const int kpack = (!C::CK_PACK || w.tile >= s.t_ck)
+                              ? 1
+                              : (w.tile < p.ck_cr_tiles ? p.ck_kpack_cr : p.ck_kpack_cc);
+        if (kpack == 1) {
+          for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+            // Inline fast path: the stage is usually full already.
+            if (!mbar_try_wait(&full_bar[stage], phase) &&
+                !wait_bar(&full_bar[stage], phase, aux, limit)) {
+              if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // Descriptors advance linearly with the (16-byte granular) address.
+            const uint64_t ad0 = ring_desc + (uint64_t)((stage * C::STAGE_BYTES) >> 4);
+            const uint64_t bd0 = ad0 + (uint64_t)(C::A_BYTES >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(a_addr + kk * 32);
-            const uint64_t bd = sdesc_sw128(b_addr + kk * 32);
-            const uint32_t acc = (kb > w.kb_begin || kk > 0) ? 1u : 0u;
-            umma_f16(d, ad, bd, idesc, acc);
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint32_t acc = (kb > w.kb_begin || kk > 0) ? 1u : 0u;
+              umma_f16(d, ad0 + 2 * kk, bd0 + 2 * kk, idesc, acc);
+            }
+            issued = true;
+            umma_commit(&empty_bar[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
-          issued = true;
-          umma_commit(&empty_bar[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
+        } else {
+          // Packed checksum stages: A(k), A(k+1), enc(k), enc(k+1).
+          for (int kb = w.kb_begin; kb < w.kb_end; kb += 2) {
+            if (!wait_bar(&full_bar[stage], phase, aux, limit)) {
+              if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t st_addr = smem_u32(ring + stage * C::STAGE_BYTES);
+            const int nk = min(2, w.kb_end - kb);
+            for (int j = 0; j < nk; ++j) {
+              const uint32_t a_addr = st_addr + j * C::A_BYTES;
+              const uint32_t b_addr = st_addr + 2 * C::A_BYTES + j * C::ENC_SLOT;
+#pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk) {
+                const uint64_t ad = sdesc_sw128(a_addr + kk * 32);
+                const uint64_t bd = sdesc_sw128(b_addr + kk * 32);
+                const uint32_t acc = (kb > w.kb_begin || j > 0 || kk > 0) ? 1u : 0u;
+                umma_f16(d, ad, bd, idesc, acc);
+              }
+            }
+            issued = true;
+            umma_commit(&empty_bar[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
         if (!ok) break;
