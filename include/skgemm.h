@@ -143,7 +143,15 @@ typedef struct {
                            columns, row by row inside a band (L2 reuse);
                            0 = chosen by the library; >= the number of tile
                            columns = plain row-major order */
-  int32_t reserved1;
+  int32_t cta_pair;     /* 0 = the library decides (pairs when their 256 x 256
+                           tiles fill every resident cluster and neither grid
+                           nor BLK_N 128 is requested),
+                           1 = single CTAs, 2 = clusters of two CTAs that run
+                           256 x 256 tiles with one M = 256 tcgen05 MMA (each
+                           CTA loads its 128 rows of A and half of B per
+                           k-step); requires BLK_N 256, and with ABFT the
+                           checksum GEMMs then run as separate launches.
+                           `grid` counts CTAs and must then be even. */
 } skg_opts_t;
 
 /* One segment of a schedule (Stream-K page, Algorithm 5 / §5.2). k_iter_*

@@ -60,7 +60,9 @@ int sm_count_cached() {
 
 struct Resolved {
   int sched;
-  int grid;
+  int grid;     // CTAs launched for the output tiles (two per cluster with pairs)
+  int pair;     // 1: clusters of two CTAs, 256 x BLK_N tiles, one M = 256 MMA
+  int grid_max; // CTAs that can be resident (pairs: two per resident cluster)
   int grid_ck;  // dedicated checksum-tile CTAs launched after the grid ones
   int bn;
   int abft;
@@ -98,7 +100,36 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
   r.grid = pl.grid;
   r.grid_ck = 0;
   r.bn = pl.bn;
-  r.ws_grid = r.abft ? ms : r.grid;
+  r.pair = 0;
+  r.grid_max = ms;
+  if (o->cta_pair < 0 || o->cta_pair > 2) return SKG_ERR_ARG;
+  if (o->cta_pair == 2 && o->tile_n != 0 && o->tile_n != 256) return SKG_ERR_UNSUPPORTED;
+  bool use_pair = o->cta_pair == 2;
+  if (o->cta_pair == 0 && o->grid == 0 && (o->tile_n == 0 || o->tile_n == 256) && sms > 0 &&
+      m > 0 && n > 0 && k > 0) {
+    // Automatic: pairs once their 256 x 256 tiles fill every resident
+    // cluster at least once (measured faster from there; below, a wave of
+    // 128-row tiles on more SMs wins).
+    const int clusters = pair_clusters_resident();
+    const int64_t ptiles = ((m + 2 * kBM - 1) / (2 * kBM)) * ((n + 255) / 256);
+    use_pair = clusters > 0 && ptiles >= clusters;
+  }
+  if (use_pair) {
+    // CTA pairs: the model plans 256-row tiles on the resident clusters.
+    const int clusters = sms > 0 ? pair_clusters_resident() : ms / 2;
+    if (clusters <= 0) return SKG_ERR_UNSUPPORTED;
+    r.grid_max = 2 * clusters;
+    if (o->grid > 0 && (o->grid % 2 != 0 || o->grid / 2 > clusters)) return SKG_ERR_UNSUPPORTED;
+    const int want_pairs = o->grid > 0 ? o->grid / 2 : (want_sched >= 0 ? clusters : 0);
+    const int64_t m_pairs = ((m > 0 ? m : 1) + 2 * kBM - 1) / (2 * kBM) * kBM;
+    const Plan pp = choose_plan(m_pairs, n > 0 ? n : 1, k > 0 ? k : 1, 256, want_sched,
+                                want_pairs, clusters);
+    r.pair = 1;
+    r.bn = 256;
+    r.sched = pp.sched;
+    r.grid = 2 * pp.grid;
+  }
+  r.ws_grid = r.abft ? (ms > r.grid ? ms : r.grid) : r.grid;
   r.k_for_plan = k > 0 ? k : 1;  // ABFT checksum GEMMs may use up to every SM
   r.tau_row = o->tau_row;
   r.tau_col = o->tau_col;
@@ -218,13 +249,13 @@ struct Gemm {
   int in_dtype, out_dtype;
 };
 
-template <int BN, bool ABFT>
+template <int BN, bool ABFT, bool PAIR = false>
 cudaError_t dispatch_out(int out_dtype, const Maps& mp, const KernelParams& p, int grid,
                          cudaStream_t st) {
   switch (out_dtype) {
-    case SKG_OUT_F32: return launch_gemm<BN, ABFT, 0>(mp, p, grid, st);
-    case SKG_OUT_F16: return launch_gemm<BN, ABFT, 1>(mp, p, grid, st);
-    default: return launch_gemm<BN, ABFT, 2>(mp, p, grid, st);
+    case SKG_OUT_F32: return launch_gemm<BN, ABFT, 0, PAIR>(mp, p, grid, st);
+    case SKG_OUT_F16: return launch_gemm<BN, ABFT, 1, PAIR>(mp, p, grid, st);
+    default: return launch_gemm<BN, ABFT, 2, PAIR>(mp, p, grid, st);
   }
 }
 
@@ -248,40 +279,47 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   Maps mp;
   if (make_map(&mp.a, in_t, 2, g.A, (uint64_t)g.k, (uint64_t)g.m, (uint64_t)g.lda, kBK, kBM) !=
           CUDA_SUCCESS ||
-      make_map(&mp.b, in_t, 2, g.B, (uint64_t)g.k, (uint64_t)g.n, (uint64_t)g.ldb, kBK, r.bn) !=
-          CUDA_SUCCESS ||
+      make_map(&mp.b, in_t, 2, g.B, (uint64_t)g.k, (uint64_t)g.n, (uint64_t)g.ldb, kBK,
+               r.pair ? r.bn / 2 : r.bn) != CUDA_SUCCESS ||
       make_map(&mp.c, out_t, out_bytes, g.C, (uint64_t)g.n, (uint64_t)g.m, (uint64_t)g.ldc,
                128 / out_bytes, 32) != CUDA_SUCCESS)
     return SKG_ERR_UNSUPPORTED;
   mp.b128 = mp.be = mp.ea = mp.cr = mp.cc = mp.a;
   int t_ck = 0, ck_cr = 0;
+  // CTA pairs: a side tile is two 128-row checksum tiles, the encoding rows
+  // (the MMA's N) are split between the two CTAs, so N rounds up to 32.
+  const int ck_half = r.pair ? 2 : 1;
+  const int ck_round = r.pair ? 32 : 16;
   if (fuse_ck) {
     const int n_cr = kEncRows * L.tiles_b, n_cc = kEncRows * L.tiles_a;
     if (make_map(&mp.b128, in_t, 2, g.B, (uint64_t)g.k, (uint64_t)g.n, (uint64_t)g.ldb, kBK,
                  kBM) != CUDA_SUCCESS ||
         make_map(&mp.be, in_t, 2, ws + L.enc_b, (uint64_t)L.kp, (uint64_t)n_cr, (uint64_t)L.kp,
-                 kBK, (uint32_t)round_up(n_cr, 16)) != CUDA_SUCCESS ||
+                 kBK, (uint32_t)(round_up(n_cr, ck_round) / ck_half)) != CUDA_SUCCESS ||
         make_map(&mp.ea, in_t, 2, ws + L.enc_a, (uint64_t)L.kp, (uint64_t)n_cc, (uint64_t)L.kp,
-                 kBK, (uint32_t)round_up(n_cc, 16)) != CUDA_SUCCESS ||
+                 kBK, (uint32_t)(round_up(n_cc, ck_round) / ck_half)) != CUDA_SUCCESS ||
         make_map(&mp.cr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws + L.cr, (uint64_t)n_cr,
                  (uint64_t)g.m, (uint64_t)L.ld_cr, 32, 32) != CUDA_SUCCESS ||
         make_map(&mp.cc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws + L.cc, (uint64_t)n_cc,
                  (uint64_t)g.n, (uint64_t)L.ld_cc, 32, 32) != CUDA_SUCCESS)
       return SKG_ERR_UNSUPPORTED;
-    ck_cr = (int)((g.m + kBM - 1) / kBM);
-    t_ck = ck_cr + (int)((g.n + kBM - 1) / kBM);
+    ck_cr = (int)(((g.m + kBM - 1) / kBM + ck_half - 1) / ck_half);
+    t_ck = ck_cr + (int)(((g.n + kBM - 1) / kBM + ck_half - 1) / ck_half);
   }
 
   KernelParams p;
   memset(&p, 0, sizeof(p));
-  p.s = make_schedule(g.m, g.n, g.k, kBM, r.bn, kBK, r.grid, r.sched, t_ck, t_ck ? r.grid_ck : 0);
+  // CTA pairs: 256-row tiles, one schedule CTA per cluster.
+  const int sched_ctas = r.pair ? r.grid / 2 : r.grid;
+  p.s = make_schedule(g.m, g.n, g.k, r.pair ? 2 * kBM : kBM, r.bn, kBK, sched_ctas, r.sched, t_ck,
+                      t_ck ? r.grid_ck : 0);
   const int launch_grid = r.grid + p.s.g_ck;
   // Banded raster: a wave of g tiles covers about (g / band) rows x band
   // columns; band ~ sqrt(g * BLK_M / BLK_N) minimises the A + B bytes one
   // wave touches per k-step.
   int band = r.raster_band;
   if (band == 0) {
-    const double b = sqrt((double)r.grid * kBM / r.bn);
+    const double b = sqrt((double)sched_ctas * (r.pair ? 2 * kBM : kBM) / r.bn);
     band = (int)(b + 0.5);
   }
   if (band < 1) band = 1;
@@ -291,18 +329,18 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   p.k = (int)g.k;
   p.alpha = g.alpha;
   p.beta = g.beta;
-  p.idesc_main = idesc_f16(g.in_dtype == SKG_IN_BF16, kBM, r.bn);
+  p.idesc_main = idesc_f16(g.in_dtype == SKG_IN_BF16, r.pair ? 2 * kBM : kBM, r.bn);
   p.ck_cr_tiles = ck_cr;
   p.ck_n_cr = kEncRows * L.tiles_b;
   p.ck_n_cc = kEncRows * L.tiles_a;
-  p.ck_rows_cr = (int)round_up(p.ck_n_cr, 16);
-  p.ck_rows_cc = (int)round_up(p.ck_n_cc, 16);
+  p.ck_rows_cr = (int)round_up(p.ck_n_cr, ck_round);
+  p.ck_rows_cc = (int)round_up(p.ck_n_cc, ck_round);
   // Two checksum k-blocks per ring stage when the encoding box fits its
   // 8 KB slot (64 rows of 128 bytes) and the stage holds two A tiles.
-  p.ck_kpack_cr = (r.bn == 256 && p.ck_rows_cr <= 64) ? 2 : 1;
-  p.ck_kpack_cc = (r.bn == 256 && p.ck_rows_cc <= 64) ? 2 : 1;
-  p.idesc_cr = idesc_f16(g.in_dtype == SKG_IN_BF16, kBM, (uint32_t)round_up(p.ck_n_cr, 16));
-  p.idesc_cc = idesc_f16(g.in_dtype == SKG_IN_BF16, kBM, (uint32_t)round_up(p.ck_n_cc, 16));
+  p.ck_kpack_cr = (!r.pair && r.bn == 256 && p.ck_rows_cr <= 64) ? 2 : 1;
+  p.ck_kpack_cc = (!r.pair && r.bn == 256 && p.ck_rows_cc <= 64) ? 2 : 1;
+  p.idesc_cr = idesc_f16(g.in_dtype == SKG_IN_BF16, ck_half * kBM, (uint32_t)p.ck_rows_cr);
+  p.idesc_cc = idesc_f16(g.in_dtype == SKG_IN_BF16, ck_half * kBM, (uint32_t)p.ck_rows_cc);
   p.hdr = (WsHeader*)ws;
   p.report = (skg_report_t*)(ws + 256);
   p.flags = (uint32_t*)(ws + L.flags);
@@ -329,7 +367,10 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   p.drop_signal = r.drop_signal;
 
   cudaError_t e;
-  if (r.bn == 128)
+  if (r.pair)
+    e = abft_epilogue ? dispatch_out<256, true, true>(g.out_dtype, mp, p, launch_grid, stream)
+                      : dispatch_out<256, false, true>(g.out_dtype, mp, p, launch_grid, stream);
+  else if (r.bn == 128)
     e = abft_epilogue ? dispatch_out<128, true>(g.out_dtype, mp, p, launch_grid, stream)
                       : dispatch_out<128, false>(g.out_dtype, mp, p, launch_grid, stream);
   else
@@ -354,6 +395,7 @@ skg_status_t reference_checksums(const Gemm& g, const Resolved& r, uint8_t* ws, 
   }
   Resolved rc = r;
   rc.abft = 0;
+  rc.pair = 0;
   rc.inject_tile = -1;
   rc.trace = nullptr;
   rc.cta_clock = nullptr;
@@ -385,8 +427,22 @@ void replan_fused(int64_t m, int64_t n, const skg_opts_t* opts, Resolved& r) {
     opts = &d;
   }
   if (opts->grid != 0) return;
-  const int t_ck = (int)((m + kBM - 1) / kBM + (n + kBM - 1) / kBM);
   const int want_sched = opts->sched == SKG_SCHED_AUTO ? -1 : opts->sched;
+  if (r.pair) {
+    // 256-row tiles and pair side tiles on the resident clusters; the side
+    // tiles are always split over the grid (no dedicated CTAs).
+    const int clusters = r.grid_max / 2;
+    const int64_t tm = (m + kBM - 1) / kBM, tn = (n + kBM - 1) / kBM;
+    const int t_ck = (int)((tm + 1) / 2 + (tn + 1) / 2);
+    const int64_t m_pairs = (m + 2 * kBM - 1) / (2 * kBM) * kBM;
+    const Plan pp = choose_plan(m_pairs, n, r.k_for_plan, 256, want_sched,
+                                want_sched >= 0 ? clusters : 0, clusters, t_ck, false);
+    r.grid = 2 * pp.grid;
+    r.sched = pp.sched;
+    r.grid_ck = 0;
+    return;
+  }
+  const int t_ck = (int)((m + kBM - 1) / kBM + (n + kBM - 1) / kBM);
   const Plan pl = choose_plan(m, n, r.k_for_plan, r.bn, want_sched,
                               want_sched >= 0 ? r.ws_grid : 0, r.ws_grid, t_ck);
   r.grid = pl.grid;

@@ -6,9 +6,9 @@
 
 namespace skg {
 
-template <int BN, bool ABFT, int OUT>
+template <int BN, bool ABFT, int OUT, bool PAIR>
 cudaError_t launch_gemm(const Maps& mp, const KernelParams& p, int grid, cudaStream_t stream) {
-  using C = Cfg<BN, ABFT, OUT>;
+  using C = Cfg<BN, ABFT, OUT, PAIR>;
   // The shared-memory opt-in is per device; set it once per device.
   static std::atomic<uint64_t> done_mask{0};
   int dev = 0;
@@ -21,8 +21,9 @@ cudaError_t launch_gemm(const Maps& mp, const KernelParams& p, int grid, cudaStr
     if (e != cudaSuccess) return e;
     done_mask.fetch_or(bit, std::memory_order_acq_rel);
   }
-  return launch_pdl(skg_gemm_kernel<C>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, stream, mp.a,
-                    mp.b, mp.c, mp.b128, mp.be, mp.ea, mp.cr, mp.cc, p);
+  return launch_pdl_cluster(skg_gemm_kernel<C>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, stream,
+                            PAIR ? 2 : 1, mp.a, mp.b, mp.c, mp.b128, mp.be, mp.ea, mp.cr, mp.cc,
+                            p);
 }
 
 #define SKG_INST(OUT)                                                                        \

@@ -1,0 +1,69 @@
+// Instantiations of the CTA-pair persistent kernel (256 x 256 tiles per
+// cluster of two) for ABFT = 0
+// (one translation unit each so the build compiles them in parallel).
+#include <atomic>
+
+#include "skg_internal.h"
+
+namespace skg {
+
+template <int BN, bool ABFT, int OUT, bool PAIR>
+cudaError_t launch_gemm(const Maps& mp, const KernelParams& p, int grid, cudaStream_t stream) {
+  using C = Cfg<BN, ABFT, OUT, PAIR>;
+  // The shared-memory opt-in is per device; set it once per device.
+  static std::atomic<uint64_t> done_mask{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (!bit || !(done_mask.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(skg_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    done_mask.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  return launch_pdl_cluster(skg_gemm_kernel<C>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, stream,
+                            PAIR ? 2 : 1, mp.a, mp.b, mp.c, mp.b128, mp.be, mp.ea, mp.cr, mp.cc,
+                            p);
+}
+
+#define SKG_INST(OUT)                                                                        \
+  template cudaError_t launch_gemm<256, false, OUT, true>( \
+      const Maps&, const KernelParams&, int, cudaStream_t);
+SKG_INST(0)
+SKG_INST(1)
+SKG_INST(2)
+
+}  // namespace skg
+
+namespace skg {
+
+int pair_clusters_resident() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int have = cached[dev].load(std::memory_order_acquire);
+  if (have != 0) return have > 0 ? have : 0;
+  using C = Cfg<256, false, 2, true>;
+  int n = 0;
+  if (cudaFuncSetAttribute(skg_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)C::SMEM_BYTES) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 256);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, skg_gemm_kernel<C>, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  cached[dev].store(n > 0 ? n : -1, std::memory_order_release);
+  return n;
+}
+
+}  // namespace skg

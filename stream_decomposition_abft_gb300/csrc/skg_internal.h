@@ -10,24 +10,38 @@ namespace skg {
 // Launch with programmatic stream serialization: the kernel may begin while
 // the previous kernel in the stream finishes; every kernel of this library
 // calls griddepcontrol.wait before it reads anything an earlier kernel wrote.
+// `cluster` > 1 launches clusters of that many CTAs along x.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t stream, Args... args) {
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t stream, int cluster, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-#ifdef SKG_NO_PDL
-  cfg.numAttrs = 0;  // build variant without programmatic dependent launch
-#else
-  cfg.numAttrs = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+#ifndef SKG_NO_PDL
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
 #endif
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  return launch_pdl_cluster(kernel, grid, block, smem, stream, 1, args...);
 }
 
 // TMA descriptors of one launch: A (box 64 x 128), B (64 x BLK_N), C (store
@@ -38,10 +52,15 @@ struct Maps {
   CUtensorMap a, b, c, b128, be, ea, cr, cc;
 };
 
-// Launch the persistent kernel instantiated for (BN, ABFT, OUT) on `grid`
-// CTAs. Defined in the skg_inst_*.cu translation units.
-template <int BN, bool ABFT, int OUT>
+// Launch the persistent kernel instantiated for (BN, ABFT, OUT, PAIR) on
+// `grid` CTAs (PAIR: grid / 2 clusters of two). Defined in the
+// skg_inst_*.cu translation units.
+template <int BN, bool ABFT, int OUT, bool PAIR = false>
 cudaError_t launch_gemm(const Maps& mp, const KernelParams& p, int grid, cudaStream_t stream);
+
+// Clusters of two CTAs of the pair kernel (BLK_N = 256) that can be resident
+// at once on the current device; 0 when unavailable.
+int pair_clusters_resident();
 
 // ABFT encode pass (skg_encode.cu): e^T A per 128-row tile of A and B e
 // per bn-row tile of the stored n x k B, as hi / lo rows in the input type

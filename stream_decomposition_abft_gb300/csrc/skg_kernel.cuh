@@ -109,6 +109,8 @@ struct KernelParams {
   // Tile j < ck_cr_tiles computes rows [128 j, 128 j + 128) of
   // cr_all = A x [Be_hi; Be_lo]^T (ck_n_cr columns); the others compute rows
   // of ccT_all = B x [eA_hi; eA_lo]^T (ck_n_cc columns). Both store fp32.
+  // With CTA pairs a side tile is two such 128-row tiles (2j for the leader,
+  // 2j + 1 for its peer), and each CTA loads half of the encoding rows.
   int ck_cr_tiles;
   int ck_n_cr, ck_n_cc;
   int ck_rows_cr, ck_rows_cc;  // encoding rows loaded per k-step (N rounded up to 16)
@@ -131,23 +133,27 @@ __host__ __device__ constexpr int pow2_at_least(int v) {
   return p;
 }
 
-template <int BN_, bool ABFT_, int OUT_>
+template <int BN_, bool ABFT_, int OUT_, bool PAIR_ = false>
 struct Cfg {
   static constexpr int BN = BN_;
   static constexpr bool ABFT = ABFT_;
   static constexpr int OUT = OUT_;  // 0 = f32, 1 = f16, 2 = bf16
+  // CTA pairs: a cluster of two CTAs runs 256 x BN tiles with one M = 256
+  // MMA; each CTA loads its 128 rows of A and BN / 2 rows of B per stage.
+  static constexpr bool PAIR = PAIR_;
   static constexpr int OUT_BYTES = OUT == 0 ? 4 : 2;
   static constexpr int EPI_COLS = 128 / OUT_BYTES;  // one 128-byte staging row
   static constexpr int ACC_COLS = BN;
   static constexpr int ACC_BUFS = (2 * ACC_COLS <= 512) ? 2 : 1;
   static constexpr int TMEM_COLS = pow2_at_least(ACC_BUFS * ACC_COLS);
   static constexpr int A_BYTES = kBM * kBK * 2;
-  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
+  static constexpr int B_BYTES = B_ROWS * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES;
   // Packed checksum stage: two A tiles, then two encoding slots of ENC_SLOT bytes.
   static constexpr int ENC_SLOT = 8192;
-  static constexpr bool CK_PACK = STAGE_BYTES >= 2 * A_BYTES + 2 * ENC_SLOT;
+  static constexpr bool CK_PACK = !PAIR && STAGE_BYTES >= 2 * A_BYTES + 2 * ENC_SLOT;
   static constexpr int EPI_BUF_BYTES = 32 * 128;
   static constexpr int EPI_BUFS = 2;
   static constexpr int EPI_BYTES = 4 * EPI_BUFS * EPI_BUF_BYTES;
@@ -193,11 +199,15 @@ __device__ __forceinline__ bool aborted(Aux* aux) {
 // Drains (copies or MMAs this thread issued) pass honor_abort = false so
 // they always wait for their own operations, up to the time limit.
 static __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Aux* aux,
-                                             uint64_t limit_ns, bool honor_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                             uint64_t limit_ns, bool honor_abort = true,
+                                             bool cluster_scope = false) {
+  auto ready = [&]() {
+    return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (ready()) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (ready()) return true;
     if ((i & 31) == 0) {
       if (honor_abort && aborted(aux)) return false;
       if (globaltimer() - t0 > limit_ns) return false;
@@ -207,12 +217,18 @@ static __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Aux
 
 // wait_bar, inlined: loads issued before it stay in flight during the wait
 // (a call would make the compiler wait for them first).
+template <bool CLUSTER>
+__device__ __forceinline__ bool try_wait_scoped(uint64_t* bar, uint32_t parity) {
+  return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+}
+
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bar_inline(uint64_t* bar, uint32_t parity, Aux* aux,
                                                 uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (try_wait_scoped<CLUSTER>(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_wait_scoped<CLUSTER>(bar, parity)) return true;
     if ((i & 31) == 0) {
       if (aborted(aux)) return false;
       if (globaltimer() - t0 > limit_ns) return false;
@@ -339,13 +355,14 @@ __device__ __forceinline__ float* partial_at(float* slot, int c4, int r) {
 // peers waits for one L2 round trip per group rather than per peer.
 template <int BN>
 __device__ __forceinline__ void add_peer_partials(float (&v)[32], float* partials, int first,
-                                                  int last, int c32, int r) {
+                                                  int last, int c32, int r, int slot_stride = 1,
+                                                  int slot_offset = 0) {
   int peer = first;
   for (; peer + 3 <= last; peer += 4) {
     float4 t[4][8];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      float* ps = partials + (size_t)(peer + u) * kBM * BN;
+      float* ps = partials + (size_t)((peer + u) * slot_stride + slot_offset) * kBM * BN;
 #pragma unroll
       for (int j = 0; j < 8; ++j) t[u][j] = ld_cg_f4(partial_at(ps, c32 * 8 + j, r));
     }
@@ -361,7 +378,7 @@ __device__ __forceinline__ void add_peer_partials(float (&v)[32], float* partial
   }
   for (; peer <= last; ++peer) {
     float4 t[8];
-    float* ps = partials + (size_t)peer * kBM * BN;
+    float* ps = partials + (size_t)(peer * slot_stride + slot_offset) * kBM * BN;
 #pragma unroll
     for (int j = 0; j < 8; ++j) t[j] = ld_cg_f4(partial_at(ps, c32 * 8 + j, r));
 #pragma unroll
@@ -403,6 +420,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const Schedule& s = p.s;
   const uint64_t limit = p.timeout_ns;
+  // CTA pairs: rank within the cluster (0 = leader, which issues the MMAs)
+  // and the schedule's CTA index, shared by both CTAs of a pair.
+  const uint32_t crank = C::PAIR ? cluster_ctarank() : 0u;
+  const bool leader = crank == 0;
+  const int unit = C::PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  // This CTA's flag and partial slot, and its row offset inside a tile.
+  const int slot_stride = C::PAIR ? 2 : 1;
+  const int my_slot_idx = unit * slot_stride + (int)crank;
+  const int row_half = (int)crank * kBM;
+  constexpr int kCkHalf = C::PAIR ? 2 : 1;  // 128-row checksum tiles per side tile
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
@@ -421,7 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull_bar[i], 1);
-      mbar_init(&tempty_bar[i], kEpiThreads);
+      // A pair's accumulator is released by the epilogue threads of both CTAs.
+      mbar_init(&tempty_bar[i], C::PAIR ? 2 * kEpiThreads : kEpiThreads);
     }
     for (int i = 0; i < 4; ++i) mbar_init(&c0_bar[i], 1);
     mbar_init(drain_bar, 1);
@@ -431,11 +459,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&aux->tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (C::PAIR) {
+      tmem_alloc_pair(&aux->tmem_slot, C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&aux->tmem_slot, C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  // A pair's barriers must be initialised before the peer signals them.
+  if constexpr (C::PAIR) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = aux->tmem_slot;
   // Everything above touched only this CTA's shared memory and TMEM; from
@@ -451,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       Cursor cur;
-      cur.init(s, blockIdx.x);
+      cur.init(s, unit);
       Work w;
       int stage = 0;
       uint32_t phase = 0;
@@ -469,32 +504,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w.tile >= s.t_ck) {
           int tm, tn;
           tile_coords(s, w.tile, tm, tn);
-          rowA = tm * kBM;
-          rowB = tn * BN;
+          rowA = tm * (C::PAIR ? 2 * kBM : kBM) + row_half;
+          rowB = tn * BN + (C::PAIR ? (int)crank * C::B_ROWS : 0);
         } else if (w.tile < p.ck_cr_tiles) {
           // Checksum tile: the encoding box holds only the rows the MMA uses.
           mapB = &tmBE;
-          rowA = w.tile * kBM;
-          rowB = 0;
-          tx = C::A_BYTES + p.ck_rows_cr * kBK * 2;
+          rowA = (w.tile * kCkHalf + (int)crank) * kBM;
+          rowB = (int)crank * (p.ck_rows_cr / kCkHalf);
+          tx = C::A_BYTES + p.ck_rows_cr / kCkHalf * kBK * 2;
           kpack = C::CK_PACK ? p.ck_kpack_cr : 1;
         } else {
           mapA = &tmB128;
           mapB = &tmEA;
-          rowA = (w.tile - p.ck_cr_tiles) * kBM;
-          rowB = 0;
-          tx = C::A_BYTES + p.ck_rows_cc * kBK * 2;
+          rowA = ((w.tile - p.ck_cr_tiles) * kCkHalf + (int)crank) * kBM;
+          rowB = (int)crank * (p.ck_rows_cc / kCkHalf);
+          tx = C::A_BYTES + p.ck_rows_cc / kCkHalf * kBK * 2;
           kpack = C::CK_PACK ? p.ck_kpack_cc : 1;
         }
         for (int kb = w.kb_begin; kb < w.kb_end; kb += kpack) {
-          if (!mbar_try_wait(&empty_bar[stage], phase ^ 1) &&
-              !wait_bar(&empty_bar[stage], phase ^ 1, aux, limit)) {
+          if (!try_wait_scoped<C::PAIR>(&empty_bar[stage], phase ^ 1) &&
+              !wait_bar(&empty_bar[stage], phase ^ 1, aux, limit, true, C::PAIR)) {
             if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
             ok = false;
             break;
           }
           uint8_t* st = ring + stage * C::STAGE_BYTES;
-          if (kpack == 1) {
+          if constexpr (C::PAIR) {
+            // Both CTAs' copies complete on the leader's full barrier; the
+            // leader expects the pair's bytes.
+            const uint32_t fb = cluster_addr(&full_bar[stage], 0);
+            if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * tx);
+            tma_load_2d_pair(st, mapA, fb, kb * kBK, rowA);
+            tma_load_2d_pair(st + C::A_BYTES, mapB, fb, kb * kBK, rowB);
+          } else if (kpack == 1) {
             mbar_arrive_expect_tx(&full_bar[stage], tx);
             tma_load_2d(st, mapA, &full_bar[stage], kb * kBK, rowA);
             tma_load_2d(st + C::A_BYTES, mapB, &full_bar[stage], kb * kBK, rowB);
@@ -507,8 +549,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                           (kb + j) * kBK, rowB);
             }
           }
-          pending |= 1u << stage;
-          pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+          if (leader) {
+            pending |= 1u << stage;
+            pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -522,13 +566,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (one thread; in a CTA pair only the leader's issues, for both CTAs)
+    if (lane == 0 && leader) {
       // Shared-memory descriptor of the ring's first byte; the ring lies in
       // the first 256 KB of shared memory, so adding (offset >> 4) to the
       // 14-bit address field never carries out of it.
       const uint64_t ring_desc = sdesc_sw128(smem_u32(ring));
       Cursor cur;
-      cur.init(s, blockIdx.x);
+      cur.init(s, unit);
       Work w;
       int stage = 0;
       uint32_t phase = 0;
@@ -537,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       bool issued = false;
       while (ok && cur.next(s, w)) {
-        if (!wait_bar(&tempty_bar[ab], aphase ^ 1, aux, limit)) {
+        if (!wait_bar(&tempty_bar[ab], aphase ^ 1, aux, limit, true, C::PAIR)) {
           if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
           break;
         }
@@ -564,10 +609,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               const uint32_t acc = (kb > w.kb_begin || kk > 0) ? 1u : 0u;
-              umma_f16(d, ad0 + 2 * kk, bd0 + 2 * kk, idesc, acc);
+              if constexpr (C::PAIR) umma_f16_pair(d, ad0 + 2 * kk, bd0 + 2 * kk, idesc, acc);
+              else umma_f16(d, ad0 + 2 * kk, bd0 + 2 * kk, idesc, acc);
             }
             issued = true;
-            umma_commit(&empty_bar[stage]);
+            if constexpr (C::PAIR) umma_commit_pair(&empty_bar[stage]);  // both CTAs' stage
+            else umma_commit(&empty_bar[stage]);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1;
@@ -604,7 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        umma_commit(&tfull_bar[ab]);
+        if constexpr (C::PAIR) umma_commit_pair(&tfull_bar[ab]);  // both CTAs' accumulator
+        else umma_commit(&tfull_bar[ab]);
         if (++ab == ACC_BUFS) {
           ab = 0;
           aphase ^= 1;
@@ -612,8 +660,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (issued) {
         // All MMAs this thread issued complete before TMEM is released.
-        umma_commit(drain_bar);
-        wait_bar(drain_bar, 0, aux, limit, false);
+        if constexpr (C::PAIR) umma_commit_pair(drain_bar);
+        else umma_commit(drain_bar);
+        wait_bar(drain_bar, 0, aux, limit, false, C::PAIR);
       }
     }
     __syncwarp();
@@ -630,9 +679,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       return reinterpret_cast<float*>(epi + ew_of_q * C::EPI_BUFS * C::EPI_BUF_BYTES);
     };
     const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr->epoch) + 1u;
+    // Hand an accumulator buffer back to the MMA thread (the leader's, for
+    // a CTA pair).
+    auto release_acc = [&](int b) {
+      if constexpr (C::PAIR) mbar_arrive_cluster(cluster_addr(&tempty_bar[b], 0));
+      else mbar_arrive(&tempty_bar[b]);
+    };
 
     Cursor cur;
-    cur.init(s, blockIdx.x);
+    cur.init(s, unit);
     Work w;
     int ab = 0;
     uint32_t aphase = 0;
@@ -656,6 +711,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool is_ck = w.tile < s.t_ck;  // a fused checksum-GEMM tile
       int tm = 0, tn = 0;
       if (!is_ck) tile_coords(s, w.tile, tm, tn);
+      // This CTA's 128-row tile: a pair tile is two of them.
+      if (C::PAIR) tm = 2 * tm + (int)crank;
       const int m0 = tm * kBM;
       const int n0 = tn * BN;
 
@@ -668,7 +725,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int h = 0; h < BN / 128; ++h) pf_cc0[h] = pf_cc1[h] = 0.f;
       int pf_ea = 0, pf_eb = 0;
-      if (C::ABFT && !is_ck && w.role != kRolePeer) {
+      // (A CTA pair's second half lies past m when m has an odd number of
+      // 128-row tiles: nothing there to check.)
+      const bool verify_here = C::ABFT && !is_ck && w.role != kRolePeer && m0 < p.m;
+      if (verify_here) {
         if (s.t_ck > 0 && !ck_ready) {
           // The fused checksum tiles must all be stored first. Every CTA runs
           // its own share of them before its first output tile, and dedicated
@@ -676,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool fine = true;
           if (et == 0) {
             const uint64_t t0 = globaltimer();
-            while (ld_acquire_gpu(&p.hdr->ck_done) < (uint32_t)s.t_ck) {
+            while (ld_acquire_gpu(&p.hdr->ck_done) < (uint32_t)(kCkHalf * s.t_ck)) {
               nanosleep_ns(128);
               if (globaltimer() - t0 > limit) {
                 record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
@@ -717,17 +777,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
-      bool got = wait_bar_inline(&tfull_bar[ab], aphase, aux, limit);
+      bool got = wait_bar_inline<C::PAIR>(&tfull_bar[ab], aphase, aux, limit);
       if (!got && !aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
       if (!epi_all(got && store_ok && !aborted(aux))) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + ab * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
-      const int out_tile = w.tile - s.t_ck;  // output-tile number the caller sees
+      const int out_tile = tm * s.tiles_n + tn;  // row-major 128 x BLK_N tile number
       const bool inject_here = !is_ck && (out_tile == p.inject_tile) && (w.role != kRolePeer);
       // This segment's region of fixup storage.
       uint32_t* rflags = p.flags + (size_t)w.region * p.ws_ctas;
       float* rpartials = p.partials + (size_t)w.region * p.ws_ctas * kBM * BN;
-      float* my_slot = rpartials + (size_t)blockIdx.x * kBM * BN;
+      float* my_slot = rpartials + (size_t)my_slot_idx * kBM * BN;
       // Columns of the accumulator that carry data: a checksum tile uses
       // only its first ck_n_* columns.
       const int live_chunks =
@@ -747,11 +807,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  f32_of(u[4 * j + 3])));
         }
         tc_fence_before();
-        mbar_arrive(&tempty_bar[ab]);
+        release_acc(ab);
         named_bar_sync(1, kEpiThreads);
         if (et == 0 && (int)blockIdx.x != p.drop_signal) {
           __threadfence();
-          st_release_gpu(&rflags[blockIdx.x], epoch);
+          st_release_gpu(&rflags[my_slot_idx], epoch);
         }
       } else {
         const bool owner = (w.role == kRoleOwner);
@@ -759,11 +819,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Wait for every later CTA that covers part of this tile.
           bool fine = true;
           if (et == 0) {
-            for (int peer = blockIdx.x + 1; peer <= w.peer_last && fine; ++peer) {
-              if (ld_acquire_gpu(&rflags[peer]) == epoch) continue;
+            for (int peer = unit + 1; peer <= w.peer_last && fine; ++peer) {
+              const int fi = peer * slot_stride + (int)crank;
+              if (ld_acquire_gpu(&rflags[fi]) == epoch) continue;
               const uint64_t t0 = globaltimer();
               uint32_t spins = 0;
-              while (ld_acquire_gpu(&rflags[peer]) != epoch) {
+              while (ld_acquire_gpu(&rflags[fi]) != epoch) {
                 if (++spins > 64) nanosleep_ns(64);
                 if ((spins & 15) == 0 && globaltimer() - t0 > limit) {
                   record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
@@ -775,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!epi_all(fine && !aborted(aux))) {
             tc_fence_before();
-            mbar_arrive(&tempty_bar[ab]);
+            release_acc(ab);
             break;
           }
         }
@@ -788,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const CUtensorMap* mapC = cr_side ? &tmCr : &tmCc;
           const int rows = cr_side ? p.m : p.n;
           const int ncols = cr_side ? p.ck_n_cr : p.ck_n_cc;
-          const int r0 = (cr_side ? w.tile : w.tile - p.ck_cr_tiles) * kBM;
+          const int r0 = ((cr_side ? w.tile : w.tile - p.ck_cr_tiles) * kCkHalf + (int)crank) * kBM;
           const int nchunks = (ncols + 31) / 32;
           const bool live = (r0 + q * 32) < rows;
 #pragma unroll 1
@@ -798,10 +859,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tacc + c * 32, u);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
-            if (owner) add_peer_partials<BN>(v, rpartials, blockIdx.x + 1, w.peer_last, c, r);
+            if (owner) add_peer_partials<BN>(v, rpartials, unit + 1, w.peer_last, c, r, slot_stride,
+                                            (int)crank);
             if (c == nchunks - 1) {
               tc_fence_before();
-              mbar_arrive(&tempty_bar[ab]);
+              release_acc(ab);
             }
             if (!live || !store_ok) continue;  // warp-uniform
             uint8_t* buf = ebuf + bsel * C::EPI_BUF_BYTES;
@@ -836,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ ABFT verify
         int fix_row = -1, fix_col = -1;
         float fix_val = 0.f;
-        if (C::ABFT) {
+        if (verify_here) {
           // This warp's staging buffers hold its column sums below: its own
           // earlier TMA stores must have finished reading them.
           if (lane == 0) bulk_wait_read<0>();
@@ -850,7 +912,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
-            if (owner) add_peer_partials<BN>(v, rpartials, blockIdx.x + 1, w.peer_last, c32, r);
+            if (owner) add_peer_partials<BN>(v, rpartials, unit + 1, w.peer_last, c32, r, slot_stride,
+                                            (int)crank);
             // Fault injection: one bit of one fp32 accumulator, after the
             // fixup and before the check (warp-uniform chunk selection).
             const bool inj_chunk = inject_here && (p.inject_row >> 5) == q &&
@@ -1041,7 +1104,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
             if (!C::ABFT && owner)
-              add_peer_partials<BN>(v, rpartials, blockIdx.x + 1, w.peer_last, c32, r);
+              add_peer_partials<BN>(v, rpartials, unit + 1, w.peer_last, c32, r, slot_stride,
+                                            (int)crank);
 #pragma unroll
             for (int i = 0; i < 32; ++i) y[hh * 32 + i] = v[i];
             if (!C::ABFT) {
@@ -1063,7 +1127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c == BN / C::EPI_COLS - 1) {
             // Accumulator fully read: hand the TMEM buffer back to the MMA warp.
             tc_fence_before();
-            mbar_arrive(&tempty_bar[ab]);
+            release_acc(ab);
           }
           const int col0 = n0 + c * C::EPI_COLS;
           if (!rows_live || col0 >= p.n || !store_ok) continue;  // warp-uniform
@@ -1115,9 +1179,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (C::PAIR) {
+    // A peer's copies complete on the leader's barriers, so after an abort
+    // this CTA cannot see its own copies land: give them time before the
+    // pair parts. Then neither CTA leaves while the other may still signal
+    // its barriers or read its shared memory.
+    if (aborted(aux)) {
+      const uint64_t t0 = globaltimer();
+      while (globaltimer() - t0 < 100000) nanosleep_ns(1000);
+    }
+    cluster_sync();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (C::PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
   if (threadIdx.x == 0) {
     if (p.cta_clock) p.cta_clock[2 * blockIdx.x + 1] = globaltimer();

@@ -89,7 +89,7 @@ struct Plan {
 // Best (BLK_N, schedule, g) for an m x n x k launch on `sms` SMs. Fixed
 // choices (want_* != 0 / >= 0) are kept; the rest are searched.
 inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_sched,
-                        int want_grid, int sms, int t_ck) {
+                        int want_grid, int sms, int t_ck, bool side_ctas = true) {
   static const int kCands[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 76, 96, 112, 128, 144};
   Plan best{want_bn ? want_bn : 256, want_sched >= 0 ? want_sched : kSchedSK2DP,
             want_grid ? want_grid : sms, 1e300, 0};
@@ -127,7 +127,7 @@ inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_s
         // Side tiles split over the grid, or (automatic grid only) one each
         // on SMs the grid leaves idle: every verification waits for all side
         // tiles, so they must end with the output CTAs' first tiles.
-        const int spare = want_grid ? 0 : sms - cands[i];
+        const int spare = (want_grid || !side_ctas) ? 0 : sms - cands[i];
         const int gck_opts[2] = {0, t_ck <= spare ? t_ck : 0};
         for (int oi = 0; oi < (gck_opts[1] > 0 ? 2 : 1); ++oi) {
           const int gck = gck_opts[oi];
@@ -149,32 +149,32 @@ inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_s
 // search_plan behind a small cache: the search walks up to ~150 candidate
 // schedules of up to `sms` CTAs each, far more host time than a launch.
 inline Plan choose_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_sched,
-                        int want_grid, int sms, int t_ck = 0) {
+                        int want_grid, int sms, int t_ck = 0, bool side_ctas = true) {
   struct Key {
     int64_t m, n, k;
-    int bn, sched, grid, sms, t_ck;
+    int bn, sched, grid, sms, t_ck, side;
     bool operator==(const Key& o) const {
       return m == o.m && n == o.n && k == o.k && bn == o.bn && sched == o.sched &&
-             grid == o.grid && sms == o.sms && t_ck == o.t_ck;
+             grid == o.grid && sms == o.sms && t_ck == o.t_ck && side == o.side;
     }
   };
   struct Hash {
     size_t operator()(const Key& x) const {
       uint64_t h = 1469598103934665603ull;
-      const int64_t v[8] = {x.m, x.n, x.k, x.bn, x.sched, x.grid, x.sms, x.t_ck};
+      const int64_t v[9] = {x.m, x.n, x.k, x.bn, x.sched, x.grid, x.sms, x.t_ck, x.side};
       for (int64_t e : v) h = (h ^ (uint64_t)e) * 1099511628211ull;
       return (size_t)h;
     }
   };
   static std::mutex mu;
   static std::unordered_map<Key, Plan, Hash> cache;
-  const Key key{m, n, k, want_bn, want_sched, want_grid, sms, t_ck};
+  const Key key{m, n, k, want_bn, want_sched, want_grid, sms, t_ck, side_ctas ? 1 : 0};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
-  const Plan p = search_plan(m, n, k, want_bn, want_sched, want_grid, sms, t_ck);
+  const Plan p = search_plan(m, n, k, want_bn, want_sched, want_grid, sms, t_ck, side_ctas);
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();
   cache.emplace(key, p);

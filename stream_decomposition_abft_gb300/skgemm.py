@@ -41,7 +41,7 @@ class Opts(ctypes.Structure):
                 ("inject_bit", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64),
                 ("trace", ctypes.c_void_p), ("cta_clock", ctypes.c_void_p),
                 ("test_drop_signal", ctypes.c_int32), ("abft_preencoded", ctypes.c_int32),
-                ("raster_band", ctypes.c_int32), ("reserved1", ctypes.c_int32)]
+                ("raster_band", ctypes.c_int32), ("cta_pair", ctypes.c_int32)]
 
 
 class Segment(ctypes.Structure):

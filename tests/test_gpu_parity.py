@@ -347,3 +347,80 @@ def test_abft_f16_large_encodings(tile_n):
     assert rep.detected == 1 and rep.corrected == 1
     assert (rep.records[0].tile, rep.records[0].row, rep.records[0].col) == (3, 9, 17)
     check_full(p, C, ref)
+
+
+# --------------------------------------------------------------------------- CTA pairs
+@pytest.mark.parametrize("shape", [(256, 256, 64), (384, 512, 320), (1000, 1300, 520),
+                                   (2048, 1536, 1024), (129, 3000, 256)])
+@pytest.mark.parametrize("mode", ["dp", "sk", "sk2_dp"])
+def test_cta_pairs_parity(shape, mode):
+    # Clusters of two CTAs (256 x 256 tiles, one M = 256 MMA): element-wise
+    # parity, ragged m (an odd number of 128-row tiles leaves the last pair's
+    # second half empty), ragged n and k, alpha / beta.
+    m, n, k = shape
+    p = inputs.make_problem(m, n, k, seed=m * 7 + n, in_dtype="bf16", out_dtype="f32",
+                            law_a="normal", law_b="normal", alpha=0.75, beta=0.5)
+    opts = skgemm.opts_default(sched=mode, cta_pair=2)
+    tile_n, grid, _ = skgemm.launch_shape(m, n, k, opts)
+    assert tile_n == 256 and grid % 2 == 0
+    C, ws, st = run(p, opts)
+    assert st == skgemm.OK
+    check_full(p, C)
+    assert ws.report().status_bits == 0
+
+
+@pytest.mark.parametrize("out", ["f16", "bf16"])
+def test_cta_pairs_fp16_outputs(out):
+    p = inputs.make_problem(640, 768, 512, seed=5, in_dtype="f16", out_dtype=out,
+                            law_a="uniform", law_b="uniform")
+    C, ws, st = run(p, skgemm.opts_default(cta_pair=2, grid=min(96, sms() // 2 * 2)))
+    assert st == skgemm.OK
+    check_full(p, C)
+
+
+@pytest.mark.parametrize("shape", [(300, 300, 200), (1000, 1300, 520), (2000, 2100, 1000)])
+def test_cta_pairs_abft_clean(shape):
+    # Fused checksum side tiles in pairs (two 128-row checksum tiles per side
+    # tile, encoding rows split between the CTAs): no false positives and
+    # every 128-row tile with rows checked.
+    m, n, k = shape
+    p = inputs.make_problem(m, n, k, seed=m + n + 1, in_dtype="bf16", out_dtype="f32",
+                            law_a="normal", law_b="normal", alpha=0.5, beta=1.5)
+    opts = skgemm.opts_default(abft=1, cta_pair=2)
+    ws = None
+    for _ in range(2):
+        C, ws, st = run(p, opts, ws=ws)
+        assert st == skgemm.OK
+        check_full(p, C)
+        rep = ws.report(reset=True)
+        assert rep.detected == 0 and rep.status_bits == 0
+        assert rep.tiles_checked == ((m + 127) // 128) * ((n + 255) // 256)
+        assert rep.max_ratio_row < 0.1 and rep.max_ratio_col < 0.1
+
+
+@pytest.mark.parametrize("bit", [30, 26])
+def test_cta_pairs_abft_injection(bit):
+    # A flipped exponent bit in the second CTA of a pair (tile row 1 of a
+    # 256-row pair tile) is located and corrected.
+    m, n, k = 512, 768, 1024
+    p = inputs.make_problem(m, n, k, seed=91, in_dtype="bf16", out_dtype="f32",
+                            law_a="normal", law_b="normal", scale_b=0.02)
+    ref = reference(p)
+    tiles_n = (n + 255) // 256
+    tm, tn, row, col = 3, 1, 17, 200
+    tile = tm * tiles_n + tn
+    v = ref[tm * 128 + row, tn * 256 + col] / p.alpha
+    ma, mb = ab.tile_maxima(p.A.double().numpy(), p.B.double().numpy(), tm, tn, 128, 256)
+    tau = ab.default_tau(k, 256, ma, mb)
+    kind, _ = ab.classify_flip(v, bit, tau, 1e-3 * tau)
+    if kind != ab.MUST_DETECT:
+        pytest.skip(f"bit {bit} of {v} is {kind}")
+    opts = skgemm.opts_default(abft=1, cta_pair=2, inject_tile=tile, inject_row=row,
+                               inject_col=col, inject_bit=bit)
+    C, ws, st = run(p, opts)
+    assert st == skgemm.OK
+    rep = ws.report()
+    assert rep.detected == 1 and rep.corrected == 1
+    rec = rep.records[0]
+    assert (rec.tile, rec.row, rec.col, rec.injected) == (tile, row, col, 1)
+    check_full(p, C, ref)
