@@ -138,7 +138,7 @@ def run_ours(args, rank, world, local_rank):
         ws = skgemm.Workspace(skgemm.workspace_size(size, size, size, opts), dev)
         problems.append(dict(size=size, p=p, A=A, B=B, C=C, ws=ws))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    plans = {pr["size"]: skgemm.launch_shape(pr["size"], pr["size"], pr["size"], opts)
+    plans = {pr["size"]: skgemm.launch_plan(pr["size"], pr["size"], pr["size"], opts)
              for pr in problems}
     sched_names = {v: k for k, v in skgemm.SCHED_NAMES.items()}
 
@@ -250,9 +250,13 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": "square bf16 sweep m=n=k in {1024,2048,3072,4096,5120,6144}, "
                                "N(0,1)/sqrt(k) inputs (seed 1), fp32 accumulate, bf16 out, "
                                "ABFT verify on",
-                   "plan_per_shape": {str(sz): {"tile": f"128x{tn}x64", "grid": g,
-                                                "sched": sched_names[sc]}
-                                      for sz, (tn, g, sc) in plans.items()},
+                   "plan_per_shape": {str(sz): {"tile": f"{pl.tile_m}x{pl.tile_n}x64",
+                                                "ctas": pl.ctas + pl.side_ctas,
+                                                "cta_pairs": pl.cta_pair == 2,
+                                                "sched": sched_names[pl.sched],
+                                                "checksum_tiles": ("fused" if pl.fused_checksums
+                                                                   else "separate launches")}
+                                      for sz, pl in plans.items()},
                    "sms": sms,
                    "l2": "flushed between launches (256 MiB write)",
                    "parallelism": f"replicas x{world}"},
@@ -267,9 +271,8 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)",
                      "traffic": traffic},
         "abft": abft,
-        "gpu_launches": args.steps * sum(
-            2 if (2 * ((sz + 127) // 128) <= tn and 2 * ((sz + tn - 1) // tn) <= tn) else 4
-            for sz, (tn, _, _) in plans.items()),
+        "gpu_launches": args.steps * sum(2 if pl.fused_checksums else 4
+                                         for pl in plans.values()),
         "clocks": clocks,
         "wall_s_timed": round(wall, 3),
         "e2e": e2e,

@@ -281,6 +281,25 @@ skg_status_t skg_schedule_cost(int64_t m, int64_t n, int64_t k, int32_t bm, int3
 skg_status_t skg_launch_shape(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts,
                               int32_t* tile_n, int32_t* grid, int32_t* sched);
 
+/* The launch plan skg_gemm would use for this shape and options. */
+typedef struct {
+  int32_t tile_m;      /* output rows per tile: 128, or 256 for CTA pairs */
+  int32_t tile_n;      /* BLK_N: 128 or 256 */
+  int32_t ctas;        /* CTAs launched for the output tiles */
+  int32_t cta_pair;    /* 1 = single CTAs, 2 = clusters of two CTAs */
+  int32_t sched;       /* skg_sched_t */
+  int32_t side_ctas;   /* extra CTAs running whole ABFT checksum tiles (0 =
+                          checksum tiles split over the CTAs above) */
+  int32_t fused_checksums; /* ABFT: 1 = checksum GEMMs run inside the main
+                          launch, 0 = as separate launches (or no ABFT) */
+  int32_t reserved;
+} skg_plan_t;
+
+/* Same choice as skg_launch_shape, with the CTA-pair and checksum-tile
+ * placement. */
+skg_status_t skg_launch_plan(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts,
+                             skg_plan_t* out);
+
 /* Copy the workspace report to host memory (synchronises `stream` first);
  * reset != 0 also clears the counters and records. */
 skg_status_t skg_report_read(const void* workspace, skg_report_t* out, int32_t reset,

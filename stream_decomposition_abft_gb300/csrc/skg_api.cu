@@ -643,6 +643,27 @@ skg_status_t skg_launch_shape(int64_t m, int64_t n, int64_t k, const skg_opts_t*
   return SKG_OK;
 }
 
+skg_status_t skg_launch_plan(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts,
+                             skg_plan_t* out) {
+  if (m < 0 || n < 0 || k < 0 || !out) return SKG_ERR_ARG;
+  Resolved r;
+  const int sms = sm_count_cached();
+  skg_status_t st = resolve(m, n, k, opts, r, sms);
+  if (st != SKG_OK) return st;
+  const bool fused =
+      r.abft && m > 0 && n > 0 && k > 0 && can_fuse_checksums(layout(m, n, k, r), r.bn);
+  if (fused) replan_fused(m, n, opts, r);
+  memset(out, 0, sizeof(*out));
+  out->tile_m = r.pair ? 2 * kBM : kBM;
+  out->tile_n = r.bn;
+  out->ctas = r.grid;
+  out->cta_pair = r.pair ? 2 : 1;
+  out->sched = r.sched;
+  out->side_ctas = fused ? r.grid_ck : 0;
+  out->fused_checksums = fused ? 1 : 0;
+  return SKG_OK;
+}
+
 skg_status_t skg_report_read(const void* workspace, skg_report_t* out, int32_t reset,
                              void* stream) {
   if (!workspace || !out) return SKG_ERR_ARG;

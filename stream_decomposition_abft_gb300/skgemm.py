@@ -60,6 +60,13 @@ class FaultRecord(ctypes.Structure):
                 ("pad", ctypes.c_uint32 * 3)]
 
 
+class Plan(ctypes.Structure):
+    _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("ctas", ctypes.c_int32),
+                ("cta_pair", ctypes.c_int32), ("sched", ctypes.c_int32),
+                ("side_ctas", ctypes.c_int32), ("fused_checksums", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
 class Report(ctypes.Structure):
     _fields_ = [("status_bits", ctypes.c_uint32), ("launches", ctypes.c_uint32),
                 ("tiles_checked", ctypes.c_uint32), ("detected", ctypes.c_uint32),
@@ -72,7 +79,8 @@ class Report(ctypes.Structure):
 
 SYMBOLS = ("skg_opts_default", "skg_workspace_size", "skg_workspace_init", "skg_gemm",
            "skg_gemm_verify", "skg_abft_encode", "skg_schedule_query", "skg_launch_shape", "skg_report_read",
-           "skg_device_sm_count", "skg_status_string", "skg_gemm_noalloc", "skg_schedule_cost")
+           "skg_device_sm_count", "skg_status_string", "skg_gemm_noalloc", "skg_schedule_cost",
+           "skg_launch_plan")
 
 _lib = None
 
@@ -118,6 +126,8 @@ def lib() -> ctypes.CDLL:
     L.skg_launch_shape.argtypes = [i64, i64, i64, ctypes.POINTER(Opts), ctypes.POINTER(i32),
                                    ctypes.POINTER(i32), ctypes.POINTER(i32)]
     L.skg_launch_shape.restype = i32
+    L.skg_launch_plan.argtypes = [i64, i64, i64, ctypes.POINTER(Opts), ctypes.POINTER(Plan)]
+    L.skg_launch_plan.restype = i32
     L.skg_report_read.argtypes = [vp, ctypes.POINTER(Report), i32, vp]
     L.skg_report_read.restype = i32
     L.skg_gemm_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, i32,
@@ -198,6 +208,16 @@ def schedule_cost(m: int, n: int, k: int, bm: int, bn: int, bk: int, g: int, sch
     if st != OK:
         raise SkgError(st, "skg_schedule_cost")
     return us.value
+
+
+def launch_plan(m: int, n: int, k: int, opts: Optional[Opts] = None) -> Plan:
+    """The launch plan skg_gemm would use (tile shape, CTAs, pairs, schedule,
+    checksum-tile placement)."""
+    out = Plan()
+    st = lib().skg_launch_plan(m, n, k, ctypes.byref(opts) if opts else None, ctypes.byref(out))
+    if st != OK:
+        raise SkgError(st, "skg_launch_plan")
+    return out
 
 
 def launch_shape(m: int, n: int, k: int, opts: Optional[Opts] = None) -> Tuple[int, int, int]:

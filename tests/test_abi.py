@@ -41,6 +41,7 @@ def test_struct_sizes_match_header():
     assert ctypes.sizeof(skgemm.Segment) == 20
     assert ctypes.sizeof(skgemm.FaultRecord) == 64
     assert ctypes.sizeof(skgemm.Report) == 64 + 64 * 64
+    assert ctypes.sizeof(skgemm.Plan) == 32
 
 
 def test_defaults(lib):
@@ -177,3 +178,22 @@ def test_plan_honours_explicit_options_and_picks_minimum(lib):
         best = skgemm.schedule_cost(m, n, k, 128, tn, 64, g, sc)
         for bn in (128, 256):
             assert best <= skgemm.schedule_cost(m, n, k, 128, bn, 64, sms, skgemm.SCHED_SK2_DP) + 1e-9
+
+
+def test_launch_plan_agrees_with_launch_shape(lib):
+    for (m, n, k, kw) in [(1024, 1024, 1024, {}), (4096, 4096, 4096, dict(abft=1)),
+                          (8192, 1024, 8192, dict(tile_n=128)),
+                          (2048, 2048, 2048, dict(cta_pair=2, abft=1)),
+                          (512, 512, 512, dict(cta_pair=1, sched="sk", grid=40))]:
+        o = skgemm.opts_default(**kw)
+        pl = skgemm.launch_plan(m, n, k, o)
+        tn, g, sc = skgemm.launch_shape(m, n, k, o)
+        assert (pl.tile_n, pl.ctas + pl.side_ctas, pl.sched) == (tn, g, sc)
+        assert pl.tile_m == (256 if pl.cta_pair == 2 else 128)
+        if kw.get("cta_pair") == 2:
+            assert pl.cta_pair == 2 and pl.ctas % 2 == 0 and pl.tile_n == 256
+            assert pl.fused_checksums == 1 and pl.side_ctas == 0
+    assert skgemm.lib().skg_launch_plan(4, 4, 4, None, None) == skgemm.ERR_ARG
+    bad = skgemm.opts_default(cta_pair=3)
+    assert skgemm.lib().skg_launch_plan(4, 4, 4, ctypes.byref(bad),
+                                        ctypes.byref(skgemm.Plan())) == skgemm.ERR_ARG
