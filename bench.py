@@ -4,10 +4,12 @@
 Workload: C = A B with m = n = k in {1024, 2048, 3072, 4096, 5120, 6144},
 bf16 inputs drawn N(0,1)/sqrt(k) (seed 1), fp32 accumulation, bf16 output,
 ABFT checksum verification on. One step runs the whole hot path on every
-shape once: the ABFT encode pass (skg_abft_encode) and the persistent
-Stream-K kernel (skg_gemm), each launch bracketed by CUDA events on the
-launching stream, with a 256 MiB write between launches so no shape starts
-with its operands in the 129 MB L2.
+shape once: one skg_gemm call with ABFT on (the library issues the encode
+pass and the persistent Stream-K kernel, or one launch when the encode runs
+inside it), bracketed by CUDA events on the launching stream, with a
+256 MiB write before each shape so none starts with its operands in the
+129 MB L2. The main kernel alone (pre-encoded checksums) is timed the same
+way in a separate loop for the roofline.
 
 Metric: GEMM TFLOPS = 2mnk / time, geomean over the sweep, and its fraction
 of the GB300 dense bf16 peak. The JSON line also carries the roofline of the
@@ -126,7 +128,8 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     sms = skgemm.device_sm_count()
-    opts = skgemm.opts_default(abft=1, abft_preencoded=1)
+    opts = skgemm.opts_default(abft=1)                       # one ABFT GEMM call
+    main_opts = skgemm.opts_default(abft=1, abft_preencoded=1)  # main kernel alone
     enc_opts = skgemm.opts_default(abft=1)
 
     problems = []
@@ -142,30 +145,25 @@ def run_ours(args, rank, world, local_rank):
              for pr in problems}
     sched_names = {v: k for k, v in skgemm.SCHED_NAMES.items()}
 
-    def launch(pr):
+    def launch(pr, o):
         s = pr["size"]
-        st = skgemm.abft_encode(s, s, s, pr["A"].data_ptr(), s, pr["B"].data_ptr(), s,
-                                skgemm.IN_BF16, enc_opts, pr["ws"].ptr, pr["ws"].nbytes, sh)
-        if st != skgemm.OK:
-            raise skgemm.SkgError(st, "skg_abft_encode")
-        pr["ev"][1].record(stream)
         st = skgemm.gemm(s, s, s, 1.0, pr["A"].data_ptr(), s, pr["B"].data_ptr(), s, 0.0,
-                         pr["C"].data_ptr(), s, skgemm.IN_BF16, skgemm.OUT_BF16, 0, 0, opts,
+                         pr["C"].data_ptr(), s, skgemm.IN_BF16, skgemm.OUT_BF16, 0, 0, o,
                          pr["ws"].ptr, pr["ws"].nbytes, sh)
         if st != skgemm.OK:
             raise skgemm.SkgError(st, "skg_gemm")
 
     def step(record):
+        # One step: for every shape, an L2 flush, then the whole ABFT GEMM
+        # (encode pass + main kernel, issued by the library) between events.
         for pr in problems:
             flush.zero_()
             if record:
-                pr["ev"] = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                pr["ev"] = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
                 pr["ev"][0].record(stream)
-            else:
-                pr["ev"] = [None, _Dummy(), None]
-            launch(pr)
+            launch(pr, opts)
             if record:
-                pr["ev"][2].record(stream)
+                pr["ev"][1].record(stream)
                 pr["events"].append(pr["ev"])
 
     for pr in problems:
@@ -191,21 +189,39 @@ def run_ours(args, rank, world, local_rank):
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
 
+    # The dominant kernel alone (roofline): the main kernel on pre-encoded
+    # checksums, L2 flushed before each launch, CUDA events on this stream.
+    main_reps = max(5, min(args.steps, 30))
+    for pr in problems:
+        s = pr["size"]
+        st = skgemm.abft_encode(s, s, s, pr["A"].data_ptr(), s, pr["B"].data_ptr(), s,
+                                skgemm.IN_BF16, enc_opts, pr["ws"].ptr, pr["ws"].nbytes, sh)
+        if st != skgemm.OK:
+            raise skgemm.SkgError(st, "skg_abft_encode")
+        evs = []
+        for _ in range(main_reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch(pr, main_opts)
+            e1.record(stream)
+            evs.append((e0, e1))
+        pr["main_events"] = evs
+    torch.cuda.synchronize()
+
     per_shape = []
     total_main_ms = 0.0
     total_main_flops = 0.0
     abft = {"tiles_checked": 0, "detected": 0, "max_ratio_row": 0.0, "max_ratio_col": 0.0}
     for pr in problems:
         s = pr["size"]
-        full = [e[0].elapsed_time(e[2]) for e in pr["events"]]
-        main = [e[1].elapsed_time(e[2]) for e in pr["events"]]
-        enc = [e[0].elapsed_time(e[1]) for e in pr["events"]]
+        full = [e[0].elapsed_time(e[1]) for e in pr["events"]]
+        main = [a.elapsed_time(b) for a, b in pr["main_events"]]
         t_full = statistics.mean(full)
         t_main = statistics.mean(main)
         flops = 2.0 * s * s * s
         per_shape.append({"m": s, "n": s, "k": s, "ms": round(t_full, 5),
                           "ms_main_kernel": round(t_main, 5),
-                          "ms_encode": round(statistics.mean(enc), 5),
                           "tflops": round(flops / t_full / 1e9, 2),
                           "tflops_main_kernel": round(flops / t_main / 1e9, 2)})
         total_main_ms += sum(main)
@@ -255,7 +271,9 @@ def run_ours(args, rank, world, local_rank):
                                                 "cta_pairs": pl.cta_pair == 2,
                                                 "sched": sched_names[pl.sched],
                                                 "checksum_tiles": ("fused" if pl.fused_checksums
-                                                                   else "separate launches")}
+                                                                   else "separate launches"),
+                                                "launches": ((1 if pl.encode_in_kernel else 2)
+                                                             if pl.fused_checksums else 4)}
                                       for sz, pl in plans.items()},
                    "sms": sms,
                    "l2": "flushed between launches (256 MiB write)",
@@ -271,8 +289,9 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)",
                      "traffic": traffic},
         "abft": abft,
-        "gpu_launches": args.steps * sum(2 if pl.fused_checksums else 4
-                                         for pl in plans.values()),
+        "gpu_launches": args.steps * sum(
+            (1 if pl.encode_in_kernel else 2) if pl.fused_checksums else 4
+            for pl in plans.values()),
         "clocks": clocks,
         "wall_s_timed": round(wall, 3),
         "e2e": e2e,
@@ -280,11 +299,6 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     print(json.dumps(line), flush=True)
-
-
-class _Dummy:
-    def record(self, stream=None):
-        pass
 
 
 def measure_e2e(args, problems, dev, stream, opts, enc_opts):
@@ -525,6 +539,7 @@ def workload_hostile(args):
                                          dict(sched="sk2_dp", grid=sms, tile_n=128))):
             opts = skgemm.opts_default(**kw)
             tn, g, sc = skgemm.launch_shape(m, n, k, opts)
+            pl = skgemm.launch_plan(m, n, k, opts)
             clk = torch.zeros(2 * g, dtype=torch.int64, device=dev)
             opts.cta_clock = clk.data_ptr()
             ws = skgemm.Workspace(skgemm.workspace_size(m, n, k, opts), dev)
@@ -541,7 +556,8 @@ def workload_hostile(args):
             c = clk.view(g, 2).cpu().double()
             busy = (c[:, 1] - c[:, 0])
             spread = float((busy.max() - busy.min()) / busy.max())
-            out.append({"m": m, "n": n, "k": k, "plan": label, "tile": f"128x{tn}x64",
+            out.append({"m": m, "n": n, "k": k, "plan": label,
+                        "tile": f"{pl.tile_m}x{tn}x64", "cta_pairs": pl.cta_pair == 2,
                         "grid": g, "sched": names[sc], "ms": round(ms, 4),
                         "tflops": round(2.0 * m * n * k / ms / 1e9, 1),
                         "pct_of_peak_measured": round(100 * 2.0 * m * n * k / ms / 1e9 / burst, 1),
@@ -673,7 +689,10 @@ def workload_mlp(args):
                         camp["corrected"] += 1
             else:
                 camp["harmless_or_grey"] += 1
-        results.append({"m": m, "n": n, "k": k, "plan": f"128x{tn}x64 g={g}",
+        pl = skgemm.launch_plan(m, n, k, o_on)
+        results.append({"m": m, "n": n, "k": k,
+                        "plan": f"{pl.tile_m}x{tn}x64 ctas={g}"
+                                + (" (CTA pairs)" if pl.cta_pair == 2 else ""),
                         "ms_abft_on": round(t_on, 4), "ms_abft_off": round(t_off, 4),
                         "abft_overhead_pct": round(100 * (t_on / t_off - 1), 2),
                         "tflops_abft_on": round(2.0 * m * n * k / t_on / 1e9, 1),

@@ -292,11 +292,14 @@ typedef struct {
                           checksum tiles split over the CTAs above) */
   int32_t fused_checksums; /* ABFT: 1 = checksum GEMMs run inside the main
                           launch, 0 = as separate launches (or no ABFT) */
-  int32_t reserved;
+  int32_t encode_in_kernel; /* ABFT: 1 = the side CTAs also run the encode
+                          pass, so the call is a single launch */
 } skg_plan_t;
 
 /* Same choice as skg_launch_shape, with the CTA-pair and checksum-tile
- * placement. */
+ * placement. Both queries plan for bf16 inputs: for fp16 with ABFT the
+ * encode pass is always a separate launch and the side CTAs are only the
+ * checksum tiles' (one per tile). */
 skg_status_t skg_launch_plan(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts,
                              skg_plan_t* out);
 

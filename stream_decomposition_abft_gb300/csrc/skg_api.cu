@@ -74,6 +74,7 @@ struct Resolved {
   int drop_signal;
   int preencoded;
   int raster_band;
+  int enc_inkernel;  // the dedicated side CTAs run the encode pass (no encode launch)
   int ws_grid;
   int64_t k_for_plan;  // CTAs the workspace's flags and partial slots are sized for
 };
@@ -147,6 +148,7 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
   r.preencoded = o->abft_preencoded ? 1 : 0;
   if (o->raster_band < 0) return SKG_ERR_ARG;
   r.raster_band = o->raster_band;
+  r.enc_inkernel = 0;
   return SKG_OK;
 }
 
@@ -284,7 +286,7 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
       make_map(&mp.c, out_t, out_bytes, g.C, (uint64_t)g.n, (uint64_t)g.m, (uint64_t)g.ldc,
                128 / out_bytes, 32) != CUDA_SUCCESS)
     return SKG_ERR_UNSUPPORTED;
-  mp.b128 = mp.be = mp.ea = mp.cr = mp.cc = mp.a;
+  mp.b128 = mp.be = mp.ea = mp.cr = mp.cc = mp.enca = mp.encb = mp.a;
   int t_ck = 0, ck_cr = 0;
   // CTA pairs: a side tile is two 128-row checksum tiles, the encoding rows
   // (the MMA's N) are split between the two CTAs, so N rounds up to 32.
@@ -355,6 +357,21 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   p.umax = (const float*)(ws + L.umax);
   p.enc_slices = encode_slices(L.kp);
   p.enc_tiles_a = L.tiles_a;
+  if (fuse_ck && r.enc_inkernel) {
+    if (make_map(&mp.enca, in_t, 2, g.A, (uint64_t)g.k, (uint64_t)g.m, (uint64_t)g.lda,
+                 kEncBoxCols, kEncBoxRows, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS ||
+        make_map(&mp.encb, in_t, 2, g.B, (uint64_t)g.k, (uint64_t)g.n, (uint64_t)g.ldb,
+                 kEncBoxCols, kEncBoxRows, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return SKG_ERR_UNSUPPORTED;
+    p.enc_inkernel = 1;
+    p.enc_tiles_b = L.tiles_b;
+    p.enc_bn = r.bn;
+    p.enc_kp = L.kp;
+    p.enc_a_w = ws + L.enc_a;
+    p.enc_b_w = ws + L.enc_b;
+    p.umax_w = (float*)(ws + L.umax);
+    p.pub_w = (TilePub*)(ws + L.pub);
+  }
   p.tau_row = r.tau_row;
   p.tau_col = r.tau_col;
   p.inject_tile = r.inject_tile;
@@ -450,6 +467,22 @@ void replan_fused(int64_t m, int64_t n, const skg_opts_t* opts, Resolved& r) {
   r.grid_ck = pl.grid_ck;
 }
 
+// Plan of a call whose checksum GEMMs are fused: grid and schedule with the
+// side tiles, then their placement. Checksum tiles on dedicated CTAs leave
+// SMs idle while the output tiles run, so those CTAs take every idle SM and
+// the encode pass too (bf16 encodings need no per-tile scale).
+void plan_fused(int64_t m, int64_t n, const skg_opts_t* opts, int32_t in_dtype, Resolved& r) {
+  replan_fused(m, n, opts, r);
+  // Only with plenty of idle SMs (at least four per checksum tile): the
+  // side CTAs' encode-then-checksum chain must end with the output tiles.
+  r.enc_inkernel = (!r.preencoded && r.grid_ck > 0 && !r.pair && in_dtype == SKG_IN_BF16 &&
+                    r.grid_max - r.grid >= 4 * r.grid_ck && kEncBoxCols == kEncInCols &&
+                    kEncBoxRows == kEncInRows)
+                       ? 1
+                       : 0;
+  if (r.enc_inkernel) r.grid_ck = r.grid_max - r.grid;
+}
+
 skg_status_t check_inputs(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
                           const void* B, int64_t ldb) {
   if (!A || !B) return SKG_ERR_ARG;
@@ -508,8 +541,8 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
     // The checksum-GEMM tiles run ahead of the output tiles in the same
     // launch, after the encode pass (skipped when pre-encoded).
     fuse = true;
-    replan_fused(m, n, opts, r);
-    if (!r.preencoded) {
+    plan_fused(m, n, opts, in_dtype, r);
+    if (!r.enc_inkernel && !r.preencoded) {
       st = run_encode(in_dtype, A, lda, m, B, ldb, n, k, r, ws, L, sms, stream);
       if (st != SKG_OK) return st;
     }
@@ -636,7 +669,7 @@ skg_status_t skg_launch_shape(int64_t m, int64_t n, int64_t k, const skg_opts_t*
   skg_status_t st = resolve(m, n, k, opts, r, sms);
   if (st != SKG_OK) return st;
   if (r.abft && m > 0 && n > 0 && k > 0 && can_fuse_checksums(layout(m, n, k, r), r.bn))
-    replan_fused(m, n, opts, r);
+    plan_fused(m, n, opts, SKG_IN_BF16, r);
   if (tile_n) *tile_n = r.bn;
   if (grid) *grid = r.grid + r.grid_ck;
   if (sched) *sched = r.sched;
@@ -652,7 +685,7 @@ skg_status_t skg_launch_plan(int64_t m, int64_t n, int64_t k, const skg_opts_t* 
   if (st != SKG_OK) return st;
   const bool fused =
       r.abft && m > 0 && n > 0 && k > 0 && can_fuse_checksums(layout(m, n, k, r), r.bn);
-  if (fused) replan_fused(m, n, opts, r);
+  if (fused) plan_fused(m, n, opts, SKG_IN_BF16, r);
   memset(out, 0, sizeof(*out));
   out->tile_m = r.pair ? 2 * kBM : kBM;
   out->tile_n = r.bn;
@@ -661,6 +694,7 @@ skg_status_t skg_launch_plan(int64_t m, int64_t n, int64_t k, const skg_opts_t* 
   out->sched = r.sched;
   out->side_ctas = fused ? r.grid_ck : 0;
   out->fused_checksums = fused ? 1 : 0;
+  out->encode_in_kernel = r.enc_inkernel;
   return SKG_OK;
 }
 

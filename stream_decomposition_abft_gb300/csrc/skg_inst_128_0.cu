@@ -21,8 +21,9 @@ cudaError_t launch_gemm(const Maps& mp, const KernelParams& p, int grid, cudaStr
     if (e != cudaSuccess) return e;
     done_mask.fetch_or(bit, std::memory_order_acq_rel);
   }
-  return launch_pdl(skg_gemm_kernel<C>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, stream, mp.a,
-                    mp.b, mp.c, mp.b128, mp.be, mp.ea, mp.cr, mp.cc, p);
+  return launch_pdl_cluster(skg_gemm_kernel<C>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, stream,
+                            PAIR ? 2 : 1, mp.a, mp.b, mp.c, mp.b128, mp.be, mp.ea, mp.cr, mp.cc,
+                            mp.enca, mp.encb, p);
 }
 
 #define SKG_INST(OUT)                                                                        \

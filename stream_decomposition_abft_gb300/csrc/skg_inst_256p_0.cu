@@ -24,7 +24,7 @@ cudaError_t launch_gemm(const Maps& mp, const KernelParams& p, int grid, cudaStr
   }
   return launch_pdl_cluster(skg_gemm_kernel<C>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, stream,
                             PAIR ? 2 : 1, mp.a, mp.b, mp.c, mp.b128, mp.be, mp.ea, mp.cr, mp.cc,
-                            p);
+                            mp.enca, mp.encb, p);
 }
 
 #define SKG_INST(OUT)                                                                        \

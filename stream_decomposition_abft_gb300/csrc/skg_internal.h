@@ -50,6 +50,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // fp32 checksum outputs cr_all and ccT_all (32 x 32). Unused ones repeat A.
 struct Maps {
   CUtensorMap a, b, c, b128, be, ea, cr, cc;
+  CUtensorMap enca, encb;  // in-kernel encode boxes of A and B (64 x 256, no swizzle)
 };
 
 // Launch the persistent kernel instantiated for (BN, ABFT, OUT, PAIR) on

@@ -60,10 +60,11 @@ constexpr uint32_t kSmemLimit = 232448;
 
 // Workspace header (device). The report follows at offset 256.
 struct WsHeader {
-  uint32_t epoch;    // launches completed on this workspace
-  uint32_t done;     // CTA tickets of the running launch
-  uint32_t ck_done;  // fused checksum tiles stored by the running launch
-  uint32_t pad[61];
+  uint32_t epoch;     // launches completed on this workspace
+  uint32_t done;      // CTA tickets of the running launch
+  uint32_t ck_done;   // fused checksum tiles stored by the running launch
+  uint32_t enc_done;  // side CTAs done with the in-kernel encode pass
+  uint32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
@@ -105,6 +106,15 @@ struct KernelParams {
   // per tile; A tiles first): a tile's maximum is the max over its units.
   const float* umax;
   int enc_slices, enc_tiles_a;
+  // In-kernel encode pass (bf16; the separate encode kernel's work, run by
+  // the dedicated side CTAs before their checksum tiles): units of one
+  // operand tile x 256 k-columns, boxes of 64 rows.
+  int enc_inkernel;
+  int enc_tiles_b, enc_bn, enc_kp;
+  void* enc_a_w;
+  void* enc_b_w;
+  float* umax_w;
+  TilePub* pub_w;
   // Fused reference-checksum GEMMs: tiles [0, s.t_ck) of the schedule.
   // Tile j < ck_cr_tiles computes rows [128 j, 128 j + 128) of
   // cr_all = A x [Be_hi; Be_lo]^T (ck_n_cr columns); the others compute rows
@@ -391,6 +401,36 @@ __device__ __forceinline__ void add_peer_partials(float (&v)[32], float* partial
   }
 }
 
+// In-kernel encode pass: boxes of 64 rows x 256 k-columns (no swizzle). A
+// unit is one operand tile (128 rows of A, enc_bn stored rows of B) x 256
+// k-columns; side CTA sx of gs takes a contiguous range of units, split
+// evenly in boxes.
+constexpr int kEncInCols = 256;
+constexpr int kEncInRows = 64;
+constexpr int kEncInBoxBytes = kEncInCols * kEncInRows * 2;
+
+__device__ __forceinline__ void enc_in_units(const KernelParams& p, int sx, int gs, int& u0,
+                                             int& u1) {
+  const int sub_a = kBM / kEncInRows, sub_b = p.enc_bn / kEncInRows;
+  const int units_a = p.enc_tiles_a * p.enc_slices;
+  const int units = units_a + p.enc_tiles_b * p.enc_slices;
+  const int64_t boxes = (int64_t)units_a * sub_a + (int64_t)(units - units_a) * sub_b;
+  auto first_unit_at = [&](int64_t box) -> int {
+    const int64_t in_a = (int64_t)units_a * sub_a;
+    if (box <= in_a) return (int)((box + sub_a - 1) / sub_a);
+    return units_a + (int)((box - in_a + sub_b - 1) / sub_b);
+  };
+  u0 = first_unit_at(boxes * sx / gs);
+  u1 = first_unit_at(boxes * (sx + 1) / gs);
+}
+
+__device__ __forceinline__ int enc_in_boxes(const KernelParams& p, int u0, int u1) {
+  const int units_a = p.enc_tiles_a * p.enc_slices;
+  int n = 0;
+  for (int u = u0; u < u1; ++u) n += u < units_a ? kBM / kEncInRows : p.enc_bn / kEncInRows;
+  return n;
+}
+
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     skg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -399,7 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmBE,
                     const __grid_constant__ CUtensorMap tmEA,
                     const __grid_constant__ CUtensorMap tmCr,
-                    const __grid_constant__ CUtensorMap tmCc, const KernelParams p) {
+                    const __grid_constant__ CUtensorMap tmCc,
+                    const __grid_constant__ CUtensorMap tmEncA,
+                    const __grid_constant__ CUtensorMap tmEncB, const KernelParams p) {
   constexpr int BN = C::BN;
   constexpr int STAGES = C::STAGES;
   constexpr int ACC_BUFS = C::ACC_BUFS;
@@ -430,6 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int my_slot_idx = unit * slot_stride + (int)crank;
   const int row_half = (int)crank * kBM;
   constexpr int kCkHalf = C::PAIR ? 2 : 1;  // 128-row checksum tiles per side tile
+  // Dedicated side CTA that first runs its share of the encode pass.
+  const bool enc_here = C::ABFT && !C::PAIR && p.enc_inkernel && (int)blockIdx.x >= s.g;
+  static_assert(C::STAGE_BYTES >= kEncInBoxBytes, "an encode box fills one ring stage");
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
@@ -493,6 +538,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pending = 0;  // bit i: stage i has a load this thread issued
       uint32_t pend_par = 0; // parity of that load's phase
       bool ok = true;
+      if (enc_here) {
+        // Encode pass: this side CTA's units, one box per ring stage.
+        if (threadIdx.x == 0) {
+          prefetch_tmap(&tmEncA);
+          prefetch_tmap(&tmEncB);
+        }
+        int u0, u1;
+        enc_in_units(p, (int)blockIdx.x - s.g, s.g_ck, u0, u1);
+        const int units_a = p.enc_tiles_a * p.enc_slices;
+        for (int u = u0; ok && u < u1; ++u) {
+          const bool is_a = u < units_a;
+          const int t = u / p.enc_slices, sl = u - t * p.enc_slices;
+          const CUtensorMap* map = is_a ? &tmEncA : &tmEncB;
+          const int row0 = is_a ? t * kBM : (t - p.enc_tiles_a) * p.enc_bn;
+          const int nsub = is_a ? kBM / kEncInRows : p.enc_bn / kEncInRows;
+          for (int h = 0; h < nsub; ++h) {
+            if (!mbar_try_wait(&empty_bar[stage], phase ^ 1) &&
+                !wait_bar(&empty_bar[stage], phase ^ 1, aux, limit)) {
+              if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full_bar[stage], kEncInBoxBytes);
+            tma_load_2d(ring + stage * C::STAGE_BYTES, map, &full_bar[stage], sl * kEncInCols,
+                        row0 + h * kEncInRows);
+            pending |= 1u << stage;
+            pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+        // The checksum tiles read every side CTA's encodings: wait for all.
+        if (ok) {
+          const uint64_t t0 = globaltimer();
+          while (ld_acquire_gpu(&p.hdr->enc_done) < (uint32_t)s.g_ck) {
+            nanosleep_ns(64);
+            if (globaltimer() - t0 > limit) {
+              if (!aborted(aux)) record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
+              ok = false;
+              break;
+            }
+          }
+          // Written through the generic proxy, read by TMA (async proxy).
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+      }
       while (ok && cur.next(s, w)) {
         // Operand maps and row coordinates of this tile: an output tile, or
         // a tile of one of the fused checksum GEMMs.
@@ -581,6 +674,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t aphase = 0;
       bool ok = true;
       bool issued = false;
+      if (enc_here) {
+        // The ring's first stages carry this CTA's encode boxes. Start only
+        // once every side CTA's encode pass is done: by then all of this
+        // CTA's boxes have landed and been consumed, so the first wait below
+        // cannot mistake an earlier phase of a stage for the one it wants
+        // (a parity wait only tells phases apart one at a time).
+        int u0, u1;
+        enc_in_units(p, (int)blockIdx.x - s.g, s.g_ck, u0, u1);
+        const int nb = enc_in_boxes(p, u0, u1);
+        stage = nb % STAGES;
+        phase = (uint32_t)((nb / STAGES) & 1);
+        const uint64_t t0 = globaltimer();
+        while (ld_acquire_gpu(&p.hdr->enc_done) < (uint32_t)s.g_ck) {
+          nanosleep_ns(64);
+          if (globaltimer() - t0 > limit) {
+            if (!aborted(aux)) record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
+            ok = false;
+            break;
+          }
+        }
+      }
       while (ok && cur.next(s, w)) {
         if (!wait_bar(&tempty_bar[ab], aphase ^ 1, aux, limit, true, C::PAIR)) {
           if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
@@ -696,6 +810,92 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nseg = 0;
     bool store_ok = true;
     bool ck_ready = false;
+    if (enc_here) {
+      // Encode pass (bf16): column sums of each unit's boxes out of the ring,
+      // then the unit's hi / lo encoding rows and its max |element|.
+      int u0, u1;
+      enc_in_units(p, (int)blockIdx.x - s.g, s.g_ck, u0, u1);
+      const int units_a = p.enc_tiles_a * p.enc_slices;
+      float* part = reinterpret_cast<float*>(epi);  // [4 warps][256 columns]
+      int est = 0;
+      uint32_t eph = 0;
+      bool eok = true;
+      for (int u = u0; u < u1 && eok; ++u) {
+        const bool is_a = u < units_a;
+        const int t = u / p.enc_slices, sl = u - t * p.enc_slices;
+        const int nsub = is_a ? kBM / kEncInRows : p.enc_bn / kEncInRows;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        float amax = 0.f;
+        for (int h = 0; h < nsub; ++h) {
+          const bool got = wait_bar(&full_bar[est], eph, aux, limit);
+          if (!got && !aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+          if (!epi_all(got && !aborted(aux))) {
+            eok = false;
+            break;
+          }
+          // Warp ew sums rows ew, ew + 4, ...; lane l holds columns 8l .. 8l + 7.
+          const uint8_t* st = ring + est * C::STAGE_BYTES + lane * 16;
+#pragma unroll 4
+          for (int i = 0; i < kEncInRows / 4; ++i) {
+            const uint4 v = *reinterpret_cast<const uint4*>(st + (ew + 4 * i) * (kEncInCols * 2));
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float lo = __uint_as_float(wv[j] << 16);
+              const float hi = __uint_as_float(wv[j] & 0xffff0000u);
+              acc[2 * j] += lo;
+              acc[2 * j + 1] += hi;
+              amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+            }
+          }
+          named_bar_sync(1, kEpiThreads);  // the stage is read
+          if (et == 0) mbar_arrive(&empty_bar[est]);
+          if (++est == STAGES) {
+            est = 0;
+            eph ^= 1;
+          }
+        }
+        if (!eok) break;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part[ew * kEncInCols + lane * 8 + i] = acc[i];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (lane == 0) aux->tmax_a[ew] = amax;
+        named_bar_sync(1, kEpiThreads);
+        __nv_bfloat16* enc = static_cast<__nv_bfloat16*>(is_a ? p.enc_a_w : p.enc_b_w);
+        const int tile = is_a ? t : t - p.enc_tiles_a;
+        __nv_bfloat16* hi_row = enc + (int64_t)(kEncRows * tile) * p.enc_kp;
+        __nv_bfloat16* lo_row = hi_row + p.enc_kp;
+#pragma unroll
+        for (int hh = 0; hh < kEncInCols / kEpiThreads; ++hh) {
+          const int c = hh * kEpiThreads + et;
+          const float x = part[c] + part[kEncInCols + c] + part[2 * kEncInCols + c] +
+                          part[3 * kEncInCols + c];
+          const int col = sl * kEncInCols + c;
+          if (col < p.enc_kp) {  // columns in [k, kp) hold zero sums
+            const __nv_bfloat16 hv = __float2bfloat16_rn(x);
+            hi_row[col] = hv;
+            lo_row[col] = __float2bfloat16_rn(x - __bfloat162float(hv));
+          }
+        }
+        if (et == 0) {
+          p.umax_w[u] = fmaxf(fmaxf(aux->tmax_a[0], aux->tmax_a[1]),
+                              fmaxf(aux->tmax_a[2], aux->tmax_a[3]));
+          if (sl == 0) p.pub_w[t].scale_exp = 0;
+        }
+        named_bar_sync(1, kEpiThreads);  // part and tmax reused by the next unit
+      }
+      // Every encode write of this CTA lands before the counter moves.
+      __threadfence();
+      named_bar_sync(1, kEpiThreads);
+      if (et == 0 && eok) {
+        __threadfence();
+        atomicAdd(&p.hdr->enc_done, 1u);
+      }
+    }
     while (cur.next(s, w)) {
       if (p.trace && et == 0) {
         int32_t* tr = p.trace + (size_t)blockIdx.x * SKG_TRACE_STRIDE;
@@ -1203,6 +1403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Last CTA of the launch: every CTA has read the epoch, so advance it.
       p.hdr->done = 0;
       p.hdr->ck_done = 0;
+      p.hdr->enc_done = 0;
       atomicAdd(&p.report->launches, 1u);
       __threadfence();
       atomicAdd(&p.hdr->epoch, 1u);

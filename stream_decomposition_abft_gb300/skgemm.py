@@ -64,7 +64,7 @@ class Plan(ctypes.Structure):
     _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("ctas", ctypes.c_int32),
                 ("cta_pair", ctypes.c_int32), ("sched", ctypes.c_int32),
                 ("side_ctas", ctypes.c_int32), ("fused_checksums", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("encode_in_kernel", ctypes.c_int32)]
 
 
 class Report(ctypes.Structure):

@@ -424,3 +424,48 @@ def test_cta_pairs_abft_injection(bit):
     rec = rep.records[0]
     assert (rec.tile, rec.row, rec.col, rec.injected) == (tile, row, col, 1)
     check_full(p, C, ref)
+
+
+# --------------------------------------------------------------------------- single-launch ABFT
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (384, 640, 320), (300, 1000, 520)])
+def test_abft_encode_in_kernel(shape):
+    # Small bf16 shapes whose output tiles leave SMs idle: the checksum tiles
+    # run on extra CTAs that first run the encode pass, so the whole ABFT
+    # call is one launch. Clean run, a reused workspace, then a fault.
+    m, n, k = shape
+    p = inputs.make_problem(m, n, k, seed=m + 3 * n, in_dtype="bf16", out_dtype="bf16",
+                            law_a="normal", law_b="normal", scale_a=k ** -0.5,
+                            scale_b=k ** -0.5)
+    opts = skgemm.opts_default(abft=1)
+    plan = skgemm.launch_plan(m, n, k, opts)
+    assert plan.fused_checksums == 1 and plan.encode_in_kernel == 1 and plan.side_ctas > 0
+    ref = reference(p)
+    ws = None
+    for _ in range(2):
+        C, ws, st = run(p, opts, ws=ws)
+        assert st == skgemm.OK
+        check_full(p, C, ref)
+        rep = ws.report(reset=True)
+        assert rep.detected == 0 and rep.status_bits == 0
+        assert rep.tiles_checked == ((m + 127) // 128) * ((n + plan.tile_n - 1) // plan.tile_n)
+        assert rep.max_ratio_row < 0.1 and rep.max_ratio_col < 0.1
+    tiles_n = (n + plan.tile_n - 1) // plan.tile_n
+    tm, tn, row, col = (m - 1) // 128, tiles_n - 1, 3, 5
+    gi, gj = tm * 128 + row, tn * plan.tile_n + col
+    if gi >= m or gj >= n:
+        tm, tn = 0, 0
+        gi, gj = row, col
+    v = ref[gi, gj] / p.alpha
+    ma, mb = ab.tile_maxima(p.A.double().numpy(), p.B.double().numpy(), tm, tn, 128,
+                            plan.tile_n)
+    kind, _ = ab.classify_flip(v, 30, ab.default_tau(k, plan.tile_n, ma, mb), 1e-3)
+    assert kind == ab.MUST_DETECT
+    oi = skgemm.opts_default(abft=1, inject_tile=tm * tiles_n + tn, inject_row=row,
+                             inject_col=col, inject_bit=30)
+    C, ws, st = run(p, oi, ws=ws)
+    assert st == skgemm.OK
+    rep = ws.report()
+    assert rep.detected == 1 and rep.corrected == 1
+    assert (rep.records[0].tile, rep.records[0].row, rep.records[0].col) == \
+        (tm * tiles_n + tn, row, col)
+    check_full(p, C, ref)
