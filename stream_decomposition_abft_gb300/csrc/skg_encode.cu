@@ -84,17 +84,18 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v
   return old;
 }
 
-// Named barrier 1 over the consumer warps (512 threads) that also ANDs a
-// predicate.
+// Named barrier 1 over the kEncWorkerThreads consumer threads that also
+// ANDs a predicate (the count comes from the same constant as the launch).
+static_assert(kEncWorkerThreads % 32 == 0 && kEncWorkerThreads <= 1024, "barrier count");
 __device__ __forceinline__ bool workers_all(bool v) {
   uint32_t out;
   asm volatile(
       "{\n\t.reg .pred pi, po;\n\t"
       "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.and.pred po, 1, 512, pi;\n\t"
+      "bar.red.and.pred po, 1, %2, pi;\n\t"
       "selp.u32 %0, 1, 0, po;\n\t}"
       : "=r"(out)
-      : "r"((uint32_t)v)
+      : "r"((uint32_t)v), "n"(kEncWorkerThreads)
       : "memory");
   return out != 0;
 }

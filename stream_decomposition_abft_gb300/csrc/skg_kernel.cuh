@@ -55,6 +55,8 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
+static_assert(kThreads == 64 + kEpiThreads && kEpiThreads == 128,
+              "epi_all and the named barriers count the four epilogue warps");
 constexpr int kEncRows = 2;  // hi and lo terms of each encoding
 constexpr uint32_t kSmemLimit = 232448;
 
