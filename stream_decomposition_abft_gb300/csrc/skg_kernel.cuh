@@ -58,6 +58,7 @@ constexpr int kEpiThreads = 128;
 static_assert(kThreads == 64 + kEpiThreads && kEpiThreads == 128,
               "epi_all and the named barriers count the four epilogue warps");
 constexpr int kEncRows = 2;  // hi and lo terms of each encoding
+constexpr int kFixSlots = 4;  // per epilogue warp: staged partial pieces in flight
 constexpr uint32_t kSmemLimit = 232448;
 
 // Workspace header (device). The report follows at offset 256.
@@ -185,7 +186,7 @@ struct Cfg {
 
 // Shared-memory bookkeeping that lives after the stage ring and staging.
 struct Aux {
-  uint64_t bars[48];      // full[S], empty[S], tfull[2], tempty[2], c0[4], drain
+  uint64_t bars[48];      // full[S], empty[S], tfull[2], tempty[2], c0[4], drain, fix, c0r[4]
   uint32_t tmem_slot;
   int32_t abort_flag;
   int32_t nbad_r, nbad_c, bad_row, bad_col;
@@ -355,11 +356,20 @@ __device__ __forceinline__ void st_cg_f4(float* p, float4 v) {
   __stcg(reinterpret_cast<float4*>(p), v);
 }
 
-// Partial tile layout (per CTA slot): 4-column groups of 128 rows, so the 32
-// lanes of a warp touch 512 contiguous bytes: float index (c4*128 + r)*4 + e.
-__device__ __forceinline__ float* partial_at(float* slot, int c4, int r) {
-  return slot + ((size_t)c4 * kBM + r) * 4;
+// Partial tile layouts (per CTA slot). Output tiles (region 0) use one band
+// per 32-row lane quadrant (32 x BN floats, contiguous, so an owner can pull
+// a quadrant's partial with a single bulk copy); inside a band, 4-column
+// groups of 32 rows: float index ((r / 32) * BN / 4 + c4) * 128 + (r % 32) * 4 + e.
+// Checksum tiles (region 1) use only their first columns and keep them
+// together: 4-column groups of all 128 rows, float index (c4 * 128 + r) * 4 + e.
+// Either way the 32 lanes of a warp touch 512 contiguous bytes.
+template <int BN>
+__device__ __forceinline__ float* partial_at(float* slot, int c4, int r, bool band) {
+  return band ? slot + ((size_t)((r >> 5) * (BN / 4) + c4) * 32 + (r & 31)) * 4
+              : slot + ((size_t)c4 * kBM + r) * 4;
 }
+template <int BN>
+constexpr uint32_t kPartialBandBytes = 32u * BN * 4u;
 
 // LoadPartials for one 32-column chunk: v += the partials of peers
 // first..last (ascending CTA order, so the sum is deterministic). Loads are
@@ -367,8 +377,8 @@ __device__ __forceinline__ float* partial_at(float* slot, int c4, int r) {
 // peers waits for one L2 round trip per group rather than per peer.
 template <int BN>
 __device__ __forceinline__ void add_peer_partials(float (&v)[32], float* partials, int first,
-                                                  int last, int c32, int r, int slot_stride = 1,
-                                                  int slot_offset = 0) {
+                                                  int last, int c32, int r, bool band,
+                                                  int slot_stride = 1, int slot_offset = 0) {
   int peer = first;
   for (; peer + 3 <= last; peer += 4) {
     float4 t[4][8];
@@ -376,7 +386,7 @@ __device__ __forceinline__ void add_peer_partials(float (&v)[32], float* partial
     for (int u = 0; u < 4; ++u) {
       float* ps = partials + (size_t)((peer + u) * slot_stride + slot_offset) * kBM * BN;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) t[u][j] = ld_cg_f4(partial_at(ps, c32 * 8 + j, r));
+      for (int j = 0; j < 8; ++j) t[u][j] = ld_cg_f4(partial_at<BN>(ps, c32 * 8 + j, r, band));
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u)
@@ -392,7 +402,7 @@ __device__ __forceinline__ void add_peer_partials(float (&v)[32], float* partial
     float4 t[8];
     float* ps = partials + (size_t)(peer * slot_stride + slot_offset) * kBM * BN;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) t[j] = ld_cg_f4(partial_at(ps, c32 * 8 + j, r));
+    for (int j = 0; j < 8; ++j) t[j] = ld_cg_f4(partial_at<BN>(ps, c32 * 8 + j, r, band));
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       v[4 * j] += t[j].x;
@@ -433,6 +443,77 @@ __device__ __forceinline__ int enc_in_boxes(const KernelParams& p, int u0, int u
   return n;
 }
 
+// LoadPartials through the idle stage ring (one epilogue warp, its 32-row
+// quadrant q of the tile): every peer's band of the quadrant in half-band
+// pieces (two per peer), `slots` pieces in flight through
+// `qring`, each folded into the accumulator columns in TMEM as it lands.
+// bars[0, slots) are this warp's piece barriers (fresh: parities start at 0).
+// Returns false after a timeout, with every copy it issued landed.
+template <int BN>
+static __device__ __noinline__ bool fixup_through_ring(uint8_t* qring, int slots,
+                                                       const float* rpartials, int unit,
+                                                       int peer_last, int slot_stride, int crank,
+                                                       int q, int lane, uint32_t tacc,
+                                                       uint64_t* bars, const KernelParams& p,
+                                                       Aux* aux, uint64_t limit) {
+  constexpr uint32_t kHalf = kPartialBandBytes<BN> / 2;
+  const int items = 2 * (peer_last - unit);  // (peer, half) pieces
+  auto issue = [&](int i) {
+    const int sl = i % slots;
+    const int slot_i = (unit + 1 + (i >> 1)) * slot_stride + crank;
+    const float* src = rpartials + (size_t)slot_i * kBM * BN + (size_t)q * 32 * BN +
+                       (size_t)(i & 1) * (kHalf / 4);
+    mbar_arrive_expect_tx(&bars[sl], kHalf);
+    bulk_load_g2s(qring + sl * kHalf, src, kHalf, &bars[sl]);
+  };
+  const int first = min(slots, items);
+  if (lane == 0) {
+    fence_proxy_async_global();
+    for (int i = 0; i < first; ++i) issue(i);
+  }
+  __syncwarp();
+  int issued = first;
+  bool fine = true;
+  int i = 0;
+  for (; i < items; ++i) {
+    const int sl = i % slots;
+    fine = __all_sync(0xffffffffu, wait_bar(&bars[sl], (uint32_t)((i / slots) & 1), aux, limit));
+    if (!fine) break;
+    const int h = i & 1;
+#pragma unroll 1
+    for (int c32 = h * (BN / 64); c32 < (h + 1) * (BN / 64); ++c32) {
+      uint32_t u[32];
+      tmem_ld32(tacc + c32 * 32, u);
+      const uint8_t* src = qring + sl * kHalf + (c32 - h * (BN / 64)) * 4096 + lane * 16;
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const float4 t = *reinterpret_cast<const float4*>(src + jj * 512);
+        u[4 * jj] = __float_as_uint(f32_of(u[4 * jj]) + t.x);
+        u[4 * jj + 1] = __float_as_uint(f32_of(u[4 * jj + 1]) + t.y);
+        u[4 * jj + 2] = __float_as_uint(f32_of(u[4 * jj + 2]) + t.z);
+        u[4 * jj + 3] = __float_as_uint(f32_of(u[4 * jj + 3]) + t.w);
+      }
+      tmem_st32(tacc + c32 * 32, u);
+    }
+    // The slot's reads are done before its next copy lands.
+    __syncwarp();
+    fence_proxy_async_smem();
+    if (lane == 0 && issued < items) issue(issued);
+    issued += issued < items ? 1 : 0;
+    __syncwarp();
+  }
+  if (!fine) {
+    // Never leave with a copy in flight into the ring.
+    if (lane == 0) {
+      if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+      for (int j = i; j < issued; ++j)
+        wait_bar(&bars[j % slots], (uint32_t)((j / slots) & 1), aux, limit, false);
+    }
+    __syncwarp();
+  }
+  return fine;
+}
+
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     skg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -459,6 +540,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* c0_bar = tempty_bar + 2;
   uint64_t* drain_bar = c0_bar + 4;
+  uint64_t* fix_bar = drain_bar + 1;  // [epilogue warp][slot]: staged peer partials
+  uint64_t* c0r_bar = fix_bar + 4 * kFixSlots;  // per epilogue warp: C0 staged in the ring
+  static_assert(2 * 8 + 2 + 2 + 4 + 1 + 4 * kFixSlots + 4 <= 48, "barrier slots");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -500,6 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 4; ++i) mbar_init(&c0_bar[i], 1);
     mbar_init(drain_bar, 1);
+    for (int i = 0; i < 4 * kFixSlots; ++i) mbar_init(&fix_bar[i], 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&c0r_bar[i], 1);
     aux->abort_flag = 0;
     aux->nbad_r = aux->nbad_c = 0;
     aux->bad_row = aux->bad_col = -1;
@@ -809,6 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t aphase = 0;
     int bsel = 0;
     uint32_t c0_phase = 0;
+    bool c0r_pending = false;  // C0 copies into the ring not yet waited for
     int nseg = 0;
     bool store_ok = true;
     bool ck_ready = false;
@@ -911,12 +998,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++nseg;
       const bool is_ck = w.tile < s.t_ck;  // a fused checksum-GEMM tile
+      // The CTA's last work item: once its accumulator is full, no copy or
+      // MMA touches the stage ring again.
+      bool last_item;
+      {
+        Cursor peek = cur;
+        Work wn;
+        last_item = !peek.next(s, wn);
+      }
       int tm = 0, tn = 0;
       if (!is_ck) tile_coords(s, w.tile, tm, tn);
       // This CTA's 128-row tile: a pair tile is two of them.
       if (C::PAIR) tm = 2 * tm + (int)crank;
       const int m0 = tm * kBM;
       const int n0 = tn * BN;
+      // beta != 0: pull this warp's rows of C0 into L2 while the mainloop
+      // runs, so the epilogue's C0 loads do not wait on DRAM.
+      if (p.beta != 0.f && !is_ck && w.role != kRolePeer && lane == 0 && m0 + q * 32 < p.m) {
+#pragma unroll 1
+        for (int c = 0; c < BN / C::EPI_COLS && n0 + c * C::EPI_COLS < p.n; ++c)
+          tma_prefetch_l2_2d(&tmC, n0 + c * C::EPI_COLS, m0 + q * 32);
+      }
 
       // Inputs of this tile's ABFT check that do not depend on its
       // accumulator (the encode pass's maxima and scales, the reference
@@ -1004,7 +1106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tacc + c32 * 32, u);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            st_cg_f4(partial_at(my_slot, c32 * 8 + j, r),
+            st_cg_f4(partial_at<BN>(my_slot, c32 * 8 + j, r, w.region == 0),
                      make_float4(f32_of(u[4 * j]), f32_of(u[4 * j + 1]), f32_of(u[4 * j + 2]),
                                  f32_of(u[4 * j + 3])));
         }
@@ -1042,6 +1144,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
         }
+        // The CTA's last output tile: once its accumulator is full the stage
+        // ring is idle, so each epilogue warp takes a quarter of it and
+        // fetches what its 32 rows still need with bulk copies in flight
+        // together, rather than one round trip per 32-column chunk:
+        //  - beta != 0: the quadrant's rows of C0, read by the store pass;
+        //  - LoadPartials (owner): every peer's band of this quadrant, in
+        //    half-band pieces through a few pipelined slots, folded into the
+        //    accumulator in TMEM, so the passes below see it fixed up.
+        // (Runs at most once per CTA, so the barrier parities start at 0.)
+        bool add_partials = owner;
+        bool c0_ring = false;
+        constexpr uint32_t kQuarter = (uint32_t)(STAGES * C::STAGE_BYTES / 4) & ~1023u;
+        constexpr uint32_t kC0Bytes = 32u * BN * C::OUT_BYTES;
+        constexpr uint32_t kC0Off = (kQuarter - kC0Bytes) & ~1023u;
+        constexpr uint32_t kHalf = kPartialBandBytes<BN> / 2;
+        static_assert(kC0Bytes <= kQuarter && kC0Off >= kHalf, "ring quarter too small");
+        uint8_t* qring = ring + ew * kQuarter;
+        if (last_item && !is_ck && w.role != kRolePeer) {
+          c0_ring = p.beta != 0.f && m0 + q * 32 < p.m;  // warp-uniform
+          if (c0_ring && lane == 0) {
+            int nbox = 0;
+            while (nbox < BN / C::EPI_COLS && n0 + nbox * C::EPI_COLS < p.n) ++nbox;
+            mbar_arrive_expect_tx(&c0r_bar[ew], (uint32_t)nbox * C::EPI_BUF_BYTES);
+            for (int c = 0; c < nbox; ++c)
+              tma_load_2d(qring + kC0Off + c * C::EPI_BUF_BYTES, &tmC, &c0r_bar[ew],
+                          n0 + c * C::EPI_COLS, m0 + q * 32);
+          }
+          c0r_pending = c0_ring;
+        }
+        if (owner && !is_ck && last_item) {
+          const uint32_t room = c0_ring ? kC0Off : kQuarter;
+          const int slots = min(kFixSlots, (int)(room / kHalf));
+          const bool fine = fixup_through_ring<BN>(
+              qring, slots, rpartials, unit, w.peer_last, slot_stride, (int)crank, q, lane, tacc,
+              &fix_bar[ew * kFixSlots], p, aux, limit);
+          if (!epi_all(fine && !aborted(aux))) {
+            tc_fence_before();
+            release_acc(ab);
+            break;
+          }
+          add_partials = false;
+        }
 
         if (C::ABFT && is_ck) {
           // -------------------------------------------- fused checksum tile
@@ -1061,8 +1205,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tacc + c * 32, u);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
-            if (owner) add_peer_partials<BN>(v, rpartials, unit + 1, w.peer_last, c, r, slot_stride,
-                                            (int)crank);
+            if (owner)
+              add_peer_partials<BN>(v, rpartials, unit + 1, w.peer_last, c, r, w.region == 0,
+                                    slot_stride, (int)crank);
             if (c == nchunks - 1) {
               tc_fence_before();
               release_acc(ab);
@@ -1114,8 +1259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
-            if (owner) add_peer_partials<BN>(v, rpartials, unit + 1, w.peer_last, c32, r, slot_stride,
-                                            (int)crank);
+            if (add_partials)
+              add_peer_partials<BN>(v, rpartials, unit + 1, w.peer_last, c32, r, w.region == 0,
+                                    slot_stride, (int)crank);
             // Fault injection: one bit of one fp32 accumulator, after the
             // fixup and before the check (warp-uniform chunk selection).
             const bool inj_chunk = inject_here && (p.inject_row >> 5) == q &&
@@ -1129,7 +1275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   v[i] = __uint_as_float(__float_as_uint(v[i]) ^ (1u << p.inject_bit));
                 }
             }
-            if (owner || inj_chunk) {
+            if (add_partials || inj_chunk) {
               uint32_t wv[32];
 #pragma unroll
               for (int i = 0; i < 32; ++i) wv[i] = __float_as_uint(v[i]);
@@ -1296,6 +1442,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool rows_live = (m0 + q * 32) < p.m;
 #pragma unroll 1
         for (int c = 0; c < BN / C::EPI_COLS; ++c) {
+          const int col0 = n0 + c * C::EPI_COLS;
+          const bool st_chunk = rows_live && col0 < p.n && store_ok;  // warp-uniform
+          uint8_t* buf = ebuf + bsel * C::EPI_BUF_BYTES;
+          if (st_chunk) {
+            // Free the staging buffer and start its C0 load before the
+            // accumulator columns are read, so the latencies overlap.
+            if (lane == 0) bulk_wait_read<C::EPI_BUFS - 1>();
+            __syncwarp();
+            if (p.beta != 0.f && !c0_ring && lane == 0) {
+              mbar_arrive_expect_tx(&c0_bar[ew], C::EPI_BUF_BYTES);
+              tma_load_2d(buf, &tmC, &c0_bar[ew], col0, m0 + q * 32);
+            }
+          }
           float y[C::EPI_COLS];
 #pragma unroll
           for (int hh = 0; hh < C::EPI_COLS / 32; ++hh) {
@@ -1305,9 +1464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tacc + c32 * 32, u);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
-            if (!C::ABFT && owner)
-              add_peer_partials<BN>(v, rpartials, unit + 1, w.peer_last, c32, r, slot_stride,
-                                            (int)crank);
+            if (!C::ABFT && add_partials)
+              add_peer_partials<BN>(v, rpartials, unit + 1, w.peer_last, c32, r, w.region == 0,
+                                    slot_stride, (int)crank);
 #pragma unroll
             for (int i = 0; i < 32; ++i) y[hh * 32 + i] = v[i];
             if (!C::ABFT) {
@@ -1331,25 +1490,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             release_acc(ab);
           }
-          const int col0 = n0 + c * C::EPI_COLS;
-          if (!rows_live || col0 >= p.n || !store_ok) continue;  // warp-uniform
-          uint8_t* buf = ebuf + bsel * C::EPI_BUF_BYTES;
-          if (lane == 0) bulk_wait_read<C::EPI_BUFS - 1>();
-          __syncwarp();
+          if (!st_chunk) continue;
           if (p.beta != 0.f) {
-            if (lane == 0) {
-              mbar_arrive_expect_tx(&c0_bar[ew], C::EPI_BUF_BYTES);
-              tma_load_2d(buf, &tmC, &c0_bar[ew], col0, m0 + q * 32);
+            const uint8_t* c0src = buf;
+            bool got_c0;
+            if (c0_ring) {
+              got_c0 = !c0r_pending ||
+                       __all_sync(0xffffffffu, wait_bar(&c0r_bar[ew], 0, aux, limit));
+              if (got_c0) c0r_pending = false;
+              c0src = qring + kC0Off + c * C::EPI_BUF_BYTES;
+            } else {
+              got_c0 = __all_sync(0xffffffffu, wait_bar(&c0_bar[ew], c0_phase, aux, limit));
             }
-            const bool got_c0 = __all_sync(0xffffffffu, wait_bar(&c0_bar[ew], c0_phase, aux, limit));
             if (!got_c0) {
               if (lane == 0 && !aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
               store_ok = false;  // stop storing; the next tile boundary exits
               continue;
             }
-            c0_phase ^= 1;
+            if (!c0_ring) c0_phase ^= 1;
             uint32_t w0[32];
-            staging_read(buf, lane, w0);
+            staging_read(c0src, lane, w0);
             float c0v[C::EPI_COLS];
             unpack_row<C::OUT>(w0, c0v);
 #pragma unroll
@@ -1375,7 +1535,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         aphase ^= 1;
       }
     }
-    if (lane == 0) bulk_wait<0>();
+    // C0 copies into the ring that an early exit left unwaited land before
+    // the CTA leaves; output stores only need to have read their staging
+    // (the grid's completion makes the writes visible to later work).
+    if (c0r_pending && lane == 0) wait_bar(&c0r_bar[ew], 0, aux, limit, false);
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
   }
 
