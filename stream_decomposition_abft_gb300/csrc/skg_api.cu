@@ -95,8 +95,10 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
   r.abft = o->abft ? 1 : 0;
   const int want_sched = o->sched == SKG_SCHED_AUTO ? -1 : o->sched;
   const int want_grid = o->grid > 0 ? o->grid : (want_sched >= 0 ? ms : 0);
+  // Launches without ABFT reduce shared tiles together (the model knows).
+  const bool share = !o->abft;
   const Plan pl = choose_plan(m > 0 ? m : 1, n > 0 ? n : 1, k > 0 ? k : 1, o->tile_n, want_sched,
-                              want_grid, ms);
+                              want_grid, ms, 0, true, share);
   r.sched = pl.sched;
   r.grid = pl.grid;
   r.grid_ck = 0;
@@ -124,7 +126,7 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
     const int want_pairs = o->grid > 0 ? o->grid / 2 : (want_sched >= 0 ? clusters : 0);
     const int64_t m_pairs = ((m > 0 ? m : 1) + 2 * kBM - 1) / (2 * kBM) * kBM;
     const Plan pp = choose_plan(m_pairs, n > 0 ? n : 1, k > 0 ? k : 1, 256, want_sched,
-                                want_pairs, clusters);
+                                want_pairs, clusters, 0, true, share);
     r.pair = 1;
     r.bn = 256;
     r.sched = pp.sched;
@@ -382,6 +384,8 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   p.trace = r.trace;
   p.cta_clock = r.cta_clock;
   p.drop_signal = r.drop_signal;
+  p.c_ptr = g.C;
+  p.ldc = g.ldc;
 
   cudaError_t e;
   if (r.pair)
@@ -453,7 +457,7 @@ void replan_fused(int64_t m, int64_t n, const skg_opts_t* opts, Resolved& r) {
     const int t_ck = (int)((tm + 1) / 2 + (tn + 1) / 2);
     const int64_t m_pairs = (m + 2 * kBM - 1) / (2 * kBM) * kBM;
     const Plan pp = choose_plan(m_pairs, n, r.k_for_plan, 256, want_sched,
-                                want_sched >= 0 ? clusters : 0, clusters, t_ck, false);
+                                want_sched >= 0 ? clusters : 0, clusters, t_ck, false, false);
     r.grid = 2 * pp.grid;
     r.sched = pp.sched;
     r.grid_ck = 0;
@@ -461,7 +465,7 @@ void replan_fused(int64_t m, int64_t n, const skg_opts_t* opts, Resolved& r) {
   }
   const int t_ck = (int)((m + kBM - 1) / kBM + (n + kBM - 1) / kBM);
   const Plan pl = choose_plan(m, n, r.k_for_plan, r.bn, want_sched,
-                              want_sched >= 0 ? r.ws_grid : 0, r.ws_grid, t_ck);
+                              want_sched >= 0 ? r.ws_grid : 0, r.ws_grid, t_ck, true, false);
   r.grid = pl.grid;
   r.sched = pl.sched;
   r.grid_ck = pl.grid_ck;
@@ -657,7 +661,7 @@ skg_status_t skg_schedule_cost(int64_t m, int64_t n, int64_t k, int32_t bm, int3
   if (bm != kTileM || bk != kTileK || (bn != 128 && bn != 256)) return SKG_ERR_UNSUPPORTED;
   if (sched < SKG_SCHED_DP || sched > SKG_SCHED_SK2_DP) return SKG_ERR_ARG;
   const Schedule s = make_schedule(m, n, k, bm, bn, bk, g, sched);
-  *us = predict_us(s, bn == 128 ? kModel128 : kModel256);
+  *us = predict_us(s, bn == 128 ? kModel128 : kModel256, true);
   return SKG_OK;
 }
 

@@ -58,7 +58,8 @@ constexpr int kEpiThreads = 128;
 static_assert(kThreads == 64 + kEpiThreads && kEpiThreads == 128,
               "epi_all and the named barriers count the four epilogue warps");
 constexpr int kEncRows = 2;  // hi and lo terms of each encoding
-constexpr int kFixSlots = 4;  // per epilogue warp: staged partial pieces in flight
+constexpr int kFixSlots = 6;  // per epilogue warp: staged partial pieces in flight
+constexpr int kAuxBytes = 1024;  // shared-memory bookkeeping (struct Aux) after the staging
 constexpr uint32_t kSmemLimit = 232448;
 
 // Workspace header (device). The report follows at offset 256.
@@ -138,7 +139,12 @@ struct KernelParams {
   int32_t* trace;
   uint64_t* cta_clock;
   int drop_signal;  // testing: CTA index that skips its Signal, or -1
+  // C (and C0) for the shared tile reduction's plain stores: ldc elements
+  // per row, the output type of the launch.
+  void* c_ptr;
+  int64_t ldc;
 };
+
 
 __host__ __device__ constexpr int pow2_at_least(int v) {
   int p = 32;
@@ -170,7 +176,7 @@ struct Cfg {
   static constexpr int EPI_BUF_BYTES = 32 * 128;
   static constexpr int EPI_BUFS = 2;
   static constexpr int EPI_BYTES = 4 * EPI_BUFS * EPI_BUF_BYTES;
-  static constexpr int AUX_BYTES = 512;
+  static constexpr int AUX_BYTES = kAuxBytes;
   // The ABFT column partial sums of warp q (BN floats) live in warp q's own
   // first staging buffer, which is idle while a tile is being verified.
   static_assert(BN * 4 <= EPI_BUF_BYTES, "column sums must fit one staging buffer");
@@ -186,7 +192,7 @@ struct Cfg {
 
 // Shared-memory bookkeeping that lives after the stage ring and staging.
 struct Aux {
-  uint64_t bars[48];      // full[S], empty[S], tfull[2], tempty[2], c0[4], drain, fix, c0r[4]
+  uint64_t bars[56];      // full[S], empty[S], tfull[2], tempty[2], c0[4], drain, fix, c0r[4]
   uint32_t tmem_slot;
   int32_t abort_flag;
   int32_t nbad_r, nbad_c, bad_row, bad_col;
@@ -195,7 +201,7 @@ struct Aux {
   float d_row, d_col;
   float tmax_a[4], tmax_b[4];  // per epilogue warp: partial tile maxima
 };
-static_assert(sizeof(Aux) <= 512, "aux size");
+static_assert(sizeof(Aux) <= kAuxBytes, "aux size");
 
 __device__ __forceinline__ void record_error(const KernelParams& p, Aux* aux, int code) {
   atomicOr(&p.report->status_bits, 1u << code);
@@ -514,6 +520,95 @@ static __device__ __noinline__ bool fixup_through_ring(uint8_t* qring, int slots
   return fine;
 }
 
+// Shared LoadPartials + StoreTile (no ABFT): a tile covered by CTAs
+// owner .. contrib_last of which owner .. part_last end their ranges in it.
+// Each of those stored its whole partial and signalled; after every cover's
+// flag is set, participant j = unit - owner reduces its share of the tile's
+// (32-row quadrant, 4-column group) items over all covers' partials in
+// ascending CTA order, then applies alpha / beta and stores C with plain
+// stores. The k=0 CTA no longer sums every peer alone, so no CTA of a deep,
+// many-way split tile waits on one SM's read bandwidth. Called by all 128
+// epilogue threads; false after a timeout.
+template <class C>
+static __device__ __noinline__ bool reduce_share(const KernelParams& p, float* rpartials,
+                                                 uint32_t* rflags, int owner, int contrib_last,
+                                                 int part_last, int unit, int slot_stride,
+                                                 int crank, int m0, int n0, int ew, int lane,
+                                                 uint32_t epoch, bool inject_here, Aux* aux,
+                                                 uint64_t limit) {
+  constexpr int BN = C::BN;
+  bool fine = true;
+  if (ew == 0) {
+    for (int u = owner + lane; u <= contrib_last && fine; u += 32) {
+      if (u == unit) continue;
+      const int fi = u * slot_stride + crank;
+      if (ld_acquire_gpu(&rflags[fi]) == epoch) continue;
+      const uint64_t t0 = globaltimer();
+      uint32_t spins = 0;
+      while (ld_acquire_gpu(&rflags[fi]) != epoch) {
+        if (++spins > 64) nanosleep_ns(64);
+        if ((spins & 15) == 0 && globaltimer() - t0 > limit) {
+          record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
+          fine = false;
+          break;
+        }
+      }
+    }
+  }
+  if (!epi_all(fine && !aborted(aux))) return false;
+  const int parts = part_last - owner + 1;
+  const int j = unit - owner;
+  const int items = 4 * (BN / 4);  // quadrant x 4-column group
+  const int per = items / parts, extra = items % parts;
+  const int ib = j * per + (j < extra ? j : extra);
+  const int ie = ib + per + (j < extra ? 1 : 0);
+  const int covers = contrib_last - owner + 1;
+  for (int t = ib + ew; t < ie; t += 4) {
+    const int qi = t / (BN / 4), c4 = t - qi * (BN / 4);
+    const int r = qi * 32 + lane;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < covers; c0 += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c0 + u < covers)
+          v[u] = ld_cg_f4(partial_at<BN>(
+              rpartials + (size_t)((owner + c0 + u) * slot_stride + crank) * kBM * BN, c4, r,
+              true));
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c0 + u < covers) {
+          acc.x += v[u].x;
+          acc.y += v[u].y;
+          acc.z += v[u].z;
+          acc.w += v[u].w;
+        }
+    }
+    const int64_t gr = (int64_t)m0 + r;
+    if (gr >= p.m) continue;
+    float y[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int col = n0 + 4 * c4 + e;
+      if (col >= p.n) continue;
+      if (inject_here && r == p.inject_row && 4 * c4 + e == p.inject_col)
+        y[e] = __uint_as_float(__float_as_uint(y[e]) ^ (1u << p.inject_bit));
+      const int64_t off = gr * p.ldc + col;
+      float c0v = 0.f;
+      if (p.beta != 0.f) {
+        if constexpr (C::OUT == 0) c0v = static_cast<const float*>(p.c_ptr)[off];
+        else if constexpr (C::OUT == 1) c0v = __half2float(static_cast<const __half*>(p.c_ptr)[off]);
+        else c0v = __bfloat162float(static_cast<const __nv_bfloat16*>(p.c_ptr)[off]);
+      }
+      const float out = p.alpha * y[e] + p.beta * c0v;
+      if constexpr (C::OUT == 0) static_cast<float*>(p.c_ptr)[off] = out;
+      else if constexpr (C::OUT == 1) static_cast<__half*>(p.c_ptr)[off] = __float2half_rn(out);
+      else static_cast<__nv_bfloat16*>(p.c_ptr)[off] = __float2bfloat16_rn(out);
+    }
+  }
+  return true;
+}
+
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     skg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -542,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain_bar = c0_bar + 4;
   uint64_t* fix_bar = drain_bar + 1;  // [epilogue warp][slot]: staged peer partials
   uint64_t* c0r_bar = fix_bar + 4 * kFixSlots;  // per epilogue warp: C0 staged in the ring
-  static_assert(2 * 8 + 2 + 2 + 4 + 1 + 4 * kFixSlots + 4 <= 48, "barrier slots");
+  static_assert(2 * 8 + 2 + 2 + 4 + 1 + 4 * kFixSlots + 4 <= 56, "barrier slots");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1036,7 +1131,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (s.t_ck > 0 && !ck_ready) {
           // The fused checksum tiles must all be stored first. Every CTA runs
           // its own share of them before its first output tile, and dedicated
-          // checksum CTAs wait for nothing, so this wait ends.
+          // checksum CTAs wait only for each other (all resident), so this
+          // wait ends.
           bool fine = true;
           if (et == 0) {
             const uint64_t t0 = globaltimer();
@@ -1098,7 +1194,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           !is_ck ? BN / 32
                  : ((w.tile < p.ck_cr_tiles ? p.ck_n_cr : p.ck_n_cc) + 31) / 32;
 
-      if (w.role == kRolePeer) {
+      // Shared reduction of a tile that at least kShareMin CTAs end in (all
+      // of them store partials, the owner too, which holds no other one; see
+      // reduce_share).
+      const bool share = !C::ABFT && w.region == 0 && w.role != kRoleFull &&
+                         w.share_parts >= kShareMin && unit <= w.part_last;
+      if (w.role == kRolePeer || share) {
         // StorePartials + Signal (Algorithm 5, non-started segment).
 #pragma unroll 1
         for (int c32 = 0; c32 < live_chunks; ++c32) {
@@ -1117,13 +1218,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           __threadfence();
           st_release_gpu(&rflags[my_slot_idx], epoch);
         }
+        if (share && !reduce_share<C>(p, rpartials, rflags, w.owner, w.contrib_last, w.part_last,
+                                      unit, slot_stride, (int)crank, m0, n0, ew, lane, epoch,
+                                      out_tile == p.inject_tile, aux, limit))
+          break;
       } else {
         const bool owner = (w.role == kRoleOwner);
         if (owner) {
-          // Wait for every later CTA that covers part of this tile.
+          // Wait for every later CTA that covers part of this tile: the
+          // lanes of one warp poll up to 32 peers' flags at once.
           bool fine = true;
-          if (et == 0) {
-            for (int peer = unit + 1; peer <= w.peer_last && fine; ++peer) {
+          if (ew == 0) {
+            for (int peer = unit + 1 + lane; peer <= w.peer_last && fine; peer += 32) {
               const int fi = peer * slot_stride + (int)crank;
               if (ld_acquire_gpu(&rflags[fi]) == epoch) continue;
               const uint64_t t0 = globaltimer();

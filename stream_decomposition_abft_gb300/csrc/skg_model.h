@@ -35,9 +35,31 @@ struct CostModel {
 constexpr CostModel kModel128 = {2.64, 0.334, 0.17, 4.67, 1.03};
 constexpr CostModel kModel256 = {3.47, 0.364, 0.00, 8.18, 1.73};
 
-// Segment counts of CTA x in an evenly split region of `total` iterations.
-inline void region_counts(int64_t q, int r, int64_t total, int64_t I, int x, int64_t& iters,
-                          int64_t& tiles, int64_t& partial, int64_t& peers) {
+// Whether the tile starting at iteration ti of an evenly split region is
+// reduced by its covering CTAs together (see Work::share_parts): its owner's
+// range starts at ti and at least kShareMin covering CTAs end in it. Gives
+// the number of those (parts) and of all covering CTAs (covers).
+inline bool shared_tile(int64_t q, int r, int64_t ti, int64_t I, int& parts, int& covers) {
+  const int owner = even_cta_of(q, r, ti);
+  int64_t ob, oe;
+  even_range(q, r, owner, ob, oe);
+  if (ob != ti) return false;
+  const int last = even_cta_of(q, r, ti + I - 1);
+  int64_t lb, le;
+  even_range(q, r, last, lb, le);
+  const int part_last = last - (le > ti + I ? 1 : 0);
+  parts = part_last - owner + 1;
+  covers = last - owner + 1;
+  return parts >= kShareMin;
+}
+
+// Segment counts of CTA x in an evenly split region of `total` iterations;
+// `fix` counts the partial tiles' worth of fixup reads. With `share`
+// (launches without ABFT) a shared tile costs each of its parts one partial
+// store and covers / parts partial tiles of reads instead of the owner
+// reading every peer.
+inline void region_counts(int64_t q, int r, int64_t total, int64_t I, int x, bool share,
+                          int64_t& iters, int64_t& tiles, int64_t& partial, double& fix) {
   if (total <= 0) return;
   int64_t b, e;
   even_range(q, r, x, b, e);
@@ -45,36 +67,53 @@ inline void region_counts(int64_t q, int r, int64_t total, int64_t I, int x, int
   iters += e - b;
   if (b % I != 0) partial += 1;
   const int64_t first = (b % I == 0) ? b : (b / I + 1) * I;
+  int parts = 0, covers = 0;
   if (first < e) {
     const int64_t started = (e - 1 - first) / I + 1;
     tiles += started;
     const int64_t last = first + (started - 1) * I;
-    if (last + I > e) peers += even_cta_of(q, r, last + I - 1) - x;
+    if (last + I > e) {  // owns an unfinished tile
+      if (share && shared_tile(q, r, last, I, parts, covers)) {
+        partial += 1;
+        fix += (double)covers / parts;
+      } else {
+        fix += even_cta_of(q, r, last + I - 1) - x;
+      }
+    }
+  } else if (share && shared_tile(q, r, (b / I) * I, I, parts, covers)) {
+    // The whole range lies inside a tile another CTA started and owns.
+    fix += (double)covers / parts;
   }
 }
 
 // Predicted time (us) of one launch with schedule s: max over CTAs. O(g).
 // Side-tile iterations (fused checksum GEMMs) are costed like output ones.
-inline double predict_us(const Schedule& s, const CostModel& M) {
+// `share`: the launch reduces shared tiles together (no ABFT).
+inline double predict_us(const Schedule& s, const CostModel& M, bool share) {
   if (s.t == 0 || s.ipt == 0) return 0.0;
   const int64_t I = s.ipt;
   double worst = 0.0;
   for (int x = 0; x < s.g; ++x) {
-    int64_t iters = 0, tiles = 0, partial = 0, peers = 0;
+    int64_t iters = 0, tiles = 0, partial = 0;
+    double fix = 0.0;
     if (x < s.t_dp) {
       const int64_t nd = (s.t_dp - 1 - x) / s.g + 1;
       iters += nd * I;
       tiles += nd;
     }
-    region_counts(s.sk_q, s.sk_r, s.sk_total, I, x, iters, tiles, partial, peers);
-    region_counts(s.ck_q, s.ck_r, s.ck_total, I, x, iters, tiles, partial, peers);
+    region_counts(s.sk_q, s.sk_r, s.sk_total, I, x, share, iters, tiles, partial, fix);
+    if (s.g_ck == 0)
+      region_counts(s.ck_q, s.ck_r, s.ck_total, I, x, false, iters, tiles, partial, fix);
     const double tx = M.a + M.c * (double)iters + M.e * (double)tiles + M.b * (double)partial +
-                      M.d * (double)peers;
+                      M.d * fix;
     if (tx > worst) worst = tx;
   }
-  if (s.g_ck > 0) {  // dedicated side CTAs: whole side tiles
-    const int64_t nt = (s.t_ck + s.g_ck - 1) / s.g_ck;
-    const double tx = M.a + M.c * (double)(nt * I) + M.e * (double)nt;
+  for (int x = 0; x < s.g_ck; ++x) {  // dedicated side CTAs: the side region split over them
+    int64_t iters = 0, tiles = 0, partial = 0;
+    double fix = 0.0;
+    region_counts(s.ck_q, s.ck_r, s.ck_total, I, x, false, iters, tiles, partial, fix);
+    const double tx = M.a + M.c * (double)iters + M.e * (double)tiles + M.b * (double)partial +
+                      M.d * fix;
     if (tx > worst) worst = tx;
   }
   return worst;
@@ -89,7 +128,7 @@ struct Plan {
 // Best (BLK_N, schedule, g) for an m x n x k launch on `sms` SMs. Fixed
 // choices (want_* != 0 / >= 0) are kept; the rest are searched.
 inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_sched,
-                        int want_grid, int sms, int t_ck, bool side_ctas = true) {
+                        int want_grid, int sms, int t_ck, bool side_ctas, bool share) {
   static const int kCands[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 76, 96, 112, 128, 144};
   Plan best{want_bn ? want_bn : 256, want_sched >= 0 ? want_sched : kSchedSK2DP,
             want_grid ? want_grid : sms, 1e300, 0};
@@ -133,7 +172,7 @@ inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_s
           const int gck = gck_opts[oi];
           const Schedule s =
               make_schedule(m, n, k, kTileM, bn, kTileK, cands[i], sched, t_ck, gck);
-          const double us = predict_us(s, M);
+          const double us = predict_us(s, M, share);
           // Prefer fewer CTAs on ties (less fixup storage and traffic).
           if (us < best.us - 1e-9 ||
               (us < best.us + 1e-9 && cands[i] + gck < best.grid + best.grid_ck)) {
@@ -149,32 +188,35 @@ inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_s
 // search_plan behind a small cache: the search walks up to ~150 candidate
 // schedules of up to `sms` CTAs each, far more host time than a launch.
 inline Plan choose_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_sched,
-                        int want_grid, int sms, int t_ck = 0, bool side_ctas = true) {
+                        int want_grid, int sms, int t_ck = 0, bool side_ctas = true,
+                        bool share = true) {
   struct Key {
     int64_t m, n, k;
-    int bn, sched, grid, sms, t_ck, side;
+    int bn, sched, grid, sms, t_ck, side, share;
     bool operator==(const Key& o) const {
       return m == o.m && n == o.n && k == o.k && bn == o.bn && sched == o.sched &&
-             grid == o.grid && sms == o.sms && t_ck == o.t_ck && side == o.side;
+             grid == o.grid && sms == o.sms && t_ck == o.t_ck && side == o.side &&
+             share == o.share;
     }
   };
   struct Hash {
     size_t operator()(const Key& x) const {
       uint64_t h = 1469598103934665603ull;
-      const int64_t v[9] = {x.m, x.n, x.k, x.bn, x.sched, x.grid, x.sms, x.t_ck, x.side};
+      const int64_t v[10] = {x.m, x.n, x.k, x.bn, x.sched, x.grid, x.sms, x.t_ck, x.side, x.share};
       for (int64_t e : v) h = (h ^ (uint64_t)e) * 1099511628211ull;
       return (size_t)h;
     }
   };
   static std::mutex mu;
   static std::unordered_map<Key, Plan, Hash> cache;
-  const Key key{m, n, k, want_bn, want_sched, want_grid, sms, t_ck, side_ctas ? 1 : 0};
+  const Key key{m, n, k, want_bn, want_sched, want_grid, sms, t_ck, side_ctas ? 1 : 0,
+                share ? 1 : 0};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
-  const Plan p = search_plan(m, n, k, want_bn, want_sched, want_grid, sms, t_ck, side_ctas);
+  const Plan p = search_plan(m, n, k, want_bn, want_sched, want_grid, sms, t_ck, side_ctas, share);
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();
   cache.emplace(key, p);

@@ -37,6 +37,11 @@ constexpr int kTileM = 128;
 constexpr int kTileK = 64;
 enum : int { kRoleFull = 0, kRoleOwner = 1, kRolePeer = 2 };
 
+// Tiles of an output Stream-K region that this many covering CTAs end their
+// ranges in, the k = 0 CTA's range starting at the tile, are reduced by all
+// of those together in launches without ABFT (Work::share_parts).
+constexpr int kShareMin = 3;
+
 struct Schedule {
   int tiles_m, tiles_n;
   int ipt;            // MAC iterations per tile, ceil(k / BLK_K)
@@ -47,10 +52,11 @@ struct Schedule {
   int64_t sk_total;   // Stream-K iterations of the output tiles after the DP ones
   int64_t sk_q;       // floor(sk_total / g)
   int sk_r;           // sk_total mod g
-  int64_t ck_total;   // side-tile iterations split over the g CTAs (0 with g_ck)
-  int64_t ck_q;       // floor(ck_total / g)
-  int ck_r;           // ck_total mod g
-  int g_ck;           // dedicated side CTAs g .. g + g_ck - 1 (0: side tiles split)
+  int64_t ck_total;   // side-tile iterations, split over the g CTAs or, with
+                      // g_ck > 0, over the dedicated side CTAs
+  int64_t ck_q;       // floor(ck_total / (g_ck ? g_ck : g))
+  int ck_r;           // ck_total mod (g_ck ? g_ck : g)
+  int g_ck;           // dedicated side CTAs g .. g + g_ck - 1 (0: none)
   int band;           // tile columns per raster band (tiles_n = row-major)
 };
 
@@ -78,12 +84,12 @@ SKG_HD int dp_tiles(int t, int g, int mode) {
 
 // The page's schedule over the output tiles (DP tiles first, then the
 // Stream-K region) on g CTAs, plus `t_ck` full-k side tiles (the fused ABFT
-// checksum GEMMs), placed one of two ways:
-//   - g_ck == 0: a region of their own whose iterations are split evenly
-//     over the g CTAs, so every CTA starts with the same small share of side
-//     work, whatever the schedule of the output tiles;
-//   - g_ck > 0: whole tiles on g_ck more CTAs (side tile j on CTA
-//     g + j mod g_ck), for launches that leave SMs idle.
+// checksum GEMMs) in a Stream-K region of their own (own partial slots and
+// flags), its iterations split evenly either
+//   - g_ck == 0: over the g CTAs, so every CTA starts with the same small
+//     share of side work, whatever the schedule of the output tiles; or
+//   - g_ck > 0: over g_ck more CTAs that run nothing else, for launches that
+//     leave SMs idle (g_ck = t_ck gives one whole side tile each).
 SKG_HD Schedule make_schedule(int64_t m, int64_t n, int64_t k, int bm, int bn, int bk, int g,
                               int mode, int t_ck = 0, int g_ck = 0) {
   Schedule s;
@@ -99,9 +105,10 @@ SKG_HD Schedule make_schedule(int64_t m, int64_t n, int64_t k, int bm, int bn, i
   s.sk_q = s.sk_total / g;
   s.sk_r = (int)(s.sk_total % g);
   s.g_ck = s.t_ck > 0 ? g_ck : 0;
-  s.ck_total = s.g_ck > 0 ? 0 : (int64_t)s.t_ck * s.ipt;
-  s.ck_q = s.ck_total / g;
-  s.ck_r = (int)(s.ck_total % g);
+  s.ck_total = (int64_t)s.t_ck * s.ipt;
+  const int ck_ctas = s.g_ck > 0 ? s.g_ck : g;
+  s.ck_q = s.ck_total / ck_ctas;
+  s.ck_r = (int)(s.ck_total % ck_ctas);
   s.band = s.tiles_n > 0 ? s.tiles_n : 1;
   return s;
 }
@@ -134,6 +141,12 @@ struct Work {
   int role;
   int peer_last;         // OWNER: last peer CTA (peers are cta+1 .. peer_last)
   int region;            // 0: output tiles, 1: side tiles (own partial slots and flags)
+  // CTAs covering the tile: owner .. contrib_last; those up to part_last
+  // end their ranges inside it (the tile is their last work in the region).
+  // share_parts = part_last - owner + 1 when the owner's range also begins
+  // at the tile's first iteration (so the owner holds no other partial in
+  // the region), else 0.
+  int owner, contrib_last, part_last, share_parts;
 };
 
 // Walks one CTA's segments in execution order: its share of the side
@@ -142,26 +155,30 @@ struct Work {
 struct Cursor {
   int x;
   int next_dp;
-  int next_side;  // dedicated side CTA: next side tile, else -1
+  int ck_base;  // first CTA of the split side region (g for dedicated side CTAs)
   int64_t ck_it, ck_end;
   int64_t it, it_end;
 
   SKG_HD void init(const Schedule& s, int cta) {
     x = cta;
     next_dp = cta;
-    next_side = -1;
+    ck_base = 0;
     it = it_end = ck_it = ck_end = 0;
     if (cta >= s.g) {
-      next_side = cta - s.g;
+      // Dedicated side CTA: its share of the side region, nothing else.
+      next_dp = s.t_dp;
+      ck_base = s.g;
+      if (s.ck_total > 0) even_range(s.ck_q, s.ck_r, cta - s.g, ck_it, ck_end);
       return;
     }
     if (s.sk_total > 0) sk_range(s, cta, it, it_end);
-    if (s.ck_total > 0) even_range(s.ck_q, s.ck_r, cta, ck_it, ck_end);
+    if (s.ck_total > 0 && s.g_ck == 0) even_range(s.ck_q, s.ck_r, cta, ck_it, ck_end);
   }
 
   // Next segment of a split region whose tiles start at `base`.
+  // CTA indices of the split are cta_base + (index within the split).
   SKG_HD static void cut(const Schedule& s, int64_t q, int r, int base, int region, int x,
-                         int64_t& pos, int64_t end, Work& w) {
+                         int cta_base, int64_t& pos, int64_t end, Work& w) {
     const int64_t tile_rel = pos / s.ipt;
     const int64_t tile_iter = tile_rel * s.ipt;
     const int64_t tile_iter_end = tile_iter + s.ipt;
@@ -171,25 +188,24 @@ struct Cursor {
     w.kb_begin = (int)(pos - tile_iter);
     w.kb_end = (int)((end < tile_iter_end ? end : tile_iter_end) - tile_iter);
     w.role = !started ? kRolePeer : (ended ? kRoleFull : kRoleOwner);
-    w.peer_last = (w.role == kRoleOwner) ? even_cta_of(q, r, tile_iter_end - 1) : x;
+    const int last_rel = even_cta_of(q, r, tile_iter_end - 1);
+    int64_t last_b, last_e;
+    even_range(q, r, last_rel, last_b, last_e);
+    const int owner_rel = even_cta_of(q, r, tile_iter);
+    int64_t owner_b, owner_e;
+    even_range(q, r, owner_rel, owner_b, owner_e);
+    w.owner = cta_base + owner_rel;
+    w.contrib_last = cta_base + last_rel;
+    w.part_last = w.contrib_last - (last_e > tile_iter_end ? 1 : 0);
+    w.share_parts = owner_b == tile_iter ? w.part_last - w.owner + 1 : 0;
+    w.peer_last = (w.role == kRoleOwner) ? w.contrib_last : x;
     w.region = region;
     pos = tile_iter_end;
   }
 
   SKG_HD bool next(const Schedule& s, Work& w) {
-    if (next_side >= 0) {
-      if (next_side >= s.t_ck) return false;
-      w.tile = next_side;
-      w.kb_begin = 0;
-      w.kb_end = s.ipt;
-      w.role = kRoleFull;
-      w.peer_last = x;
-      w.region = 1;
-      next_side += s.g_ck;
-      return true;
-    }
     if (ck_it < ck_end) {
-      cut(s, s.ck_q, s.ck_r, 0, 1, x, ck_it, ck_end, w);
+      cut(s, s.ck_q, s.ck_r, 0, 1, x, ck_base, ck_it, ck_end, w);
       return true;
     }
     if (next_dp < s.t_dp) {
@@ -199,11 +215,13 @@ struct Cursor {
       w.role = kRoleFull;
       w.peer_last = x;
       w.region = 0;
+      w.owner = w.contrib_last = w.part_last = x;
+      w.share_parts = 0;
       next_dp += s.g;
       return true;
     }
     if (it < it_end) {
-      cut(s, s.sk_q, s.sk_r, s.t_ck + s.t_dp, 0, x, it, it_end, w);
+      cut(s, s.sk_q, s.sk_r, s.t_ck + s.t_dp, 0, x, 0, it, it_end, w);
       return true;
     }
     return false;

@@ -138,17 +138,42 @@ MODEL = {128: (2.64, 0.334, 0.17, 4.67, 1.03), 256: (3.47, 0.364, 0.00, 8.18, 1.
 
 
 def brute_force_cost(m, n, k, bn, g, mode):
-    """The model evaluated on the simulator's explicit segment lists."""
+    """The model evaluated on the simulator's explicit segment lists.
+
+    A launch without ABFT reduces a tile with its covering CTAs together when
+    the owner's Stream-K work begins with the tile and at least three covering
+    CTAs end their work in it: each of those stores a partial (the owner too)
+    and reads covers / parts partial tiles; otherwise the owner reads every
+    peer's partial."""
     a, c, e, b, d = MODEL[bn]
     sch = ss.schedule(m, n, k, 128, bn, 64, g, mode=mode)
     op = ss.owners_and_peers(sch)
+    tm, tn, _ = ss.tile_grid(m, n, k, 128, bn, 64)
+    t_dp = ss.dp_tile_count(tm * tn, g, mode)
+    shared = {}
+    for tile, (owner, peers) in op.items():
+        if not peers:
+            continue
+        sk = [s for s in sch[owner] if s.tile >= t_dp]
+        if sk[0].tile != tile:
+            continue
+        parts = {x for x in [owner] + list(peers) if sch[x][-1].tile == tile}
+        if len(parts) >= 3:
+            shared[tile] = (len(parts), 1 + len(peers), parts)
     worst = 0.0
-    for segs in sch:
+    for x, segs in enumerate(sch):
         iters = sum(s.k_iter_end - s.k_iter_begin for s in segs)
         tiles = sum(1 for s in segs if s.role != ss.PEER)
         partial = sum(1 for s in segs if s.role == ss.PEER)
-        peers = sum(len(op[s.tile][1]) for s in segs if s.role == ss.OWNER)
-        worst = max(worst, a + c * iters + e * tiles + b * partial + d * peers)
+        fix = 0.0
+        for s in segs:
+            if s.tile in shared and x in shared[s.tile][2]:
+                nparts, covers, _ = shared[s.tile]
+                fix += covers / nparts
+                partial += 1 if s.role == ss.OWNER else 0
+            elif s.role == ss.OWNER:
+                fix += len(op[s.tile][1])
+        worst = max(worst, a + c * iters + e * tiles + b * partial + d * fix)
     return worst
 
 

@@ -137,6 +137,45 @@ def test_many_peers_per_tile(g):
     assert rows == ss.flatten(ss.schedule(256, 256, 8192, 128, 128, 64, g, mode="sk"))
 
 
+@pytest.mark.parametrize("out", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("pair", [1, 2])
+def test_shared_tile_reduction(out, pair):
+    # Deep-k tiles split over many CTAs that all end their ranges in them
+    # (grids that divide the iterations evenly, so every owner's range starts
+    # at its tile): each of those CTAs stores its partial and reduces a share
+    # of the tile (plain stores of C, alpha / beta with C0, ragged m and n, a
+    # CTA-pair half past m).
+    g = 128 if pair == 2 else 48
+    if g > sms():
+        pytest.skip("needs more SMs")
+    p = inputs.make_problem(300, 200, 16384, seed=11 + pair, in_dtype="f16", out_dtype=out,
+                            law_a="uniform", law_b="uniform", alpha=1.5, beta=0.5)
+    opts = skgemm.opts_default(sched="sk", tile_n=256 if pair == 2 else 128, grid=g,
+                               cta_pair=pair)
+    C, ws, st = run(p, opts)
+    assert st == skgemm.OK
+    check_full(p, C)
+    assert ws.report().status_bits == 0
+
+
+def test_shared_tile_reduction_injection():
+    # A bit flipped in one accumulator of a shared-reduction tile reaches C
+    # at that element only (no ABFT).
+    p = inputs.make_problem(256, 256, 16384, seed=21, in_dtype="bf16", out_dtype="f32",
+                            law_a="normal", law_b="normal")
+    ref = reference(p)
+    opts = skgemm.opts_default(sched="sk", tile_n=128, grid=min(64, sms()), inject_tile=2,
+                               inject_row=37, inject_col=101, inject_bit=30)
+    C, ws, st = run(p, opts)
+    assert st == skgemm.OK
+    got = C.cpu().double().numpy()
+    bad = (128 + 37, 101)
+    diff = np.abs(got - ref)
+    assert not (diff[bad] < 1e-3)
+    diff[bad] = 0
+    assert diff.max() < 1e-2
+
+
 def test_workspace_reuse_across_launches():
     # Flags carry the launch epoch: back-to-back launches on one workspace
     # never read a stale partial.
