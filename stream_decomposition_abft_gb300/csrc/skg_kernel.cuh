@@ -45,6 +45,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "skg_ptx.cuh"
 #include "skg_sched.cuh"
 #include "skgemm.h"
@@ -501,9 +503,9 @@ static __device__ __noinline__ bool fixup_through_ring(uint8_t* qring, int slots
       }
       tmem_st32(tacc + c32 * 32, u);
     }
-    // The slot's reads are done before its next copy lands.
+    // The slot's reads are done (their values consumed) before lane 0 issues
+    // its next copy.
     __syncwarp();
-    fence_proxy_async_smem();
     if (lane == 0 && issued < items) issue(issued);
     issued += issued < items ? 1 : 0;
     __syncwarp();
@@ -518,6 +520,63 @@ static __device__ __noinline__ bool fixup_through_ring(uint8_t* qring, int slots
     __syncwarp();
   }
   return fine;
+}
+
+// Elements of C in the launch's output type, one at a time or four at once
+// (the shared tile reduction's plain loads and stores).
+template <int OUT>
+__device__ __forceinline__ float load_out(const void* c, int64_t i) {
+  if constexpr (OUT == 0) return static_cast<const float*>(c)[i];
+  else if constexpr (OUT == 1) return __half2float(static_cast<const __half*>(c)[i]);
+  else return __bfloat162float(static_cast<const __nv_bfloat16*>(c)[i]);
+}
+template <int OUT>
+__device__ __forceinline__ void store_out(void* c, int64_t i, float v) {
+  if constexpr (OUT == 0) static_cast<float*>(c)[i] = v;
+  else if constexpr (OUT == 1) static_cast<__half*>(c)[i] = __float2half_rn(v);
+  else static_cast<__nv_bfloat16*>(c)[i] = __float2bfloat16_rn(v);
+}
+template <int OUT>
+__device__ __forceinline__ void unpack4(float4 w, float (&y)[4]) {
+  y[0] = w.x;
+  y[1] = w.y;
+  y[2] = w.z;
+  y[3] = w.w;
+}
+template <int OUT>
+__device__ __forceinline__ void unpack4(uint2 w, float (&y)[4]) {
+  const uint32_t h[2] = {w.x, w.y};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if constexpr (OUT == 1) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+      y[2 * i] = f.x;
+      y[2 * i + 1] = f.y;
+    } else {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&h[i]));
+      y[2 * i] = f.x;
+      y[2 * i + 1] = f.y;
+    }
+  }
+}
+template <int OUT, class Vec>
+__device__ __forceinline__ Vec pack4(const float (&y)[4]) {
+  if constexpr (OUT == 0) {
+    return make_float4(y[0], y[1], y[2], y[3]);
+  } else {
+    uint32_t h[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if constexpr (OUT == 1) {
+        const __half2 v = __floats2half2_rn(y[2 * i], y[2 * i + 1]);
+        h[i] = *reinterpret_cast<const uint32_t*>(&v);
+      } else {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(y[2 * i], y[2 * i + 1]);
+        h[i] = *reinterpret_cast<const uint32_t*>(&v);
+      }
+    }
+    return make_uint2(h[0], h[1]);
+  }
 }
 
 // Shared LoadPartials + StoreTile (no ABFT): a tile covered by CTAs
@@ -563,47 +622,84 @@ static __device__ __noinline__ bool reduce_share(const KernelParams& p, float* r
   const int ib = j * per + (j < extra ? j : extra);
   const int ie = ib + per + (j < extra ? 1 : 0);
   const int covers = contrib_last - owner + 1;
-  for (int t = ib + ew; t < ie; t += 4) {
-    const int qi = t / (BN / 4), c4 = t - qi * (BN / 4);
-    const int r = qi * 32 + lane;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = 0; c0 < covers; c0 += 4) {
-      float4 v[4];
+  // A warp takes items ib + ew, ib + ew + 4, ...; kBatch of them at a time
+  // with their C0 values and kCov covers' partials in flight together, so
+  // the loop waits for one round trip per batch and kCov covers. C0 and C
+  // move as one 16-byte (fp32) or 8-byte (16-bit) vector per item and lane
+  // when its four columns lie inside n.
+  constexpr int kBatch = 2, kCov = 8;
+  using Vec = typename std::conditional<C::OUT == 0, float4, uint2>::type;
+  for (int t0 = ib + ew; t0 < ie; t0 += 4 * kBatch) {
+    int64_t off[kBatch];
+    int ncol[kBatch];  // columns of the item inside n (0 when the row is past m)
+    float c0v[kBatch][4];
+    float4 acc[kBatch];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (c0 + u < covers)
-          v[u] = ld_cg_f4(partial_at<BN>(
-              rpartials + (size_t)((owner + c0 + u) * slot_stride + crank) * kBM * BN, c4, r,
-              true));
+    for (int bi = 0; bi < kBatch; ++bi) {
+      const int t = t0 + 4 * bi;
+      const int qi = t / (BN / 4), c4 = t - qi * (BN / 4);
+      const int64_t gr = (int64_t)m0 + qi * 32 + lane;
+      const int col = n0 + 4 * c4;
+      acc[bi] = make_float4(0.f, 0.f, 0.f, 0.f);
+      ncol[bi] = (t < ie && gr < p.m) ? max(0, min(4, p.n - col)) : 0;
+      off[bi] = gr * p.ldc + col;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (c0 + u < covers) {
-          acc.x += v[u].x;
-          acc.y += v[u].y;
-          acc.z += v[u].z;
-          acc.w += v[u].w;
-        }
-    }
-    const int64_t gr = (int64_t)m0 + r;
-    if (gr >= p.m) continue;
-    float y[4] = {acc.x, acc.y, acc.z, acc.w};
+      for (int e = 0; e < 4; ++e) c0v[bi][e] = 0.f;
+      if (p.beta != 0.f && ncol[bi] == 4) {
+        const Vec w = *reinterpret_cast<const Vec*>(static_cast<const char*>(p.c_ptr) +
+                                                    off[bi] * C::OUT_BYTES);
+        unpack4<C::OUT>(w, c0v[bi]);
+      } else if (p.beta != 0.f) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int col = n0 + 4 * c4 + e;
-      if (col >= p.n) continue;
-      if (inject_here && r == p.inject_row && 4 * c4 + e == p.inject_col)
-        y[e] = __uint_as_float(__float_as_uint(y[e]) ^ (1u << p.inject_bit));
-      const int64_t off = gr * p.ldc + col;
-      float c0v = 0.f;
-      if (p.beta != 0.f) {
-        if constexpr (C::OUT == 0) c0v = static_cast<const float*>(p.c_ptr)[off];
-        else if constexpr (C::OUT == 1) c0v = __half2float(static_cast<const __half*>(p.c_ptr)[off]);
-        else c0v = __bfloat162float(static_cast<const __nv_bfloat16*>(p.c_ptr)[off]);
+        for (int e = 0; e < 4; ++e)
+          if (e < ncol[bi]) c0v[bi][e] = load_out<C::OUT>(p.c_ptr, off[bi] + e);
       }
-      const float out = p.alpha * y[e] + p.beta * c0v;
-      if constexpr (C::OUT == 0) static_cast<float*>(p.c_ptr)[off] = out;
-      else if constexpr (C::OUT == 1) static_cast<__half*>(p.c_ptr)[off] = __float2half_rn(out);
-      else static_cast<__nv_bfloat16*>(p.c_ptr)[off] = __float2bfloat16_rn(out);
+    }
+    for (int cv0 = 0; cv0 < covers; cv0 += kCov) {
+      float4 v[kBatch][kCov];
+#pragma unroll
+      for (int bi = 0; bi < kBatch; ++bi) {
+        const int t = t0 + 4 * bi;
+        const int qi = t / (BN / 4), c4 = t - qi * (BN / 4);
+#pragma unroll
+        for (int u = 0; u < kCov; ++u)
+          if (t < ie && cv0 + u < covers)
+            v[bi][u] = ld_cg_f4(partial_at<BN>(
+                rpartials + (size_t)((owner + cv0 + u) * slot_stride + crank) * kBM * BN, c4,
+                qi * 32 + lane, true));
+      }
+#pragma unroll
+      for (int bi = 0; bi < kBatch; ++bi)
+#pragma unroll
+        for (int u = 0; u < kCov; ++u)
+          if (t0 + 4 * bi < ie && cv0 + u < covers) {
+            acc[bi].x += v[bi][u].x;
+            acc[bi].y += v[bi][u].y;
+            acc[bi].z += v[bi][u].z;
+            acc[bi].w += v[bi][u].w;
+          }
+    }
+#pragma unroll
+    for (int bi = 0; bi < kBatch; ++bi) {
+      if (ncol[bi] == 0) continue;
+      const int t = t0 + 4 * bi;
+      const int qi = t / (BN / 4), c4 = t - qi * (BN / 4);
+      const int r = qi * 32 + lane;
+      float y[4] = {acc[bi].x, acc[bi].y, acc[bi].z, acc[bi].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (inject_here && r == p.inject_row && 4 * c4 + e == p.inject_col)
+          y[e] = __uint_as_float(__float_as_uint(y[e]) ^ (1u << p.inject_bit));
+        y[e] = p.alpha * y[e] + p.beta * c0v[bi][e];
+      }
+      if (ncol[bi] == 4) {
+        *reinterpret_cast<Vec*>(static_cast<char*>(p.c_ptr) + off[bi] * C::OUT_BYTES) =
+            pack4<C::OUT, Vec>(y);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (e < ncol[bi]) store_out<C::OUT>(p.c_ptr, off[bi] + e, y[e]);
+      }
     }
   }
   return true;
@@ -657,33 +753,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool enc_here = C::ABFT && !C::PAIR && p.enc_inkernel && (int)blockIdx.x >= s.g;
   static_assert(C::STAGE_BYTES >= kEncInBoxBytes, "an encode box fills one ring stage");
 
-  if (threadIdx.x == 0) {
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
-    prefetch_tmap(&tmC);
-    if (C::ABFT && p.s.t_ck > 0) {
-      prefetch_tmap(&tmB128);
-      prefetch_tmap(&tmBE);
-      prefetch_tmap(&tmEA);
-      prefetch_tmap(&tmCr);
-      prefetch_tmap(&tmCc);
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      prefetch_tmap(&tmC);
+      if (C::ABFT && p.s.t_ck > 0) {
+        prefetch_tmap(&tmB128);
+        prefetch_tmap(&tmBE);
+        prefetch_tmap(&tmEA);
+        prefetch_tmap(&tmCr);
+        prefetch_tmap(&tmCc);
+      }
+      aux->abort_flag = 0;
+      aux->nbad_r = aux->nbad_c = 0;
+      aux->bad_row = aux->bad_col = -1;
     }
-    for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
+    // The barriers in one go, a lane each: every one counts a single
+    // arrival except the accumulator-empty ones, which the epilogue threads
+    // release (both CTAs' for a pair).
+    const int nbars = (int)(c0r_bar + 4 - full_bar);
+    for (int i = lane; i < nbars; i += 32) {
+      uint64_t* bar = full_bar + i;
+      const bool acc_empty = bar >= tempty_bar && bar < tempty_bar + 2;
+      mbar_init(bar, acc_empty ? (C::PAIR ? 2 * kEpiThreads : kEpiThreads) : 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&tfull_bar[i], 1);
-      // A pair's accumulator is released by the epilogue threads of both CTAs.
-      mbar_init(&tempty_bar[i], C::PAIR ? 2 * kEpiThreads : kEpiThreads);
-    }
-    for (int i = 0; i < 4; ++i) mbar_init(&c0_bar[i], 1);
-    mbar_init(drain_bar, 1);
-    for (int i = 0; i < 4 * kFixSlots; ++i) mbar_init(&fix_bar[i], 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&c0r_bar[i], 1);
-    aux->abort_flag = 0;
-    aux->nbad_r = aux->nbad_c = 0;
-    aux->bad_row = aux->bad_col = -1;
     fence_barrier_init();
   }
   if (warp == 1) {

@@ -35,6 +35,12 @@ struct CostModel {
 constexpr CostModel kModel128 = {2.64, 0.334, 0.17, 4.67, 1.03};
 constexpr CostModel kModel256 = {3.47, 0.364, 0.00, 8.18, 1.73};
 
+// A shared tile also costs each part about this many d-units per covering
+// CTA (every part waits for every cover's flag and reads a slice of every
+// cover's partial): fitted on the GB300 from deep-k launches split 16 and 32
+// ways (9.4 and 13.9 us beyond the MAC iterations).
+constexpr double kShareCoverCost = 0.27;
+
 // Whether the tile starting at iteration ti of an evenly split region is
 // reduced by its covering CTAs together (see Work::share_parts): its owner's
 // range starts at ti and at least kShareMin covering CTAs end in it. Gives
@@ -75,14 +81,14 @@ inline void region_counts(int64_t q, int r, int64_t total, int64_t I, int x, boo
     if (last + I > e) {  // owns an unfinished tile
       if (share && shared_tile(q, r, last, I, parts, covers)) {
         partial += 1;
-        fix += (double)covers / parts;
+        fix += (double)covers / parts + kShareCoverCost * covers;
       } else {
         fix += even_cta_of(q, r, last + I - 1) - x;
       }
     }
   } else if (share && shared_tile(q, r, (b / I) * I, I, parts, covers)) {
     // The whole range lies inside a tile another CTA started and owns.
-    fix += (double)covers / parts;
+    fix += (double)covers / parts + kShareCoverCost * covers;
   }
 }
 

@@ -40,7 +40,7 @@ enum : int { kRoleFull = 0, kRoleOwner = 1, kRolePeer = 2 };
 // Tiles of an output Stream-K region that this many covering CTAs end their
 // ranges in, the k = 0 CTA's range starting at the tile, are reduced by all
 // of those together in launches without ABFT (Work::share_parts).
-constexpr int kShareMin = 3;
+constexpr int kShareMin = 8;
 
 struct Schedule {
   int tiles_m, tiles_n;

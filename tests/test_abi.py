@@ -141,10 +141,10 @@ def brute_force_cost(m, n, k, bn, g, mode):
     """The model evaluated on the simulator's explicit segment lists.
 
     A launch without ABFT reduces a tile with its covering CTAs together when
-    the owner's Stream-K work begins with the tile and at least three covering
+    the owner's Stream-K work begins with the tile and at least eight covering
     CTAs end their work in it: each of those stores a partial (the owner too)
-    and reads covers / parts partial tiles; otherwise the owner reads every
-    peer's partial."""
+    and pays covers / parts + 0.27 * covers peer reads; otherwise the owner
+    reads every peer's partial."""
     a, c, e, b, d = MODEL[bn]
     sch = ss.schedule(m, n, k, 128, bn, 64, g, mode=mode)
     op = ss.owners_and_peers(sch)
@@ -158,7 +158,7 @@ def brute_force_cost(m, n, k, bn, g, mode):
         if sk[0].tile != tile:
             continue
         parts = {x for x in [owner] + list(peers) if sch[x][-1].tile == tile}
-        if len(parts) >= 3:
+        if len(parts) >= 8:
             shared[tile] = (len(parts), 1 + len(peers), parts)
     worst = 0.0
     for x, segs in enumerate(sch):
@@ -169,7 +169,7 @@ def brute_force_cost(m, n, k, bn, g, mode):
         for s in segs:
             if s.tile in shared and x in shared[s.tile][2]:
                 nparts, covers, _ = shared[s.tile]
-                fix += covers / nparts
+                fix += covers / nparts + 0.27 * covers
                 partial += 1 if s.role == ss.OWNER else 0
             elif s.role == ss.OWNER:
                 fix += len(op[s.tile][1])
