@@ -437,13 +437,30 @@ def run_reference(args, rank):
 
 def ncu_target(args):
     """Profiling target (no timing): every sweep shape's ABFT GEMM through
-    skg_gemm, `--steps` times, with the library's default plan."""
+    skg_gemm, `--steps` times, with the library's default plan; with
+    `--workload hostile`, the quantisation-hostile shapes' plain GEMMs
+    (automatic plan) instead."""
     import torch
     from stream_decomposition_abft_gb300 import _build, inputs, skgemm
     if not os.path.exists(skgemm.LIB_PATH):
         _build.build()
     dev = torch.device("cuda")
     sh = torch.cuda.current_stream().cuda_stream
+    if args.workload == "hostile":
+        for (m, n, k) in inputs.HOSTILE_SHAPES:
+            p = inputs.hostile(m, n, k)
+            A, B, C = p.A.to(dev), p.B.to(dev), p.C0.to(dev)
+            o = skgemm.opts_default()
+            ws = skgemm.Workspace(skgemm.workspace_size(m, n, k, o), dev)
+            for _ in range(args.steps):
+                st = skgemm.gemm(m, n, k, p.alpha, A.data_ptr(), k, B.data_ptr(), k, p.beta,
+                                 C.data_ptr(), n, skgemm.IN_F16, skgemm.OUT_F16, 0, 0, o,
+                                 ws.ptr, ws.nbytes, sh)
+                if st != skgemm.OK:
+                    raise skgemm.SkgError(st, "skg_gemm")
+            torch.cuda.synchronize()
+            print((m, n, k), skgemm.launch_shape(m, n, k, o), flush=True)
+        return
     opts = skgemm.opts_default(abft=1)
     sizes = [int(x) for x in args.sizes.split(",")] if args.sizes else list(inputs.SQUARE_SIZES)
     for size in sizes:
@@ -556,20 +573,24 @@ def workload_hostile(args):
                     raise skgemm.SkgError(st, "skg_gemm")
 
             ms = _time_launch(launch, flush, max(5, args.steps // 10), stream)
-            spreads = []
+            spreads, spreads90 = [], []
             for _ in range(7):
                 flush.zero_()
                 launch()
                 c = clk.view(g, 2).cpu().double()
                 busy = (c[:, 1] - c[:, 0])
                 spreads.append(float((busy.max() - busy.min()) / busy.max()))
+                q = torch.quantile(busy, torch.tensor([0.05, 0.95], dtype=busy.dtype))
+                spreads90.append(float((q[1] - q[0]) / busy.max()))
             spread = statistics.median(spreads)
+            spread90 = statistics.median(spreads90)
             out.append({"m": m, "n": n, "k": k, "plan": label,
                         "tile": f"{pl.tile_m}x{tn}x64", "cta_pairs": pl.cta_pair == 2,
                         "grid": g, "sched": names[sc], "ms": round(ms, 4),
                         "tflops": round(2.0 * m * n * k / ms / 1e9, 1),
                         "pct_of_peak_measured": round(100 * 2.0 * m * n * k / ms / 1e9 / burst, 1),
-                        "sm_busy_spread": round(spread, 4), "sms_used": g,
+                        "sm_busy_spread": round(spread, 4),
+                        "sm_busy_spread_p5_p95": round(spread90, 4), "sms_used": g,
                         "status_bits": ws.report().status_bits})
     print(json.dumps({"workload": "hostile fp16 shapes, alpha 1.5 beta 0.5 (C0 U[-1,1])",
                       "unit": "TFLOPS", "results": out}), flush=True)
