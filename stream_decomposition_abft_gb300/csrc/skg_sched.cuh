@@ -6,7 +6,7 @@
 //   - Algorithm 5 (§4): the MAC iterations of all tiles form one linear
 //     m -> n -> k space split over g CTAs; a CTA's range is cut at tile
 //     boundaries into segments; tile_started / tile_ended give the role.
-//   - §A1: iterations are split evenly "to within one iteration": CTA x gets
+//   - §A1: iterations are split evenly, CTA counts differing by one at most: CTA x gets
 //     q + [x < r] iterations starting at x*q + min(x, r), (q, r) = divmod(T, g).
 //   - §5.2: "DP + one-tile SK" keeps w = floor(t/g) full DP waves; "two-tile
 //     SK + DP" gives one of them up when w >= 2 so every Stream-K CTA holds
