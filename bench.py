@@ -24,6 +24,7 @@ With torchrun (N > 1) every rank runs the same sweep on its own GPU
 from __future__ import annotations
 
 import argparse
+import re
 import hashlib
 import json
 import math
@@ -44,11 +45,19 @@ KERNEL_SOURCES = ("stream_decomposition_abft_gb300/csrc/skg_kernel.cuh",
                   "stream_decomposition_abft_gb300/csrc/skg_sched.cuh")
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and with whitespace collapsed, so that a
+    change to comments alone keeps the hash (the compiled kernel is the same)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_hash() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
