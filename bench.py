@@ -126,6 +126,21 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------- ours
+def replica_value(sizes, times_ms, world, device):
+    """Whole-job throughput of `world` replicas of the square sweep: each
+    shape's time is the max over ranks (all_reduce MAX when world > 1), and
+    the value is the geomean over shapes of world * 2 s^3 / that time, in
+    TFLOPS. Returns (per-shape max times in ms, value)."""
+    import torch
+    times = list(times_ms)
+    if world > 1:
+        t = torch.tensor(times, dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        times = t.tolist()
+    value = geomean([world * 2.0 * s ** 3 / t / 1e9 for s, t in zip(sizes, times)])
+    return times, value
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from stream_decomposition_abft_gb300 import _build, inputs, skgemm
@@ -241,13 +256,8 @@ def run_ours(args, rank, world, local_rank):
         abft["max_ratio_row"] = max(abft["max_ratio_row"], rep.max_ratio_row)
         abft["max_ratio_col"] = max(abft["max_ratio_col"], rep.max_ratio_col)
 
-    # Aggregate over ranks (replicas): per-shape time = max over ranks.
-    times = [ps["ms"] for ps in per_shape]
-    if world > 1:
-        t = torch.tensor(times, dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        times = t.tolist()
-    value = geomean([world * 2.0 * ps["m"] ** 3 / t / 1e9 for ps, t in zip(per_shape, times)])
+    times, value = replica_value([ps["m"] for ps in per_shape], [ps["ms"] for ps in per_shape],
+                                 world, dev)
 
     e2e = measure_e2e(args, problems, dev, stream, opts, enc_opts)
 
