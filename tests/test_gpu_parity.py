@@ -158,6 +158,28 @@ def test_shared_tile_reduction(out, pair):
     assert ws.report().status_bits == 0
 
 
+def test_shared_tile_reduction_timeout_reports_and_returns():
+    # One CTA of a shared-reduction tile skips its Signal: every other CTA of
+    # the tile runs out its bounded flag wait; the launch records
+    # SKG_ERR_FIXUP_TIMEOUT and the device stays usable.
+    p = inputs.make_problem(256, 256, 16384, seed=22, in_dtype="bf16", out_dtype="f32")
+    g = min(64, sms())
+    rows = ss.flatten(ss.schedule(256, 256, 16384, 128, 128, 64, g, mode="sk"))
+    peer = next(r[0] for r in rows if r[4] == ss.PEER)
+    opts = skgemm.opts_default(sched="sk", grid=g, tile_n=128, timeout_ns=50_000_000,
+                               test_drop_signal=peer + 1)
+    C, ws, st = run(p, opts)
+    assert st == skgemm.OK
+    rep = ws.report()
+    assert rep.status_bits & (1 << skgemm.ERR_FIXUP_TIMEOUT)
+    assert rep.timeouts >= 1
+    p2 = inputs.make_problem(256, 256, 16384, seed=23, in_dtype="bf16", out_dtype="f32")
+    C2, ws2, st2 = run(p2, skgemm.opts_default(sched="sk", grid=g, tile_n=128))
+    assert st2 == skgemm.OK
+    check_full(p2, C2)
+    assert ws2.report().status_bits == 0
+
+
 def test_shared_tile_reduction_injection():
     # A bit flipped in one accumulator of a shared-reduction tile reaches C
     # at that element only (no ABFT).
