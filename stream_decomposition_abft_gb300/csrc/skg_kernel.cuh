@@ -1761,7 +1761,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (C::PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
     else tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
-  if (threadIdx.x == 0) {
+  // A launch of whole tiles only (no Stream-K region, no side tiles) sets no
+  // flag and no counter, so it leaves the epoch alone and skips the CTA
+  // ticket (a fence and a returning atomic at every CTA's exit).
+  const bool flagless = s.sk_total == 0 && s.t_ck == 0 && !p.enc_inkernel;
+  if (threadIdx.x == 0 && flagless) {
+    if (p.cta_clock) p.cta_clock[2 * blockIdx.x + 1] = globaltimer();
+    if (blockIdx.x == 0) atomicAdd(&p.report->launches, 1u);
+  } else if (threadIdx.x == 0) {
     if (p.cta_clock) p.cta_clock[2 * blockIdx.x + 1] = globaltimer();
     __threadfence();
     const uint32_t ticket = atomicAdd(&p.hdr->done, 1u);
