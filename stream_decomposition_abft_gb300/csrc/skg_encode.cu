@@ -78,12 +78,6 @@ constexpr size_t kEncSmem = 1024 + (size_t)kEncStages * kEncStageBytes + kEncPar
 
 int encode_slices(int kp) { return (kp + kEncSliceCols - 1) / kEncSliceCols; }
 
-__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
 // Named barrier 1 over the kEncWorkerThreads consumer threads that also
 // ANDs a predicate (the count comes from the same constant as the launch).
 static_assert(kEncWorkerThreads % 32 == 0 && kEncWorkerThreads <= 1024, "barrier count");

@@ -65,12 +65,16 @@ constexpr int kAuxBytes = 1024;  // shared-memory bookkeeping (struct Aux) after
 constexpr uint32_t kSmemLimit = 232448;
 
 // Workspace header (device). The report follows at offset 256.
+// The epoch is advanced once per launch by the CTA that takes the launch's
+// last ticket (every CTA takes one after reading the epoch); a launch that
+// read epoch e flags with e + 1 and counts in ck_done[e & 1] / enc_done[e & 1],
+// and the last-ticket CTA clears the other parity for the next launch.
 struct WsHeader {
-  uint32_t epoch;     // launches completed on this workspace
-  uint32_t done;      // CTA tickets of the running launch
-  uint32_t ck_done;   // fused checksum tiles stored by the running launch
-  uint32_t enc_done;  // side CTAs done with the in-kernel encode pass
-  uint32_t pad[60];
+  uint32_t epoch;        // launches on this workspace
+  uint32_t done;         // CTA tickets of the running launch
+  uint32_t ck_done[2];   // fused checksum tiles stored, by epoch parity
+  uint32_t enc_done[2];  // side CTAs done with the in-kernel encode pass, by parity
+  uint32_t pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
@@ -202,6 +206,8 @@ struct Aux {
   float inj_clean;
   float d_row, d_col;
   float tmax_a[4], tmax_b[4];  // per epilogue warp: partial tile maxima
+  uint32_t epoch;              // this launch's flag value (workspace epoch + 1)
+  int32_t epoch_ready;         // epoch published by the epilogue
 };
 static_assert(sizeof(Aux) <= kAuxBytes, "aux size");
 
@@ -213,6 +219,18 @@ __device__ __forceinline__ void record_error(const KernelParams& p, Aux* aux, in
 
 __device__ __forceinline__ bool aborted(Aux* aux) {
   return *(volatile int32_t*)&aux->abort_flag != 0;
+}
+
+// This launch's epoch as the epilogue publishes it in shared memory (the
+// producer and MMA threads of an encode side CTA need its parity for the
+// encode counter). Bounded: 0 after the limit, and the caller's counter
+// wait then runs out and reports.
+__device__ __forceinline__ uint32_t published_epoch(Aux* aux, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer();
+  while (*(volatile int32_t*)&aux->epoch_ready == 0)
+    if (globaltimer() - t0 > limit_ns) return 0u;
+  __threadfence_block();
+  return *(volatile uint32_t*)&aux->epoch;
 }
 
 // Bounded mbarrier wait: true when the phase of `parity` completed; false
@@ -768,6 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       aux->abort_flag = 0;
       aux->nbad_r = aux->nbad_c = 0;
       aux->bad_row = aux->bad_col = -1;
+      aux->epoch_ready = 0;
     }
     // The barriers in one go, a lane each: every one counts a single
     // arrival except the accumulator-empty ones, which the epilogue threads
@@ -795,6 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = aux->tmem_slot;
+  uint32_t ticket = 0;  // this CTA's launch ticket (taken by epilogue thread 0)
   // Everything above touched only this CTA's shared memory and TMEM; from
   // here on the kernel reads the previous kernel's outputs (inputs, ABFT
   // checksums, the workspace epoch).
@@ -850,8 +870,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // The checksum tiles read every side CTA's encodings: wait for all.
         if (ok) {
+          const uint32_t par = (published_epoch(aux, limit) - 1u) & 1u;
           const uint64_t t0 = globaltimer();
-          while (ld_acquire_gpu(&p.hdr->enc_done) < (uint32_t)s.g_ck) {
+          while (ld_acquire_gpu(&p.hdr->enc_done[par]) < (uint32_t)s.g_ck) {
             nanosleep_ns(64);
             if (globaltimer() - t0 > limit) {
               if (!aborted(aux)) record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
@@ -962,8 +983,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nb = enc_in_boxes(p, u0, u1);
         stage = nb % STAGES;
         phase = (uint32_t)((nb / STAGES) & 1);
+        const uint32_t par = (published_epoch(aux, limit) - 1u) & 1u;
         const uint64_t t0 = globaltimer();
-        while (ld_acquire_gpu(&p.hdr->enc_done) < (uint32_t)s.g_ck) {
+        while (ld_acquire_gpu(&p.hdr->enc_done[par]) < (uint32_t)s.g_ck) {
           nanosleep_ns(64);
           if (globaltimer() - t0 > limit) {
             if (!aborted(aux)) record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
@@ -1069,7 +1091,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ew_of_q = (qq + 2) & 3;  // warps 2..5 own quadrants 2, 3, 0, 1
       return reinterpret_cast<float*>(epi + ew_of_q * C::EPI_BUFS * C::EPI_BUF_BYTES);
     };
-    const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr->epoch) + 1u;
+    // This launch's epoch: read once, published to the other roles, then
+    // this CTA's ticket (its value is first used at the CTA's exit, so the
+    // round trip stays off every path).
+    if (et == 0) {
+      aux->epoch = ld_acquire_gpu(&p.hdr->epoch) + 1u;
+      __threadfence_block();
+      *reinterpret_cast<volatile int32_t*>(&aux->epoch_ready) = 1;
+    }
+    named_bar_sync(1, kEpiThreads);
+    const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&aux->epoch);
+    const uint32_t par = (epoch - 1u) & 1u;  // this launch's counters
+    if (et == 0) ticket = atom_add_acq_rel_gpu(&p.hdr->done, 1u);
     // Hand an accumulator buffer back to the MMA thread (the leader's, for
     // a CTA pair).
     auto release_acc = [&](int b) {
@@ -1171,7 +1204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1, kEpiThreads);
       if (et == 0 && eok) {
         __threadfence();
-        atomicAdd(&p.hdr->enc_done, 1u);
+        atomicAdd(&p.hdr->enc_done[par], 1u);
       }
     }
     while (cur.next(s, w)) {
@@ -1230,7 +1263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool fine = true;
           if (et == 0) {
             const uint64_t t0 = globaltimer();
-            while (ld_acquire_gpu(&p.hdr->ck_done) < (uint32_t)(kCkHalf * s.t_ck)) {
+            while (ld_acquire_gpu(&p.hdr->ck_done[par]) < (uint32_t)(kCkHalf * s.t_ck)) {
               nanosleep_ns(128);
               if (globaltimer() - t0 > limit) {
                 record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
@@ -1433,7 +1466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_bar_sync(1, kEpiThreads);
           if (et == 0) {
             __threadfence();
-            atomicAdd(&p.hdr->ck_done, 1u);
+            atomicAdd(&p.hdr->ck_done[par], 1u);
           }
           if (++ab == ACC_BUFS) {
             ab = 0;
@@ -1761,25 +1794,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (C::PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
     else tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
-  // A launch of whole tiles only (no Stream-K region, no side tiles) sets no
-  // flag and no counter, so it leaves the epoch alone and skips the CTA
-  // ticket (a fence and a returning atomic at every CTA's exit).
-  const bool flagless = s.sk_total == 0 && s.t_ck == 0 && !p.enc_inkernel;
-  if (threadIdx.x == 0 && flagless) {
+  // The CTA with the launch's last ticket (every CTA took one after reading
+  // the epoch) readies the workspace for the next launch: tickets back to
+  // zero, the next parity's counters cleared, the epoch advanced.
+  if (threadIdx.x == 64) {  // epilogue thread 0, which holds the ticket
     if (p.cta_clock) p.cta_clock[2 * blockIdx.x + 1] = globaltimer();
-    if (blockIdx.x == 0) atomicAdd(&p.report->launches, 1u);
-  } else if (threadIdx.x == 0) {
-    if (p.cta_clock) p.cta_clock[2 * blockIdx.x + 1] = globaltimer();
-    __threadfence();
-    const uint32_t ticket = atomicAdd(&p.hdr->done, 1u);
     if (ticket == gridDim.x - 1) {
-      // Last CTA of the launch: every CTA has read the epoch, so advance it.
+      const uint32_t e = aux->epoch - 1u;
       p.hdr->done = 0;
-      p.hdr->ck_done = 0;
-      p.hdr->enc_done = 0;
+      p.hdr->ck_done[(e + 1u) & 1u] = 0;
+      p.hdr->enc_done[(e + 1u) & 1u] = 0;
       atomicAdd(&p.report->launches, 1u);
-      __threadfence();
-      atomicAdd(&p.hdr->epoch, 1u);
+      st_release_gpu(&p.hdr->epoch, e + 1u);
     }
   }
 }
