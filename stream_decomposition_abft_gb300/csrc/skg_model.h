@@ -167,8 +167,14 @@ inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_s
         // Basic Stream-K keeps its tile-processing skew for the whole
         // launch, which costs cache reuse the model does not see (§5.2);
         // with two or more full waves the hybrids exist to bound it, so the
-        // automatic choice does not take basic SK there.
-        if (want_sched < 0 && sched == kSchedSK && t >= 2 * (int64_t)cands[i]) continue;
+        // automatic choice does not take basic SK there. Measured on GB300,
+        // the skew also loses from one full wave on when tiles are deep
+        // (8192 x 1024 x 8192 on 76 clusters: basic SK 115 us, DP + one-tile
+        // SK 92 us; at k = 4096 basic SK was still ahead by 3-4 %).
+        const int64_t ipt = (k + kTileK - 1) / kTileK;
+        if (want_sched < 0 && sched == kSchedSK &&
+            (t >= 2 * (int64_t)cands[i] || (t >= cands[i] && ipt >= 128)))
+          continue;
         // Side tiles split over the grid, or (automatic grid only) one each
         // on SMs the grid leaves idle: every verification waits for all side
         // tiles, so they must end with the output CTAs' first tiles.
