@@ -16,16 +16,21 @@
 //               thread): a PEER segment writes its fp32 partial tile to the
 //               workspace and releases a flag carrying the launch epoch
 //               (StorePartials / Signal); an OWNER waits for its later peers'
-//               flags and adds their partials (Wait / LoadPartials); then
-//               alpha / beta, the output cast, a swizzled staging buffer and
-//               a TMA store (StoreTile). Only the tile's k = 0 CTA writes C
-//               (§4), so C needs no atomics.
+//               flags and adds their partials (Wait / LoadPartials), pulled
+//               through the idle stage ring with bulk copies since an owned
+//               tile is always its CTA's last work; then alpha / beta, the
+//               output cast, a swizzled staging buffer and a TMA store
+//               (StoreTile). The tile's k = 0 CTA writes C (§4), except that
+//               without ABFT a tile split over eight or more CTAs that all
+//               end in it is reduced and written in slices by all of them
+//               (reduce_share); either way C needs no atomics.
 //
 // ABFT ("Anatomy of High-Performance GEMM with Online Fault Tolerance on
-// GPUs", Figs. 3 and 5-7): before this kernel runs, the encode pass forms
-// e^T A per 128-row tile and B e per BLK_N-column tile, and two skinny
-// tensor-core GEMMs (this same kernel, fp32 out) form the reference
-// checksums cr = A (B e) and cc = (e^T A) B of every output tile. Here the
+// GPUs", Figs. 3 and 5-7): an encode pass (its own launch, or the first work
+// of dedicated side CTAs) forms e^T A per 128-row tile and B e per
+// BLK_N-column tile; two skinny tensor-core GEMMs, run as the first tiles of
+// this same launch (side tiles), form the reference checksums
+// cr = A (B e) and cc = (e^T A) B of every output tile. The
 // epilogue of each tile's owner, after the Stream-K fixup, forms the row sums
 // (in-thread) and column sums (warp transpose-reduction + shared memory) of
 // the fp32 accumulator, compares them with cr and cc, locates a single fault
