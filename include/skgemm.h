@@ -14,8 +14,9 @@
  *  - Work decomposition: same page, Algorithm 5 (§4, Stream-K), Algorithm 2
  *    (§3.2, data-parallel) and the hybrids of §5.2.
  *  - Partial-tile fixup: same page, Algorithm 5 (StorePartials / Signal /
- *    Wait / LoadPartials) and §4 ("the CTA that executes a tile's k = 0
- *    iteration writes it").
+ *    Wait / LoadPartials) and §4 (the CTA that runs a tile's first
+ *    k-iteration writes the tile; here, without ABFT, a tile that eight or
+ *    more covering CTAs end in is written in slices by those CTAs).
  *  - ABFT: "Anatomy of High-Performance GEMM with Online Fault Tolerance on
  *    GPUs", thread-level FT-GEMM (Fig. 3: checksums C^c = e^T A B and
  *    C^r = A B e, locate by the mismatching row and column, correct from the
