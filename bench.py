@@ -480,6 +480,28 @@ def ncu_target(args):
             torch.cuda.synchronize()
             print((m, n, k), skgemm.launch_shape(m, n, k, o), flush=True)
         return
+    if args.shape:
+        # Given shapes, bf16 with ABFT (or fp16 without, with --plain), the
+        # library's default plan.
+        for spec in args.shape.split(","):
+            m, n, k = (int(x) for x in spec.split("x"))
+            dt = "f16" if args.plain else "bf16"
+            p = inputs.make_problem(m, n, k, seed=5, in_dtype=dt, out_dtype=dt,
+                                    law_a="normal", law_b="normal")
+            A, B = p.A.to(dev), p.B.to(dev)
+            C = torch.empty((m, n), dtype=A.dtype, device=dev)
+            o = skgemm.opts_default(abft=0 if args.plain else 1)
+            ws = skgemm.Workspace(skgemm.workspace_size(m, n, k, o), dev)
+            code = skgemm.IN_F16 if args.plain else skgemm.IN_BF16
+            out = skgemm.OUT_F16 if args.plain else skgemm.OUT_BF16
+            for _ in range(args.steps):
+                st = skgemm.gemm(m, n, k, 1.0, A.data_ptr(), k, B.data_ptr(), k, 0.0,
+                                 C.data_ptr(), n, code, out, 0, 0, o, ws.ptr, ws.nbytes, sh)
+                if st != skgemm.OK:
+                    raise skgemm.SkgError(st, "skg_gemm")
+            torch.cuda.synchronize()
+            print((m, n, k), skgemm.launch_shape(m, n, k, o), flush=True)
+        return
     opts = skgemm.opts_default(abft=1)
     sizes = [int(x) for x in args.sizes.split(",")] if args.sizes else list(inputs.SQUARE_SIZES)
     for size in sizes:
@@ -760,6 +782,10 @@ def main():
     ap.add_argument("--ncu-target", action="store_true",
                     help="run the sweep GEMMs untimed (profiling target)")
     ap.add_argument("--sizes", default="", help="with --ncu-target: comma-separated sizes")
+    ap.add_argument("--shape", default="",
+                    help="with --ncu-target: MxNxK[,MxNxK...] (bf16 with ABFT, or --plain)")
+    ap.add_argument("--plain", action="store_true",
+                    help="with --ncu-target --shape: fp16 without ABFT")
     ap.add_argument("--write-traffic", default="",
                     help="write the traffic JSON from an ncu CSV of the main kernel")
     ap.add_argument("--workload", choices=["square", "hostile", "random", "mlp"],
