@@ -153,6 +153,16 @@ typedef struct {
                            k-step); requires BLK_N 256, and with ABFT the
                            checksum GEMMs then run as separate launches.
                            `grid` counts CTAs and must then be even. */
+  int32_t abft_local;   /* ABFT reference checksums formed inside each CTA
+                           from the operand tiles in shared memory while the
+                           MMAs run ("Anatomy of High-Performance GEMM with
+                           Online Fault Tolerance on GPUs", threadblock-level
+                           FT-GEMM): no encode pass and no checksum GEMMs, for
+                           a data-parallel plan of at most one 128 x 128
+                           output tile per SM on single CTAs. The CUDA-core
+                           sums take several times the MMAs' time per k-step
+                           on GB300, so 0 (default) and 1 = never, 2 =
+                           whenever the shape allows it. */
 } skg_opts_t;
 
 /* One segment of a schedule (Stream-K page, Algorithm 5 / §5.2). k_iter_*
@@ -295,6 +305,8 @@ typedef struct {
                           launch, 0 = as separate launches (or no ABFT) */
   int32_t encode_in_kernel; /* ABFT: 1 = the side CTAs also run the encode
                           pass, so the call is a single launch */
+  int32_t local_checksums; /* ABFT: 1 = the reference checksums are formed in
+                          each CTA (skg_opts_t.abft_local), a single launch */
 } skg_plan_t;
 
 /* Same choice as skg_launch_shape, with the CTA-pair and checksum-tile

@@ -58,6 +58,12 @@ int sm_count_cached() {
   return v;
 }
 
+// The library does not pick in-CTA ABFT references by itself: on GB300 the
+// four epilogue warps (one per SM sub-partition, little latency hiding)
+// take ~1.5 us per 128 x 128 x 64 k-step for the sums, several times the
+// MMA's time, so a 1024^3 call took 35 us against 23 us on the fused
+// checksum path. skg_opts_t.abft_local = 2 selects them.
+
 struct Resolved {
   int sched;
   int grid;     // CTAs launched for the output tiles (two per cluster with pairs)
@@ -75,6 +81,7 @@ struct Resolved {
   int preencoded;
   int raster_band;
   int enc_inkernel;  // the dedicated side CTAs run the encode pass (no encode launch)
+  int abft_local;    // ABFT references formed in each CTA (one whole tile per CTA)
   int ws_grid;
   int64_t k_for_plan;  // CTAs the workspace's flags and partial slots are sized for
 };
@@ -151,6 +158,27 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
   if (o->raster_band < 0) return SKG_ERR_ARG;
   r.raster_band = o->raster_band;
   r.enc_inkernel = 0;
+  if (o->abft_local < 0 || o->abft_local > 2) return SKG_ERR_ARG;
+  // In-CTA ABFT references (on request): a data-parallel plan of at most
+  // one 128 x 128 tile per SM on single CTAs, so each CTA's epilogue warps
+  // can read every stage of its one tile.
+  r.abft_local = 0;
+  if (r.abft && o->abft_local == 2 && m > 0 && n > 0 && k > 0 && o->cta_pair != 2 &&
+      (o->tile_n == 0 || o->tile_n == 128) &&
+      (o->sched == SKG_SCHED_AUTO || o->sched == SKG_SCHED_DP)) {
+    const int64_t tiles = ((m + kBM - 1) / kBM) * ((n + 127) / 128);
+    const bool fits = tiles <= ms && (o->grid == 0 || o->grid >= tiles);
+    if (fits) {
+      r.abft_local = 1;
+      r.bn = 128;
+      r.sched = SKG_SCHED_DP;
+      r.grid = (int)tiles;
+      r.pair = 0;
+      r.grid_max = ms;
+      r.grid_ck = 0;
+      r.ws_grid = ms > r.grid ? ms : r.grid;
+    }
+  }
   return SKG_OK;
 }
 
@@ -253,13 +281,13 @@ struct Gemm {
   int in_dtype, out_dtype;
 };
 
-template <int BN, bool ABFT, bool PAIR = false>
+template <int BN, bool ABFT, bool PAIR = false, bool LOCAL = false>
 cudaError_t dispatch_out(int out_dtype, const Maps& mp, const KernelParams& p, int grid,
                          cudaStream_t st) {
   switch (out_dtype) {
-    case SKG_OUT_F32: return launch_gemm<BN, ABFT, 0, PAIR>(mp, p, grid, st);
-    case SKG_OUT_F16: return launch_gemm<BN, ABFT, 1, PAIR>(mp, p, grid, st);
-    default: return launch_gemm<BN, ABFT, 2, PAIR>(mp, p, grid, st);
+    case SKG_OUT_F32: return launch_gemm<BN, ABFT, 0, PAIR, LOCAL>(mp, p, grid, st);
+    case SKG_OUT_F16: return launch_gemm<BN, ABFT, 1, PAIR, LOCAL>(mp, p, grid, st);
+    default: return launch_gemm<BN, ABFT, 2, PAIR, LOCAL>(mp, p, grid, st);
   }
 }
 
@@ -386,14 +414,17 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   p.drop_signal = r.drop_signal;
   p.c_ptr = g.C;
   p.ldc = g.ldc;
+  p.in_f16 = g.in_dtype == SKG_IN_F16 ? 1 : 0;
 
   cudaError_t e;
   if (r.pair)
     e = abft_epilogue ? dispatch_out<256, true, true>(g.out_dtype, mp, p, launch_grid, stream)
                       : dispatch_out<256, false, true>(g.out_dtype, mp, p, launch_grid, stream);
   else if (r.bn == 128)
-    e = abft_epilogue ? dispatch_out<128, true>(g.out_dtype, mp, p, launch_grid, stream)
-                      : dispatch_out<128, false>(g.out_dtype, mp, p, launch_grid, stream);
+    e = (abft_epilogue && r.abft_local && !fuse_ck)
+            ? dispatch_out<128, true, false, true>(g.out_dtype, mp, p, launch_grid, stream)
+        : abft_epilogue ? dispatch_out<128, true>(g.out_dtype, mp, p, launch_grid, stream)
+                        : dispatch_out<128, false>(g.out_dtype, mp, p, launch_grid, stream);
   else
     e = abft_epilogue ? dispatch_out<256, true>(g.out_dtype, mp, p, launch_grid, stream)
                       : dispatch_out<256, false>(g.out_dtype, mp, p, launch_grid, stream);
@@ -541,7 +572,9 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
   uint8_t* ws = (uint8_t*)workspace;
   const Gemm g{m, n, k, A, lda, B, ldb, C, ldc, alpha, beta, in_dtype, out_dtype};
   bool fuse = false;
-  if (r.abft && can_fuse_checksums(L, r.bn)) {
+  if (r.abft && r.abft_local) {
+    // The reference checksums are formed inside the CTAs: one launch.
+  } else if (r.abft && can_fuse_checksums(L, r.bn)) {
     // The checksum-GEMM tiles run ahead of the output tiles in the same
     // launch, after the encode pass (skipped when pre-encoded).
     fuse = true;
@@ -687,8 +720,8 @@ skg_status_t skg_launch_plan(int64_t m, int64_t n, int64_t k, const skg_opts_t* 
   const int sms = sm_count_cached();
   skg_status_t st = resolve(m, n, k, opts, r, sms);
   if (st != SKG_OK) return st;
-  const bool fused =
-      r.abft && m > 0 && n > 0 && k > 0 && can_fuse_checksums(layout(m, n, k, r), r.bn);
+  const bool fused = r.abft && !r.abft_local && m > 0 && n > 0 && k > 0 &&
+                     can_fuse_checksums(layout(m, n, k, r), r.bn);
   if (fused) plan_fused(m, n, opts, SKG_IN_BF16, r);
   memset(out, 0, sizeof(*out));
   out->tile_m = r.pair ? 2 * kBM : kBM;
@@ -699,6 +732,7 @@ skg_status_t skg_launch_plan(int64_t m, int64_t n, int64_t k, const skg_opts_t* 
   out->side_ctas = fused ? r.grid_ck : 0;
   out->fused_checksums = fused ? 1 : 0;
   out->encode_in_kernel = r.enc_inkernel;
+  out->local_checksums = r.abft_local;
   return SKG_OK;
 }
 

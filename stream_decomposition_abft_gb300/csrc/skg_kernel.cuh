@@ -150,6 +150,7 @@ struct KernelParams {
   int32_t* trace;
   uint64_t* cta_clock;
   int drop_signal;  // testing: CTA index that skips its Signal, or -1
+  int in_f16;       // inputs are fp16 (else bf16): the in-CTA ABFT sums read them
   // C (and C0) for the shared tile reduction's plain stores: ldc elements
   // per row, the output type of the launch.
   void* c_ptr;
@@ -163,10 +164,14 @@ __host__ __device__ constexpr int pow2_at_least(int v) {
   return p;
 }
 
-template <int BN_, bool ABFT_, int OUT_, bool PAIR_ = false>
+template <int BN_, bool ABFT_, int OUT_, bool PAIR_ = false, bool LOCAL_ = false>
 struct Cfg {
   static constexpr int BN = BN_;
   static constexpr bool ABFT = ABFT_;
+  // In-CTA ABFT references (local_checksums): the epilogue warps also read
+  // every stage, for launches of at most one whole tile per CTA.
+  static constexpr bool LOCAL = LOCAL_;
+  static_assert(!LOCAL || (ABFT_ && !PAIR_), "in-CTA references need ABFT on single CTAs");
   static constexpr int OUT = OUT_;  // 0 = f32, 1 = f16, 2 = bf16
   // CTA pairs: a cluster of two CTAs runs 256 x BN tiles with one M = 256
   // MMA; each CTA loads its 128 rows of A and BN / 2 rows of B per stage.
@@ -728,6 +733,174 @@ static __device__ __noinline__ bool reduce_share(const KernelParams& p, float* r
   return true;
 }
 
+// Eight consecutive 16-bit inputs (one 16-byte chunk of a stage row) as fp32.
+template <bool F16>
+__device__ __forceinline__ void unpack8_in(uint4 q, float (&x)[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (F16) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    } else {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+}
+
+// In-CTA ABFT references, for launches of at most one whole output tile per
+// CTA ("Anatomy of High-Performance GEMM with Online Fault Tolerance on
+// GPUs", threadblock-level FT-GEMM: the checksums are updated at every
+// k-step from the operand tiles the block holds). For each stage of the
+// tile the four epilogue warps read the A tile (128 rows) and the B tile (BN
+// rows = output columns) out of shared memory (128-byte swizzle), form
+//   e^T A_s (64 values: the stage's A rows summed) and B_s e (its B rows
+//   summed), and accumulate in fp32
+//   cr[r] += A_s[r, :] . (B_s e)    (row reference of the accumulator row r
+//                                    the thread reads from TMEM),
+//   cc[j] += (e^T A_s) . B_s[j, :]  (column references, j = r, r + 128),
+// with the tile's max |a| and max |b| for the thresholds; every sum keeps
+// eight independent chains. Then the stage goes back to the producer (its
+// empty barrier counts the MMA commit and this arrival). `scratch` is 640
+// floats of shared memory; the walk of the ring starts at (stage, phase)
+// and the result says where it stands. ok = false after a timeout
+// (recorded).
+template <int BN>
+struct LocalSums {
+  float cr, cc[BN / 128], ma, mb;
+  int stage;
+  uint32_t phase;
+  bool ok;
+};
+
+template <class C, bool F16>
+static __device__ __noinline__ LocalSums<C::BN> local_checksums(
+    const KernelParams& p, uint8_t* ring, uint64_t* full_bar, uint64_t* empty_bar, int stage,
+    uint32_t phase, int nk, float* scratch, int ew, int lane, int et, int r, Aux* aux,
+    uint64_t limit) {
+  constexpr int BN = C::BN;
+  const int ch = lane & 7;              // 16-byte chunk: k values 8 ch .. 8 ch + 7
+  const int rg = ew * 4 + (lane >> 3);  // row group 0..15
+  float* part = scratch;                // [warp][e^T A_s (64), B_s e (64)]
+  float* fin = scratch + 4 * 128;       // e^T A_s (64), B_s e (64) of the whole CTA
+  float cr8[8], cc8[BN / 128][8], ma8[8], mb8[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    cr8[e] = ma8[e] = mb8[e] = 0.f;
+#pragma unroll
+    for (int h = 0; h < BN / 128; ++h) cc8[h][e] = 0.f;
+  }
+  LocalSums<BN> out;
+  out.ok = true;
+  for (int kb = 0; kb < nk; ++kb) {
+    const bool got = wait_bar(&full_bar[stage], phase, aux, limit);
+    if (!got && !aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+    if (!epi_all(got && !aborted(aux))) {
+      out.ok = false;
+      break;
+    }
+    const uint8_t* sa = ring + stage * C::STAGE_BYTES;
+    const uint8_t* sb = sa + C::A_BYTES;
+    // Column sums of the stage: the thread's chunk over its row group.
+    float as[8], bs[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) as[e] = bs[e] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kBM / 16; ++i) {
+      const int row = rg + 16 * i;
+      float x[8];
+      unpack8_in<F16>(
+          *reinterpret_cast<const uint4*>(sa + row * 128 + ((ch ^ (row & 7)) << 4)), x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) as[e] += x[e];
+    }
+#pragma unroll
+    for (int i = 0; i < BN / 16; ++i) {
+      const int row = rg + 16 * i;
+      float x[8];
+      unpack8_in<F16>(
+          *reinterpret_cast<const uint4*>(sb + row * 128 + ((ch ^ (row & 7)) << 4)), x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) bs[e] += x[e];
+    }
+    // The warp's four row groups (lane bits 3 and 4), then the four warps.
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      as[e] += __shfl_xor_sync(0xffffffffu, as[e], 8);
+      bs[e] += __shfl_xor_sync(0xffffffffu, bs[e], 8);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      as[e] += __shfl_xor_sync(0xffffffffu, as[e], 16);
+      bs[e] += __shfl_xor_sync(0xffffffffu, bs[e], 16);
+    }
+    if (lane < 8) {
+      float4* pa = reinterpret_cast<float4*>(part + ew * 128 + ch * 8);
+      float4* pb = reinterpret_cast<float4*>(part + ew * 128 + 64 + ch * 8);
+      pa[0] = make_float4(as[0], as[1], as[2], as[3]);
+      pa[1] = make_float4(as[4], as[5], as[6], as[7]);
+      pb[0] = make_float4(bs[0], bs[1], bs[2], bs[3]);
+      pb[1] = make_float4(bs[4], bs[5], bs[6], bs[7]);
+    }
+    named_bar_sync(1, kEpiThreads);
+    fin[et] = (part[et] + part[128 + et]) + (part[256 + et] + part[384 + et]);
+    named_bar_sync(1, kEpiThreads);
+    // Row reference of row r against B_s e; column references of columns
+    // r (+128) against e^T A_s.
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float x[8];
+      unpack8_in<F16>(*reinterpret_cast<const uint4*>(sa + r * 128 + ((c ^ (r & 7)) << 4)), x);
+      const float4 b0 = *reinterpret_cast<const float4*>(fin + 64 + 8 * c);
+      const float4 b1 = *reinterpret_cast<const float4*>(fin + 64 + 8 * c + 4);
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        cr8[e] = fmaf(x[e], bv[e], cr8[e]);
+        ma8[e] = fmaxf(ma8[e], fabsf(x[e]));
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < BN / 128; ++h) {
+      const int j = r + 128 * h;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        float x[8];
+        unpack8_in<F16>(*reinterpret_cast<const uint4*>(sb + j * 128 + ((c ^ (j & 7)) << 4)),
+                        x);
+        const float4 a0 = *reinterpret_cast<const float4*>(fin + 8 * c);
+        const float4 a1 = *reinterpret_cast<const float4*>(fin + 8 * c + 4);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          cc8[h][e] = fmaf(x[e], av[e], cc8[h][e]);
+          mb8[e] = fmaxf(mb8[e], fabsf(x[e]));
+        }
+      }
+    }
+    named_bar_sync(1, kEpiThreads);  // every read of the stage and of fin is done
+    if (et == 0) mbar_arrive(&empty_bar[stage]);
+    if (++stage == C::STAGES) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+  out.cr = ((cr8[0] + cr8[1]) + (cr8[2] + cr8[3])) + ((cr8[4] + cr8[5]) + (cr8[6] + cr8[7]));
+#pragma unroll
+  for (int h = 0; h < BN / 128; ++h)
+    out.cc[h] = ((cc8[h][0] + cc8[h][1]) + (cc8[h][2] + cc8[h][3])) +
+                ((cc8[h][4] + cc8[h][5]) + (cc8[h][6] + cc8[h][7]));
+  out.ma = fmaxf(fmaxf(fmaxf(ma8[0], ma8[1]), fmaxf(ma8[2], ma8[3])),
+                 fmaxf(fmaxf(ma8[4], ma8[5]), fmaxf(ma8[6], ma8[7])));
+  out.mb = fmaxf(fmaxf(fmaxf(mb8[0], mb8[1]), fmaxf(mb8[2], mb8[3])),
+                 fmaxf(fmaxf(mb8[4], mb8[5]), fmaxf(mb8[6], mb8[7])));
+  out.stage = stage;
+  out.phase = phase;
+  return out;
+}
+
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     skg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -800,7 +973,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = lane; i < nbars; i += 32) {
       uint64_t* bar = full_bar + i;
       const bool acc_empty = bar >= tempty_bar && bar < tempty_bar + 2;
-      mbar_init(bar, acc_empty ? (C::PAIR ? 2 * kEpiThreads : kEpiThreads) : 1);
+      // In-CTA ABFT: the epilogue also reads every stage, so a stage is
+      // free once the MMA commit and the epilogue have both arrived.
+      const bool stage_empty = bar >= empty_bar && bar < empty_bar + STAGES;
+      mbar_init(bar, acc_empty ? (C::PAIR ? 2 * kEpiThreads : kEpiThreads)
+                               : ((C::LOCAL && stage_empty) ? 2 : 1));
     }
     fence_barrier_init();
   }
@@ -1123,6 +1300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int bsel = 0;
     uint32_t c0_phase = 0;
     bool c0r_pending = false;  // C0 copies into the ring not yet waited for
+    int estage = 0;            // in-CTA ABFT: the epilogue's place in the stage ring
+    uint32_t ephase = 0;
     int nseg = 0;
     bool store_ok = true;
     bool ck_ready = false;
@@ -1259,7 +1438,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (A CTA pair's second half lies past m when m has an odd number of
       // 128-row tiles: nothing there to check.)
       const bool verify_here = C::ABFT && !is_ck && w.role != kRolePeer && m0 < p.m;
-      if (verify_here) {
+      if constexpr (C::LOCAL) {
+        // Reference checksums formed here from the shared-memory stages
+        // while the MMAs run (one whole tile per CTA).
+        float* scratch = reinterpret_cast<float*>(epi);
+        const int nk = w.kb_end - w.kb_begin;
+        const LocalSums<BN> ls =
+            p.in_f16 ? local_checksums<C, true>(p, ring, full_bar, empty_bar, estage, ephase, nk,
+                                                scratch, ew, lane, et, r, aux, limit)
+                     : local_checksums<C, false>(p, ring, full_bar, empty_bar, estage, ephase, nk,
+                                                 scratch, ew, lane, et, r, aux, limit);
+        if (!ls.ok) break;
+        estage = ls.stage;
+        ephase = ls.phase;
+        pf_cr0 = ls.cr;
+#pragma unroll
+        for (int h = 0; h < BN / 128; ++h) pf_cc0[h] = ls.cc[h];
+        pf_ma = ls.ma;
+        pf_mb = ls.mb;
+      } else if (verify_here) {
         if (s.t_ck > 0 && !ck_ready) {
           // The fused checksum tiles must all be stored first. Every CTA runs
           // its own share of them before its first output tile, and dedicated

@@ -41,7 +41,8 @@ class Opts(ctypes.Structure):
                 ("inject_bit", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64),
                 ("trace", ctypes.c_void_p), ("cta_clock", ctypes.c_void_p),
                 ("test_drop_signal", ctypes.c_int32), ("abft_preencoded", ctypes.c_int32),
-                ("raster_band", ctypes.c_int32), ("cta_pair", ctypes.c_int32)]
+                ("raster_band", ctypes.c_int32), ("cta_pair", ctypes.c_int32),
+                ("abft_local", ctypes.c_int32)]
 
 
 class Segment(ctypes.Structure):
@@ -64,7 +65,7 @@ class Plan(ctypes.Structure):
     _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("ctas", ctypes.c_int32),
                 ("cta_pair", ctypes.c_int32), ("sched", ctypes.c_int32),
                 ("side_ctas", ctypes.c_int32), ("fused_checksums", ctypes.c_int32),
-                ("encode_in_kernel", ctypes.c_int32)]
+                ("encode_in_kernel", ctypes.c_int32), ("local_checksums", ctypes.c_int32)]
 
 
 class Report(ctypes.Structure):

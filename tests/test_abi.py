@@ -37,11 +37,11 @@ def test_exports_every_declared_symbol(lib):
 
 def test_struct_sizes_match_header():
     # Sizes fixed by the header's field lists (x86-64 and aarch64 ABIs agree).
-    assert ctypes.sizeof(skgemm.Opts) == 80
+    assert ctypes.sizeof(skgemm.Opts) == 88
     assert ctypes.sizeof(skgemm.Segment) == 20
     assert ctypes.sizeof(skgemm.FaultRecord) == 64
     assert ctypes.sizeof(skgemm.Report) == 64 + 64 * 64
-    assert ctypes.sizeof(skgemm.Plan) == 32
+    assert ctypes.sizeof(skgemm.Plan) == 36
 
 
 def test_defaults(lib):

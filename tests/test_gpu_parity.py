@@ -324,6 +324,63 @@ def test_injected_fault_detected_located_corrected(mode, bit):
         pytest.skip(f"bit {bit} of {v} is {kind} at tau {tau}")
 
 
+@pytest.mark.parametrize("shape", [(300, 200, 200), (1000, 1300, 520), (1024, 1024, 1024),
+                                   (129, 3000, 4104)])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_abft_local_matches_fused(shape, dtype):
+    # Reference checksums formed inside the CTAs (abft_local = 2) against the
+    # encode pass + checksum GEMMs (abft_local = 1): the same output bits (the
+    # same MMAs and epilogue), no false positive, every tile checked, ragged
+    # m, n and k.
+    m, n, k = shape
+    tiles = ((m + 127) // 128) * ((n + 127) // 128)
+    if tiles > sms():
+        pytest.skip("more tiles than SMs")
+    p = inputs.make_problem(m, n, k, seed=m + k, in_dtype=dtype, out_dtype="f32",
+                            law_a="normal", law_b="normal", alpha=0.5, beta=1.5)
+    local = skgemm.opts_default(abft=1, abft_local=2)
+    assert skgemm.launch_plan(m, n, k, local).local_checksums == 1
+    ws = None
+    for _ in range(2):
+        C1, ws, st = run(p, local, ws=ws)
+        assert st == skgemm.OK
+        check_full(p, C1)
+        rep = ws.report(reset=True)
+        assert rep.detected == 0 and rep.status_bits == 0
+        assert rep.tiles_checked == tiles
+        assert rep.max_ratio_row < 0.1 and rep.max_ratio_col < 0.1
+    C2, ws2, st2 = run(p, skgemm.opts_default(abft=1, abft_local=1, tile_n=128, sched="dp"))
+    assert st2 == skgemm.OK and ws2.report().detected == 0
+    assert torch.equal(C1, C2)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("bit", [30, 28])
+def test_abft_local_injection(dtype, bit):
+    # A flipped accumulator bit under in-CTA references is detected, located
+    # and corrected as under the fused checksum path.
+    p = inputs.make_problem(512, 640, 1024, seed=78, in_dtype=dtype, out_dtype="f32",
+                            law_a="normal", law_b="normal", scale_b=0.02)
+    ref = reference(p)
+    tile, row, col = 13, 101, 7
+    tm, tn = divmod(tile, 5)
+    v = ref[tm * 128 + row, tn * 128 + col] / p.alpha
+    ma, mb = ab.tile_maxima(p.A.double().numpy(), p.B.double().numpy(), tm, tn, 128, 128)
+    tau = ab.default_tau(p.k, 128, ma, mb)
+    kind, _ = ab.classify_flip(v, bit, tau, 1e-3 * tau)
+    if kind != ab.MUST_DETECT:
+        pytest.skip(f"bit {bit} of {v} is {kind} at tau {tau}")
+    assert skgemm.launch_plan(512, 640, 1024,
+                              skgemm.opts_default(abft=1, abft_local=2)).local_checksums == 1
+    C, ws, st = _inject(p, dict(abft_local=2), tile, row, col, bit)
+    assert st == skgemm.OK
+    rep = ws.report()
+    assert rep.detected == 1 and rep.corrected == 1 and rep.uncorrectable == 0
+    rec = rep.records[0]
+    assert (rec.tile, rec.row, rec.col, rec.injected) == (tile, row, col, 1)
+    check_full(p, C, ref)
+
+
 def test_injection_without_abft_corrupts_output():
     p = inputs.make_problem(256, 256, 256, seed=9, in_dtype="bf16", out_dtype="f32",
                             law_a="normal", law_b="normal")
