@@ -52,13 +52,25 @@ typedef enum { SKG_IN_F16 = 0, SKG_IN_BF16 = 1 } skg_in_t;
 /* Element type of C (and of C0 when beta != 0). */
 typedef enum { SKG_OUT_F32 = 0, SKG_OUT_F16 = 1, SKG_OUT_BF16 = 2 } skg_out_t;
 
-/* Storage of A: row-major m x k (element (i,l) at A[i*lda + l]). This is
- * the "K-major" order the tensor cores read directly. */
-typedef enum { SKG_A_ROW = 0 } skg_a_layout_t;
+/* Storage of A (Stream-K page, problem statement: C = alpha A B + beta C
+ * with m, n, k and leading dimensions):
+ *   SKG_A_ROW  row-major m x k, element (i,l) at A[i*lda + l], lda >= k:
+ *              the "K-major" order the tensor cores read directly;
+ *   SKG_A_COL  column-major, element (i,l) at A[l*lda + i], lda >= m
+ *              ("M-major"). */
+typedef enum { SKG_A_ROW = 0, SKG_A_COL = 1 } skg_a_layout_t;
 
-/* Storage of B: K-major means B is stored n x k, element (l,j) at
- * B[j*ldb + l] (the "NT" form, as for a weight matrix of a linear layer). */
-typedef enum { SKG_B_KMAJOR = 0 } skg_b_layout_t;
+/* Storage of B:
+ *   SKG_B_KMAJOR  stored n x k, element (l,j) at B[j*ldb + l], ldb >= k (the
+ *                 "NT" form, as for a weight matrix of a linear layer);
+ *   SKG_B_NMAJOR  stored k x n, element (l,j) at B[l*ldb + j], ldb >= n (the
+ *                 plain row-major "NN" form).
+ * The MMAs read K-major operands. An operand given in the other form is
+ * first copied into a K-major buffer at the end of the workspace by a
+ * data-movement kernel (one extra read and write of that operand, bound by
+ * HBM bandwidth), and the GEMM runs on the copy; size the workspace with
+ * skg_workspace_size_layout. */
+typedef enum { SKG_B_KMAJOR = 0, SKG_B_NMAJOR = 1 } skg_b_layout_t;
 
 /* Schedules (Stream-K page, §3.2, §4, §5.2):
  *  DP       one persistent CTA walks tiles x, x+g, ... (Algorithm 2 folded
@@ -224,18 +236,30 @@ void skg_opts_default(skg_opts_t* opts);
  * checksums, and with ABFT the split encodings e^T A and B e. */
 size_t skg_workspace_size(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts);
 
+/* skg_workspace_size for the given operand layouts: the same bytes plus room
+ * for the K-major copies of MN-major operands (m x k and n x k elements, rows
+ * rounded up to 16 bytes). Equal to skg_workspace_size for SKG_A_ROW /
+ * SKG_B_KMAJOR; 0 for an unknown layout or invalid arguments. */
+size_t skg_workspace_size_layout(int64_t m, int64_t n, int64_t k, int32_t a_layout,
+                                 int32_t b_layout, const skg_opts_t* opts);
+
 /* Zero a workspace (`bytes` from skg_workspace_size) before its first use.
  * Afterwards the library keeps it consistent itself (flags carry a launch
  * epoch, so they never need clearing). Asynchronous on `stream`. */
 skg_status_t skg_workspace_init(void* workspace, size_t bytes, void* stream);
 
 /* C = alpha * A B + beta * C, asynchronous on `stream`.
- *   A: device, in_dtype, row-major m x k, lda >= k (elements).
- *   B: device, in_dtype, K-major (stored n x k), ldb >= k.
+ *   A: device, in_dtype, stored as a_layout says (skg_a_layout_t), lda in
+ *      elements (>= k row-major, >= m column-major).
+ *   B: device, in_dtype, stored as b_layout says (skg_b_layout_t), ldb
+ *      >= k (K-major) or >= n (N-major).
  *   C: device, out_dtype, row-major m x n, ldc >= n; read only if beta != 0.
  *   A, B, C must be 16-byte aligned and lda, ldb, ldc must be multiples of
- *   16 bytes (the TMA engine's rule); otherwise SKG_ERR_UNSUPPORTED.
- *   workspace: device, >= skg_workspace_size(m, n, k, opts) bytes, zeroed
+ *   16 bytes (the TMA engine's rule); otherwise SKG_ERR_UNSUPPORTED. An
+ *   unknown layout value or a leading dimension below its minimum is
+ *   SKG_ERR_ARG.
+ *   workspace: device, >= skg_workspace_size_layout(m, n, k, a_layout,
+ *   b_layout, opts) bytes (skg_workspace_size for K-major operands), zeroed
  *   once with skg_workspace_init; one workspace per stream (two launches
  *   that share a workspace must not overlap).
  *   opts: NULL for defaults. m, n or k of zero is valid (k = 0 gives

@@ -519,14 +519,46 @@ void plan_fused(int64_t m, int64_t n, const skg_opts_t* opts, int32_t in_dtype, 
 }
 
 skg_status_t check_inputs(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
-                          const void* B, int64_t ldb) {
+                          const void* B, int64_t ldb, int32_t a_layout = SKG_A_ROW,
+                          int32_t b_layout = SKG_B_KMAJOR) {
   if (!A || !B) return SKG_ERR_ARG;
-  if (lda < k || ldb < k) return SKG_ERR_ARG;
+  // The leading dimension spans the operand's contiguous index: k for the
+  // K-major forms, m (A column-major) or n (B stored k x n) otherwise.
+  if (lda < (a_layout == SKG_A_COL ? m : k) || ldb < (b_layout == SKG_B_NMAJOR ? n : k))
+    return SKG_ERR_ARG;
   if (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 || (ldb * 2) % 16)
     return SKG_ERR_UNSUPPORTED;
-  (void)m;
-  (void)n;
   return SKG_OK;
+}
+
+// K-major copies of MN-major operands, placed after the rest of the
+// workspace: A as m x ldk, B as n x ldk (ldk = k rounded up to 8 elements,
+// so rows start on 16-byte boundaries as the TMA engine requires).
+struct Relayout {
+  size_t a = 0, b = 0, total = 0;  // offsets from the workspace base; total = end
+  int64_t ldk = 0;
+};
+
+Relayout relayout_plan(int64_t m, int64_t n, int64_t k, int32_t a_layout, int32_t b_layout,
+                       size_t base) {
+  Relayout R;
+  R.ldk = (int64_t)round_up((size_t)(k > 0 ? k : 1), 8);
+  size_t off = round_up(base, 256);
+  if (a_layout == SKG_A_COL) {
+    R.a = off;
+    off = round_up(off + (size_t)m * R.ldk * 2, 256);
+  }
+  if (b_layout == SKG_B_NMAJOR) {
+    R.b = off;
+    off = round_up(off + (size_t)n * R.ldk * 2, 256);
+  }
+  R.total = (a_layout == SKG_A_COL || b_layout == SKG_B_NMAJOR) ? off : base;
+  return R;
+}
+
+bool layout_valid(int32_t a_layout, int32_t b_layout) {
+  return (a_layout == SKG_A_ROW || a_layout == SKG_A_COL) &&
+         (b_layout == SKG_B_KMAJOR || b_layout == SKG_B_NMAJOR);
 }
 
 skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void* A, int64_t lda,
@@ -539,7 +571,7 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
   if (m > INT32_MAX / 4 || n > INT32_MAX / 4 || k > INT32_MAX / 4) return SKG_ERR_UNSUPPORTED;
   if (in_dtype != SKG_IN_F16 && in_dtype != SKG_IN_BF16) return SKG_ERR_ARG;
   if (out_dtype < SKG_OUT_F32 || out_dtype > SKG_OUT_BF16) return SKG_ERR_ARG;
-  if (a_layout != SKG_A_ROW || b_layout != SKG_B_KMAJOR) return SKG_ERR_UNSUPPORTED;
+  if (!layout_valid(a_layout, b_layout)) return SKG_ERR_ARG;
   if (m == 0 || n == 0) return SKG_OK;
   const int out_bytes = out_dtype == SKG_OUT_F32 ? 4 : 2;
   if (!C) return SKG_ERR_ARG;
@@ -550,7 +582,7 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
                ? SKG_OK
                : SKG_ERR_CUDA;
   }
-  skg_status_t st = check_inputs(m, n, k, A, lda, B, ldb);
+  skg_status_t st = check_inputs(m, n, k, A, lda, B, ldb, a_layout, b_layout);
   if (st != SKG_OK) return st;
 
   const int sms = sm_count_cached();
@@ -566,10 +598,24 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
   st = resolve(m, n, k, opts, r, sms);
   if (st != SKG_OK) return st;
   const Layout L = layout(m, n, k, r);
-  if (!workspace || !aligned16(workspace) || ws_bytes < L.total) return SKG_ERR_WORKSPACE;
+  const Relayout R = relayout_plan(m, n, k, a_layout, b_layout, L.total);
+  if (!workspace || !aligned16(workspace) || ws_bytes < R.total) return SKG_ERR_WORKSPACE;
   if (!tensor_map_encoder()) return SKG_ERR_CUDA;
 
   uint8_t* ws = (uint8_t*)workspace;
+  // MN-major operands: the GEMM runs on K-major copies in the workspace.
+  if (a_layout == SKG_A_COL) {
+    if (launch_relayout(A, lda, m, k, ws + R.a, R.ldk, sms, stream) != cudaSuccess)
+      return SKG_ERR_CUDA;
+    A = ws + R.a;
+    lda = R.ldk;
+  }
+  if (b_layout == SKG_B_NMAJOR) {
+    if (launch_relayout(B, ldb, n, k, ws + R.b, R.ldk, sms, stream) != cudaSuccess)
+      return SKG_ERR_CUDA;
+    B = ws + R.b;
+    ldb = R.ldk;
+  }
   const Gemm g{m, n, k, A, lda, B, ldb, C, ldc, alpha, beta, in_dtype, out_dtype};
   bool fuse = false;
   if (r.abft && r.abft_local) {
@@ -607,6 +653,14 @@ size_t skg_workspace_size(int64_t m, int64_t n, int64_t k, const skg_opts_t* opt
   const int sms = sm_count_cached();
   if (resolve(m, n, k, opts, r, sms) != SKG_OK) return 0;
   return layout(m, n, k, r).total;
+}
+
+size_t skg_workspace_size_layout(int64_t m, int64_t n, int64_t k, int32_t a_layout,
+                                 int32_t b_layout, const skg_opts_t* opts) {
+  if (!layout_valid(a_layout, b_layout)) return 0;
+  const size_t base = skg_workspace_size(m, n, k, opts);
+  if (base == 0) return 0;
+  return relayout_plan(m, n, k, a_layout, b_layout, base).total;
 }
 
 skg_status_t skg_workspace_init(void* workspace, size_t bytes, void* stream) {

@@ -91,6 +91,14 @@ constexpr int kEncBoxRows = SKG_ENC_BOX_ROWS;
 // kEncBoxCols-column slices of the encode pass.
 int encode_slices(int kp);
 
+// MN-major operand -> K-major copy (skg_relayout.cu): `src` holds `cols`
+// lines of `rows` 16-bit elements (element (r, c) at src[c * ld_src + r]);
+// dst receives element (r, c) at dst[r * ld_dst + c]. ld_src and ld_dst are
+// multiples of 8 elements, both bases 16-byte aligned. Launched with
+// programmatic stream serialization like every kernel of the library.
+cudaError_t launch_relayout(const void* src, int64_t ld_src, int64_t rows, int64_t cols,
+                            void* dst, int64_t ld_dst, int sms, cudaStream_t stream);
+
 // C = beta * C for k == 0 (skg_encode.cu).
 cudaError_t launch_scale(int out_dtype, void* C, int64_t ldc, int m, int n, float beta,
                          cudaStream_t stream);

@@ -76,7 +76,7 @@ extern "C" skg_status_t skg_gemm_noalloc(int64_t m, int64_t n, int64_t k, float 
     skg_opts_default(&o);
   }
   if (o.tile_n == 0) o.tile_n = 128;
-  const size_t need = skg_workspace_size(m, n, k, &o);
+  const size_t need = skg_workspace_size_layout(m, n, k, a_layout, b_layout, &o);
   if (need == 0) return SKG_ERR_ARG;
   if (need > (size_t)SKG_NOALLOC_SCRATCH_BYTES) return SKG_ERR_WORKSPACE;
   void* scratch = nullptr;

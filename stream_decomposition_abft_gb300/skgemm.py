@@ -19,7 +19,9 @@ LIB_PATH = os.path.join(_HERE, "libskgemm.so")
 IN_F16, IN_BF16 = 0, 1
 OUT_F32, OUT_F16, OUT_BF16 = 0, 1, 2
 A_ROW = 0
+A_COL = 1
 B_KMAJOR = 0
+B_NMAJOR = 1
 SCHED_DP, SCHED_SK, SCHED_DP_SK1, SCHED_SK2_DP, SCHED_AUTO = 0, 1, 2, 3, 4
 ROLE_FULL, ROLE_OWNER, ROLE_PEER = 0, 1, 2
 OK = 0
@@ -81,7 +83,7 @@ class Report(ctypes.Structure):
 SYMBOLS = ("skg_opts_default", "skg_workspace_size", "skg_workspace_init", "skg_gemm",
            "skg_gemm_verify", "skg_abft_encode", "skg_schedule_query", "skg_launch_shape", "skg_report_read",
            "skg_device_sm_count", "skg_status_string", "skg_gemm_noalloc", "skg_schedule_cost",
-           "skg_launch_plan")
+           "skg_launch_plan", "skg_workspace_size_layout")
 
 _lib = None
 
@@ -107,6 +109,8 @@ def lib() -> ctypes.CDLL:
     L.skg_opts_default.restype = None
     L.skg_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(Opts)]
     L.skg_workspace_size.restype = sz
+    L.skg_workspace_size_layout.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(Opts)]
+    L.skg_workspace_size_layout.restype = sz
     L.skg_workspace_init.argtypes = [vp, sz, vp]
     L.skg_workspace_init.restype = i32
     gemm_args = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, i32, i32, i32, i32,
@@ -155,6 +159,12 @@ def opts_default(**kw) -> Opts:
 
 def workspace_size(m: int, n: int, k: int, opts: Optional[Opts] = None) -> int:
     return int(lib().skg_workspace_size(m, n, k, ctypes.byref(opts) if opts else None))
+
+
+def workspace_size_layout(m: int, n: int, k: int, a_layout: int, b_layout: int,
+                          opts: Optional[Opts] = None) -> int:
+    return int(lib().skg_workspace_size_layout(m, n, k, a_layout, b_layout,
+                                               ctypes.byref(opts) if opts else None))
 
 
 def workspace_init(ws_ptr: int, nbytes: int, stream: int = 0) -> int:
@@ -288,14 +298,16 @@ class Workspace:
 
 
 def matmul(A, B, C, alpha: float = 1.0, beta: float = 0.0, opts: Optional[Opts] = None,
-           workspace: Optional[Workspace] = None, verify: bool = False, stream=None):
-    """C = alpha * A @ B^T + beta * C through skg_gemm (or skg_gemm_verify).
+           workspace: Optional[Workspace] = None, verify: bool = False, stream=None,
+           a_layout: int = A_ROW, b_layout: int = B_KMAJOR):
+    """C = alpha * op(A) op(B) + beta * C through skg_gemm (or skg_gemm_verify).
 
-    A: (m, k) row-major, B: (n, k) row-major ("K-major" B), C: (m, n); all on
-    the same CUDA device, unit stride in the last dimension. Returns C."""
+    A: (m, k) row-major (a_layout A_ROW) or (k, m) (A_COL); B: (n, k)
+    ("K-major", B_KMAJOR) or (k, n) (B_NMAJOR); C: (m, n). All on the same
+    CUDA device, unit stride in the last dimension. Returns C."""
     import torch
-    m, k = A.shape
-    n, kb = B.shape
+    m, k = A.shape if a_layout == A_ROW else A.shape[::-1]
+    n, kb = B.shape if b_layout == B_KMAJOR else B.shape[::-1]
     if kb != k or tuple(C.shape) != (m, n):
         raise ValueError("shape mismatch")
     for t in (A, B, C):
@@ -304,11 +316,11 @@ def matmul(A, B, C, alpha: float = 1.0, beta: float = 0.0, opts: Optional[Opts] 
     if A.dtype != B.dtype:
         raise ValueError("A and B must have the same dtype")
     if workspace is None:
-        workspace = Workspace(workspace_size(m, n, k, opts), A.device)
+        workspace = Workspace(workspace_size_layout(m, n, k, a_layout, b_layout, opts), A.device)
     st_handle = (stream or torch.cuda.current_stream(A.device)).cuda_stream
     fn = gemm_verify if verify else gemm
     st = fn(m, n, k, alpha, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), beta,
-            C.data_ptr(), C.stride(0), _IN[_dt_name(A)], _OUT[_dt_name(C)], A_ROW, B_KMAJOR,
+            C.data_ptr(), C.stride(0), _IN[_dt_name(A)], _OUT[_dt_name(C)], a_layout, b_layout,
             opts, workspace.ptr, workspace.nbytes, st_handle)
     if st != OK:
         raise SkgError(st, "skg_gemm_verify" if verify else "skg_gemm")

@@ -56,18 +56,20 @@ def run(p: inputs.Problem, opts=None, ws=None, dev="cuda", verify=False, lda=Non
     A, B = to_device(p, dev, lda, ldb)
     C = out_init(p, dev)
     if ws is None:
-        ws = skgemm.Workspace(skgemm.workspace_size(p.m, p.n, p.k, opts), dev)
+        ws = skgemm.Workspace(skgemm.workspace_size_layout(p.m, p.n, p.k, p.a_layout, p.b_layout,
+                                                           opts), dev)
     stream = torch.cuda.current_stream().cuda_stream
     fn = skgemm.gemm_verify if verify else skgemm.gemm
     st = fn(p.m, p.n, p.k, p.alpha, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), p.beta,
-            C.data_ptr(), C.stride(0), IN_CODE[p.in_dtype], OUT_CODE[p.out_dtype], 0, 0, opts,
-            ws.ptr, ws.nbytes, stream)
+            C.data_ptr(), C.stride(0), IN_CODE[p.in_dtype], OUT_CODE[p.out_dtype], p.a_layout,
+            p.b_layout, opts, ws.ptr, ws.nbytes, stream)
     return C, ws, st
 
 
 def reference(p: inputs.Problem) -> np.ndarray:
     C0 = p.C0.float() if p.C0 is not None else None
-    return oracle.gemm(p.A, p.B, alpha=p.alpha, beta=p.beta, C0=C0)
+    return oracle.gemm(p.A, p.B, alpha=p.alpha, beta=p.beta, C0=C0, a_layout=p.a_layout,
+                       b_layout=p.b_layout)
 
 
 def check_full(p: inputs.Problem, C: torch.Tensor, ref: np.ndarray = None):
@@ -104,7 +106,8 @@ def check_sampled(p: inputs.Problem, C: torch.Tensor, seed: int = 0, count: int 
                   rows: int = 8, cols: int = 8):
     r, c = sample_plan(p.m, p.n, seed, count, rows, cols)
     C0 = p.C0.float() if p.C0 is not None else None
-    ref = oracle.gemm_entries(p.A, p.B, r, c, alpha=p.alpha, beta=p.beta, C0=C0)
+    ref = oracle.gemm_entries(p.A, p.B, r, c, alpha=p.alpha, beta=p.beta, C0=C0,
+                              a_layout=p.a_layout, b_layout=p.b_layout)
     got = C[torch.as_tensor(r, device=C.device), torch.as_tensor(c, device=C.device)]
     got = got.float().cpu().double().numpy()
     tol = tolerance(p, ref)

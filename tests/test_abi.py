@@ -106,7 +106,12 @@ def test_argument_errors_are_synchronous(lib):
     assert call(-1, 4, 4) == skgemm.ERR_ARG
     assert call(4, 4, 4, in_dtype=7) == skgemm.ERR_ARG
     assert call(4, 4, 4, out_dtype=9) == skgemm.ERR_ARG
-    assert call(4, 4, 4, a_layout=1) == skgemm.ERR_UNSUPPORTED
+    assert call(4, 4, 4, a_layout=2) == skgemm.ERR_ARG      # unknown layouts
+    assert call(4, 4, 4, b_layout=-1) == skgemm.ERR_ARG
+    # MN-major operands: the leading dimension spans m (A) or n (B).
+    assert call(128, 4, 4, a_layout=skgemm.A_COL, lda=64) == skgemm.ERR_ARG
+    assert call(4, 128, 4, b_layout=skgemm.B_NMAJOR, ldb=64) == skgemm.ERR_ARG
+    assert call(48, 4, 4, a_layout=skgemm.A_COL, lda=60) == skgemm.ERR_UNSUPPORTED  # 120 bytes
     assert call(0, 4, 4) == skgemm.OK                 # empty output: nothing to do
     assert call(4, 4, 4, C=None) == skgemm.ERR_ARG
     assert call(4, 64, 4, ldc=32) == skgemm.ERR_ARG     # ldc < n
@@ -128,6 +133,23 @@ def test_workspace_size_scales_with_grid_not_problem(lib):
     assert skgemm.workspace_size(1024, 1024, 1024, o2) < small
     oa = skgemm.opts_default(grid=148, tile_n=128, abft=1)
     assert skgemm.workspace_size(1024, 1024, 1024, oa) > small
+
+
+def test_workspace_size_layout_adds_the_k_major_copies(lib):
+    # MN-major operands are copied K-major into the end of the workspace:
+    # m x k and n x k elements of 2 bytes, rows rounded up to 16 bytes.
+    o = skgemm.opts_default(grid=148, tile_n=128)
+    m, n, k = 1000, 700, 333
+    base = skgemm.workspace_size(m, n, k, o)
+    kr = (k + 7) // 8 * 8
+    assert skgemm.workspace_size_layout(m, n, k, skgemm.A_ROW, skgemm.B_KMAJOR, o) == base
+    a = skgemm.workspace_size_layout(m, n, k, skgemm.A_COL, skgemm.B_KMAJOR, o)
+    b = skgemm.workspace_size_layout(m, n, k, skgemm.A_ROW, skgemm.B_NMAJOR, o)
+    ab = skgemm.workspace_size_layout(m, n, k, skgemm.A_COL, skgemm.B_NMAJOR, o)
+    assert base + m * kr * 2 <= a < base + m * kr * 2 + 512
+    assert base + n * kr * 2 <= b < base + n * kr * 2 + 512
+    assert ab >= base + (m + n) * kr * 2 and ab > max(a, b)
+    assert skgemm.workspace_size_layout(m, n, k, 2, 0, o) == 0
 
 
 # ----------------------------------------------------------------------------

@@ -544,6 +544,84 @@ def test_cta_pairs_abft_injection(bit):
     check_full(p, C, ref)
 
 
+# --------------------------------------------------------------------------- MN-major operands
+def _ld16(x):
+    """Row stride of the stored matrix, rounded up to 16 bytes (TMA rule)."""
+    return (x.shape[1] + 7) // 8 * 8
+
+
+@pytest.mark.parametrize("layouts", [(1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("shape", [(200, 136, 72), (1000, 1304, 520), (129, 3000, 4104),
+                                   (77, 50, 77)])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_mn_major_layouts(layouts, shape, dtype):
+    # Column-major A (stored k x m) and / or N-major B (stored k x n), ragged
+    # in every dimension, padded leading dimensions, alpha and beta: element
+    # by element against the oracle, which indexes the stored operands as
+    # given; and bit for bit against the same logical product from K-major
+    # operands (the copy is exact and the plan depends only on m, n, k).
+    a_layout, b_layout = layouts
+    m, n, k = shape
+    p = inputs.make_problem(m, n, k, seed=m + 3 * n + k, in_dtype=dtype, out_dtype="f32",
+                            law_a="normal", law_b="normal", alpha=0.5, beta=1.5,
+                            a_layout=a_layout, b_layout=b_layout)
+    C, ws, st = run(p, skgemm.opts_default(), lda=_ld16(p.A) + 8, ldb=_ld16(p.B))
+    assert st == skgemm.OK
+    check_full(p, C)
+    A_k = p.A.t().contiguous() if a_layout else p.A
+    B_k = p.B.t().contiguous() if b_layout else p.B
+    pk = inputs.Problem(m, n, k, A_k, B_k, p.C0, p.alpha, p.beta, p.in_dtype, p.out_dtype, 0, 0)
+    if k % 8 == 0:  # K-major storage needs 16-byte rows
+        Ck, _, stk = run(pk, skgemm.opts_default())
+        assert stk == skgemm.OK
+        assert torch.equal(C, Ck)
+
+
+@pytest.mark.parametrize("layouts", [(1, 1), (1, 0)])
+def test_mn_major_layouts_abft(layouts):
+    # ABFT on the copies: clean run, every tile checked, and the same bits as
+    # the K-major call at a sweep size.
+    a_layout, b_layout = layouts
+    s = 2048
+    p = inputs.make_problem(s, s, s, seed=11, in_dtype="bf16", out_dtype="bf16",
+                            law_a="normal", law_b="normal", scale_a=s ** -0.5, scale_b=s ** -0.5,
+                            a_layout=a_layout, b_layout=b_layout)
+    o = skgemm.opts_default(abft=1)
+    C, ws, st = run(p, o)
+    assert st == skgemm.OK
+    rep = ws.report()
+    assert rep.detected == 0 and rep.status_bits == 0 and rep.tiles_checked > 0
+    check_sampled(p, C, seed=5)
+    A_k = p.A.t().contiguous() if a_layout else p.A
+    B_k = p.B.t().contiguous() if b_layout else p.B
+    pk = inputs.Problem(s, s, s, A_k, B_k, p.C0, p.alpha, p.beta, p.in_dtype, p.out_dtype, 0, 0)
+    Ck, wsk, stk = run(pk, o)
+    assert stk == skgemm.OK and wsk.report().tiles_checked == rep.tiles_checked
+    assert torch.equal(C, Ck)
+
+
+def test_mn_major_noalloc_and_matmul():
+    # The allocation-free entry point and the torch helper take the layouts
+    # too; an MN-major leading dimension below m is an argument error.
+    m, n, k = 256, 384, 192
+    p = inputs.make_problem(m, n, k, seed=21, in_dtype="bf16", out_dtype="bf16",
+                            law_a="normal", law_b="normal", a_layout=1, b_layout=1)
+    A, B = p.A.cuda(), p.B.cuda()
+    C = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    skgemm.matmul(A, B, C, a_layout=skgemm.A_COL, b_layout=skgemm.B_NMAJOR)
+    check_full(p, C)
+    C2 = torch.empty_like(C)
+    st = skgemm.gemm_noalloc(m, n, k, 1.0, A.data_ptr(), m, B.data_ptr(), n, 0.0, C2.data_ptr(), n,
+                             skgemm.IN_BF16, skgemm.OUT_BF16, 1, 1, None,
+                             torch.cuda.current_stream().cuda_stream)
+    assert st == skgemm.OK
+    assert torch.equal(C, C2)
+    st = skgemm.gemm_noalloc(m, n, k, 1.0, A.data_ptr(), m - 8, B.data_ptr(), n, 0.0,
+                             C2.data_ptr(), n, skgemm.IN_BF16, skgemm.OUT_BF16, 1, 1, None,
+                             torch.cuda.current_stream().cuda_stream)
+    assert st == skgemm.ERR_ARG
+
+
 # --------------------------------------------------------------------------- single-launch ABFT
 @pytest.mark.parametrize("shape", [(1024, 1024, 1024), (384, 640, 320), (300, 1000, 520)])
 def test_abft_encode_in_kernel(shape):
