@@ -286,9 +286,11 @@ skg_status_t skg_gemm_verify(int64_t m, int64_t n, int64_t k, float alpha, const
  * plus per-tile max |A| and max |B| for the default thresholds ("Anatomy of
  * High-Performance GEMM with Online Fault Tolerance on GPUs",
  * threadblock-level ABFT, Fig. 5: the encodings e^T A and B e of each
- * threadblock's operands). Arguments as for skg_gemm; opts must be the
- * options of the gemm call that follows with opts->abft_preencoded = 1.
- * Asynchronous on `stream`. */
+ * threadblock's operands). Arguments as for skg_gemm with K-major operands
+ * (A row-major, B stored n x k; the encodings do not depend on the layout,
+ * so they also serve a following call with MN-major operands); opts must
+ * be the options of the gemm call that follows with opts->abft_preencoded
+ * = 1. Asynchronous on `stream`. */
 skg_status_t skg_abft_encode(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
                              const void* B, int64_t ldb, int32_t in_dtype,
                              const skg_opts_t* opts, void* workspace, size_t ws_bytes,
