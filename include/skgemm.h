@@ -65,10 +65,12 @@ typedef enum { SKG_A_ROW = 0, SKG_A_COL = 1 } skg_a_layout_t;
  *                 "NT" form, as for a weight matrix of a linear layer);
  *   SKG_B_NMAJOR  stored k x n, element (l,j) at B[l*ldb + j], ldb >= n (the
  *                 plain row-major "NN" form).
- * The MMAs read K-major operands. An operand given in the other form is
- * first copied into a K-major buffer at the end of the workspace by a
- * data-movement kernel (one extra read and write of that operand, bound by
- * HBM bandwidth), and the GEMM runs on the copy; size the workspace with
+ * Without ABFT the MMAs read an MN-major operand directly (TMA boxes of 64
+ * MN elements x 64 k, MN-major shared-memory operand descriptors). With
+ * ABFT (whose encode pass and checksum GEMMs read K-major operands) such an
+ * operand is first copied into a K-major buffer at the end of the workspace
+ * by a data-movement kernel (one extra read and write of that operand, bound
+ * by HBM bandwidth) and the call runs on the copy; size the workspace with
  * skg_workspace_size_layout. */
 typedef enum { SKG_B_KMAJOR = 0, SKG_B_NMAJOR = 1 } skg_b_layout_t;
 
@@ -236,10 +238,10 @@ void skg_opts_default(skg_opts_t* opts);
  * checksums, and with ABFT the split encodings e^T A and B e. */
 size_t skg_workspace_size(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts);
 
-/* skg_workspace_size for the given operand layouts: the same bytes plus room
- * for the K-major copies of MN-major operands (m x k and n x k elements, rows
- * rounded up to 16 bytes). Equal to skg_workspace_size for SKG_A_ROW /
- * SKG_B_KMAJOR; 0 for an unknown layout or invalid arguments. */
+/* skg_workspace_size for the given operand layouts: with ABFT on in opts,
+ * the same bytes plus room for the K-major copies of MN-major operands
+ * (m x k and n x k elements, rows rounded up to 16 bytes); otherwise equal
+ * to skg_workspace_size. 0 for an unknown layout or invalid arguments. */
 size_t skg_workspace_size_layout(int64_t m, int64_t n, int64_t k, int32_t a_layout,
                                  int32_t b_layout, const skg_opts_t* opts);
 

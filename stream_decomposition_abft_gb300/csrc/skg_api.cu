@@ -279,6 +279,9 @@ struct Gemm {
   int64_t ldc;
   float alpha, beta;
   int in_dtype, out_dtype;
+  // MN-major operands read directly by the MMAs (A stored k x m, B stored
+  // k x n); launches without ABFT only.
+  int a_mn = 0, b_mn = 0;
 };
 
 template <int BN, bool ABFT, bool PAIR = false, bool LOCAL = false>
@@ -309,10 +312,19 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
                                                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int out_bytes = g.out_dtype == SKG_OUT_F32 ? 4 : 2;
   Maps mp;
-  if (make_map(&mp.a, in_t, 2, g.A, (uint64_t)g.k, (uint64_t)g.m, (uint64_t)g.lda, kBK, kBM) !=
-          CUDA_SUCCESS ||
-      make_map(&mp.b, in_t, 2, g.B, (uint64_t)g.k, (uint64_t)g.n, (uint64_t)g.ldb, kBK,
-               r.pair ? r.bn / 2 : r.bn) != CUDA_SUCCESS ||
+  // K-major operands: one kBK x rows box per stage; MN-major ones: boxes of
+  // 64 MN elements x kBK (the kernel issues rows / 64 of them).
+  const CUresult ra =
+      g.a_mn ? make_map(&mp.a, in_t, 2, g.A, (uint64_t)g.m, (uint64_t)g.k, (uint64_t)g.lda,
+                        kMnBox, kBK)
+             : make_map(&mp.a, in_t, 2, g.A, (uint64_t)g.k, (uint64_t)g.m, (uint64_t)g.lda, kBK,
+                        kBM);
+  const CUresult rb =
+      g.b_mn ? make_map(&mp.b, in_t, 2, g.B, (uint64_t)g.n, (uint64_t)g.k, (uint64_t)g.ldb,
+                        kMnBox, kBK)
+             : make_map(&mp.b, in_t, 2, g.B, (uint64_t)g.k, (uint64_t)g.n, (uint64_t)g.ldb, kBK,
+                        r.pair ? r.bn / 2 : r.bn);
+  if (ra != CUDA_SUCCESS || rb != CUDA_SUCCESS ||
       make_map(&mp.c, out_t, out_bytes, g.C, (uint64_t)g.n, (uint64_t)g.m, (uint64_t)g.ldc,
                128 / out_bytes, 32) != CUDA_SUCCESS)
     return SKG_ERR_UNSUPPORTED;
@@ -361,7 +373,10 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   p.k = (int)g.k;
   p.alpha = g.alpha;
   p.beta = g.beta;
-  p.idesc_main = idesc_f16(g.in_dtype == SKG_IN_BF16, r.pair ? 2 * kBM : kBM, r.bn);
+  p.idesc_main = idesc_f16(g.in_dtype == SKG_IN_BF16, r.pair ? 2 * kBM : kBM, r.bn) |
+                 ((uint32_t)(g.a_mn != 0) << 15) | ((uint32_t)(g.b_mn != 0) << 16);
+  p.a_mn = g.a_mn;
+  p.b_mn = g.b_mn;
   p.ck_cr_tiles = ck_cr;
   p.ck_n_cr = kEncRows * L.tiles_b;
   p.ck_n_cc = kEncRows * L.tiles_a;
@@ -556,6 +571,15 @@ Relayout relayout_plan(int64_t m, int64_t n, int64_t k, int32_t a_layout, int32_
   return R;
 }
 
+// The layout whose operand gets a K-major copy: MN-major operands of ABFT
+// calls (the MMAs of plain calls read MN-major operands directly).
+int32_t copy_layout_a(int32_t a_layout, const Resolved& r) {
+  return r.abft ? a_layout : SKG_A_ROW;
+}
+int32_t copy_layout_b(int32_t b_layout, const Resolved& r) {
+  return r.abft ? b_layout : SKG_B_KMAJOR;
+}
+
 bool layout_valid(int32_t a_layout, int32_t b_layout) {
   return (a_layout == SKG_A_ROW || a_layout == SKG_A_COL) &&
          (b_layout == SKG_B_KMAJOR || b_layout == SKG_B_NMAJOR);
@@ -598,25 +622,32 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
   st = resolve(m, n, k, opts, r, sms);
   if (st != SKG_OK) return st;
   const Layout L = layout(m, n, k, r);
-  const Relayout R = relayout_plan(m, n, k, a_layout, b_layout, L.total);
+  const Relayout R = relayout_plan(m, n, k, copy_layout_a(a_layout, r),
+                                   copy_layout_b(b_layout, r), L.total);
   if (!workspace || !aligned16(workspace) || ws_bytes < R.total) return SKG_ERR_WORKSPACE;
   if (!tensor_map_encoder()) return SKG_ERR_CUDA;
 
   uint8_t* ws = (uint8_t*)workspace;
-  // MN-major operands: the GEMM runs on K-major copies in the workspace.
-  if (a_layout == SKG_A_COL) {
+  // MN-major operands: read directly by the MMAs without ABFT; with ABFT
+  // (whose encode pass and checksum tiles read K-major operands) the GEMM
+  // runs on K-major copies in the workspace.
+  if (copy_layout_a(a_layout, r) == SKG_A_COL) {
     if (launch_relayout(A, lda, m, k, ws + R.a, R.ldk, sms, stream) != cudaSuccess)
       return SKG_ERR_CUDA;
     A = ws + R.a;
     lda = R.ldk;
   }
-  if (b_layout == SKG_B_NMAJOR) {
+  if (copy_layout_b(b_layout, r) == SKG_B_NMAJOR) {
     if (launch_relayout(B, ldb, n, k, ws + R.b, R.ldk, sms, stream) != cudaSuccess)
       return SKG_ERR_CUDA;
     B = ws + R.b;
     ldb = R.ldk;
   }
-  const Gemm g{m, n, k, A, lda, B, ldb, C, ldc, alpha, beta, in_dtype, out_dtype};
+  Gemm g{m, n, k, A, lda, B, ldb, C, ldc, alpha, beta, in_dtype, out_dtype};
+  if (!r.abft) {
+    g.a_mn = a_layout == SKG_A_COL;
+    g.b_mn = b_layout == SKG_B_NMAJOR;
+  }
   bool fuse = false;
   if (r.abft && r.abft_local) {
     // The reference checksums are formed inside the CTAs: one launch.
@@ -658,9 +689,13 @@ size_t skg_workspace_size(int64_t m, int64_t n, int64_t k, const skg_opts_t* opt
 size_t skg_workspace_size_layout(int64_t m, int64_t n, int64_t k, int32_t a_layout,
                                  int32_t b_layout, const skg_opts_t* opts) {
   if (!layout_valid(a_layout, b_layout)) return 0;
-  const size_t base = skg_workspace_size(m, n, k, opts);
-  if (base == 0) return 0;
-  return relayout_plan(m, n, k, a_layout, b_layout, base).total;
+  if (m < 0 || n < 0 || k < 0) return 0;
+  Resolved r;
+  const int sms = sm_count_cached();
+  if (resolve(m, n, k, opts, r, sms) != SKG_OK) return 0;
+  return relayout_plan(m, n, k, copy_layout_a(a_layout, r), copy_layout_b(b_layout, r),
+                       layout(m, n, k, r).total)
+      .total;
 }
 
 skg_status_t skg_workspace_init(void* workspace, size_t bytes, void* stream) {

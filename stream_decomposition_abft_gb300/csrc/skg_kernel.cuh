@@ -60,6 +60,9 @@ namespace skg {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
+// MN-major operand box: 64 MN elements (one 128-byte swizzled row) x kBK.
+constexpr int kMnBox = 64;
+constexpr int kMnBoxBytes = kMnBox * kBK * 2;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 static_assert(kThreads == 64 + kEpiThreads && kEpiThreads == 128,
@@ -101,6 +104,11 @@ struct KernelParams {
   int m, n, k;
   float alpha, beta;
   uint32_t idesc_main;
+  // MN-major output-tile operands (launches without ABFT): A stored k x m
+  // and / or B stored k x n, loaded as 64 x 64-element boxes (64 MN
+  // elements = one 128-byte swizzled row per k) and read by the MMAs as
+  // MN-major shared-memory operands.
+  int32_t a_mn, b_mn;
   WsHeader* hdr;
   skg_report_t* report;
   // Fixup storage: region 0 (output tiles) uses flags[0, ws_ctas) and
@@ -1107,12 +1115,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             // leader expects the pair's bytes.
             const uint32_t fb = cluster_addr(&full_bar[stage], 0);
             if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * tx);
-            tma_load_2d_pair(st, mapA, fb, kb * kBK, rowA);
-            tma_load_2d_pair(st + C::A_BYTES, mapB, fb, kb * kBK, rowB);
+            if (!p.a_mn) {
+              tma_load_2d_pair(st, mapA, fb, kb * kBK, rowA);
+            } else {
+              for (int h = 0; h < kBM / kMnBox; ++h)
+                tma_load_2d_pair(st + h * kMnBoxBytes, mapA, fb, rowA + h * kMnBox, kb * kBK);
+            }
+            if (!p.b_mn) {
+              tma_load_2d_pair(st + C::A_BYTES, mapB, fb, kb * kBK, rowB);
+            } else {
+              for (int h = 0; h < C::B_ROWS / kMnBox; ++h)
+                tma_load_2d_pair(st + C::A_BYTES + h * kMnBoxBytes, mapB, fb, rowB + h * kMnBox,
+                                 kb * kBK);
+            }
           } else if (kpack == 1) {
             mbar_arrive_expect_tx(&full_bar[stage], tx);
-            tma_load_2d(st, mapA, &full_bar[stage], kb * kBK, rowA);
-            tma_load_2d(st + C::A_BYTES, mapB, &full_bar[stage], kb * kBK, rowB);
+            if (!p.a_mn) {
+              tma_load_2d(st, mapA, &full_bar[stage], kb * kBK, rowA);
+            } else {
+              for (int h = 0; h < kBM / kMnBox; ++h)
+                tma_load_2d(st + h * kMnBoxBytes, mapA, &full_bar[stage], rowA + h * kMnBox,
+                            kb * kBK);
+            }
+            if (!p.b_mn) {
+              tma_load_2d(st + C::A_BYTES, mapB, &full_bar[stage], kb * kBK, rowB);
+            } else {
+              for (int h = 0; h < C::B_ROWS / kMnBox; ++h)
+                tma_load_2d(st + C::A_BYTES + h * kMnBoxBytes, mapB, &full_bar[stage],
+                            rowB + h * kMnBox, kb * kBK);
+            }
           } else {  // packed checksum stage
             const int nk = min(2, w.kb_end - kb);
             mbar_arrive_expect_tx(&full_bar[stage], tx * nk);
@@ -1145,6 +1176,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the first 256 KB of shared memory, so adding (offset >> 4) to the
       // 14-bit address field never carries out of it.
       const uint64_t ring_desc = sdesc_sw128(smem_u32(ring));
+      // MN-major operands: leading byte offset = the distance between the
+      // 64-element MN boxes (the K-major descriptor carries 1 there), and a
+      // 16-k slice is two 8-row groups of 1024 bytes.
+      const uint64_t mn_lbo = (uint64_t)((kMnBoxBytes >> 4) - 1) << 16;
+      const uint64_t a_lbo = p.a_mn ? mn_lbo : 0, b_lbo = p.b_mn ? mn_lbo : 0;
+      const int a_step = p.a_mn ? (2048 >> 4) : 2, b_step = p.b_mn ? (2048 >> 4) : 2;
       Cursor cur;
       cur.init(s, unit);
       Work w;
@@ -1198,14 +1235,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            // Descriptors advance linearly with the (16-byte granular) address.
-            const uint64_t ad0 = ring_desc + (uint64_t)((stage * C::STAGE_BYTES) >> 4);
-            const uint64_t bd0 = ad0 + (uint64_t)(C::A_BYTES >> 4);
+            // Descriptors advance linearly with the (16-byte granular)
+            // address: by 32 bytes per 16-k slice inside a K-major 128-byte
+            // row, or by two 8-row k groups (2048 bytes) of an MN-major box.
+            const uint64_t ad0 = ring_desc + (uint64_t)((stage * C::STAGE_BYTES) >> 4) + a_lbo;
+            const uint64_t bd0 = ring_desc +
+                                 (uint64_t)((stage * C::STAGE_BYTES + C::A_BYTES) >> 4) + b_lbo;
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               const uint32_t acc = (kb > w.kb_begin || kk > 0) ? 1u : 0u;
-              if constexpr (C::PAIR) umma_f16_pair(d, ad0 + 2 * kk, bd0 + 2 * kk, idesc, acc);
-              else umma_f16(d, ad0 + 2 * kk, bd0 + 2 * kk, idesc, acc);
+              const uint64_t ad = ad0 + (uint64_t)(kk * a_step), bd = bd0 + (uint64_t)(kk * b_step);
+              if constexpr (C::PAIR) umma_f16_pair(d, ad, bd, idesc, acc);
+              else umma_f16(d, ad, bd, idesc, acc);
             }
             issued = true;
             if constexpr (C::PAIR) umma_commit_pair(&empty_bar[stage]);  // both CTAs' stage

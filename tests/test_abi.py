@@ -136,9 +136,14 @@ def test_workspace_size_scales_with_grid_not_problem(lib):
 
 
 def test_workspace_size_layout_adds_the_k_major_copies(lib):
-    # MN-major operands are copied K-major into the end of the workspace:
-    # m x k and n x k elements of 2 bytes, rows rounded up to 16 bytes.
-    o = skgemm.opts_default(grid=148, tile_n=128)
+    # With ABFT, MN-major operands are copied K-major into the end of the
+    # workspace: m x k and n x k elements of 2 bytes, rows rounded up to 16
+    # bytes. Without ABFT the MMAs read them in place: no extra bytes.
+    plain = skgemm.opts_default(grid=148, tile_n=128)
+    for al, bl in ((0, 0), (1, 0), (0, 1), (1, 1)):
+        assert skgemm.workspace_size_layout(1000, 700, 333, al, bl, plain) == \
+            skgemm.workspace_size(1000, 700, 333, plain)
+    o = skgemm.opts_default(grid=148, tile_n=128, abft=1)
     m, n, k = 1000, 700, 333
     base = skgemm.workspace_size(m, n, k, o)
     kr = (k + 7) // 8 * 8

@@ -577,6 +577,25 @@ def test_mn_major_layouts(layouts, shape, dtype):
         assert torch.equal(C, Ck)
 
 
+@pytest.mark.parametrize("layouts", [(1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("cfg", [dict(tile_n=128, sched="sk", grid=37), dict(tile_n=256),
+                                 dict(tile_n=256, cta_pair=2), dict(tile_n=256, cta_pair=2,
+                                                                    sched="sk2_dp")])
+def test_mn_major_tile_configs(layouts, cfg):
+    # MN-major operands read by the MMAs in every mainloop form: 128- and
+    # 256-column tiles, single CTAs and CTA pairs, Stream-K fixup; ragged m
+    # and n, a padded leading dimension.
+    a_layout, b_layout = layouts
+    m, n, k = 1000, 1304, 1032
+    p = inputs.make_problem(m, n, k, seed=7, in_dtype="bf16", out_dtype="bf16",
+                            law_a="normal", law_b="normal", alpha=1.25, beta=0.5,
+                            a_layout=a_layout, b_layout=b_layout)
+    o = skgemm.opts_default(**cfg)
+    C, ws, st = run(p, o, lda=_ld16(p.A) + 16, ldb=_ld16(p.B))
+    assert st == skgemm.OK
+    check_full(p, C)
+
+
 @pytest.mark.parametrize("layouts", [(1, 1), (1, 0)])
 def test_mn_major_layouts_abft(layouts):
     # ABFT on the copies: clean run, every tile checked, and the same bits as
