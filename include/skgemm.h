@@ -373,6 +373,30 @@ skg_status_t skg_gemm_noalloc(int64_t m, int64_t n, int64_t k, float alpha, cons
                               int64_t ldc, int32_t in_dtype, int32_t out_dtype, int32_t a_layout,
                               int32_t b_layout, const skg_opts_t* opts, void* stream);
 
+/* Bytes of device staging memory skg_gemm_host needs for this problem:
+ * packed device copies of A and B as stored (rows rounded up to 16 bytes)
+ * and of C (m rows of n outputs, rounded up to 16 bytes). 0 for invalid
+ * arguments. */
+size_t skg_host_staging_size(int64_t m, int64_t n, int64_t k, int32_t in_dtype,
+                             int32_t out_dtype, int32_t a_layout, int32_t b_layout);
+
+/* skg_gemm on operands in HOST memory, asynchronous on `stream`: copies A
+ * and B (and C when beta != 0) into `staging` (device memory, >=
+ * skg_host_staging_size bytes, caller-owned), runs skg_gemm (or
+ * skg_gemm_verify when opts->abft = 1) on the device copies, and copies C
+ * back to the host. A, B, C are host pointers with the meanings of
+ * skg_gemm (any alignment; leading dimensions in elements); page-locked
+ * host memory lets the copies run asynchronously and overlap with work on
+ * other streams. workspace as for skg_gemm with these layouts
+ * (skg_workspace_size_layout). Copies are one cudaMemcpy2DAsync per matrix.
+ * The host buffers must stay valid, and C unread, until `stream` has
+ * reached this point. */
+skg_status_t skg_gemm_host(int64_t m, int64_t n, int64_t k, float alpha, const void* A,
+                           int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+                           int64_t ldc, int32_t in_dtype, int32_t out_dtype, int32_t a_layout,
+                           int32_t b_layout, const skg_opts_t* opts, void* staging,
+                           size_t staging_bytes, void* workspace, size_t ws_bytes, void* stream);
+
 /* Number of SMs of the current device (0 if there is no device). */
 int32_t skg_device_sm_count(void);
 

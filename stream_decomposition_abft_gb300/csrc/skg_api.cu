@@ -585,6 +585,40 @@ bool layout_valid(int32_t a_layout, int32_t b_layout) {
          (b_layout == SKG_B_KMAJOR || b_layout == SKG_B_NMAJOR);
 }
 
+// Device staging of skg_gemm_host: packed copies of A and B as stored and
+// of C, each row rounded up to 16 bytes.
+struct Staging {
+  int64_t a_rows, a_cols, b_rows, b_cols;  // stored shapes (elements)
+  int64_t lda, ldb, ldc;                   // device leading dimensions
+  size_t a, b, c, total;                   // byte offsets, total size
+  int out_bytes;
+};
+
+bool staging_plan(int64_t m, int64_t n, int64_t k, int32_t in_dtype, int32_t out_dtype,
+                  int32_t a_layout, int32_t b_layout, Staging& S) {
+  if (m < 0 || n < 0 || k < 0) return false;
+  if (in_dtype != SKG_IN_F16 && in_dtype != SKG_IN_BF16) return false;
+  if (out_dtype < SKG_OUT_F32 || out_dtype > SKG_OUT_BF16) return false;
+  if (!layout_valid(a_layout, b_layout)) return false;
+  S.out_bytes = out_dtype == SKG_OUT_F32 ? 4 : 2;
+  S.a_rows = a_layout == SKG_A_ROW ? m : k;
+  S.a_cols = a_layout == SKG_A_ROW ? k : m;
+  S.b_rows = b_layout == SKG_B_KMAJOR ? n : k;
+  S.b_cols = b_layout == SKG_B_KMAJOR ? k : n;
+  S.lda = (int64_t)round_up((size_t)(S.a_cols > 0 ? S.a_cols : 1), 8);
+  S.ldb = (int64_t)round_up((size_t)(S.b_cols > 0 ? S.b_cols : 1), 8);
+  S.ldc = (int64_t)round_up((size_t)(n > 0 ? n : 1), (size_t)(16 / S.out_bytes));
+  size_t off = 0;
+  S.a = off;
+  off = round_up(off + (size_t)S.a_rows * S.lda * 2, 256);
+  S.b = off;
+  off = round_up(off + (size_t)S.b_rows * S.ldb * 2, 256);
+  S.c = off;
+  off = round_up(off + (size_t)m * S.ldc * S.out_bytes, 256);
+  S.total = off;
+  return true;
+}
+
 skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void* A, int64_t lda,
                        const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
                        int32_t in_dtype, int32_t out_dtype, int32_t a_layout, int32_t b_layout,
@@ -839,6 +873,48 @@ skg_status_t skg_report_read(const void* workspace, skg_report_t* out, int32_t r
       return SKG_ERR_CUDA;
   }
   return SKG_OK;
+}
+
+size_t skg_host_staging_size(int64_t m, int64_t n, int64_t k, int32_t in_dtype,
+                             int32_t out_dtype, int32_t a_layout, int32_t b_layout) {
+  Staging S;
+  return staging_plan(m, n, k, in_dtype, out_dtype, a_layout, b_layout, S) ? S.total : 0;
+}
+
+skg_status_t skg_gemm_host(int64_t m, int64_t n, int64_t k, float alpha, const void* A,
+                           int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+                           int64_t ldc, int32_t in_dtype, int32_t out_dtype, int32_t a_layout,
+                           int32_t b_layout, const skg_opts_t* opts, void* staging,
+                           size_t staging_bytes, void* workspace, size_t ws_bytes,
+                           void* stream_v) {
+  Staging S;
+  if (!staging_plan(m, n, k, in_dtype, out_dtype, a_layout, b_layout, S)) return SKG_ERR_ARG;
+  if (m == 0 || n == 0) return SKG_OK;
+  if (!C || ldc < n) return SKG_ERR_ARG;
+  if (k > 0 && (!A || !B || lda < S.a_cols || ldb < S.b_cols)) return SKG_ERR_ARG;
+  if (!staging || !aligned16(staging) || staging_bytes < S.total) return SKG_ERR_WORKSPACE;
+  cudaStream_t stream = (cudaStream_t)stream_v;
+  uint8_t* sb = (uint8_t*)staging;
+  const int ob = S.out_bytes;
+  if (k > 0) {
+    if (cudaMemcpy2DAsync(sb + S.a, (size_t)S.lda * 2, A, (size_t)lda * 2, (size_t)S.a_cols * 2,
+                          (size_t)S.a_rows, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpy2DAsync(sb + S.b, (size_t)S.ldb * 2, B, (size_t)ldb * 2, (size_t)S.b_cols * 2,
+                          (size_t)S.b_rows, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return SKG_ERR_CUDA;
+  }
+  if (beta != 0.f &&
+      cudaMemcpy2DAsync(sb + S.c, (size_t)S.ldc * ob, C, (size_t)ldc * ob, (size_t)n * ob,
+                        (size_t)m, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return SKG_ERR_CUDA;
+  const skg_status_t st = gemm_impl(m, n, k, alpha, sb + S.a, S.lda, sb + S.b, S.ldb, beta,
+                                    sb + S.c, S.ldc, in_dtype, out_dtype, a_layout, b_layout,
+                                    opts, 0, workspace, ws_bytes, stream);
+  if (st != SKG_OK) return st;
+  return cudaMemcpy2DAsync(C, (size_t)ldc * ob, sb + S.c, (size_t)S.ldc * ob, (size_t)n * ob,
+                           (size_t)m, cudaMemcpyDeviceToHost, stream) == cudaSuccess
+             ? SKG_OK
+             : SKG_ERR_CUDA;
 }
 
 int32_t skg_device_sm_count(void) { return sm_count_cached(); }

@@ -83,7 +83,8 @@ class Report(ctypes.Structure):
 SYMBOLS = ("skg_opts_default", "skg_workspace_size", "skg_workspace_init", "skg_gemm",
            "skg_gemm_verify", "skg_abft_encode", "skg_schedule_query", "skg_launch_shape", "skg_report_read",
            "skg_device_sm_count", "skg_status_string", "skg_gemm_noalloc", "skg_schedule_cost",
-           "skg_launch_plan", "skg_workspace_size_layout")
+           "skg_launch_plan", "skg_workspace_size_layout", "skg_host_staging_size",
+           "skg_gemm_host")
 
 _lib = None
 
@@ -117,6 +118,10 @@ def lib() -> ctypes.CDLL:
                  ctypes.POINTER(Opts), vp, sz, vp]
     L.skg_gemm.argtypes = gemm_args
     L.skg_gemm.restype = i32
+    L.skg_host_staging_size.argtypes = [i64, i64, i64, i32, i32, i32, i32]
+    L.skg_host_staging_size.restype = sz
+    L.skg_gemm_host.argtypes = gemm_args[:-3] + [vp, sz, vp, sz, vp]
+    L.skg_gemm_host.restype = i32
     L.skg_gemm_verify.argtypes = gemm_args
     L.skg_gemm_verify.restype = i32
     L.skg_abft_encode.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, ctypes.POINTER(Opts),
@@ -176,6 +181,21 @@ def gemm(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, in_dtype, out
     return int(lib().skg_gemm(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc,
                               in_dtype, out_dtype, a_layout, b_layout,
                               ctypes.byref(opts) if opts else None, ws_ptr, ws_bytes, stream))
+
+
+def host_staging_size(m, n, k, in_dtype, out_dtype, a_layout=A_ROW, b_layout=B_KMAJOR) -> int:
+    return int(lib().skg_host_staging_size(m, n, k, in_dtype, out_dtype, a_layout, b_layout))
+
+
+def gemm_host(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, in_dtype, out_dtype,
+              a_layout, b_layout, opts, staging_ptr, staging_bytes, ws_ptr, ws_bytes,
+              stream) -> int:
+    """skg_gemm_host: A, B, C are host addresses; staging and workspace are
+    device memory."""
+    return int(lib().skg_gemm_host(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc,
+                                   in_dtype, out_dtype, a_layout, b_layout,
+                                   ctypes.byref(opts) if opts else None, staging_ptr,
+                                   staging_bytes, ws_ptr, ws_bytes, stream))
 
 
 def gemm_verify(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, in_dtype, out_dtype,

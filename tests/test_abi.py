@@ -157,6 +157,32 @@ def test_workspace_size_layout_adds_the_k_major_copies(lib):
     assert skgemm.workspace_size_layout(m, n, k, 2, 0, o) == 0
 
 
+def test_host_staging_size_and_argument_errors(lib):
+    # Packed device copies of A and B as stored and of C, rows rounded up to
+    # 16 bytes, each region aligned to 256 bytes.
+    r256 = lambda x: (x + 255) // 256 * 256
+    m, n, k = 100, 60, 33
+    want = r256(m * 40 * 2) + r256(n * 40 * 2) + r256(m * 60 * 4)
+    assert skgemm.host_staging_size(m, n, k, skgemm.IN_BF16, skgemm.OUT_F32) == want
+    want_mn = r256(k * 104 * 2) + r256(k * 64 * 2) + r256(m * 64 * 2)
+    assert skgemm.host_staging_size(m, n, k, skgemm.IN_F16, skgemm.OUT_BF16, skgemm.A_COL,
+                                    skgemm.B_NMAJOR) == want_mn
+    assert skgemm.host_staging_size(m, n, k, 5, skgemm.OUT_F32) == 0
+    assert skgemm.host_staging_size(m, n, k, skgemm.IN_F16, skgemm.OUT_F32, 3, 0) == 0
+    # Argument errors come back before any copy is issued.
+    o = skgemm.opts_default()
+    call = lambda **kw: skgemm.gemm_host(
+        kw.get("m", m), n, k, 1.0, kw.get("A", 64), kw.get("lda", k), 64, k, 0.0, 64,
+        kw.get("ldc", n), skgemm.IN_BF16, skgemm.OUT_F32, 0, 0, o, kw.get("staging", None),
+        kw.get("staging_bytes", 0), None, 0, None)
+    assert call(m=-1) == skgemm.ERR_ARG
+    assert call(lda=k - 1) == skgemm.ERR_ARG
+    assert call(ldc=n - 1) == skgemm.ERR_ARG
+    assert call(A=None) == skgemm.ERR_ARG
+    assert call() == skgemm.ERR_WORKSPACE           # no staging buffer
+    assert call(staging=16, staging_bytes=want - 1) == skgemm.ERR_WORKSPACE
+
+
 # ----------------------------------------------------------------------------
 # Grid-size model (Stream-K page, App. A.1)
 # ----------------------------------------------------------------------------

@@ -641,6 +641,43 @@ def test_mn_major_noalloc_and_matmul():
     assert st == skgemm.ERR_ARG
 
 
+# --------------------------------------------------------------------------- host buffers
+@pytest.mark.parametrize("layouts", [(0, 0), (1, 1)])
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("abft", [0, 1])
+def test_gemm_host_buffers(layouts, pinned, abft):
+    # skg_gemm_host: operands and C in host memory (page-locked or not),
+    # copied through the caller's device staging; the same bits as the
+    # device-pointer call, and with ABFT a clean report.
+    a_layout, b_layout = layouts
+    m, n, k = 1000, 1304, 520
+    p = inputs.make_problem(m, n, k, seed=31, in_dtype="bf16", out_dtype="f32",
+                            law_a="normal", law_b="normal", alpha=0.5, beta=1.5,
+                            a_layout=a_layout, b_layout=b_layout)
+    hA, hB, hC = p.A.contiguous(), p.B.contiguous(), p.C0.clone()
+    if pinned:
+        hA, hB, hC = hA.pin_memory(), hB.pin_memory(), hC.pin_memory()
+    o = skgemm.opts_default(abft=abft)
+    staging = torch.empty(skgemm.host_staging_size(m, n, k, skgemm.IN_BF16, skgemm.OUT_F32,
+                                                   a_layout, b_layout),
+                          dtype=torch.uint8, device="cuda")
+    ws = skgemm.Workspace(skgemm.workspace_size_layout(m, n, k, a_layout, b_layout, o), "cuda")
+    st = skgemm.gemm_host(m, n, k, p.alpha, hA.data_ptr(), hA.stride(0), hB.data_ptr(),
+                          hB.stride(0), p.beta, hC.data_ptr(), hC.stride(0), skgemm.IN_BF16,
+                          skgemm.OUT_F32, a_layout, b_layout, o, staging.data_ptr(),
+                          staging.numel(), ws.ptr, ws.nbytes,
+                          torch.cuda.current_stream().cuda_stream)
+    assert st == skgemm.OK
+    torch.cuda.synchronize()
+    check_full(p, hC)
+    if abft:
+        rep = ws.report()
+        assert rep.detected == 0 and rep.status_bits == 0 and rep.tiles_checked > 0
+    Cd, _, std = run(p, o)
+    assert std == skgemm.OK
+    assert torch.equal(hC, Cd.cpu())
+
+
 # --------------------------------------------------------------------------- single-launch ABFT
 @pytest.mark.parametrize("shape", [(1024, 1024, 1024), (384, 640, 320), (300, 1000, 520)])
 def test_abft_encode_in_kernel(shape):
