@@ -65,12 +65,13 @@ typedef enum { SKG_A_ROW = 0, SKG_A_COL = 1 } skg_a_layout_t;
  *                 "NT" form, as for a weight matrix of a linear layer);
  *   SKG_B_NMAJOR  stored k x n, element (l,j) at B[l*ldb + j], ldb >= n (the
  *                 plain row-major "NN" form).
- * Without ABFT the MMAs read an MN-major operand directly (TMA boxes of 64
- * MN elements x 64 k, MN-major shared-memory operand descriptors). With
- * ABFT (whose encode pass and checksum GEMMs read K-major operands) such an
- * operand is first copied into a K-major buffer at the end of the workspace
- * by a data-movement kernel (one extra read and write of that operand, bound
- * by HBM bandwidth) and the call runs on the copy; size the workspace with
+ * The MMAs read an MN-major operand in place (TMA boxes of 64 MN elements x
+ * 64 k, MN-major shared-memory operand descriptors), in the output tiles and
+ * in the ABFT checksum GEMMs, and the ABFT encode pass sums its stored rows
+ * directly. Only the in-CTA ABFT references (skg_opts_t.abft_local = 2),
+ * whose epilogue warps read the stages as K-major rows, run on a K-major
+ * copy that a data-movement kernel writes at the end of the workspace (one
+ * extra read and write of that operand); size the workspace with
  * skg_workspace_size_layout. */
 typedef enum { SKG_B_KMAJOR = 0, SKG_B_NMAJOR = 1 } skg_b_layout_t;
 
@@ -238,10 +239,11 @@ void skg_opts_default(skg_opts_t* opts);
  * checksums, and with ABFT the split encodings e^T A and B e. */
 size_t skg_workspace_size(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts);
 
-/* skg_workspace_size for the given operand layouts: with ABFT on in opts,
- * the same bytes plus room for the K-major copies of MN-major operands
- * (m x k and n x k elements, rows rounded up to 16 bytes); otherwise equal
- * to skg_workspace_size. 0 for an unknown layout or invalid arguments. */
+/* skg_workspace_size for the given operand layouts: when opts select the
+ * in-CTA ABFT references, the same bytes plus room for the K-major copies of
+ * MN-major operands (m x k and n x k elements, rows rounded up to 16 bytes);
+ * otherwise equal to skg_workspace_size. 0 for an unknown layout or invalid
+ * arguments. */
 size_t skg_workspace_size_layout(int64_t m, int64_t n, int64_t k, int32_t a_layout,
                                  int32_t b_layout, const skg_opts_t* opts);
 
@@ -290,9 +292,10 @@ skg_status_t skg_gemm_verify(int64_t m, int64_t n, int64_t k, float alpha, const
  * threadblock-level ABFT, Fig. 5: the encodings e^T A and B e of each
  * threadblock's operands). Arguments as for skg_gemm with K-major operands
  * (A row-major, B stored n x k; the encodings do not depend on the layout,
- * so they also serve a following call with MN-major operands); opts must
- * be the options of the gemm call that follows with opts->abft_preencoded
- * = 1. Asynchronous on `stream`. */
+ * so the encodings of K-major copies of MN-major operands also serve a
+ * call on the MN-major originals); opts must be the options of the gemm
+ * call that follows with opts->abft_preencoded = 1. Asynchronous on
+ * `stream`. */
 skg_status_t skg_abft_encode(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
                              const void* B, int64_t ldb, int32_t in_dtype,
                              const skg_opts_t* opts, void* workspace, size_t ws_bytes,

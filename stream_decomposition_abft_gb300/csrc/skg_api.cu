@@ -267,6 +267,53 @@ skg_status_t run_encode(int32_t in_dtype, const void* A, int64_t lda, int64_t m,
              : SKG_ERR_CUDA;
 }
 
+// The encode pass for any operand layouts: one launch when both operands
+// are K-major; otherwise each operand on its own, an MN-major one with the
+// row-segment kernels and a K-major one with the pass above restricted to
+// its tiles (the per-tile arrays offset past A's tiles for B).
+skg_status_t run_encode_layouts(int32_t in_dtype, const void* A, int64_t lda, int a_mn, int64_t m,
+                                const void* B, int64_t ldb, int b_mn, int64_t n, int64_t k,
+                                const Resolved& r, uint8_t* ws, const Layout& L, int sms,
+                                cudaStream_t stream) {
+  if (!a_mn && !b_mn) return run_encode(in_dtype, A, lda, m, B, ldb, n, k, r, ws, L, sms, stream);
+  const int bf16 = in_dtype == SKG_IN_BF16;
+  const int slices = encode_slices(L.kp);
+  float* sums = (float*)(ws + L.sums);
+  float* umax = (float*)(ws + L.umax);
+  TilePub* pub = (TilePub*)(ws + L.pub);
+  TileStat* stat = (TileStat*)(ws + L.stat);
+  const CUtensorMapDataType in_t = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cudaError_t e;
+  if (a_mn) {
+    e = launch_encode_mn(bf16, A, lda, m, k, kBM, L.tiles_a, L.kp, sums, umax, ws + L.enc_a, pub,
+                         sms, stream);
+  } else {
+    CUtensorMap ma;
+    if (make_map(&ma, in_t, 2, A, (uint64_t)k, (uint64_t)m, (uint64_t)lda, kEncBoxCols,
+                 kEncBoxRows, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return SKG_ERR_UNSUPPORTED;
+    e = launch_encode(bf16, ma, ma, (int)m, 0, L.kp, r.bn, sms, sums, ws + L.enc_a, ws + L.enc_b,
+                      stat, pub, umax, (skg_report_t*)(ws + 256), r.timeout_ns, stream);
+  }
+  if (e != cudaSuccess) return SKG_ERR_CUDA;
+  const int ta = L.tiles_a;
+  if (b_mn) {
+    e = launch_encode_mn(bf16, B, ldb, n, k, r.bn, L.tiles_b, L.kp, sums + (size_t)ta * L.kp,
+                         umax + (size_t)ta * slices, ws + L.enc_b, pub + ta, sms, stream);
+  } else {
+    CUtensorMap mb;
+    if (make_map(&mb, in_t, 2, B, (uint64_t)k, (uint64_t)n, (uint64_t)ldb, kEncBoxCols,
+                 kEncBoxRows, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return SKG_ERR_UNSUPPORTED;
+    e = launch_encode(bf16, mb, mb, 0, (int)n, L.kp, r.bn, sms, sums + (size_t)ta * L.kp,
+                      ws + L.enc_a, ws + L.enc_b, stat + ta, pub + ta,
+                      umax + (size_t)ta * slices, (skg_report_t*)(ws + 256), r.timeout_ns,
+                      stream);
+  }
+  return e == cudaSuccess ? SKG_OK : SKG_ERR_CUDA;
+}
+
 // One launch of the persistent kernel: C = alpha A B^T + beta C with A
 // (m x k, row stride lda) and B (n x k, row stride ldb) in `in_dtype`.
 struct Gemm {
@@ -336,8 +383,12 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   const int ck_round = r.pair ? 32 : 16;
   if (fuse_ck) {
     const int n_cr = kEncRows * L.tiles_b, n_cc = kEncRows * L.tiles_a;
-    if (make_map(&mp.b128, in_t, 2, g.B, (uint64_t)g.k, (uint64_t)g.n, (uint64_t)g.ldb, kBK,
-                 kBM) != CUDA_SUCCESS ||
+    const CUresult rb128 =
+        g.b_mn ? make_map(&mp.b128, in_t, 2, g.B, (uint64_t)g.n, (uint64_t)g.k,
+                          (uint64_t)g.ldb, kMnBox, kBK)
+               : make_map(&mp.b128, in_t, 2, g.B, (uint64_t)g.k, (uint64_t)g.n,
+                          (uint64_t)g.ldb, kBK, kBM);
+    if (rb128 != CUDA_SUCCESS ||
         make_map(&mp.be, in_t, 2, ws + L.enc_b, (uint64_t)L.kp, (uint64_t)n_cr, (uint64_t)L.kp,
                  kBK, (uint32_t)(round_up(n_cr, ck_round) / ck_half)) != CUDA_SUCCESS ||
         make_map(&mp.ea, in_t, 2, ws + L.enc_a, (uint64_t)L.kp, (uint64_t)n_cc, (uint64_t)L.kp,
@@ -386,8 +437,11 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   // 8 KB slot (64 rows of 128 bytes) and the stage holds two A tiles.
   p.ck_kpack_cr = (!r.pair && r.bn == 256 && p.ck_rows_cr <= 64) ? 2 : 1;
   p.ck_kpack_cc = (!r.pair && r.bn == 256 && p.ck_rows_cc <= 64) ? 2 : 1;
-  p.idesc_cr = idesc_f16(g.in_dtype == SKG_IN_BF16, ck_half * kBM, (uint32_t)p.ck_rows_cr);
-  p.idesc_cc = idesc_f16(g.in_dtype == SKG_IN_BF16, ck_half * kBM, (uint32_t)p.ck_rows_cc);
+  // The checksum tiles' A operand is A (cr) or B (cc), MN-major as stored.
+  p.idesc_cr = idesc_f16(g.in_dtype == SKG_IN_BF16, ck_half * kBM, (uint32_t)p.ck_rows_cr) |
+               ((uint32_t)(g.a_mn != 0) << 15);
+  p.idesc_cc = idesc_f16(g.in_dtype == SKG_IN_BF16, ck_half * kBM, (uint32_t)p.ck_rows_cc) |
+               ((uint32_t)(g.b_mn != 0) << 15);
   p.hdr = (WsHeader*)ws;
   p.report = (skg_report_t*)(ws + 256);
   p.flags = (uint32_t*)(ws + L.flags);
@@ -456,8 +510,9 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
 skg_status_t reference_checksums(const Gemm& g, const Resolved& r, uint8_t* ws, const Layout& L,
                                  cudaStream_t stream, bool skip_encode) {
   if (!skip_encode) {
-    const skg_status_t st = run_encode(g.in_dtype, g.A, g.lda, g.m, g.B, g.ldb, g.n, g.k, r, ws,
-                                       L, sm_count_cached(), stream);
+    const skg_status_t st =
+        run_encode_layouts(g.in_dtype, g.A, g.lda, g.a_mn, g.m, g.B, g.ldb, g.b_mn, g.n, g.k, r,
+                           ws, L, sm_count_cached(), stream);
     if (st != SKG_OK) return st;
   }
   Resolved rc = r;
@@ -468,16 +523,18 @@ skg_status_t reference_checksums(const Gemm& g, const Resolved& r, uint8_t* ws, 
   rc.cta_clock = nullptr;
   rc.drop_signal = -1;
   rc.raster_band = 0;
-  const Gemm g1{g.m, (int64_t)kEncRows * L.tiles_b, g.k, g.A, g.lda, ws + L.enc_b, L.kp,
-                ws + L.cr, L.ld_cr, 1.f, 0.f, g.in_dtype, SKG_OUT_F32};
+  Gemm g1{g.m, (int64_t)kEncRows * L.tiles_b, g.k, g.A, g.lda, ws + L.enc_b, L.kp,
+          ws + L.cr, L.ld_cr, 1.f, 0.f, g.in_dtype, SKG_OUT_F32};
+  g1.a_mn = g.a_mn;  // the encodings (B operand) are K-major
   Plan pl = choose_plan(g1.m, g1.n, g1.k, 0, -1, 0, r.ws_grid);
   rc.bn = pl.bn;
   rc.sched = pl.sched;
   rc.grid = pl.grid;
   skg_status_t st = launch_one(g1, rc, false, false, ws, L, stream);
   if (st != SKG_OK) return st;
-  const Gemm g2{g.n, (int64_t)kEncRows * L.tiles_a, g.k, g.B, g.ldb, ws + L.enc_a, L.kp,
-                ws + L.cc, L.ld_cc, 1.f, 0.f, g.in_dtype, SKG_OUT_F32};
+  Gemm g2{g.n, (int64_t)kEncRows * L.tiles_a, g.k, g.B, g.ldb, ws + L.enc_a, L.kp,
+          ws + L.cc, L.ld_cc, 1.f, 0.f, g.in_dtype, SKG_OUT_F32};
+  g2.a_mn = g.b_mn;  // B as the A operand
   pl = choose_plan(g2.m, g2.n, g2.k, 0, -1, 0, r.ws_grid);
   rc.bn = pl.bn;
   rc.sched = pl.sched;
@@ -521,16 +578,34 @@ void replan_fused(int64_t m, int64_t n, const skg_opts_t* opts, Resolved& r) {
 // side tiles, then their placement. Checksum tiles on dedicated CTAs leave
 // SMs idle while the output tiles run, so those CTAs take every idle SM and
 // the encode pass too (bf16 encodings need no per-tile scale).
-void plan_fused(int64_t m, int64_t n, const skg_opts_t* opts, int32_t in_dtype, Resolved& r) {
+void plan_fused(int64_t m, int64_t n, const skg_opts_t* opts, int32_t in_dtype, bool k_major,
+                Resolved& r) {
   replan_fused(m, n, opts, r);
   // Only with plenty of idle SMs (at least four per checksum tile): the
   // side CTAs' encode-then-checksum chain must end with the output tiles.
-  r.enc_inkernel = (!r.preencoded && r.grid_ck > 0 && !r.pair && in_dtype == SKG_IN_BF16 &&
+  r.enc_inkernel = (k_major && !r.preencoded && r.grid_ck > 0 && !r.pair &&
+                    in_dtype == SKG_IN_BF16 &&
                     r.grid_max - r.grid >= 4 * r.grid_ck && kEncBoxCols == kEncInCols &&
                     kEncBoxRows == kEncInRows)
                        ? 1
                        : 0;
   if (r.enc_inkernel) r.grid_ck = r.grid_max - r.grid;
+}
+
+// Whether an ABFT call runs on K-major copies of its MN-major operands.
+// Everything else reads them in place; two paths read K-major stages only:
+// the in-CTA references (epilogue warps read the stages as K-major rows) and
+// the in-kernel encode pass of dedicated side CTAs. Where the plan would use
+// the latter (small bf16 shapes with many idle SMs), two short copies and
+// one launch beat the separate MN-major encode launches.
+bool abft_wants_copies(int64_t m, int64_t n, const skg_opts_t* opts, int32_t in_dtype,
+                       const Resolved& r, const Layout& L) {
+  if (!r.abft) return false;
+  if (r.abft_local) return true;
+  if (!can_fuse_checksums(L, r.bn)) return false;
+  Resolved probe = r;
+  plan_fused(m, n, opts, in_dtype, true, probe);
+  return probe.enc_inkernel != 0;
 }
 
 skg_status_t check_inputs(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
@@ -571,13 +646,11 @@ Relayout relayout_plan(int64_t m, int64_t n, int64_t k, int32_t a_layout, int32_
   return R;
 }
 
-// The layout whose operand gets a K-major copy: MN-major operands of ABFT
-// calls (the MMAs of plain calls read MN-major operands directly).
-int32_t copy_layout_a(int32_t a_layout, const Resolved& r) {
-  return r.abft ? a_layout : SKG_A_ROW;
-}
-int32_t copy_layout_b(int32_t b_layout, const Resolved& r) {
-  return r.abft ? b_layout : SKG_B_KMAJOR;
+// The layout whose operand gets a K-major copy (`copies`, below): the
+// MN-major ones, or none.
+int32_t copy_layout_a(int32_t a_layout, bool copies) { return copies ? a_layout : SKG_A_ROW; }
+int32_t copy_layout_b(int32_t b_layout, bool copies) {
+  return copies ? b_layout : SKG_B_KMAJOR;
 }
 
 bool layout_valid(int32_t a_layout, int32_t b_layout) {
@@ -656,32 +729,32 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
   st = resolve(m, n, k, opts, r, sms);
   if (st != SKG_OK) return st;
   const Layout L = layout(m, n, k, r);
-  const Relayout R = relayout_plan(m, n, k, copy_layout_a(a_layout, r),
-                                   copy_layout_b(b_layout, r), L.total);
+  const bool copies = (a_layout == SKG_A_COL || b_layout == SKG_B_NMAJOR) &&
+                      abft_wants_copies(m, n, opts, in_dtype, r, L);
+  const Relayout R = relayout_plan(m, n, k, copy_layout_a(a_layout, copies),
+                                   copy_layout_b(b_layout, copies), L.total);
   if (!workspace || !aligned16(workspace) || ws_bytes < R.total) return SKG_ERR_WORKSPACE;
   if (!tensor_map_encoder()) return SKG_ERR_CUDA;
 
   uint8_t* ws = (uint8_t*)workspace;
-  // MN-major operands: read directly by the MMAs without ABFT; with ABFT
-  // (whose encode pass and checksum tiles read K-major operands) the GEMM
-  // runs on K-major copies in the workspace.
-  if (copy_layout_a(a_layout, r) == SKG_A_COL) {
+  // MN-major operands are read in place (output and checksum tiles, encode
+  // pass) unless abft_wants_copies: then the call runs on K-major copies in
+  // the workspace.
+  if (copy_layout_a(a_layout, copies) == SKG_A_COL) {
     if (launch_relayout(A, lda, m, k, ws + R.a, R.ldk, sms, stream) != cudaSuccess)
       return SKG_ERR_CUDA;
     A = ws + R.a;
     lda = R.ldk;
   }
-  if (copy_layout_b(b_layout, r) == SKG_B_NMAJOR) {
+  if (copy_layout_b(b_layout, copies) == SKG_B_NMAJOR) {
     if (launch_relayout(B, ldb, n, k, ws + R.b, R.ldk, sms, stream) != cudaSuccess)
       return SKG_ERR_CUDA;
     B = ws + R.b;
     ldb = R.ldk;
   }
   Gemm g{m, n, k, A, lda, B, ldb, C, ldc, alpha, beta, in_dtype, out_dtype};
-  if (!r.abft) {
-    g.a_mn = a_layout == SKG_A_COL;
-    g.b_mn = b_layout == SKG_B_NMAJOR;
-  }
+  g.a_mn = !copies && a_layout == SKG_A_COL;
+  g.b_mn = !copies && b_layout == SKG_B_NMAJOR;
   bool fuse = false;
   if (r.abft && r.abft_local) {
     // The reference checksums are formed inside the CTAs: one launch.
@@ -689,9 +762,10 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
     // The checksum-GEMM tiles run ahead of the output tiles in the same
     // launch, after the encode pass (skipped when pre-encoded).
     fuse = true;
-    plan_fused(m, n, opts, in_dtype, r);
+    plan_fused(m, n, opts, in_dtype, !g.a_mn && !g.b_mn, r);
     if (!r.enc_inkernel && !r.preencoded) {
-      st = run_encode(in_dtype, A, lda, m, B, ldb, n, k, r, ws, L, sms, stream);
+      st = run_encode_layouts(in_dtype, A, lda, g.a_mn, m, B, ldb, g.b_mn, n, k, r, ws, L, sms,
+                              stream);
       if (st != SKG_OK) return st;
     }
   } else if (r.abft) {
@@ -727,8 +801,13 @@ size_t skg_workspace_size_layout(int64_t m, int64_t n, int64_t k, int32_t a_layo
   Resolved r;
   const int sms = sm_count_cached();
   if (resolve(m, n, k, opts, r, sms) != SKG_OK) return 0;
-  return relayout_plan(m, n, k, copy_layout_a(a_layout, r), copy_layout_b(b_layout, r),
-                       layout(m, n, k, r).total)
+  const Layout L = layout(m, n, k, r);
+  // The copies are planned for bf16, the input type for which they can be
+  // chosen (abft_wants_copies), so the size covers either type.
+  const bool copies = (a_layout == SKG_A_COL || b_layout == SKG_B_NMAJOR) &&
+                      abft_wants_copies(m, n, opts, SKG_IN_BF16, r, L);
+  return relayout_plan(m, n, k, copy_layout_a(a_layout, copies),
+                       copy_layout_b(b_layout, copies), L.total)
       .total;
 }
 
@@ -829,7 +908,7 @@ skg_status_t skg_launch_shape(int64_t m, int64_t n, int64_t k, const skg_opts_t*
   skg_status_t st = resolve(m, n, k, opts, r, sms);
   if (st != SKG_OK) return st;
   if (r.abft && m > 0 && n > 0 && k > 0 && can_fuse_checksums(layout(m, n, k, r), r.bn))
-    plan_fused(m, n, opts, SKG_IN_BF16, r);
+    plan_fused(m, n, opts, SKG_IN_BF16, true, r);
   if (tile_n) *tile_n = r.bn;
   if (grid) *grid = r.grid + r.grid_ck;
   if (sched) *sched = r.sched;
@@ -845,7 +924,7 @@ skg_status_t skg_launch_plan(int64_t m, int64_t n, int64_t k, const skg_opts_t* 
   if (st != SKG_OK) return st;
   const bool fused = r.abft && !r.abft_local && m > 0 && n > 0 && k > 0 &&
                      can_fuse_checksums(layout(m, n, k, r), r.bn);
-  if (fused) plan_fused(m, n, opts, SKG_IN_BF16, r);
+  if (fused) plan_fused(m, n, opts, SKG_IN_BF16, true, r);
   memset(out, 0, sizeof(*out));
   out->tile_m = r.pair ? 2 * kBM : kBM;
   out->tile_n = r.bn;

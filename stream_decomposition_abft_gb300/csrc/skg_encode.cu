@@ -442,6 +442,167 @@ cudaError_t launch_encode(int in_bf16, const CUtensorMap& tmA, const CUtensorMap
                  : launch_encode_t<__half>(tmA, tmB, p, grid, stream);
 }
 
+// ----------------------------------------------------------------------------
+// Encodings of an MN-major operand (A stored k x m, or B stored k x n). The
+// tile's encoding at k is the sum of the tile's tw consecutive elements of
+// stored row k -- the same e^T A / B e as above, here a contiguous row
+// segment. Pass 1: one block per unit (tile, kEncSliceCols rows of k); a
+// row segment is read by tw / 8 lanes with one 16-byte load each (four rows
+// in flight per lane) and summed with shuffles; bf16 writes its hi / lo
+// terms at once (scale 2^0), fp16 stores the fp32 sum; the block's max
+// |element| goes to the unit's umax. Pass 2 (fp16 only): one block per tile
+// picks the tile's scale from its largest |sum| and writes the hi / lo rows
+// as the K-major pass does.
+constexpr int kMnEncThreads = 256;
+constexpr int kMnEncUnroll = 4;
+
+template <typename T>
+__global__ void __launch_bounds__(kMnEncThreads)
+    encode_mn_kernel(const T* __restrict__ src, int64_t ld, int64_t rows, int64_t k, int tw,
+                     int tiles, int slices, int kp, float* __restrict__ sums,
+                     float* __restrict__ umax, T* __restrict__ enc, TilePub* __restrict__ pub) {
+  // bf16 needs no per-tile scale: its hi / lo terms are written here and the
+  // finishing pass is skipped; fp16 stores the fp32 sums for that pass.
+  constexpr bool kScaled = std::is_same<T, __half>::value;
+  using T2 = typename Pair<T>::type;
+  __shared__ float wmax[kMnEncThreads / 32];
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lanes_per_row = tw / 8;             // 16 (tw = 128) or 32 (tw = 256)
+  const int rows_per_pass = 32 / lanes_per_row;  // rows of k one warp covers at once
+  const int sub = lane / lanes_per_row, cl = lane % lanes_per_row;
+  const int stride = (kMnEncThreads / 32) * rows_per_pass;  // rows between a lane's rows
+  const int64_t units = (int64_t)tiles * slices;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int t = (int)(u / slices), sl = (int)(u % slices);
+    const int64_t c = (int64_t)t * tw + 8 * cl;  // this lane's first element of the segment
+    T2 amax2 = zero2<T2>();
+    for (int i0 = warp * rows_per_pass + sub; i0 < kEncSliceCols; i0 += kMnEncUnroll * stride) {
+      uint4 q[kMnEncUnroll];
+#pragma unroll
+      for (int j = 0; j < kMnEncUnroll; ++j) {
+        const int64_t l = (int64_t)sl * kEncSliceCols + i0 + j * stride;
+        q[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (l < k && c < rows) {
+          const T* ptr = src + l * ld + c;
+          if (c + 8 <= rows) {
+            q[j] = *reinterpret_cast<const uint4*>(ptr);
+          } else {
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(ptr);
+            for (int e = 0; c + e < rows; ++e) w[e >> 1] |= (uint32_t)h[e] << (16 * (e & 1));
+            q[j] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kMnEncUnroll; ++j) {
+        const uint32_t w4[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+        float x = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const T2 pr = as_pair<T2>(w4[e]);
+          x += to_f<T>(lo_of(pr)) + to_f<T>(hi_of(pr));
+          amax2 = pair_max(amax2, as_pair<T2>(w4[e] & 0x7fff7fffu));
+        }
+        for (int off = lanes_per_row / 2; off >= 1; off >>= 1)
+          x += __shfl_xor_sync(0xffffffffu, x, off);
+        const int l = sl * kEncSliceCols + i0 + j * stride;
+        if (cl == 0 && l < kp) {  // rows in [k, kp) sum to zero
+          if constexpr (kScaled) {
+            sums[(int64_t)t * kp + l] = x;
+          } else {
+            T* hi_row = enc + (int64_t)(kEncRows * t) * kp;
+            const T hi = from_f<T>(x);
+            hi_row[l] = hi;
+            hi_row[kp + l] = from_f<T>(x - to_f<T>(hi));
+          }
+        }
+      }
+    }
+    if (!kScaled && sl == 0 && threadIdx.x == 0) pub[t].scale_exp = 0;
+    float amax = fmaxf(to_f<T>(lo_of(amax2)), to_f<T>(hi_of(amax2)));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) wmax[warp] = amax;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float mx = wmax[0];
+      for (int w = 1; w < kMnEncThreads / 32; ++w) mx = fmaxf(mx, wmax[w]);
+      umax[u] = mx;
+    }
+    __syncthreads();  // wmax is rewritten by the next unit
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kMnEncThreads)
+    encode_finish_kernel(const float* __restrict__ sums, int tiles, int kp, T* __restrict__ enc,
+                         TilePub* __restrict__ pub) {
+  constexpr bool kScaled = std::is_same<T, __half>::value;
+  __shared__ float wmax[kMnEncThreads / 32];
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+    const float* ts = sums + (int64_t)t * kp;
+    int e = 0;
+    if constexpr (kScaled) {
+      float mx = 0.f;
+      for (int c = threadIdx.x; c < kp; c += kMnEncThreads) mx = fmaxf(mx, fabsf(ts[c]));
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      if (lane == 0) wmax[warp] = mx;
+      __syncthreads();
+      float emax = wmax[0];
+      for (int w = 1; w < kMnEncThreads / 32; ++w) emax = fmaxf(emax, wmax[w]);
+      int ex = 0;
+      if (emax > 0.f) frexpf(emax, &ex);
+      e = (emax > 0.f) ? 15 - ex : 0;  // emax * 2^e in [2^14, 2^15)
+    }
+    T* hi_row = enc + (int64_t)(kEncRows * t) * kp;
+    T* lo_row = hi_row + kp;
+    for (int c = threadIdx.x * kEncColsPerThread; c < kp; c += kMnEncThreads * kEncColsPerThread) {
+      float x[kEncColsPerThread];
+#pragma unroll
+      for (int j = 0; j < kEncColsPerThread; ++j) x[j] = ts[c + j];
+      split_store<T>(hi_row, lo_row, c, x, e);
+    }
+    if (threadIdx.x == 0) pub[t].scale_exp = e;
+    __syncthreads();  // wmax is rewritten by the next tile
+  }
+}
+
+template <typename T>
+cudaError_t launch_encode_mn_t(const void* src, int64_t ld, int64_t rows, int64_t k, int tw,
+                               int tiles, int kp, float* sums, float* umax, void* enc,
+                               TilePub* pub, int sms, cudaStream_t stream) {
+  const int slices = encode_slices(kp);
+  const int64_t units = (int64_t)tiles * slices;
+  const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 8;
+  const int grid1 = (int)(units < cap ? units : cap);
+  const int grid2 = tiles < 4 * (sms > 0 ? sms : 1) ? tiles : 4 * sms;
+  if (grid1 <= 0 || grid2 <= 0) return cudaSuccess;
+  cudaError_t e = launch_pdl(encode_mn_kernel<T>, dim3(grid1), dim3(kMnEncThreads), 0, stream,
+                             static_cast<const T*>(src), ld, rows, k, tw, tiles, slices, kp, sums,
+                             umax, static_cast<T*>(enc), pub);
+  if (e != cudaSuccess || !std::is_same<T, __half>::value) return e;
+  return launch_pdl(encode_finish_kernel<T>, dim3(grid2), dim3(kMnEncThreads), 0, stream,
+                    static_cast<const float*>(sums), tiles, kp, static_cast<T*>(enc), pub);
+}
+
+cudaError_t launch_encode_mn(int in_bf16, const void* src, int64_t ld, int64_t rows, int64_t k,
+                             int tw, int tiles, int kp, float* sums, float* umax, void* enc,
+                             TilePub* pub, int sms, cudaStream_t stream) {
+  return in_bf16 ? launch_encode_mn_t<__nv_bfloat16>(src, ld, rows, k, tw, tiles, kp, sums, umax,
+                                                     enc, pub, sms, stream)
+                 : launch_encode_mn_t<__half>(src, ld, rows, k, tw, tiles, kp, sums, umax, enc,
+                                              pub, sms, stream);
+}
+
 // C = beta * C (beta == 0 writes zeros without reading C).
 template <typename T>
 __global__ void scale_kernel(T* C, int64_t ldc, int m, int n, float beta) {

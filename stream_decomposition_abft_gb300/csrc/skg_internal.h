@@ -91,6 +91,16 @@ constexpr int kEncBoxRows = SKG_ENC_BOX_ROWS;
 // kEncBoxCols-column slices of the encode pass.
 int encode_slices(int kp);
 
+// Encode pass of one MN-major operand (skg_encode.cu): `src` stored k x rows
+// (row stride ld), tiles of tw consecutive stored columns (128 for A, BLK_N
+// for B). Writes the fp32 sums (tiles x kp) to `sums`, the max |element| of
+// every (tile, slice) unit to `umax`, the hi / lo rows (2 tiles x kp) to
+// `enc` and the per-tile scales to `pub`, as launch_encode does for those
+// tiles. Two kernels, programmatic stream serialization.
+cudaError_t launch_encode_mn(int in_bf16, const void* src, int64_t ld, int64_t rows, int64_t k,
+                             int tw, int tiles, int kp, float* sums, float* umax, void* enc,
+                             TilePub* pub, int sms, cudaStream_t stream);
+
 // MN-major operand -> K-major copy (skg_relayout.cu): `src` holds `cols`
 // lines of `rows` 16-bit elements (element (r, c) at src[c * ld_src + r]);
 // dst receives element (r, c) at dst[r * ld_dst + c]. ld_src and ld_dst are

@@ -108,10 +108,11 @@ struct KernelParams {
   int m, n, k;
   float alpha, beta;
   uint32_t idesc_main;
-  // MN-major output-tile operands (launches without ABFT): A stored k x m
-  // and / or B stored k x n, loaded as 64 x 64-element boxes (64 MN
-  // elements = one 128-byte swizzled row per k) and read by the MMAs as
-  // MN-major shared-memory operands.
+  // MN-major operands: A stored k x m and / or B stored k x n, loaded as
+  // 64 x 64-element boxes (64 MN elements = one 128-byte swizzled row per k)
+  // and read by the MMAs as MN-major shared-memory operands. They also form
+  // the A operand of the fused checksum tiles (A for cr, B for cc); the
+  // encodings (their B operand) are always K-major.
   int32_t a_mn, b_mn;
   WsHeader* hdr;
   skg_report_t* report;
@@ -1086,12 +1087,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tx = C::TX_BYTES;
         int kpack = 1;
         int rowA, rowB;
+        bool amn = p.a_mn != 0, bmn = p.b_mn != 0;  // MN-major A / B operand boxes
         if (w.tile >= s.t_ck) {
           int tm, tn;
           tile_coords(s, w.tile, tm, tn);
           rowA = tm * (C::PAIR ? 2 * kBM : kBM) + row_half;
           rowB = tn * BN + (C::PAIR ? (int)crank * C::B_ROWS : 0);
         } else if (w.tile < p.ck_cr_tiles) {
+          bmn = false;
           // Checksum tile: the encoding box holds only the rows the MMA uses.
           mapB = &tmBE;
           rowA = (w.tile * kCkHalf + (int)crank) * kBM;
@@ -1099,6 +1102,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tx = C::A_BYTES + p.ck_rows_cr / kCkHalf * kBK * 2;
           kpack = C::CK_PACK ? p.ck_kpack_cr : 1;
         } else {
+          amn = p.b_mn != 0;
+          bmn = false;
           mapA = &tmB128;
           mapB = &tmEA;
           rowA = ((w.tile - p.ck_cr_tiles) * kCkHalf + (int)crank) * kBM;
@@ -1119,13 +1124,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // leader expects the pair's bytes.
             const uint32_t fb = cluster_addr(&full_bar[stage], 0);
             if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * tx);
-            if (!p.a_mn) {
+            if (!amn) {
               tma_load_2d_pair(st, mapA, fb, kb * kBK, rowA);
             } else {
               for (int h = 0; h < kBM / kMnBox; ++h)
                 tma_load_2d_pair(st + h * kMnBoxBytes, mapA, fb, rowA + h * kMnBox, kb * kBK);
             }
-            if (!p.b_mn) {
+            if (!bmn) {
               tma_load_2d_pair(st + C::A_BYTES, mapB, fb, kb * kBK, rowB);
             } else {
               for (int h = 0; h < C::B_ROWS / kMnBox; ++h)
@@ -1134,14 +1139,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else if (kpack == 1) {
             mbar_arrive_expect_tx(&full_bar[stage], tx);
-            if (!p.a_mn) {
+            if (!amn) {
               tma_load_2d(st, mapA, &full_bar[stage], kb * kBK, rowA);
             } else {
               for (int h = 0; h < kBM / kMnBox; ++h)
                 tma_load_2d(st + h * kMnBoxBytes, mapA, &full_bar[stage], rowA + h * kMnBox,
                             kb * kBK);
             }
-            if (!p.b_mn) {
+            if (!bmn) {
               tma_load_2d(st + C::A_BYTES, mapB, &full_bar[stage], kb * kBK, rowB);
             } else {
               for (int h = 0; h < C::B_ROWS / kMnBox; ++h)
@@ -1152,7 +1157,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nk = min(2, w.kb_end - kb);
             mbar_arrive_expect_tx(&full_bar[stage], tx * nk);
             for (int j = 0; j < nk; ++j) {
-              tma_load_2d(st + j * C::A_BYTES, mapA, &full_bar[stage], (kb + j) * kBK, rowA);
+              if (!amn) {
+                tma_load_2d(st + j * C::A_BYTES, mapA, &full_bar[stage], (kb + j) * kBK, rowA);
+              } else {
+                for (int h = 0; h < kBM / kMnBox; ++h)
+                  tma_load_2d(st + j * C::A_BYTES + h * kMnBoxBytes, mapA, &full_bar[stage],
+                              rowA + h * kMnBox, (kb + j) * kBK);
+              }
               tma_load_2d(st + 2 * C::A_BYTES + j * C::ENC_SLOT, mapB, &full_bar[stage],
                           (kb + j) * kBK, rowB);
             }
@@ -1184,8 +1195,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 64-element MN boxes (the K-major descriptor carries 1 there), and a
       // 16-k slice is two 8-row groups of 1024 bytes.
       const uint64_t mn_lbo = (uint64_t)((kMnBoxBytes >> 4) - 1) << 16;
-      const uint64_t a_lbo = p.a_mn ? mn_lbo : 0, b_lbo = p.b_mn ? mn_lbo : 0;
-      const int a_step = p.a_mn ? (2048 >> 4) : 2, b_step = p.b_mn ? (2048 >> 4) : 2;
       Cursor cur;
       cur.init(s, unit);
       Work w;
@@ -1229,6 +1238,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kpack = (!C::CK_PACK || w.tile >= s.t_ck)
                               ? 1
                               : (w.tile < p.ck_cr_tiles ? p.ck_kpack_cr : p.ck_kpack_cc);
+        // MN-major operands of this item (the producer's choice, above).
+        const bool amn = w.tile >= s.t_ck ? p.a_mn != 0
+                                          : (w.tile < p.ck_cr_tiles ? p.a_mn != 0 : p.b_mn != 0);
+        const bool bmn = w.tile >= s.t_ck && p.b_mn != 0;
+        const uint64_t a_lbo = amn ? mn_lbo : 0, b_lbo = bmn ? mn_lbo : 0;
+        const int a_step = amn ? (2048 >> 4) : 2, b_step = bmn ? (2048 >> 4) : 2;
         if (kpack == 1) {
           for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
             // Inline fast path: the stage is usually full already.
@@ -1276,7 +1291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t b_addr = st_addr + 2 * C::A_BYTES + j * C::ENC_SLOT;
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk) {
-                const uint64_t ad = sdesc_sw128(a_addr + kk * 32);
+                const uint64_t ad = sdesc_sw128(a_addr) + a_lbo + (uint64_t)(kk * a_step);
                 const uint64_t bd = sdesc_sw128(b_addr + kk * 32);
                 const uint32_t acc = (kb > w.kb_begin || j > 0 || kk > 0) ? 1u : 0u;
                 umma_f16(d, ad, bd, idesc, acc);

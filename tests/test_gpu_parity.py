@@ -596,27 +596,67 @@ def test_mn_major_tile_configs(layouts, cfg):
     check_full(p, C)
 
 
-@pytest.mark.parametrize("layouts", [(1, 1), (1, 0)])
-def test_mn_major_layouts_abft(layouts):
-    # ABFT on the copies: clean run, every tile checked, and the same bits as
-    # the K-major call at a sweep size.
+@pytest.mark.parametrize("layouts", [(1, 1), (1, 0), (0, 1)])
+@pytest.mark.parametrize("case", [(2048, 2048, 2048, "bf16", {}),
+                                  (1000, 1304, 1032, "f16", {}),
+                                  (640, 768, 1536, "bf16", dict(cta_pair=2, tile_n=256)),
+                                  (16768, 256, 512, "bf16", {}),
+                                  (1024, 1024, 1024, "bf16", {}),
+                                  (1024, 1024, 1024, "bf16", dict(abft_local=2))])
+def test_mn_major_layouts_abft(layouts, case):
+    # ABFT with MN-major operands: the encode pass sums stored rows, the
+    # checksum tiles read A / B as MN-major MMA operands (fused into the
+    # launch, or as separate GEMMs when there are too many tiles to fuse:
+    # 16768 rows), CTA pairs, fp16 (scaled encodings); the in-CTA references
+    # and small bf16 shapes whose plan encodes in the side CTAs (1024^3) run
+    # on K-major copies. Clean run, every tile checked, and the same output
+    # bits as the K-major call.
     a_layout, b_layout = layouts
-    s = 2048
-    p = inputs.make_problem(s, s, s, seed=11, in_dtype="bf16", out_dtype="bf16",
-                            law_a="normal", law_b="normal", scale_a=s ** -0.5, scale_b=s ** -0.5,
+    m, n, k, dt, extra = case
+    p = inputs.make_problem(m, n, k, seed=11 + m, in_dtype=dt, out_dtype=dt,
+                            law_a="normal", law_b="normal", scale_a=k ** -0.5, scale_b=k ** -0.5,
                             a_layout=a_layout, b_layout=b_layout)
-    o = skgemm.opts_default(abft=1)
+    o = skgemm.opts_default(abft=1, **extra)
+    if "abft_local" in extra:
+        assert skgemm.launch_plan(m, n, k, o).local_checksums == 1
     C, ws, st = run(p, o)
     assert st == skgemm.OK
     rep = ws.report()
     assert rep.detected == 0 and rep.status_bits == 0 and rep.tiles_checked > 0
+    assert rep.max_ratio_row < 0.1 and rep.max_ratio_col < 0.1
     check_sampled(p, C, seed=5)
     A_k = p.A.t().contiguous() if a_layout else p.A
     B_k = p.B.t().contiguous() if b_layout else p.B
-    pk = inputs.Problem(s, s, s, A_k, B_k, p.C0, p.alpha, p.beta, p.in_dtype, p.out_dtype, 0, 0)
+    pk = inputs.Problem(m, n, k, A_k, B_k, p.C0, p.alpha, p.beta, p.in_dtype, p.out_dtype, 0, 0)
     Ck, wsk, stk = run(pk, o)
     assert stk == skgemm.OK and wsk.report().tiles_checked == rep.tiles_checked
     assert torch.equal(C, Ck)
+
+
+@pytest.mark.parametrize("bit", [30, 28])
+def test_mn_major_abft_injection(bit):
+    # A flipped accumulator bit with both operands MN-major is detected,
+    # located and corrected against the in-place references.
+    p = inputs.make_problem(512, 640, 1024, seed=78, in_dtype="bf16", out_dtype="f32",
+                            law_a="normal", law_b="normal", scale_b=0.02, a_layout=1, b_layout=1)
+    ref = reference(p)
+    tile, row, col = 13, 101, 7
+    tm, tn = divmod(tile, 5)
+    v = ref[tm * 128 + row, tn * 128 + col] / p.alpha
+    A_k = p.A.t().double().numpy()
+    B_k = p.B.t().double().numpy()
+    ma, mb = ab.tile_maxima(A_k, B_k, tm, tn, 128, 128)
+    tau = ab.default_tau(p.k, 128, ma, mb)
+    kind, _ = ab.classify_flip(v, bit, tau, 1e-3 * tau)
+    if kind != ab.MUST_DETECT:
+        pytest.skip(f"bit {bit} of {v} is {kind} at tau {tau}")
+    C, ws, st = _inject(p, dict(tile_n=128), tile, row, col, bit)
+    assert st == skgemm.OK
+    rep = ws.report()
+    assert rep.detected == 1 and rep.corrected == 1 and rep.uncorrectable == 0
+    rec = rep.records[0]
+    assert (rec.tile, rec.row, rec.col, rec.injected) == (tile, row, col, 1)
+    check_full(p, C, ref)
 
 
 def test_mn_major_noalloc_and_matmul():
