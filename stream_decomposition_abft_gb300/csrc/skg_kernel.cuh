@@ -1111,72 +1111,80 @@ __global__ void __launch_bounds__(kThreads, 1)
           tx = C::A_BYTES + p.ck_rows_cc / kCkHalf * kBK * 2;
           kpack = C::CK_PACK ? p.ck_kpack_cc : 1;
         }
-        for (int kb = w.kb_begin; kb < w.kb_end; kb += kpack) {
-          if (!try_wait_scoped<C::PAIR>(&empty_bar[stage], phase ^ 1) &&
-              !wait_bar(&empty_bar[stage], phase ^ 1, aux, limit, true, C::PAIR)) {
-            if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
-            ok = false;
-            break;
-          }
-          uint8_t* st = ring + stage * C::STAGE_BYTES;
-          if constexpr (C::PAIR) {
-            // Both CTAs' copies complete on the leader's full barrier; the
-            // leader expects the pair's bytes.
-            const uint32_t fb = cluster_addr(&full_bar[stage], 0);
-            if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * tx);
-            if (!amn) {
-              tma_load_2d_pair(st, mapA, fb, kb * kBK, rowA);
-            } else {
-              for (int h = 0; h < kBM / kMnBox; ++h)
-                tma_load_2d_pair(st + h * kMnBoxBytes, mapA, fb, rowA + h * kMnBox, kb * kBK);
+        // The k-loop, compiled twice: for K-major operands only (the common
+        // case: no layout branch in the loop) and with MN-major boxes.
+        auto k_loop = [&](auto mn_tag) {
+          constexpr bool kMn = decltype(mn_tag)::value;
+          const bool a_box = kMn && amn, b_box = kMn && bmn;
+          for (int kb = w.kb_begin; kb < w.kb_end; kb += kpack) {
+            if (!try_wait_scoped<C::PAIR>(&empty_bar[stage], phase ^ 1) &&
+                !wait_bar(&empty_bar[stage], phase ^ 1, aux, limit, true, C::PAIR)) {
+              if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+              ok = false;
+              break;
             }
-            if (!bmn) {
-              tma_load_2d_pair(st + C::A_BYTES, mapB, fb, kb * kBK, rowB);
-            } else {
-              for (int h = 0; h < C::B_ROWS / kMnBox; ++h)
-                tma_load_2d_pair(st + C::A_BYTES + h * kMnBoxBytes, mapB, fb, rowB + h * kMnBox,
-                                 kb * kBK);
-            }
-          } else if (kpack == 1) {
-            mbar_arrive_expect_tx(&full_bar[stage], tx);
-            if (!amn) {
-              tma_load_2d(st, mapA, &full_bar[stage], kb * kBK, rowA);
-            } else {
-              for (int h = 0; h < kBM / kMnBox; ++h)
-                tma_load_2d(st + h * kMnBoxBytes, mapA, &full_bar[stage], rowA + h * kMnBox,
-                            kb * kBK);
-            }
-            if (!bmn) {
-              tma_load_2d(st + C::A_BYTES, mapB, &full_bar[stage], kb * kBK, rowB);
-            } else {
-              for (int h = 0; h < C::B_ROWS / kMnBox; ++h)
-                tma_load_2d(st + C::A_BYTES + h * kMnBoxBytes, mapB, &full_bar[stage],
-                            rowB + h * kMnBox, kb * kBK);
-            }
-          } else {  // packed checksum stage
-            const int nk = min(2, w.kb_end - kb);
-            mbar_arrive_expect_tx(&full_bar[stage], tx * nk);
-            for (int j = 0; j < nk; ++j) {
-              if (!amn) {
-                tma_load_2d(st + j * C::A_BYTES, mapA, &full_bar[stage], (kb + j) * kBK, rowA);
+            uint8_t* st = ring + stage * C::STAGE_BYTES;
+            if constexpr (C::PAIR) {
+              // Both CTAs' copies complete on the leader's full barrier; the
+              // leader expects the pair's bytes.
+              const uint32_t fb = cluster_addr(&full_bar[stage], 0);
+              if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * tx);
+              if (!a_box) {
+                tma_load_2d_pair(st, mapA, fb, kb * kBK, rowA);
               } else {
                 for (int h = 0; h < kBM / kMnBox; ++h)
-                  tma_load_2d(st + j * C::A_BYTES + h * kMnBoxBytes, mapA, &full_bar[stage],
-                              rowA + h * kMnBox, (kb + j) * kBK);
+                  tma_load_2d_pair(st + h * kMnBoxBytes, mapA, fb, rowA + h * kMnBox, kb * kBK);
               }
-              tma_load_2d(st + 2 * C::A_BYTES + j * C::ENC_SLOT, mapB, &full_bar[stage],
-                          (kb + j) * kBK, rowB);
+              if (!b_box) {
+                tma_load_2d_pair(st + C::A_BYTES, mapB, fb, kb * kBK, rowB);
+              } else {
+                for (int h = 0; h < C::B_ROWS / kMnBox; ++h)
+                  tma_load_2d_pair(st + C::A_BYTES + h * kMnBoxBytes, mapB, fb, rowB + h * kMnBox,
+                                   kb * kBK);
+              }
+            } else if (kpack == 1) {
+              mbar_arrive_expect_tx(&full_bar[stage], tx);
+              if (!a_box) {
+                tma_load_2d(st, mapA, &full_bar[stage], kb * kBK, rowA);
+              } else {
+                for (int h = 0; h < kBM / kMnBox; ++h)
+                  tma_load_2d(st + h * kMnBoxBytes, mapA, &full_bar[stage], rowA + h * kMnBox,
+                              kb * kBK);
+              }
+              if (!b_box) {
+                tma_load_2d(st + C::A_BYTES, mapB, &full_bar[stage], kb * kBK, rowB);
+              } else {
+                for (int h = 0; h < C::B_ROWS / kMnBox; ++h)
+                  tma_load_2d(st + C::A_BYTES + h * kMnBoxBytes, mapB, &full_bar[stage],
+                              rowB + h * kMnBox, kb * kBK);
+              }
+            } else {  // packed checksum stage
+              const int nk = min(2, w.kb_end - kb);
+              mbar_arrive_expect_tx(&full_bar[stage], tx * nk);
+              for (int j = 0; j < nk; ++j) {
+                if (!a_box) {
+                  tma_load_2d(st + j * C::A_BYTES, mapA, &full_bar[stage], (kb + j) * kBK, rowA);
+                } else {
+                  for (int h = 0; h < kBM / kMnBox; ++h)
+                    tma_load_2d(st + j * C::A_BYTES + h * kMnBoxBytes, mapA, &full_bar[stage],
+                                rowA + h * kMnBox, (kb + j) * kBK);
+                }
+                tma_load_2d(st + 2 * C::A_BYTES + j * C::ENC_SLOT, mapB, &full_bar[stage],
+                            (kb + j) * kBK, rowB);
+              }
+            }
+            if (leader) {
+              pending |= 1u << stage;
+              pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+            }
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
             }
           }
-          if (leader) {
-            pending |= 1u << stage;
-            pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
-          }
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
+        };
+        if (amn || bmn) k_loop(std::true_type{});
+        else k_loop(std::false_type{});
       }
       // Never leave with a copy in flight into this CTA's shared memory.
       for (int i = 0; i < STAGES; ++i)
