@@ -291,15 +291,22 @@ skg_status_t skg_gemm_verify(int64_t m, int64_t n, int64_t k, float alpha, const
  * High-Performance GEMM with Online Fault Tolerance on GPUs",
  * threadblock-level ABFT, Fig. 5: the encodings e^T A and B e of each
  * threadblock's operands). Arguments as for skg_gemm with K-major operands
- * (A row-major, B stored n x k; the encodings do not depend on the layout,
- * so the encodings of K-major copies of MN-major operands also serve a
- * call on the MN-major originals); opts must be the options of the gemm
- * call that follows with opts->abft_preencoded = 1. Asynchronous on
- * `stream`. */
+ * (A row-major, B stored n x k; skg_abft_encode_layout takes the layouts);
+ * opts must be the options of the gemm call that follows with
+ * opts->abft_preencoded = 1. Asynchronous on `stream`. */
 skg_status_t skg_abft_encode(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
                              const void* B, int64_t ldb, int32_t in_dtype,
                              const skg_opts_t* opts, void* workspace, size_t ws_bytes,
                              void* stream);
+
+/* skg_abft_encode for operands in any layout (skg_a_layout_t,
+ * skg_b_layout_t): an MN-major operand's encodings are the sums of its
+ * stored row segments. For a following pre-encoded call with the same
+ * layouts (which then reads MN-major operands in place). */
+skg_status_t skg_abft_encode_layout(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
+                                    const void* B, int64_t ldb, int32_t in_dtype,
+                                    int32_t a_layout, int32_t b_layout, const skg_opts_t* opts,
+                                    void* workspace, size_t ws_bytes, void* stream);
 
 /* The schedule the kernel runs, computed on the host: for every CTA, its
  * ordered segments (tile, k-iteration range, role). bm, bn, bk are the tile

@@ -838,11 +838,20 @@ skg_status_t skg_abft_encode(int64_t m, int64_t n, int64_t k, const void* A, int
                              const void* B, int64_t ldb, int32_t in_dtype,
                              const skg_opts_t* opts, void* workspace, size_t ws_bytes,
                              void* stream) {
+  return skg_abft_encode_layout(m, n, k, A, lda, B, ldb, in_dtype, SKG_A_ROW, SKG_B_KMAJOR, opts,
+                                workspace, ws_bytes, stream);
+}
+
+skg_status_t skg_abft_encode_layout(int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
+                                    const void* B, int64_t ldb, int32_t in_dtype,
+                                    int32_t a_layout, int32_t b_layout, const skg_opts_t* opts,
+                                    void* workspace, size_t ws_bytes, void* stream) {
   if (m < 0 || n < 0 || k < 0) return SKG_ERR_ARG;
   if (m > INT32_MAX / 4 || n > INT32_MAX / 4 || k > INT32_MAX / 4) return SKG_ERR_UNSUPPORTED;
   if (in_dtype != SKG_IN_F16 && in_dtype != SKG_IN_BF16) return SKG_ERR_ARG;
+  if (!layout_valid(a_layout, b_layout)) return SKG_ERR_ARG;
   if (m == 0 || n == 0 || k == 0) return SKG_OK;
-  skg_status_t st = check_inputs(m, n, k, A, lda, B, ldb);
+  skg_status_t st = check_inputs(m, n, k, A, lda, B, ldb, a_layout, b_layout);
   if (st != SKG_OK) return st;
   const int sms = sm_count_cached();
   if (sms <= 0) return SKG_ERR_CUDA;
@@ -857,7 +866,8 @@ skg_status_t skg_abft_encode(int64_t m, int64_t n, int64_t k, const void* A, int
   if (!workspace || !aligned16(workspace) || ws_bytes < L.total) return SKG_ERR_WORKSPACE;
   if (!tensor_map_encoder()) return SKG_ERR_CUDA;
   uint8_t* ws = (uint8_t*)workspace;
-  return run_encode(in_dtype, A, lda, m, B, ldb, n, k, r, ws, L, sms, (cudaStream_t)stream);
+  return run_encode_layouts(in_dtype, A, lda, a_layout == SKG_A_COL, m, B, ldb,
+                            b_layout == SKG_B_NMAJOR, n, k, r, ws, L, sms, (cudaStream_t)stream);
 }
 
 skg_status_t skg_schedule_query(int64_t m, int64_t n, int64_t k, int32_t bm, int32_t bn,

@@ -84,7 +84,7 @@ SYMBOLS = ("skg_opts_default", "skg_workspace_size", "skg_workspace_init", "skg_
            "skg_gemm_verify", "skg_abft_encode", "skg_schedule_query", "skg_launch_shape", "skg_report_read",
            "skg_device_sm_count", "skg_status_string", "skg_gemm_noalloc", "skg_schedule_cost",
            "skg_launch_plan", "skg_workspace_size_layout", "skg_host_staging_size",
-           "skg_gemm_host")
+           "skg_gemm_host", "skg_abft_encode_layout")
 
 _lib = None
 
@@ -127,6 +127,9 @@ def lib() -> ctypes.CDLL:
     L.skg_abft_encode.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, ctypes.POINTER(Opts),
                                   vp, sz, vp]
     L.skg_abft_encode.restype = i32
+    L.skg_abft_encode_layout.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, i32, i32,
+                                         ctypes.POINTER(Opts), vp, sz, vp]
+    L.skg_abft_encode_layout.restype = i32
     L.skg_schedule_query.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32,
                                      ctypes.POINTER(Segment), i64, ctypes.POINTER(i64)]
     L.skg_schedule_query.restype = i32
@@ -207,10 +210,14 @@ def gemm_verify(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, in_dty
 
 
 def abft_encode(m, n, k, A_ptr, lda, B_ptr, ldb, in_dtype, opts, ws_ptr, ws_bytes,
-                stream) -> int:
-    return int(lib().skg_abft_encode(m, n, k, A_ptr, lda, B_ptr, ldb, in_dtype,
-                                     ctypes.byref(opts) if opts else None, ws_ptr, ws_bytes,
-                                     stream))
+                stream, a_layout: int = A_ROW, b_layout: int = B_KMAJOR) -> int:
+    """skg_abft_encode (K-major operands) or skg_abft_encode_layout."""
+    o = ctypes.byref(opts) if opts else None
+    if a_layout == A_ROW and b_layout == B_KMAJOR:
+        return int(lib().skg_abft_encode(m, n, k, A_ptr, lda, B_ptr, ldb, in_dtype, o, ws_ptr,
+                                         ws_bytes, stream))
+    return int(lib().skg_abft_encode_layout(m, n, k, A_ptr, lda, B_ptr, ldb, in_dtype, a_layout,
+                                            b_layout, o, ws_ptr, ws_bytes, stream))
 
 
 def schedule_query(m: int, n: int, k: int, bm: int, bn: int, bk: int, g: int,

@@ -633,6 +633,36 @@ def test_mn_major_layouts_abft(layouts, case):
     assert torch.equal(C, Ck)
 
 
+@pytest.mark.parametrize("layouts", [(1, 1), (1, 0), (0, 1)])
+def test_mn_major_preencoded(layouts):
+    # skg_abft_encode_layout, then the pre-encoded call on the same MN-major
+    # operands: the same output bits and report as the one-call ABFT.
+    a_layout, b_layout = layouts
+    m, n, k = 1024, 768, 1536
+    p = inputs.make_problem(m, n, k, seed=44, in_dtype="bf16", out_dtype="bf16",
+                            law_a="normal", law_b="normal", scale_a=k ** -0.5, scale_b=k ** -0.5,
+                            a_layout=a_layout, b_layout=b_layout)
+    o = skgemm.opts_default(abft=1)
+    C1, ws1, st1 = run(p, o)
+    assert st1 == skgemm.OK
+    A, B = p.A.cuda(), p.B.cuda()
+    op = skgemm.opts_default(abft=1, abft_preencoded=1)
+    ws = skgemm.Workspace(skgemm.workspace_size_layout(m, n, k, a_layout, b_layout, op), "cuda")
+    sh = torch.cuda.current_stream().cuda_stream
+    assert skgemm.abft_encode(m, n, k, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0),
+                              skgemm.IN_BF16, op, ws.ptr, ws.nbytes, sh, a_layout,
+                              b_layout) == skgemm.OK
+    C2 = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    assert skgemm.gemm(m, n, k, 1.0, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), 0.0,
+                       C2.data_ptr(), n, skgemm.IN_BF16, skgemm.OUT_BF16, a_layout, b_layout, op,
+                       ws.ptr, ws.nbytes, sh) == skgemm.OK
+    torch.cuda.synchronize()
+    r1, r2 = ws1.report(), ws.report()
+    assert r2.detected == 0 and r2.status_bits == 0 and r2.tiles_checked == r1.tiles_checked
+    assert torch.equal(C1, C2)
+    check_sampled(p, C2, seed=2)
+
+
 @pytest.mark.parametrize("bit", [30, 28])
 def test_mn_major_abft_injection(bit):
     # A flipped accumulator bit with both operands MN-major is detected,
