@@ -327,7 +327,7 @@ struct Gemm {
   float alpha, beta;
   int in_dtype, out_dtype;
   // MN-major operands read directly by the MMAs (A stored k x m, B stored
-  // k x n); launches without ABFT only.
+  // k x n), in the output tiles and as the A operand of the checksum tiles.
   int a_mn = 0, b_mn = 0;
 };
 

@@ -3,9 +3,10 @@
 //
 //   C = alpha * A B + beta * C,   A: m x k (K-major), B: stored n x k (K-major)
 //
-// (Without ABFT either operand may also be MN-major -- A stored k x m, B
-// stored k x n: the producer then loads 64 x 64-element boxes and the MMAs
-// read MN-major shared-memory operands; see KernelParams::a_mn.)
+// (Either operand may also be MN-major -- A stored k x m, B stored k x n:
+// the producer then loads 64 x 64-element boxes and the MMAs read MN-major
+// shared-memory operands, in output and checksum tiles alike; see
+// KernelParams::a_mn.)
 //
 // Work decomposition: "Stream-K: Work-centric Parallel Decomposition for
 // Dense Matrix-Matrix Multiplication on the GPU", Algorithm 5 and §5.2
