@@ -39,6 +39,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "GEMM TFLOPS (2mnk/s) and % of GB300 dense bf16 peak; geomean over shape sweep"
+WORKLOAD = ("square bf16 sweep m=n=k in {1024,2048,3072,4096,5120,6144}, "
+            "N(0,1)/sqrt(k) inputs (seed 1), fp32 accumulate, bf16 out, ABFT verify on")
 FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ("stream_decomposition_abft_gb300/csrc/skg_kernel.cuh",
                   "stream_decomposition_abft_gb300/csrc/skg_ptx.cuh",
@@ -283,9 +285,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "square bf16 sweep m=n=k in {1024,2048,3072,4096,5120,6144}, "
-                               "N(0,1)/sqrt(k) inputs (seed 1), fp32 accumulate, bf16 out, "
-                               "ABFT verify on",
+        "config": {"workload": WORKLOAD,
                    "plan_per_shape": {str(sz): {"tile": f"{pl.tile_m}x{pl.tile_n}x64",
                                                 "ctas": pl.ctas + pl.side_ctas,
                                                 "cta_pairs": pl.cta_pair == 2,
@@ -470,8 +470,8 @@ def run_reference(args, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * wall / max(1, args.steps), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "square bf16 sweep m=n=k in {1024,...,6144} (oracle: one "
-                                   "row of C per shape per step)"},
+            "config": {"workload": WORKLOAD, "sample": "one whole row of C per shape per step",
+                       "parallelism": "oracle on the host cores"},
             "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.threads(),
                              "kind": "oracle",
                              "sample": "one whole row of C per sweep shape per step"},
