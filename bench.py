@@ -512,17 +512,19 @@ def ncu_target(args):
         for spec in args.shape.split(","):
             m, n, k = (int(x) for x in spec.split("x"))
             dt = "f16" if args.plain else "bf16"
+            al, bl = int(args.a_col), int(args.b_nmajor)
             p = inputs.make_problem(m, n, k, seed=5, in_dtype=dt, out_dtype=dt,
-                                    law_a="normal", law_b="normal")
+                                    law_a="normal", law_b="normal", a_layout=al, b_layout=bl)
             A, B = p.A.to(dev), p.B.to(dev)
             C = torch.empty((m, n), dtype=A.dtype, device=dev)
             o = skgemm.opts_default(abft=0 if args.plain else 1)
-            ws = skgemm.Workspace(skgemm.workspace_size(m, n, k, o), dev)
+            ws = skgemm.Workspace(skgemm.workspace_size_layout(m, n, k, al, bl, o), dev)
             code = skgemm.IN_F16 if args.plain else skgemm.IN_BF16
             out = skgemm.OUT_F16 if args.plain else skgemm.OUT_BF16
             for _ in range(args.steps):
-                st = skgemm.gemm(m, n, k, 1.0, A.data_ptr(), k, B.data_ptr(), k, 0.0,
-                                 C.data_ptr(), n, code, out, 0, 0, o, ws.ptr, ws.nbytes, sh)
+                st = skgemm.gemm(m, n, k, 1.0, A.data_ptr(), A.stride(0), B.data_ptr(),
+                                 B.stride(0), 0.0, C.data_ptr(), n, code, out, al, bl, o, ws.ptr,
+                                 ws.nbytes, sh)
                 if st != skgemm.OK:
                     raise skgemm.SkgError(st, "skg_gemm")
             torch.cuda.synchronize()
@@ -810,6 +812,10 @@ def main():
     ap.add_argument("--sizes", default="", help="with --ncu-target: comma-separated sizes")
     ap.add_argument("--shape", default="",
                     help="with --ncu-target: MxNxK[,MxNxK...] (bf16 with ABFT, or --plain)")
+    ap.add_argument("--a-col", action="store_true",
+                    help="with --ncu-target --shape: A stored column-major (k x m)")
+    ap.add_argument("--b-nmajor", action="store_true",
+                    help="with --ncu-target --shape: B stored k x n")
     ap.add_argument("--plain", action="store_true",
                     help="with --ncu-target --shape: fp16 without ABFT")
     ap.add_argument("--write-traffic", default="",

@@ -446,14 +446,16 @@ cudaError_t launch_encode(int in_bf16, const CUtensorMap& tmA, const CUtensorMap
 // Encodings of an MN-major operand (A stored k x m, or B stored k x n). The
 // tile's encoding at k is the sum of the tile's tw consecutive elements of
 // stored row k -- the same e^T A / B e as above, here a contiguous row
-// segment. Pass 1: one block per unit (tile, kEncSliceCols rows of k); a
-// row segment is read by tw / 8 lanes with one 16-byte load each (four rows
-// in flight per lane) and summed with shuffles; bf16 writes its hi / lo
+// segment. Pass 1: one block of 32 warps per unit (tile, kEncSliceCols rows
+// of k); a row segment is read by tw / 8 lanes with one 16-byte load each
+// (four rows in flight per lane) and summed with shuffles; bf16 writes its hi / lo
 // terms at once (scale 2^0), fp16 stores the fp32 sum; the block's max
 // |element| goes to the unit's umax. Pass 2 (fp16 only): one block per tile
 // picks the tile's scale from its largest |sum| and writes the hi / lo rows
 // as the K-major pass does.
-constexpr int kMnEncThreads = 256;
+// 32 warps per unit keep 64 KB of loads in flight per block (an SM needs
+// ~64 KB outstanding to stream at the HBM rate).
+constexpr int kMnEncThreads = 1024;
 constexpr int kMnEncUnroll = 4;
 
 template <typename T>
@@ -582,7 +584,7 @@ cudaError_t launch_encode_mn_t(const void* src, int64_t ld, int64_t rows, int64_
                                TilePub* pub, int sms, cudaStream_t stream) {
   const int slices = encode_slices(kp);
   const int64_t units = (int64_t)tiles * slices;
-  const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 8;
+  const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 2;
   const int grid1 = (int)(units < cap ? units : cap);
   const int grid2 = tiles < 4 * (sms > 0 ? sms : 1) ? tiles : 4 * sms;
   if (grid1 <= 0 || grid2 <= 0) return cudaSuccess;
