@@ -1112,11 +1112,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tx = C::A_BYTES + p.ck_rows_cc / kCkHalf * kBK * 2;
           kpack = C::CK_PACK ? p.ck_kpack_cc : 1;
         }
-        // The k-loop, compiled once per operand-layout pair so that no
-        // layout branch sits in the loop (a runtime one cost 5-9 % of the
-        // pair kernel's time).
-        auto k_loop = [&](auto a_tag, auto b_tag) {
-          constexpr bool a_box = decltype(a_tag)::value, b_box = decltype(b_tag)::value;
+        // The k-loop, compiled twice: for K-major operands only, with no
+        // layout branch in the loop (a runtime one cost 5-9 % of the pair
+        // kernel's time), and for any MN-major operand. One copy per layout
+        // pair made MN-major calls as fast as K-major ones but cost the
+        // K-major single-CTA ABFT kernel ~1.3 us at 2048^3 (code size).
+        auto k_loop = [&](auto mn_tag) {
+          constexpr bool kMn = decltype(mn_tag)::value;
+          const bool a_box = kMn && amn, b_box = kMn && bmn;
           for (int kb = w.kb_begin; kb < w.kb_end; kb += kpack) {
             if (!try_wait_scoped<C::PAIR>(&empty_bar[stage], phase ^ 1) &&
                 !wait_bar(&empty_bar[stage], phase ^ 1, aux, limit, true, C::PAIR)) {
@@ -1130,13 +1133,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               // leader expects the pair's bytes.
               const uint32_t fb = cluster_addr(&full_bar[stage], 0);
               if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * tx);
-              if constexpr (!a_box) {
+              if (!a_box) {
                 tma_load_2d_pair(st, mapA, fb, kb * kBK, rowA);
               } else {
                 for (int h = 0; h < kBM / kMnBox; ++h)
                   tma_load_2d_pair(st + h * kMnBoxBytes, mapA, fb, rowA + h * kMnBox, kb * kBK);
               }
-              if constexpr (!b_box) {
+              if (!b_box) {
                 tma_load_2d_pair(st + C::A_BYTES, mapB, fb, kb * kBK, rowB);
               } else {
                 for (int h = 0; h < C::B_ROWS / kMnBox; ++h)
@@ -1145,14 +1148,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             } else if (kpack == 1) {
               mbar_arrive_expect_tx(&full_bar[stage], tx);
-              if constexpr (!a_box) {
+              if (!a_box) {
                 tma_load_2d(st, mapA, &full_bar[stage], kb * kBK, rowA);
               } else {
                 for (int h = 0; h < kBM / kMnBox; ++h)
                   tma_load_2d(st + h * kMnBoxBytes, mapA, &full_bar[stage], rowA + h * kMnBox,
                               kb * kBK);
               }
-              if constexpr (!b_box) {
+              if (!b_box) {
                 tma_load_2d(st + C::A_BYTES, mapB, &full_bar[stage], kb * kBK, rowB);
               } else {
                 for (int h = 0; h < C::B_ROWS / kMnBox; ++h)
@@ -1163,7 +1166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int nk = min(2, w.kb_end - kb);
               mbar_arrive_expect_tx(&full_bar[stage], tx * nk);
               for (int j = 0; j < nk; ++j) {
-                if constexpr (!a_box) {
+                if (!a_box) {
                   tma_load_2d(st + j * C::A_BYTES, mapA, &full_bar[stage], (kb + j) * kBK, rowA);
                 } else {
                   for (int h = 0; h < kBM / kMnBox; ++h)
@@ -1184,13 +1187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         };
-        if (amn) {
-          if (bmn) k_loop(std::true_type{}, std::true_type{});
-          else k_loop(std::true_type{}, std::false_type{});
-        } else {
-          if (bmn) k_loop(std::false_type{}, std::true_type{});
-          else k_loop(std::false_type{}, std::false_type{});
-        }
+        if (amn || bmn) k_loop(std::true_type{});
+        else k_loop(std::false_type{});
       }
       // Never leave with a copy in flight into this CTA's shared memory.
       for (int i = 0; i < STAGES; ++i)
