@@ -331,14 +331,23 @@ struct Gemm {
   int a_mn = 0, b_mn = 0;
 };
 
-template <int BN, bool ABFT, bool PAIR = false, bool LOCAL = false>
+template <int BN, bool ABFT, bool PAIR = false, bool LOCAL = false, bool MN = false>
 cudaError_t dispatch_out(int out_dtype, const Maps& mp, const KernelParams& p, int grid,
                          cudaStream_t st) {
   switch (out_dtype) {
-    case SKG_OUT_F32: return launch_gemm<BN, ABFT, 0, PAIR, LOCAL>(mp, p, grid, st);
-    case SKG_OUT_F16: return launch_gemm<BN, ABFT, 1, PAIR, LOCAL>(mp, p, grid, st);
-    default: return launch_gemm<BN, ABFT, 2, PAIR, LOCAL>(mp, p, grid, st);
+    case SKG_OUT_F32: return launch_gemm<BN, ABFT, 0, PAIR, LOCAL, MN>(mp, p, grid, st);
+    case SKG_OUT_F16: return launch_gemm<BN, ABFT, 1, PAIR, LOCAL, MN>(mp, p, grid, st);
+    default: return launch_gemm<BN, ABFT, 2, PAIR, LOCAL, MN>(mp, p, grid, st);
   }
+}
+
+// The instantiation for the launch's operand layouts: K-major kernels carry
+// no MN-major code.
+template <int BN, bool ABFT, bool PAIR = false>
+cudaError_t dispatch_layout(bool mn, int out_dtype, const Maps& mp, const KernelParams& p,
+                            int grid, cudaStream_t st) {
+  return mn ? dispatch_out<BN, ABFT, PAIR, false, true>(out_dtype, mp, p, grid, st)
+            : dispatch_out<BN, ABFT, PAIR>(out_dtype, mp, p, grid, st);
 }
 
 // Fused ABFT checksum GEMMs fit one tile column each when 2 * tiles <= BN.
@@ -485,18 +494,21 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   p.ldc = g.ldc;
   p.in_f16 = g.in_dtype == SKG_IN_F16 ? 1 : 0;
 
+  const bool mn = g.a_mn || g.b_mn;
+  const int od = g.out_dtype;
+  const int lg = launch_grid;
   cudaError_t e;
   if (r.pair)
-    e = abft_epilogue ? dispatch_out<256, true, true>(g.out_dtype, mp, p, launch_grid, stream)
-                      : dispatch_out<256, false, true>(g.out_dtype, mp, p, launch_grid, stream);
+    e = abft_epilogue ? dispatch_layout<256, true, true>(mn, od, mp, p, lg, stream)
+                      : dispatch_layout<256, false, true>(mn, od, mp, p, lg, stream);
   else if (r.bn == 128)
     e = (abft_epilogue && r.abft_local && !fuse_ck)
-            ? dispatch_out<128, true, false, true>(g.out_dtype, mp, p, launch_grid, stream)
-        : abft_epilogue ? dispatch_out<128, true>(g.out_dtype, mp, p, launch_grid, stream)
-                        : dispatch_out<128, false>(g.out_dtype, mp, p, launch_grid, stream);
+            ? dispatch_out<128, true, false, true>(od, mp, p, lg, stream)
+        : abft_epilogue ? dispatch_layout<128, true>(mn, od, mp, p, lg, stream)
+                        : dispatch_layout<128, false>(mn, od, mp, p, lg, stream);
   else
-    e = abft_epilogue ? dispatch_out<256, true>(g.out_dtype, mp, p, launch_grid, stream)
-                      : dispatch_out<256, false>(g.out_dtype, mp, p, launch_grid, stream);
+    e = abft_epilogue ? dispatch_layout<256, true>(mn, od, mp, p, lg, stream)
+                      : dispatch_layout<256, false>(mn, od, mp, p, lg, stream);
   return e == cudaSuccess ? SKG_OK : SKG_ERR_CUDA;
 }
 

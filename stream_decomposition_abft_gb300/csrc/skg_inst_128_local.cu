@@ -7,9 +7,9 @@
 
 namespace skg {
 
-template <int BN, bool ABFT, int OUT, bool PAIR, bool LOCAL>
+template <int BN, bool ABFT, int OUT, bool PAIR, bool LOCAL, bool MN>
 cudaError_t launch_gemm(const Maps& mp, const KernelParams& p, int grid, cudaStream_t stream) {
-  using C = Cfg<BN, ABFT, OUT, PAIR, LOCAL>;
+  using C = Cfg<BN, ABFT, OUT, PAIR, LOCAL, MN>;
   // The shared-memory opt-in is per device; set it once per device.
   static std::atomic<uint64_t> done_mask{0};
   int dev = 0;

@@ -53,10 +53,11 @@ struct Maps {
   CUtensorMap enca, encb;  // in-kernel encode boxes of A and B (64 x 256, no swizzle)
 };
 
-// Launch the persistent kernel instantiated for (BN, ABFT, OUT, PAIR, LOCAL)
-// on `grid` CTAs (PAIR: grid / 2 clusters of two; LOCAL: in-CTA ABFT
-// references). Defined in the skg_inst_*.cu translation units.
-template <int BN, bool ABFT, int OUT, bool PAIR = false, bool LOCAL = false>
+// Launch the persistent kernel instantiated for (BN, ABFT, OUT, PAIR, LOCAL,
+// MN) on `grid` CTAs (PAIR: grid / 2 clusters of two; LOCAL: in-CTA ABFT
+// references; MN: MN-major operands possible). Defined in the skg_inst_*.cu
+// translation units.
+template <int BN, bool ABFT, int OUT, bool PAIR = false, bool LOCAL = false, bool MN = false>
 cudaError_t launch_gemm(const Maps& mp, const KernelParams& p, int grid, cudaStream_t stream);
 
 // Clusters of two CTAs of the pair kernel (BLK_N = 256) that can be resident

@@ -178,10 +178,14 @@ __host__ __device__ constexpr int pow2_at_least(int v) {
   return p;
 }
 
-template <int BN_, bool ABFT_, int OUT_, bool PAIR_ = false, bool LOCAL_ = false>
+template <int BN_, bool ABFT_, int OUT_, bool PAIR_ = false, bool LOCAL_ = false, bool MN_ = false>
 struct Cfg {
   static constexpr int BN = BN_;
   static constexpr bool ABFT = ABFT_;
+  // MN-major operands possible (KernelParams::a_mn / b_mn); the K-major-only
+  // instantiations carry no layout code in the producer and MMA loops.
+  static constexpr bool MN = MN_;
+  static_assert(!(MN_ && LOCAL_), "in-CTA references read K-major stages");
   // In-CTA ABFT references (local_checksums): the epilogue warps also read
   // every stage, for launches of at most one whole tile per CTA.
   static constexpr bool LOCAL = LOCAL_;
@@ -1088,7 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tx = C::TX_BYTES;
         int kpack = 1;
         int rowA, rowB;
-        bool amn = p.a_mn != 0, bmn = p.b_mn != 0;  // MN-major A / B operand boxes
+        bool amn = C::MN && p.a_mn != 0, bmn = C::MN && p.b_mn != 0;  // MN-major boxes
         if (w.tile >= s.t_ck) {
           int tm, tn;
           tile_coords(s, w.tile, tm, tn);
@@ -1112,14 +1116,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tx = C::A_BYTES + p.ck_rows_cc / kCkHalf * kBK * 2;
           kpack = C::CK_PACK ? p.ck_kpack_cc : 1;
         }
-        // The k-loop, compiled twice: for K-major operands only, with no
-        // layout branch in the loop (a runtime one cost 5-9 % of the pair
-        // kernel's time), and for any MN-major operand. One copy per layout
-        // pair made MN-major calls as fast as K-major ones but cost the
-        // K-major single-CTA ABFT kernel ~1.3 us at 2048^3 (code size).
-        auto k_loop = [&](auto mn_tag) {
-          constexpr bool kMn = decltype(mn_tag)::value;
-          const bool a_box = kMn && amn, b_box = kMn && bmn;
+        // The k-loop, compiled once per operand-layout pair so that no
+        // layout branch sits in the loop (a runtime one cost 5-9 %); the
+        // K-major instantiations compile only the K-major copy (more copies
+        // in one kernel cost ~1.3 us at 2048^3 through code size).
+        auto k_loop = [&](auto a_tag, auto b_tag) {
+          constexpr bool a_box = decltype(a_tag)::value, b_box = decltype(b_tag)::value;
           for (int kb = w.kb_begin; kb < w.kb_end; kb += kpack) {
             if (!try_wait_scoped<C::PAIR>(&empty_bar[stage], phase ^ 1) &&
                 !wait_bar(&empty_bar[stage], phase ^ 1, aux, limit, true, C::PAIR)) {
@@ -1133,13 +1135,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               // leader expects the pair's bytes.
               const uint32_t fb = cluster_addr(&full_bar[stage], 0);
               if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * tx);
-              if (!a_box) {
+              if constexpr (!a_box) {
                 tma_load_2d_pair(st, mapA, fb, kb * kBK, rowA);
               } else {
                 for (int h = 0; h < kBM / kMnBox; ++h)
                   tma_load_2d_pair(st + h * kMnBoxBytes, mapA, fb, rowA + h * kMnBox, kb * kBK);
               }
-              if (!b_box) {
+              if constexpr (!b_box) {
                 tma_load_2d_pair(st + C::A_BYTES, mapB, fb, kb * kBK, rowB);
               } else {
                 for (int h = 0; h < C::B_ROWS / kMnBox; ++h)
@@ -1148,14 +1150,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             } else if (kpack == 1) {
               mbar_arrive_expect_tx(&full_bar[stage], tx);
-              if (!a_box) {
+              if constexpr (!a_box) {
                 tma_load_2d(st, mapA, &full_bar[stage], kb * kBK, rowA);
               } else {
                 for (int h = 0; h < kBM / kMnBox; ++h)
                   tma_load_2d(st + h * kMnBoxBytes, mapA, &full_bar[stage], rowA + h * kMnBox,
                               kb * kBK);
               }
-              if (!b_box) {
+              if constexpr (!b_box) {
                 tma_load_2d(st + C::A_BYTES, mapB, &full_bar[stage], kb * kBK, rowB);
               } else {
                 for (int h = 0; h < C::B_ROWS / kMnBox; ++h)
@@ -1166,7 +1168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int nk = min(2, w.kb_end - kb);
               mbar_arrive_expect_tx(&full_bar[stage], tx * nk);
               for (int j = 0; j < nk; ++j) {
-                if (!a_box) {
+                if constexpr (!a_box) {
                   tma_load_2d(st + j * C::A_BYTES, mapA, &full_bar[stage], (kb + j) * kBK, rowA);
                 } else {
                   for (int h = 0; h < kBM / kMnBox; ++h)
@@ -1187,8 +1189,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         };
-        if (amn || bmn) k_loop(std::true_type{});
-        else k_loop(std::false_type{});
+        if constexpr (!C::MN) {
+          k_loop(std::false_type{}, std::false_type{});
+        } else if (amn) {
+          if (bmn) k_loop(std::true_type{}, std::true_type{});
+          else k_loop(std::true_type{}, std::false_type{});
+        } else {
+          if (bmn) k_loop(std::false_type{}, std::true_type{});
+          else k_loop(std::false_type{}, std::false_type{});
+        }
       }
       // Never leave with a copy in flight into this CTA's shared memory.
       for (int i = 0; i < STAGES; ++i)
@@ -1251,9 +1260,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                               ? 1
                               : (w.tile < p.ck_cr_tiles ? p.ck_kpack_cr : p.ck_kpack_cc);
         // MN-major operands of this item (the producer's choice, above).
-        const bool amn = w.tile >= s.t_ck ? p.a_mn != 0
-                                          : (w.tile < p.ck_cr_tiles ? p.a_mn != 0 : p.b_mn != 0);
-        const bool bmn = w.tile >= s.t_ck && p.b_mn != 0;
+        const bool amn = C::MN && (w.tile >= s.t_ck ? p.a_mn != 0
+                                                    : (w.tile < p.ck_cr_tiles ? p.a_mn != 0
+                                                                              : p.b_mn != 0));
+        const bool bmn = C::MN && w.tile >= s.t_ck && p.b_mn != 0;
         const uint64_t a_lbo = amn ? mn_lbo : 0, b_lbo = bmn ? mn_lbo : 0;
         const int a_step = amn ? (2048 >> 4) : 2, b_step = bmn ? (2048 >> 4) : 2;
         if (kpack == 1) {
