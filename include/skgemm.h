@@ -407,6 +407,29 @@ skg_status_t skg_gemm_host(int64_t m, int64_t n, int64_t k, float alpha, const v
                            int32_t b_layout, const skg_opts_t* opts, void* staging,
                            size_t staging_bytes, void* workspace, size_t ws_bytes, void* stream);
 
+/* Bytes of device workspace skg_gemm_f64 needs: a header (launch epoch,
+ * exit tickets), the report, one flag and one 64 x 64 fp64 partial-tile slot
+ * per CTA (Stream-K page, §4: fixup storage scales with g). */
+size_t skg_workspace_size_f64(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts);
+
+/* fp64 Stream-K GEMM (Stream-K page, §6 evaluates FP64 as well as FP16):
+ * C = alpha * A B + beta * C, all double, asynchronous on `stream`. A
+ * row-major m x k (lda >= k), B stored n x k (ldb >= k), C row-major m x n
+ * (ldc >= n), device pointers, leading dimensions in elements. The MAC
+ * iterations of 64 x 64 x 16 tiles are split over opts->grid persistent CTAs
+ * (0 = one per SM) with opts->sched (SKG_SCHED_AUTO = the two-tile hybrid),
+ * partial tiles fixed up through the workspace with epoch flags as in
+ * skg_gemm; CUDA-core FMAs (GB300's fp64 rate is far below its 16-bit
+ * tensor rate). workspace: device, 256-byte aligned, >=
+ * skg_workspace_size_f64 bytes, zeroed once with skg_workspace_init; one
+ * per stream. A fixup wait that runs out is reported as
+ * SKG_ERR_FIXUP_TIMEOUT in the report (skg_report_read). k = 0 gives
+ * C = beta * C. No ABFT in this variant. */
+skg_status_t skg_gemm_f64(int64_t m, int64_t n, int64_t k, double alpha, const double* A,
+                          int64_t lda, const double* B, int64_t ldb, double beta, double* C,
+                          int64_t ldc, const skg_opts_t* opts, void* workspace, size_t ws_bytes,
+                          void* stream);
+
 /* Number of SMs of the current device (0 if there is no device). */
 int32_t skg_device_sm_count(void);
 

@@ -84,7 +84,7 @@ SYMBOLS = ("skg_opts_default", "skg_workspace_size", "skg_workspace_init", "skg_
            "skg_gemm_verify", "skg_abft_encode", "skg_schedule_query", "skg_launch_shape", "skg_report_read",
            "skg_device_sm_count", "skg_status_string", "skg_gemm_noalloc", "skg_schedule_cost",
            "skg_launch_plan", "skg_workspace_size_layout", "skg_host_staging_size",
-           "skg_gemm_host", "skg_abft_encode_layout")
+           "skg_gemm_host", "skg_abft_encode_layout", "skg_workspace_size_f64", "skg_gemm_f64")
 
 _lib = None
 
@@ -118,6 +118,12 @@ def lib() -> ctypes.CDLL:
                  ctypes.POINTER(Opts), vp, sz, vp]
     L.skg_gemm.argtypes = gemm_args
     L.skg_gemm.restype = i32
+    f64 = ctypes.c_double
+    L.skg_workspace_size_f64.argtypes = [i64, i64, i64, ctypes.POINTER(Opts)]
+    L.skg_workspace_size_f64.restype = sz
+    L.skg_gemm_f64.argtypes = [i64, i64, i64, f64, vp, i64, vp, i64, f64, vp, i64,
+                               ctypes.POINTER(Opts), vp, sz, vp]
+    L.skg_gemm_f64.restype = i32
     L.skg_host_staging_size.argtypes = [i64, i64, i64, i32, i32, i32, i32]
     L.skg_host_staging_size.restype = sz
     L.skg_gemm_host.argtypes = gemm_args[:-3] + [vp, sz, vp, sz, vp]
@@ -184,6 +190,18 @@ def gemm(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, in_dtype, out
     return int(lib().skg_gemm(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc,
                               in_dtype, out_dtype, a_layout, b_layout,
                               ctypes.byref(opts) if opts else None, ws_ptr, ws_bytes, stream))
+
+
+def workspace_size_f64(m: int, n: int, k: int, opts: Optional[Opts] = None) -> int:
+    return int(lib().skg_workspace_size_f64(m, n, k, ctypes.byref(opts) if opts else None))
+
+
+def gemm_f64(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, opts, ws_ptr, ws_bytes,
+             stream) -> int:
+    """skg_gemm_f64: fp64 Stream-K GEMM on device pointers."""
+    return int(lib().skg_gemm_f64(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc,
+                                  ctypes.byref(opts) if opts else None, ws_ptr, ws_bytes,
+                                  stream))
 
 
 def host_staging_size(m, n, k, in_dtype, out_dtype, a_layout=A_ROW, b_layout=B_KMAJOR) -> int:

@@ -173,6 +173,25 @@ def test_host_staging_size_and_argument_errors(lib):
     assert call(staging=16, staging_bytes=want - 1) == skgemm.ERR_WORKSPACE
 
 
+def test_f64_workspace_and_argument_errors(lib):
+    # One 64 x 64 fp64 slot (32 KB) and one flag per CTA after a fixed
+    # header and the report.
+    a = skgemm.workspace_size_f64(1000, 1000, 1000, skgemm.opts_default(grid=1))
+    b = skgemm.workspace_size_f64(1000, 1000, 1000, skgemm.opts_default(grid=148))
+    assert b - a == 147 * 32768 + 512  # flags: 4 -> 592 bytes, rounded to 256
+    assert skgemm.workspace_size_f64(64, 64, 64, skgemm.opts_default(grid=148)) == b
+    o = skgemm.opts_default()
+    call = lambda m=64, n=64, k=64, lda=64, ldb=64, ldc=64, A=16, grid=0: skgemm.gemm_f64(
+        m, n, k, 1.0, A, lda, 16, ldb, 0.0, 16, ldc, skgemm.opts_default(grid=grid), None, 0,
+        None)
+    assert call(m=-1) == skgemm.ERR_ARG
+    assert call(lda=63) == skgemm.ERR_ARG
+    assert call(ldc=32) == skgemm.ERR_ARG
+    assert call(A=None) == skgemm.ERR_ARG
+    assert call(grid=-3) == skgemm.ERR_ARG
+    assert call(m=0) == skgemm.OK
+
+
 # ----------------------------------------------------------------------------
 # Grid-size model (Stream-K page, App. A.1)
 # ----------------------------------------------------------------------------

@@ -3,10 +3,13 @@
 Floating point is compared under the parity tolerance of gpu_util; the
 schedule (device trace) and ABFT decisions are compared exactly.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from oracle import abft_ref as ab
 from oracle import schedule_sim as ss
 from stream_decomposition_abft_gb300 import _build, inputs, skgemm
@@ -709,6 +712,67 @@ def test_mn_major_noalloc_and_matmul():
                              C2.data_ptr(), n, skgemm.IN_BF16, skgemm.OUT_BF16, 1, 1, None,
                              torch.cuda.current_stream().cuda_stream)
     assert st == skgemm.ERR_ARG
+
+
+# --------------------------------------------------------------------------- fp64 Stream-K
+F64_SHAPES = [(64, 64, 16), (100, 70, 33), (300, 500, 257), (1000, 1000, 1000),
+              (128, 128, 4096)]
+
+
+def _f64_problem(m, n, k, seed):
+    gen = torch.Generator().manual_seed(seed)
+    A = torch.rand((m, k), generator=gen, dtype=torch.float64) * 2 - 1
+    B = torch.rand((n, k), generator=gen, dtype=torch.float64) * 2 - 1
+    C0 = torch.rand((m, n), generator=gen, dtype=torch.float64) * 2 - 1
+    return A, B, C0
+
+
+def _run_f64(A, B, C0, alpha, beta, o, ws=None):
+    m, k = A.shape
+    n = B.shape[0]
+    if ws is None:
+        ws = skgemm.Workspace(skgemm.workspace_size_f64(m, n, k, o), "cuda")
+    Ad, Bd, C = A.cuda(), B.cuda(), C0.clone().cuda()
+    st = skgemm.gemm_f64(m, n, k, alpha, Ad.data_ptr(), max(k, 1), Bd.data_ptr(), max(k, 1),
+                         beta, C.data_ptr(), n, o, ws.ptr, ws.nbytes,
+                         torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    return C.cpu(), ws, st
+
+
+@pytest.mark.parametrize("shape", F64_SHAPES)
+@pytest.mark.parametrize("mode", MODES)
+def test_f64_stream_k(shape, mode):
+    # fp64 Stream-K (Stream-K page, §6: FP64 as well as FP16) against the
+    # fp64 oracle on every schedule, a small grid (many peers per tile) and
+    # a full one; the same workspace twice (launch epochs keep old flags
+    # from counting). Only the summation order differs from the oracle:
+    # |C - C_ref| <= 1e-12 sqrt(k) max|A| max|B| (inputs in [-1, 1]).
+    m, n, k = shape
+    A, B, C0 = _f64_problem(m, n, k, seed=m + 3 * n + k)
+    alpha, beta = 1.25, -0.5
+    ref = oracle.gemm(A.numpy(), B.numpy(), alpha, beta, C0.numpy())
+    tol = 1e-12 * math.sqrt(k) + 1e-15
+    for g in (7, sms()):
+        o = skgemm.opts_default(sched=mode, grid=g)
+        ws = None
+        for _ in range(2):
+            C, ws, st = _run_f64(A, B, C0, alpha, beta, o, ws)
+            assert st == skgemm.OK
+            assert float(np.abs(C.numpy() - ref).max()) <= tol, (g, mode)
+        assert ws.report().timeouts == 0
+
+
+def test_f64_k_zero_and_beta_zero():
+    A, B, C0 = _f64_problem(50, 40, 0, seed=5)
+    C, _, st = _run_f64(A, B, C0, 1.0, 3.0, skgemm.opts_default())
+    assert st == skgemm.OK and torch.equal(C, 3.0 * C0)
+    A, B, C0 = _f64_problem(200, 300, 96, seed=6)
+    C0[0, 0] = float("nan")  # beta = 0 does not read C
+    C, _, st = _run_f64(A, B, C0, 2.0, 0.0, skgemm.opts_default(sched="sk", grid=16))
+    assert st == skgemm.OK
+    ref = oracle.gemm(A.numpy(), B.numpy(), 2.0, 0.0, None)
+    assert float(np.abs(C.numpy() - ref).max()) <= 1e-12 * math.sqrt(96)
 
 
 # --------------------------------------------------------------------------- host buffers
