@@ -82,6 +82,19 @@ def test_schedule_query_matches_simulator_random(lib):
         assert got == want, (m, n, k, bn, bk, g, mode)
 
 
+def test_schedule_query_matches_simulator_f64_tiles(lib):
+    # The fp64 kernel's 64 x 64 x 16 tiles run the same schedule code: the
+    # query for those tiles equals the simulator, bit for bit.
+    rnd = random.Random(64)
+    for _ in range(150):
+        m, n, k = rnd.randint(1, 1500), rnd.randint(1, 1500), rnd.randint(1, 4200)
+        g = rnd.randint(1, 160)
+        mode = rnd.choice(list(MODES))
+        got = skgemm.schedule_query(m, n, k, 64, 64, 16, g, MODES[mode])
+        want = ss.flatten(ss.schedule(m, n, k, 64, 64, 16, g, mode=mode))
+        assert got == want, (m, n, k, g, mode)
+
+
 def test_schedule_query_page_example(lib):
     # Stream-K page, Fig. 2b: 384x384x128, BLK_K = 4, g = 4 -> 72 iterations each.
     rows = skgemm.schedule_query(384, 384, 128, 128, 128, 4, 4, skgemm.SCHED_SK)
