@@ -211,3 +211,80 @@ def test_inputs_are_seeded_and_rounded():
     shapes = inputs.random_shapes(1000)
     assert len(shapes) == 1000
     assert all(128 <= d <= 8192 and d % 128 == 0 for s in shapes for d in s)
+
+
+# ----------------------------------------------------------------------------
+# Detection threshold and tile maxima (written out by hand)
+# ----------------------------------------------------------------------------
+def test_default_tau_hand_computed():
+    # tau = 2^-12 * sqrt(k) * sqrt(side) * max|A| * max|B|, values picked so
+    # every factor is a power of two: 2^-12 * 4 * 8 * 2 * 0.5 = 2^-7.
+    assert ab.default_tau(16, 64, 2.0, 0.5) == 2.0 ** -7
+    # side enters under a square root (a row check over 256 columns is twice
+    # the threshold of one over 64), and so does k.
+    assert ab.default_tau(16, 256, 2.0, 0.5) == 2.0 ** -6
+    assert ab.default_tau(64, 64, 2.0, 0.5) == 2.0 ** -6
+    # linear in each maximum
+    assert ab.default_tau(16, 64, 6.0, 0.5) == 3.0 * 2.0 ** -7
+    # k = 1536, side 256 / 128, max 2 and 2: the values the grey-band tests use
+    assert abs(ab.default_tau(1536, 256, 2.0, 2.0) - 2.0 ** -10 * math.sqrt(1536) * 16) < 1e-15
+    assert ab.default_tau(0, 128, 1.0, 1.0) == 0.0
+
+
+def test_tile_maxima_hand_placed():
+    # A stored m x k = 4 x 3, B stored n x k = 6 x 3, tiles of 2 rows of A
+    # and 3 stored rows of B (= 3 output columns).
+    A = np.array([[0.5, -1.0, 0.25],
+                  [0.0, 0.75, -0.5],      # tile tm = 0: max |.| = 1.0
+                  [-4.0, 0.5, 1.0],
+                  [2.0, -3.0, 0.0]])      # tile tm = 1: max |.| = 4.0
+    B = np.array([[1.0, 0.0, -2.0],
+                  [0.5, 0.5, 0.5],
+                  [-1.5, 0.0, 0.0],       # tile tn = 0 (stored rows 0..2): max 2.0
+                  [0.0, -8.0, 0.0],
+                  [0.25, 0.0, 3.0],
+                  [0.0, 0.0, -0.125]])    # tile tn = 1 (stored rows 3..5): max 8.0
+    assert ab.tile_maxima(A, B, 0, 0, 2, 3) == (1.0, 2.0)
+    assert ab.tile_maxima(A, B, 1, 0, 2, 3) == (4.0, 2.0)
+    assert ab.tile_maxima(A, B, 0, 1, 2, 3) == (1.0, 8.0)
+    assert ab.tile_maxima(A, B, 1, 1, 2, 3) == (4.0, 8.0)
+    # A ragged last tile (rows past m are absent, not zero-padded maxima).
+    assert ab.tile_maxima(A, B, 1, 1, 3, 4) == (3.0, 3.0)
+
+
+def test_verify_tile_grey_band_and_patterns():
+    # Integer tile with exact checksums; faults planted by hand.
+    rng = np.random.default_rng(5)
+    C = rng.integers(-20, 21, size=(8, 8)).astype(np.float64)
+    cc, cr = C.sum(axis=0), C.sum(axis=1)
+    clean = ab.verify_tile(C, cr, cc, 0.6, 0.4)
+    assert clean["status"] == ab.CLEAN and clean["bad_rows"] == [] and clean["bad_cols"] == []
+    # |delta| = 0.5 between tau_col = 0.4 and tau_row = 0.6: the column sees
+    # it, the row does not -> one bad column, no bad row, uncorrectable.
+    g = C.copy()
+    g[3, 5] += 0.5
+    res = ab.verify_tile(g, cr, cc, 0.6, 0.4)
+    assert (res["bad_rows"], res["bad_cols"], res["status"]) == ([], [5], ab.UNCORRECTABLE)
+    # Two faults in one row: one bad row, two bad columns.
+    g = C.copy()
+    g[2, 1] += 4.0
+    g[2, 6] -= 8.0
+    res = ab.verify_tile(g, cr, cc, 0.6, 0.4)
+    assert (res["bad_rows"], res["bad_cols"], res["status"]) == ([2], [1, 6], ab.UNCORRECTABLE)
+    # Two faults in one column: two bad rows, one bad column.
+    g = C.copy()
+    g[0, 4] += 4.0
+    g[7, 4] += 4.0
+    res = ab.verify_tile(g, cr, cc, 0.6, 0.4)
+    assert (res["bad_rows"], res["bad_cols"], res["status"]) == ([0, 7], [4], ab.UNCORRECTABLE)
+    # Two faults that cancel in their shared row: the row checksum is clean.
+    g = C.copy()
+    g[6, 0] += 3.0
+    g[6, 2] -= 3.0
+    res = ab.verify_tile(g, cr, cc, 0.6, 0.4)
+    assert (res["bad_rows"], res["bad_cols"], res["status"]) == ([], [0, 2], ab.UNCORRECTABLE)
+    # One fault: corrected back to the clean value from the row checksum.
+    g = C.copy()
+    g[4, 3] = 1e30
+    res = ab.verify_tile(g, cr, cc, 0.6, 0.4)
+    assert (res["status"], res["row"], res["col"], res["value"]) == (ab.CORRECTED, 4, 3, C[4, 3])
