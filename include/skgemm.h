@@ -178,6 +178,28 @@ typedef struct {
                            sums take several times the MMAs' time per k-step
                            on GB300, so 0 (default) and 1 = never, 2 =
                            whenever the shape allows it. */
+  int32_t inject2_tile; /* a second injected flip for testing, in the same
+                           form as inject_*: < 0 = none. Two flips in one
+                           tile make the mismatch pattern the single-fault
+                           rule cannot correct; in two tiles, two corrections */
+  int32_t inject2_row;
+  int32_t inject2_col;
+  int32_t inject2_bit;
+  int32_t inject_kstep; /* < 0 (default): the inject_* flip is applied to the
+                           fixed-up accumulator just before the check. >= 0:
+                           it is applied inside the mainloop instead, in TMEM,
+                           right after the MMAs of the tile's MAC iteration
+                           inject_kstep (0 <= inject_kstep < ceil(k / 64)),
+                           to the partial accumulator of the CTA that runs
+                           that iteration; later iterations and the Stream-K
+                           fixup then add onto the faulty value. inject2_* is
+                           always applied before the check. */
+  int32_t stagger;      /* StaggerU-style k-offset staggering: 0 or 1 = off;
+                           s > 1 = CTA x starts each of its work items at
+                           MAC iteration ((x mod s) * n) / s of the item's n
+                           iterations and wraps around to its first one, so
+                           CTAs that read the same operand columns do not all
+                           start at the same k. Sums are re-associated only. */
 } skg_opts_t;
 
 /* One segment of a schedule (Stream-K page, Algorithm 5 / §5.2). k_iter_*
@@ -222,9 +244,12 @@ typedef struct {
   uint32_t n_records;     /* records written (at most SKG_MAX_RECORDS kept) */
   float max_ratio_row;    /* largest |row mismatch| / tau_row over rows that passed */
   float max_ratio_col;    /* same for columns */
-  float tau_row;          /* thresholds used by the latest ABFT launch */
+  float tau_row;          /* largest thresholds used by the ABFT launches */
   float tau_col;
-  uint32_t reserved[4];
+  uint32_t mid_injected;  /* mid-mainloop flips applied (skg_opts_t.inject_kstep) */
+  float mid_before;       /* the partial accumulator value the latest one flipped */
+  float mid_after;        /* and the value it left in TMEM */
+  uint32_t reserved;
   skg_fault_record_t records[SKG_MAX_RECORDS];
 } skg_report_t;
 
@@ -248,8 +273,11 @@ size_t skg_workspace_size_layout(int64_t m, int64_t n, int64_t k, int32_t a_layo
                                  int32_t b_layout, const skg_opts_t* opts);
 
 /* Zero a workspace (`bytes` from skg_workspace_size) before its first use.
- * Afterwards the library keeps it consistent itself (flags carry a launch
- * epoch, so they never need clearing). Asynchronous on `stream`. */
+ * Afterwards the library keeps it consistent itself, also when the same
+ * workspace serves calls of other shapes and options (large enough for each):
+ * the header, report and flags sit at fixed offsets and the flags carry a
+ * launch epoch, so they never need clearing, and every other region is
+ * written by a call before that call reads it. Asynchronous on `stream`. */
 skg_status_t skg_workspace_init(void* workspace, size_t bytes, void* stream);
 
 /* C = alpha * A B + beta * C, asynchronous on `stream`.
@@ -371,17 +399,27 @@ skg_status_t skg_report_read(const void* workspace, skg_report_t* out, int32_t r
  * SKG_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU loading the library
  * holds until exit; nothing is allocated per call. The first call on a
  * device sets that device up (looks up the array's address and clears its
- * header on `stream`), so make it before any stream capture. All calls
- * share the array and it keeps the last call's contents: calls whose
- * launches overlap on the GPU race and must not be issued. BLK_N defaults
- * to 128 here; a shape or option set whose workspace exceeds the array
- * returns SKG_ERR_WORKSPACE (ABFT does on a 152-SM GPU). Device-side
- * outcomes are not reported through this entry point. Other arguments as
- * for skg_gemm. */
+ * header, report and flags on `stream`), so make it before any stream
+ * capture. All calls share the array and it keeps the last call's contents;
+ * calls of different shapes and options may follow each other, but calls
+ * whose launches overlap on the GPU race and must not be issued. BLK_N
+ * defaults to 128 here (unless opts asks for CTA pairs). A shape or option
+ * set whose workspace exceeds the array returns SKG_ERR_WORKSPACE: on a
+ * 152-SM GB300 that is every ABFT call with opts->grid = 0 (its checksum
+ * GEMMs may use every SM, about 40 MB of partial slots); ABFT with a small
+ * explicit grid fits. Device-side outcomes are read with
+ * skg_noalloc_report_read. Other arguments and errors as for skg_gemm. */
 skg_status_t skg_gemm_noalloc(int64_t m, int64_t n, int64_t k, float alpha, const void* A,
                               int64_t lda, const void* B, int64_t ldb, float beta, void* C,
                               int64_t ldc, int32_t in_dtype, int32_t out_dtype, int32_t a_layout,
                               int32_t b_layout, const skg_opts_t* opts, void* stream);
+
+/* skg_report_read for the current device's skg_gemm_noalloc array: copies
+ * its report (timeouts, ABFT detections and corrections of every noalloc
+ * call since the last reset) to host memory after synchronising `stream`;
+ * reset != 0 also clears it. Sets the device up like skg_gemm_noalloc's
+ * first call when that has not happened yet. */
+skg_status_t skg_noalloc_report_read(skg_report_t* out, int32_t reset, void* stream);
 
 /* Bytes of device staging memory skg_gemm_host needs for this problem:
  * packed device copies of A and B as stored (rows rounded up to 16 bytes)

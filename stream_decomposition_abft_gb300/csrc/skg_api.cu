@@ -73,7 +73,9 @@ struct Resolved {
   int bn;
   int abft;
   float tau_row, tau_col;
-  int inject_tile, inject_row, inject_col, inject_bit;
+  int inj_tile[2], inj_row[2], inj_col[2], inj_bit[2];  // testing: up to two flips
+  int inj_kb;   // >= 0: flip 0 inside the mainloop after this MAC iteration
+  int stagger;  // StaggerU-style k staggering (> 1 = on)
   uint64_t timeout_ns;
   int32_t* trace;
   uint64_t* cta_clock;
@@ -139,17 +141,32 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
     r.sched = pp.sched;
     r.grid = 2 * pp.grid;
   }
-  r.ws_grid = r.abft ? (ms > r.grid ? ms : r.grid) : r.grid;
+  // With ABFT the checksum GEMMs may use every SM unless the caller fixes
+  // the grid, which then bounds every launch of the call.
+  r.ws_grid = (r.abft && o->grid == 0) ? (ms > r.grid ? ms : r.grid) : r.grid;
   r.k_for_plan = k > 0 ? k : 1;  // ABFT checksum GEMMs may use up to every SM
   r.tau_row = o->tau_row;
   r.tau_col = o->tau_col;
-  r.inject_tile = o->inject_tile;
-  r.inject_row = o->inject_row;
-  r.inject_col = o->inject_col;
-  r.inject_bit = o->inject_bit;
-  if (r.inject_tile >= 0 && (r.inject_row < 0 || r.inject_row >= kBM || r.inject_col < 0 ||
-                             r.inject_col >= r.bn || r.inject_bit < 0 || r.inject_bit > 31))
-    return SKG_ERR_ARG;
+  const int32_t it[2] = {o->inject_tile, o->inject2_tile};
+  const int32_t ir[2] = {o->inject_row, o->inject2_row};
+  const int32_t ic[2] = {o->inject_col, o->inject2_col};
+  const int32_t ib[2] = {o->inject_bit, o->inject2_bit};
+  for (int sl = 0; sl < 2; ++sl) {
+    r.inj_tile[sl] = it[sl] >= 0 ? it[sl] : -1;
+    r.inj_row[sl] = ir[sl];
+    r.inj_col[sl] = ic[sl];
+    r.inj_bit[sl] = ib[sl];
+    if (r.inj_tile[sl] >= 0 && (ir[sl] < 0 || ir[sl] >= kBM || ic[sl] < 0 || ic[sl] >= r.bn ||
+                                ib[sl] < 0 || ib[sl] > 31))
+      return SKG_ERR_ARG;
+  }
+  r.inj_kb = -1;
+  if (o->inject_kstep >= 0 && r.inj_tile[0] >= 0) {
+    if (o->inject_kstep >= (k + kBK - 1) / kBK) return SKG_ERR_ARG;
+    r.inj_kb = o->inject_kstep;
+  }
+  if (o->stagger < 0) return SKG_ERR_ARG;
+  r.stagger = o->stagger;
   r.timeout_ns = o->timeout_ns ? o->timeout_ns : kDefaultTimeoutNs;
   r.trace = o->trace;
   r.cta_clock = o->cta_clock;
@@ -168,6 +185,7 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
       (o->sched == SKG_SCHED_AUTO || o->sched == SKG_SCHED_DP)) {
     const int64_t tiles = ((m + kBM - 1) / kBM) * ((n + 127) / 128);
     const bool fits = tiles <= ms && (o->grid == 0 || o->grid >= tiles);
+    if (fits && r.inj_kb >= 0) return SKG_ERR_UNSUPPORTED;  // epilogue reads every stage
     if (fits) {
       r.abft_local = 1;
       r.bn = 128;
@@ -176,19 +194,27 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
       r.pair = 0;
       r.grid_max = ms;
       r.grid_ck = 0;
-      r.ws_grid = ms > r.grid ? ms : r.grid;
+      const int bound = o->grid > 0 ? o->grid : ms;
+      r.ws_grid = bound > r.grid ? bound : r.grid;
     }
   }
   return SKG_OK;
 }
 
-// Workspace layout. Partial-tile slots are sized for the widest tile any
-// launch of the call uses (the ABFT checksum GEMMs may use BLK_N = 256).
+// Workspace layout. The header, the report and the flags (two regions of
+// kMaxCtas) sit at fixed offsets for every shape and option set, so a
+// workspace reused for another call finds only flags where its flags lie
+// (their epochs keep them valid across launches). Everything after them is
+// written by the call before the call reads it. Partial-tile slots are sized
+// for the widest tile any launch of the call uses (the ABFT checksum GEMMs
+// may use BLK_N = 256).
 struct Layout {
-  size_t flags, partials, sums, enc_a, enc_b, stat, pub, umax, cr, cc, total;
+  size_t flags, partials, sums, enc_a, enc_b, pub, umax, cr, cc, total;
   int kp, tiles_a, tiles_b;
   int64_t ld_cr, ld_cc;
 };
+
+constexpr size_t kFlagBytes = 2 * (size_t)kMaxCtas * 4;
 
 Layout layout(int64_t m, int64_t n, int64_t k, const Resolved& r) {
   Layout L;
@@ -197,7 +223,7 @@ Layout layout(int64_t m, int64_t n, int64_t k, const Resolved& r) {
   // flags and partial slots of its own.
   const size_t regions = r.abft ? 2 : 1;
   L.flags = off;
-  off = round_up(off + regions * r.ws_grid * 4, 256);
+  off += kFlagBytes;
   L.partials = off;
   const int slot_n = r.abft ? 256 : r.bn;
   off = round_up(off + regions * r.ws_grid * kBM * slot_n * 4, 256);
@@ -206,7 +232,7 @@ Layout layout(int64_t m, int64_t n, int64_t k, const Resolved& r) {
   L.tiles_b = (int)((n + r.bn - 1) / r.bn);
   L.ld_cr = (int64_t)round_up((size_t)kEncRows * L.tiles_b, 4);
   L.ld_cc = (int64_t)round_up((size_t)kEncRows * L.tiles_a, 4);
-  L.sums = L.enc_a = L.enc_b = L.stat = L.pub = L.umax = L.cr = L.cc = off;
+  L.sums = L.enc_a = L.enc_b = L.pub = L.umax = L.cr = L.cc = off;
   if (r.abft) {
     const size_t tiles = (size_t)L.tiles_a + L.tiles_b;
     const size_t groups = (size_t)((m + kBM - 1) / kBM + (n + kBM - 1) / kBM);
@@ -216,8 +242,6 @@ Layout layout(int64_t m, int64_t n, int64_t k, const Resolved& r) {
     off = round_up(off + (size_t)kEncRows * L.tiles_a * L.kp * 2, 256);
     L.enc_b = off;
     off = round_up(off + (size_t)kEncRows * L.tiles_b * L.kp * 2, 256);
-    L.stat = off;
-    off = round_up(off + tiles * sizeof(TileStat), 256);
     L.pub = off;
     off = round_up(off + tiles * sizeof(TilePub), 256);
     L.umax = off;
@@ -259,8 +283,7 @@ skg_status_t run_encode(int32_t in_dtype, const void* A, int64_t lda, int64_t m,
                CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
     return SKG_ERR_UNSUPPORTED;
   return launch_encode(in_dtype == SKG_IN_BF16, ma, mb, (int)m, (int)n, L.kp, r.bn, sms,
-                       (float*)(ws + L.sums), ws + L.enc_a, ws + L.enc_b, (TileStat*)(ws + L.stat),
-                       (TilePub*)(ws + L.pub), (float*)(ws + L.umax), (skg_report_t*)(ws + 256),
+                       (float*)(ws + L.sums), ws + L.enc_a, ws + L.enc_b, (TilePub*)(ws + L.pub), (float*)(ws + L.umax), (skg_report_t*)(ws + 256),
                        r.timeout_ns,
                        stream) == cudaSuccess
              ? SKG_OK
@@ -281,7 +304,6 @@ skg_status_t run_encode_layouts(int32_t in_dtype, const void* A, int64_t lda, in
   float* sums = (float*)(ws + L.sums);
   float* umax = (float*)(ws + L.umax);
   TilePub* pub = (TilePub*)(ws + L.pub);
-  TileStat* stat = (TileStat*)(ws + L.stat);
   const CUtensorMapDataType in_t = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   cudaError_t e;
@@ -294,7 +316,7 @@ skg_status_t run_encode_layouts(int32_t in_dtype, const void* A, int64_t lda, in
                  kEncBoxRows, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
       return SKG_ERR_UNSUPPORTED;
     e = launch_encode(bf16, ma, ma, (int)m, 0, L.kp, r.bn, sms, sums, ws + L.enc_a, ws + L.enc_b,
-                      stat, pub, umax, (skg_report_t*)(ws + 256), r.timeout_ns, stream);
+                      pub, umax, (skg_report_t*)(ws + 256), r.timeout_ns, stream);
   }
   if (e != cudaSuccess) return SKG_ERR_CUDA;
   const int ta = L.tiles_a;
@@ -307,7 +329,7 @@ skg_status_t run_encode_layouts(int32_t in_dtype, const void* A, int64_t lda, in
                  kEncBoxRows, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
       return SKG_ERR_UNSUPPORTED;
     e = launch_encode(bf16, mb, mb, 0, (int)n, L.kp, r.bn, sms, sums + (size_t)ta * L.kp,
-                      ws + L.enc_a, ws + L.enc_b, stat + ta, pub + ta,
+                      ws + L.enc_a, ws + L.enc_b, pub + ta,
                       umax + (size_t)ta * slices, (skg_report_t*)(ws + 256), r.timeout_ns,
                       stream);
   }
@@ -418,6 +440,7 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   p.s = make_schedule(g.m, g.n, g.k, r.pair ? 2 * kBM : kBM, r.bn, kBK, sched_ctas, r.sched, t_ck,
                       t_ck ? r.grid_ck : 0);
   const int launch_grid = r.grid + p.s.g_ck;
+  if (launch_grid > kMaxCtas) return SKG_ERR_UNSUPPORTED;  // flags per region
   // Banded raster: a wave of g tiles covers about (g / band) rows x band
   // columns; band ~ sqrt(g * BLK_M / BLK_N) minimises the A + B bytes one
   // wave touches per k-step.
@@ -482,10 +505,14 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   }
   p.tau_row = r.tau_row;
   p.tau_col = r.tau_col;
-  p.inject_tile = r.inject_tile;
-  p.inject_row = r.inject_row;
-  p.inject_col = r.inject_col;
-  p.inject_bit = r.inject_bit;
+  for (int sl = 0; sl < 2; ++sl) {
+    p.inj_tile[sl] = r.inj_tile[sl];
+    p.inj_row[sl] = r.inj_row[sl];
+    p.inj_col[sl] = r.inj_col[sl];
+    p.inj_bit[sl] = r.inj_bit[sl];
+  }
+  p.inj_kb = r.inj_kb;
+  p.stagger = r.stagger;
   p.timeout_ns = r.timeout_ns;
   p.trace = r.trace;
   p.cta_clock = r.cta_clock;
@@ -530,7 +557,9 @@ skg_status_t reference_checksums(const Gemm& g, const Resolved& r, uint8_t* ws, 
   Resolved rc = r;
   rc.abft = 0;
   rc.pair = 0;
-  rc.inject_tile = -1;
+  rc.inj_tile[0] = rc.inj_tile[1] = -1;
+  rc.inj_kb = -1;
+  rc.stagger = 0;
   rc.trace = nullptr;
   rc.cta_clock = nullptr;
   rc.drop_signal = -1;
@@ -789,6 +818,31 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
 
 }  // namespace
 
+namespace skg {
+
+skg_status_t workspace_need(int64_t m, int64_t n, int64_t k, int32_t a_layout, int32_t b_layout,
+                            const skg_opts_t* opts, size_t* need) {
+  if (!layout_valid(a_layout, b_layout)) return SKG_ERR_ARG;
+  if (m < 0 || n < 0 || k < 0) return SKG_ERR_ARG;
+  Resolved r;
+  const int sms = sm_count_cached();
+  const skg_status_t st = resolve(m, n, k, opts, r, sms);
+  if (st != SKG_OK) return st;
+  const Layout L = layout(m, n, k, r);
+  // The copies are planned for bf16, the input type for which they can be
+  // chosen (abft_wants_copies), so the size covers either type.
+  const bool copies = (a_layout == SKG_A_COL || b_layout == SKG_B_NMAJOR) &&
+                      abft_wants_copies(m, n, opts, SKG_IN_BF16, r, L);
+  *need = relayout_plan(m, n, k, copy_layout_a(a_layout, copies),
+                        copy_layout_b(b_layout, copies), L.total)
+              .total;
+  return SKG_OK;
+}
+
+size_t fixed_header_bytes() { return kHeaderBytes + kFlagBytes; }
+
+}  // namespace skg
+
 extern "C" {
 
 void skg_opts_default(skg_opts_t* o) {
@@ -796,6 +850,8 @@ void skg_opts_default(skg_opts_t* o) {
   memset(o, 0, sizeof(*o));
   o->sched = SKG_SCHED_AUTO;
   o->inject_tile = -1;
+  o->inject2_tile = -1;
+  o->inject_kstep = -1;
 }
 
 size_t skg_workspace_size(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts) {
@@ -808,19 +864,8 @@ size_t skg_workspace_size(int64_t m, int64_t n, int64_t k, const skg_opts_t* opt
 
 size_t skg_workspace_size_layout(int64_t m, int64_t n, int64_t k, int32_t a_layout,
                                  int32_t b_layout, const skg_opts_t* opts) {
-  if (!layout_valid(a_layout, b_layout)) return 0;
-  if (m < 0 || n < 0 || k < 0) return 0;
-  Resolved r;
-  const int sms = sm_count_cached();
-  if (resolve(m, n, k, opts, r, sms) != SKG_OK) return 0;
-  const Layout L = layout(m, n, k, r);
-  // The copies are planned for bf16, the input type for which they can be
-  // chosen (abft_wants_copies), so the size covers either type.
-  const bool copies = (a_layout == SKG_A_COL || b_layout == SKG_B_NMAJOR) &&
-                      abft_wants_copies(m, n, opts, SKG_IN_BF16, r, L);
-  return relayout_plan(m, n, k, copy_layout_a(a_layout, copies),
-                       copy_layout_b(b_layout, copies), L.total)
-      .total;
+  size_t need = 0;
+  return skg::workspace_need(m, n, k, a_layout, b_layout, opts, &need) == SKG_OK ? need : 0;
 }
 
 skg_status_t skg_workspace_init(void* workspace, size_t bytes, void* stream) {

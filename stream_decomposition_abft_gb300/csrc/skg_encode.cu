@@ -23,10 +23,10 @@
 // when its last box is in.
 //   - bf16 has the exponent range of fp32: the unit writes its hi / lo terms
 //     directly and the tile's scale is 2^0. No CTA waits for another.
-//   - fp16: the unit stores its fp32 sums and folds its largest |sum| into
-//     the tile's; the last unit of the tile to finish (per-tile counter)
-//     picks the tile's scale, converts the tile's sums to hi / lo terms and
-//     resets the tile's scratch for the next launch.
+//   - fp16: the unit stores its fp32 sums; a second, short kernel
+//     (encode_finish_kernel) then picks each tile's scale from its largest
+//     |sum| and writes the tile's hi / lo terms. No state survives a pass, so
+//     a workspace needs nothing cleared between calls of any shape.
 // Every unit also stores its largest |element|; the main kernel's epilogue
 // takes a tile's maximum (for the default threshold) over its units. Every
 // wait is bounded; on expiry the kernel records a pipeline timeout in the
@@ -75,6 +75,9 @@ constexpr int kEncLanesPerRow = kEncSliceCols / kEncColsPerThread;
 constexpr int kEncRowsPerPass = kEncWorkerThreads / kEncLanesPerRow;
 static_assert(kEncBoxRows % kEncRowsPerPass == 0, "whole passes per box");
 constexpr size_t kEncSmem = 1024 + (size_t)kEncStages * kEncStageBytes + kEncPartBytes + 256;
+// Block size of the row-segment encode of MN-major operands and of the
+// fp16 finishing pass.
+constexpr int kMnEncThreads = 512;
 
 int encode_slices(int kp) { return (kp + kEncSliceCols - 1) / kEncSliceCols; }
 
@@ -154,7 +157,6 @@ struct EncParams {
   float* sums;
   void* enc_a;
   void* enc_b;
-  TileStat* stat;
   TilePub* pub;
   float* umax;
   skg_report_t* report;
@@ -182,9 +184,7 @@ __global__ void __launch_bounds__(kEncThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(part + kEncWorkers * kEncSliceCols);
   uint64_t* empty = full + kEncStages;
   int* abort_flag = reinterpret_cast<int*>(empty + kEncStages);
-  int* last_unit = abort_flag + 1;
   float* wmax = reinterpret_cast<float*>(abort_flag + 2);  // [workers]
-  float* wsmax = wmax + kEncWorkers;                        // [workers]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -262,9 +262,6 @@ __global__ void __launch_bounds__(kEncThreads, 1)
   const int rsub = wt / kEncLanesPerRow;  // first row of this thread in a box
   int stage = 0;
   uint32_t phase = 0;
-  // fp16: running max |sum| and unit count of the current tile (thread 0).
-  float run_smax = 0.f;
-  int run_units = 0;
   for (int u = u_begin; u < u_end; ++u) {
     const int t = u / p.slices, sl = u - t * p.slices;
     const bool is_a = t < p.tiles_a;
@@ -336,66 +333,17 @@ __global__ void __launch_bounds__(kEncThreads, 1)
       float x = 0.f;
 #pragma unroll
       for (int w = 0; w < kEncWorkers; ++w) x += part[w * kEncSliceCols + wt];
-      float smax = 0.f;
       if (col < p.kp) {  // columns in [k, kp) hold zero sums
         if constexpr (kScaled) {
           __stcg(p.sums + (int64_t)t * p.kp + col, x);
-          smax = fabsf(x);
         } else {
           const T hi = from_f<T>(x);
           hi_row[col] = hi;
           lo_row[col] = from_f<T>(x - to_f<T>(hi));
         }
       }
-      if constexpr (kScaled) {
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-          smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, off));
-        if (lane == 0) wsmax[ww] = smax;
-      }
     }
-    named_bar_sync(1, kEncWorkerThreads);
-    if constexpr (kScaled) {
-      // wsmax and part are rewritten only after the next unit's first barrier.
-      if (wt == 0)
-        for (int w = 0; w < kEncSliceCols / 32; ++w) run_smax = fmaxf(run_smax, wsmax[w]);
-      ++run_units;
-      // Hand this CTA's share of the tile to the tile's counter when the tile
-      // ends here (next unit is another tile, or the range ends).
-      const bool tile_ends = (u + 1 == u_end) || ((u + 1) / p.slices != t);
-      if (!tile_ends) continue;
-      if (wt < kEncSliceCols) __threadfence();  // this tile's sums before the counter
-      named_bar_sync(1, kEncWorkerThreads);
-      if (wt == 0) {
-        // Non-negative floats order like their bit patterns.
-        atomicMax(&p.stat[t].encmax_bits, __float_as_uint(run_smax));
-        const uint32_t before = atom_add_acq_rel_gpu(&p.stat[t].count, (uint32_t)run_units);
-        *last_unit = before + (uint32_t)run_units == (uint32_t)p.slices ? 1 : 0;
-      }
-      run_smax = 0.f;
-      run_units = 0;
-      named_bar_sync(1, kEncWorkerThreads);
-      if (*last_unit) {
-        // Last share of this tile: every slice's sums and maxima are in.
-        __threadfence();
-        const float emax = __uint_as_float(atomicAdd(&p.stat[t].encmax_bits, 0u));
-        int ex = 0;
-        if (emax > 0.f) frexpf(emax, &ex);
-        const int e = (emax > 0.f) ? 15 - ex : 0;  // emax * 2^e in [2^14, 2^15)
-        const float* tsums = p.sums + (int64_t)t * p.kp;
-        for (int c = wt * kEncColsPerThread; c < p.kp; c += kEncWorkerThreads * kEncColsPerThread) {
-          const float4 a = __ldcg(reinterpret_cast<const float4*>(tsums + c));
-          const float4 b = __ldcg(reinterpret_cast<const float4*>(tsums + c + 4));
-          const float x[kEncColsPerThread] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-          split_store<T>(hi_row, lo_row, c, x, e);
-        }
-        if (wt == 0) {
-          p.pub[t].scale_exp = e;
-          p.stat[t].encmax_bits = 0;
-          p.stat[t].count = 0;
-        }
-      }
-    }
+    named_bar_sync(1, kEncWorkerThreads);  // part is rewritten by the next unit
   }
 }
 
@@ -417,9 +365,14 @@ cudaError_t launch_encode_t(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
                     p);
 }
 
+template <typename T>
+__global__ void __launch_bounds__(kMnEncThreads)
+    encode_finish_kernel(const float* __restrict__ sums, int tiles_a, int tiles, int kp,
+                         T* __restrict__ enc_a, T* __restrict__ enc_b, TilePub* __restrict__ pub);
+
 cudaError_t launch_encode(int in_bf16, const CUtensorMap& tmA, const CUtensorMap& tmB, int m,
                           int n, int kp, int bn, int sms, float* sums, void* enc_a, void* enc_b,
-                          TileStat* stat, TilePub* pub, float* umax, skg_report_t* report,
+                          TilePub* pub, float* umax, skg_report_t* report,
                           uint64_t timeout_ns, cudaStream_t stream) {
   EncParams p;
   p.kp = kp;
@@ -430,7 +383,6 @@ cudaError_t launch_encode(int in_bf16, const CUtensorMap& tmA, const CUtensorMap
   p.sums = sums;
   p.enc_a = enc_a;
   p.enc_b = enc_b;
-  p.stat = stat;
   p.pub = pub;
   p.umax = umax;
   p.report = report;
@@ -438,8 +390,15 @@ cudaError_t launch_encode(int in_bf16, const CUtensorMap& tmA, const CUtensorMap
   const int64_t units = (int64_t)(p.tiles_a + p.tiles_b) * p.slices;
   const int grid = (int)(units < sms ? units : sms);
   if (grid <= 0) return cudaSuccess;
-  return in_bf16 ? launch_encode_t<__nv_bfloat16>(tmA, tmB, p, grid, stream)
-                 : launch_encode_t<__half>(tmA, tmB, p, grid, stream);
+  if (in_bf16) return launch_encode_t<__nv_bfloat16>(tmA, tmB, p, grid, stream);
+  // fp16: the sums, then each tile's scale and hi / lo terms.
+  const cudaError_t e = launch_encode_t<__half>(tmA, tmB, p, grid, stream);
+  if (e != cudaSuccess) return e;
+  const int tiles = p.tiles_a + p.tiles_b;
+  const int grid2 = tiles < 4 * sms ? tiles : 4 * sms;
+  return launch_pdl(encode_finish_kernel<__half>, dim3(grid2), dim3(kMnEncThreads), 0, stream,
+                    static_cast<const float*>(sums), p.tiles_a, tiles, kp,
+                    static_cast<__half*>(enc_a), static_cast<__half*>(enc_b), pub);
 }
 
 // ----------------------------------------------------------------------------
@@ -456,7 +415,6 @@ cudaError_t launch_encode(int in_bf16, const CUtensorMap& tmA, const CUtensorMap
 // 16 warps per unit, up to four blocks per SM: 32 KB of loads in flight
 // per block (measured against 8 and 32 warps: best at 4096^3, within 5 % of
 // the best at 8192^3).
-constexpr int kMnEncThreads = 512;
 constexpr int kMnEncUnroll = 4;
 
 template <typename T>
@@ -544,9 +502,12 @@ __global__ void __launch_bounds__(kMnEncThreads)
   }
 }
 
+// Tiles [0, tiles_a) write their rows to enc_a, tiles [tiles_a, tiles) to
+// enc_b (row t - tiles_a); sums and pub are indexed by t.
 template <typename T>
 __global__ void __launch_bounds__(kMnEncThreads)
-    encode_finish_kernel(const float* __restrict__ sums, int tiles, int kp, T* __restrict__ enc,
+    encode_finish_kernel(const float* __restrict__ sums, int tiles_a, int tiles, int kp,
+                         T* __restrict__ enc_a, T* __restrict__ enc_b,
                          TilePub* __restrict__ pub) {
   constexpr bool kScaled = std::is_same<T, __half>::value;
   __shared__ float wmax[kMnEncThreads / 32];
@@ -570,7 +531,8 @@ __global__ void __launch_bounds__(kMnEncThreads)
       if (emax > 0.f) frexpf(emax, &ex);
       e = (emax > 0.f) ? 15 - ex : 0;  // emax * 2^e in [2^14, 2^15)
     }
-    T* hi_row = enc + (int64_t)(kEncRows * t) * kp;
+    T* hi_row = t < tiles_a ? enc_a + (int64_t)(kEncRows * t) * kp
+                            : enc_b + (int64_t)(kEncRows * (t - tiles_a)) * kp;
     T* lo_row = hi_row + kp;
     for (int c = threadIdx.x * kEncColsPerThread; c < kp; c += kMnEncThreads * kEncColsPerThread) {
       float x[kEncColsPerThread];
@@ -598,7 +560,8 @@ cudaError_t launch_encode_mn_t(const void* src, int64_t ld, int64_t rows, int64_
                              umax, static_cast<T*>(enc), pub);
   if (e != cudaSuccess || !std::is_same<T, __half>::value) return e;
   return launch_pdl(encode_finish_kernel<T>, dim3(grid2), dim3(kMnEncThreads), 0, stream,
-                    static_cast<const float*>(sums), tiles, kp, static_cast<T*>(enc), pub);
+                    static_cast<const float*>(sums), tiles, tiles, kp, static_cast<T*>(enc),
+                    static_cast<T*>(enc), pub);
 }
 
 cudaError_t launch_encode_mn(int in_bf16, const void* src, int64_t ld, int64_t rows, int64_t k,

@@ -195,14 +195,20 @@ int f64_sched(const skg_opts_t* o) {
 
 using namespace skg;
 
+namespace {
+// Workspace of the fp64 kernel: header, report, then kMaxCtas flags at a
+// fixed place (a workspace reused for another shape or grid finds only flags
+// there), then the partial-tile slots.
+size_t f64_flags_offset() { return kF64Report + ((sizeof(skg_report_t) + 255) / 256) * 256; }
+size_t f64_slots_offset() { return f64_flags_offset() + (size_t)kMaxCtas * 4; }
+}  // namespace
+
 extern "C" {
 
 size_t skg_workspace_size_f64(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts) {
   if (m < 0 || n < 0 || k < 0) return 0;
   const size_t g = (size_t)f64_grid(opts, skg_device_sm_count());
-  const size_t flags = kF64Report + ((sizeof(skg_report_t) + 255) / 256) * 256;
-  const size_t slots = flags + ((g * 4 + 255) / 256) * 256;
-  return slots + g * kF64SlotBytes;
+  return f64_slots_offset() + g * kF64SlotBytes;
 }
 
 skg_status_t skg_gemm_f64(int64_t m, int64_t n, int64_t k, double alpha, const double* A,
@@ -244,8 +250,9 @@ skg_status_t skg_gemm_f64(int64_t m, int64_t n, int64_t k, double alpha, const d
   p.C = C;
   p.ldc = ldc;
   uint8_t* ws = (uint8_t*)workspace;
-  const size_t flags = kF64Report + ((sizeof(skg_report_t) + 255) / 256) * 256;
-  const size_t slots = flags + (((size_t)g * 4 + 255) / 256) * 256;
+  const size_t flags = f64_flags_offset();
+  const size_t slots = f64_slots_offset();
+  if (g > kMaxCtas) return SKG_ERR_UNSUPPORTED;
   p.hdr = (uint32_t*)ws;
   p.report = (skg_report_t*)(ws + kF64Report);
   p.flags = (uint32_t*)(ws + flags);

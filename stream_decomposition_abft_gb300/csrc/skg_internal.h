@@ -70,12 +70,12 @@ int pair_clusters_resident();
 // `pub` and the max |element| of every unit (tile x slice) in `umax` (A tiles
 // first). tmA / tmB map A (k x m) and the stored B (k x n) with
 // kEncBoxCols x kEncBoxRows boxes and no swizzle. `sums` is fp32 scratch,
-// (tiles_a + tiles_b) x kp (fp16 only); `stat` is scratch that must start at
-// zero and is left at zero. A wait that times out sets
-// SKG_ERR_PIPELINE_TIMEOUT in `report`.
+// (tiles_a + tiles_b) x kp (fp16 only: a second kernel turns it into the
+// scaled hi / lo rows). A wait that times out sets SKG_ERR_PIPELINE_TIMEOUT
+// in `report`.
 cudaError_t launch_encode(int in_bf16, const CUtensorMap& tmA, const CUtensorMap& tmB, int m,
                           int n, int kp, int bn, int sms, float* sums, void* enc_a, void* enc_b,
-                          TileStat* stat, TilePub* pub, float* umax, skg_report_t* report,
+                          TilePub* pub, float* umax, skg_report_t* report,
                           uint64_t timeout_ns, cudaStream_t stream);
 
 // k-columns and rows of one encode box (one work unit covers kEncBoxCols
@@ -113,5 +113,14 @@ cudaError_t launch_relayout(const void* src, int64_t ld_src, int64_t rows, int64
 // C = beta * C for k == 0 (skg_encode.cu).
 cudaError_t launch_scale(int out_dtype, void* C, int64_t ldc, int m, int n, float beta,
                          cudaStream_t stream);
+
+// skg_workspace_size_layout with the reason when there is no size: the
+// status resolve() gives for the options (SKG_ERR_ARG, SKG_ERR_UNSUPPORTED).
+skg_status_t workspace_need(int64_t m, int64_t n, int64_t k, int32_t a_layout, int32_t b_layout,
+                            const skg_opts_t* opts, size_t* need);
+
+// Bytes at the start of every workspace that must be zero before its first
+// use: the header with the report, and the flags (skg_workspace_init).
+size_t fixed_header_bytes();
 
 }  // namespace skg

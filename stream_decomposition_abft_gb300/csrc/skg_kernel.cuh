@@ -76,6 +76,11 @@ constexpr int kEncRows = 2;  // hi and lo terms of each encoding
 constexpr int kFixSlots = 6;  // per epilogue warp: staged partial pieces in flight
 constexpr int kAuxBytes = 1024;  // shared-memory bookkeeping (struct Aux) after the staging
 constexpr uint32_t kSmemLimit = 232448;
+// Flags per fixup region. The flag array has a fixed place and size in every
+// workspace (two regions of kMaxCtas), so a workspace reused for another
+// shape or option set never finds other data where its flags now lie; a
+// launch uses at most kMaxCtas CTAs.
+constexpr int kMaxCtas = 1024;
 
 // Workspace header (device). The report follows at offset 256.
 // The epoch is advanced once per launch by the CTA that takes the launch's
@@ -91,14 +96,8 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
-// ABFT encode pass, per operand tile (fp16 inputs only): the running max
-// |encoding| and a unit counter (scratch, left at zero after every pass) ...
-struct TileStat {
-  uint32_t encmax_bits;  // max |encoding| over the tile (fp32 bits)
-  uint32_t count;        // units of the tile finished
-  uint32_t pad[2];
-};
-// ... and what the pass publishes for the main kernel's epilogue.
+// What the ABFT encode pass publishes per operand tile for the main
+// kernel's epilogue.
 struct TilePub {
   int32_t scale_exp;  // the tile's encodings are stored scaled by 2^scale_exp
   int32_t pad;
@@ -117,9 +116,10 @@ struct KernelParams {
   int32_t a_mn, b_mn;
   WsHeader* hdr;
   skg_report_t* report;
-  // Fixup storage: region 0 (output tiles) uses flags[0, ws_ctas) and
-  // partial slots [0, ws_ctas); region 1 (fused checksum tiles) the next
-  // ws_ctas of each. Slot x holds kBM x BN fp32 values.
+  // Fixup storage: region 0 (output tiles) uses flags[0, kMaxCtas) and
+  // partial slots [0, ws_ctas); region 1 (fused checksum tiles) flags
+  // [kMaxCtas, 2 kMaxCtas) and the next ws_ctas slots. Slot x holds
+  // kBM x BN fp32 values.
   uint32_t* flags;
   float* partials;
   int ws_ctas;
@@ -159,7 +159,16 @@ struct KernelParams {
   int ck_kpack_cr, ck_kpack_cc;
   uint32_t idesc_cr, idesc_cc;
   float tau_row, tau_col;  // <= 0: derive from the encode pass maxima
-  int inject_tile, inject_row, inject_col, inject_bit;
+  // Fault injection (testing only): up to two single-bit flips of the fp32
+  // accumulator, slot s at (inj_row[s], inj_col[s]) of 128 x BLK_N output
+  // tile inj_tile[s] (< 0: slot unused). inj_kb >= 0 applies slot 0 inside
+  // the mainloop, after the tile's MAC iteration inj_kb, instead of after
+  // the fixup.
+  int inj_tile[2], inj_row[2], inj_col[2], inj_bit[2];
+  int inj_kb;
+  // StaggerU-style k staggering: > 1 rotates each work item's k order by
+  // ((unit mod stagger) * n) / stagger of its n iterations.
+  int stagger;
   uint64_t timeout_ns;
   int32_t* trace;
   uint64_t* cta_clock;
@@ -226,7 +235,8 @@ struct Cfg {
 
 // Shared-memory bookkeeping that lives after the stage ring and staging.
 struct Aux {
-  uint64_t bars[56];      // full[S], empty[S], tfull[2], tempty[2], c0[4], drain, fix, c0r[4]
+  uint64_t bars[56];      // full[S], empty[S], tfull[2], tempty[2], c0[4], drain, fix, c0r[4],
+                          // inj, injdone
   uint32_t tmem_slot;
   int32_t abort_flag;
   int32_t nbad_r, nbad_c, bad_row, bad_col;
@@ -304,6 +314,52 @@ __device__ __forceinline__ bool wait_bar_inline(uint64_t* bar, uint32_t parity, 
 }
 
 __device__ __forceinline__ float f32_of(uint32_t u) { return __uint_as_float(u); }
+
+// Fault injection (testing only). The flips of the slots that land in the
+// 32-column chunk c32 of row r of 128 x BLK_N output tile `tile`, applied to
+// v (slot 0 only when it is not applied inside the mainloop). Returns true
+// when v changed; *clean gets the value before the first flip.
+__device__ __forceinline__ bool apply_flips(const KernelParams& p, int tile, int r, int c32,
+                                            float (&v)[32], float* clean) {
+  bool hit = false;
+#pragma unroll
+  for (int sl = 0; sl < 2; ++sl) {
+    if (p.inj_tile[sl] != tile || (sl == 0 && p.inj_kb >= 0)) continue;
+    if (r != p.inj_row[sl] || (p.inj_col[sl] >> 5) != c32) continue;
+    const int jc = p.inj_col[sl] & 31;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i == jc) {
+        if (!hit && clean) *clean = v[i];
+        v[i] = __uint_as_float(__float_as_uint(v[i]) ^ (1u << p.inj_bit[sl]));
+      }
+    hit = true;
+  }
+  return hit;
+}
+
+// Whether work item w runs slot 0's mid-mainloop MAC iteration (inj_kb) of
+// the injected tile: for this CTA's 128-row half `half` of the item's tile,
+// or (half < 0) for either half of a CTA pair's 256-row tile.
+template <bool PAIR>
+__device__ __forceinline__ bool mid_inject_item(const KernelParams& p, const Schedule& s,
+                                                const Work& w, int half) {
+  if (p.inj_kb < 0 || p.inj_tile[0] < 0 || w.tile < s.t_ck || p.inj_kb < w.kb_begin ||
+      p.inj_kb >= w.kb_end)
+    return false;
+  int tm, tn;
+  tile_coords(s, w.tile, tm, tn);
+  const int tm0 = PAIR ? 2 * tm : tm;
+  if (half >= 0) return p.inj_tile[0] == (tm0 + half) * s.tiles_n + tn;
+  return p.inj_tile[0] == tm0 * s.tiles_n + tn ||
+         (PAIR && p.inj_tile[0] == (tm0 + 1) * s.tiles_n + tn);
+}
+
+// First MAC iteration of a work item of n iterations under k staggering
+// (offset from kb_begin; the item then wraps around to kb_begin).
+__device__ __forceinline__ int stagger_offset(const KernelParams& p, int unit, int n) {
+  return p.stagger > 1 ? (int)(((int64_t)(unit % p.stagger) * n) / p.stagger) : 0;
+}
 
 // Sum over the 32 lanes of a warp for each of 32 columns: on return lane l
 // holds the sum of column l (recursive halving, 31 shuffles).
@@ -639,7 +695,7 @@ static __device__ __noinline__ bool reduce_share(const KernelParams& p, float* r
                                                  uint32_t* rflags, int owner, int contrib_last,
                                                  int part_last, int unit, int slot_stride,
                                                  int crank, int m0, int n0, int ew, int lane,
-                                                 uint32_t epoch, bool inject_here, Aux* aux,
+                                                 uint32_t epoch, int out_tile, Aux* aux,
                                                  uint64_t limit) {
   constexpr int BN = C::BN;
   bool fine = true;
@@ -734,8 +790,11 @@ static __device__ __noinline__ bool reduce_share(const KernelParams& p, float* r
       float y[4] = {acc[bi].x, acc[bi].y, acc[bi].z, acc[bi].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        if (inject_here && r == p.inject_row && 4 * c4 + e == p.inject_col)
-          y[e] = __uint_as_float(__float_as_uint(y[e]) ^ (1u << p.inject_bit));
+#pragma unroll
+        for (int sl = 0; sl < 2; ++sl)  // fault injection (testing only)
+          if (p.inj_tile[sl] == out_tile && !(sl == 0 && p.inj_kb >= 0) &&
+              r == p.inj_row[sl] && 4 * c4 + e == p.inj_col[sl])
+            y[e] = __uint_as_float(__float_as_uint(y[e]) ^ (1u << p.inj_bit[sl]));
         y[e] = p.alpha * y[e] + p.beta * c0v[bi][e];
       }
       if (ncol[bi] == 4) {
@@ -947,7 +1006,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain_bar = c0_bar + 4;
   uint64_t* fix_bar = drain_bar + 1;  // [epilogue warp][slot]: staged peer partials
   uint64_t* c0r_bar = fix_bar + 4 * kFixSlots;  // per epilogue warp: C0 staged in the ring
-  static_assert(2 * 8 + 2 + 2 + 4 + 1 + 4 * kFixSlots + 4 <= 56, "barrier slots");
+  // Mid-mainloop fault injection: the MMAs up to the chosen iteration are
+  // done (inj), the flipped value is back in TMEM (injdone, the leader's).
+  uint64_t* inj_bar = c0r_bar + 4;
+  uint64_t* injdone_bar = inj_bar + 1;
+  static_assert(2 * 8 + 2 + 2 + 4 + 1 + 4 * kFixSlots + 4 + 2 <= 56, "barrier slots");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -987,7 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The barriers in one go, a lane each: every one counts a single
     // arrival except the accumulator-empty ones, which the epilogue threads
     // release (both CTAs' for a pair).
-    const int nbars = (int)(c0r_bar + 4 - full_bar);
+    const int nbars = (int)(injdone_bar + 1 - full_bar);
     for (int i = lane; i < nbars; i += 32) {
       uint64_t* bar = full_bar + i;
       const bool acc_empty = bar >= tempty_bar && bar < tempty_bar + 2;
@@ -1122,7 +1185,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // in one kernel cost ~1.3 us at 2048^3 through code size).
         auto k_loop = [&](auto a_tag, auto b_tag) {
           constexpr bool a_box = decltype(a_tag)::value, b_box = decltype(b_tag)::value;
-          for (int kb = w.kb_begin; kb < w.kb_end; kb += kpack) {
+          // k order: from the item's staggered start, wrapping to kb_begin
+          // (the MMA thread walks the same order).
+          const int nk = w.kb_end - w.kb_begin;
+          int kb = w.kb_begin + (w.tile >= s.t_ck ? stagger_offset(p, unit, nk) : 0);
+          for (int i = 0; i < nk; i += kpack) {
             if (!try_wait_scoped<C::PAIR>(&empty_bar[stage], phase ^ 1) &&
                 !wait_bar(&empty_bar[stage], phase ^ 1, aux, limit, true, C::PAIR)) {
               if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
@@ -1187,6 +1254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               stage = 0;
               phase ^= 1;
             }
+            kb += kpack;
+            if (kb >= w.kb_end) kb -= nk;
           }
         };
         if constexpr (!C::MN) {
@@ -1267,7 +1336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t a_lbo = amn ? mn_lbo : 0, b_lbo = bmn ? mn_lbo : 0;
         const int a_step = amn ? (2048 >> 4) : 2, b_step = bmn ? (2048 >> 4) : 2;
         if (kpack == 1) {
-          for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          // The producer's k order (staggered start, wrap-around).
+          const int nk = w.kb_end - w.kb_begin;
+          int kb = w.kb_begin + (w.tile >= s.t_ck ? stagger_offset(p, unit, nk) : 0);
+          const int inj_kb_here = mid_inject_item<C::PAIR>(p, s, w, -1) ? p.inj_kb : -1;
+          for (int i = 0; i < nk; ++i) {
             // Inline fast path: the stage is usually full already.
             if (!mbar_try_wait(&full_bar[stage], phase) &&
                 !wait_bar(&full_bar[stage], phase, aux, limit)) {
@@ -1284,7 +1357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  (uint64_t)((stage * C::STAGE_BYTES + C::A_BYTES) >> 4) + b_lbo;
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
-              const uint32_t acc = (kb > w.kb_begin || kk > 0) ? 1u : 0u;
+              const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
               const uint64_t ad = ad0 + (uint64_t)(kk * a_step), bd = bd0 + (uint64_t)(kk * b_step);
               if constexpr (C::PAIR) umma_f16_pair(d, ad, bd, idesc, acc);
               else umma_f16(d, ad, bd, idesc, acc);
@@ -1292,10 +1365,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             issued = true;
             if constexpr (C::PAIR) umma_commit_pair(&empty_bar[stage]);  // both CTAs' stage
             else umma_commit(&empty_bar[stage]);
+            if (kb == inj_kb_here) {
+              // Mid-mainloop fault injection (testing only): once these MMAs
+              // are done, the epilogue warp of the row's lane quadrant flips
+              // the value in TMEM; the next MMAs accumulate onto it.
+              if constexpr (C::PAIR) umma_commit_pair(inj_bar);
+              else umma_commit(inj_bar);
+              if (!wait_bar(injdone_bar, 0, aux, limit, true, C::PAIR)) {
+                if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1;
             }
+            if (++kb == w.kb_end) kb = w.kb_begin;
           }
         } else {
           // Packed checksum stages: A(k), A(k+1), enc(k), enc(k+1).
@@ -1588,15 +1675,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
+      // Mid-mainloop fault injection (testing only): once the MMAs up to MAC
+      // iteration inj_kb are done, the warp of the row's lane quadrant flips
+      // the value in TMEM and releases the MMA thread.
+      if (mid_inject_item<C::PAIR>(p, s, w, (int)crank) && q == (p.inj_row[0] >> 5)) {
+        const bool fine = __all_sync(0xffffffffu, wait_bar(inj_bar, 0, aux, limit, true, C::PAIR));
+        if (fine) {
+          tc_fence_after();
+          const uint32_t ta = tmem_base + ab * C::ACC_COLS + ((uint32_t)(q * 32) << 16) +
+                              (uint32_t)((p.inj_col[0] >> 5) * 32);
+          uint32_t u[32];
+          tmem_ld32(ta, u);
+          if (lane == (p.inj_row[0] & 31)) {
+            const int jc = p.inj_col[0] & 31;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i == jc) {
+                const uint32_t before = u[i];
+                u[i] ^= 1u << p.inj_bit[0];
+                p.report->mid_before = __uint_as_float(before);
+                p.report->mid_after = __uint_as_float(u[i]);
+                atomicAdd(&p.report->mid_injected, 1u);
+              }
+          }
+          tmem_st32(ta, u);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (C::PAIR) mbar_arrive_cluster(cluster_addr(injdone_bar, 0));
+            else mbar_arrive(injdone_bar);
+          }
+        } else if (lane == 0 && !aborted(aux)) {
+          record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+        }
+      }
+
       bool got = wait_bar_inline<C::PAIR>(&tfull_bar[ab], aphase, aux, limit);
       if (!got && !aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
       if (!epi_all(got && store_ok && !aborted(aux))) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + ab * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
       const int out_tile = tm * s.tiles_n + tn;  // row-major 128 x BLK_N tile number
-      const bool inject_here = !is_ck && (out_tile == p.inject_tile) && (w.role != kRolePeer);
-      // This segment's region of fixup storage.
-      uint32_t* rflags = p.flags + (size_t)w.region * p.ws_ctas;
+      // Fault injection (testing only): this tile gets a flip after its fixup.
+      const bool inject_here = !is_ck && w.role != kRolePeer &&
+                               ((out_tile == p.inj_tile[0] && p.inj_kb < 0) ||
+                                out_tile == p.inj_tile[1]);
+      // ... or got one in the mainloop (fault records say "injected").
+      const bool injected_tile =
+          !is_ck && (out_tile == p.inj_tile[0] || out_tile == p.inj_tile[1]);
+      // This segment's region of fixup storage (flags at a fixed place).
+      uint32_t* rflags = p.flags + (size_t)w.region * kMaxCtas;
       float* rpartials = p.partials + (size_t)w.region * p.ws_ctas * kBM * BN;
       float* my_slot = rpartials + (size_t)my_slot_idx * kBM * BN;
       // Columns of the accumulator that carry data: a checksum tile uses
@@ -1631,7 +1759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (share && !reduce_share<C>(p, rpartials, rflags, w.owner, w.contrib_last, w.part_last,
                                       unit, slot_stride, (int)crank, m0, n0, ew, lane, epoch,
-                                      out_tile == p.inject_tile, aux, limit))
+                                      out_tile, aux, limit))
           break;
       } else {
         const bool owner = (w.role == kRoleOwner);
@@ -1779,18 +1907,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (add_partials)
               add_peer_partials<BN>(v, rpartials, unit + 1, w.peer_last, c32, r, w.region == 0,
                                     slot_stride, (int)crank);
-            // Fault injection: one bit of one fp32 accumulator, after the
-            // fixup and before the check (warp-uniform chunk selection).
-            const bool inj_chunk = inject_here && (p.inject_row >> 5) == q &&
-                                   (p.inject_col >> 5) == c32;
-            if (inj_chunk && lane == (p.inject_row & 31)) {
-              const int jc = p.inject_col & 31;
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (i == jc) {
-                  aux->inj_clean = v[i];
-                  v[i] = __uint_as_float(__float_as_uint(v[i]) ^ (1u << p.inject_bit));
-                }
+            // Fault injection (testing only): bits of fp32 accumulators,
+            // after the fixup and before the check.
+            bool inj_chunk = false;
+            if (inject_here) {
+              float clean = 0.f;
+              const bool hit = apply_flips(p, out_tile, r, c32, v, &clean);
+              if (hit) aux->inj_clean = clean;
+              inj_chunk = __any_sync(0xffffffffu, hit);
             }
             if (add_partials || inj_chunk) {
               uint32_t wv[32];
@@ -1910,7 +2034,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rec->status = SKG_ABFT_CORRECTED;
                 rec->n_bad_rows = nbr;
                 rec->n_bad_cols = nbc;
-                rec->injected = inject_here ? 1u : 0u;
+                rec->injected = injected_tile ? 1u : 0u;
                 rec->before = before;
                 rec->after = after;
                 rec->delta_row = aux->d_row;
@@ -1932,7 +2056,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               rec->status = SKG_ABFT_UNCORRECTABLE;
               rec->n_bad_rows = nbr;
               rec->n_bad_cols = nbc;
-              rec->injected = inject_here ? 1u : 0u;
+              rec->injected = injected_tile ? 1u : 0u;
               rec->before = 0.f;
               rec->after = 0.f;
               rec->delta_row = nbr ? aux->d_row : 0.f;
@@ -1987,13 +2111,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) y[hh * 32 + i] = v[i];
             if (!C::ABFT) {
-              if (inject_here && r == p.inject_row && (p.inject_col >> 5) == c32) {
-                const int jc = p.inject_col & 31;
+              if (inject_here && apply_flips(p, out_tile, r, c32, v, nullptr)) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (i == jc)
-                    y[hh * 32 + i] =
-                        __uint_as_float(__float_as_uint(y[hh * 32 + i]) ^ (1u << p.inject_bit));
+                for (int i = 0; i < 32; ++i) y[hh * 32 + i] = v[i];
               }
             } else if (r == fix_row && (fix_col >> 5) == c32) {
               const int jc = fix_col & 31;

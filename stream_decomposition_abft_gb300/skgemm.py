@@ -44,7 +44,10 @@ class Opts(ctypes.Structure):
                 ("trace", ctypes.c_void_p), ("cta_clock", ctypes.c_void_p),
                 ("test_drop_signal", ctypes.c_int32), ("abft_preencoded", ctypes.c_int32),
                 ("raster_band", ctypes.c_int32), ("cta_pair", ctypes.c_int32),
-                ("abft_local", ctypes.c_int32)]
+                ("abft_local", ctypes.c_int32), ("inject2_tile", ctypes.c_int32),
+                ("inject2_row", ctypes.c_int32), ("inject2_col", ctypes.c_int32),
+                ("inject2_bit", ctypes.c_int32), ("inject_kstep", ctypes.c_int32),
+                ("stagger", ctypes.c_int32)]
 
 
 class Segment(ctypes.Structure):
@@ -77,14 +80,17 @@ class Report(ctypes.Structure):
                 ("timeouts", ctypes.c_uint32), ("n_records", ctypes.c_uint32),
                 ("max_ratio_row", ctypes.c_float), ("max_ratio_col", ctypes.c_float),
                 ("tau_row", ctypes.c_float), ("tau_col", ctypes.c_float),
-                ("reserved", ctypes.c_uint32 * 4), ("records", FaultRecord * MAX_RECORDS)]
+                ("mid_injected", ctypes.c_uint32), ("mid_before", ctypes.c_float),
+                ("mid_after", ctypes.c_float), ("reserved", ctypes.c_uint32),
+                ("records", FaultRecord * MAX_RECORDS)]
 
 
 SYMBOLS = ("skg_opts_default", "skg_workspace_size", "skg_workspace_init", "skg_gemm",
            "skg_gemm_verify", "skg_abft_encode", "skg_schedule_query", "skg_launch_shape", "skg_report_read",
            "skg_device_sm_count", "skg_status_string", "skg_gemm_noalloc", "skg_schedule_cost",
            "skg_launch_plan", "skg_workspace_size_layout", "skg_host_staging_size",
-           "skg_gemm_host", "skg_abft_encode_layout", "skg_workspace_size_f64", "skg_gemm_f64")
+           "skg_gemm_host", "skg_abft_encode_layout", "skg_workspace_size_f64", "skg_gemm_f64",
+           "skg_noalloc_report_read")
 
 _lib = None
 
@@ -152,6 +158,8 @@ def lib() -> ctypes.CDLL:
     L.skg_gemm_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, i32,
                                    i32, i32, i32, ctypes.POINTER(Opts), vp]
     L.skg_gemm_noalloc.restype = i32
+    L.skg_noalloc_report_read.argtypes = [ctypes.POINTER(Report), i32, vp]
+    L.skg_noalloc_report_read.restype = i32
     L.skg_device_sm_count.argtypes = []
     L.skg_device_sm_count.restype = i32
     L.skg_status_string.argtypes = [i32]
@@ -301,6 +309,15 @@ def gemm_noalloc(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, in_dt
     return int(lib().skg_gemm_noalloc(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc,
                                       in_dtype, out_dtype, a_layout, b_layout,
                                       ctypes.byref(opts) if opts else None, stream))
+
+
+def noalloc_report_read(reset: bool = False, stream: int = 0) -> Report:
+    """skg_noalloc_report_read: the report of skg_gemm_noalloc's array."""
+    rep = Report()
+    st = lib().skg_noalloc_report_read(ctypes.byref(rep), 1 if reset else 0, stream)
+    if st != OK:
+        raise SkgError(st, "skg_noalloc_report_read")
+    return rep
 
 
 def device_sm_count() -> int:

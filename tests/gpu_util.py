@@ -140,3 +140,31 @@ def check_checksum_probe(p: inputs.Problem, C: torch.Tensor):
     tol_r = p.n * base + u * Cd.abs().sum(dim=1).cpu()
     assert bool(((col - cc).abs() <= tol_c).all()), "column checksum probe failed"
     assert bool(((row - cr).abs() <= tol_r).all()), "row checksum probe failed"
+
+
+def draw_must_detect(ref, A_km, B_km, alpha, k, m, n, bn, bit, seed, tiles=None, bm=128):
+    """A seeded (tile, row, col) of a 128 x bn ABFT tile whose accumulator
+    flips by more than ten thresholds when `bit` flips (the fault model's
+    must-detect class), so an injection test never has to skip. `ref` is the
+    oracle's C (alpha applied), A_km / B_km the K-major stored operands
+    (m x k and n x k) for the tile maxima; `tiles` restricts the draw to some
+    tile numbers (row-major over 128 x bn tiles)."""
+    from oracle import abft_ref as ab
+    rng = np.random.default_rng(seed)
+    tiles_n = (n + bn - 1) // bn
+    tiles_m = (m + bm - 1) // bm
+    pool = list(tiles) if tiles is not None else list(range(tiles_m * tiles_n))
+    for _ in range(20000):
+        tile = int(pool[int(rng.integers(0, len(pool)))])
+        tm, tn = divmod(tile, tiles_n)
+        row, col = int(rng.integers(0, bm)), int(rng.integers(0, bn))
+        gi, gj = tm * bm + row, tn * bn + col
+        if gi >= m or gj >= n:
+            continue
+        v = ref[gi, gj] / alpha
+        ma, mb = ab.tile_maxima(A_km, B_km, tm, tn, bm, bn)
+        tau = max(ab.default_tau(k, bn, ma, mb), ab.default_tau(k, bm, ma, mb))
+        kind, _ = ab.classify_flip(v, bit, tau, 1e-3 * tau)
+        if kind == ab.MUST_DETECT:
+            return tile, row, col
+    raise AssertionError(f"no must-detect position for bit {bit}")

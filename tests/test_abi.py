@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_struct_sizes_match_header():
     # Sizes fixed by the header's field lists (x86-64 and aarch64 ABIs agree).
-    assert ctypes.sizeof(skgemm.Opts) == 88
+    assert ctypes.sizeof(skgemm.Opts) == 112
     assert ctypes.sizeof(skgemm.Segment) == 20
     assert ctypes.sizeof(skgemm.FaultRecord) == 64
     assert ctypes.sizeof(skgemm.Report) == 64 + 64 * 64
@@ -47,6 +47,7 @@ def test_struct_sizes_match_header():
 def test_defaults(lib):
     o = skgemm.opts_default()
     assert o.sched == skgemm.SCHED_AUTO and o.inject_tile == -1 and o.abft == 0
+    assert o.inject2_tile == -1 and o.inject_kstep == -1 and o.stagger == 0
     assert skgemm.status_string(0) == "ok"
     assert "timed out" in skgemm.status_string(skgemm.ERR_FIXUP_TIMEOUT)
 
@@ -187,11 +188,12 @@ def test_host_staging_size_and_argument_errors(lib):
 
 
 def test_f64_workspace_and_argument_errors(lib):
-    # One 64 x 64 fp64 slot (32 KB) and one flag per CTA after a fixed
-    # header and the report.
+    # One 64 x 64 fp64 slot (32 KB) per CTA after a fixed header, the report
+    # and a fixed flag array (1024 flags), whatever the grid.
     a = skgemm.workspace_size_f64(1000, 1000, 1000, skgemm.opts_default(grid=1))
     b = skgemm.workspace_size_f64(1000, 1000, 1000, skgemm.opts_default(grid=148))
-    assert b - a == 147 * 32768 + 512  # flags: 4 -> 592 bytes, rounded to 256
+    assert b - a == 147 * 32768
+    assert a % 256 == 0 and a > 4096 + 32768
     assert skgemm.workspace_size_f64(64, 64, 64, skgemm.opts_default(grid=148)) == b
     o = skgemm.opts_default()
     call = lambda m=64, n=64, k=64, lda=64, ldb=64, ldc=64, A=16, grid=0: skgemm.gemm_f64(

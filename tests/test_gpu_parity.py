@@ -14,7 +14,8 @@ from oracle import abft_ref as ab
 from oracle import schedule_sim as ss
 from stream_decomposition_abft_gb300 import _build, inputs, skgemm
 
-from gpu_util import check_full, check_sampled, check_checksum_probe, reference, run
+from gpu_util import (check_full, check_sampled, check_checksum_probe, draw_must_detect,
+                      reference, run)
 
 pytestmark = pytest.mark.gpu
 
@@ -302,29 +303,19 @@ def test_injected_fault_detected_located_corrected(mode, bit):
     p = inputs.make_problem(512, 640, 1024, seed=77, in_dtype="bf16", out_dtype="f32",
                             law_a="normal", law_b="normal", scale_b=0.02)
     ref = reference(p)
-    tiles_n = (640 + 127) // 128
-    rng = np.random.default_rng(bit)
-    tile = int(rng.integers(0, 4 * tiles_n))
-    row, col = int(rng.integers(0, 128)), int(rng.integers(0, 128))
-    tm, tn = divmod(tile, tiles_n)
-    gi, gj = tm * 128 + row, tn * 128 + col
-    v = ref[gi, gj] / p.alpha
-    ma, mb = ab.tile_maxima(p.A.double().numpy(), p.B.double().numpy(), tm, tn, 128, 128)
-    tau = ab.default_tau(p.k, 128, ma, mb)
-    kind, delta = ab.classify_flip(v, bit, tau, 1e-3 * tau)
+    # A position where this bit is must-detect (seeded draw: never skips).
+    tile, row, col = draw_must_detect(ref, p.A.double().numpy(), p.B.double().numpy(), p.alpha,
+                                      p.k, 512, 640, 128, bit, seed=bit)
     C, ws, st = _inject(p, dict(sched=mode, tile_n=128, grid=min(64, sms())), tile, row, col, bit)
     assert st == skgemm.OK
     rep = ws.report()
-    if kind == ab.MUST_DETECT:
-        assert rep.detected == 1 and rep.corrected == 1 and rep.uncorrectable == 0
-        rec = rep.records[0]
-        assert (rec.tile, rec.row, rec.col, rec.injected) == (tile, row, col, 1)
-        # the flip is exactly one bit of the GPU's own pre-fault value
-        assert ab.flip_f32(rec.clean_value, bit) == rec.before or \
-            (np.isnan(rec.before) and np.isnan(ab.flip_f32(rec.clean_value, bit)))
-        check_full(p, C, ref)   # corrected output is within parity tolerance
-    else:
-        pytest.skip(f"bit {bit} of {v} is {kind} at tau {tau}")
+    assert rep.detected == 1 and rep.corrected == 1 and rep.uncorrectable == 0
+    rec = rep.records[0]
+    assert (rec.tile, rec.row, rec.col, rec.injected) == (tile, row, col, 1)
+    # the flip is exactly one bit of the GPU's own pre-fault value
+    assert ab.flip_f32(rec.clean_value, bit) == rec.before or \
+        (np.isnan(rec.before) and np.isnan(ab.flip_f32(rec.clean_value, bit)))
+    check_full(p, C, ref)   # corrected output is within parity tolerance
 
 
 @pytest.mark.parametrize("shape", [(300, 200, 200), (1000, 1300, 520), (1024, 1024, 1024),
@@ -365,14 +356,8 @@ def test_abft_local_injection(dtype, bit):
     p = inputs.make_problem(512, 640, 1024, seed=78, in_dtype=dtype, out_dtype="f32",
                             law_a="normal", law_b="normal", scale_b=0.02)
     ref = reference(p)
-    tile, row, col = 13, 101, 7
-    tm, tn = divmod(tile, 5)
-    v = ref[tm * 128 + row, tn * 128 + col] / p.alpha
-    ma, mb = ab.tile_maxima(p.A.double().numpy(), p.B.double().numpy(), tm, tn, 128, 128)
-    tau = ab.default_tau(p.k, 128, ma, mb)
-    kind, _ = ab.classify_flip(v, bit, tau, 1e-3 * tau)
-    if kind != ab.MUST_DETECT:
-        pytest.skip(f"bit {bit} of {v} is {kind} at tau {tau}")
+    tile, row, col = draw_must_detect(ref, p.A.double().numpy(), p.B.double().numpy(), p.alpha,
+                                      p.k, 512, 640, 128, bit, seed=100 + bit)
     assert skgemm.launch_plan(512, 640, 1024,
                               skgemm.opts_default(abft=1, abft_local=2)).local_checksums == 1
     C, ws, st = _inject(p, dict(abft_local=2), tile, row, col, bit)
@@ -528,14 +513,10 @@ def test_cta_pairs_abft_injection(bit):
                             law_a="normal", law_b="normal", scale_b=0.02)
     ref = reference(p)
     tiles_n = (n + 255) // 256
-    tm, tn, row, col = 3, 1, 17, 200
-    tile = tm * tiles_n + tn
-    v = ref[tm * 128 + row, tn * 256 + col] / p.alpha
-    ma, mb = ab.tile_maxima(p.A.double().numpy(), p.B.double().numpy(), tm, tn, 128, 256)
-    tau = ab.default_tau(k, 256, ma, mb)
-    kind, _ = ab.classify_flip(v, bit, tau, 1e-3 * tau)
-    if kind != ab.MUST_DETECT:
-        pytest.skip(f"bit {bit} of {v} is {kind}")
+    # tiles in odd 128-row tile rows: the second CTA of a pair
+    odd = [tm * tiles_n + tn for tm in (1, 3) for tn in range(tiles_n)]
+    tile, row, col = draw_must_detect(ref, p.A.double().numpy(), p.B.double().numpy(), p.alpha,
+                                      k, m, n, 256, bit, seed=200 + bit, tiles=odd)
     opts = skgemm.opts_default(abft=1, cta_pair=2, inject_tile=tile, inject_row=row,
                                inject_col=col, inject_bit=bit)
     C, ws, st = run(p, opts)
@@ -673,16 +654,10 @@ def test_mn_major_abft_injection(bit):
     p = inputs.make_problem(512, 640, 1024, seed=78, in_dtype="bf16", out_dtype="f32",
                             law_a="normal", law_b="normal", scale_b=0.02, a_layout=1, b_layout=1)
     ref = reference(p)
-    tile, row, col = 13, 101, 7
-    tm, tn = divmod(tile, 5)
-    v = ref[tm * 128 + row, tn * 128 + col] / p.alpha
     A_k = p.A.t().double().numpy()
     B_k = p.B.t().double().numpy()
-    ma, mb = ab.tile_maxima(A_k, B_k, tm, tn, 128, 128)
-    tau = ab.default_tau(p.k, 128, ma, mb)
-    kind, _ = ab.classify_flip(v, bit, tau, 1e-3 * tau)
-    if kind != ab.MUST_DETECT:
-        pytest.skip(f"bit {bit} of {v} is {kind} at tau {tau}")
+    tile, row, col = draw_must_detect(ref, A_k, B_k, p.alpha, p.k, 512, 640, 128, bit,
+                                      seed=300 + bit)
     C, ws, st = _inject(p, dict(tile_n=128), tile, row, col, bit)
     assert st == skgemm.OK
     rep = ws.report()

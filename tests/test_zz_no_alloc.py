@@ -6,11 +6,16 @@ cudaMalloc's implicit synchronisation).
 Two calls in a row through the C ABI must each match skg_gemm (which takes
 a caller workspace) within the parity tolerance of the other GPU tests. The
 second call reuses the shared scratch array as the first call left it.
-This file is collected last on purpose; it passes alone or after the rest.
+A longer sequence mixes shapes, input types, grids, CTA pairs and ABFT on
+the one array, and the array's report (skg_noalloc_report_read) shows what
+the device decided. This file is collected last on purpose; it passes alone
+or after the rest.
 """
 import numpy as np
 import pytest
 import torch
+
+from oracle import schedule_sim as ss
 
 from stream_decomposition_abft_gb300 import _build, inputs, skgemm
 
@@ -67,3 +72,65 @@ def test_noalloc_rejects_oversized_workspace():
     A, B = to_device(p, "cuda")
     C = out_init(p, "cuda")
     assert _call("noalloc", p, A, B, C, opts) == skgemm.ERR_WORKSPACE
+
+
+def test_noalloc_sequence_of_shapes_and_options():
+    # Calls whose workspace layouts differ, one after the other on the shared
+    # array: every result equals skg_gemm's with the same options on a
+    # workspace of its own (same plan, same summation order), and the
+    # array's report shows the ABFT checks of exactly these calls.
+    seq = [
+        (inputs.make_problem(2048, 2048, 1024, seed=61, in_dtype="bf16", out_dtype="bf16",
+                             law_a="normal", law_b="normal"), dict(tile_n=128)),
+        (inputs.make_problem(700, 900, 520, seed=62, in_dtype="f16", out_dtype="f16",
+                             alpha=1.5, beta=0.5), dict(abft=1, grid=16, tile_n=128)),
+        (inputs.make_problem(1000, 1300, 520, seed=63, in_dtype="bf16", out_dtype="f32",
+                             law_a="normal", law_b="normal"),
+         dict(abft=1, cta_pair=2, tile_n=256, grid=16)),
+        (inputs.make_problem(384, 4096, 704, seed=64, in_dtype="bf16", out_dtype="bf16",
+                             law_a="normal", law_b="normal"), dict(sched="sk", tile_n=128)),
+        (inputs.make_problem(2048, 2048, 1024, seed=61, in_dtype="bf16", out_dtype="bf16",
+                             law_a="normal", law_b="normal"), dict(tile_n=128)),
+    ]
+    stream = torch.cuda.current_stream().cuda_stream
+    skgemm.noalloc_report_read(reset=True, stream=stream)
+    for i, (p, kw) in enumerate(seq):
+        opts = skgemm.opts_default(**kw)
+        A, B = to_device(p, "cuda")
+        ws = skgemm.Workspace(skgemm.workspace_size(p.m, p.n, p.k, opts), "cuda")
+        C_ref = out_init(p, "cuda")
+        assert _call("gemm", p, A, B, C_ref, opts, ws) == skgemm.OK, i
+        C_new = out_init(p, "cuda")
+        assert _call("noalloc", p, A, B, C_new, opts) == skgemm.OK, i
+        rep = skgemm.noalloc_report_read(reset=True, stream=stream)
+        ref_rep = ws.report()
+        assert torch.equal(C_new, C_ref), i
+        assert rep.status_bits == 0 and rep.detected == 0, i
+        assert rep.tiles_checked == ref_rep.tiles_checked, i
+        assert (rep.tiles_checked > 0) == bool(kw.get("abft")), i
+
+
+def test_noalloc_report_shows_a_timeout():
+    # A device-side failure on this path is not silent: a CTA that skips its
+    # Stream-K signal makes its owner's bounded wait run out, and the array's
+    # report says so; the next call on the array is correct again.
+    stream = torch.cuda.current_stream().cuda_stream
+    p = inputs.make_problem(256, 256, 4096, seed=65, in_dtype="bf16", out_dtype="f32")
+    rows = ss.flatten(ss.schedule(256, 256, 4096, 128, 128, 64, 8, mode="sk"))
+    peer = next(r[0] for r in rows if r[4] == ss.PEER)
+    opts = skgemm.opts_default(sched="sk", grid=8, tile_n=128, timeout_ns=50_000_000,
+                               test_drop_signal=peer + 1)
+    A, B = to_device(p, "cuda")
+    C = out_init(p, "cuda")
+    skgemm.noalloc_report_read(reset=True, stream=stream)
+    assert _call("noalloc", p, A, B, C, opts) == skgemm.OK
+    rep = skgemm.noalloc_report_read(reset=True, stream=stream)
+    assert rep.status_bits & (1 << skgemm.ERR_FIXUP_TIMEOUT) and rep.timeouts >= 1
+    good = skgemm.opts_default(sched="sk", grid=8, tile_n=128)
+    C2 = out_init(p, "cuda")
+    assert _call("noalloc", p, A, B, C2, good) == skgemm.OK
+    ws = skgemm.Workspace(skgemm.workspace_size(p.m, p.n, p.k, good), "cuda")
+    C3 = out_init(p, "cuda")
+    assert _call("gemm", p, A, B, C3, good, ws) == skgemm.OK
+    assert torch.equal(C2, C3)
+    assert skgemm.noalloc_report_read(reset=True, stream=stream).status_bits == 0
