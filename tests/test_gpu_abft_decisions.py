@@ -320,16 +320,21 @@ def test_mid_mainloop_flip_in_a_peer_partial():
 
 
 def test_mid_mainloop_argument_checks():
+    # An iteration past the tile's last one is an argument error; in-CTA
+    # references (whose epilogue warps read every stage while the MMAs run)
+    # cannot take a mid-mainloop flip. Both are refused before any launch.
     p = integer_problem(seed=10)
+    ws = skgemm.Workspace(skgemm.workspace_size(M, N, K, skgemm.opts_default(abft=1)), "cuda")
     o = skgemm.opts_default(abft=1, inject_tile=0, inject_row=0, inject_col=0, inject_bit=30,
                             inject_kstep=(K + 63) // 64)
-    C, ws, st = run(p, o)
+    assert skgemm.workspace_size(M, N, K, o) == 0
+    C, ws, st = run(p, o, ws=ws)
     assert st == skgemm.ERR_ARG
     o.inject_kstep = 0
     o.abft_local = 2
     small = inputs.make_problem(256, 256, 256, seed=1, in_dtype="bf16", out_dtype="f32",
                                 law_a="integer", law_b="integer")
-    C, ws, st = run(small, o)
+    C, ws, st = run(small, o, ws=ws)
     assert st == skgemm.ERR_UNSUPPORTED
 
 
