@@ -4,12 +4,14 @@
 Workload: C = A B with m = n = k in {1024, 2048, 3072, 4096, 5120, 6144},
 bf16 inputs drawn N(0,1)/sqrt(k) (seed 1), fp32 accumulation, bf16 output,
 ABFT checksum verification on. One step runs the whole hot path on every
-shape once: one skg_gemm call with ABFT on (the library issues the encode
-pass and the persistent Stream-K kernel, or one launch when the encode runs
-inside it), bracketed by CUDA events on the launching stream, with a
-256 MiB write before each shape so none starts with its operands in the
-129 MB L2. The main kernel alone (pre-encoded checksums) is timed the same
-way in a separate loop for the roofline.
+shape: skg_gemm calls with ABFT on (the library issues the encode pass and
+the persistent Stream-K kernel, or one launch when the encode runs inside
+it), each bracketed by CUDA events on the launching stream, with a 256 MiB
+write before each call so none starts with its operands in the 129 MB L2.
+Each shape is repeated within a step so that over the timed steps it gets
+at least 20 launches and 200 ms of timed GEMM time; a shape's time is the
+median of its launches. The main kernel alone (pre-encoded checksums) is
+timed the same way in a separate loop for the roofline.
 
 Metric: GEMM TFLOPS = 2mnk / time, geomean over the sweep, and its fraction
 of the GB300 dense bf16 peak. The JSON line also carries the roofline of the
@@ -42,6 +44,8 @@ METRIC = "GEMM TFLOPS (2mnk/s) and % of GB300 dense bf16 peak; geomean over shap
 WORKLOAD = ("square bf16 sweep m=n=k in {1024,2048,3072,4096,5120,6144}, "
             "N(0,1)/sqrt(k) inputs (seed 1), fp32 accumulate, bf16 out, ABFT verify on")
 FLUSH_BYTES = 256 << 20
+MIN_LAUNCHES = 20      # per shape, over the timed steps
+MIN_TIMED_S = 0.2      # per shape: at least this much timed GEMM time
 KERNEL_SOURCES = ("stream_decomposition_abft_gb300/csrc/skg_kernel.cuh",
                   "stream_decomposition_abft_gb300/csrc/skg_ptx.cuh",
                   "stream_decomposition_abft_gb300/csrc/skg_sched.cuh")
@@ -181,23 +185,31 @@ def run_ours(args, rank, world, local_rank):
             raise skgemm.SkgError(st, "skg_gemm")
 
     def step(record):
-        # One step: for every shape, an L2 flush, then the whole ABFT GEMM
-        # (encode pass + main kernel, issued by the library) between events.
+        # One step: for every shape, pr["per_step"] times an L2 flush, then
+        # the whole ABFT GEMM (encode pass + main kernel, issued by the
+        # library) between events on the launching stream.
         for pr in problems:
-            flush.zero_()
-            if record:
-                pr["ev"] = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-                pr["ev"][0].record(stream)
-            launch(pr, opts)
-            if record:
-                pr["ev"][1].record(stream)
-                pr["events"].append(pr["ev"])
+            for _ in range(pr["per_step"] if record else 1):
+                flush.zero_()
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                ev[0].record(stream)
+                launch(pr, opts)
+                ev[1].record(stream)
+                pr["events" if record else "warm_events"].append(ev)
 
     for pr in problems:
-        pr["events"] = []
+        pr["events"], pr["warm_events"] = [], []
+        pr["per_step"] = 1
     for _ in range(args.warmup):
         step(False)
     torch.cuda.synchronize()
+    # Launches per shape and step: over the K timed steps every shape gets at
+    # least MIN_LAUNCHES launches and MIN_TIMED_S of timed launches (median
+    # of them per shape), whatever K is.
+    for pr in problems:
+        est = statistics.median(a.elapsed_time(b) for a, b in pr["warm_events"]) * 1e-3
+        total = max(MIN_LAUNCHES, math.ceil(MIN_TIMED_S / max(est, 1e-6)))
+        pr["per_step"] = max(1, math.ceil(total / args.steps))
     for pr in problems:
         pr["ws"].report(reset=True)
 
@@ -218,7 +230,7 @@ def run_ours(args, rank, world, local_rank):
 
     # The dominant kernel alone (roofline): the main kernel on pre-encoded
     # checksums, L2 flushed before each launch, CUDA events on this stream.
-    main_reps = max(5, min(args.steps, 30))
+    main_reps = max(MIN_LAUNCHES, 3 * args.steps)
     for pr in problems:
         s = pr["size"]
         st = skgemm.abft_encode(s, s, s, pr["A"].data_ptr(), s, pr["B"].data_ptr(), s,
@@ -244,11 +256,12 @@ def run_ours(args, rank, world, local_rank):
         s = pr["size"]
         full = [e[0].elapsed_time(e[1]) for e in pr["events"]]
         main = [a.elapsed_time(b) for a, b in pr["main_events"]]
-        t_full = statistics.mean(full)
-        t_main = statistics.mean(main)
+        t_full = statistics.median(full)
+        t_main = statistics.median(main)
         flops = 2.0 * s * s * s
         per_shape.append({"m": s, "n": s, "k": s, "ms": round(t_full, 5),
-                          "ms_main_kernel": round(t_main, 5),
+                          "ms_main_kernel": round(t_main, 5), "launches": len(full),
+                          "timed_ms": round(sum(full), 2),
                           "tflops": round(flops / t_full / 1e9, 2),
                           "tflops_main_kernel": round(flops / t_main / 1e9, 2)})
         total_main_ms += sum(main)
@@ -296,6 +309,10 @@ def run_ours(args, rank, world, local_rank):
                                                              if pl.fused_checksums else 4)}
                                       for sz, pl in plans.items()},
                    "sms": sms,
+                   "launches_per_shape_per_step": {str(pr["size"]): pr["per_step"]
+                                                   for pr in problems},
+                   "timing": "per shape: median event time of all its timed launches "
+                             f"(>= {MIN_LAUNCHES} launches and >= {MIN_TIMED_S * 1e3:.0f} ms)",
                    "l2": "flushed between launches (256 MiB write)",
                    "parallelism": f"replicas x{world}"},
         "pct_of_peak": {"measured_burst": round(100 * value / world / burst, 2),
@@ -306,12 +323,15 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "tensor", "kernel": "skg_gemm_kernel (Stream-K mainloop + ABFT)",
                      "achieved": round(achieved, 2), "peak": burst,
                      "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
+                     "frac_geomean_per_shape": round(geomean(
+                         [ps["tflops_main_kernel"] / burst for ps in per_shape]), 4),
                      "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)",
                      "traffic": traffic},
         "abft": abft,
         "gpu_launches": args.steps * sum(
-            (1 if pl.encode_in_kernel else 2) if pl.fused_checksums else 4
-            for pl in plans.values()),
+            pr["per_step"] * ((1 if plans[pr["size"]].encode_in_kernel else 2)
+                              if plans[pr["size"]].fused_checksums else 4)
+            for pr in problems),
         "clocks": clocks,
         "wall_s_timed": round(wall, 3),
         "e2e": e2e,

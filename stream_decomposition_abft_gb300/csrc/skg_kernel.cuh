@@ -361,6 +361,54 @@ __device__ __forceinline__ int stagger_offset(const KernelParams& p, int unit, i
   return p.stagger > 1 ? (int)(((int64_t)(unit % p.stagger) * n) / p.stagger) : 0;
 }
 
+// The k order of one work item as at most three ascending ranges of MAC
+// iterations, run one after the other: a staggered item runs
+// [kb_begin + off, kb_end) then [kb_begin, kb_begin + off); a mid-mainloop
+// injection at iteration inj_kb cuts the range that holds it after inj_kb
+// (`pause` = the range after which the MMA thread waits for the flip). The
+// loops over one range are the plain ascending k loops, so a launch without
+// either option runs exactly one range per item with nothing extra per
+// k-step.
+struct KOrder {
+  int lo0, hi0, lo1, hi1, lo2, hi2;
+  int n, pause;
+  __device__ __forceinline__ int lo(int r) const { return r == 0 ? lo0 : (r == 1 ? lo1 : lo2); }
+  __device__ __forceinline__ int hi(int r) const { return r == 0 ? hi0 : (r == 1 ? hi1 : hi2); }
+};
+
+__device__ __forceinline__ KOrder k_order(int kb_begin, int kb_end, int off, int inj_kb) {
+  KOrder o;
+  o.lo0 = o.hi0 = o.lo1 = o.hi1 = o.lo2 = o.hi2 = 0;
+  o.n = 0;
+  o.pause = -1;
+  auto push = [&](int a, int b) {
+    if (o.n == 0) {
+      o.lo0 = a;
+      o.hi0 = b;
+    } else if (o.n == 1) {
+      o.lo1 = a;
+      o.hi1 = b;
+    } else {
+      o.lo2 = a;
+      o.hi2 = b;
+    }
+    ++o.n;
+  };
+  auto add = [&](int a, int b) {
+    if (a >= b) return;
+    if (inj_kb >= a && inj_kb < b) {
+      push(a, inj_kb + 1);
+      o.pause = o.n - 1;
+      if (inj_kb + 1 < b) push(inj_kb + 1, b);
+    } else {
+      push(a, b);
+    }
+  };
+  add(kb_begin + off, kb_end);
+  add(kb_begin, kb_begin + off);
+  return o;
+}
+
 // Sum over the 32 lanes of a warp for each of 32 columns: on return lane l
 // holds the sum of column l (recursive halving, 31 shuffles).
 __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
@@ -978,6 +1026,45 @@ static __device__ __noinline__ LocalSums<C::BN> local_checksums(
   return out;
 }
 
+// Mid-mainloop fault injection (testing only), by the epilogue warp of lane
+// quadrant q: wait until the MMAs up to the chosen iteration are done (inj),
+// flip the bit in TMEM (accumulator columns at acc_base), record the value
+// before and after in the report, and let the MMA thread go on (injdone, the
+// leader's for a CTA pair).
+template <bool PAIR>
+static __device__ __noinline__ void mid_inject_flip(const KernelParams& p, uint32_t acc_base,
+                                                    int q, int lane, uint64_t* inj_bar,
+                                                    uint64_t* injdone_bar, Aux* aux,
+                                                    uint64_t limit) {
+  if (!__all_sync(0xffffffffu, wait_bar(inj_bar, 0, aux, limit, true, PAIR))) {
+    if (lane == 0 && !aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+    return;
+  }
+  tc_fence_after();
+  const uint32_t ta = acc_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((p.inj_col[0] >> 5) * 32);
+  uint32_t u[32];
+  tmem_ld32(ta, u);
+  if (lane == (p.inj_row[0] & 31)) {
+    const int jc = p.inj_col[0] & 31;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i == jc) {
+        const uint32_t before = u[i];
+        u[i] ^= 1u << p.inj_bit[0];
+        p.report->mid_before = __uint_as_float(before);
+        p.report->mid_after = __uint_as_float(u[i]);
+        atomicAdd(&p.report->mid_injected, 1u);
+      }
+  }
+  tmem_st32(ta, u);
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) {
+    if constexpr (PAIR) mbar_arrive_cluster(cluster_addr(injdone_bar, 0));
+    else mbar_arrive(injdone_bar);
+  }
+}
+
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     skg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -1185,11 +1272,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // in one kernel cost ~1.3 us at 2048^3 through code size).
         auto k_loop = [&](auto a_tag, auto b_tag) {
           constexpr bool a_box = decltype(a_tag)::value, b_box = decltype(b_tag)::value;
-          // k order: from the item's staggered start, wrapping to kb_begin
-          // (the MMA thread walks the same order).
-          const int nk = w.kb_end - w.kb_begin;
-          int kb = w.kb_begin + (w.tile >= s.t_ck ? stagger_offset(p, unit, nk) : 0);
-          for (int i = 0; i < nk; i += kpack) {
+          // k order: the item's ranges (the MMA thread walks the same ones).
+          const KOrder ko =
+              k_order(w.kb_begin, w.kb_end,
+                      w.tile >= s.t_ck ? stagger_offset(p, unit, w.kb_end - w.kb_begin) : 0, -1);
+          for (int rg = 0; rg < ko.n && ok; ++rg)
+          for (int kb = ko.lo(rg), kb_hi = ko.hi(rg); kb < kb_hi; kb += kpack) {
             if (!try_wait_scoped<C::PAIR>(&empty_bar[stage], phase ^ 1) &&
                 !wait_bar(&empty_bar[stage], phase ^ 1, aux, limit, true, C::PAIR)) {
               if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
@@ -1254,8 +1342,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               stage = 0;
               phase ^= 1;
             }
-            kb += kpack;
-            if (kb >= w.kb_end) kb -= nk;
           }
         };
         if constexpr (!C::MN) {
@@ -1336,36 +1422,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t a_lbo = amn ? mn_lbo : 0, b_lbo = bmn ? mn_lbo : 0;
         const int a_step = amn ? (2048 >> 4) : 2, b_step = bmn ? (2048 >> 4) : 2;
         if (kpack == 1) {
-          // The producer's k order (staggered start, wrap-around).
-          const int nk = w.kb_end - w.kb_begin;
-          int kb = w.kb_begin + (w.tile >= s.t_ck ? stagger_offset(p, unit, nk) : 0);
-          const int inj_kb_here = mid_inject_item<C::PAIR>(p, s, w, -1) ? p.inj_kb : -1;
-          for (int i = 0; i < nk; ++i) {
-            // Inline fast path: the stage is usually full already.
-            if (!mbar_try_wait(&full_bar[stage], phase) &&
-                !wait_bar(&full_bar[stage], phase, aux, limit)) {
-              if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
-              ok = false;
-              break;
+          // The producer's k ranges, cut after a mid-mainloop injection.
+          const KOrder ko =
+              k_order(w.kb_begin, w.kb_end,
+                      w.tile >= s.t_ck ? stagger_offset(p, unit, w.kb_end - w.kb_begin) : 0,
+                      mid_inject_item<C::PAIR>(p, s, w, -1) ? p.inj_kb : -1);
+          const int kb_first = ko.lo0;  // the item's first MMA starts the accumulator
+          for (int rg = 0; rg < ko.n && ok; ++rg) {
+            for (int kb = ko.lo(rg), kb_hi = ko.hi(rg); kb < kb_hi; ++kb) {
+              // Inline fast path: the stage is usually full already.
+              if (!mbar_try_wait(&full_bar[stage], phase) &&
+                  !wait_bar(&full_bar[stage], phase, aux, limit)) {
+                if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              // Descriptors advance linearly with the (16-byte granular)
+              // address: by 32 bytes per 16-k slice inside a K-major 128-byte
+              // row, or by two 8-row k groups (2048 bytes) of an MN-major box.
+              const uint64_t ad0 = ring_desc + (uint64_t)((stage * C::STAGE_BYTES) >> 4) + a_lbo;
+              const uint64_t bd0 = ring_desc +
+                                   (uint64_t)((stage * C::STAGE_BYTES + C::A_BYTES) >> 4) + b_lbo;
+  #pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk) {
+                const uint32_t acc = (kb != kb_first || kk > 0) ? 1u : 0u;
+                const uint64_t ad = ad0 + (uint64_t)(kk * a_step), bd = bd0 + (uint64_t)(kk * b_step);
+                if constexpr (C::PAIR) umma_f16_pair(d, ad, bd, idesc, acc);
+                else umma_f16(d, ad, bd, idesc, acc);
+              }
+              issued = true;
+              if constexpr (C::PAIR) umma_commit_pair(&empty_bar[stage]);  // both CTAs' stage
+              else umma_commit(&empty_bar[stage]);
+              if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1;
+              }
             }
-            tc_fence_after();
-            // Descriptors advance linearly with the (16-byte granular)
-            // address: by 32 bytes per 16-k slice inside a K-major 128-byte
-            // row, or by two 8-row k groups (2048 bytes) of an MN-major box.
-            const uint64_t ad0 = ring_desc + (uint64_t)((stage * C::STAGE_BYTES) >> 4) + a_lbo;
-            const uint64_t bd0 = ring_desc +
-                                 (uint64_t)((stage * C::STAGE_BYTES + C::A_BYTES) >> 4) + b_lbo;
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-              const uint64_t ad = ad0 + (uint64_t)(kk * a_step), bd = bd0 + (uint64_t)(kk * b_step);
-              if constexpr (C::PAIR) umma_f16_pair(d, ad, bd, idesc, acc);
-              else umma_f16(d, ad, bd, idesc, acc);
-            }
-            issued = true;
-            if constexpr (C::PAIR) umma_commit_pair(&empty_bar[stage]);  // both CTAs' stage
-            else umma_commit(&empty_bar[stage]);
-            if (kb == inj_kb_here) {
+            if (ok && rg == ko.pause) {
               // Mid-mainloop fault injection (testing only): once these MMAs
               // are done, the epilogue warp of the row's lane quadrant flips
               // the value in TMEM; the next MMAs accumulate onto it.
@@ -1374,15 +1468,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!wait_bar(injdone_bar, 0, aux, limit, true, C::PAIR)) {
                 if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
                 ok = false;
-                break;
               }
               tc_fence_after();
             }
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1;
-            }
-            if (++kb == w.kb_end) kb = w.kb_begin;
           }
         } else {
           // Packed checksum stages: A(k), A(k+1), enc(k), enc(k+1).
@@ -1677,38 +1765,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // Mid-mainloop fault injection (testing only): once the MMAs up to MAC
       // iteration inj_kb are done, the warp of the row's lane quadrant flips
-      // the value in TMEM and releases the MMA thread.
-      if (mid_inject_item<C::PAIR>(p, s, w, (int)crank) && q == (p.inj_row[0] >> 5)) {
-        const bool fine = __all_sync(0xffffffffu, wait_bar(inj_bar, 0, aux, limit, true, C::PAIR));
-        if (fine) {
-          tc_fence_after();
-          const uint32_t ta = tmem_base + ab * C::ACC_COLS + ((uint32_t)(q * 32) << 16) +
-                              (uint32_t)((p.inj_col[0] >> 5) * 32);
-          uint32_t u[32];
-          tmem_ld32(ta, u);
-          if (lane == (p.inj_row[0] & 31)) {
-            const int jc = p.inj_col[0] & 31;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i == jc) {
-                const uint32_t before = u[i];
-                u[i] ^= 1u << p.inj_bit[0];
-                p.report->mid_before = __uint_as_float(before);
-                p.report->mid_after = __uint_as_float(u[i]);
-                atomicAdd(&p.report->mid_injected, 1u);
-              }
-          }
-          tmem_st32(ta, u);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            if constexpr (C::PAIR) mbar_arrive_cluster(cluster_addr(injdone_bar, 0));
-            else mbar_arrive(injdone_bar);
-          }
-        } else if (lane == 0 && !aborted(aux)) {
-          record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
-        }
-      }
+      // the value in TMEM and releases the MMA thread (kept out of line).
+      if (p.inj_kb >= 0 && mid_inject_item<C::PAIR>(p, s, w, (int)crank) &&
+          q == (p.inj_row[0] >> 5))
+        mid_inject_flip<C::PAIR>(p, tmem_base + ab * C::ACC_COLS, q, lane, inj_bar, injdone_bar,
+                                 aux, limit);
 
       bool got = wait_bar_inline<C::PAIR>(&tfull_bar[ab], aphase, aux, limit);
       if (!got && !aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
