@@ -200,6 +200,16 @@ typedef struct {
                            iterations and wraps around to its first one, so
                            CTAs that read the same operand columns do not all
                            start at the same k. Sums are re-associated only. */
+  int32_t abft_inloop;  /* ABFT reference checksums accumulated inside the
+                           mainloop: every k-step also runs the checksum MMAs
+                           cr += A_s (B e)_s and cc += B_s (e^T A)_s on the
+                           stage's operand tiles and the encodings of that
+                           k-step, into TMEM next to the accumulator, so no
+                           separate checksum tiles run and no verification
+                           waits for other CTAs. Data-parallel plans of
+                           128 x 128 tiles or 256 x 256 CTA-pair tiles,
+                           K-major operands. 0 = the library decides,
+                           1 = never, 2 = whenever the call allows it. */
 } skg_opts_t;
 
 /* One segment of a schedule (Stream-K page, Algorithm 5 / §5.2). k_iter_*
@@ -373,6 +383,9 @@ typedef struct {
                           pass, so the call is a single launch */
   int32_t local_checksums; /* ABFT: 1 = the reference checksums are formed in
                           each CTA (skg_opts_t.abft_local), a single launch */
+  int32_t inloop_checksums; /* ABFT: 1 = the reference checksums are
+                          accumulated by the output tiles' MMAs
+                          (skg_opts_t.abft_inloop), after the encode pass */
 } skg_plan_t;
 
 /* Same choice as skg_launch_shape, with the CTA-pair and checksum-tile

@@ -84,9 +84,22 @@ struct Resolved {
   int raster_band;
   int enc_inkernel;  // the dedicated side CTAs run the encode pass (no encode launch)
   int abft_local;    // ABFT references formed in each CTA (one whole tile per CTA)
+  int ilc;           // ABFT references accumulated by the output tiles' MMAs (DP plan)
   int ws_grid;
   int64_t k_for_plan;  // CTAs the workspace's flags and partial slots are sized for
 };
+
+// Whether an ABFT call runs its reference checksums inside the mainloop
+// (skg_opts_t.abft_inloop): always when asked, never when refused; left to
+// the library, for shapes whose data-parallel plan needs at most two waves
+// of tiles, where the separate checksum tiles' chain of global
+// synchronisations is longer than the mainloop (measured on GB300).
+bool ilc_wanted(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, const Resolved& r,
+                int ms) {
+  if (o->abft_inloop == 1) return false;
+  if (o->abft_inloop == 2) return true;
+  return false;
+}
 
 // Schedule, g and BLK_N: whatever the options leave open is chosen by the
 // grid-size model (skg_model.h). A fixed schedule with grid 0 runs on all
@@ -176,6 +189,31 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
   r.raster_band = o->raster_band;
   r.enc_inkernel = 0;
   if (o->abft_local < 0 || o->abft_local > 2) return SKG_ERR_ARG;
+  if (o->abft_inloop < 0 || o->abft_inloop > 2) return SKG_ERR_ARG;
+  // In-loop reference checksums: a data-parallel plan over 128 x 128 tiles
+  // on single CTAs or 256 x 256 tiles on CTA pairs (the choice above).
+  r.ilc = 0;
+  if (r.abft && o->abft_local != 2 && m > 0 && n > 0 && k > 0 &&
+      (o->sched == SKG_SCHED_AUTO || o->sched == SKG_SCHED_DP) &&
+      ilc_wanted(m, n, k, o, r, ms)) {
+    if (r.pair) {
+      const int clusters = r.grid_max / 2;
+      const int64_t ptiles = ((m + 2 * kBM - 1) / (2 * kBM)) * ((n + 255) / 256);
+      const int64_t want = o->grid > 0 ? o->grid / 2 : (ptiles < clusters ? ptiles : clusters);
+      r.grid = 2 * (int)want;
+      r.ilc = 1;
+    } else if (o->tile_n == 0 || o->tile_n == 128) {
+      const int64_t tiles = ((m + kBM - 1) / kBM) * ((n + 127) / 128);
+      r.bn = 128;
+      r.grid = o->grid > 0 ? o->grid : (int)(tiles < ms ? tiles : ms);
+      r.ilc = 1;
+    }
+    if (r.ilc) {
+      r.sched = SKG_SCHED_DP;
+      r.grid_ck = 0;
+      if (r.ws_grid < r.grid) r.ws_grid = r.grid;
+    }
+  }
   // In-CTA ABFT references (on request): a data-parallel plan of at most
   // one 128 x 128 tile per SM on single CTAs, so each CTA's epilogue warps
   // can read every stage of its one tile.
@@ -353,13 +391,14 @@ struct Gemm {
   int a_mn = 0, b_mn = 0;
 };
 
-template <int BN, bool ABFT, bool PAIR = false, bool LOCAL = false, bool MN = false>
+template <int BN, bool ABFT, bool PAIR = false, bool LOCAL = false, bool MN = false,
+          bool ILC = false>
 cudaError_t dispatch_out(int out_dtype, const Maps& mp, const KernelParams& p, int grid,
                          cudaStream_t st) {
   switch (out_dtype) {
-    case SKG_OUT_F32: return launch_gemm<BN, ABFT, 0, PAIR, LOCAL, MN>(mp, p, grid, st);
-    case SKG_OUT_F16: return launch_gemm<BN, ABFT, 1, PAIR, LOCAL, MN>(mp, p, grid, st);
-    default: return launch_gemm<BN, ABFT, 2, PAIR, LOCAL, MN>(mp, p, grid, st);
+    case SKG_OUT_F32: return launch_gemm<BN, ABFT, 0, PAIR, LOCAL, MN, ILC>(mp, p, grid, st);
+    case SKG_OUT_F16: return launch_gemm<BN, ABFT, 1, PAIR, LOCAL, MN, ILC>(mp, p, grid, st);
+    default: return launch_gemm<BN, ABFT, 2, PAIR, LOCAL, MN, ILC>(mp, p, grid, st);
   }
 }
 
@@ -433,6 +472,16 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
     t_ck = ck_cr + (int)(((g.n + kBM - 1) / kBM + ck_half - 1) / ck_half);
   }
 
+  // In-loop checksums: the encodings of one k-step (hi and lo rows) are
+  // loaded with each stage as the N = 16 operand of the checksum MMAs.
+  const bool ilc = abft_epilogue && r.ilc;
+  if (ilc &&
+      (make_map(&mp.ea, in_t, 2, ws + L.enc_a, (uint64_t)L.kp, (uint64_t)kEncRows * L.tiles_a,
+                (uint64_t)L.kp, kBK, kEncRows) != CUDA_SUCCESS ||
+       make_map(&mp.be, in_t, 2, ws + L.enc_b, (uint64_t)L.kp, (uint64_t)kEncRows * L.tiles_b,
+                (uint64_t)L.kp, kBK, kEncRows) != CUDA_SUCCESS))
+    return SKG_ERR_UNSUPPORTED;
+
   KernelParams p;
   memset(&p, 0, sizeof(p));
   // CTA pairs: 256-row tiles, one schedule CTA per cluster.
@@ -474,6 +523,10 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
                ((uint32_t)(g.a_mn != 0) << 15);
   p.idesc_cc = idesc_f16(g.in_dtype == SKG_IN_BF16, ck_half * kBM, (uint32_t)p.ck_rows_cc) |
                ((uint32_t)(g.b_mn != 0) << 15);
+  if (ilc) {  // checksum MMAs of the output tiles: M = the tile's rows, N = 16
+    p.idesc_cr = idesc_f16(g.in_dtype == SKG_IN_BF16, r.pair ? 2 * kBM : kBM, 16);
+    p.idesc_cc = p.idesc_cr;
+  }
   p.hdr = (WsHeader*)ws;
   p.report = (skg_report_t*)(ws + 256);
   p.flags = (uint32_t*)(ws + L.flags);
@@ -525,7 +578,10 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   const int od = g.out_dtype;
   const int lg = launch_grid;
   cudaError_t e;
-  if (r.pair)
+  if (ilc)
+    e = r.pair ? dispatch_out<256, true, true, false, false, true>(od, mp, p, lg, stream)
+               : dispatch_out<128, true, false, false, false, true>(od, mp, p, lg, stream);
+  else if (r.pair)
     e = abft_epilogue ? dispatch_layout<256, true, true>(mn, od, mp, p, lg, stream)
                       : dispatch_layout<256, false, true>(mn, od, mp, p, lg, stream);
   else if (r.bn == 128)
@@ -797,8 +853,16 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
   g.a_mn = !copies && a_layout == SKG_A_COL;
   g.b_mn = !copies && b_layout == SKG_B_NMAJOR;
   bool fuse = false;
+  if (r.ilc && (g.a_mn || g.b_mn)) r.ilc = 0;  // in-loop checksums read K-major stages
   if (r.abft && r.abft_local) {
     // The reference checksums are formed inside the CTAs: one launch.
+  } else if (r.abft && r.ilc) {
+    // The encode pass, then one launch whose MMAs also accumulate the
+    // reference checksums.
+    if (!r.preencoded) {
+      st = run_encode_layouts(in_dtype, A, lda, 0, m, B, ldb, 0, n, k, r, ws, L, sms, stream);
+      if (st != SKG_OK) return st;
+    }
   } else if (r.abft && can_fuse_checksums(L, r.bn)) {
     // The checksum-GEMM tiles run ahead of the output tiles in the same
     // launch, after the encode pass (skipped when pre-encoded).
@@ -974,7 +1038,8 @@ skg_status_t skg_launch_shape(int64_t m, int64_t n, int64_t k, const skg_opts_t*
   const int sms = sm_count_cached();
   skg_status_t st = resolve(m, n, k, opts, r, sms);
   if (st != SKG_OK) return st;
-  if (r.abft && m > 0 && n > 0 && k > 0 && can_fuse_checksums(layout(m, n, k, r), r.bn))
+  if (r.abft && !r.abft_local && !r.ilc && m > 0 && n > 0 && k > 0 &&
+      can_fuse_checksums(layout(m, n, k, r), r.bn))
     plan_fused(m, n, opts, SKG_IN_BF16, true, r);
   if (tile_n) *tile_n = r.bn;
   if (grid) *grid = r.grid + r.grid_ck;
@@ -989,7 +1054,7 @@ skg_status_t skg_launch_plan(int64_t m, int64_t n, int64_t k, const skg_opts_t* 
   const int sms = sm_count_cached();
   skg_status_t st = resolve(m, n, k, opts, r, sms);
   if (st != SKG_OK) return st;
-  const bool fused = r.abft && !r.abft_local && m > 0 && n > 0 && k > 0 &&
+  const bool fused = r.abft && !r.abft_local && !r.ilc && m > 0 && n > 0 && k > 0 &&
                      can_fuse_checksums(layout(m, n, k, r), r.bn);
   if (fused) plan_fused(m, n, opts, SKG_IN_BF16, true, r);
   memset(out, 0, sizeof(*out));
@@ -1002,6 +1067,7 @@ skg_status_t skg_launch_plan(int64_t m, int64_t n, int64_t k, const skg_opts_t* 
   out->fused_checksums = fused ? 1 : 0;
   out->encode_in_kernel = r.enc_inkernel;
   out->local_checksums = r.abft_local;
+  out->inloop_checksums = r.ilc;
   return SKG_OK;
 }
 

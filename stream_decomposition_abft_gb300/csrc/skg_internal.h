@@ -54,10 +54,12 @@ struct Maps {
 };
 
 // Launch the persistent kernel instantiated for (BN, ABFT, OUT, PAIR, LOCAL,
-// MN) on `grid` CTAs (PAIR: grid / 2 clusters of two; LOCAL: in-CTA ABFT
-// references; MN: MN-major operands possible). Defined in the skg_inst_*.cu
+// MN, ILC) on `grid` CTAs (PAIR: grid / 2 clusters of two; LOCAL: in-CTA ABFT
+// references; MN: MN-major operands possible; ILC: reference checksums
+// accumulated by MMAs in the mainloop). Defined in the skg_inst_*.cu
 // translation units.
-template <int BN, bool ABFT, int OUT, bool PAIR = false, bool LOCAL = false, bool MN = false>
+template <int BN, bool ABFT, int OUT, bool PAIR = false, bool LOCAL = false, bool MN = false,
+          bool ILC = false>
 cudaError_t launch_gemm(const Maps& mp, const KernelParams& p, int grid, cudaStream_t stream);
 
 // Clusters of two CTAs of the pair kernel (BLK_N = 256) that can be resident

@@ -187,10 +187,19 @@ __host__ __device__ constexpr int pow2_at_least(int v) {
   return p;
 }
 
-template <int BN_, bool ABFT_, int OUT_, bool PAIR_ = false, bool LOCAL_ = false, bool MN_ = false>
+template <int BN_, bool ABFT_, int OUT_, bool PAIR_ = false, bool LOCAL_ = false, bool MN_ = false,
+          bool ILC_ = false>
 struct Cfg {
   static constexpr int BN = BN_;
   static constexpr bool ABFT = ABFT_;
+  // In-loop reference checksums: every k-step also issues the checksum MMAs
+  // cr += A_s (B e)_s and cc += B_s (e^T A)_s into TMEM columns next to the
+  // accumulator, from encodings the encode pass wrote (loaded with each
+  // stage), so no separate checksum tiles run. Data-parallel plans only (no
+  // tile is split), K-major operands.
+  static constexpr bool ILC = ILC_;
+  static_assert(!ILC_ || (ABFT_ && !LOCAL_ && !MN_), "in-loop checksums: ABFT, K-major");
+  static_assert(!ILC_ || BN_ == 128 || PAIR_, "in-loop checksums: 128-wide tiles or CTA pairs");
   // MN-major operands possible (KernelParams::a_mn / b_mn); the K-major-only
   // instantiations carry no layout code in the producer and MMA loops.
   static constexpr bool MN = MN_;
@@ -205,14 +214,27 @@ struct Cfg {
   static constexpr bool PAIR = PAIR_;
   static constexpr int OUT_BYTES = OUT == 0 ? 4 : 2;
   static constexpr int EPI_COLS = 128 / OUT_BYTES;  // one 128-byte staging row
-  static constexpr int ACC_COLS = BN;
+  // TMEM columns per accumulator buffer: the tile, then (ILC) 16 columns of
+  // row-checksum sums (cr: hi, lo) and 16 of column-checksum sums (cc: hi,
+  // lo; for a CTA pair also the other half's at +8).
+  static constexpr int CR_COL = BN;
+  static constexpr int CC_COL = BN + 16;
+  static constexpr int ACC_COLS = BN + (ILC ? 32 : 0);
   static constexpr int ACC_BUFS = (2 * ACC_COLS <= 512) ? 2 : 1;
   static constexpr int TMEM_COLS = pow2_at_least(ACC_BUFS * ACC_COLS);
   static constexpr int A_BYTES = kBM * kBK * 2;
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
   static constexpr int B_BYTES = B_ROWS * kBK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  // ILC: each stage also holds the k-step's encodings as the N = 16 B operand
+  // of the checksum MMAs (rows hi, lo, then zeros; a CTA pair splits N, so
+  // each CTA holds 8 rows): e^T A of this CTA's 128 rows, and B e of the tile.
+  static constexpr int ENC_ROWS = PAIR ? 8 : 16;
+  static constexpr int ENC_SLOT_BYTES = ILC ? ENC_ROWS * 128 : 0;
+  static constexpr int ENCA_OFF = A_BYTES + B_BYTES;
+  static constexpr int ENCB_OFF = ENCA_OFF + ENC_SLOT_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + 2 * ENC_SLOT_BYTES;
   static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t ENC_BOX_BYTES = 2 * kBK * 2;  // hi and lo rows of one k-step
   // Packed checksum stage: two A tiles, then two encoding slots of ENC_SLOT bytes.
   static constexpr int ENC_SLOT = 8192;
   static constexpr bool CK_PACK = !PAIR && STAGE_BYTES >= 2 * A_BYTES + 2 * ENC_SLOT;
@@ -223,10 +245,15 @@ struct Cfg {
   // The ABFT column partial sums of warp q (BN floats) live in warp q's own
   // first staging buffer, which is idle while a tile is being verified.
   static_assert(BN * 4 <= EPI_BUF_BYTES, "column sums must fit one staging buffer");
+  // ILC with CTA pairs: each CTA's TMEM holds the column sums of its 128 B
+  // rows for both halves' e^T A; the halves swap the other's through this
+  // buffer (two tiles' worth, 128 floats each).
+  static constexpr int XBUF_BYTES = (ILC && PAIR) ? 2 * 128 * 4 : 0;
   static constexpr int STAGES_FIT =
-      (int)((kSmemLimit - 1024 - EPI_BYTES - AUX_BYTES) / STAGE_BYTES);
+      (int)((kSmemLimit - 1024 - EPI_BYTES - AUX_BYTES - XBUF_BYTES) / STAGE_BYTES);
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + AUX_BYTES;
+  static constexpr uint32_t SMEM_BYTES =
+      1024 + STAGES * STAGE_BYTES + EPI_BYTES + AUX_BYTES + XBUF_BYTES;
   static_assert(STAGES >= 2, "shared memory too small for two stages");
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory over the per-CTA limit");
   static_assert(TMEM_COLS <= 512, "TMEM over 512 columns");
@@ -236,7 +263,7 @@ struct Cfg {
 // Shared-memory bookkeeping that lives after the stage ring and staging.
 struct Aux {
   uint64_t bars[56];      // full[S], empty[S], tfull[2], tempty[2], c0[4], drain, fix, c0r[4],
-                          // inj, injdone
+                          // inj, injdone, xch
   uint32_t tmem_slot;
   int32_t abort_flag;
   int32_t nbad_r, nbad_c, bad_row, bad_col;
@@ -1097,7 +1124,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // done (inj), the flipped value is back in TMEM (injdone, the leader's).
   uint64_t* inj_bar = c0r_bar + 4;
   uint64_t* injdone_bar = inj_bar + 1;
-  static_assert(2 * 8 + 2 + 2 + 4 + 1 + 4 * kFixSlots + 4 + 2 <= 56, "barrier slots");
+  // ILC with CTA pairs: the peer's column checksums have landed in xbuf.
+  uint64_t* xch_bar = injdone_bar + 1;
+  static_assert(2 * 8 + 2 + 2 + 4 + 1 + 4 * kFixSlots + 4 + 2 + 1 <= 56, "barrier slots");
+  float* xbuf = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(aux) + C::AUX_BYTES);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1137,10 +1167,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The barriers in one go, a lane each: every one counts a single
     // arrival except the accumulator-empty ones, which the epilogue threads
     // release (both CTAs' for a pair).
-    const int nbars = (int)(injdone_bar + 1 - full_bar);
+    const int nbars = (int)(xch_bar + 1 - full_bar);
     for (int i = lane; i < nbars; i += 32) {
       uint64_t* bar = full_bar + i;
       const bool acc_empty = bar >= tempty_bar && bar < tempty_bar + 2;
+      // The exchange barrier counts the peer's 128 epilogue threads.
+      if (bar == xch_bar) {
+        mbar_init(bar, kEpiThreads);
+        continue;
+      }
       // In-CTA ABFT: the epilogue also reads every stage, so a stage is
       // free once the MMA commit and the epilogue have both arrived.
       const bool stage_empty = bar >= empty_bar && bar < empty_bar + STAGES;
@@ -1148,6 +1183,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                : ((C::LOCAL && stage_empty) ? 2 : 1));
     }
     fence_barrier_init();
+  }
+  if constexpr (C::ILC) {
+    // Encoding slots: the TMA writes rows 0 and 1 of each (hi, lo); the
+    // other rows stay zero for the N = 16 checksum MMAs that read them.
+    constexpr int kSlotChunks = 2 * C::ENC_SLOT_BYTES / 16;
+    for (int i = threadIdx.x; i < STAGES * kSlotChunks; i += kThreads)
+      *reinterpret_cast<uint4*>(ring + (i / kSlotChunks) * C::STAGE_BYTES + C::ENCA_OFF +
+                                (i % kSlotChunks) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
   }
   if (warp == 1) {
     if constexpr (C::PAIR) {
@@ -1242,12 +1286,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tx = C::TX_BYTES;
         int kpack = 1;
         int rowA, rowB;
+        int enc_ra = 0, enc_rb = 0;  // ILC: hi rows of this CTA's e^T A and the tile's B e
         bool amn = C::MN && p.a_mn != 0, bmn = C::MN && p.b_mn != 0;  // MN-major boxes
         if (w.tile >= s.t_ck) {
           int tm, tn;
           tile_coords(s, w.tile, tm, tn);
           rowA = tm * (C::PAIR ? 2 * kBM : kBM) + row_half;
           rowB = tn * BN + (C::PAIR ? (int)crank * C::B_ROWS : 0);
+          enc_ra = kEncRows * (rowA / kBM);
+          enc_rb = kEncRows * tn;
         } else if (w.tile < p.ck_cr_tiles) {
           bmn = false;
           // Checksum tile: the encoding box holds only the rows the MMA uses.
@@ -1289,7 +1336,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               // Both CTAs' copies complete on the leader's full barrier; the
               // leader expects the pair's bytes.
               const uint32_t fb = cluster_addr(&full_bar[stage], 0);
-              if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * tx);
+              // ILC: both CTAs load their e^T A rows, the leader the tile's B e.
+              if (leader)
+                mbar_arrive_expect_tx(&full_bar[stage], 2 * tx + (C::ILC ? 3 * C::ENC_BOX_BYTES : 0));
+              if constexpr (C::ILC) {
+                tma_load_2d_pair(st + C::ENCA_OFF, &tmEA, fb, kb * kBK, enc_ra);
+                if (leader) tma_load_2d_pair(st + C::ENCB_OFF, &tmBE, fb, kb * kBK, enc_rb);
+              }
               if constexpr (!a_box) {
                 tma_load_2d_pair(st, mapA, fb, kb * kBK, rowA);
               } else {
@@ -1304,7 +1357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    kb * kBK);
               }
             } else if (kpack == 1) {
-              mbar_arrive_expect_tx(&full_bar[stage], tx);
+              mbar_arrive_expect_tx(&full_bar[stage], tx + (C::ILC ? 2 * C::ENC_BOX_BYTES : 0));
+              if constexpr (C::ILC) {
+                tma_load_2d(st + C::ENCA_OFF, &tmEA, &full_bar[stage], kb * kBK, enc_ra);
+                tma_load_2d(st + C::ENCB_OFF, &tmBE, &full_bar[stage], kb * kBK, enc_rb);
+              }
               if constexpr (!a_box) {
                 tma_load_2d(st, mapA, &full_bar[stage], kb * kBK, rowA);
               } else {
@@ -1451,6 +1508,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (C::PAIR) umma_f16_pair(d, ad, bd, idesc, acc);
                 else umma_f16(d, ad, bd, idesc, acc);
               }
+              if constexpr (C::ILC) {
+                // The reference checksums of this k-step: cr += A_s (B e)_s
+                // (A as the A operand, the B e rows as N) and cc += B_s
+                // (e^T A)_s (B's rows as the A operand, the e^T A rows as N).
+                const uint64_t ea0 = ring_desc + (uint64_t)((stage * C::STAGE_BYTES + C::ENCA_OFF) >> 4);
+                const uint64_t eb0 = ring_desc + (uint64_t)((stage * C::STAGE_BYTES + C::ENCB_OFF) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                  const uint32_t acc = (kb != kb_first || kk > 0) ? 1u : 0u;
+                  if constexpr (C::PAIR) {
+                    umma_f16_pair(d + C::CR_COL, ad0 + kk * 2, eb0 + kk * 2, p.idesc_cr, acc);
+                    umma_f16_pair(d + C::CC_COL, bd0 + kk * 2, ea0 + kk * 2, p.idesc_cc, acc);
+                  } else {
+                    umma_f16(d + C::CR_COL, ad0 + kk * 2, eb0 + kk * 2, p.idesc_cr, acc);
+                    umma_f16(d + C::CC_COL, bd0 + kk * 2, ea0 + kk * 2, p.idesc_cc, acc);
+                  }
+                }
+              }
               issued = true;
               if constexpr (C::PAIR) umma_commit_pair(&empty_bar[stage]);  // both CTAs' stage
               else umma_commit(&empty_bar[stage]);
@@ -1559,6 +1634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool c0r_pending = false;  // C0 copies into the ring not yet waited for
     int estage = 0;            // in-CTA ABFT: the epilogue's place in the stage ring
     uint32_t ephase = 0;
+    int xpar = 0;              // ILC pairs: exchange slot (and barrier parity) of the next tile
     int nseg = 0;
     bool store_ok = true;
     bool ck_ready = false;
@@ -1714,7 +1790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pf_ma = ls.ma;
         pf_mb = ls.mb;
       } else if (verify_here) {
-        if (s.t_ck > 0 && !ck_ready) {
+        if (!C::ILC && s.t_ck > 0 && !ck_ready) {
           // The fused checksum tiles must all be stored first. Every CTA runs
           // its own share of them before its first output tile, and dedicated
           // checksum CTAs wait only for each other (all resident), so this
@@ -1742,7 +1818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         pf_ea = p.pub_a[tm].scale_exp;
         pf_eb = p.pub_b[tn].scale_exp;
-        if (m0 + r < p.m) {
+        if (!C::ILC && m0 + r < p.m) {
           const float* crp = p.cr_all + (int64_t)(m0 + r) * p.ld_cr + kEncRows * tn;
           pf_cr0 = __ldcg(crp);
           pf_cr1 = __ldcg(crp + 1);
@@ -1750,7 +1826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < BN / 128; ++h) {
           const int col = n0 + h * 128 + r;
-          if (col < p.n) {
+          if (!C::ILC && col < p.n) {
             const float* ccp = p.cc_all + (int64_t)col * p.ld_cc + kEncRows * tm;
             pf_cc0[h] = __ldcg(ccp);
             pf_cc1[h] = __ldcg(ccp + 1);
@@ -1777,6 +1853,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tacc = tmem_base + ab * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
       const int out_tile = tm * s.tiles_n + tn;  // row-major 128 x BLK_N tile number
+      if constexpr (C::ILC) {
+        if (!is_ck) {
+          // The reference checksums the MMAs accumulated next to the tile:
+          // row r's cr (hi, lo) and, in lane r, the cc of B row r.
+          uint32_t u[32];
+          tmem_ld32(tacc + C::CR_COL, u);
+          pf_cr0 = f32_of(u[0]);
+          pf_cr1 = f32_of(u[1]);
+          if constexpr (!C::PAIR) {
+            pf_cc0[0] = f32_of(u[16]);
+            pf_cc1[0] = f32_of(u[17]);
+          } else {
+            // Lane r of CTA c holds B row c * 128 + r: its column sums for
+            // this half's e^T A (cols 16 + 8c) and for the other half's
+            // (16 + 8 (1 - c)). The halves swap the latter through xbuf.
+            const float s0 = f32_of(u[16]) + f32_of(u[17]);  // for half 0's e^T A
+            const float s1 = f32_of(u[24]) + f32_of(u[25]);  // for half 1's e^T A
+            const float mine = crank == 0 ? s0 : s1, theirs = crank == 0 ? s1 : s0;
+            float* slot = xbuf + xpar * 128 + r;
+            st_shared_cluster_f32(cluster_addr(slot, 1u - crank), theirs);
+            mbar_arrive_cluster(cluster_addr(xch_bar, 1u - crank));
+            const bool got_x = wait_bar(xch_bar, (uint32_t)xpar, aux, limit, true, true);
+            if (!got_x && !aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+            const float peer = got_x ? *reinterpret_cast<volatile float*>(slot) : 0.f;
+            // columns h * 128 + r: h = crank from this CTA, the other from the peer
+            pf_cc0[0] = crank == 0 ? mine : peer;
+            pf_cc0[1] = crank == 0 ? peer : mine;
+            pf_cc1[0] = pf_cc1[1] = 0.f;
+            xpar ^= 1;  // next tile: the other slot and barrier phase parity
+          }
+        }
+      }
       // Fault injection (testing only): this tile gets a flip after its fixup.
       const bool inject_here = !is_ck && w.role != kRolePeer &&
                                ((out_tile == p.inj_tile[0] && p.inj_kb < 0) ||
@@ -1865,7 +1973,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t kC0Bytes = 32u * BN * C::OUT_BYTES;
         constexpr uint32_t kC0Off = (kQuarter - kC0Bytes) & ~1023u;
         constexpr uint32_t kHalf = kPartialBandBytes<BN> / 2;
-        static_assert(kC0Bytes <= kQuarter && kC0Off >= kHalf, "ring quarter too small");
+        // (ILC launches split no tile, so they have no owner fixup to fit.)
+        static_assert(kC0Bytes <= kQuarter && (C::ILC || kC0Off >= kHalf),
+                      "ring quarter too small");
         uint8_t* qring = ring + ew * kQuarter;
         if (last_item && !is_ck && w.role != kRolePeer) {
           c0_ring = p.beta != 0.f && m0 + q * 32 < p.m;  // warp-uniform
@@ -1879,7 +1989,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           c0r_pending = c0_ring;
         }
-        if (owner && !is_ck && last_item) {
+        if (!C::ILC && owner && !is_ck && last_item) {
           const uint32_t room = c0_ring ? kC0Off : kQuarter;
           const int slots = min(kFixSlots, (int)(room / kHalf));
           const bool fine = fixup_through_ring<BN>(

@@ -9,9 +9,9 @@
 
 namespace skg {
 
-template <int BN, bool ABFT, int OUT, bool PAIR, bool LOCAL, bool MN>
+template <int BN, bool ABFT, int OUT, bool PAIR, bool LOCAL, bool MN, bool ILC>
 cudaError_t launch_gemm(const Maps& mp, const KernelParams& p, int grid, cudaStream_t stream) {
-  using C = Cfg<BN, ABFT, OUT, PAIR, LOCAL, MN>;
+  using C = Cfg<BN, ABFT, OUT, PAIR, LOCAL, MN, ILC>;
   // The shared-memory opt-in is per device; set it once per device.
   static std::atomic<uint64_t> done_mask{0};
   int dev = 0;

@@ -102,6 +102,12 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Store one float into the shared memory of either CTA of the cluster (a
+// shared::cluster address from cluster_addr).
+__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr_cluster, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr_cluster), "f"(v) : "memory");
+}
+
 // Arrive on an mbarrier of either CTA of the cluster (release, cluster scope).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)

@@ -47,7 +47,7 @@ class Opts(ctypes.Structure):
                 ("abft_local", ctypes.c_int32), ("inject2_tile", ctypes.c_int32),
                 ("inject2_row", ctypes.c_int32), ("inject2_col", ctypes.c_int32),
                 ("inject2_bit", ctypes.c_int32), ("inject_kstep", ctypes.c_int32),
-                ("stagger", ctypes.c_int32)]
+                ("stagger", ctypes.c_int32), ("abft_inloop", ctypes.c_int32)]
 
 
 class Segment(ctypes.Structure):
@@ -70,7 +70,8 @@ class Plan(ctypes.Structure):
     _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("ctas", ctypes.c_int32),
                 ("cta_pair", ctypes.c_int32), ("sched", ctypes.c_int32),
                 ("side_ctas", ctypes.c_int32), ("fused_checksums", ctypes.c_int32),
-                ("encode_in_kernel", ctypes.c_int32), ("local_checksums", ctypes.c_int32)]
+                ("encode_in_kernel", ctypes.c_int32), ("local_checksums", ctypes.c_int32),
+                ("inloop_checksums", ctypes.c_int32)]
 
 
 class Report(ctypes.Structure):

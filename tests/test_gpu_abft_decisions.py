@@ -175,6 +175,9 @@ PLANS = {
     "sk_128": dict(tile_n=128, sched="sk", cta_pair=1, grid=37),
     "sk2dp_256": dict(tile_n=256, sched="sk2_dp", cta_pair=1, grid=19),
     "pairs_256": dict(tile_n=256, cta_pair=2, sched="sk", grid=12),
+    # reference checksums accumulated in the mainloop, several tiles per CTA
+    "inloop_128": dict(tile_n=128, cta_pair=1, abft_inloop=2, grid=5),
+    "inloop_pairs": dict(tile_n=256, cta_pair=2, abft_inloop=2, grid=4),
 }
 
 
@@ -534,3 +537,55 @@ def test_workspace_reused_across_shapes_and_options():
         else:
             from gpu_util import check_sampled
             check_sampled(p, C, seed=i)
+
+
+# --------------------------------------------------------------------------- in-loop checksums
+@pytest.mark.parametrize("pair", [1, 2])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("shape", [(300, 200, 200), (1000, 1300, 520), (1024, 1024, 1024),
+                                   (129, 3000, 4104), (2048, 2048, 2048)])
+def test_inloop_checksums_clean(shape, dtype, pair):
+    # The checksum MMAs run in the output tiles' mainloop: every tile
+    # verified, no false positive, ragged m, n and k, fp16 encodings scaled
+    # per tile, one or several tiles per CTA.
+    m, n, k = shape
+    p = inputs.make_problem(m, n, k, seed=m + n + k, in_dtype=dtype, out_dtype="f32",
+                            law_a="normal", law_b="normal", alpha=0.75, beta=0.5)
+    bn = 256 if pair == 2 else 128
+    for grid in (0, 4):
+        o = skgemm.opts_default(abft=1, abft_inloop=2, cta_pair=pair, tile_n=bn, grid=grid)
+        plan = skgemm.launch_plan(m, n, k, o)
+        assert plan.inloop_checksums == 1 and plan.fused_checksums == 0
+        assert plan.sched == skgemm.SCHED_DP and plan.side_ctas == 0
+        ws = None
+        for _ in range(2):
+            C, ws, st = run(p, o, ws=ws)
+            assert st == skgemm.OK
+            check_full(p, C)
+            rep = ws.report(reset=True)
+            assert rep.detected == 0 and rep.status_bits == 0
+            assert rep.tiles_checked == -(-m // 128) * -(-n // bn)
+            assert rep.max_ratio_row < 0.1 and rep.max_ratio_col < 0.1
+
+
+def test_inloop_mid_mainloop_flip():
+    # A flip inside the mainloop of an in-loop-checksum launch: the checksum
+    # MMAs see the clean operands, the accumulator the faulty partial sum.
+    p = integer_problem(seed=11)
+    C_exact = reference(p)
+    for kw in (PLANS["inloop_128"], PLANS["inloop_pairs"]):
+        bn = kw["tile_n"]
+        tiles_n = N // bn
+        tile = 5
+        tm, tn = divmod(tile, tiles_n)
+        r, c, j = 77, 100, 3
+        o = skgemm.opts_default(abft=1, inject_tile=tile, inject_row=r, inject_col=c,
+                                inject_bit=30, inject_kstep=j, **kw)
+        C, ws, st = run(p, o)
+        assert st == skgemm.OK
+        rep = ws.report()
+        assert rep.mid_injected == 1 and rep.detected == 1 and rep.corrected == 1
+        rec = gpu_records(rep)[tile]
+        assert (rec.row, rec.col) == (r, c)
+        assert rec.after == C_exact[tm * 128 + r, tn * bn + c]
+        assert np.array_equal(C.cpu().double().numpy(), C_exact)
