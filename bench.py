@@ -819,6 +819,92 @@ def workload_mlp(args):
                                   "launches", "results": results}), flush=True)
 
 
+def workload_fp64(args):
+    """fp64 GEMM rate: skg_gemm_f64 against the library DGEMM (torch.matmul on
+    double, which is cuBLAS), m = n = k in {2048, 4096, 8192}, inputs resident
+    (the fp64 peak the fp64 kernel is compared with)."""
+    import torch
+    from stream_decomposition_abft_gb300 import _build, skgemm
+    if not os.path.exists(skgemm.LIB_PATH):
+        _build.build()
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    res = []
+    for s in (2048, 4096, 8192):
+        gen = torch.Generator(device=dev).manual_seed(s)
+        a = torch.randn(s, s, dtype=torch.float64, device=dev, generator=gen)
+        b = torch.randn(s, s, dtype=torch.float64, device=dev, generator=gen)
+        c = torch.empty(s, s, dtype=torch.float64, device=dev)
+        o = skgemm.opts_default()
+        ws = skgemm.Workspace(skgemm.workspace_size_f64(s, s, s, o), dev)
+
+        def ours():
+            st = skgemm.gemm_f64(s, s, s, 1.0, a.data_ptr(), s, b.data_ptr(), s, 0.0, c.data_ptr(),
+                                 s, o, ws.ptr, ws.nbytes, sh)
+            if st != skgemm.OK:
+                raise skgemm.SkgError(st, "skg_gemm_f64")
+
+        row = {"size": s}
+        for name, fn in (("torch_matmul_fp64", lambda: torch.matmul(a, b)), ("skg_gemm_f64", ours)):
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(max(5, args.steps // 20)):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e-3)
+            row[name + "_tflops"] = round(2.0 * s ** 3 / statistics.median(ts) / 1e12, 3)
+        res.append(row)
+    print(json.dumps({"workload": "fp64 GEMM rate (inputs resident)", "results": res}), flush=True)
+
+
+def workload_stagger(args):
+    """k staggering (skg_opts_t.stagger) A/B on the power-of-two square shapes,
+    bf16, with and without ABFT, L2 flushed before each launch: median
+    event time (us) per stagger value."""
+    import torch
+    from stream_decomposition_abft_gb300 import _build, inputs, skgemm
+    if not os.path.exists(skgemm.LIB_PATH):
+        _build.build()
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = []
+    for size in (1024, 2048, 4096, 8192):
+        p = inputs.make_problem(size, size, size, seed=1, in_dtype="bf16", out_dtype="bf16",
+                                law_a="normal", law_b="normal", scale_a=size ** -0.5,
+                                scale_b=size ** -0.5)
+        A, B = p.A.to(dev), p.B.to(dev)
+        C = torch.empty((size, size), dtype=torch.bfloat16, device=dev)
+        row = {"size": size}
+        for abft in (0, 1):
+            for sg in (0, 2, 4, 8):
+                o = skgemm.opts_default(abft=abft, stagger=sg)
+                ws = skgemm.Workspace(skgemm.workspace_size(size, size, size, o), dev)
+
+                def launch():
+                    st = skgemm.gemm(size, size, size, 1.0, A.data_ptr(), size, B.data_ptr(), size,
+                                     0.0, C.data_ptr(), size, skgemm.IN_BF16, skgemm.OUT_BF16, 0, 0,
+                                     o, ws.ptr, ws.nbytes, sh)
+                    if st != skgemm.OK:
+                        raise skgemm.SkgError(st, "skg_gemm")
+
+                for _ in range(4):
+                    flush.zero_()
+                    launch()
+                row[f"{'abft' if abft else 'plain'}_stagger{sg}_us"] = round(
+                    1e3 * _time_launch(launch, flush, 30, stream), 2)
+                if ws.report().detected:
+                    raise RuntimeError("ABFT reported a fault on a clean run")
+        out.append(row)
+    print(json.dumps({"workload": "k staggering A/B, square bf16", "results": out}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -840,7 +926,7 @@ def main():
                     help="with --ncu-target --shape: fp16 without ABFT")
     ap.add_argument("--write-traffic", default="",
                     help="write the traffic JSON from an ncu CSV of the main kernel")
-    ap.add_argument("--workload", choices=["square", "hostile", "random", "mlp"],
+    ap.add_argument("--workload", choices=["square", "hostile", "random", "mlp", "fp64", "stagger"],
                     default="square", help="square = the metric's sweep (default)")
     ap.add_argument("--limit", type=int, default=0, help="random: first N shapes only")
     ap.add_argument("--launches", type=int, default=300, help="mlp: launches per shape")
@@ -852,8 +938,8 @@ def main():
         ncu_target(args)
         return
     if args.workload != "square":
-        {"hostile": workload_hostile, "random": workload_random,
-         "mlp": workload_mlp}[args.workload](args)
+        {"hostile": workload_hostile, "random": workload_random, "mlp": workload_mlp,
+         "fp64": workload_fp64, "stagger": workload_stagger}[args.workload](args)
         return
     if args.warmup < 3:
         args.warmup = 3

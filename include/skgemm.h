@@ -375,7 +375,7 @@ typedef struct {
   int32_t ctas;        /* CTAs launched for the output tiles */
   int32_t cta_pair;    /* 1 = single CTAs, 2 = clusters of two CTAs */
   int32_t sched;       /* skg_sched_t */
-  int32_t side_ctas;   /* extra CTAs running whole ABFT checksum tiles (0 =
+  int32_t side_ctas;   /* extra CTAs for the ABFT checksum tiles (0 =
                           checksum tiles split over the CTAs above) */
   int32_t fused_checksums; /* ABFT: 1 = checksum GEMMs run inside the main
                           launch, 0 = as separate launches (or no ABFT) */
@@ -386,6 +386,9 @@ typedef struct {
   int32_t inloop_checksums; /* ABFT: 1 = the reference checksums are
                           accumulated by the output tiles' MMAs
                           (skg_opts_t.abft_inloop), after the encode pass */
+  int32_t side_checksum_ctas; /* of the side CTAs, the first this many run the
+                          checksum tiles (split evenly over them); the others
+                          only take part in the in-kernel encode pass */
 } skg_plan_t;
 
 /* Same choice as skg_launch_shape, with the CTA-pair and checksum-tile

@@ -69,7 +69,8 @@ struct Resolved {
   int grid;     // CTAs launched for the output tiles (two per cluster with pairs)
   int pair;     // 1: clusters of two CTAs, 256 x BLK_N tiles, one M = 256 MMA
   int grid_max; // CTAs that can be resident (pairs: two per resident cluster)
-  int grid_ck;  // dedicated checksum-tile CTAs launched after the grid ones
+  int grid_ck;  // dedicated side CTAs launched after the grid ones
+  int grid_ckt; // of those, the ones that run checksum tiles (the rest only encode)
   int bn;
   int abft;
   float tau_row, tau_col;
@@ -124,6 +125,7 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
   r.sched = pl.sched;
   r.grid = pl.grid;
   r.grid_ck = 0;
+  r.grid_ckt = 0;
   r.bn = pl.bn;
   r.pair = 0;
   r.grid_max = ms;
@@ -487,7 +489,7 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   // CTA pairs: 256-row tiles, one schedule CTA per cluster.
   const int sched_ctas = r.pair ? r.grid / 2 : r.grid;
   p.s = make_schedule(g.m, g.n, g.k, r.pair ? 2 * kBM : kBM, r.bn, kBK, sched_ctas, r.sched, t_ck,
-                      t_ck ? r.grid_ck : 0);
+                      t_ck ? r.grid_ck : 0, t_ck ? r.grid_ckt : -1);
   const int launch_grid = r.grid + p.s.g_ck;
   if (launch_grid > kMaxCtas) return SKG_ERR_UNSUPPORTED;  // flags per region
   // Banded raster: a wave of g tiles covers about (g / band) rows x band
@@ -669,6 +671,7 @@ void replan_fused(int64_t m, int64_t n, const skg_opts_t* opts, Resolved& r) {
   r.grid = pl.grid;
   r.sched = pl.sched;
   r.grid_ck = pl.grid_ck;
+  r.grid_ckt = pl.grid_ck;
 }
 
 // Plan of a call whose checksum GEMMs are fused: grid and schedule with the
@@ -1064,6 +1067,7 @@ skg_status_t skg_launch_plan(int64_t m, int64_t n, int64_t k, const skg_opts_t* 
   out->cta_pair = r.pair ? 2 : 1;
   out->sched = r.sched;
   out->side_ctas = fused ? r.grid_ck : 0;
+  out->side_checksum_ctas = fused ? (r.grid_ck ? r.grid_ckt : 0) : 0;
   out->fused_checksums = fused ? 1 : 0;
   out->encode_in_kernel = r.enc_inkernel;
   out->local_checksums = r.abft_local;

@@ -114,7 +114,7 @@ inline double predict_us(const Schedule& s, const CostModel& M, bool share) {
                       M.d * fix;
     if (tx > worst) worst = tx;
   }
-  for (int x = 0; x < s.g_ck; ++x) {  // dedicated side CTAs: the side region split over them
+  for (int x = 0; x < s.g_ckt; ++x) {  // dedicated side CTAs: the side region split over them
     int64_t iters = 0, tiles = 0, partial = 0;
     double fix = 0.0;
     region_counts(s.ck_q, s.ck_r, s.ck_total, I, x, false, iters, tiles, partial, fix);

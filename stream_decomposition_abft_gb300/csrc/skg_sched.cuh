@@ -53,10 +53,12 @@ struct Schedule {
   int64_t sk_q;       // floor(sk_total / g)
   int sk_r;           // sk_total mod g
   int64_t ck_total;   // side-tile iterations, split over the g CTAs or, with
-                      // g_ck > 0, over the dedicated side CTAs
-  int64_t ck_q;       // floor(ck_total / (g_ck ? g_ck : g))
-  int ck_r;           // ck_total mod (g_ck ? g_ck : g)
+                      // g_ck > 0, over the first g_ckt dedicated side CTAs
+  int64_t ck_q;       // floor(ck_total / (g_ck ? g_ckt : g))
+  int ck_r;           // ck_total mod (g_ck ? g_ckt : g)
   int g_ck;           // dedicated side CTAs g .. g + g_ck - 1 (0: none)
+  int g_ckt;          // of those, the ones that run side tiles (the others
+                      // only take part in the in-kernel encode pass)
   int band;           // tile columns per raster band (tiles_n = row-major)
 };
 
@@ -88,10 +90,11 @@ SKG_HD int dp_tiles(int t, int g, int mode) {
 // flags), its iterations split evenly either
 //   - g_ck == 0: over the g CTAs, so every CTA starts with the same small
 //     share of side work, whatever the schedule of the output tiles; or
-//   - g_ck > 0: over g_ck more CTAs that run nothing else, for launches that
-//     leave SMs idle (g_ck = t_ck gives one whole side tile each).
+//   - g_ck > 0: over g_ckt <= g_ck more CTAs that run nothing else, for
+//     launches that leave SMs idle (g_ckt = t_ck gives one whole side tile
+//     each); g_ckt < 0 means all g_ck.
 SKG_HD Schedule make_schedule(int64_t m, int64_t n, int64_t k, int bm, int bn, int bk, int g,
-                              int mode, int t_ck = 0, int g_ck = 0) {
+                              int mode, int t_ck = 0, int g_ck = 0, int g_ckt = -1) {
   Schedule s;
   s.tiles_m = (int)((m + bm - 1) / bm);
   s.tiles_n = (int)((n + bn - 1) / bn);
@@ -105,8 +108,9 @@ SKG_HD Schedule make_schedule(int64_t m, int64_t n, int64_t k, int bm, int bn, i
   s.sk_q = s.sk_total / g;
   s.sk_r = (int)(s.sk_total % g);
   s.g_ck = s.t_ck > 0 ? g_ck : 0;
+  s.g_ckt = (g_ckt < 0 || g_ckt > s.g_ck) ? s.g_ck : g_ckt;
   s.ck_total = (int64_t)s.t_ck * s.ipt;
-  const int ck_ctas = s.g_ck > 0 ? s.g_ck : g;
+  const int ck_ctas = s.g_ck > 0 ? s.g_ckt : g;
   s.ck_q = s.ck_total / ck_ctas;
   s.ck_r = (int)(s.ck_total % ck_ctas);
   s.band = s.tiles_n > 0 ? s.tiles_n : 1;
@@ -165,10 +169,12 @@ struct Cursor {
     ck_base = 0;
     it = it_end = ck_it = ck_end = 0;
     if (cta >= s.g) {
-      // Dedicated side CTA: its share of the side region, nothing else.
+      // Dedicated side CTA: its share of the side region (the first g_ckt
+      // of them), nothing else.
       next_dp = s.t_dp;
       ck_base = s.g;
-      if (s.ck_total > 0) even_range(s.ck_q, s.ck_r, cta - s.g, ck_it, ck_end);
+      if (s.ck_total > 0 && cta - s.g < s.g_ckt)
+        even_range(s.ck_q, s.ck_r, cta - s.g, ck_it, ck_end);
       return;
     }
     if (s.sk_total > 0) sk_range(s, cta, it, it_end);

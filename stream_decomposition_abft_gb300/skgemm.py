@@ -71,7 +71,7 @@ class Plan(ctypes.Structure):
                 ("cta_pair", ctypes.c_int32), ("sched", ctypes.c_int32),
                 ("side_ctas", ctypes.c_int32), ("fused_checksums", ctypes.c_int32),
                 ("encode_in_kernel", ctypes.c_int32), ("local_checksums", ctypes.c_int32),
-                ("inloop_checksums", ctypes.c_int32)]
+                ("inloop_checksums", ctypes.c_int32), ("side_checksum_ctas", ctypes.c_int32)]
 
 
 class Report(ctypes.Structure):

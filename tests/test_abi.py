@@ -41,7 +41,7 @@ def test_struct_sizes_match_header():
     assert ctypes.sizeof(skgemm.Segment) == 20
     assert ctypes.sizeof(skgemm.FaultRecord) == 64
     assert ctypes.sizeof(skgemm.Report) == 64 + 64 * 64
-    assert ctypes.sizeof(skgemm.Plan) == 40
+    assert ctypes.sizeof(skgemm.Plan) == 44
 
 
 def test_defaults(lib):

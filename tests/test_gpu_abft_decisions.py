@@ -403,15 +403,16 @@ def _trace(p, opts, ctas):
     return out, C, ws
 
 
-def _expected(m, n, k, bm, bn, g, mode, t_ck=0, g_ck=0):
+def _expected(m, n, k, bm, bn, g, mode, t_ck=0, g_ck=0, g_ckt=None):
     """Per schedule CTA: the side-tile region (t_ck full-k tiles split evenly
-    over the g CTAs, or over g_ck extra CTAs), then the output schedule, as
-    the simulator gives them; side tiles carry the numbers -t_ck .. -1."""
+    over the g CTAs, or over the first g_ckt of g_ck extra CTAs), then the
+    output schedule, as the simulator gives them; side tiles carry the
+    numbers -t_ck .. -1."""
     ipt = -(-k // 64)
     out = [[] for _ in range(g + g_ck)]
     if t_ck:
         total = t_ck * ipt
-        split = g_ck if g_ck else g
+        split = (g_ckt if g_ckt is not None else g_ck) if g_ck else g
         base = g if g_ck else 0
         for x in range(split):
             b, e = ss.sk_range(x, total, split)
@@ -482,7 +483,7 @@ def test_trace_abft_dedicated_side_ctas():
     # the output schedule's raster is banded; the trace holds schedule tile
     # indices, so the simulator's row-major numbering applies to them
     want = _expected(m, n, k, 128, plan.tile_n, plan.ctas, names[plan.sched], t_ck,
-                     plan.side_ctas)
+                     plan.side_ctas, plan.side_checksum_ctas)
     assert got == want
     check_full(p, C)
     assert ws.report().detected == 0
