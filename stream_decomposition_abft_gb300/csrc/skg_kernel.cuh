@@ -1479,72 +1479,85 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t a_lbo = amn ? mn_lbo : 0, b_lbo = bmn ? mn_lbo : 0;
         const int a_step = amn ? (2048 >> 4) : 2, b_step = bmn ? (2048 >> 4) : 2;
         if (kpack == 1) {
-          // The producer's k ranges, cut after a mid-mainloop injection.
-          const KOrder ko =
-              k_order(w.kb_begin, w.kb_end,
-                      w.tile >= s.t_ck ? stagger_offset(p, unit, w.kb_end - w.kb_begin) : 0,
-                      mid_inject_item<C::PAIR>(p, s, w, -1) ? p.inj_kb : -1);
-          const int kb_first = ko.lo0;  // the item's first MMA starts the accumulator
-          for (int rg = 0; rg < ko.n && ok; ++rg) {
-            for (int kb = ko.lo(rg), kb_hi = ko.hi(rg); kb < kb_hi; ++kb) {
-              // Inline fast path: the stage is usually full already.
-              if (!mbar_try_wait(&full_bar[stage], phase) &&
-                  !wait_bar(&full_bar[stage], phase, aux, limit)) {
-                if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              // Descriptors advance linearly with the (16-byte granular)
-              // address: by 32 bytes per 16-k slice inside a K-major 128-byte
-              // row, or by two 8-row k groups (2048 bytes) of an MN-major box.
-              const uint64_t ad0 = ring_desc + (uint64_t)((stage * C::STAGE_BYTES) >> 4) + a_lbo;
-              const uint64_t bd0 = ring_desc +
-                                   (uint64_t)((stage * C::STAGE_BYTES + C::A_BYTES) >> 4) + b_lbo;
-  #pragma unroll
+          // One k-step of MMAs (and, ILC, its checksum MMAs); false after a
+          // timeout. kb_first is the item's first k-step, whose first MMA
+          // starts the accumulator.
+          auto mma_kstep = [&](int kb, int kb_first) -> bool {
+            // Inline fast path: the stage is usually full already.
+            if (!mbar_try_wait(&full_bar[stage], phase) &&
+                !wait_bar(&full_bar[stage], phase, aux, limit)) {
+              if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+              ok = false;
+              return false;
+            }
+            tc_fence_after();
+            // Descriptors advance linearly with the (16-byte granular)
+            // address: by 32 bytes per 16-k slice inside a K-major 128-byte
+            // row, or by two 8-row k groups (2048 bytes) of an MN-major box.
+            const uint64_t ad0 = ring_desc + (uint64_t)((stage * C::STAGE_BYTES) >> 4) + a_lbo;
+            const uint64_t bd0 = ring_desc +
+                                 (uint64_t)((stage * C::STAGE_BYTES + C::A_BYTES) >> 4) + b_lbo;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint32_t acc = (kb != kb_first || kk > 0) ? 1u : 0u;
+              const uint64_t ad = ad0 + (uint64_t)(kk * a_step), bd = bd0 + (uint64_t)(kk * b_step);
+              if constexpr (C::PAIR) umma_f16_pair(d, ad, bd, idesc, acc);
+              else umma_f16(d, ad, bd, idesc, acc);
+            }
+            if constexpr (C::ILC) {
+              // The reference checksums of this k-step: cr += A_s (B e)_s
+              // (A as the A operand, the B e rows as N) and cc += B_s
+              // (e^T A)_s (B's rows as the A operand, the e^T A rows as N).
+              const uint64_t ea0 = ring_desc + (uint64_t)((stage * C::STAGE_BYTES + C::ENCA_OFF) >> 4);
+              const uint64_t eb0 = ring_desc + (uint64_t)((stage * C::STAGE_BYTES + C::ENCB_OFF) >> 4);
+#pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk) {
                 const uint32_t acc = (kb != kb_first || kk > 0) ? 1u : 0u;
-                const uint64_t ad = ad0 + (uint64_t)(kk * a_step), bd = bd0 + (uint64_t)(kk * b_step);
-                if constexpr (C::PAIR) umma_f16_pair(d, ad, bd, idesc, acc);
-                else umma_f16(d, ad, bd, idesc, acc);
-              }
-              if constexpr (C::ILC) {
-                // The reference checksums of this k-step: cr += A_s (B e)_s
-                // (A as the A operand, the B e rows as N) and cc += B_s
-                // (e^T A)_s (B's rows as the A operand, the e^T A rows as N).
-                const uint64_t ea0 = ring_desc + (uint64_t)((stage * C::STAGE_BYTES + C::ENCA_OFF) >> 4);
-                const uint64_t eb0 = ring_desc + (uint64_t)((stage * C::STAGE_BYTES + C::ENCB_OFF) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
-                  const uint32_t acc = (kb != kb_first || kk > 0) ? 1u : 0u;
-                  if constexpr (C::PAIR) {
-                    umma_f16_pair(d + C::CR_COL, ad0 + kk * 2, eb0 + kk * 2, p.idesc_cr, acc);
-                    umma_f16_pair(d + C::CC_COL, bd0 + kk * 2, ea0 + kk * 2, p.idesc_cc, acc);
-                  } else {
-                    umma_f16(d + C::CR_COL, ad0 + kk * 2, eb0 + kk * 2, p.idesc_cr, acc);
-                    umma_f16(d + C::CC_COL, bd0 + kk * 2, ea0 + kk * 2, p.idesc_cc, acc);
-                  }
+                if constexpr (C::PAIR) {
+                  umma_f16_pair(d + C::CR_COL, ad0 + kk * 2, eb0 + kk * 2, p.idesc_cr, acc);
+                  umma_f16_pair(d + C::CC_COL, bd0 + kk * 2, ea0 + kk * 2, p.idesc_cc, acc);
+                } else {
+                  umma_f16(d + C::CR_COL, ad0 + kk * 2, eb0 + kk * 2, p.idesc_cr, acc);
+                  umma_f16(d + C::CC_COL, bd0 + kk * 2, ea0 + kk * 2, p.idesc_cc, acc);
                 }
               }
-              issued = true;
-              if constexpr (C::PAIR) umma_commit_pair(&empty_bar[stage]);  // both CTAs' stage
-              else umma_commit(&empty_bar[stage]);
-              if (++stage == STAGES) {
-                stage = 0;
-                phase ^= 1;
-              }
             }
-            if (ok && rg == ko.pause) {
-              // Mid-mainloop fault injection (testing only): once these MMAs
-              // are done, the epilogue warp of the row's lane quadrant flips
-              // the value in TMEM; the next MMAs accumulate onto it.
-              if constexpr (C::PAIR) umma_commit_pair(inj_bar);
-              else umma_commit(inj_bar);
-              if (!wait_bar(injdone_bar, 0, aux, limit, true, C::PAIR)) {
-                if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
-                ok = false;
+            issued = true;
+            if constexpr (C::PAIR) umma_commit_pair(&empty_bar[stage]);  // both CTAs' stage
+            else umma_commit(&empty_bar[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+            return true;
+          };
+          const int koff =
+              w.tile >= s.t_ck ? stagger_offset(p, unit, w.kb_end - w.kb_begin) : 0;
+          const int inj_kb_here = mid_inject_item<C::PAIR>(p, s, w, -1) ? p.inj_kb : -1;
+          if (koff == 0 && inj_kb_here < 0) {
+            // The plain ascending k loop: every launch without k staggering
+            // or a mid-mainloop flip.
+            for (int kb = w.kb_begin; kb < w.kb_end; ++kb)
+              if (!mma_kstep(kb, w.kb_begin)) break;
+          } else {
+            // The producer's k ranges (staggered start, wrap-around), cut
+            // after a mid-mainloop injection's iteration.
+            const KOrder ko = k_order(w.kb_begin, w.kb_end, koff, inj_kb_here);
+            for (int rg = 0; rg < ko.n && ok; ++rg) {
+              for (int kb = ko.lo(rg), kb_hi = ko.hi(rg); kb < kb_hi; ++kb)
+                if (!mma_kstep(kb, ko.lo0)) break;
+              if (ok && rg == ko.pause) {
+                // Mid-mainloop fault injection (testing only): once these MMAs
+                // are done, the epilogue warp of the row's lane quadrant flips
+                // the value in TMEM; the next MMAs accumulate onto it.
+                if constexpr (C::PAIR) umma_commit_pair(inj_bar);
+                else umma_commit(inj_bar);
+                if (!wait_bar(injdone_bar, 0, aux, limit, true, C::PAIR)) {
+                  if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+                  ok = false;
+                }
+                tc_fence_after();
               }
-              tc_fence_after();
             }
           }
         } else {
