@@ -208,7 +208,7 @@ def run_ours(args, rank, world, local_rank):
     # of them per shape), whatever K is.
     for pr in problems:
         est = statistics.median(a.elapsed_time(b) for a, b in pr["warm_events"]) * 1e-3
-        total = max(MIN_LAUNCHES, math.ceil(MIN_TIMED_S / max(est, 1e-6)))
+        total = max(args.min_launches, math.ceil(args.min_timed_ms * 1e-3 / max(est, 1e-6)))
         pr["per_step"] = max(1, math.ceil(total / args.steps))
     for pr in problems:
         pr["ws"].report(reset=True)
@@ -230,7 +230,7 @@ def run_ours(args, rank, world, local_rank):
 
     # The dominant kernel alone (roofline): the main kernel on pre-encoded
     # checksums, L2 flushed before each launch, CUDA events on this stream.
-    main_reps = max(MIN_LAUNCHES, 3 * args.steps)
+    main_reps = max(args.min_launches, 3 * args.steps)
     for pr in problems:
         s = pr["size"]
         st = skgemm.abft_encode(s, s, s, pr["A"].data_ptr(), s, pr["B"].data_ptr(), s,
@@ -312,7 +312,7 @@ def run_ours(args, rank, world, local_rank):
                    "launches_per_shape_per_step": {str(pr["size"]): pr["per_step"]
                                                    for pr in problems},
                    "timing": "per shape: median event time of all its timed launches "
-                             f"(>= {MIN_LAUNCHES} launches and >= {MIN_TIMED_S * 1e3:.0f} ms)",
+                             f"(>= {args.min_launches} launches and >= {args.min_timed_ms:.0f} ms)",
                    "l2": "flushed between launches (256 MiB write)",
                    "parallelism": f"replicas x{world}"},
         "pct_of_peak": {"measured_burst": round(100 * value / world / burst, 2),
@@ -911,6 +911,11 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--min-launches", type=int, default=MIN_LAUNCHES,
+                    help="square sweep: timed launches per shape, at least")
+    ap.add_argument("--min-timed-ms", type=float, default=MIN_TIMED_S * 1e3,
+                    help="square sweep: timed GEMM time per shape, at least (ms); 0 for "
+                         "profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ncu-target", action="store_true",
