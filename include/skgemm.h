@@ -130,7 +130,13 @@ typedef struct {
                            or the number of SMs (fixed schedule). At most the
                            number of SMs: all CTAs must be co-resident, since
                            a tile owner waits for later CTAs. */
-  int32_t tile_n;       /* BLK_N: 128 or 256; 0 = chosen by the model */
+  int32_t tile_n;       /* BLK_N: 64, 128 or 256; 0 = chosen by the model.
+                           64 (the small-tile configuration: 128 x 64 tiles,
+                           half the operand bytes per MAC iteration and per
+                           partial tile) is for GEMMs without ABFT on single
+                           CTAs: with abft or cta_pair = 2 it returns
+                           SKG_ERR_UNSUPPORTED, and the model picks it by
+                           itself only for those GEMMs. */
   int32_t abft;         /* 0 = off; 1 = verify every output tile, locate and
                            correct a single fault, report the rest */
   float tau_row;        /* ABFT row threshold; <= 0 = the default
@@ -358,7 +364,7 @@ skg_status_t skg_schedule_query(int64_t m, int64_t n, int64_t k, int32_t bm, int
 /* Predicted run time (microseconds) of one launch with this schedule under
  * the library's grid-size model (Stream-K page, App. A.1: the slowest CTA's
  * fixed cost + per-iteration cost + partial-store cost + per-peer cost, with
- * constants fitted on GB300). bm must be 128 and bn 128 or 256. */
+ * constants fitted on GB300). bm must be 128 and bn 64, 128 or 256. */
 skg_status_t skg_schedule_cost(int64_t m, int64_t n, int64_t k, int32_t bm, int32_t bn,
                                int32_t bk, int32_t g, int32_t sched, double* us);
 
@@ -371,7 +377,7 @@ skg_status_t skg_launch_shape(int64_t m, int64_t n, int64_t k, const skg_opts_t*
 /* The launch plan skg_gemm would use for this shape and options. */
 typedef struct {
   int32_t tile_m;      /* output rows per tile: 128, or 256 for CTA pairs */
-  int32_t tile_n;      /* BLK_N: 128 or 256 */
+  int32_t tile_n;      /* BLK_N: 64, 128 or 256 */
   int32_t ctas;        /* CTAs launched for the output tiles */
   int32_t cta_pair;    /* 1 = single CTAs, 2 = clusters of two CTAs */
   int32_t sched;       /* skg_sched_t */

@@ -111,7 +111,10 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
   skg_opts_default(&d);
   if (!o) o = &d;
   if (o->sched < SKG_SCHED_DP || o->sched > SKG_SCHED_AUTO) return SKG_ERR_ARG;
-  if (o->tile_n != 0 && o->tile_n != 128 && o->tile_n != 256) return SKG_ERR_UNSUPPORTED;
+  if (o->tile_n != 0 && o->tile_n != 64 && o->tile_n != 128 && o->tile_n != 256)
+    return SKG_ERR_UNSUPPORTED;
+  // 64-wide tiles: GEMMs without ABFT on single CTAs.
+  if (o->tile_n == 64 && (o->abft || o->cta_pair == 2)) return SKG_ERR_UNSUPPORTED;
   if (o->grid < 0) return SKG_ERR_ARG;
   const int ms = sms > 0 ? sms : 256;  // no device: plan for a large part
   if (o->grid > 0 && sms > 0 && o->grid > sms) return SKG_ERR_UNSUPPORTED;  // co-residency
@@ -121,7 +124,7 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
   // Launches without ABFT reduce shared tiles together (the model knows).
   const bool share = !o->abft;
   const Plan pl = choose_plan(m > 0 ? m : 1, n > 0 ? n : 1, k > 0 ? k : 1, o->tile_n, want_sched,
-                              want_grid, ms, 0, true, share);
+                              want_grid, ms, 0, true, share, !o->abft && o->cta_pair != 2);
   r.sched = pl.sched;
   r.grid = pl.grid;
   r.grid_ck = 0;
@@ -586,6 +589,9 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   else if (r.pair)
     e = abft_epilogue ? dispatch_layout<256, true, true>(mn, od, mp, p, lg, stream)
                       : dispatch_layout<256, false, true>(mn, od, mp, p, lg, stream);
+  else if (r.bn == 64)
+    e = abft_epilogue ? cudaErrorInvalidValue  // resolve() keeps ABFT off 64-wide tiles
+                      : dispatch_layout<64, false>(mn, od, mp, p, lg, stream);
   else if (r.bn == 128)
     e = (abft_epilogue && r.abft_local && !fuse_ck)
             ? dispatch_out<128, true, false, true>(od, mp, p, lg, stream)
@@ -1027,10 +1033,11 @@ skg_status_t skg_schedule_query(int64_t m, int64_t n, int64_t k, int32_t bm, int
 skg_status_t skg_schedule_cost(int64_t m, int64_t n, int64_t k, int32_t bm, int32_t bn,
                                int32_t bk, int32_t g, int32_t sched, double* us) {
   if (m < 0 || n < 0 || k < 0 || g <= 0 || !us) return SKG_ERR_ARG;
-  if (bm != kTileM || bk != kTileK || (bn != 128 && bn != 256)) return SKG_ERR_UNSUPPORTED;
+  if (bm != kTileM || bk != kTileK || (bn != 64 && bn != 128 && bn != 256))
+    return SKG_ERR_UNSUPPORTED;
   if (sched < SKG_SCHED_DP || sched > SKG_SCHED_SK2_DP) return SKG_ERR_ARG;
   const Schedule s = make_schedule(m, n, k, bm, bn, bk, g, sched);
-  *us = predict_us(s, bn == 128 ? kModel128 : kModel256, true);
+  *us = predict_us(s, model_for(bn), true);
   return SKG_OK;
 }
 

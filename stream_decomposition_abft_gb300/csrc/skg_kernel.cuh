@@ -192,6 +192,13 @@ template <int BN_, bool ABFT_, int OUT_, bool PAIR_ = false, bool LOCAL_ = false
 struct Cfg {
   static constexpr int BN = BN_;
   static constexpr bool ABFT = ABFT_;
+  // 64-wide tiles (the small-tile configuration): plain GEMMs on single
+  // CTAs; the ABFT column references come in 128-column groups.
+  static_assert(BN_ >= 128 || (!ABFT_ && !PAIR_ && !LOCAL_ && !ILC_),
+                "64-wide tiles: plain GEMMs on single CTAs");
+  // 128-column groups of the tile (ABFT column references; at least one so
+  // that the arrays sized by it exist for 64-wide tiles too).
+  static constexpr int CC_GROUPS = BN_ >= 128 ? BN_ / 128 : 1;
   // In-loop reference checksums: every k-step also issues the checksum MMAs
   // cr += A_s (B e)_s and cc += B_s (e^T A)_s into TMEM columns next to the
   // accumulator, from encodings the encode pass wrote (loaded with each
@@ -1145,7 +1152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kCkHalf = C::PAIR ? 2 : 1;  // 128-row checksum tiles per side tile
   // Dedicated side CTA that first runs its share of the encode pass.
   const bool enc_here = C::ABFT && !C::PAIR && p.enc_inkernel && (int)blockIdx.x >= s.g;
-  static_assert(C::STAGE_BYTES >= kEncInBoxBytes, "an encode box fills one ring stage");
+  static_assert(!C::ABFT || C::STAGE_BYTES >= kEncInBoxBytes, "an encode box fills one ring stage");
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1777,9 +1784,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // checksums): their loads are issued before the accumulator wait and
       // first used after it, so their latency hides behind the mainloop.
       float pf_ma = 0.f, pf_mb = 0.f, pf_cr0 = 0.f, pf_cr1 = 0.f;
-      float pf_cc0[BN / 128], pf_cc1[BN / 128];
+      float pf_cc0[C::CC_GROUPS], pf_cc1[C::CC_GROUPS];
 #pragma unroll
-      for (int h = 0; h < BN / 128; ++h) pf_cc0[h] = pf_cc1[h] = 0.f;
+      for (int h = 0; h < C::CC_GROUPS; ++h) pf_cc0[h] = pf_cc1[h] = 0.f;
       int pf_ea = 0, pf_eb = 0;
       // (A CTA pair's second half lies past m when m has an odd number of
       // 128-row tiles: nothing there to check.)
@@ -1799,7 +1806,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ephase = ls.phase;
         pf_cr0 = ls.cr;
 #pragma unroll
-        for (int h = 0; h < BN / 128; ++h) pf_cc0[h] = ls.cc[h];
+        for (int h = 0; h < C::CC_GROUPS; ++h) pf_cc0[h] = ls.cc[h];
         pf_ma = ls.ma;
         pf_mb = ls.mb;
       } else if (verify_here) {
@@ -1837,7 +1844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pf_cr1 = __ldcg(crp + 1);
         }
 #pragma unroll
-        for (int h = 0; h < BN / 128; ++h) {
+        for (int h = 0; h < C::CC_GROUPS; ++h) {
           const int col = n0 + h * 128 + r;
           if (!C::ILC && col < p.n) {
             const float* ccp = p.cc_all + (int64_t)col * p.ld_cc + kEncRows * tm;
@@ -2116,9 +2123,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // power of two; tile maxima for the thresholds are the max over
           // the tile's encode units.
           const float cr = ldexpf(pf_cr0 + pf_cr1, -pf_eb);
-          float cc[BN / 128];
+          float cc[C::CC_GROUPS];
 #pragma unroll
-          for (int h = 0; h < BN / 128; ++h) cc[h] = ldexpf(pf_cc0[h] + pf_cc1[h], -pf_ea);
+          for (int h = 0; h < C::CC_GROUPS; ++h) cc[h] = ldexpf(pf_cc0[h] + pf_cc1[h], -pf_ea);
           {
             float ma = pf_ma, mb = pf_mb;
 #pragma unroll
@@ -2159,7 +2166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             aux->d_row = d_r;
           }
 #pragma unroll
-          for (int h = 0; h < BN / 128; ++h) {
+          for (int h = 0; h < C::CC_GROUPS; ++h) {
             const int j = h * 128 + r;
             const float tot =
                 colsum_of(0)[j] + colsum_of(1)[j] + colsum_of(2)[j] + colsum_of(3)[j];

@@ -16,8 +16,11 @@
 // per-tile term e is an addition to the page's four.
 //
 // The page uses the model to pick g; here it also picks the schedule (DP,
-// basic SK, or two-tile SK + DP) and BLK_N (128 or 256), the two-kernel
-// ensemble the page suggests for bandwidth-bound shapes (§A4).
+// basic SK, or two-tile SK + DP) and BLK_N: 256 or 128, and for GEMMs
+// without ABFT also 64 (the small-tile configuration: half the operand
+// bytes per MAC iteration and per partial tile, twice the tiles), the
+// kernel ensemble the page's conclusion suggests for bandwidth-bound and
+// small shapes.
 #pragma once
 #include <stdint.h>
 
@@ -32,8 +35,19 @@ struct CostModel {
   double a, c, e, b, d;  // microseconds
 };
 
+// BLK_N = 64 was fitted against the 128-wide constants: in-kernel spans of
+// 480 launches of each width (20 small and skinny shapes, three schedules,
+// g from 4 to 152, back to back with the L2 flushed), scored by the spans
+// of the plans the search then picks. Per MAC iteration it costs about what
+// a 128-wide one does (the k-step is latency-bound at these sizes), so it
+// wins only where the fixed cost and the tile count decide.
+constexpr CostModel kModel64 = {2.15, 0.360, 0.11, 4.50, 0.80};
 constexpr CostModel kModel128 = {2.64, 0.334, 0.17, 4.67, 1.03};
 constexpr CostModel kModel256 = {3.47, 0.364, 0.00, 8.18, 1.73};
+
+inline const CostModel& model_for(int bn) {
+  return bn == 64 ? kModel64 : bn == 128 ? kModel128 : kModel256;
+}
 
 // A shared tile also costs each part about this many d-units per covering
 // CTA (every part waits for every cover's flag and reads a slice of every
@@ -132,15 +146,17 @@ struct Plan {
 };
 
 // Best (BLK_N, schedule, g) for an m x n x k launch on `sms` SMs. Fixed
-// choices (want_* != 0 / >= 0) are kept; the rest are searched.
+// choices (want_* != 0 / >= 0) are kept; the rest are searched (BLK_N = 64
+// only with `small_tiles`).
 inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_sched,
-                        int want_grid, int sms, int t_ck, bool side_ctas, bool share) {
+                        int want_grid, int sms, int t_ck, bool side_ctas, bool share,
+                        bool small_tiles) {
   static const int kCands[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 76, 96, 112, 128, 144};
   Plan best{want_bn ? want_bn : 256, want_sched >= 0 ? want_sched : kSchedSK2DP,
             want_grid ? want_grid : sms, 1e300, 0};
-  for (int bn = 128; bn <= 256; bn += 128) {
-    if (want_bn && bn != want_bn) continue;
-    const CostModel& M = bn == 128 ? kModel128 : kModel256;
+  for (int bn = 64; bn <= 256; bn *= 2) {
+    if (want_bn ? bn != want_bn : (bn == 64 && !small_tiles)) continue;
+    const CostModel& M = model_for(bn);
     const int64_t t = ((m + kTileM - 1) / kTileM) * ((n + bn - 1) / bn) + t_ck;
     int cands[64];
     int nc = 0;
@@ -201,20 +217,21 @@ inline Plan search_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_s
 // schedules of up to `sms` CTAs each, far more host time than a launch.
 inline Plan choose_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_sched,
                         int want_grid, int sms, int t_ck = 0, bool side_ctas = true,
-                        bool share = true) {
+                        bool share = true, bool small_tiles = false) {
   struct Key {
     int64_t m, n, k;
-    int bn, sched, grid, sms, t_ck, side, share;
+    int bn, sched, grid, sms, t_ck, side, share, small;
     bool operator==(const Key& o) const {
       return m == o.m && n == o.n && k == o.k && bn == o.bn && sched == o.sched &&
              grid == o.grid && sms == o.sms && t_ck == o.t_ck && side == o.side &&
-             share == o.share;
+             share == o.share && small == o.small;
     }
   };
   struct Hash {
     size_t operator()(const Key& x) const {
       uint64_t h = 1469598103934665603ull;
-      const int64_t v[10] = {x.m, x.n, x.k, x.bn, x.sched, x.grid, x.sms, x.t_ck, x.side, x.share};
+      const int64_t v[11] = {x.m,    x.n,    x.k,    x.bn,    x.sched,
+                             x.grid, x.sms,  x.t_ck, x.side, x.share, x.small};
       for (int64_t e : v) h = (h ^ (uint64_t)e) * 1099511628211ull;
       return (size_t)h;
     }
@@ -222,13 +239,14 @@ inline Plan choose_plan(int64_t m, int64_t n, int64_t k, int want_bn, int want_s
   static std::mutex mu;
   static std::unordered_map<Key, Plan, Hash> cache;
   const Key key{m, n, k, want_bn, want_sched, want_grid, sms, t_ck, side_ctas ? 1 : 0,
-                share ? 1 : 0};
+                share ? 1 : 0, small_tiles ? 1 : 0};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
-  const Plan p = search_plan(m, n, k, want_bn, want_sched, want_grid, sms, t_ck, side_ctas, share);
+  const Plan p =
+      search_plan(m, n, k, want_bn, want_sched, want_grid, sms, t_ck, side_ctas, share, small_tiles);
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();
   cache.emplace(key, p);

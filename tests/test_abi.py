@@ -211,7 +211,8 @@ def test_f64_workspace_and_argument_errors(lib):
 # Grid-size model (Stream-K page, App. A.1)
 # ----------------------------------------------------------------------------
 # Model constants (a, c, e, b, d) in microseconds, as fitted for each BLK_N.
-MODEL = {128: (2.64, 0.334, 0.17, 4.67, 1.03), 256: (3.47, 0.364, 0.00, 8.18, 1.73)}
+MODEL = {64: (2.15, 0.360, 0.11, 4.50, 0.80), 128: (2.64, 0.334, 0.17, 4.67, 1.03),
+         256: (3.47, 0.364, 0.00, 8.18, 1.73)}
 
 
 def brute_force_cost(m, n, k, bn, g, mode):
@@ -258,7 +259,7 @@ def test_model_cost_matches_segment_walk(lib):
     rnd = random.Random(99)
     for _ in range(200):
         m, n, k = rnd.randint(1, 4000), rnd.randint(1, 4000), rnd.randint(1, 9000)
-        bn = rnd.choice([128, 256])
+        bn = rnd.choice([64, 128, 256])
         g = rnd.randint(1, 152)
         mode = rnd.choice(["dp", "sk", "sk2_dp", "dp_sk1"])
         got = skgemm.schedule_cost(m, n, k, 128, bn, 64, g, MODES[mode])
@@ -278,8 +279,27 @@ def test_plan_honours_explicit_options_and_picks_minimum(lib):
                       (128, 19072, 2048), (8192, 1024, 8192)]:
         tn, g, sc = skgemm.launch_shape(m, n, k, skgemm.opts_default())
         best = skgemm.schedule_cost(m, n, k, 128, tn, 64, g, sc)
-        for bn in (128, 256):
+        for bn in (64, 128, 256):
             assert best <= skgemm.schedule_cost(m, n, k, 128, bn, 64, sms, skgemm.SCHED_SK2_DP) + 1e-9
+
+
+def test_small_tiles_only_without_abft(lib):
+    # BLK_N = 64: GEMMs without ABFT on single CTAs; the model may choose it
+    # by itself only for those.
+    for kw in (dict(tile_n=64, abft=1), dict(tile_n=64, cta_pair=2), dict(tile_n=96)):
+        o = skgemm.opts_default(**kw)
+        assert skgemm.lib().skg_launch_plan(512, 512, 512, ctypes.byref(o),
+                                            ctypes.byref(skgemm.Plan())) == skgemm.ERR_UNSUPPORTED
+        assert skgemm.workspace_size(512, 512, 512, o) == 0
+    pl = skgemm.launch_plan(256, 256, 384, skgemm.opts_default(tile_n=64, sched="sk", grid=9))
+    assert (pl.tile_n, pl.ctas, pl.sched, pl.cta_pair) == (64, 9, skgemm.SCHED_SK, 1)
+    for (m, n, k) in [(256, 256, 384), (640, 640, 256), (128, 128, 8192), (4096, 4096, 4096)]:
+        assert skgemm.launch_plan(m, n, k, skgemm.opts_default(abft=1)).tile_n != 64
+    # a tiny GEMM: fewer MAC iterations per CTA and a cheaper fixed cost
+    assert skgemm.launch_plan(256, 256, 384, skgemm.opts_default()).tile_n == 64
+    assert skgemm.launch_plan(4096, 4096, 4096, skgemm.opts_default()).tile_n != 64
+    assert skgemm.schedule_cost(256, 256, 384, 128, 64, 64, 8, skgemm.SCHED_DP) < \
+        skgemm.schedule_cost(256, 256, 384, 128, 128, 64, 4, skgemm.SCHED_DP)
 
 
 def test_launch_plan_agrees_with_launch_shape(lib):

@@ -57,7 +57,7 @@ def test_example_384_parity_and_trace(mode, g):
     g = min(g, sms())
     p = inputs.example_384()
     ref = reference(p)
-    for tile_n in (128, 256):
+    for tile_n in (64, 128, 256):
         rows, C, ws = device_trace(p, dict(sched=mode, tile_n=tile_n), g)
         check_full(p, C, ref)
         want = ss.flatten(ss.schedule(384, 384, 128, 128, tile_n, 64, g, mode=mode))
@@ -85,7 +85,7 @@ def test_small_shapes(shape, mode):
     p = inputs.make_problem(m, n, k, seed=m * 7 + n, in_dtype=dt_in, out_dtype=dt_out,
                             law_a="normal", law_b="uniform", alpha=0.75, beta=-0.5)
     ref = reference(p)
-    for tile_n in (128, 256):
+    for tile_n in (64, 128, 256):
         for g in (7, sms()):
             C, ws, st = run(p, skgemm.opts_default(sched=mode, tile_n=tile_n, grid=g))
             assert st == skgemm.OK
@@ -236,6 +236,81 @@ def test_fixup_timeout_reports_and_returns():
     assert st2 == skgemm.OK
     check_full(p2, C2)
     assert ws2.report().status_bits == 0
+
+
+# --------------------------------------------------------------------------- 64-wide tiles
+# The small-tile configuration (BLK_N = 64, GEMMs without ABFT): the same
+# persistent kernel and schedule with 128 x 64 tiles.
+@pytest.mark.parametrize("g", [3, 16, 148])
+def test_small_tiles_many_peers(g):
+    g = min(g, sms())
+    p = inputs.make_problem(256, 200, 8192, seed=30 + g, in_dtype="bf16", out_dtype="f32",
+                            law_a="uniform", law_b="uniform", alpha=1.5, beta=0.5)
+    ref = reference(p)
+    for mode in MODES:
+        rows, C, ws = device_trace(p, dict(sched=mode, tile_n=64), g)
+        check_full(p, C, ref)
+        assert rows == ss.flatten(ss.schedule(256, 200, 8192, 128, 64, 64, g, mode=mode))
+        assert ws.report().status_bits == 0
+
+
+@pytest.mark.parametrize("out", ["f32", "f16", "bf16"])
+def test_small_tiles_shared_reduction(out):
+    # Deep-k 128 x 64 tiles split evenly over many CTAs: the shared
+    # reduction (every covering CTA reduces a share of the tile).
+    g = min(96, sms())
+    p = inputs.make_problem(300, 130, 16384, seed=41, in_dtype="f16", out_dtype=out,
+                            law_a="uniform", law_b="uniform", alpha=1.5, beta=0.5)
+    C, ws, st = run(p, skgemm.opts_default(sched="sk", tile_n=64, grid=g))
+    assert st == skgemm.OK
+    check_full(p, C)
+    assert ws.report().status_bits == 0
+
+
+@pytest.mark.parametrize("a_layout,b_layout", [(1, 0), (0, 1), (1, 1)])
+def test_small_tiles_mn_major(a_layout, b_layout):
+    p = inputs.make_problem(384, 200, 1000, seed=42, in_dtype="bf16", out_dtype="f32",
+                            law_a="normal", law_b="normal", a_layout=a_layout,
+                            b_layout=b_layout)
+    ref = reference(p)
+    for mode, g in (("dp", 12), ("sk", 40), ("sk2_dp", 7)):
+        C, ws, st = run(p, skgemm.opts_default(sched=mode, tile_n=64, grid=min(g, sms())))
+        assert st == skgemm.OK
+        check_full(p, C, ref)
+
+
+def test_small_tiles_workspace_shared_with_wider_tiles():
+    # One workspace for 64-, 128- and 256-wide Stream-K launches of several
+    # shapes in a row (the flags sit at fixed offsets and carry the epoch).
+    shapes = [(256, 256, 4096), (384, 200, 2048), (128, 520, 3000)]
+    size = max(skgemm.workspace_size(m, n, k, skgemm.opts_default(sched="sk", tile_n=t, grid=g))
+               for (m, n, k) in shapes for t in (64, 128, 256) for g in (37, sms()))
+    ws = skgemm.Workspace(size, "cuda")
+    launches = 0
+    for i, (m, n, k) in enumerate(shapes):
+        for t in (64, 128, 256, 64):
+            p = inputs.make_problem(m, n, k, seed=50 + 7 * i + t, in_dtype="bf16", out_dtype="f32",
+                                    law_a="normal", law_b="normal")
+            g = 37 if t != 256 else sms()
+            C, _, st = run(p, skgemm.opts_default(sched="sk", tile_n=t, grid=g), ws=ws)
+            assert st == skgemm.OK
+            check_full(p, C)
+            launches += 1
+    rep = ws.report()
+    assert rep.status_bits == 0 and rep.launches == launches
+
+
+def test_small_tiles_chosen_for_tiny_shapes():
+    # The grid-size model takes 64-wide tiles for small GEMMs without ABFT,
+    # never with ABFT, and keeps wide tiles for large ones.
+    assert skgemm.launch_plan(256, 256, 384, skgemm.opts_default()).tile_n == 64
+    assert skgemm.launch_plan(256, 256, 384, skgemm.opts_default(abft=1)).tile_n != 64
+    assert skgemm.launch_plan(4096, 4096, 4096, skgemm.opts_default()).tile_n != 64
+    p = inputs.make_problem(256, 256, 384, seed=43, in_dtype="f16", out_dtype="f16",
+                            law_a="normal", law_b="normal")
+    C, ws, st = run(p, skgemm.opts_default())
+    assert st == skgemm.OK
+    check_full(p, C)
 
 
 # --------------------------------------------------------------------------- workloads
