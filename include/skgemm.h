@@ -277,7 +277,12 @@ void skg_opts_default(skg_opts_t* opts);
  * (opts may be NULL): a header with the launch epoch and the report, one
  * flag and one fp32 BLK_M x BLK_N partial-sum slot per CTA (Stream-K page,
  * §4: fixup storage scales with g, not with the problem), the partial
- * checksums, and with ABFT the split encodings e^T A and B e. */
+ * checksums, and with ABFT the split encodings e^T A and B e. Two banks of
+ * flags and slots: with ABFT the second serves the fused checksum tiles;
+ * without, the split reduction (a Stream-K tile that two or more of its
+ * CTAs end their ranges in is finished by those CTAs together, each storing
+ * a range of its columns), whose owners keep their partial there when they
+ * already hold one of an earlier tile. */
 size_t skg_workspace_size(int64_t m, int64_t n, int64_t k, const skg_opts_t* opts);
 
 /* skg_workspace_size for the given operand layouts: when opts select the

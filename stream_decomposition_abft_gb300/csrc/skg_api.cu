@@ -88,6 +88,11 @@ struct Resolved {
   int ilc;           // ABFT references accumulated by the output tiles' MMAs (DP plan)
   int ws_grid;
   int64_t k_for_plan;  // CTAs the workspace's flags and partial slots are sized for
+  // Shared reduction of the output Stream-K tiles (no ABFT): Schedule's
+  // share_min and share_bank2 (bank 2 takes the second region's storage).
+  int share_min;
+  int share_bank2;
+  int split;  // split reduction of the output tiles (Schedule::split_max)
 };
 
 // Whether an ABFT call runs its reference checksums inside the mainloop
@@ -106,7 +111,7 @@ bool ilc_wanted(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, const Reso
 // grid-size model (skg_model.h). A fixed schedule with grid 0 runs on all
 // SMs, as the page's persistent launches do.
 skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resolved& r,
-                     int sms) {
+                     int sms, bool compact = false) {
   skg_opts_t d;
   skg_opts_default(&d);
   if (!o) o = &d;
@@ -132,6 +137,11 @@ skg_status_t resolve(int64_t m, int64_t n, int64_t k, const skg_opts_t* o, Resol
   r.bn = pl.bn;
   r.pair = 0;
   r.grid_max = ms;
+  r.share_min = kShareMin;
+  r.share_bank2 = 0;
+  // Split reduction for launches without ABFT; it takes the second region's
+  // storage for owners' partials (bank 2), which compact workspaces leave out.
+  r.split = (!o->abft && !compact) ? 1 : 0;
   if (o->cta_pair < 0 || o->cta_pair > 2) return SKG_ERR_ARG;
   if (o->cta_pair == 2 && o->tile_n != 0 && o->tile_n != 256) return SKG_ERR_UNSUPPORTED;
   bool use_pair = o->cta_pair == 2;
@@ -264,7 +274,7 @@ Layout layout(int64_t m, int64_t n, int64_t k, const Resolved& r) {
   size_t off = kHeaderBytes;
   // With ABFT the fused checksum tiles form a second split region with
   // flags and partial slots of its own.
-  const size_t regions = r.abft ? 2 : 1;
+  const size_t regions = (r.abft || r.share_bank2 || r.split) ? 2 : 1;
   L.flags = off;
   off += kFlagBytes;
   L.partials = off;
@@ -505,6 +515,12 @@ skg_status_t launch_one(const Gemm& g, const Resolved& r, bool abft_epilogue, bo
   }
   if (band < 1) band = 1;
   if (band < p.s.tiles_n) p.s.band = band;
+  if (!abft_epilogue) {
+    p.s.share_min = r.share_min;
+    p.s.share_bank2 = (r.share_bank2 || r.split) ? 1 : 0;
+    // Split parts own whole staging chunks (BLK_N / EPI_COLS of them).
+    p.s.split_max = (r.split && !r.pair) ? r.bn * out_bytes / 128 : 0;
+  }
   p.m = (int)g.m;
   p.n = (int)g.n;
   p.k = (int)g.k;
@@ -802,7 +818,7 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
                        const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
                        int32_t in_dtype, int32_t out_dtype, int32_t a_layout, int32_t b_layout,
                        const skg_opts_t* opts, int force_abft, void* workspace,
-                       size_t ws_bytes, void* stream_v) {
+                       size_t ws_bytes, void* stream_v, bool compact = false) {
   cudaStream_t stream = (cudaStream_t)stream_v;
   if (m < 0 || n < 0 || k < 0) return SKG_ERR_ARG;
   if (m > INT32_MAX / 4 || n > INT32_MAX / 4 || k > INT32_MAX / 4) return SKG_ERR_UNSUPPORTED;
@@ -832,7 +848,7 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
     forced.abft = 1;
     opts = &forced;
   }
-  st = resolve(m, n, k, opts, r, sms);
+  st = resolve(m, n, k, opts, r, sms, compact);
   if (st != SKG_OK) return st;
   const Layout L = layout(m, n, k, r);
   const bool copies = (a_layout == SKG_A_COL || b_layout == SKG_B_NMAJOR) &&
@@ -894,12 +910,12 @@ skg_status_t gemm_impl(int64_t m, int64_t n, int64_t k, float alpha, const void*
 namespace skg {
 
 skg_status_t workspace_need(int64_t m, int64_t n, int64_t k, int32_t a_layout, int32_t b_layout,
-                            const skg_opts_t* opts, size_t* need) {
+                            const skg_opts_t* opts, size_t* need, bool compact) {
   if (!layout_valid(a_layout, b_layout)) return SKG_ERR_ARG;
   if (m < 0 || n < 0 || k < 0) return SKG_ERR_ARG;
   Resolved r;
   const int sms = sm_count_cached();
-  const skg_status_t st = resolve(m, n, k, opts, r, sms);
+  const skg_status_t st = resolve(m, n, k, opts, r, sms, compact);
   if (st != SKG_OK) return st;
   const Layout L = layout(m, n, k, r);
   // The copies are planned for bf16, the input type for which they can be
@@ -913,6 +929,15 @@ skg_status_t workspace_need(int64_t m, int64_t n, int64_t k, int32_t a_layout, i
 }
 
 size_t fixed_header_bytes() { return kHeaderBytes + kFlagBytes; }
+
+skg_status_t gemm_compact(int64_t m, int64_t n, int64_t k, float alpha, const void* A,
+                          int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+                          int64_t ldc, int32_t in_dtype, int32_t out_dtype, int32_t a_layout,
+                          int32_t b_layout, const skg_opts_t* opts, void* workspace,
+                          size_t ws_bytes, void* stream) {
+  return gemm_impl(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, a_layout,
+                   b_layout, opts, 0, workspace, ws_bytes, stream, true);
+}
 
 }  // namespace skg
 

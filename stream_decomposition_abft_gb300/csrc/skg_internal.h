@@ -118,8 +118,18 @@ cudaError_t launch_scale(int out_dtype, void* C, int64_t ldc, int m, int n, floa
 
 // skg_workspace_size_layout with the reason when there is no size: the
 // status resolve() gives for the options (SKG_ERR_ARG, SKG_ERR_UNSUPPORTED).
+// compact: the plan leaves out storage that only speeds launches up (the
+// second bank of partial slots of the split reduction), for fixed-size
+// workspaces.
 skg_status_t workspace_need(int64_t m, int64_t n, int64_t k, int32_t a_layout, int32_t b_layout,
-                            const skg_opts_t* opts, size_t* need);
+                            const skg_opts_t* opts, size_t* need, bool compact = false);
+
+// skg_gemm planned as workspace_need(..., compact = true) sizes it.
+skg_status_t gemm_compact(int64_t m, int64_t n, int64_t k, float alpha, const void* A,
+                          int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+                          int64_t ldc, int32_t in_dtype, int32_t out_dtype, int32_t a_layout,
+                          int32_t b_layout, const skg_opts_t* opts, void* workspace,
+                          size_t ws_bytes, void* stream);
 
 // Bytes at the start of every workspace that must be zero before its first
 // use: the header with the report, and the flags (skg_workspace_init).

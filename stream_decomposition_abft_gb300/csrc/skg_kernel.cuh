@@ -706,6 +706,85 @@ static __device__ __noinline__ bool fixup_through_ring(uint8_t* qring, int slots
   return fine;
 }
 
+// Split reduction, LoadPartials of one part: the partials of every other
+// CTA covering the tile (owner .. contrib_last, ascending, without `unit`;
+// the owner's in bank 2 when owner_bank2), restricted to this part's columns
+// [col_lo, col_hi) of quadrant q's band, in pieces of at most BLK_N / 2
+// columns through `slots` pipelined slots of `qring`, each folded into the
+// accumulator columns in TMEM as it lands. bars[0, slots) are this warp's
+// piece barriers (fresh). Returns false after a timeout, with every copy it
+// issued landed.
+template <int BN>
+static __device__ __noinline__ bool fold_split_through_ring(
+    uint8_t* qring, int slots, const float* rpartials, size_t bank2, int owner, int owner_bank2,
+    int contrib_last, int unit, int slot_stride, int crank, int q, int lane, uint32_t tacc,
+    int col_lo, int col_hi, uint64_t* bars, const KernelParams& p, Aux* aux, uint64_t limit) {
+  constexpr int kPieceCols = BN / 2;
+  constexpr uint32_t kSlotBytes = kPartialBandBytes<BN> / 2;
+  const int npieces = (col_hi - col_lo + kPieceCols - 1) / kPieceCols;
+  const int items = (contrib_last - owner) * npieces;  // other covers x pieces
+  auto piece_cols = [&](int i, int& a, int& b) {
+    a = col_lo + (i % npieces) * kPieceCols;
+    b = min(col_hi, a + kPieceCols);
+  };
+  auto issue = [&](int i) {
+    const int sl = i % slots;
+    const int oi = i / npieces;
+    const int u = owner + oi + (owner + oi >= unit ? 1 : 0);
+    int a, b;
+    piece_cols(i, a, b);
+    const float* src = rpartials + (size_t)(u * slot_stride + crank) * kBM * BN +
+                       (u == owner && owner_bank2 ? bank2 : 0) + (size_t)q * 32 * BN +
+                       (size_t)a * 32;
+    mbar_arrive_expect_tx(&bars[sl], (uint32_t)(b - a) * 128u);
+    bulk_load_g2s(qring + sl * kSlotBytes, src, (uint32_t)(b - a) * 128u, &bars[sl]);
+  };
+  const int first = min(slots, items);
+  if (lane == 0) {
+    fence_proxy_async_global();
+    for (int i = 0; i < first; ++i) issue(i);
+  }
+  __syncwarp();
+  int issued = first;
+  bool fine = true;
+  int i = 0;
+  for (; i < items; ++i) {
+    const int sl = i % slots;
+    fine = __all_sync(0xffffffffu, wait_bar(&bars[sl], (uint32_t)((i / slots) & 1), aux, limit));
+    if (!fine) break;
+    int a, b;
+    piece_cols(i, a, b);
+#pragma unroll 1
+    for (int c32 = a / 32; c32 < b / 32; ++c32) {
+      uint32_t u[32];
+      tmem_ld32(tacc + c32 * 32, u);
+      const uint8_t* src = qring + sl * kSlotBytes + (c32 * 32 - a) * 128 + lane * 16;
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const float4 t = *reinterpret_cast<const float4*>(src + jj * 512);
+        u[4 * jj] = __float_as_uint(f32_of(u[4 * jj]) + t.x);
+        u[4 * jj + 1] = __float_as_uint(f32_of(u[4 * jj + 1]) + t.y);
+        u[4 * jj + 2] = __float_as_uint(f32_of(u[4 * jj + 2]) + t.z);
+        u[4 * jj + 3] = __float_as_uint(f32_of(u[4 * jj + 3]) + t.w);
+      }
+      tmem_st32(tacc + c32 * 32, u);
+    }
+    __syncwarp();
+    if (lane == 0 && issued < items) issue(issued);
+    issued += issued < items ? 1 : 0;
+    __syncwarp();
+  }
+  if (!fine) {
+    if (lane == 0) {
+      if (!aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
+      for (int j = i; j < issued; ++j)
+        wait_bar(&bars[j % slots], (uint32_t)((j / slots) & 1), aux, limit, false);
+    }
+    __syncwarp();
+  }
+  return fine;
+}
+
 // Elements of C in the launch's output type, one at a time or four at once
 // (the shared tile reduction's plain loads and stores).
 template <int OUT>
@@ -765,8 +844,9 @@ __device__ __forceinline__ Vec pack4(const float (&y)[4]) {
 
 // Shared LoadPartials + StoreTile (no ABFT): a tile covered by CTAs
 // owner .. contrib_last of which owner .. part_last end their ranges in it.
-// Each of those stored its whole partial and signalled; after every cover's
-// flag is set, participant j = unit - owner reduces its share of the tile's
+// Each of those stored its whole partial and signalled (the owner in bank 2,
+// the second region's flags and slots, when owner_bank2); after every
+// cover's flag is set, participant j = unit - owner reduces its share of the tile's
 // (32-row quadrant, 4-column group) items over all covers' partials in
 // ascending CTA order, then applies alpha / beta and stores C with plain
 // stores. The k=0 CTA no longer sums every peer alone, so no CTA of a deep,
@@ -774,17 +854,19 @@ __device__ __forceinline__ Vec pack4(const float (&y)[4]) {
 // epilogue threads; false after a timeout.
 template <class C>
 static __device__ __noinline__ bool reduce_share(const KernelParams& p, float* rpartials,
-                                                 uint32_t* rflags, int owner, int contrib_last,
-                                                 int part_last, int unit, int slot_stride,
-                                                 int crank, int m0, int n0, int ew, int lane,
-                                                 uint32_t epoch, int out_tile, Aux* aux,
-                                                 uint64_t limit) {
+                                                 uint32_t* rflags, int owner, int owner_bank2,
+                                                 int contrib_last, int part_last, int unit,
+                                                 int slot_stride, int crank, int m0, int n0,
+                                                 int ew, int lane, uint32_t epoch, int out_tile,
+                                                 Aux* aux, uint64_t limit) {
   constexpr int BN = C::BN;
+  // Bank 2 of the owner's flag and partial slot.
+  const size_t bank2 = (size_t)p.ws_ctas * kBM * BN;
   bool fine = true;
   if (ew == 0) {
     for (int u = owner + lane; u <= contrib_last && fine; u += 32) {
       if (u == unit) continue;
-      const int fi = u * slot_stride + crank;
+      const int fi = u * slot_stride + crank + (u == owner && owner_bank2 ? kMaxCtas : 0);
       if (ld_acquire_gpu(&rflags[fi]) == epoch) continue;
       const uint64_t t0 = globaltimer();
       uint32_t spins = 0;
@@ -849,8 +931,9 @@ static __device__ __noinline__ bool reduce_share(const KernelParams& p, float* r
         for (int u = 0; u < kCov; ++u)
           if (t < ie && cv0 + u < covers)
             v[bi][u] = ld_cg_f4(partial_at<BN>(
-                rpartials + (size_t)((owner + cv0 + u) * slot_stride + crank) * kBM * BN, c4,
-                qi * 32 + lane, true));
+                rpartials + (size_t)((owner + cv0 + u) * slot_stride + crank) * kBM * BN +
+                    (cv0 + u == 0 && owner_bank2 ? bank2 : 0),
+                c4, qi * 32 + lane, true));
       }
 #pragma unroll
       for (int bi = 0; bi < kBatch; ++bi)
@@ -1906,7 +1989,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Fault injection (testing only): this tile gets a flip after its fixup.
-      const bool inject_here = !is_ck && w.role != kRolePeer &&
+      // Split reduction (see Schedule::split_max): this CTA is one of the
+      // parts that finish the tile, each storing a range of its columns.
+      constexpr int kChunks = BN / C::EPI_COLS;
+      // (Single CTAs only: the pair kernels have no registers to spare.)
+      const bool split = !C::ABFT && !C::PAIR && !is_ck && Cursor::split(s, w) &&
+                         unit <= w.part_last && w.share_parts <= kChunks;
+      const bool inject_here = !is_ck && (w.role != kRolePeer || split) &&
                                ((out_tile == p.inj_tile[0] && p.inj_kb < 0) ||
                                 out_tile == p.inj_tile[1]);
       // ... or got one in the mainloop (fault records say "injected").
@@ -1922,13 +2011,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           !is_ck ? BN / 32
                  : ((w.tile < p.ck_cr_tiles ? p.ck_n_cr : p.ck_n_cc) + 31) / 32;
 
-      // Shared reduction of a tile that at least kShareMin CTAs end in (all
-      // of them store partials, the owner too, which holds no other one; see
-      // reduce_share).
-      const bool share = !C::ABFT && w.region == 0 && w.role != kRoleFull &&
-                         w.share_parts >= kShareMin && unit <= w.part_last;
-      if (w.role == kRolePeer || share) {
-        // StorePartials + Signal (Algorithm 5, non-started segment).
+      // Shared reduction of a tile that at least share_min CTAs end in (all
+      // of them store partials, the owner too; see reduce_share). An owner
+      // whose range began in an earlier tile keeps this partial and its flag
+      // in bank 2 (the second region's storage), since its slot holds the
+      // earlier tile's partial.
+      const bool share = !C::ABFT && Cursor::shared(s, w) && unit <= w.part_last;
+      // A split part `sj` of `sp` finishes the tile's column chunks [c_lo, c_hi).
+      int c_lo = 0, c_hi = kChunks;
+      if (split) {
+        const int sp = w.share_parts, sj = unit - w.owner;
+        c_lo = sj * kChunks / sp;
+        c_hi = (sj + 1) * kChunks / sp;
+      }
+      if ((share || split) && w.role == kRoleOwner && w.owner_bank2) {
+        rflags += kMaxCtas;
+        my_slot += (size_t)p.ws_ctas * kBM * BN;
+      }
+      // StorePartials + Signal (Algorithm 5, non-started segment): peers,
+      // the parts of a shared reduction, and the parts of a split one (which
+      // keep the accumulator for their own columns).
+      const bool stores_partial = w.role == kRolePeer || share || split;
+      if (stores_partial) {
 #pragma unroll 1
         for (int c32 = 0; c32 < live_chunks; ++c32) {
           uint32_t u[32];
@@ -1939,30 +2043,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                      make_float4(f32_of(u[4 * j]), f32_of(u[4 * j + 1]), f32_of(u[4 * j + 2]),
                                  f32_of(u[4 * j + 3])));
         }
-        tc_fence_before();
-        release_acc(ab);
+        if (!split) {
+          tc_fence_before();
+          release_acc(ab);
+        }
         named_bar_sync(1, kEpiThreads);
         if (et == 0 && (int)blockIdx.x != p.drop_signal) {
           __threadfence();
           st_release_gpu(&rflags[my_slot_idx], epoch);
         }
-        if (share && !reduce_share<C>(p, rpartials, rflags, w.owner, w.contrib_last, w.part_last,
-                                      unit, slot_stride, (int)crank, m0, n0, ew, lane, epoch,
-                                      out_tile, aux, limit))
+        if (share && !reduce_share<C>(p, rpartials, p.flags, w.owner, w.owner_bank2,
+                                      w.contrib_last, w.part_last, unit, slot_stride, (int)crank,
+                                      m0, n0, ew, lane, epoch, out_tile, aux, limit))
           break;
-      } else {
+      }
+      if (!stores_partial || split) {
         const bool owner = (w.role == kRoleOwner);
-        if (owner) {
-          // Wait for every later CTA that covers part of this tile: the
-          // lanes of one warp poll up to 32 peers' flags at once.
+        if (owner || split) {
+          // Wait for every other CTA that covers part of this tile (an
+          // owner: the later ones; a split part: all of them, the owner's
+          // flag in bank 2 when it began earlier): the lanes of one warp
+          // poll up to 32 flags at once.
+          const int first_cover = split ? w.owner : unit + 1;
+          const int last_cover = split ? w.contrib_last : w.peer_last;
           bool fine = true;
           if (ew == 0) {
-            for (int peer = unit + 1 + lane; peer <= w.peer_last && fine; peer += 32) {
-              const int fi = peer * slot_stride + (int)crank;
+            for (int peer = first_cover + lane; peer <= last_cover && fine; peer += 32) {
+              if (peer == unit) continue;
+              const int fi = peer * slot_stride + (int)crank +
+                             (split && peer == w.owner && w.owner_bank2 ? kMaxCtas : 0);
+              const uint32_t* pf = split ? p.flags : rflags;
+              if (ld_acquire_gpu(&pf[fi]) == epoch) continue;
               if (ld_acquire_gpu(&rflags[fi]) == epoch) continue;
               const uint64_t t0 = globaltimer();
               uint32_t spins = 0;
-              while (ld_acquire_gpu(&rflags[fi]) != epoch) {
+              while (ld_acquire_gpu(&pf[fi]) != epoch) {
                 if (++spins > 64) nanosleep_ns(64);
                 if ((spins & 15) == 0 && globaltimer() - t0 > limit) {
                   record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
@@ -1987,7 +2102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         //    half-band pieces through a few pipelined slots, folded into the
         //    accumulator in TMEM, so the passes below see it fixed up.
         // (Runs at most once per CTA, so the barrier parities start at 0.)
-        bool add_partials = owner;
+        bool add_partials = owner && !split;
         bool c0_ring = false;
         constexpr uint32_t kQuarter = (uint32_t)(STAGES * C::STAGE_BYTES / 4) & ~1023u;
         constexpr uint32_t kC0Bytes = 32u * BN * C::OUT_BYTES;
@@ -1997,19 +2112,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         static_assert(kC0Bytes <= kQuarter && (C::ILC || kC0Off >= kHalf),
                       "ring quarter too small");
         uint8_t* qring = ring + ew * kQuarter;
-        if (last_item && !is_ck && w.role != kRolePeer) {
+        if (last_item && !is_ck && (w.role != kRolePeer || split)) {
           c0_ring = p.beta != 0.f && m0 + q * 32 < p.m;  // warp-uniform
           if (c0_ring && lane == 0) {
-            int nbox = 0;
-            while (nbox < BN / C::EPI_COLS && n0 + nbox * C::EPI_COLS < p.n) ++nbox;
-            mbar_arrive_expect_tx(&c0r_bar[ew], (uint32_t)nbox * C::EPI_BUF_BYTES);
-            for (int c = 0; c < nbox; ++c)
+            int nbox = c_lo;
+            while (nbox < c_hi && n0 + nbox * C::EPI_COLS < p.n) ++nbox;
+            mbar_arrive_expect_tx(&c0r_bar[ew], (uint32_t)(nbox - c_lo) * C::EPI_BUF_BYTES);
+            for (int c = c_lo; c < nbox; ++c)
               tma_load_2d(qring + kC0Off + c * C::EPI_BUF_BYTES, &tmC, &c0r_bar[ew],
                           n0 + c * C::EPI_COLS, m0 + q * 32);
           }
           c0r_pending = c0_ring;
         }
-        if (!C::ILC && owner && !is_ck && last_item) {
+        if (split) {
+          const uint32_t room = c0_ring ? kC0Off : kQuarter;
+          const int slots = min(kFixSlots, (int)(room / kHalf));
+          const bool fine = fold_split_through_ring<BN>(
+              qring, slots, rpartials, (size_t)p.ws_ctas * kBM * BN, w.owner, w.owner_bank2,
+              w.contrib_last, unit, slot_stride, (int)crank, q, lane, tacc, c_lo * C::EPI_COLS,
+              c_hi * C::EPI_COLS, &fix_bar[ew * kFixSlots], p, aux, limit);
+          if (!epi_all(fine && !aborted(aux))) {
+            tc_fence_before();
+            release_acc(ab);
+            break;
+          }
+        } else if (!C::ILC && owner && !is_ck && last_item) {
           const uint32_t room = c0_ring ? kC0Off : kQuarter;
           const int slots = min(kFixSlots, (int)(room / kHalf));
           const bool fine = fixup_through_ring<BN>(
@@ -2273,7 +2400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ StoreTile
         const bool rows_live = (m0 + q * 32) < p.m;
 #pragma unroll 1
-        for (int c = 0; c < BN / C::EPI_COLS; ++c) {
+        for (int c = c_lo; c < c_hi; ++c) {
           const int col0 = n0 + c * C::EPI_COLS;
           const bool st_chunk = rows_live && col0 < p.n && store_ok;  // warp-uniform
           uint8_t* buf = ebuf + bsel * C::EPI_BUF_BYTES;
@@ -2313,7 +2440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i == jc) y[hh * 32 + i] = fix_val;
             }
           }
-          if (c == BN / C::EPI_COLS - 1) {
+          if (c == c_hi - 1) {
             // Accumulator fully read: hand the TMEM buffer back to the MMA warp.
             tc_fence_before();
             release_acc(ab);

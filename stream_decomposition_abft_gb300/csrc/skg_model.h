@@ -56,21 +56,23 @@ inline const CostModel& model_for(int bn) {
 constexpr double kShareCoverCost = 0.27;
 
 // Whether the tile starting at iteration ti of an evenly split region is
-// reduced by its covering CTAs together (see Work::share_parts): its owner's
-// range starts at ti and at least kShareMin covering CTAs end in it. Gives
-// the number of those (parts) and of all covering CTAs (covers).
-inline bool shared_tile(int64_t q, int r, int64_t ti, int64_t I, int& parts, int& covers) {
+// reduced by its covering CTAs together (see Work::share_parts): at least
+// share_min covering CTAs end in it, and its owner's range starts at ti
+// unless bank2. Gives the number of those (parts) and of all covering CTAs
+// (covers).
+inline bool shared_tile(int64_t q, int r, int64_t ti, int64_t I, int share_min, bool bank2,
+                        int& parts, int& covers) {
   const int owner = even_cta_of(q, r, ti);
   int64_t ob, oe;
   even_range(q, r, owner, ob, oe);
-  if (ob != ti) return false;
+  if (ob != ti && !bank2) return false;
   const int last = even_cta_of(q, r, ti + I - 1);
   int64_t lb, le;
   even_range(q, r, last, lb, le);
   const int part_last = last - (le > ti + I ? 1 : 0);
   parts = part_last - owner + 1;
   covers = last - owner + 1;
-  return parts >= kShareMin;
+  return parts >= share_min;
 }
 
 // Segment counts of CTA x in an evenly split region of `total` iterations;
@@ -79,7 +81,8 @@ inline bool shared_tile(int64_t q, int r, int64_t ti, int64_t I, int& parts, int
 // store and covers / parts partial tiles of reads instead of the owner
 // reading every peer.
 inline void region_counts(int64_t q, int r, int64_t total, int64_t I, int x, bool share,
-                          int64_t& iters, int64_t& tiles, int64_t& partial, double& fix) {
+                          int share_min, bool bank2, int64_t& iters, int64_t& tiles,
+                          int64_t& partial, double& fix) {
   if (total <= 0) return;
   int64_t b, e;
   even_range(q, r, x, b, e);
@@ -93,14 +96,14 @@ inline void region_counts(int64_t q, int r, int64_t total, int64_t I, int x, boo
     tiles += started;
     const int64_t last = first + (started - 1) * I;
     if (last + I > e) {  // owns an unfinished tile
-      if (share && shared_tile(q, r, last, I, parts, covers)) {
+      if (share && shared_tile(q, r, last, I, share_min, bank2, parts, covers)) {
         partial += 1;
         fix += (double)covers / parts + kShareCoverCost * covers;
       } else {
         fix += even_cta_of(q, r, last + I - 1) - x;
       }
     }
-  } else if (share && shared_tile(q, r, (b / I) * I, I, parts, covers)) {
+  } else if (share && shared_tile(q, r, (b / I) * I, I, share_min, bank2, parts, covers)) {
     // The whole range lies inside a tile another CTA started and owns.
     fix += (double)covers / parts + kShareCoverCost * covers;
   }
@@ -121,9 +124,11 @@ inline double predict_us(const Schedule& s, const CostModel& M, bool share) {
       iters += nd * I;
       tiles += nd;
     }
-    region_counts(s.sk_q, s.sk_r, s.sk_total, I, x, share, iters, tiles, partial, fix);
+    region_counts(s.sk_q, s.sk_r, s.sk_total, I, x, share, s.share_min, s.share_bank2 != 0, iters,
+                  tiles, partial, fix);
     if (s.g_ck == 0)
-      region_counts(s.ck_q, s.ck_r, s.ck_total, I, x, false, iters, tiles, partial, fix);
+      region_counts(s.ck_q, s.ck_r, s.ck_total, I, x, false, kShareMin, false, iters, tiles,
+                    partial, fix);
     const double tx = M.a + M.c * (double)iters + M.e * (double)tiles + M.b * (double)partial +
                       M.d * fix;
     if (tx > worst) worst = tx;
@@ -131,7 +136,8 @@ inline double predict_us(const Schedule& s, const CostModel& M, bool share) {
   for (int x = 0; x < s.g_ckt; ++x) {  // dedicated side CTAs: the side region split over them
     int64_t iters = 0, tiles = 0, partial = 0;
     double fix = 0.0;
-    region_counts(s.ck_q, s.ck_r, s.ck_total, I, x, false, iters, tiles, partial, fix);
+    region_counts(s.ck_q, s.ck_r, s.ck_total, I, x, false, kShareMin, false, iters, tiles,
+                  partial, fix);
     const double tx = M.a + M.c * (double)iters + M.e * (double)tiles + M.b * (double)partial +
                       M.d * fix;
     if (tx > worst) worst = tx;

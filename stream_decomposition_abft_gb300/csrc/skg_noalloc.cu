@@ -82,14 +82,15 @@ extern "C" skg_status_t skg_gemm_noalloc(int64_t m, int64_t n, int64_t k, float 
   // tiles only, so a request for pairs keeps the library's choice.
   if (o.tile_n == 0 && o.cta_pair != 2) o.tile_n = 128;
   size_t need = 0;
-  const skg_status_t st_need = skg::workspace_need(m, n, k, a_layout, b_layout, &o, &need);
+  const skg_status_t st_need = skg::workspace_need(m, n, k, a_layout, b_layout, &o, &need, true);
   if (st_need != SKG_OK) return st_need;
   if (need > (size_t)SKG_NOALLOC_SCRATCH_BYTES) return SKG_ERR_WORKSPACE;
   void* scratch = nullptr;
   const skg_status_t st = scratch_for_current_device(&scratch, (cudaStream_t)stream);
   if (st != SKG_OK) return st;
-  return skg_gemm(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, a_layout,
-                  b_layout, &o, scratch, (size_t)SKG_NOALLOC_SCRATCH_BYTES, stream);
+  return skg::gemm_compact(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype,
+                           a_layout, b_layout, &o, scratch, (size_t)SKG_NOALLOC_SCRATCH_BYTES,
+                           stream);
 }
 
 extern "C" skg_status_t skg_noalloc_report_read(skg_report_t* out, int32_t reset, void* stream) {

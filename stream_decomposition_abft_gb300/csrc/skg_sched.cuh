@@ -39,7 +39,8 @@ enum : int { kRoleFull = 0, kRoleOwner = 1, kRolePeer = 2 };
 
 // Tiles of an output Stream-K region that this many covering CTAs end their
 // ranges in, the k = 0 CTA's range starting at the tile, are reduced by all
-// of those together in launches without ABFT (Work::share_parts).
+// of those together in launches without ABFT (Work::share_parts): the
+// default of Schedule::share_min.
 constexpr int kShareMin = 8;
 
 struct Schedule {
@@ -60,6 +61,21 @@ struct Schedule {
   int g_ckt;          // of those, the ones that run side tiles (the others
                       // only take part in the in-kernel encode pass)
   int band;           // tile columns per raster band (tiles_n = row-major)
+  // Shared reduction (launches without ABFT): a Stream-K tile that at least
+  // share_min covering CTAs end their ranges in is reduced by all of those.
+  // With share_bank2 the owner may also be a CTA whose range began in an
+  // earlier tile (it already holds a partial there): its partial of the
+  // shared tile and its flag then live in a second bank (the storage of the
+  // otherwise unused second region).
+  int share_min;
+  int share_bank2;
+  // Split reduction (launches without ABFT): a Stream-K tile that 2 ..
+  // split_max covering CTAs end their ranges in (fewer than share_min) is
+  // finished by those CTAs together, each owning a range of the tile's
+  // columns: every one stores its partial, then folds the other covering
+  // CTAs' partials of its columns into its own accumulator and stores them
+  // (0 = off; needs share_bank2 when an owner began in an earlier tile).
+  int split_max;
 };
 
 // Output-tile coordinates of tile index `tile` (>= t_ck) under the banded
@@ -114,6 +130,9 @@ SKG_HD Schedule make_schedule(int64_t m, int64_t n, int64_t k, int bm, int bn, i
   s.ck_q = s.ck_total / ck_ctas;
   s.ck_r = (int)(s.ck_total % ck_ctas);
   s.band = s.tiles_n > 0 ? s.tiles_n : 1;
+  s.share_min = kShareMin;
+  s.share_bank2 = 0;
+  s.split_max = 0;
   return s;
 }
 
@@ -146,11 +165,11 @@ struct Work {
   int peer_last;         // OWNER: last peer CTA (peers are cta+1 .. peer_last)
   int region;            // 0: output tiles, 1: side tiles (own partial slots and flags)
   // CTAs covering the tile: owner .. contrib_last; those up to part_last
-  // end their ranges inside it (the tile is their last work in the region).
-  // share_parts = part_last - owner + 1 when the owner's range also begins
-  // at the tile's first iteration (so the owner holds no other partial in
-  // the region), else 0.
-  int owner, contrib_last, part_last, share_parts;
+  // end their ranges inside it (the tile is their last work in the region);
+  // share_parts = part_last - owner + 1 of them. owner_bank2: the owner's
+  // range began in an earlier tile, so it holds another partial in the
+  // region (a shared reduction keeps its partial of this tile in bank 2).
+  int owner, contrib_last, part_last, share_parts, owner_bank2;
 };
 
 // Walks one CTA's segments in execution order: its share of the side
@@ -203,10 +222,25 @@ struct Cursor {
     w.owner = cta_base + owner_rel;
     w.contrib_last = cta_base + last_rel;
     w.part_last = w.contrib_last - (last_e > tile_iter_end ? 1 : 0);
-    w.share_parts = owner_b == tile_iter ? w.part_last - w.owner + 1 : 0;
+    w.share_parts = w.part_last - w.owner + 1;
+    w.owner_bank2 = owner_b != tile_iter ? 1 : 0;
     w.peer_last = (w.role == kRoleOwner) ? w.contrib_last : x;
     w.region = region;
     pos = tile_iter_end;
+  }
+
+  // Whether segment w's tile is reduced by its parts together (launches
+  // without ABFT; the caller also checks that it is one of the parts).
+  SKG_HD static bool shared(const Schedule& s, const Work& w) {
+    return w.region == 0 && w.role != kRoleFull && w.share_parts >= s.share_min &&
+           (!w.owner_bank2 || s.share_bank2);
+  }
+  // Whether segment w's tile is finished by a split reduction (see
+  // Schedule::split_max; the caller also checks that it is one of the parts).
+  SKG_HD static bool split(const Schedule& s, const Work& w) {
+    return w.region == 0 && w.role != kRoleFull && w.share_parts >= 2 &&
+           w.share_parts <= s.split_max && w.share_parts < s.share_min &&
+           (!w.owner_bank2 || s.share_bank2);
   }
 
   SKG_HD bool next(const Schedule& s, Work& w) {
@@ -223,6 +257,7 @@ struct Cursor {
       w.region = 0;
       w.owner = w.contrib_last = w.part_last = x;
       w.share_parts = 0;
+      w.owner_bank2 = 0;
       next_dp += s.g;
       return true;
     }

@@ -162,6 +162,64 @@ def test_shared_tile_reduction(out, pair):
     assert ws.report().status_bits == 0
 
 
+# Split reduction (no ABFT, single CTAs): a Stream-K tile that 2 .. BLK_N /
+# (staging chunk) CTAs end their ranges in is finished by those CTAs
+# together, each folding the others' partials into its own columns; owners
+# whose range began in an earlier tile keep that partial in bank 2.
+SPLIT_CASES = [(256, 17, "sk"), (128, 37, "sk"), (64, 70, "sk"), (256, 8, "dp_sk1"),
+               (128, 13, "sk2_dp")]
+
+
+@pytest.mark.parametrize("out", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("case", SPLIT_CASES)
+def test_split_reduction(out, case):
+    tile_n, g, mode = case
+    g = min(g, sms())
+    for (m, n, k) in ((640, 512, 8192), (600, 500, 8000)):
+        p = inputs.make_problem(m, n, k, seed=60 + g, in_dtype="f16", out_dtype=out,
+                                law_a="uniform", law_b="uniform", alpha=1.5, beta=0.5)
+        ref = reference(p)
+        rows, C, ws = device_trace(p, dict(sched=mode, tile_n=tile_n), g)
+        check_full(p, C, ref)
+        assert rows == ss.flatten(ss.schedule(m, n, k, 128, tile_n, 64, g, mode=mode))
+        assert ws.report().status_bits == 0
+
+
+@pytest.mark.parametrize("a_layout,b_layout", [(1, 1), (0, 1)])
+def test_split_reduction_mn_major(a_layout, b_layout):
+    p = inputs.make_problem(640, 512, 8192, seed=71, in_dtype="bf16", out_dtype="f32",
+                            law_a="normal", law_b="normal", alpha=1.5, beta=0.5,
+                            a_layout=a_layout, b_layout=b_layout)
+    C, ws, st = run(p, skgemm.opts_default(sched="sk", tile_n=256, grid=min(17, sms())))
+    assert st == skgemm.OK
+    check_full(p, C)
+
+
+def test_split_reduction_injection():
+    # A flip in a column that the second part of a split tile stores reaches
+    # C at that element only.
+    p = inputs.make_problem(640, 512, 8192, seed=72, in_dtype="bf16", out_dtype="f32",
+                            law_a="normal", law_b="normal")
+    ref = reference(p)
+    g = min(17, sms())
+    sch = ss.schedule(640, 512, 8192, 128, 256, 64, g, mode="sk")
+    op = ss.owners_and_peers(sch)
+    # a tile covered by three CTAs: the owner and the middle one end in it
+    tile = next(t for t, (o, peers) in sorted(op.items()) if len(peers) == 2)
+    col = 200  # in the last quarter: the middle part's columns
+    opts = skgemm.opts_default(sched="sk", tile_n=256, grid=g, inject_tile=tile, inject_row=5,
+                               inject_col=col, inject_bit=30)
+    C, ws, st = run(p, opts)
+    assert st == skgemm.OK
+    got = C.cpu().double().numpy()
+    tm, tn = divmod(tile, 2)
+    bad = (tm * 128 + 5, tn * 256 + col)
+    diff = np.abs(got - ref)
+    assert not (diff[bad] < 1e-3)
+    diff[bad] = 0
+    assert diff.max() < 1e-2
+
+
 def test_shared_tile_reduction_timeout_reports_and_returns():
     # One CTA of a shared-reduction tile skips its Signal: every other CTA of
     # the tile runs out its bounded flag wait; the launch records
