@@ -649,8 +649,8 @@ def workload_hostile(args):
             opts = skgemm.opts_default(**kw)
             tn, g, sc = skgemm.launch_shape(m, n, k, opts)
             pl = skgemm.launch_plan(m, n, k, opts)
-            clk = torch.zeros(2 * g, dtype=torch.int64, device=dev)
-            opts.cta_clock = clk.data_ptr()
+            nclk = 7
+            clk = torch.zeros(nclk, 2 * g, dtype=torch.int64, device=dev)
             ws = skgemm.Workspace(skgemm.workspace_size(m, n, k, opts), dev)
 
             def launch():
@@ -662,11 +662,17 @@ def workload_hostile(args):
                     raise skgemm.SkgError(st, "skg_gemm")
 
             ms = _time_launch(launch, flush, max(5, args.steps // 10), stream)
-            spreads, spreads90 = [], []
-            for _ in range(7):
+            # Per-CTA busy time of nclk launches issued back to back (as the
+            # timed ones are), each with its own clock buffer.
+            for i in range(nclk):
+                opts.cta_clock = clk[i].data_ptr()
                 flush.zero_()
                 launch()
-                c = clk.view(g, 2).cpu().double()
+            opts.cta_clock = None
+            torch.cuda.synchronize()
+            spreads, spreads90 = [], []
+            for i in range(nclk):
+                c = clk[i].view(g, 2).cpu().double()
                 busy = (c[:, 1] - c[:, 0])
                 spreads.append(float((busy.max() - busy.min()) / busy.max()))
                 q = torch.quantile(busy, torch.tensor([0.05, 0.95], dtype=busy.dtype))
