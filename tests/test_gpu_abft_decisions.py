@@ -507,6 +507,15 @@ def _sequence():
                              law_a="normal", law_b="normal"), dict(abft=1)),
         (inputs.make_problem(384, 4096, 704, seed=55, in_dtype="bf16", out_dtype="bf16",
                              law_a="normal", law_b="normal"), dict(sched="sk", tile_n=256)),
+        # split reductions whose owners keep their partial in bank 2 (the
+        # storage the ABFT calls use for their checksum tiles), 256 and 64 wide
+        (inputs.make_problem(640, 512, 8192, seed=56, in_dtype="f16", out_dtype="f16",
+                             law_a="uniform", law_b="uniform", alpha=1.5, beta=0.5),
+         dict(sched="sk", tile_n=256, grid=17)),
+        (inputs.make_problem(1536, 640, 2048, seed=57, in_dtype="bf16", out_dtype="f32",
+                             law_a="normal", law_b="normal"), dict(abft=1, tile_n=128)),
+        (inputs.make_problem(640, 512, 8192, seed=58, in_dtype="bf16", out_dtype="f32",
+                             law_a="normal", law_b="normal"), dict(sched="sk", tile_n=64, grid=70)),
         (inputs.make_problem(2048, 2048, 1024, seed=51, in_dtype="bf16", out_dtype="bf16",
                              law_a="normal", law_b="normal"), dict()),
     ]
