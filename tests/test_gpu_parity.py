@@ -220,6 +220,29 @@ def test_split_reduction_injection():
     assert diff.max() < 1e-2
 
 
+def test_split_reduction_timeout_reports_and_returns():
+    # The middle part of a split tile skips its Signal: the owner part's
+    # bounded wait runs out, the launch records SKG_ERR_FIXUP_TIMEOUT, and
+    # the device stays usable.
+    p = inputs.make_problem(640, 512, 8192, seed=73, in_dtype="bf16", out_dtype="f32")
+    g = min(17, sms())
+    sch = ss.schedule(640, 512, 8192, 128, 256, 64, g, mode="sk")
+    op = ss.owners_and_peers(sch)
+    middle = next(peers[0] for t, (o, peers) in sorted(op.items()) if len(peers) == 2)
+    opts = skgemm.opts_default(sched="sk", grid=g, tile_n=256, timeout_ns=50_000_000,
+                               test_drop_signal=middle + 1)
+    C, ws, st = run(p, opts)
+    assert st == skgemm.OK
+    rep = ws.report()
+    assert rep.status_bits & (1 << skgemm.ERR_FIXUP_TIMEOUT)
+    assert rep.timeouts >= 1
+    p2 = inputs.make_problem(640, 512, 8192, seed=74, in_dtype="bf16", out_dtype="f32")
+    C2, ws2, st2 = run(p2, skgemm.opts_default(sched="sk", grid=g, tile_n=256))
+    assert st2 == skgemm.OK
+    check_full(p2, C2)
+    assert ws2.report().status_bits == 0
+
+
 def test_shared_tile_reduction_timeout_reports_and_returns():
     # One CTA of a shared-reduction tile skips its Signal: every other CTA of
     # the tile runs out its bounded flag wait; the launch records
