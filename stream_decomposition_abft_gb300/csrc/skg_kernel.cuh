@@ -157,6 +157,13 @@ struct KernelParams {
   // needs only the A (or B) tile and a few encoding rows, so two fit in one
   // BLK_N = 256 stage; packed stages hold A(k), A(k+1), enc(k), enc(k+1).
   int ck_kpack_cr, ck_kpack_cc;
+  // ck_atomic (with the in-kernel encode pass, whose CTAs zero cr_all and
+  // ccT_all before they report): every checksum-tile segment adds its rows
+  // into them with a TMA reduce-add, whatever its Stream-K role, so no
+  // segment waits for another; ck_target segment reports (kCkHalf per
+  // segment) mean all of them landed.
+  int ck_atomic;
+  int ck_target;
   uint32_t idesc_cr, idesc_cc;
   float tau_row, tau_col;  // <= 0: derive from the encode pass maxima
   // Fault injection (testing only): up to two single-bit flips of the fp32
@@ -1819,6 +1826,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_bar_sync(1, kEpiThreads);  // part and tmax reused by the next unit
       }
+      // The checksum segments add into cr_all / ccT_all: this CTA zeroes its
+      // share of them first.
+      if (p.ck_atomic) {
+        const int64_t ncr = (int64_t)p.m * p.ld_cr / 4, ncc = (int64_t)p.n * p.ld_cc / 4;
+        const int j = (int)blockIdx.x - s.g;
+        float4* zcr = reinterpret_cast<float4*>(const_cast<float*>(p.cr_all));
+        float4* zcc = reinterpret_cast<float4*>(const_cast<float*>(p.cc_all));
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int64_t i = j * (int64_t)kEpiThreads + et; i < ncr; i += (int64_t)s.g_ck * kEpiThreads)
+          zcr[i] = z;
+        for (int64_t i = j * (int64_t)kEpiThreads + et; i < ncc; i += (int64_t)s.g_ck * kEpiThreads)
+          zcc[i] = z;
+      }
       // Every encode write of this CTA lands before the counter moves.
       __threadfence();
       named_bar_sync(1, kEpiThreads);
@@ -1901,7 +1921,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool fine = true;
           if (et == 0) {
             const uint64_t t0 = globaltimer();
-            while (ld_acquire_gpu(&p.hdr->ck_done[par]) < (uint32_t)(kCkHalf * s.t_ck)) {
+            const uint32_t ck_want =
+                p.ck_atomic ? (uint32_t)p.ck_target : (uint32_t)(kCkHalf * s.t_ck);
+            while (ld_acquire_gpu(&p.hdr->ck_done[par]) < ck_want) {
               nanosleep_ns(128);
               if (globaltimer() - t0 > limit) {
                 record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
@@ -2031,7 +2053,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // StorePartials + Signal (Algorithm 5, non-started segment): peers,
       // the parts of a shared reduction, and the parts of a split one (which
       // keep the accumulator for their own columns).
-      const bool stores_partial = w.role == kRolePeer || share || split;
+      // (Checksum-tile segments that add into the reference arrays store no
+      // partial and wait for no peer.)
+      const bool ck_add = C::ABFT && is_ck && p.ck_atomic;
+      const bool stores_partial = (w.role == kRolePeer && !ck_add) || share || split;
       if (stores_partial) {
 #pragma unroll 1
         for (int c32 = 0; c32 < live_chunks; ++c32) {
@@ -2059,7 +2084,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!stores_partial || split) {
         const bool owner = (w.role == kRoleOwner);
-        if (owner || split) {
+        if ((owner && !ck_add) || split) {
           // Wait for every other CTA that covers part of this tile (an
           // owner: the later ones; a split part: all of them, the owner's
           // flag in bank 2 when it began earlier): the lanes of one warp
@@ -2152,7 +2177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (C::ABFT && is_ck) {
           // -------------------------------------------- fused checksum tile
-          // Store fp32 rows of cr_all or ccT_all, then count the tile done
+          // Store fp32 rows of cr_all or ccT_all (ck_atomic: add this
+          // segment's rows into them), then count the tile (segment) done
           // once every warp's stores have landed.
           const bool cr_side = w.tile < p.ck_cr_tiles;
           const CUtensorMap* mapC = cr_side ? &tmCr : &tmCc;
@@ -2168,7 +2194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tacc + c * 32, u);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
-            if (owner)
+            if (owner && !ck_add)
               add_peer_partials<BN>(v, rpartials, unit + 1, w.peer_last, c, r, w.region == 0,
                                     slot_stride, (int)crank);
             if (c == nchunks - 1) {
@@ -2186,7 +2212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(mapC, buf, c * 32, r0 + q * 32);
+              if (ck_add) tma_reduce_add_2d(mapC, buf, c * 32, r0 + q * 32);
+              else tma_store_2d(mapC, buf, c * 32, r0 + q * 32);
               bulk_commit();
             }
             bsel = (bsel + 1) % C::EPI_BUFS;
