@@ -175,6 +175,10 @@ PLANS = {
     "sk_128": dict(tile_n=128, sched="sk", cta_pair=1, grid=37),
     "sk2dp_256": dict(tile_n=256, sched="sk2_dp", cta_pair=1, grid=19),
     "pairs_256": dict(tile_n=256, cta_pair=2, sched="sk", grid=12),
+    # the library's own plan: idle SMs run the encode pass in the launch and
+    # the checksum tiles, split over them, add their segments into the
+    # references they zeroed
+    "inkernel_128": dict(tile_n=128, cta_pair=1),
     # reference checksums accumulated in the mainloop, several tiles per CTA
     "inloop_128": dict(tile_n=128, cta_pair=1, abft_inloop=2, grid=5),
     "inloop_pairs": dict(tile_n=256, cta_pair=2, abft_inloop=2, grid=4),
@@ -233,6 +237,12 @@ def test_decisions_match_oracle(plan, name):
         v = C_exact[tm * 128 + r, tn * bn + c]
         assert got[tm * 128 + r, tn * bn + c] == ab.flip_f32(v, b)
     assert np.array_equal(got[mask], C_exact[mask])
+
+
+def test_inkernel_plan_is_the_in_launch_encode():
+    pl = skgemm.launch_plan(M, N, K, skgemm.opts_default(abft=1, **PLANS["inkernel_128"]))
+    assert pl.encode_in_kernel == 1 and pl.side_ctas > 0
+    assert pl.side_checksum_ctas == pl.side_ctas   # checksum tiles split over all of them
 
 
 def test_clean_run_checks_every_tile_with_no_record():
