@@ -2415,7 +2415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fix_col = bcol;
             fix_val = aux->fix_value;
           }
-          named_bar_sync(1, kEpiThreads);  // everyone has read the verdict
+          named_bar_sync(1, kEpiThreads);  // everyone has read the decision
           if (et == 0) {
             aux->nbad_r = 0;
             aux->nbad_c = 0;

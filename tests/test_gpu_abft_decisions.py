@@ -60,7 +60,7 @@ def integer_problem(seed):
 
 
 def oracle_outcomes(p, C_exact, bn, flips):
-    """Oracle verdict of every tile that gets a flip.
+    """Oracle decision for every tile that gets a flip.
 
     flips: list of (tile, row, col, bit) applied to the exact product (the
     GPU's own pre-fault accumulator on integer data). Returns {tile: result
