@@ -89,6 +89,10 @@ def test_noalloc_sequence_of_shapes_and_options():
          dict(abft=1, cta_pair=2, tile_n=256, grid=16)),
         (inputs.make_problem(384, 4096, 704, seed=64, in_dtype="bf16", out_dtype="bf16",
                              law_a="normal", law_b="normal"), dict(sched="sk", tile_n=128)),
+        # 64-wide tiles; skg_gemm splits the tiles two CTAs end in, the
+        # allocation-free entry keeps the owner fixup (same sums: two parts)
+        (inputs.make_problem(640, 512, 8192, seed=65, in_dtype="bf16", out_dtype="f32",
+                             law_a="normal", law_b="normal"), dict(sched="sk", tile_n=64, grid=70)),
         (inputs.make_problem(2048, 2048, 1024, seed=61, in_dtype="bf16", out_dtype="bf16",
                              law_a="normal", law_b="normal"), dict(tile_n=128)),
     ]
