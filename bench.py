@@ -345,17 +345,18 @@ def measure_e2e(args, problems, dev, stream, opts, enc_opts):
     """Same metric through the public C ABI's host-buffer call, skg_gemm_host:
     every step copies that step's A and B from page-locked host memory into
     device staging, runs the ABFT GEMM and copies C back to host memory, all
-    inside the timed region. Consecutive steps alternate between two streams
-    (each with its own staging, workspace and host C), so one step's copies
-    overlap the neighbouring steps' GEMM and opposite-direction copy, as a
-    stream of independent calls would; the value is the steps' flops over the
-    wall time of all of them."""
+    inside the timed region. Consecutive steps rotate over `--e2e-streams`
+    streams (each with its own staging, workspace and host C), so one step's
+    copies overlap the neighbouring steps' GEMM and opposite-direction copy, as
+    a stream of independent calls would; the value is the steps' flops over
+    the wall time of all of them."""
     import torch
     from stream_decomposition_abft_gb300 import skgemm
     steps = max(6, min(args.steps, 20))
     h2d = d2h = 0
     tf = []
-    streams = [stream, torch.cuda.Stream(dev)]
+    streams = [stream] + [torch.cuda.Stream(dev) for _ in range(max(1, args.e2e_streams) - 1)]
+    ns = len(streams)
     o = skgemm.opts_default(abft=1)
     for pr in problems:
         s = pr["size"]
@@ -371,7 +372,7 @@ def measure_e2e(args, problems, dev, stream, opts, enc_opts):
                 hC=torch.empty((s, s), dtype=torch.bfloat16).pin_memory()))
 
         def issue(i):
-            ln = lanes[i % 2]
+            ln = lanes[i % ns]
             rc = skgemm.gemm_host(s, s, s, 1.0, hA.data_ptr(), s, hB.data_ptr(), s, 0.0,
                                   ln["hC"].data_ptr(), s, skgemm.IN_BF16, skgemm.OUT_BF16, 0, 0,
                                   o, ln["staging"].data_ptr(), ln["staging"].numel(),
@@ -379,17 +380,19 @@ def measure_e2e(args, problems, dev, stream, opts, enc_opts):
             if rc != skgemm.OK:
                 raise skgemm.SkgError(rc, "skg_gemm_host")
 
-        for i in range(4):  # warm-up, both lanes
+        for i in range(2 * ns):  # warm-up, every lane
             issue(i)
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t0.record(streams[0])
-        streams[1].wait_event(t0)
+        for st in streams[1:]:
+            st.wait_event(t0)
         for i in range(steps):
             issue(i)
-        e1 = torch.cuda.Event()
-        e1.record(streams[1])
-        streams[0].wait_event(e1)
+        for st in streams[1:]:
+            e1 = torch.cuda.Event()
+            e1.record(st)
+            streams[0].wait_event(e1)
         t1 = torch.cuda.Event(enable_timing=True)
         t1.record(streams[0])
         torch.cuda.synchronize()
@@ -402,7 +405,7 @@ def measure_e2e(args, problems, dev, stream, opts, enc_opts):
         d2h += s * s * 2
     return {"value": round(geomean(tf), 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "per_shape_tflops": [round(x, 2) for x in tf],
-            "api": "skg_gemm_host (host A, B, C; device staging), two streams alternating"}
+            "api": f"skg_gemm_host (host A, B, C; device staging), {ns} streams in turn"}
 
 
 def load_traffic():
@@ -923,6 +926,8 @@ def main():
                     help="square sweep: timed GEMM time per shape, at least (ms); 0 for "
                          "profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=3,
+                    help="streams the end-to-end leg's host-buffer calls rotate over")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ncu-target", action="store_true",
                     help="run the sweep GEMMs untimed (profiling target)")
