@@ -276,7 +276,7 @@ struct Cfg {
 
 // Shared-memory bookkeeping that lives after the stage ring and staging.
 struct Aux {
-  uint64_t bars[56];      // full[S], empty[S], tfull[2], tempty[2], c0[4], drain, fix, c0r[4],
+  uint64_t bars[60];      // full[S], empty[S], tfull[2], tempty[2], c0[8], drain, fix, c0r[4],
                           // inj, injdone, xch
   uint32_t tmem_slot;
   int32_t abort_flag;
@@ -1213,8 +1213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* tfull_bar = empty_bar + STAGES;
   uint64_t* tempty_bar = tfull_bar + 2;
-  uint64_t* c0_bar = tempty_bar + 2;
-  uint64_t* drain_bar = c0_bar + 4;
+  uint64_t* c0_bar = tempty_bar + 2;  // [epilogue warp][staging buffer]: C0 rows landed
+  uint64_t* drain_bar = c0_bar + 8;
   uint64_t* fix_bar = drain_bar + 1;  // [epilogue warp][slot]: staged peer partials
   uint64_t* c0r_bar = fix_bar + 4 * kFixSlots;  // per epilogue warp: C0 staged in the ring
   // Mid-mainloop fault injection: the MMAs up to the chosen iteration are
@@ -1223,7 +1223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* injdone_bar = inj_bar + 1;
   // ILC with CTA pairs: the peer's column checksums have landed in xbuf.
   uint64_t* xch_bar = injdone_bar + 1;
-  static_assert(2 * 8 + 2 + 2 + 4 + 1 + 4 * kFixSlots + 4 + 2 + 1 <= 56, "barrier slots");
+  static_assert(2 * 8 + 2 + 2 + 8 + 1 + 4 * kFixSlots + 4 + 2 + 1 <= 60, "barrier slots");
   float* xbuf = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(aux) + C::AUX_BYTES);
 
   const int warp = threadIdx.x >> 5;
@@ -1740,7 +1740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ab = 0;
     uint32_t aphase = 0;
     int bsel = 0;
-    uint32_t c0_phase = 0;
+    uint32_t c0_phase = 0;     // bit b: parity of the next C0 copy into staging buffer b
     bool c0r_pending = false;  // C0 copies into the ring not yet waited for
     int estage = 0;            // in-CTA ABFT: the epilogue's place in the stage ring
     uint32_t ephase = 0;
@@ -2426,21 +2426,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ------------------------------------------------ StoreTile
         const bool rows_live = (m0 + q * 32) < p.m;
+        // beta != 0 outside the ring: each chunk's C0 rows come through its
+        // staging buffer, and the next chunk's copy is issued into the other
+        // buffer as soon as this chunk's rows are in registers, so the round
+        // trips overlap the combine and store of the chunk before.
+        const bool c0_staged = p.beta != 0.f && !c0_ring;
+        static_assert(C::EPI_BUFS == 2, "two C0 barriers per epilogue warp");
+        bool c0_ahead = false;  // this chunk's C0 copy is already in flight
 #pragma unroll 1
         for (int c = c_lo; c < c_hi; ++c) {
           const int col0 = n0 + c * C::EPI_COLS;
           const bool st_chunk = rows_live && col0 < p.n && store_ok;  // warp-uniform
           uint8_t* buf = ebuf + bsel * C::EPI_BUF_BYTES;
-          if (st_chunk) {
+          if (st_chunk && !c0_ahead) {
             // Free the staging buffer and start its C0 load before the
             // accumulator columns are read, so the latencies overlap.
             if (lane == 0) bulk_wait_read<C::EPI_BUFS - 1>();
             __syncwarp();
-            if (p.beta != 0.f && !c0_ring && lane == 0) {
-              mbar_arrive_expect_tx(&c0_bar[ew], C::EPI_BUF_BYTES);
-              tma_load_2d(buf, &tmC, &c0_bar[ew], col0, m0 + q * 32);
+            if (c0_staged && lane == 0) {
+              mbar_arrive_expect_tx(&c0_bar[2 * ew + bsel], C::EPI_BUF_BYTES);
+              tma_load_2d(buf, &tmC, &c0_bar[2 * ew + bsel], col0, m0 + q * 32);
             }
           }
+          c0_ahead = false;
           float y[C::EPI_COLS];
 #pragma unroll
           for (int hh = 0; hh < C::EPI_COLS / 32; ++hh) {
@@ -2482,16 +2490,30 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (got_c0) c0r_pending = false;
               c0src = qring + kC0Off + c * C::EPI_BUF_BYTES;
             } else {
-              got_c0 = __all_sync(0xffffffffu, wait_bar(&c0_bar[ew], c0_phase, aux, limit));
+              got_c0 = __all_sync(0xffffffffu, wait_bar(&c0_bar[2 * ew + bsel],
+                                                        (c0_phase >> bsel) & 1u, aux, limit));
             }
             if (!got_c0) {
               if (lane == 0 && !aborted(aux)) record_error(p, aux, SKG_ERR_PIPELINE_TIMEOUT);
               store_ok = false;  // stop storing; the next tile boundary exits
               continue;
             }
-            if (!c0_ring) c0_phase ^= 1;
+            if (!c0_ring) c0_phase ^= 1u << bsel;
             uint32_t w0[32];
             staging_read(c0src, lane, w0);
+            const int cn = c + 1;
+            if (c0_staged && cn < c_hi && n0 + cn * C::EPI_COLS < p.n) {
+              // The next buffer last held the previous chunk's output: once
+              // that store has read it, it takes the next chunk's C0 rows.
+              const int nb = (bsel + 1) % C::EPI_BUFS;
+              if (lane == 0) {
+                bulk_wait_read<C::EPI_BUFS - 2>();
+                mbar_arrive_expect_tx(&c0_bar[2 * ew + nb], C::EPI_BUF_BYTES);
+                tma_load_2d(ebuf + nb * C::EPI_BUF_BYTES, &tmC, &c0_bar[2 * ew + nb],
+                            n0 + cn * C::EPI_COLS, m0 + q * 32);
+              }
+              c0_ahead = true;
+            }
             float c0v[C::EPI_COLS];
             unpack_row<C::OUT>(w0, c0v);
 #pragma unroll
