@@ -92,6 +92,24 @@ def test_small_shapes(shape, mode):
             check_full(p, C, ref)
 
 
+@pytest.mark.parametrize("out", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("tile_n,pair", [(64, 1), (128, 1), (256, 1), (256, 2)])
+def test_beta_chunks_of_earlier_tiles(out, tile_n, pair):
+    # beta != 0 on tiles that are not a CTA's last (few CTAs, several tiles
+    # each): every staging chunk's C0 rows are fetched one chunk ahead, and
+    # chunks that lie wholly past n (n = 300: the second column tile of a
+    # 256-wide tile keeps 44 of its columns) are neither fetched nor stored.
+    p = inputs.make_problem(300, 300, 192, seed=95 + tile_n, in_dtype="bf16", out_dtype=out,
+                            law_a="normal", law_b="uniform", alpha=-1.25, beta=0.75)
+    ref = reference(p)
+    for mode, g in (("dp", 2 * pair), ("sk", 2 * pair), ("sk2_dp", 3 * pair)):
+        C, ws, st = run(p, skgemm.opts_default(sched=mode, tile_n=tile_n, cta_pair=pair,
+                                               grid=g))
+        assert st == skgemm.OK
+        check_full(p, C, ref)
+        assert ws.report().status_bits == 0
+
+
 @pytest.mark.parametrize("k", [1, 7, 65, 100, 129])
 def test_ragged_k_with_padded_ld(k):
     # k not a multiple of 8 needs a padded row stride (TMA stride rule);
