@@ -1189,6 +1189,227 @@ static __device__ __noinline__ void mid_inject_flip(const KernelParams& p, uint3
   }
 }
 
+// Result of an output tile's ABFT check (check_tile): the located element
+// and its corrected value (row < 0: none located).
+struct TileFix {
+  int row, col;
+  float val;
+};
+
+// The ABFT check of one output tile in TMEM ("Anatomy of High-Performance
+// GEMM with Online Fault Tolerance on GPUs", Fig. 3 (d)-(f)): thread r of the
+// four epilogue warps sums accumulator row r (after adding the Stream-K
+// peers' partials when add_partials, and, when `flips`, the testing flips,
+// both written back to TMEM), the warps' column sums meet in their staging
+// buffers, and each sum is compared with its reference (pf_*: the row
+// checksum of row r, the column checksums of columns h * 128 + r, the
+// encode pass's tile maxima and scales) under tau_row / tau_col. Exactly
+// one mismatching row and column locate an element, whose value is
+// recomputed from the row checksum and the rest of the row; any other
+// mismatch is uncorrectable. Outcomes go to the report. The epilogue runs it
+// before the tile's stores, or (a tile stored first) after them.
+template <class C>
+static __device__ __forceinline__ TileFix check_tile(
+    const KernelParams& p, Aux* aux, uint8_t* epi, uint32_t tacc, int q, int lane, int et, int r,
+    bool add_partials, float* rpartials, int unit, int peer_last, bool region0, int slot_stride,
+    int crank, bool inject_here, bool flips, bool injected_tile, int out_tile, uint32_t epoch,
+    float pf_ma, float pf_mb, float pf_cr0, float pf_cr1, const float* pf_cc0,
+    const float* pf_cc1, int pf_ea, int pf_eb) {
+  constexpr int BN = C::BN;
+  auto colsum_of = [&](int qq) -> float* {
+    const int ew_of_q = (qq + 2) & 3;  // warps 2..5 own quadrants 2, 3, 0, 1
+    return reinterpret_cast<float*>(epi + ew_of_q * C::EPI_BUFS * C::EPI_BUF_BYTES);
+  };
+  TileFix fix{-1, -1, 0.f};
+  // This warp's staging buffers hold its column sums below: its own
+  // earlier TMA stores must have finished reading them.
+  if (lane == 0) bulk_wait_read<0>();
+  __syncwarp();
+  float* my_colsum = colsum_of(q);
+  float rowsum = 0.f;
+#pragma unroll 1
+  for (int c32 = 0; c32 < BN / 32; ++c32) {
+    uint32_t u[32];
+    tmem_ld32(tacc + c32 * 32, u);
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
+    if (add_partials)
+      add_peer_partials<BN>(v, rpartials, unit + 1, peer_last, c32, r, region0,
+                            slot_stride, crank);
+    // Fault injection (testing only): bits of fp32 accumulators,
+    // after the fixup and before the check.
+    bool inj_chunk = false;
+    if (inject_here && flips) {
+      float clean = 0.f;
+      const bool hit = apply_flips(p, out_tile, r, c32, v, &clean);
+      if (hit) aux->inj_clean = clean;
+      inj_chunk = __any_sync(0xffffffffu, hit);
+    }
+    if (add_partials || inj_chunk) {
+      uint32_t wv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) wv[i] = __float_as_uint(v[i]);
+      tmem_st32(tacc + c32 * 32, wv);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) rowsum += v[i];
+    my_colsum[c32 * 32 + lane] = warp_column_sums(v, lane);
+  }
+  // Reference checksums of this tile: thread r holds the row checksum
+  // of row r and the column checksum of columns h*128 + r, each the
+  // sum of its hi and lo partial products, unscaled by the tile's
+  // power of two; tile maxima for the thresholds are the max over
+  // the tile's encode units.
+  const float cr = ldexpf(pf_cr0 + pf_cr1, -pf_eb);
+  float cc[C::CC_GROUPS];
+#pragma unroll
+  for (int h = 0; h < C::CC_GROUPS; ++h) cc[h] = ldexpf(pf_cc0[h] + pf_cc1[h], -pf_ea);
+  {
+    float ma = pf_ma, mb = pf_mb;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, off));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+    }
+    if (lane == 0) {
+      aux->tmax_a[q] = ma;
+      aux->tmax_b[q] = mb;
+    }
+  }
+  named_bar_sync(1, kEpiThreads);  // column sums and tile maxima stored
+  // Default thresholds from the tile's own maxima:
+  //   tau = 2^-12 sqrt(k) sqrt(side) max|A_tile| max|B_tile|.
+  float tau_r = p.tau_row, tau_c = p.tau_col;
+  {
+    const float ma = fmaxf(fmaxf(aux->tmax_a[0], aux->tmax_a[1]),
+                           fmaxf(aux->tmax_a[2], aux->tmax_a[3]));
+    const float mb = fmaxf(fmaxf(aux->tmax_b[0], aux->tmax_b[1]),
+                           fmaxf(aux->tmax_b[2], aux->tmax_b[3]));
+    const float base = ldexpf(1.f, -12) * sqrtf((float)p.k) * ma * mb;
+    if (!(tau_r > 0.f)) tau_r = base * sqrtf((float)BN);
+    if (!(tau_c > 0.f)) tau_c = base * sqrtf((float)kBM);
+  }
+  if (et == 0) {  // the report keeps the largest thresholds used
+    atomicMax(reinterpret_cast<int*>(&p.report->tau_row), __float_as_int(tau_r));
+    atomicMax(reinterpret_cast<int*>(&p.report->tau_col), __float_as_int(tau_c));
+  }
+
+  const float d_r = rowsum - cr;
+  const bool bad_r = !(fabsf(d_r) <= tau_r);
+  float ratio_r = bad_r ? 0.f : fabsf(d_r) / tau_r;
+  float ratio_c = 0.f;
+  if (bad_r) {
+    atomicAdd(&aux->nbad_r, 1);
+    aux->bad_row = r;
+    aux->d_row = d_r;
+  }
+#pragma unroll
+  for (int h = 0; h < C::CC_GROUPS; ++h) {
+    const int j = h * 128 + r;
+    const float tot =
+        colsum_of(0)[j] + colsum_of(1)[j] + colsum_of(2)[j] + colsum_of(3)[j];
+    const float d_c = tot - cc[h];
+    if (!(fabsf(d_c) <= tau_c)) {
+      atomicAdd(&aux->nbad_c, 1);
+      aux->bad_col = j;
+      aux->d_col = d_c;
+    } else {
+      ratio_c = fmaxf(ratio_c, fabsf(d_c) / tau_c);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    ratio_r = fmaxf(ratio_r, __shfl_xor_sync(0xffffffffu, ratio_r, off));
+    ratio_c = fmaxf(ratio_c, __shfl_xor_sync(0xffffffffu, ratio_c, off));
+  }
+  if (lane == 0) {
+    atomicMax(reinterpret_cast<int*>(&p.report->max_ratio_row), __float_as_int(ratio_r));
+    atomicMax(reinterpret_cast<int*>(&p.report->max_ratio_col), __float_as_int(ratio_c));
+  }
+  named_bar_sync(1, kEpiThreads);  // mismatch counts complete
+
+  const int nbr = aux->nbad_r, nbc = aux->nbad_c;
+  const int brow = aux->bad_row, bcol = aux->bad_col;
+  const bool single = (nbr == 1 && nbc == 1);
+  if (et == 0) atomicAdd(&p.report->tiles_checked, 1u);
+  if (single && (brow >> 5) == q) {
+    // Locate at (brow, bcol); recompute the value from the row
+    // checksum and the rest of the row (survives Inf / NaN).
+    float rest = 0.f, before = 0.f;
+#pragma unroll 1
+    for (int c32 = 0; c32 < BN / 32; ++c32) {
+      uint32_t u[32];
+      tmem_ld32(tacc + c32 * 32, u);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float x = f32_of(u[i]);
+        if (c32 * 32 + i == bcol) before = x;
+        else rest += x;
+      }
+    }
+    if (r == brow) {
+      const float after = cr - rest;
+      aux->fix_value = after;
+      atomicAdd(&p.report->detected, 1u);
+      atomicAdd(&p.report->corrected, 1u);
+      atomicOr(&p.report->status_bits, 1u << SKG_ABFT_CORRECTED);
+      const uint32_t idx = atomicAdd(&p.report->n_records, 1u);
+      if (idx < SKG_MAX_RECORDS) {
+        skg_fault_record_t* rec = &p.report->records[idx];
+        rec->launch = epoch;
+        rec->tile = out_tile;
+        rec->row = brow;
+        rec->col = bcol;
+        rec->status = SKG_ABFT_CORRECTED;
+        rec->n_bad_rows = nbr;
+        rec->n_bad_cols = nbc;
+        rec->injected = injected_tile ? 1u : 0u;
+        rec->before = before;
+        rec->after = after;
+        rec->delta_row = aux->d_row;
+        rec->delta_col = aux->d_col;
+        rec->clean_value = inject_here ? aux->inj_clean : 0.f;
+      }
+    }
+  } else if (!single && (nbr != 0 || nbc != 0) && et == 0) {
+    atomicAdd(&p.report->detected, 1u);
+    atomicAdd(&p.report->uncorrectable, 1u);
+    atomicOr(&p.report->status_bits, 1u << SKG_ABFT_UNCORRECTABLE);
+    const uint32_t idx = atomicAdd(&p.report->n_records, 1u);
+    if (idx < SKG_MAX_RECORDS) {
+      skg_fault_record_t* rec = &p.report->records[idx];
+      rec->launch = epoch;
+      rec->tile = out_tile;
+      rec->row = nbr == 1 ? brow : -1;
+      rec->col = nbc == 1 ? bcol : -1;
+      rec->status = SKG_ABFT_UNCORRECTABLE;
+      rec->n_bad_rows = nbr;
+      rec->n_bad_cols = nbc;
+      rec->injected = injected_tile ? 1u : 0u;
+      rec->before = 0.f;
+      rec->after = 0.f;
+      rec->delta_row = nbr ? aux->d_row : 0.f;
+      rec->delta_col = nbc ? aux->d_col : 0.f;
+      rec->clean_value = inject_here ? aux->inj_clean : 0.f;
+    }
+  }
+  named_bar_sync(1, kEpiThreads);  // corrected value published
+  if (single) {
+    fix.row = brow;
+    fix.col = bcol;
+    fix.val = aux->fix_value;
+  }
+  named_bar_sync(1, kEpiThreads);  // everyone has read the decision
+  if (et == 0) {
+    aux->nbad_r = 0;
+    aux->nbad_c = 0;
+    aux->bad_row = -1;
+    aux->bad_col = -1;
+  }
+  return fix;
+}
+
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     skg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -1912,29 +2133,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < C::CC_GROUPS; ++h) pf_cc0[h] = ls.cc[h];
         pf_ma = ls.ma;
         pf_mb = ls.mb;
-      } else if (verify_here) {
-        if (!C::ILC && s.t_ck > 0 && !ck_ready) {
-          // The fused checksum tiles must all be stored first. Every CTA runs
-          // its own share of them before its first output tile, and dedicated
-          // checksum CTAs wait only for each other (all resident), so this
-          // wait ends.
-          bool fine = true;
-          if (et == 0) {
-            const uint64_t t0 = globaltimer();
-            const uint32_t ck_want =
-                p.ck_atomic ? (uint32_t)p.ck_target : (uint32_t)(kCkHalf * s.t_ck);
-            while (ld_acquire_gpu(&p.hdr->ck_done[par]) < ck_want) {
-              nanosleep_ns(128);
-              if (globaltimer() - t0 > limit) {
-                record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
-                fine = false;
-                break;
-              }
+      }
+      // A tile whose references come late -- the first output tile of a
+      // launch whose side CTAs run the encode pass, since they store the
+      // references only once every one of them has encoded and added its
+      // checksum rows -- with beta = 0 and no fixup is stored first and
+      // checked once the references are in; a located fault then has its
+      // corrected value written over the element (the accumulator stays in
+      // TMEM until the check).
+      // (Only the launches that run the encode pass in their side CTAs can
+      // have such tiles: 128-wide tiles on single CTAs.)
+      constexpr bool kStoreFirst =
+          C::ABFT && !C::PAIR && !C::LOCAL && !C::ILC && !C::MN && BN == 128;
+      const bool spec = kStoreFirst && verify_here && w.role == kRoleFull && p.beta == 0.f &&
+                        p.ck_atomic && s.t_ck > 0 && !ck_ready;
+      // Wait until the fused checksum tiles are all stored (false: timed out).
+      auto wait_references = [&]() -> bool {
+        // The fused checksum tiles must all be stored first. Every CTA runs
+        // its own share of them before its first output tile, and dedicated
+        // checksum CTAs wait only for each other (all resident), so this
+        // wait ends.
+        bool fine = true;
+        if (et == 0) {
+          const uint64_t t0 = globaltimer();
+          const uint32_t ck_want =
+              p.ck_atomic ? (uint32_t)p.ck_target : (uint32_t)(kCkHalf * s.t_ck);
+          while (ld_acquire_gpu(&p.hdr->ck_done[par]) < ck_want) {
+            nanosleep_ns(128);
+            if (globaltimer() - t0 > limit) {
+              record_error(p, aux, SKG_ERR_FIXUP_TIMEOUT);
+              fine = false;
+              break;
             }
           }
-          if (!epi_all(fine && !aborted(aux))) break;
-          ck_ready = true;
         }
+        return epi_all(fine && !aborted(aux));
+      };
+      // Loads of the references and of the thresholds' inputs (pf_*).
+      auto load_references = [&]() {
         const float* ua = p.umax + (int64_t)tm * p.enc_slices;
         const float* ub = p.umax + (int64_t)(p.enc_tiles_a + tn) * p.enc_slices;
         if (et < p.enc_slices) {
@@ -1962,6 +2198,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           pf_ma = fmaxf(pf_ma, __ldcg(ua + j));
           pf_mb = fmaxf(pf_mb, __ldcg(ub + j));
         }
+      };
+      if (!C::LOCAL && verify_here && !spec) {
+        if (!C::ILC && s.t_ck > 0 && !ck_ready) {
+          if (!wait_references()) break;
+          ck_ready = true;
+        }
+        load_references();
       }
 
       // Mid-mainloop fault injection (testing only): once the MMAs up to MAC
@@ -2235,13 +2478,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ ABFT verify
         int fix_row = -1, fix_col = -1;
         float fix_val = 0.f;
-        if (verify_here) {
-          // This warp's staging buffers hold its column sums below: its own
-          // earlier TMA stores must have finished reading them.
-          if (lane == 0) bulk_wait_read<0>();
-          __syncwarp();
-          float* my_colsum = colsum_of(q);
-          float rowsum = 0.f;
+        auto check = [&](bool flips) {
+          const TileFix f = check_tile<C>(
+              p, aux, epi, tacc, q, lane, et, r, add_partials, rpartials, unit, w.peer_last,
+              w.region == 0, slot_stride, (int)crank, inject_here, flips, injected_tile, out_tile,
+              epoch, pf_ma, pf_mb, pf_cr0, pf_cr1, pf_cc0, pf_cc1, pf_ea, pf_eb);
+          fix_row = f.row;
+          fix_col = f.col;
+          fix_val = f.val;
+        };
+        if (verify_here && !spec) check(true);
+        if (kStoreFirst && spec && inject_here) {
+          // Testing flips land in TMEM before the tile is stored.
 #pragma unroll 1
           for (int c32 = 0; c32 < BN / 32; ++c32) {
             uint32_t u[32];
@@ -2249,178 +2497,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = f32_of(u[i]);
-            if (add_partials)
-              add_peer_partials<BN>(v, rpartials, unit + 1, w.peer_last, c32, r, w.region == 0,
-                                    slot_stride, (int)crank);
-            // Fault injection (testing only): bits of fp32 accumulators,
-            // after the fixup and before the check.
-            bool inj_chunk = false;
-            if (inject_here) {
-              float clean = 0.f;
-              const bool hit = apply_flips(p, out_tile, r, c32, v, &clean);
-              if (hit) aux->inj_clean = clean;
-              inj_chunk = __any_sync(0xffffffffu, hit);
-            }
-            if (add_partials || inj_chunk) {
+            float clean = 0.f;
+            const bool hit = apply_flips(p, out_tile, r, c32, v, &clean);
+            if (hit) aux->inj_clean = clean;
+            if (__any_sync(0xffffffffu, hit)) {
               uint32_t wv[32];
 #pragma unroll
               for (int i = 0; i < 32; ++i) wv[i] = __float_as_uint(v[i]);
               tmem_st32(tacc + c32 * 32, wv);
             }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) rowsum += v[i];
-            my_colsum[c32 * 32 + lane] = warp_column_sums(v, lane);
-          }
-          // Reference checksums of this tile: thread r holds the row checksum
-          // of row r and the column checksum of columns h*128 + r, each the
-          // sum of its hi and lo partial products, unscaled by the tile's
-          // power of two; tile maxima for the thresholds are the max over
-          // the tile's encode units.
-          const float cr = ldexpf(pf_cr0 + pf_cr1, -pf_eb);
-          float cc[C::CC_GROUPS];
-#pragma unroll
-          for (int h = 0; h < C::CC_GROUPS; ++h) cc[h] = ldexpf(pf_cc0[h] + pf_cc1[h], -pf_ea);
-          {
-            float ma = pf_ma, mb = pf_mb;
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-              ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, off));
-              mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
-            }
-            if (lane == 0) {
-              aux->tmax_a[q] = ma;
-              aux->tmax_b[q] = mb;
-            }
-          }
-          named_bar_sync(1, kEpiThreads);  // column sums and tile maxima stored
-          // Default thresholds from the tile's own maxima:
-          //   tau = 2^-12 sqrt(k) sqrt(side) max|A_tile| max|B_tile|.
-          float tau_r = p.tau_row, tau_c = p.tau_col;
-          {
-            const float ma = fmaxf(fmaxf(aux->tmax_a[0], aux->tmax_a[1]),
-                                   fmaxf(aux->tmax_a[2], aux->tmax_a[3]));
-            const float mb = fmaxf(fmaxf(aux->tmax_b[0], aux->tmax_b[1]),
-                                   fmaxf(aux->tmax_b[2], aux->tmax_b[3]));
-            const float base = ldexpf(1.f, -12) * sqrtf((float)p.k) * ma * mb;
-            if (!(tau_r > 0.f)) tau_r = base * sqrtf((float)BN);
-            if (!(tau_c > 0.f)) tau_c = base * sqrtf((float)kBM);
-          }
-          if (et == 0) {  // the report keeps the largest thresholds used
-            atomicMax(reinterpret_cast<int*>(&p.report->tau_row), __float_as_int(tau_r));
-            atomicMax(reinterpret_cast<int*>(&p.report->tau_col), __float_as_int(tau_c));
-          }
-
-          const float d_r = rowsum - cr;
-          const bool bad_r = !(fabsf(d_r) <= tau_r);
-          float ratio_r = bad_r ? 0.f : fabsf(d_r) / tau_r;
-          float ratio_c = 0.f;
-          if (bad_r) {
-            atomicAdd(&aux->nbad_r, 1);
-            aux->bad_row = r;
-            aux->d_row = d_r;
-          }
-#pragma unroll
-          for (int h = 0; h < C::CC_GROUPS; ++h) {
-            const int j = h * 128 + r;
-            const float tot =
-                colsum_of(0)[j] + colsum_of(1)[j] + colsum_of(2)[j] + colsum_of(3)[j];
-            const float d_c = tot - cc[h];
-            if (!(fabsf(d_c) <= tau_c)) {
-              atomicAdd(&aux->nbad_c, 1);
-              aux->bad_col = j;
-              aux->d_col = d_c;
-            } else {
-              ratio_c = fmaxf(ratio_c, fabsf(d_c) / tau_c);
-            }
-          }
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) {
-            ratio_r = fmaxf(ratio_r, __shfl_xor_sync(0xffffffffu, ratio_r, off));
-            ratio_c = fmaxf(ratio_c, __shfl_xor_sync(0xffffffffu, ratio_c, off));
-          }
-          if (lane == 0) {
-            atomicMax(reinterpret_cast<int*>(&p.report->max_ratio_row), __float_as_int(ratio_r));
-            atomicMax(reinterpret_cast<int*>(&p.report->max_ratio_col), __float_as_int(ratio_c));
-          }
-          named_bar_sync(1, kEpiThreads);  // mismatch counts complete
-
-          const int nbr = aux->nbad_r, nbc = aux->nbad_c;
-          const int brow = aux->bad_row, bcol = aux->bad_col;
-          const bool single = (nbr == 1 && nbc == 1);
-          if (et == 0) atomicAdd(&p.report->tiles_checked, 1u);
-          if (single && (brow >> 5) == q) {
-            // Locate at (brow, bcol); recompute the value from the row
-            // checksum and the rest of the row (survives Inf / NaN).
-            float rest = 0.f, before = 0.f;
-#pragma unroll 1
-            for (int c32 = 0; c32 < BN / 32; ++c32) {
-              uint32_t u[32];
-              tmem_ld32(tacc + c32 * 32, u);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const float x = f32_of(u[i]);
-                if (c32 * 32 + i == bcol) before = x;
-                else rest += x;
-              }
-            }
-            if (r == brow) {
-              const float after = cr - rest;
-              aux->fix_value = after;
-              atomicAdd(&p.report->detected, 1u);
-              atomicAdd(&p.report->corrected, 1u);
-              atomicOr(&p.report->status_bits, 1u << SKG_ABFT_CORRECTED);
-              const uint32_t idx = atomicAdd(&p.report->n_records, 1u);
-              if (idx < SKG_MAX_RECORDS) {
-                skg_fault_record_t* rec = &p.report->records[idx];
-                rec->launch = epoch;
-                rec->tile = out_tile;
-                rec->row = brow;
-                rec->col = bcol;
-                rec->status = SKG_ABFT_CORRECTED;
-                rec->n_bad_rows = nbr;
-                rec->n_bad_cols = nbc;
-                rec->injected = injected_tile ? 1u : 0u;
-                rec->before = before;
-                rec->after = after;
-                rec->delta_row = aux->d_row;
-                rec->delta_col = aux->d_col;
-                rec->clean_value = inject_here ? aux->inj_clean : 0.f;
-              }
-            }
-          } else if (!single && (nbr != 0 || nbc != 0) && et == 0) {
-            atomicAdd(&p.report->detected, 1u);
-            atomicAdd(&p.report->uncorrectable, 1u);
-            atomicOr(&p.report->status_bits, 1u << SKG_ABFT_UNCORRECTABLE);
-            const uint32_t idx = atomicAdd(&p.report->n_records, 1u);
-            if (idx < SKG_MAX_RECORDS) {
-              skg_fault_record_t* rec = &p.report->records[idx];
-              rec->launch = epoch;
-              rec->tile = out_tile;
-              rec->row = nbr == 1 ? brow : -1;
-              rec->col = nbc == 1 ? bcol : -1;
-              rec->status = SKG_ABFT_UNCORRECTABLE;
-              rec->n_bad_rows = nbr;
-              rec->n_bad_cols = nbc;
-              rec->injected = injected_tile ? 1u : 0u;
-              rec->before = 0.f;
-              rec->after = 0.f;
-              rec->delta_row = nbr ? aux->d_row : 0.f;
-              rec->delta_col = nbc ? aux->d_col : 0.f;
-              rec->clean_value = inject_here ? aux->inj_clean : 0.f;
-            }
-          }
-          named_bar_sync(1, kEpiThreads);  // corrected value published
-          if (single) {
-            fix_row = brow;
-            fix_col = bcol;
-            fix_val = aux->fix_value;
-          }
-          named_bar_sync(1, kEpiThreads);  // everyone has read the decision
-          if (et == 0) {
-            aux->nbad_r = 0;
-            aux->nbad_c = 0;
-            aux->bad_row = -1;
-            aux->bad_col = -1;
           }
         }
 
@@ -2475,7 +2560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i == jc) y[hh * 32 + i] = fix_val;
             }
           }
-          if (c == c_hi - 1) {
+          if (c == c_hi - 1 && !spec) {
             // Accumulator fully read: hand the TMEM buffer back to the MMA warp.
             tc_fence_before();
             release_acc(ab);
@@ -2532,6 +2617,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit();
           }
           bsel = (bsel + 1) % C::EPI_BUFS;
+        }
+        if (kStoreFirst && spec) {
+          // Stored before its check: the references are in once every
+          // checksum segment has been added; check the tile against them.
+          const bool fine = wait_references();
+          if (fine) {
+            ck_ready = true;
+            load_references();
+            check(false);
+            if (fix_row >= 0 && q == (fix_row >> 5) && store_ok) {
+              // The located element was stored from the faulty accumulator:
+              // once this warp's tile stores have landed, the corrected
+              // value goes over it (beta = 0: C = alpha acc).
+              if (lane == 0) bulk_wait<0>();
+              __syncwarp();
+              if (r == fix_row && m0 + r < p.m && n0 + fix_col < p.n) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                store_out<C::OUT>(p.c_ptr, (int64_t)(m0 + r) * p.ldc + n0 + fix_col,
+                                  p.alpha * fix_val);
+              }
+            }
+          }
+          tc_fence_before();
+          release_acc(ab);
+          if (!fine) break;
         }
       }
       if (++ab == ACC_BUFS) {

@@ -962,6 +962,45 @@ def test_gemm_host_buffers(layouts, pinned, abft):
 
 
 # --------------------------------------------------------------------------- single-launch ABFT
+@pytest.mark.parametrize("out", ["f32", "f16", "bf16"])
+def test_abft_store_first_then_correct(out):
+    # The first output tile of a launch whose side CTAs run the encode pass
+    # is stored before its references are in (beta = 0); a located fault is
+    # then corrected in C by one more store, in the output type.
+    m, n, k = 384, 640, 320
+    p = inputs.make_problem(m, n, k, seed=97, in_dtype="bf16", out_dtype=out,
+                            law_a="normal", law_b="normal", alpha=1.25)
+    opts = skgemm.opts_default(abft=1)
+    plan = skgemm.launch_plan(m, n, k, opts)
+    assert plan.encode_in_kernel == 1 and plan.side_ctas > 0
+    ref = reference(p)
+    tiles_n = -(-n // plan.tile_n)
+    hits = 0
+    for (tm, tn, row, col) in [(0, 0, 5, 7), (2, tiles_n - 1, 127, 3), (1, 2, 64, 100)]:
+        gi, gj = tm * 128 + row, tn * plan.tile_n + col
+        ma, mb = ab.tile_maxima(p.A.double().numpy(), p.B.double().numpy(), tm, tn, 128,
+                                plan.tile_n)
+        kind, _ = ab.classify_flip(ref[gi, gj] / p.alpha, 30,
+                                   ab.default_tau(k, plan.tile_n, ma, mb), 1e-3)
+        if kind != ab.MUST_DETECT:
+            continue
+        hits += 1
+        o = skgemm.opts_default(abft=1, inject_tile=tm * tiles_n + tn, inject_row=row,
+                                inject_col=col, inject_bit=30)
+        C, ws, st = run(p, o)
+        assert st == skgemm.OK
+        rep = ws.report()
+        assert rep.detected == 1 and rep.corrected == 1 and rep.uncorrectable == 0
+        assert (rep.records[0].tile, rep.records[0].row, rep.records[0].col) == \
+            (tm * tiles_n + tn, row, col)
+        check_full(p, C, ref)
+    assert hits >= 2
+    C, ws, st = run(p, opts)
+    assert st == skgemm.OK
+    check_full(p, C, ref)
+    assert ws.report().detected == 0
+
+
 @pytest.mark.parametrize("shape", [(1024, 1024, 1024), (384, 640, 320), (300, 1000, 520)])
 def test_abft_encode_in_kernel(shape):
     # Small bf16 shapes whose output tiles leave SMs idle: the checksum tiles
