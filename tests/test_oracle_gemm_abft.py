@@ -288,3 +288,12 @@ def test_verify_tile_grey_band_and_patterns():
     g[4, 3] = 1e30
     res = ab.verify_tile(g, cr, cc, 0.6, 0.4)
     assert (res["status"], res["row"], res["col"], res["value"]) == (ab.CORRECTED, 4, 3, C[4, 3])
+
+
+def test_tile_bounds_ragged_edges():
+    # A 300 x 200 output in 128 x 128 tiles: the last tile row holds rows
+    # 256 .. 299 and the last tile column columns 128 .. 199; a 256-wide
+    # tile column covers all 200 columns.
+    assert ab.tile_bounds(0, 0, 128, 128, 300, 200) == (0, 128, 0, 128)
+    assert ab.tile_bounds(2, 1, 128, 128, 300, 200) == (256, 300, 128, 200)
+    assert ab.tile_bounds(1, 0, 128, 256, 300, 200) == (128, 256, 0, 200)

@@ -198,3 +198,45 @@ def test_ceil_split_can_leave_short_ctas():
     assert ss.iters_per_cta(sch) == [5, 5, 5, 3]
     sch = ss.schedule(384, 384, 128, 128, 128, 64, 4, mode="sk", split="even")
     assert ss.iters_per_cta(sch) == [5, 5, 4, 4]
+
+
+def test_sk_range_even_and_ceil_hand_computed():
+    # T = 18 MAC iterations on g = 4 CTAs. The even split of the Stream-K
+    # page's appendix A1 (counts differ by one at most) gives 5, 5, 4, 4
+    # contiguous ranges; Algorithm 5's ceil(T / g) = 5 per CTA gives 5, 5, 5, 3
+    # once clamped at T.
+    assert [ss.sk_range(x, 18, 4) for x in range(4)] == [(0, 5), (5, 10), (10, 14), (14, 18)]
+    assert [ss.sk_range(x, 18, 4, "ceil") for x in range(4)] == \
+        [(0, 5), (5, 10), (10, 15), (15, 18)]
+    # More CTAs than iterations: the last CTAs get empty ranges at T.
+    assert [ss.sk_range(x, 3, 5) for x in range(5)] == [(0, 1), (1, 2), (2, 3), (3, 3), (3, 3)]
+    assert [ss.sk_range(x, 3, 5, "ceil") for x in range(5)] == \
+        [(0, 1), (1, 2), (2, 3), (3, 3), (3, 3)]
+    with pytest.raises(ValueError):
+        ss.sk_range(0, 3, 5, "other")
+
+
+def test_walk_range_roles_hand_computed():
+    # Algorithm 5 cuts a CTA's range at tile boundaries (8 iterations per
+    # tile here): a segment that does not start its tile is a PEER, one that
+    # starts and ends it FULL, one that starts it and stops inside it the
+    # OWNER.
+    def cut(x, b, e, off=0):
+        return [(s.cta, s.tile, s.k_iter_begin, s.k_iter_end, s.role)
+                for s in ss.walk_range(x, b, e, 8, tile_offset=off)]
+    assert cut(1, 5, 20) == [(1, 0, 5, 8, ss.PEER), (1, 1, 0, 8, ss.FULL),
+                             (1, 2, 0, 4, ss.OWNER)]
+    assert cut(0, 3, 6) == [(0, 0, 3, 6, ss.PEER)]     # inside one tile, not its start
+    assert cut(0, 0, 3) == [(0, 0, 0, 3, ss.OWNER)]    # starts the tile, stops inside
+    assert cut(0, 8, 16) == [(0, 1, 0, 8, ss.FULL)]
+    assert cut(0, 7, 7) == []
+    # the hybrids' Stream-K region is numbered from tile t_dp on
+    assert [(t, role) for (_, t, _, _, role) in cut(2, 5, 20, off=10)] == \
+        [(10, ss.PEER), (11, ss.FULL), (12, ss.OWNER)]
+
+
+def test_tile_coords_row_major():
+    # Reading R2 of Algorithm 3: tile = tm * tiles_n + tn.
+    assert [ss.tile_coords(t, 3) for t in range(7)] == \
+        [(0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (1, 2), (2, 0)]
+    assert ss.tile_coords(5, 1) == (5, 0)
