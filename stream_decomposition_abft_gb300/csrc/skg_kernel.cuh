@@ -1226,7 +1226,8 @@ static __device__ __forceinline__ TileFix check_tile(
   if (lane == 0) bulk_wait_read<0>();
   __syncwarp();
   float* my_colsum = colsum_of(q);
-  float rowsum = 0.f;
+  // The row sum in four interleaved partial sums: shorter dependency chains.
+  float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
   for (int c32 = 0; c32 < BN / 32; ++c32) {
     uint32_t u[32];
@@ -1253,9 +1254,10 @@ static __device__ __forceinline__ TileFix check_tile(
       tmem_st32(tacc + c32 * 32, wv);
     }
 #pragma unroll
-    for (int i = 0; i < 32; ++i) rowsum += v[i];
+    for (int i = 0; i < 32; ++i) rs[i & 3] += v[i];
     my_colsum[c32 * 32 + lane] = warp_column_sums(v, lane);
   }
+  const float rowsum = (rs[0] + rs[1]) + (rs[2] + rs[3]);
   // Reference checksums of this tile: thread r holds the row checksum
   // of row r and the column checksum of columns h*128 + r, each the
   // sum of its hi and lo partial products, unscaled by the tile's
